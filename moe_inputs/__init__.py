@@ -1,0 +1,354 @@
+"""Seeded synthetic inputs for the quantized MoE decode layer.
+
+This module only *draws* data: layer shapes, random weights, their int4 affine
+group quantisation and packing (the storage format), token activations, and the
+per-expert router bias used to skew expert load.  It holds none of the layer's
+forward arithmetic (no gemv, routing, activation or combine).  Both the CPU
+oracle (``oracle/``) and the CUDA library's tests and bench take their inputs
+from here, so the two sides see bit-identical data.
+
+Storage conventions (the library's input format):
+
+* bf16 tensors are numpy ``uint16`` arrays of bf16 bit patterns; fp16 tensors
+  are numpy ``float16``; fp32 tensors are ``float32``.
+* Expert matrices are row-major ``[E, N_out, K_in]`` with the quantisation
+  groups of ``G`` consecutive elements along ``K_in``.  ``q`` is packed eight
+  4-bit codes per ``uint32`` word, element ``8*w + i`` in bits ``4*i..4*i+3``
+  (lowest nibble first), giving ``[E, N_out, K_in/8]``.  ``scale`` and
+  ``bias`` are ``[E, N_out, K_in/G]`` in the layer's scale dtype and a weight
+  is reconstructed as ``scale * q + bias`` (MLX-style affine quantisation, as
+  the mlx-bun decode-speed program describes its "affine 2/3/4/5/6/8-bit with
+  supported group sizes 32/64/128" weights).
+* The quantiser used to make synthetic weights is round-to-nearest over each
+  group's min/max: ``bias = min``, ``scale = (max - min) / 15`` (both rounded
+  to the scale dtype), ``q = clip(rint((w - bias) / scale), 0, 15)``.  The pages
+  give no quantiser; this one only shapes the test weights.
+"""
+from __future__ import annotations
+
+import dataclasses
+from dataclasses import dataclass, field
+from typing import Dict, List, Optional
+
+import numpy as np
+
+__all__ = [
+    "LayerSpec", "LayerWeights", "SPECS", "stack_specs", "make_layer", "make_x",
+    "draw_x_rows", "round_to_bf16_bits", "bf16_bits_to_f32", "quantize_affine_int4",
+    "pack_int4", "unpack_int4", "zipf_router_bias", "spec_for", "ROUTED_BYTES",
+]
+
+
+# ---------------------------------------------------------------------------
+# bf16 storage helpers (bit manipulation only)
+# ---------------------------------------------------------------------------
+
+def round_to_bf16_bits(a) -> np.ndarray:
+    """Round float values to bf16 (round to nearest, ties to even) and return the
+    16-bit patterns as ``uint16``.  NaN stays a quiet NaN."""
+    f = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    r = ((u + 0x7FFF + lsb) >> 16).astype(np.uint32)
+    nan = np.isnan(f)
+    r = np.where(nan, np.uint32(0x7FC0), r)
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_f32(u16) -> np.ndarray:
+    """Widen bf16 bit patterns (uint16) to float32 exactly."""
+    u = np.asarray(u16, dtype=np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32)
+
+
+def _round_to_dtype(a: np.ndarray, dtype: str) -> np.ndarray:
+    """Round to the named storage dtype; returns the storage array."""
+    if dtype == "bf16":
+        return round_to_bf16_bits(a)
+    if dtype == "fp16":
+        return np.asarray(a, dtype=np.float64).astype(np.float16)
+    if dtype == "fp32":
+        return np.asarray(a, dtype=np.float64).astype(np.float32)
+    raise ValueError(dtype)
+
+
+def _storage_to_f64(a: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "bf16":
+        return bf16_bits_to_f32(a).astype(np.float64)
+    return np.asarray(a).astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# int4 packing and the synthetic-weight quantiser
+# ---------------------------------------------------------------------------
+
+def pack_int4(q: np.ndarray) -> np.ndarray:
+    """Pack 4-bit codes ``[..., K]`` (values 0..15) into ``uint32 [..., K/8]``,
+    element ``8*w + i`` at bits ``4*i``."""
+    q = np.asarray(q)
+    if q.shape[-1] % 8:
+        raise ValueError("K must be a multiple of 8")
+    if q.size and (q.min() < 0 or q.max() > 15):
+        raise ValueError("codes must be in 0..15")
+    q = q.astype(np.uint32).reshape(*q.shape[:-1], q.shape[-1] // 8, 8)
+    shifts = (4 * np.arange(8, dtype=np.uint32))
+    return np.bitwise_or.reduce(q << shifts, axis=-1).astype(np.uint32)
+
+
+def unpack_int4(packed: np.ndarray) -> np.ndarray:
+    """Inverse of :func:`pack_int4` (used by the generator's own checks)."""
+    p = np.asarray(packed, dtype=np.uint32)
+    shifts = (4 * np.arange(8, dtype=np.uint32))
+    q = (p[..., None] >> shifts) & np.uint32(0xF)
+    return q.reshape(*p.shape[:-1], p.shape[-1] * 8).astype(np.uint8)
+
+
+def quantize_affine_int4(w: np.ndarray, group: int, scale_dtype: str):
+    """Round-to-nearest int4 affine quantisation of ``w [..., K]`` in groups of
+    ``group`` along the last axis.  Returns ``(q uint8 [..., K], scale, bias)``
+    with scale/bias in storage form ``[..., K/group]``."""
+    w = np.asarray(w, dtype=np.float64)
+    K = w.shape[-1]
+    if K % group:
+        raise ValueError("group must divide K")
+    wg = w.reshape(*w.shape[:-1], K // group, group)
+    lo = wg.min(axis=-1)
+    hi = wg.max(axis=-1)
+    bias_st = _round_to_dtype(lo, scale_dtype)
+    scale_st = _round_to_dtype((hi - lo) / 15.0, scale_dtype)
+    b = _storage_to_f64(bias_st, scale_dtype)[..., None]
+    s = _storage_to_f64(scale_st, scale_dtype)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        qf = np.where(s > 0, np.rint((wg - b) / np.where(s > 0, s, 1.0)), 0.0)
+    q = np.clip(qf, 0, 15).astype(np.uint8).reshape(w.shape)
+    return q, scale_st, bias_st
+
+
+# ---------------------------------------------------------------------------
+# Layer shapes
+# ---------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class LayerSpec:
+    """Shape and numeric format of one MoE layer."""
+    name: str
+    hidden: int                 # H
+    n_experts: int              # E
+    top_k: int                  # k
+    expert_ffn: int             # F
+    latent: int = 0             # L (0: experts act on the hidden size)
+    group_size: int = 64        # G
+    shared_ffn: int = 0         # shared expert width (0: none)
+    act: str = "swiglu"         # "swiglu" (gate+up) | "relu2" (up only)
+    router: str = "softmax"     # "softmax" | "sigmoid"
+    renormalize: bool = True
+    routed_scale: float = 1.0
+    router_bias: bool = False   # per-expert fp32 selection bias
+    act_dtype: str = "bf16"     # x, out, latent projections, shared expert
+    scale_dtype: str = "bf16"   # expert scale/bias
+    router_dtype: str = "bf16"  # router weight
+    weight_std: float = 0.02
+    bias_std: float = 0.01
+
+    @property
+    def k_in(self) -> int:
+        """Input width of the routed experts (latent size or hidden)."""
+        return self.latent if self.latent else self.hidden
+
+    @property
+    def gated(self) -> bool:
+        return self.act == "swiglu"
+
+    def with_(self, **kw) -> "LayerSpec":
+        return dataclasses.replace(self, **kw)
+
+
+SPECS: Dict[str, LayerSpec] = {
+    # tiny layer the oracle finishes in milliseconds
+    "tiny": LayerSpec(name="tiny", hidden=512, n_experts=16, top_k=2, expert_ffn=256,
+                      latent=0, group_size=64, shared_ffn=256, act="swiglu",
+                      router="softmax", renormalize=True, routed_scale=1.0),
+    # latent layer at the Bolt 74B-A9B shapes (E=496, k=9, latent 1024)
+    "latent": LayerSpec(name="latent", hidden=4096, n_experts=496, top_k=9,
+                        expert_ffn=1856, latent=1024, group_size=64, shared_ffn=3712,
+                        act="relu2", router="sigmoid", renormalize=True,
+                        routed_scale=2.5, router_bias=True),
+    # non-latent sigmoid top-8 layer with fp16 activations and an fp32 router
+    "nonlatent": LayerSpec(name="nonlatent", hidden=6144, n_experts=256, top_k=8,
+                           expert_ffn=2048, latent=0, group_size=32, shared_ffn=2048,
+                           act="swiglu", router="sigmoid", renormalize=True,
+                           routed_scale=1.0, router_bias=False, act_dtype="fp16",
+                           scale_dtype="fp16", router_dtype="fp32"),
+}
+
+STACK_EXPERTS = (240, 304, 368, 432, 496)
+
+
+def stack_specs() -> List[LayerSpec]:
+    """Five latent layers with the per-layer expert counts of the Bolt stack."""
+    return [SPECS["latent"].with_(name=f"latent_e{e}", n_experts=e) for e in STACK_EXPERTS]
+
+
+def spec_for(name: str) -> LayerSpec:
+    if name in SPECS:
+        return SPECS[name]
+    for s in stack_specs():
+        if s.name == name:
+            return s
+    raise KeyError(name)
+
+
+# ---------------------------------------------------------------------------
+# Weights
+# ---------------------------------------------------------------------------
+
+@dataclass
+class LayerWeights:
+    """Storage-form weights of one layer (numpy, host)."""
+    spec: LayerSpec
+    router_w: np.ndarray                      # [E, H] router_dtype
+    router_bias: Optional[np.ndarray]         # [E] float32 or None
+    fc1: Optional[np.ndarray]                 # [L, H] act_dtype (latent only)
+    fc2: Optional[np.ndarray]                 # [H, L] act_dtype (latent only)
+    gate_q: Optional[np.ndarray]              # [E, F, Kin/8] uint32 (gated only)
+    gate_s: Optional[np.ndarray]
+    gate_b: Optional[np.ndarray]
+    up_q: np.ndarray                          # [E, F, Kin/8]
+    up_s: np.ndarray                          # [E, F, Kin/G]
+    up_b: np.ndarray
+    down_q: np.ndarray                        # [E, Kin, F/8]
+    down_s: np.ndarray                        # [E, Kin, F/G]
+    down_b: np.ndarray
+    sh_gate: Optional[np.ndarray]             # [Fsh, H] act_dtype (gated only)
+    sh_up: Optional[np.ndarray]               # [Fsh, H]
+    sh_down: Optional[np.ndarray]             # [H, Fsh]
+    seed: int = 0
+
+    def arrays(self) -> Dict[str, np.ndarray]:
+        out = {}
+        for f in dataclasses.fields(self):
+            v = getattr(self, f.name)
+            if isinstance(v, np.ndarray):
+                out[f.name] = v
+        return out
+
+
+def _dense(rng, shape, std, dtype):
+    w = rng.standard_normal(size=shape, dtype=np.float32).astype(np.float64) * std
+    return _round_to_dtype(w, dtype)
+
+
+# Above this many elements per expert tensor, codes are drawn directly (see
+# ``_quant_expert_direct``): drawing and quantising billions of normals on a
+# host CPU takes minutes, while the kernels' cost does not depend on values.
+EXACT_QUANT_MAX_ELEMS = 1 << 26
+
+
+def _quant_expert_exact(rng, E, N, K, spec: LayerSpec):
+    """Draw N(0, weight_std) weights and quantise them group by group."""
+    q_all = np.empty((E, N, K), dtype=np.uint8)
+    s_all = None
+    b_all = None
+    G = spec.group_size
+    for e in range(E):
+        w = rng.normal(0.0, spec.weight_std, size=(N, K))
+        q, s, b = quantize_affine_int4(w, G, spec.scale_dtype)
+        if s_all is None:
+            s_all = np.empty((E,) + s.shape, dtype=s.dtype)
+            b_all = np.empty((E,) + b.shape, dtype=b.dtype)
+        q_all[e], s_all[e], b_all[e] = q, s, b
+    return pack_int4(q_all), s_all, b_all
+
+
+def _quant_expert_direct(rng, E, N, K, spec: LayerSpec):
+    """Draw packed codes uniformly (each nibble uniform on 0..15) and per-group
+    scale/bias so that the reconstructed weights have mean ~0 and standard
+    deviation ~weight_std (a uniform code has std 15/sqrt(12) ~= 4.33 steps)."""
+    G = spec.group_size
+    words = rng.integers(0, 1 << 32, size=(E, N, K // 8), dtype=np.uint32)
+    step = spec.weight_std / (15.0 / np.sqrt(12.0))
+    sg = np.abs(step * (1.0 + 0.1 * rng.standard_normal(size=(E, N, K // G))))
+    bg = -7.5 * sg + 0.1 * spec.weight_std * rng.standard_normal(size=(E, N, K // G))
+    return words, _round_to_dtype(sg, spec.scale_dtype), _round_to_dtype(bg, spec.scale_dtype)
+
+
+def _quant_expert(rng, E, N, K, spec: LayerSpec):
+    if N * K <= EXACT_QUANT_MAX_ELEMS // max(E, 1):
+        return _quant_expert_exact(rng, E, N, K, spec)
+    return _quant_expert_direct(rng, E, N, K, spec)
+
+
+def make_layer(spec: LayerSpec, seed: int = 0, router_bias: Optional[np.ndarray] = None
+               ) -> LayerWeights:
+    """Draw one layer's weights from ``PCG64(seed)``.  Dense weights are
+    N(0, weight_std) rounded to their storage dtype; router bias N(0, bias_std).
+    Expert weights are N(0, weight_std) quantised group by group when the
+    layer is small, and drawn directly as uniform codes with matching
+    scale/bias statistics when it is large (``EXACT_QUANT_MAX_ELEMS``)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    H, E, F, Kin = spec.hidden, spec.n_experts, spec.expert_ffn, spec.k_in
+    for dim, nm in ((H, "hidden"), (F, "expert_ffn"), (Kin, "k_in")):
+        if dim % spec.group_size or dim % 8:
+            raise ValueError(f"{nm}={dim} is not a multiple of the group size")
+    router_w = _dense(rng, (E, H), spec.weight_std, spec.router_dtype)
+    rb = None
+    if spec.router_bias:
+        rb = (rng.normal(0.0, spec.bias_std, size=E).astype(np.float32)
+              if router_bias is None else np.asarray(router_bias, dtype=np.float32))
+    fc1 = fc2 = None
+    if spec.latent:
+        fc1 = _dense(rng, (spec.latent, H), spec.weight_std, spec.act_dtype)
+        fc2 = _dense(rng, (H, spec.latent), spec.weight_std, spec.act_dtype)
+    gate = (None, None, None)
+    if spec.gated:
+        gate = _quant_expert(rng, E, F, Kin, spec)
+    up = _quant_expert(rng, E, F, Kin, spec)
+    down = _quant_expert(rng, E, Kin, F, spec)
+    shg = shu = shd = None
+    if spec.shared_ffn:
+        Fs = spec.shared_ffn
+        if spec.gated:
+            shg = _dense(rng, (Fs, H), spec.weight_std, spec.act_dtype)
+        shu = _dense(rng, (Fs, H), spec.weight_std, spec.act_dtype)
+        shd = _dense(rng, (H, Fs), spec.weight_std, spec.act_dtype)
+    return LayerWeights(spec=spec, router_w=router_w, router_bias=rb, fc1=fc1, fc2=fc2,
+                        gate_q=gate[0], gate_s=gate[1], gate_b=gate[2],
+                        up_q=up[0], up_s=up[1], up_b=up[2],
+                        down_q=down[0], down_s=down[1], down_b=down[2],
+                        sh_gate=shg, sh_up=shu, sh_down=shd, seed=seed)
+
+
+def zipf_router_bias(n_experts: int, seed: int, s: float = 1.1, alpha: float = 0.035
+                     ) -> np.ndarray:
+    """Per-expert selection bias that skews expert load towards a Zipf(s) shape:
+    experts get a random popularity rank r (1 = most popular) and bias
+    ``-alpha * s * ln(r)``.  ``alpha`` sets how strongly the bias dominates the
+    router scores; the realised load is measured, not assumed."""
+    rng = np.random.Generator(np.random.PCG64(seed + 7919))
+    rank = rng.permutation(n_experts) + 1
+    return (-alpha * s * np.log(rank.astype(np.float64))).astype(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# Activations
+# ---------------------------------------------------------------------------
+
+def draw_x_rows(spec: LayerSpec, n: int, rng: np.random.Generator) -> np.ndarray:
+    """Draw ``n`` activation rows N(0,1) in the layer's activation storage dtype."""
+    return _round_to_dtype(rng.normal(0.0, 1.0, size=(n, spec.hidden)), spec.act_dtype)
+
+
+def make_x(spec: LayerSpec, T: int, seed: int = 0) -> np.ndarray:
+    """``T`` activation rows from ``PCG64(seed)`` (no routing-margin filter)."""
+    rng = np.random.Generator(np.random.PCG64(1_000_003 + seed))
+    return draw_x_rows(spec, T, rng)
+
+
+def ROUTED_BYTES(spec: LayerSpec) -> int:
+    """Bytes of one routed expert: packed codes + scale + bias of all its matrices."""
+    sb = 2 if spec.scale_dtype in ("bf16", "fp16") else 4
+    n_mats_in = 2 if spec.gated else 1
+    per_in = spec.expert_ffn * spec.k_in          # up (and gate) elements
+    per_down = spec.k_in * spec.expert_ffn
+    elems = n_mats_in * per_in + per_down
+    return elems // 2 + 2 * sb * (elems // spec.group_size)
