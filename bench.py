@@ -1,0 +1,371 @@
+#!/usr/bin/env python
+"""MoE-layer decode benchmark on one GB300 (or N independent replicas).
+
+Workload: the latent MoE layer at the Bolt 74B-A9B shapes (H=4096, latent
+L=1024, E=496 routed experts, top-k=9 sigmoid router with fp32 bias and
+normalised weights x2.5, experts F=1856 squared-ReLU int4 affine group 64 with
+bf16 scale/bias, bf16 shared expert F=3712), decoding T=1 token row per step
+(T=16 reported alongside).  Inputs are seeded synthetic data resident in HBM;
+32 distinct token batches are cycled so the selected experts change, and L2 is
+flushed (a 256 MB write) before every timed step.
+
+Prints ONE JSON line: tokens/s (``value``), achieved HBM GB/s over the
+algorithmic bytes, the roofline of the dominant kernel, the end-to-end number
+through the host-buffer C-ABI call, and the fp64 CPU oracle timed on the host.
+``--impl reference`` times that oracle alone on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer decode tokens/s and achieved HBM GB/s (% of GB300 peak) at T=1/16"
+WORKLOAD = ("latent MoE layer, Bolt-like shape: H=4096, fc1/fc2 latent L=1024, E=496, "
+            "top-k=9 sigmoid+bias, normalised x2.5, F=1856 relu^2 int4 affine g64 bf16 "
+            "scale/bias, shared F=3712 bf16")
+L2_FLUSH_BYTES = 256 << 20
+STAGES = ["dense_in", "route", "expert_up", "expert_down", "dense_out"]
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--T", type=int, default=1, help="token rows per step")
+    p.add_argument("--also-T", type=int, default=16, help="second T reported alongside (0: off)")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle sample budget")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--seed", type=int, default=0)
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# byte accounting (algorithmic bytes: what the method must move)
+# ---------------------------------------------------------------------------
+
+def expert_bytes(spec):
+    """(up-side bytes, down-side bytes) of one routed expert: packed codes +
+    scale + bias (2 bytes each per group)."""
+    n_in = 2 if spec.gated else 1
+    e_in = n_in * spec.expert_ffn * spec.k_in
+    e_dn = spec.k_in * spec.expert_ffn
+    sb = 2 * 2
+    return (e_in // 2 + sb * (e_in // spec.group_size), e_dn // 2 + sb * (e_dn // spec.group_size))
+
+
+def stage_bytes(spec, T, n_uniq):
+    """Algorithmic bytes per stage for one forward of T rows with n_uniq
+    distinct selected experts."""
+    H, E, L, Fs, k = spec.hidden, spec.n_experts, spec.latent, spec.shared_ffn, spec.top_k
+    rd = 4 if spec.router_dtype == "fp32" else 2
+    n_sh_in = 2 if spec.gated else 1
+    x_bytes = T * H * 2
+    up_b, dn_b = expert_bytes(spec)
+    din = E * H * rd + L * H * 2 + n_sh_in * Fs * H * 2 + x_bytes + (E if spec.router_bias else 0) * 4
+    dout = H * L * 2 + H * Fs * 2 + x_bytes + T * H * 2
+    return {"dense_in": din, "route": T * E * 4, "expert_up": n_uniq * up_b,
+            "expert_down": n_uniq * dn_b, "dense_out": dout}
+
+
+def layer_bytes(spec, T, n_uniq):
+    b = stage_bytes(spec, T, n_uniq)
+    return b["dense_in"] + b["expert_up"] + b["expert_down"] + b["dense_out"] - T * spec.hidden * 2
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline
+# ---------------------------------------------------------------------------
+
+def time_oracle(layer, rows: int, seconds: float, seed: int):
+    """The fp64 oracle as it stands on host cores: one-row forwards until
+    ``rows`` rows or ``seconds`` elapse.  Returns (rows done, seconds)."""
+    import moe_inputs as mi
+    import oracle
+    done, t0 = 0, time.perf_counter()
+    while done < rows:
+        x = mi.make_x(layer.spec, 1, seed + 1000 + done)
+        oracle.oracle_forward(layer, x)
+        done += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    return done, time.perf_counter() - t0
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def run_reference(args):
+    import moe_inputs as mi
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    spec = mi.SPECS["latent"]
+    layer = mi.make_layer(spec, args.seed)
+    for i in range(args.warmup):
+        time_oracle(layer, 1, 1e9, args.seed + 500 + i)
+    per = []
+    for i in range(args.steps):
+        n, dt = time_oracle(layer, 1, 1e9, args.seed + i)
+        per.append(dt)
+    total = sum(per)
+    value = args.steps * args.T / total
+    cores = host_cores()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "T": 1},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{args.steps} one-row forwards of the fp64 oracle"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def measure(torch, pkg, spec, layer_h, T, steps, warmup, seed, flush, stream, profile=True):
+    """Time `steps` forwards of T rows (L2 flushed before each).  Returns a
+    dict with per-step times, per-stage times and realised distinct-expert
+    counts."""
+    import moe_inputs as mi
+    nb = 32
+    xs = [torch.from_numpy(mi.make_x(spec, T, seed + 100 * T + i).view(np.int16)).cuda()
+          .view(torch.bfloat16) for i in range(nb)]
+    out = torch.empty_like(xs[0])
+    k = spec.top_k
+    ids = torch.empty((steps, T, k), dtype=torch.int32, device="cuda")
+    wts = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    layer_h.profile(profile)
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            flush.zero_()
+            pkg.moe_layer_forward(layer_h.handle, xs[i % nb], T, out, stream.cuda_stream)
+        stream.synchronize()
+        stage_ms = np.zeros(len(STAGES))
+        for i in range(steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            pkg.moe_layer_forward_ex(layer_h.handle, xs[i % nb], T, out, stream.cuda_stream,
+                                     ids[i], wts, None)
+            evs[i][1].record(stream)
+            if profile:
+                stage_ms += np.array(layer_h.stage_times())
+        stream.synchronize()
+    layer_h.profile(False)
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    ids_np = ids.cpu().numpy()
+    n_uniq = [len(np.unique(ids_np[i])) for i in range(steps)]
+    return {"step_ms": step_ms, "stage_ms": stage_ms / steps, "n_uniq": n_uniq, "xs": xs}
+
+
+def run_ours(args):
+    import torch
+
+    import moe_inputs as mi
+    import quantized_moe_decode_gemv_gb300 as pkg
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = {}
+    pp = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pp):
+        peaks = json.load(open(pp))
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+
+    spec = mi.SPECS["latent"]
+    layer = mi.make_layer(spec, args.seed + rank)
+    maxT = max(args.T, args.also_T or 1)
+    cfg = pkg.MoEConfig.from_spec(spec, max_tokens=maxT)
+    h = pkg.MoELayer(cfg, pkg.upload_arrays(layer.arrays(), device=dev))
+    torch.cuda.empty_cache()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream()
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        m = measure(torch, pkg, spec, h, args.T, args.steps, args.warmup, args.seed, flush, stream)
+    torch.cuda.synchronize()
+    total_ms = float(sum(m["step_ms"]))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    tokens = args.steps * args.T * world
+    value = tokens / (total_ms / 1e3)
+    bytes_steps = [layer_bytes(spec, args.T, u) for u in m["n_uniq"]]
+    gbs = sum(bytes_steps) / (sum(m["step_ms"]) / 1e3) / 1e9
+
+    # dominant kernel roofline (stage with the largest share of the step)
+    st = m["stage_ms"]
+    avg_uniq = float(np.mean(m["n_uniq"]))
+    sb = stage_bytes(spec, args.T, avg_uniq)
+    dom = int(np.argmax(st))
+    dom_name = STAGES[dom]
+    achieved = sb[dom_name] / (st[dom] / 1e3) / 1e9
+    stages = {n: {"ms": round(float(st[i]), 5), "share": round(float(st[i] / st.sum()), 4),
+                  "alg_bytes": int(sb[n]), "gbs": round(sb[n] / (st[i] / 1e3) / 1e9, 1)}
+              for i, n in enumerate(STAGES)}
+
+    # second T reported alongside
+    also = None
+    if args.also_T and args.also_T != args.T:
+        m2 = measure(torch, pkg, spec, h, args.also_T, max(20, args.steps // 4), args.warmup,
+                     args.seed + 1, flush, stream, profile=False)
+        t2 = sum(m2["step_ms"])
+        b2 = sum(layer_bytes(spec, args.also_T, u) for u in m2["n_uniq"])
+        also = {"T": args.also_T, "tokens_per_s": len(m2["step_ms"]) * args.also_T / (t2 / 1e3),
+                "ms_per_step": t2 / len(m2["step_ms"]), "gbs": b2 / (t2 / 1e3) / 1e9,
+                "hbm_frac": b2 / (t2 / 1e3) / 1e9 / hbm_peak,
+                "mean_distinct_experts": float(np.mean(m2["n_uniq"]))}
+
+    # end to end through the host-buffer C-ABI call
+    xs_host = [x.cpu().pin_memory() for x in m["xs"][:8]]
+    out_host = torch.empty_like(xs_host[0]).pin_memory()
+    e2e_steps = max(20, args.steps // 4)
+    for i in range(3):
+        h.forward_host(xs_host[i % 8], out_host, stream)
+    e2e_total = 0.0
+    for i in range(e2e_steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        h.forward_host(xs_host[i % 8], out_host, stream)
+        e2e_total += time.perf_counter() - t0
+    e2e = {"value": e2e_steps * args.T * world / e2e_total, "unit": "tokens/s",
+           "h2d_bytes_per_step": args.T * spec.hidden * 2,
+           "d2h_bytes_per_step": args.T * spec.hidden * 2}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n, dt = time_oracle(layer, 10_000, args.cpu_seconds, args.seed)
+        cpu = {"value": n / dt, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
+               "sample": f"{n} one-row forwards of the same layer (fp64 NumPy, "
+                         f"selected experts dequantised per row), {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded random weights and activations)",
+            "config": {"workload": WORKLOAD, "T": args.T, "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "flushed by a 256 MB write before every timed step",
+                       "input_batches": 32},
+            "hbm_gbs": gbs, "hbm_frac": gbs / hbm_peak, "hbm_peak_gbs": hbm_peak,
+            "hbm_peak_source": peak_src,
+            "mean_distinct_experts": float(np.mean(m["n_uniq"])),
+            "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved,
+                         "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                         "traffic": None},
+            "stages": stages,
+            "also": also,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "gpu_launches": len(STAGES) * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    h.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,222 @@
+/*
+ * moe_layer.h -- C ABI of the GB300 (sm_103a) quantized MoE decode layer.
+ *
+ * One handle holds one routed mixture-of-experts layer whose expert weights are
+ * 4-bit affine group-quantised.  moe_layer_forward() runs, for every token row,
+ *
+ *   router gemv -> softmax/sigmoid top-k -> (fc1_latent_proj) -> per selected
+ *   expert: dequant gemv up (+gate), activation, dequant gemv down -> weighted
+ *   combine in fp32 -> (fc2_latent_proj) -> + shared expert -> + residual
+ *
+ * in the layer order of the Bolt 74B-A9B latent MoE (TensorFold PR #1038,
+ * native Metal backend, "What's in it": gate gemv -> tf_route_topk ->
+ * fc1_latent_proj -> routed experts -> tf_moe_combine_rows -> fc2_latent_proj
+ * -> + shared -> + residual), with the fp32 router / sigmoid top-k / per-expert
+ * norm and sum of TensorFold PR #1295 (Muse Spark Open, "What this changes"),
+ * and MLX-style affine int4 weights (mlx-bun decode-speed program, weight
+ * format table: affine, group sizes 32/64/128, a scale and a bias per group).
+ *
+ * Every call's arithmetic runs in this library's CUDA kernels on the GPU; there
+ * is no CPU fallback.  The library serves one GPU (compute capability 10.3).
+ *
+ * Conventions
+ *   - "device pointer": memory of the GPU the handle was created on;
+ *     "host pointer": ordinary or pinned host memory.
+ *   - Matrices are row-major and contiguous.
+ *   - Packed int4 codes: eight 4-bit codes per uint32, element 8*w+i in bits
+ *     4*i..4*i+3 (lowest nibble first).  A weight is scale*q + bias, with the
+ *     scale and bias of its group of group_size consecutive elements along the
+ *     input (reduction) axis.
+ *   - bf16/fp16 buffers hold IEEE/bfloat16 16-bit values.
+ *   - Every function returns a moe_status; MOE_OK is 0.  On error nothing that
+ *     the call allocated stays allocated, and moe_layer_last_error() (where a
+ *     handle exists) describes the failure.
+ */
+#ifndef MOE_LAYER_H
+#define MOE_LAYER_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null pointer, T out of range, overlapping x/out */
+  MOE_ERR_UNSUPPORTED = 2,  /* a valid request this build does not serve */
+  MOE_ERR_TOPK_GT_E = 3,    /* top_k < 1 or top_k > n_experts */
+  MOE_ERR_LATENT_PROJ = 4,  /* latent layer with a missing fc1/fc2, or non-16-bit */
+  MOE_ERR_SHAPE = 5,        /* sizes not multiples of the group size / 64 */
+  MOE_ERR_DEVICE = 6,       /* current device is not compute capability 10.3 */
+  MOE_ERR_OOM = 7,          /* device allocation failed */
+  MOE_ERR_CUDA = 8,         /* a CUDA runtime call failed */
+  MOE_ERR_TIMEOUT = 9,      /* a bounded device-side wait ran out */
+  MOE_ERR_NONFINITE = 10    /* a router selection key was NaN or infinite */
+} moe_status;
+
+typedef enum moe_act {
+  MOE_ACT_SWIGLU = 0,  /* h = silu(gate x) * (up x), silu(g) = g / (1 + exp(-g)) */
+  MOE_ACT_RELU2 = 1    /* h = max(up x, 0)^2 (no gate matrix) */
+} moe_act;
+
+typedef enum moe_router {
+  MOE_ROUTER_SOFTMAX = 0, /* key = logit z; w = softmax over the selected ids
+                             (renormalize=1) or over all experts (renormalize=0) */
+  MOE_ROUTER_SIGMOID = 1  /* key = sigmoid(z) + router_bias; w = sigmoid(z),
+                             divided by its sum over the selected ids when
+                             renormalize=1; then times routed_scale */
+} moe_router;
+
+typedef enum moe_dtype { MOE_DTYPE_BF16 = 0, MOE_DTYPE_FP16 = 1, MOE_DTYPE_FP32 = 2 } moe_dtype;
+
+/* Path used for the routed experts.  AUTO picks the dequant-gemv path. */
+typedef enum moe_path { MOE_PATH_AUTO = 0, MOE_PATH_GEMV = 1, MOE_PATH_GROUPED = 2 } moe_path;
+
+typedef struct moe_layer_config {
+  int32_t hidden;        /* H: width of x and out; multiple of 64 */
+  int32_t n_experts;     /* E: routed experts, 1..1024 */
+  int32_t top_k;         /* k: experts per token, 1..min(E, 16) */
+  int32_t expert_ffn;    /* F: routed expert width; multiple of 64 and of group_size */
+  int32_t latent;        /* L: latent width of the routed experts, 0 = none (experts on H) */
+  int32_t group_size;    /* G: 32, 64 or 128 */
+  int32_t shared_ffn;    /* shared expert width, 0 = no shared expert */
+  int32_t max_tokens;    /* largest T a forward call may pass, >= 1 */
+  int32_t act;           /* moe_act (routed and shared experts alike) */
+  int32_t router;        /* moe_router */
+  int32_t renormalize;   /* 1: normalise weights over the selected ids */
+  float routed_scale;    /* multiplies the combine weights (after normalising) */
+  int32_t has_router_bias; /* sigmoid routing: per-expert fp32 selection bias */
+  int32_t act_dtype;     /* BF16|FP16: x, out, fc1/fc2 and shared expert weights */
+  int32_t scale_dtype;   /* BF16|FP16: expert scales and biases */
+  int32_t router_dtype;  /* BF16|FP16|FP32: router weight (x is widened to fp32) */
+} moe_layer_config;
+
+/* Weights, all DEVICE pointers owned by the caller.  moe_layer_create copies
+ * them into library-owned buffers (re-laid-out for the kernels) and
+ * synchronises before returning, so the caller may free them afterwards.
+ * Shapes (Kin = latent if latent > 0 else hidden):
+ *   router_w   [E, H]           router_dtype
+ *   router_bias[E]              fp32 (has_router_bias only, else NULL)
+ *   fc1_latent [L, H], fc2_latent [H, L]  act_dtype (latent layers only)
+ *   gate_q, up_q [E, F, Kin/8]  uint32 packed codes (gate_q: SWIGLU only)
+ *   gate_s, gate_b, up_s, up_b [E, F, Kin/G]  scale_dtype
+ *   down_q     [E, Kin, F/8]    uint32 packed codes
+ *   down_s, down_b [E, Kin, F/G] scale_dtype
+ *   sh_gate, sh_up [shared_ffn, H], sh_down [H, shared_ffn]  act_dtype
+ *     (sh_gate for SWIGLU only; all NULL when shared_ffn == 0) */
+typedef struct moe_layer_weights {
+  const void *router_w;
+  const float *router_bias;
+  const void *fc1_latent, *fc2_latent;
+  const uint32_t *gate_q, *up_q, *down_q;
+  const void *gate_s, *gate_b, *up_s, *up_b, *down_s, *down_b;
+  const void *sh_gate, *sh_up, *sh_down;
+} moe_layer_weights;
+
+typedef struct moe_layer moe_layer;
+
+/* Library ABI version (MOE_ABI_VERSION of the build). */
+int32_t moe_abi_version(void);
+
+/* Host-only validation of a config and of which weight pointers are present,
+ * with the same refusals and codes as moe_layer_create; touches no device.
+ * `w` may be NULL to check the config alone.  Refusals, in order:
+ *   MOE_ERR_INVALID_ARG   null cfg, non-positive sizes, bad enum values
+ *   MOE_ERR_TOPK_GT_E     top_k < 1 or top_k > n_experts (a layer whose top-k
+ *                         exceeds its own expert count is refused before any
+ *                         weight is read: TensorFold PR #1038, "What's in it")
+ *   MOE_ERR_LATENT_PROJ   latent > 0 with fc1/fc2 missing or act_dtype not
+ *                         16-bit (missing/non-bf16 latent projections are
+ *                         refused by name in the same passage)
+ *   MOE_ERR_SHAPE         G not 32/64/128, or H, F, Kin not multiples of 64 and
+ *                         of G, or expert weights present for a shape that
+ *                         cannot hold them
+ *   MOE_ERR_UNSUPPORTED   E > 1024 or top_k > 16 or shared expert without a
+ *                         weight, router_bias with softmax routing */
+moe_status moe_layer_validate(const moe_layer_config *cfg, const moe_layer_weights *w);
+
+/* Create a layer on the current CUDA device.  Validates (as above), refuses a
+ * device that is not compute capability 10.3 (MOE_ERR_DEVICE), then allocates
+ * and fills library-owned copies of the weights and a workspace for
+ * max_tokens rows, using `stream` (a cudaStream_t, NULL = legacy default) and
+ * synchronising it before returning.  On any failure every allocation made so
+ * far is freed and *out is set to NULL. */
+moe_status moe_layer_create(const moe_layer_config *cfg, const moe_layer_weights *w,
+                            void *stream, moe_layer **out);
+
+/* out[T, H] = layer(x[T, H]); x and out are DEVICE pointers in act_dtype,
+ * row-major, must not overlap, 1 <= T <= max_tokens.  Asynchronous on
+ * `stream`; no host synchronisation.  Returns launch errors only; conditions
+ * found on the device (non-finite router keys) are reported by
+ * moe_layer_device_status().  One handle serves one stream at a time: calls
+ * on different streams must not overlap. */
+moe_status moe_layer_forward(moe_layer *h, const void *x, int32_t T, void *out, void *stream);
+
+/* As moe_layer_forward, and also writes (each may be NULL) the selected
+ * expert ids topk_ids[T, k] (int32, selection order: larger key first, ties
+ * to the lower index), the combine weights topk_w[T, k] (fp32) and
+ * delta_f32[T, H] = out - x before the final rounding (fp32).  All DEVICE
+ * pointers. */
+moe_status moe_layer_forward_ex(moe_layer *h, const void *x, int32_t T, void *out, void *stream,
+                                int32_t *topk_ids, float *topk_w, float *delta_f32);
+
+/* End-to-end form for callers holding HOST buffers: copies x_host[T, H] to the
+ * device, runs the forward and copies the result to out_host[T, H], all
+ * queued on `stream`, then synchronises the stream.  Host buffers should be
+ * pinned for asynchronous copies. */
+moe_status moe_layer_forward_host(moe_layer *h, const void *x_host, int32_t T, void *out_host,
+                                  void *stream);
+
+/* Choose the routed-expert path for later forwards (A/B testing).  A path this
+ * build cannot serve for the layer returns MOE_ERR_UNSUPPORTED. */
+moe_status moe_layer_set_path(moe_layer *h, int32_t path);
+
+/* Synchronises `stream`, reads and clears the device status word: MOE_OK, or
+ * MOE_ERR_NONFINITE / MOE_ERR_TIMEOUT for conditions kernels recorded since
+ * the last call. */
+moe_status moe_layer_device_status(moe_layer *h, void *stream);
+
+/* Kernel stages of one forward, in launch order: 0 dense projections of x
+ * (router gemv, fc1_latent_proj, shared gate/up), 1 routing, 2 expert up
+ * (+gate, activation), 3 expert down, 4 combine + fc2_latent_proj + shared
+ * down + residual. */
+#define MOE_NUM_STAGES 5
+
+/* enable != 0: later forwards record a CUDA event on their stream before each
+ * stage and after the last (for per-kernel timing); 0 turns it off. */
+moe_status moe_layer_profile(moe_layer *h, int32_t enable);
+
+/* Waits for the last profiled forward and writes min(n, MOE_NUM_STAGES)
+ * stage durations in milliseconds to ms[] (host pointer).  Returns
+ * MOE_ERR_INVALID_ARG if profiling is off or no forward was profiled. */
+moe_status moe_layer_stage_times(moe_layer *h, float *ms, int32_t n);
+
+/* Bytes of device memory the handle owns (weights + workspace). */
+int64_t moe_layer_device_bytes(const moe_layer *h);
+
+/* Frees everything the handle owns.  NULL is a no-op. */
+moe_status moe_layer_destroy(moe_layer *h);
+
+/* Static name of a status code. */
+const char *moe_status_string(moe_status s);
+
+/* Last error message of a handle ("" if none); NULL handle gives the last
+ * error of the most recent failed create on this thread. */
+const char *moe_layer_last_error(const moe_layer *h);
+
+/* Device allocations currently held by all handles of this process (for leak
+ * checks around refused creates). */
+int64_t moe_debug_live_allocations(void);
+
+/* Host-side fault injection for tests: make the n-th device allocation from
+ * now on fail with MOE_ERR_OOM (n >= 1), or disable with n = 0. */
+void moe_debug_fail_allocation(int32_t n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_LAYER_H */

@@ -1,0 +1,759 @@
+// Device kernels of the quantized MoE decode layer (sm_103a).
+//
+// The layer (TensorFold PR #1038, Bolt latent MoE, "What's in it") is split
+// into five launches, each an HBM-streaming pass over one set of weights:
+//
+//   k_dense_in   router gemv + fc1_latent_proj + shared-expert gate/up gemv:
+//                every dense matrix that reads the layer input x, in one pass
+//   k_route      sigmoid/softmax top-k per row, combine weights, and the list
+//                of distinct selected experts with the rows routed to each
+//   k_expert     int4 affine dequant gemv over the distinct experts; used for
+//                the up(+gate) projection with the activation fused, and for
+//                the down projection
+//   k_dense_out  weighted combine of the expert outputs (fp32, pick order),
+//                fc2_latent_proj, shared-expert down gemv and the residual,
+//                rounded once to the activation dtype
+//
+// Dense gemv design: a CTA owns a contiguous range of output rows (so every
+// CTA streams the same number of bytes), its 256 threads stride the reduction
+// axis of each row with 16-byte loads, every thread keeps partial sums for a
+// batch of rows and all token rows of the pass, and the partials are reduced
+// once per batch with a warp reduce-scatter and a cross-warp pass in shared
+// memory.  The token rows are staged in shared memory as fp32 with an XOR
+// swizzle so that the 16-byte reads of a warp phase hit distinct banks.
+//
+// Expert gemv design: one warp per weight row; a lane takes 32 packed codes
+// (one 16-byte load, one quantisation group or part of one).  A code q becomes
+// the float 1 + q/16 with one shift and one logic op (q placed in the top
+// mantissa bits of 1.0f), so the inner product needs no integer conversion:
+//   sum_k (s q_k + b) x_k = 16 s * sum_k (1 + q_k/16) x_k + (b - 16 s) * sum_k x_k
+// per 32-element chunk, with the chunk sums of x computed once at staging.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int NT = 256;       // threads per CTA
+constexpr int NW = NT / 32;   // warps per CTA
+constexpr int RB = 4;         // dense rows per register batch
+constexpr int MAXC = 4;       // 16-byte chunks per thread per row per round
+constexpr int RED_ROWS = 64;  // dense rows per reduction round
+constexpr int MAX_E = 1024;   // routed experts served
+constexpr int MAX_K = 16;     // top-k served
+
+enum : int { DT_BF16 = 0, DT_FP16 = 1, DT_FP32 = 2 };
+enum : int { ACT_SWIGLU = 0, ACT_RELU2 = 1 };
+enum : int { ROUTER_SOFTMAX = 0, ROUTER_SIGMOID = 1 };
+enum : int { STATUS_NONFINITE = 1, STATUS_TIMEOUT = 2 };
+
+// ---------------------------------------------------------------------------
+// small helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t ldg_u32(const void* p) {
+  uint32_t r;
+  asm("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+__device__ __forceinline__ float f16lo(uint32_t v) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(v & 0xffffu)));
+}
+__device__ __forceinline__ float f16hi(uint32_t v) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(v >> 16)));
+}
+
+// 16-bit scalar load (act / scale dtype) to fp32
+__device__ __forceinline__ float ld16(const void* base, int64_t i, int dt) {
+  const unsigned short u = reinterpret_cast<const unsigned short*>(base)[i];
+  return dt == DT_BF16 ? __uint_as_float(static_cast<uint32_t>(u) << 16)
+                       : __half2float(__ushort_as_half(u));
+}
+
+__device__ __forceinline__ float ld_any(const void* base, int64_t i, int dt) {
+  if (dt == DT_FP32) return reinterpret_cast<const float*>(base)[i];
+  return ld16(base, i, dt);
+}
+
+__device__ __forceinline__ unsigned short st16_bits(float v, int dt) {
+  return dt == DT_BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v))
+                       : __half_as_ushort(__float2half_rn(v));
+}
+
+// 8 elements of a 16-bit chunk to fp32
+__device__ __forceinline__ void cvt8(const uint4 v, int dt, float f[8]) {
+  if (dt == DT_BF16) {
+    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x); f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+    f[4] = bf16lo(v.z); f[5] = bf16hi(v.z); f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+  } else {
+    f[0] = f16lo(v.x); f[1] = f16hi(v.x); f[2] = f16lo(v.y); f[3] = f16hi(v.y);
+    f[4] = f16lo(v.z); f[5] = f16hi(v.z); f[6] = f16lo(v.w); f[7] = f16hi(v.w);
+  }
+}
+
+// code q (bits 4n..4n+3 of w) -> float 1 + q/16
+template <int N>
+__device__ __forceinline__ float nib(uint32_t w) {
+  uint32_t t = (N <= 4) ? (w << (19 - 4 * N)) : (w >> (4 * N - 19));
+  return __uint_as_float((t & 0x00780000u) | 0x3f800000u);
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+__device__ __forceinline__ float act_fn(int act, float g, float u) {
+  if (act == ACT_SWIGLU) return silu(g) * u;
+  const float r = fmaxf(u, 0.0f);
+  return r * r;
+}
+
+// Swizzled float4 slot of element-float4 index f4 for readers that take
+// (nf4m1 + 1) consecutive float4 per 16-byte weight chunk.
+__device__ __forceinline__ int swz(int f4, int nf4m1) { return f4 ^ ((f4 >> 3) & nf4m1); }
+
+// Reduce NV values held by every lane of a warp.  Afterwards the lane with
+// (lane & (32/NV - 1)) == 0 holds the warp total of value (lane / (32/NV)).
+template <int NV>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[NV], int lane) {
+  static_assert(NV == 1 || NV == 2 || NV == 4 || NV == 8 || NV == 16 || NV == 32, "NV");
+  int n = NV;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    if (n > 1) {
+      const bool upper = (lane & o) != 0;
+      const int half = n >> 1;
+#pragma unroll
+      for (int i = 0; i < NV / 2; ++i) {
+        if (i < half) {
+          const float send = upper ? v[i] : v[i + half];
+          const float keep = upper ? v[i + half] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      n = half;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+    }
+  }
+  return v[0];
+}
+
+// ---------------------------------------------------------------------------
+// dense gemv (k_dense_in / k_dense_out)
+// ---------------------------------------------------------------------------
+
+// One weight matrix of a row segment, reading the staged vector at
+// [k0, k0 + wk).  Row r of the segment is at w + r * wk elements.
+struct DensePart {
+  const void* w;
+  int dt;
+  int k0;
+  int wk;
+};
+
+// Consecutive output rows [row0, row0 + rows) computed from up to two parts
+// (concatenated along the reduction axis).
+struct DenseSeg {
+  DensePart part[2];
+  int nparts;
+  int row0;
+  int rows;
+};
+
+struct DenseInArgs {
+  DenseSeg seg[4];
+  int nseg;
+  int total_rows;
+  int K;             // staged vector length (hidden)
+  const void* x;     // [T, K] act dtype
+  int x_dt;
+  float* out;        // [T, total_rows] fp32
+  int T;
+};
+
+struct DenseOutArgs {
+  DenseSeg seg[1];
+  int nseg;
+  int total_rows;    // hidden
+  int K;             // staged vector length: (latent) + shared_ffn
+  // staging sources
+  int latent;        // L (0: non-latent)
+  int shared;        // shared_ffn
+  int k;             // top_k
+  const float* pexp; // [T*k, Kin] unweighted expert outputs
+  const float* wts;  // [T*k] combine weights
+  const float* dense_in;  // [T, R_in]
+  int r_in;          // dense_in row stride
+  int sh_g_off, sh_u_off; // column offsets of shared gate/up logits in dense_in
+  int act;
+  // epilogue
+  const void* x;     // [T, H] residual, act dtype
+  int x_dt;
+  void* out;         // [T, H] act dtype
+  float* delta;      // [T, H] fp32 or null
+  int T;
+};
+
+// Streams the rows [r_begin, r_end) of the segments against xs (staged
+// [TB][K] swizzled fp32) and leaves per-(row, t) warp partials in red.
+template <int TB>
+__device__ __forceinline__ void dense_rows(const DenseSeg* segs, int nseg, int r_begin, int r_end,
+                                           const float4* xs4, int K4, float* red) {
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  int si = 0;
+  for (int r = r_begin; r < r_end;) {
+    while (r >= segs[si].row0 + segs[si].rows) ++si;
+    const DenseSeg& S = segs[si];
+    const int nb = min(RB, min(r_end, S.row0 + S.rows) - r);
+    float acc[RB][TB];
+#pragma unroll
+    for (int i = 0; i < RB; ++i)
+#pragma unroll
+      for (int t = 0; t < TB; ++t) acc[i][t] = 0.0f;
+
+    for (int p = 0; p < S.nparts; ++p) {
+      const DensePart P = S.part[p];
+      const int epc = (P.dt == DT_FP32) ? 4 : 8;         // elements per 16-byte chunk
+      const int nch = P.wk / epc;
+      const char* wbase = static_cast<const char*>(P.w) +
+                          (static_cast<int64_t>(r - S.row0) * P.wk) * (P.dt == DT_FP32 ? 4 : 2);
+      const int64_t rstride = static_cast<int64_t>(P.wk) * (P.dt == DT_FP32 ? 4 : 2);
+      for (int cbase = 0; cbase < nch; cbase += MAXC * NT) {
+        uint4 wv[RB][MAXC];
+#pragma unroll
+        for (int i = 0; i < RB; ++i)
+#pragma unroll
+          for (int c = 0; c < MAXC; ++c) {
+            const int ci = cbase + c * NT + tid;
+            if (i < nb && ci < nch)
+              wv[i][c] = ldg_stream(wbase + i * rstride + static_cast<int64_t>(ci) * 16);
+            else
+              wv[i][c] = make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+        for (int c = 0; c < MAXC; ++c) {
+          const int ci = cbase + c * NT + tid;
+          if (ci >= nch) continue;
+          if (epc == 8) {
+            const int f4 = (P.k0 >> 2) + 2 * ci;
+            const int s0 = swz(f4, 1), s1 = swz(f4 + 1, 1);
+#pragma unroll
+            for (int i = 0; i < RB; ++i) {
+              if (i >= nb) continue;
+              float wf[8];
+              cvt8(wv[i][c], P.dt, wf);
+#pragma unroll
+              for (int t = 0; t < TB; ++t) {
+                const float4 a = xs4[t * K4 + s0];
+                const float4 b = xs4[t * K4 + s1];
+                float s = acc[i][t];
+                s = fmaf(wf[0], a.x, s); s = fmaf(wf[1], a.y, s);
+                s = fmaf(wf[2], a.z, s); s = fmaf(wf[3], a.w, s);
+                s = fmaf(wf[4], b.x, s); s = fmaf(wf[5], b.y, s);
+                s = fmaf(wf[6], b.z, s); s = fmaf(wf[7], b.w, s);
+                acc[i][t] = s;
+              }
+            }
+          } else {
+            const int s0 = swz((P.k0 >> 2) + ci, 1);
+#pragma unroll
+            for (int i = 0; i < RB; ++i) {
+              if (i >= nb) continue;
+              const uint4 v = wv[i][c];
+#pragma unroll
+              for (int t = 0; t < TB; ++t) {
+                const float4 a = xs4[t * K4 + s0];
+                float s = acc[i][t];
+                s = fmaf(__uint_as_float(v.x), a.x, s); s = fmaf(__uint_as_float(v.y), a.y, s);
+                s = fmaf(__uint_as_float(v.z), a.z, s); s = fmaf(__uint_as_float(v.w), a.w, s);
+                acc[i][t] = s;
+              }
+            }
+          }
+        }
+      }
+    }
+    // warp reduce-scatter of RB*TB values, then one partial per warp to smem
+    constexpr int NV = RB * TB;
+    float v[NV];
+#pragma unroll
+    for (int i = 0; i < RB; ++i)
+#pragma unroll
+      for (int t = 0; t < TB; ++t) v[i * TB + t] = acc[i][t];
+    const float tot = warp_reduce_scatter<NV>(v, lane);
+    constexpr int LPV = 32 / NV;  // lanes per value
+    if ((lane & (LPV - 1)) == 0) {
+      const int vi = lane / LPV;
+      const int i = vi / TB, t = vi % TB;
+      if (i < nb) red[((r - r_begin + i) * TB + t) * NW + warp] = tot;
+    }
+    r += nb;
+  }
+}
+
+// Stage rows [t0, t0 + tb) of a [T, K] activation matrix (any dtype) as fp32,
+// swizzled for 8-element chunk readers; rows tb..TB-1 are zero.
+template <int TB>
+__device__ __forceinline__ void stage_x(float* xs, const void* x, int x_dt, int K, int t0, int tb) {
+  const int K4 = K >> 2;
+  for (int i = threadIdx.x; i < TB * K4; i += NT) {
+    const int t = i / K4, f4 = i - t * K4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < tb) {
+      const int64_t e = static_cast<int64_t>(t0 + t) * K + 4 * f4;
+      v.x = ld_any(x, e, x_dt); v.y = ld_any(x, e + 1, x_dt);
+      v.z = ld_any(x, e + 2, x_dt); v.w = ld_any(x, e + 3, x_dt);
+    }
+    reinterpret_cast<float4*>(xs)[t * K4 + swz(f4, 1)] = v;
+  }
+}
+
+// Rows per CTA for a dense launch of `rows` rows over `grid` CTAs.
+__device__ __forceinline__ void cta_rows(int rows, int& b, int& e) {
+  const int64_t c = blockIdx.x, g = gridDim.x;
+  b = static_cast<int>(c * rows / g);
+  e = static_cast<int>((c + 1) * rows / g);
+}
+
+template <int TB>
+__global__ void __launch_bounds__(NT) k_dense_in(const DenseInArgs A) {
+  extern __shared__ float4 smem4[];
+  float* xs = reinterpret_cast<float*>(smem4);
+  float* red = xs + TB * A.K;
+  const int K4 = A.K >> 2;
+  int rb, re;
+  cta_rows(A.total_rows, rb, re);
+  for (int t0 = 0; t0 < A.T; t0 += TB) {
+    const int tb = min(TB, A.T - t0);
+    if (t0) __syncthreads();
+    stage_x<TB>(xs, A.x, A.x_dt, A.K, t0, tb);
+    __syncthreads();
+    for (int r0 = rb; r0 < re; r0 += RED_ROWS) {
+      const int r1 = min(re, r0 + RED_ROWS);
+      dense_rows<TB>(A.seg, A.nseg, r0, r1, smem4, K4, red);
+      __syncthreads();
+      for (int o = threadIdx.x; o < (r1 - r0) * TB; o += NT) {
+        const int rl = o / TB, t = o % TB;
+        if (t >= tb) continue;
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) s += red[o * NW + w];
+        A.out[static_cast<int64_t>(t0 + t) * A.total_rows + r0 + rl] = s;
+      }
+      __syncthreads();
+    }
+  }
+}
+
+template <int TB>
+__global__ void __launch_bounds__(NT) k_dense_out(const DenseOutArgs A) {
+  extern __shared__ float4 smem4[];
+  float* xs = reinterpret_cast<float*>(smem4);
+  float* red = xs + TB * A.K;
+  const int K4 = A.K >> 2;
+  const int L = A.latent;
+  const int Kin = L ? L : A.total_rows;
+  int rb, re;
+  cta_rows(A.total_rows, rb, re);
+  for (int t0 = 0; t0 < A.T; t0 += TB) {
+    const int tb = min(TB, A.T - t0);
+    if (t0) __syncthreads();
+    // staged vector: [combined routed output y (latent only) | shared activation]
+    for (int i = threadIdx.x; i < TB * K4; i += NT) {
+      const int t = i / K4, f4 = i - t * K4;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (t < tb) {
+        const int tt = t0 + t;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int kk = 4 * f4 + j;
+          if (kk < L) {
+            float y = 0.f;
+            for (int p = 0; p < A.k; ++p)
+              y = fmaf(A.wts[tt * A.k + p],
+                       A.pexp[static_cast<int64_t>(tt * A.k + p) * Kin + kk], y);
+            v[j] = y;
+          } else {
+            const int f = kk - L;
+            const float* di = A.dense_in + static_cast<int64_t>(tt) * A.r_in;
+            const float u = di[A.sh_u_off + f];
+            const float g = (A.act == ACT_SWIGLU) ? di[A.sh_g_off + f] : 0.f;
+            v[j] = act_fn(A.act, g, u);
+          }
+        }
+      }
+      smem4[t * K4 + swz(f4, 1)] = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    __syncthreads();
+    for (int r0 = rb; r0 < re; r0 += RED_ROWS) {
+      const int r1 = min(re, r0 + RED_ROWS);
+      if (A.nseg) dense_rows<TB>(A.seg, A.nseg, r0, r1, smem4, K4, red);
+      __syncthreads();
+      for (int o = threadIdx.x; o < (r1 - r0) * TB; o += NT) {
+        const int rl = o / TB, t = o % TB;
+        if (t >= tb) continue;
+        const int tt = t0 + t, n = r0 + rl;
+        float s = 0.f;
+        if (A.nseg) {
+#pragma unroll
+          for (int w = 0; w < NW; ++w) s += red[o * NW + w];
+        }
+        if (!L) {  // non-latent: routed output is added directly
+          float y = 0.f;
+          for (int p = 0; p < A.k; ++p)
+            y = fmaf(A.wts[tt * A.k + p], A.pexp[static_cast<int64_t>(tt * A.k + p) * Kin + n], y);
+          s += y;
+        }
+        const int64_t e = static_cast<int64_t>(tt) * A.total_rows + n;
+        const float xv = ld16(A.x, e, A.x_dt);
+        reinterpret_cast<unsigned short*>(A.out)[e] = st16_bits(xv + s, A.x_dt);
+        if (A.delta) A.delta[e] = s;
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// routing: top-k, weights, distinct-expert lists
+// ---------------------------------------------------------------------------
+
+// Route metadata (int32 buffer):
+//   [0]                      n_uniq
+//   [1, 1 + umax)            uniq_e[u]   distinct selected experts, ascending
+//   [1 + umax, 2 + 2 umax)   uniq_p0[u]  first position of u's pairs (u = n_uniq: total)
+//   [2 + 2 umax, ...)        pairs[i]    pair ids t*k + j grouped by expert, t ascending
+struct RouteArgs {
+  const float* logits;   // dense_in, row stride r_in, experts at columns [0, E)
+  int r_in;
+  const float* bias;     // [E] or null
+  int E, k, T;
+  int router, renorm;
+  float scale;
+  int* ids;              // [T*k]
+  float* w;              // [T*k]
+  int* meta;
+  int umax;
+  int* ext_ids;          // optional copies for the caller
+  float* ext_w;
+  int* status;
+};
+
+__device__ __forceinline__ bool key_better(float a, int ia, float b, int ib) {
+  return a > b || (a == b && ia < ib);
+}
+
+__global__ void __launch_bounds__(1024) k_route(const RouteArgs A) {
+  __shared__ int s_cnt[MAX_E];
+  __shared__ int s_scan_c[MAX_E];
+  __shared__ int s_wsum_u[32], s_wsum_c[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = blockDim.x >> 5;
+  const int E = A.E, k = A.k;
+  const int nper = (E + 31) >> 5;
+
+  for (int t = warp; t < A.T; t += nwarp) {
+    const float* z = A.logits + static_cast<int64_t>(t) * A.r_in;
+    float key[32];
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = lane + 32 * i;
+      float kv = -INFINITY;
+      if (i < nper && e < E) {
+        const float zz = z[e];
+        kv = (A.router == ROUTER_SOFTMAX) ? zz : 1.0f / (1.0f + expf(-zz));
+        if (A.router == ROUTER_SIGMOID && A.bias) kv += A.bias[e];
+        if (!isfinite(kv)) { bad = true; kv = -INFINITY; }
+      }
+      key[i] = kv;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(A.status, STATUS_NONFINITE);
+    uint32_t taken = 0;
+    int my_id = -1;
+    for (int j = 0; j < k; ++j) {
+      float bk = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int e = lane + 32 * i;
+        if (i < nper && e < E && !((taken >> i) & 1u) && key_better(key[i], e, bk, bi)) {
+          bk = key[i]; bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (key_better(ok, oi, bk, bi)) { bk = ok; bi = oi; }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == j) my_id = bi;
+    }
+    // combine weights (lane j < k holds pick j)
+    float zj = (lane < k) ? z[my_id] : 0.f;
+    float wv = 0.f;
+    if (A.router == ROUTER_SOFTMAX) {
+      float m = __shfl_sync(0xffffffffu, zj, 0);   // largest selected logit
+      float den = 0.f;
+      if (A.renorm) {
+        float ex = (lane < k) ? expf(zj - m) : 0.f;
+        den = ex;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        wv = ex / den;
+      } else {
+        float mm = -INFINITY;
+        for (int i = lane; i < E; i += 32) mm = fmaxf(mm, z[i]);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+        for (int i = lane; i < E; i += 32) den += expf(z[i] - mm);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        wv = (lane < k) ? expf(zj - mm) / den : 0.f;
+      }
+    } else {
+      const float s = (lane < k) ? 1.0f / (1.0f + expf(-zj)) : 0.f;
+      wv = s;
+      if (A.renorm) {
+        float den = s;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        wv = s / den;
+      }
+    }
+    wv *= A.scale;
+    if (lane < k) {
+      A.ids[t * k + lane] = my_id;
+      A.w[t * k + lane] = wv;
+      if (A.ext_ids) A.ext_ids[t * k + lane] = my_id;
+      if (A.ext_w) A.ext_w[t * k + lane] = wv;
+    }
+  }
+  // ---- distinct experts and their pairs ----
+  for (int e = tid; e < MAX_E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  const int P = A.T * k;
+  for (int p = tid; p < P; p += blockDim.x) atomicAdd(&s_cnt[A.ids[p]], 1);
+  __syncthreads();
+  // exclusive scans over experts of (cnt > 0) and cnt; blockDim == MAX_E
+  {
+    const int e = tid;
+    int vu = (e < E && s_cnt[e] > 0) ? 1 : 0;
+    int vc = (e < E) ? s_cnt[e] : 0;
+    int iu = vu, ic = vc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, iu, o);
+      const int b = __shfl_up_sync(0xffffffffu, ic, o);
+      if (lane >= o) { iu += a; ic += b; }
+    }
+    if (lane == 31) { s_wsum_u[warp] = iu; s_wsum_c[warp] = ic; }
+    __syncthreads();
+    if (warp == 0) {
+      int a = (lane < nwarp) ? s_wsum_u[lane] : 0;
+      int b = (lane < nwarp) ? s_wsum_c[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, a, o);
+        const int y = __shfl_up_sync(0xffffffffu, b, o);
+        if (lane >= o) { a += x; b += y; }
+      }
+      s_wsum_u[lane] = a;  // inclusive warp prefix
+      s_wsum_c[lane] = b;
+    }
+    __syncthreads();
+    const int pu = (warp ? s_wsum_u[warp - 1] : 0) + iu - vu;
+    const int pc = (warp ? s_wsum_c[warp - 1] : 0) + ic - vc;
+    s_scan_c[e] = pc;
+    int* uniq_e = A.meta + 1;
+    int* uniq_p0 = A.meta + 1 + A.umax;
+    if (vu) { uniq_e[pu] = e; uniq_p0[pu] = pc; }
+    if (e == MAX_E - 1) {
+      const int nu = pu + vu;
+      A.meta[0] = nu;
+      uniq_p0[nu] = pc + vc;
+    }
+  }
+  __syncthreads();
+  int* pairs = A.meta + 2 + 2 * A.umax;
+  for (int p = tid; p < P; p += blockDim.x) {
+    const int e = A.ids[p];
+    int rank = 0;
+    for (int q = 0; q < p; ++q) rank += (A.ids[q] == e);
+    pairs[s_scan_c[e] + rank] = p;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// int4 affine expert gemv (k_expert)
+// ---------------------------------------------------------------------------
+
+struct ExpertArgs {
+  int n_rows;              // output rows per expert
+  int K;                   // reduction length
+  int G;                   // group size
+  const uint32_t* q;       // [E, n_rows, K/8]
+  const uint32_t* sb;      // [E, n_rows, K/G]  (scale bits | bias bits << 16)
+  const uint32_t* q_gate;  // SWIGLU up only: gate codes, else null
+  const uint32_t* sb_gate;
+  int s_dt;                // scale dtype
+  int act;                 // activation applied to the output (-1: none)
+  const int* meta;         // route metadata
+  int umax;
+  int k;                   // top_k
+  // input row of pair p: by token (t = p / k) or by pair
+  const void* xin;
+  int xin_dt;
+  int64_t xin_stride;      // elements between rows
+  int64_t xin_off;         // element offset of the first row
+  int xin_by_pair;
+  float* out;              // [T*k, n_rows]
+};
+
+__device__ __forceinline__ void sb_decode(uint32_t v, int dt, float& s, float& b) {
+  if (dt == DT_BF16) { s = bf16lo(v); b = bf16hi(v); }
+  else { s = f16lo(v); b = f16hi(v); }
+}
+
+// one 32-code chunk (uint4) against one staged row; returns sum (1 + q/16) x
+__device__ __forceinline__ float chunk_dot(const uint4 w, const float4* x8, int c) {
+  const int sw = c & 7;
+  float s = 0.f;
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 a = x8[(2 * i) ^ sw];
+    const float4 b = x8[(2 * i + 1) ^ sw];
+    const uint32_t v = ws[i];
+    s = fmaf(nib<0>(v), a.x, s); s = fmaf(nib<1>(v), a.y, s);
+    s = fmaf(nib<2>(v), a.z, s); s = fmaf(nib<3>(v), a.w, s);
+    s = fmaf(nib<4>(v), b.x, s); s = fmaf(nib<5>(v), b.y, s);
+    s = fmaf(nib<6>(v), b.z, s); s = fmaf(nib<7>(v), b.w, s);
+  }
+  return s;
+}
+
+template <int PB>
+__global__ void __launch_bounds__(NT) k_expert(const ExpertArgs A) {
+  extern __shared__ float4 smem4[];
+  const int K = A.K, K4 = K >> 2, nchunk = K >> 5;
+  float* xsum = reinterpret_cast<float*>(smem4 + PB * K4);   // [PB][nchunk]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n_uniq = A.meta[0];
+  const int* uniq_e = A.meta + 1;
+  const int* uniq_p0 = A.meta + 1 + A.umax;
+  const int* pairs = A.meta + 2 + 2 * A.umax;
+  const int64_t total = static_cast<int64_t>(n_uniq) * A.n_rows;
+  const int64_t rb = blockIdx.x * total / gridDim.x, re = (blockIdx.x + 1) * total / gridDim.x;
+  const int ngr = K / A.G;
+  const bool gated = A.q_gate != nullptr;
+  for (int64_t r0 = rb; r0 < re;) {
+    const int u = static_cast<int>(r0 / A.n_rows);
+    const int64_t uend = min(re, static_cast<int64_t>(u + 1) * A.n_rows);
+    const int e = uniq_e[u];
+    const int pa = uniq_p0[u], pe = uniq_p0[u + 1];
+    for (int pc = pa; pc < pe; pc += PB) {
+      const int np = min(PB, pe - pc);
+      __syncthreads();
+      // stage the input rows of pairs [pc, pc + np), swizzled for 32-element chunks
+      for (int i = threadIdx.x; i < PB * K4; i += NT) {
+        const int pp = i / K4, f4 = i - pp * K4;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (pp < np) {
+          const int pid = pairs[pc + pp];
+          const int64_t row = A.xin_by_pair ? pid : (pid / A.k);
+          const int64_t base = A.xin_off + row * A.xin_stride + 4 * f4;
+          v.x = ld_any(A.xin, base, A.xin_dt); v.y = ld_any(A.xin, base + 1, A.xin_dt);
+          v.z = ld_any(A.xin, base + 2, A.xin_dt); v.w = ld_any(A.xin, base + 3, A.xin_dt);
+        }
+        smem4[pp * K4 + swz(f4, 7)] = v;
+      }
+      __syncthreads();
+      for (int i = threadIdx.x; i < PB * nchunk; i += NT) {
+        const int pp = i / nchunk, c = i - pp * nchunk;
+        const float4* x8 = smem4 + pp * K4 + 8 * c;
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) { const float4 a = x8[j]; s += (a.x + a.y) + (a.z + a.w); }
+        xsum[pp * nchunk + c] = s;
+      }
+      __syncthreads();
+      // rows of expert u in this CTA: one warp per row
+      for (int64_t r = r0 + warp; r < uend; r += NW) {
+        const int n = static_cast<int>(r - static_cast<int64_t>(u) * A.n_rows);
+        const int64_t rowq = (static_cast<int64_t>(e) * A.n_rows + n) * (K >> 3);
+        const int64_t rows = (static_cast<int64_t>(e) * A.n_rows + n) * ngr;
+        float acc[PB], accg[PB];
+#pragma unroll
+        for (int pp = 0; pp < PB; ++pp) { acc[pp] = 0.f; accg[pp] = 0.f; }
+        for (int c = lane; c < nchunk; c += 32) {
+          const uint4 w = ldg_stream(A.q + rowq + 4 * c);
+          const int g = (c << 5) / A.G;
+          float s, b;
+          sb_decode(ldg_u32(A.sb + rows + g), A.s_dt, s, b);
+          const float s16 = 16.f * s, bb = b - s16;
+          uint4 wg = make_uint4(0u, 0u, 0u, 0u);
+          float sg16 = 0.f, bbg = 0.f;
+          if (gated) {
+            wg = ldg_stream(A.q_gate + rowq + 4 * c);
+            float sg, bg;
+            sb_decode(ldg_u32(A.sb_gate + rows + g), A.s_dt, sg, bg);
+            sg16 = 16.f * sg; bbg = bg - sg16;
+          }
+#pragma unroll
+          for (int pp = 0; pp < PB; ++pp) {
+            if (pp < np) {
+              const float4* x8 = smem4 + pp * K4 + 8 * c;
+              const float xs = xsum[pp * nchunk + c];
+              acc[pp] = fmaf(s16, chunk_dot(w, x8, c), fmaf(bb, xs, acc[pp]));
+              if (gated) accg[pp] = fmaf(sg16, chunk_dot(wg, x8, c), fmaf(bbg, xs, accg[pp]));
+            }
+          }
+        }
+#pragma unroll
+        for (int pp = 0; pp < PB; ++pp) {
+          if (pp < np) {
+            float a = acc[pp], g = accg[pp];
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+              a += __shfl_xor_sync(0xffffffffu, a, o);
+              if (gated) g += __shfl_xor_sync(0xffffffffu, g, o);
+            }
+            if (lane == 0) {
+              const int pid = pairs[pc + pp];
+              const float v = (A.act >= 0) ? act_fn(A.act, g, a) : a;
+              A.out[static_cast<int64_t>(pid) * A.n_rows + n] = v;
+            }
+          }
+        }
+      }
+    }
+    r0 = uend;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// create-time re-layout: interleave a group's scale and bias into one word
+// ---------------------------------------------------------------------------
+__global__ void k_interleave_sb(const unsigned short* __restrict__ s,
+                                const unsigned short* __restrict__ b, uint32_t* __restrict__ out,
+                                int64_t n) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    out[i] = static_cast<uint32_t>(s[i]) | (static_cast<uint32_t>(b[i]) << 16);
+}
+
+}  // namespace moe

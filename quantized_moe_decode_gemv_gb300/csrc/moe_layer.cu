@@ -1,0 +1,702 @@
+// Host side of the quantized MoE decode layer: validation, create/destroy,
+// forward orchestration and the C ABI declared in include/moe_layer.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "moe_layer.h"
+#include "moe_kernels.cuh"
+
+using namespace moe;
+
+namespace {
+
+constexpr int kSmemMax = 227 * 1024;
+
+std::atomic<int64_t> g_live_allocs{0};
+std::atomic<int32_t> g_fail_countdown{0};
+thread_local std::string g_create_error;
+
+bool alloc_should_fail() {
+  int32_t c = g_fail_countdown.load();
+  while (c > 0) {
+    if (g_fail_countdown.compare_exchange_weak(c, c - 1)) return c == 1;
+  }
+  return false;
+}
+
+int dt_size(int dt) { return dt == DT_FP32 ? 4 : 2; }
+
+}  // namespace
+
+struct moe_layer {
+  moe_layer_config cfg{};
+  int device = -1;
+  int num_sms = 0;
+  int path = MOE_PATH_AUTO;
+  std::vector<void*> allocs;
+  int64_t bytes = 0;
+  std::string last_error;
+
+  // library-owned weights
+  void* router_w = nullptr;
+  float* router_bias = nullptr;
+  void* fc1 = nullptr;
+  void* fc2 = nullptr;
+  uint32_t *gate_q = nullptr, *up_q = nullptr, *down_q = nullptr;
+  uint32_t *gate_sb = nullptr, *up_sb = nullptr, *down_sb = nullptr;
+  void *sh_gate = nullptr, *sh_up = nullptr, *sh_down = nullptr;
+
+  // workspace
+  float* dense_in = nullptr;  // [Tmax, r_in]
+  int* ids = nullptr;         // [Tmax*k]
+  float* wts = nullptr;       // [Tmax*k]
+  int* meta = nullptr;
+  float* hbuf = nullptr;      // [Tmax*k, F]
+  float* pexp = nullptr;      // [Tmax*k, Kin]
+  int* status = nullptr;
+  void* x_stage = nullptr;    // [Tmax, H] act dtype (host-buffer forward)
+  void* out_stage = nullptr;
+
+  // per-stage timing
+  bool profiling = false;
+  bool profiled = false;
+  cudaEvent_t ev[MOE_NUM_STAGES + 1] = {};
+
+  int r_in = 0, off_fc1 = 0, off_shg = 0, off_shu = 0;
+  int umax = 0;
+  int kin = 0;
+
+  cudaError_t alloc(void** p, size_t n) {
+    *p = nullptr;
+    if (alloc_should_fail()) return cudaErrorMemoryAllocation;
+    cudaError_t e = cudaMalloc(p, n ? n : 16);
+    if (e == cudaSuccess) {
+      allocs.push_back(*p);
+      bytes += static_cast<int64_t>(n);
+      g_live_allocs.fetch_add(1);
+    }
+    return e;
+  }
+  void free_events() {
+    for (auto& e : ev) {
+      if (e) cudaEventDestroy(e);
+      e = nullptr;
+    }
+  }
+  void free_all() {
+    free_events();
+    for (void* p : allocs) {
+      cudaFree(p);
+      g_live_allocs.fetch_sub(1);
+    }
+    allocs.clear();
+    bytes = 0;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// validation
+// ---------------------------------------------------------------------------
+
+static moe_status validate_impl(const moe_layer_config* c, const moe_layer_weights* w,
+                                std::string* why) {
+  auto fail = [&](moe_status s, const char* msg) {
+    if (why) *why = msg;
+    return s;
+  };
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "config is NULL");
+  if (c->hidden <= 0 || c->n_experts <= 0 || c->expert_ffn <= 0 || c->max_tokens <= 0 ||
+      c->latent < 0 || c->shared_ffn < 0)
+    return fail(MOE_ERR_INVALID_ARG, "sizes must be positive (latent/shared_ffn >= 0)");
+  if (c->act != MOE_ACT_SWIGLU && c->act != MOE_ACT_RELU2)
+    return fail(MOE_ERR_INVALID_ARG, "unknown activation");
+  if (c->router != MOE_ROUTER_SOFTMAX && c->router != MOE_ROUTER_SIGMOID)
+    return fail(MOE_ERR_INVALID_ARG, "unknown router");
+  if (c->act_dtype < 0 || c->act_dtype > 2 || c->scale_dtype < 0 || c->scale_dtype > 2 ||
+      c->router_dtype < 0 || c->router_dtype > 2)
+    return fail(MOE_ERR_INVALID_ARG, "unknown dtype");
+  if (c->top_k < 1 || c->top_k > c->n_experts)
+    return fail(MOE_ERR_TOPK_GT_E, "top_k must be in 1..n_experts");
+  if (c->latent > 0) {
+    if (c->act_dtype == MOE_DTYPE_FP32)
+      return fail(MOE_ERR_LATENT_PROJ, "latent projections must be bf16 or fp16");
+    if (w && (!w->fc1_latent || !w->fc2_latent))
+      return fail(MOE_ERR_LATENT_PROJ, "latent layer without fc1_latent_proj/fc2_latent_proj");
+  } else if (w && (w->fc1_latent || w->fc2_latent)) {
+    return fail(MOE_ERR_LATENT_PROJ, "latent projections given for a non-latent layer");
+  }
+  const int G = c->group_size;
+  if (G != 32 && G != 64 && G != 128) return fail(MOE_ERR_SHAPE, "group_size must be 32, 64 or 128");
+  const int kin = c->latent > 0 ? c->latent : c->hidden;
+  if (c->hidden % 64 || c->expert_ffn % 64 || kin % 64 || (c->shared_ffn % 64))
+    return fail(MOE_ERR_SHAPE, "hidden, expert_ffn, latent and shared_ffn must be multiples of 64");
+  if (kin % G || c->expert_ffn % G)
+    return fail(MOE_ERR_SHAPE, "expert input width and expert_ffn must be multiples of group_size");
+  if (c->n_experts > MAX_E) return fail(MOE_ERR_UNSUPPORTED, "more than 1024 experts");
+  if (c->top_k > MAX_K) return fail(MOE_ERR_UNSUPPORTED, "top_k above 16");
+  if (c->act_dtype == MOE_DTYPE_FP32) return fail(MOE_ERR_UNSUPPORTED, "fp32 activations");
+  if (c->scale_dtype == MOE_DTYPE_FP32) return fail(MOE_ERR_UNSUPPORTED, "fp32 scales");
+  if (c->has_router_bias && c->router != MOE_ROUTER_SIGMOID)
+    return fail(MOE_ERR_UNSUPPORTED, "router bias is defined for sigmoid routing only");
+  if (w) {
+    if (!w->router_w) return fail(MOE_ERR_INVALID_ARG, "router weight missing");
+    if (c->has_router_bias && !w->router_bias) return fail(MOE_ERR_INVALID_ARG, "router bias missing");
+    if (!w->up_q || !w->up_s || !w->up_b || !w->down_q || !w->down_s || !w->down_b)
+      return fail(MOE_ERR_INVALID_ARG, "expert up/down weights missing");
+    if (c->act == MOE_ACT_SWIGLU && (!w->gate_q || !w->gate_s || !w->gate_b))
+      return fail(MOE_ERR_INVALID_ARG, "SwiGLU experts need gate weights");
+    if (c->act == MOE_ACT_RELU2 && (w->gate_q || w->sh_gate))
+      return fail(MOE_ERR_SHAPE, "squared-ReLU experts take no gate matrix");
+    if (c->shared_ffn > 0) {
+      if (!w->sh_up || !w->sh_down || (c->act == MOE_ACT_SWIGLU && !w->sh_gate))
+        return fail(MOE_ERR_UNSUPPORTED, "shared expert weights missing");
+    } else if (w->sh_up || w->sh_down || w->sh_gate) {
+      return fail(MOE_ERR_SHAPE, "shared expert weights given with shared_ffn = 0");
+    }
+  }
+  return MOE_OK;
+}
+
+// dense staging rows per pass that fit shared memory for a staged width K
+static int dense_tb_cap(int K) {
+  for (int tb = 8; tb >= 1; tb >>= 1)
+    if (static_cast<int64_t>(tb) * (4LL * K + 4LL * RED_ROWS * NW) <= kSmemMax) return tb;
+  return 0;
+}
+static int expert_pb_cap(int K) {
+  for (int pb = 8; pb >= 1; pb >>= 1)
+    if (static_cast<int64_t>(pb) * (4LL * K + 4LL * (K / 32)) <= kSmemMax) return pb;
+  return 0;
+}
+static int pow2_at_least(int t, int cap) {
+  int v = 1;
+  while (v < t && v < cap) v <<= 1;
+  return std::min(v, cap);
+}
+
+// ---------------------------------------------------------------------------
+// launches
+// ---------------------------------------------------------------------------
+
+template <int TB>
+static size_t dense_smem(int K) {
+  return static_cast<size_t>(TB) * (4ull * K + 4ull * RED_ROWS * NW);
+}
+
+template <typename Args, int TB>
+static cudaError_t launch_dense_in_t(const Args& a, int grid, cudaStream_t s) {
+  k_dense_in<TB><<<grid, NT, dense_smem<TB>(a.K), s>>>(a);
+  return cudaGetLastError();
+}
+template <typename Args, int TB>
+static cudaError_t launch_dense_out_t(const Args& a, int grid, cudaStream_t s) {
+  k_dense_out<TB><<<grid, NT, dense_smem<TB>(a.K), s>>>(a);
+  return cudaGetLastError();
+}
+template <int PB>
+static cudaError_t launch_expert_t(const ExpertArgs& a, int grid, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(PB) * (4ull * a.K + 4ull * (a.K / 32));
+  k_expert<PB><<<grid, NT, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+static cudaError_t launch_dense_in(const DenseInArgs& a, int tb, int grid, cudaStream_t s) {
+  switch (tb) {
+    case 1: return launch_dense_in_t<DenseInArgs, 1>(a, grid, s);
+    case 2: return launch_dense_in_t<DenseInArgs, 2>(a, grid, s);
+    case 4: return launch_dense_in_t<DenseInArgs, 4>(a, grid, s);
+    default: return launch_dense_in_t<DenseInArgs, 8>(a, grid, s);
+  }
+}
+static cudaError_t launch_dense_out(const DenseOutArgs& a, int tb, int grid, cudaStream_t s) {
+  switch (tb) {
+    case 1: return launch_dense_out_t<DenseOutArgs, 1>(a, grid, s);
+    case 2: return launch_dense_out_t<DenseOutArgs, 2>(a, grid, s);
+    case 4: return launch_dense_out_t<DenseOutArgs, 4>(a, grid, s);
+    default: return launch_dense_out_t<DenseOutArgs, 8>(a, grid, s);
+  }
+}
+static cudaError_t launch_expert(const ExpertArgs& a, int pb, int grid, cudaStream_t s) {
+  switch (pb) {
+    case 1: return launch_expert_t<1>(a, grid, s);
+    case 2: return launch_expert_t<2>(a, grid, s);
+    case 4: return launch_expert_t<4>(a, grid, s);
+    default: return launch_expert_t<8>(a, grid, s);
+  }
+}
+
+static cudaError_t set_smem_attrs() {
+  cudaError_t e = cudaSuccess;
+#define MOE_SMEM_ATTR(fn)                                                              \
+  if (e == cudaSuccess)                                                                \
+    e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),                        \
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+  MOE_SMEM_ATTR(k_dense_in<1>) MOE_SMEM_ATTR(k_dense_in<2>) MOE_SMEM_ATTR(k_dense_in<4>)
+  MOE_SMEM_ATTR(k_dense_in<8>) MOE_SMEM_ATTR(k_dense_out<1>) MOE_SMEM_ATTR(k_dense_out<2>)
+  MOE_SMEM_ATTR(k_dense_out<4>) MOE_SMEM_ATTR(k_dense_out<8>) MOE_SMEM_ATTR(k_expert<1>)
+  MOE_SMEM_ATTR(k_expert<2>) MOE_SMEM_ATTR(k_expert<4>) MOE_SMEM_ATTR(k_expert<8>)
+#undef MOE_SMEM_ATTR
+  return e;
+}
+
+// ---------------------------------------------------------------------------
+// create / destroy
+// ---------------------------------------------------------------------------
+
+#define MOE_TRY_CUDA(call, msg)                                              \
+  do {                                                                       \
+    cudaError_t _e = (call);                                                 \
+    if (_e != cudaSuccess) {                                                 \
+      why = std::string(msg) + ": " + cudaGetErrorString(_e);                \
+      st = (_e == cudaErrorMemoryAllocation) ? MOE_ERR_OOM : MOE_ERR_CUDA;   \
+      goto fail;                                                             \
+    }                                                                        \
+  } while (0)
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+moe_status moe_layer_validate(const moe_layer_config* cfg, const moe_layer_weights* w) {
+  std::string why;
+  moe_status s = validate_impl(cfg, w, &why);
+  if (s != MOE_OK) g_create_error = why;
+  return s;
+}
+
+moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights* w, void* stream,
+                            moe_layer** out) {
+  std::string why;
+  moe_status st = MOE_OK;
+  moe_layer* L = nullptr;
+  if (out) *out = nullptr;
+  if (!out || !w) {
+    g_create_error = "out and weights must not be NULL";
+    return MOE_ERR_INVALID_ARG;
+  }
+  st = validate_impl(cfg, w, &why);
+  if (st != MOE_OK) {
+    g_create_error = why;
+    return st;
+  }
+  int dev = 0;
+  cudaDeviceProp prop;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+    g_create_error = "no CUDA device";
+    return MOE_ERR_DEVICE;
+  }
+  if (!(prop.major == 10 && prop.minor == 3)) {
+    g_create_error = std::string("device ") + prop.name + " is not compute capability 10.3";
+    return MOE_ERR_DEVICE;
+  }
+  const moe_layer_config& c = *cfg;
+  const int H = c.hidden, E = c.n_experts, k = c.top_k, F = c.expert_ffn, G = c.group_size;
+  const int Lt = c.latent, Fs = c.shared_ffn, T = c.max_tokens;
+  const int kin = Lt ? Lt : H;
+  const bool gated = c.act == MOE_ACT_SWIGLU;
+  const int kout = (Lt ? Lt : 0) + Fs;
+  if (!dense_tb_cap(H) || (kout && !dense_tb_cap(kout)) || !expert_pb_cap(kin) ||
+      !expert_pb_cap(F)) {
+    g_create_error = "a reduction width exceeds the shared-memory staging limit";
+    return MOE_ERR_UNSUPPORTED;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  L = new moe_layer();
+  L->cfg = c;
+  L->device = dev;
+  L->num_sms = prop.multiProcessorCount;
+  L->kin = kin;
+  L->off_fc1 = E;
+  L->off_shg = E + Lt;
+  L->off_shu = E + Lt + (gated ? Fs : 0);
+  L->r_in = L->off_shu + Fs;
+  L->umax = std::min(E, T * k);
+  {
+    const size_t adt = dt_size(c.act_dtype), rdt = dt_size(c.router_dtype);
+    const size_t sdt = dt_size(c.scale_dtype);
+    const size_t nq_in = static_cast<size_t>(E) * F * (kin / 8);
+    const size_t ng_in = static_cast<size_t>(E) * F * (kin / G);
+    const size_t nq_dn = static_cast<size_t>(E) * kin * (F / 8);
+    const size_t ng_dn = static_cast<size_t>(E) * kin * (F / G);
+    (void)sdt;
+    MOE_TRY_CUDA(set_smem_attrs(), "kernel attributes");
+    MOE_TRY_CUDA(L->alloc(&L->router_w, static_cast<size_t>(E) * H * rdt), "router weight");
+    MOE_TRY_CUDA(cudaMemcpyAsync(L->router_w, w->router_w, static_cast<size_t>(E) * H * rdt,
+                                 cudaMemcpyDeviceToDevice, s), "router weight copy");
+    if (c.has_router_bias) {
+      MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->router_bias), E * sizeof(float)), "router bias");
+      MOE_TRY_CUDA(cudaMemcpyAsync(L->router_bias, w->router_bias, E * sizeof(float),
+                                   cudaMemcpyDeviceToDevice, s), "router bias copy");
+    }
+    if (Lt) {
+      const size_t n = static_cast<size_t>(Lt) * H * adt;
+      MOE_TRY_CUDA(L->alloc(&L->fc1, n), "fc1");
+      MOE_TRY_CUDA(cudaMemcpyAsync(L->fc1, w->fc1_latent, n, cudaMemcpyDeviceToDevice, s), "fc1 copy");
+      MOE_TRY_CUDA(L->alloc(&L->fc2, n), "fc2");
+      MOE_TRY_CUDA(cudaMemcpyAsync(L->fc2, w->fc2_latent, n, cudaMemcpyDeviceToDevice, s), "fc2 copy");
+    }
+    auto copy_q = [&](uint32_t** dst, const uint32_t* src, size_t n) -> cudaError_t {
+      cudaError_t e = L->alloc(reinterpret_cast<void**>(dst), n * 4);
+      if (e != cudaSuccess) return e;
+      return cudaMemcpyAsync(*dst, src, n * 4, cudaMemcpyDeviceToDevice, s);
+    };
+    auto copy_sb = [&](uint32_t** dst, const void* sc, const void* bi, size_t n) -> cudaError_t {
+      cudaError_t e = L->alloc(reinterpret_cast<void**>(dst), n * 4);
+      if (e != cudaSuccess) return e;
+      const int blocks = static_cast<int>(std::min<size_t>((n + 255) / 256, 4096));
+      k_interleave_sb<<<blocks, 256, 0, s>>>(static_cast<const unsigned short*>(sc),
+                                             static_cast<const unsigned short*>(bi), *dst,
+                                             static_cast<int64_t>(n));
+      return cudaGetLastError();
+    };
+    if (gated) {
+      MOE_TRY_CUDA(copy_q(&L->gate_q, w->gate_q, nq_in), "gate codes");
+      MOE_TRY_CUDA(copy_sb(&L->gate_sb, w->gate_s, w->gate_b, ng_in), "gate scales");
+    }
+    MOE_TRY_CUDA(copy_q(&L->up_q, w->up_q, nq_in), "up codes");
+    MOE_TRY_CUDA(copy_sb(&L->up_sb, w->up_s, w->up_b, ng_in), "up scales");
+    MOE_TRY_CUDA(copy_q(&L->down_q, w->down_q, nq_dn), "down codes");
+    MOE_TRY_CUDA(copy_sb(&L->down_sb, w->down_s, w->down_b, ng_dn), "down scales");
+    if (Fs) {
+      const size_t n = static_cast<size_t>(Fs) * H * adt;
+      if (gated) {
+        MOE_TRY_CUDA(L->alloc(&L->sh_gate, n), "shared gate");
+        MOE_TRY_CUDA(cudaMemcpyAsync(L->sh_gate, w->sh_gate, n, cudaMemcpyDeviceToDevice, s), "shared gate copy");
+      }
+      MOE_TRY_CUDA(L->alloc(&L->sh_up, n), "shared up");
+      MOE_TRY_CUDA(cudaMemcpyAsync(L->sh_up, w->sh_up, n, cudaMemcpyDeviceToDevice, s), "shared up copy");
+      MOE_TRY_CUDA(L->alloc(&L->sh_down, n), "shared down");
+      MOE_TRY_CUDA(cudaMemcpyAsync(L->sh_down, w->sh_down, n, cudaMemcpyDeviceToDevice, s), "shared down copy");
+    }
+    // workspace
+    const size_t P = static_cast<size_t>(T) * k;
+    MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->dense_in), static_cast<size_t>(T) * L->r_in * 4), "workspace");
+    MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->ids), P * 4), "workspace");
+    MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->wts), P * 4), "workspace");
+    MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->meta), (2 + 2 * static_cast<size_t>(L->umax) + P) * 4), "workspace");
+    MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->hbuf), P * F * 4), "workspace");
+    MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->pexp), P * kin * 4), "workspace");
+    MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->status), 4), "workspace");
+    MOE_TRY_CUDA(cudaMemsetAsync(L->status, 0, 4, s), "status clear");
+    MOE_TRY_CUDA(L->alloc(&L->x_stage, static_cast<size_t>(T) * H * adt), "workspace");
+    MOE_TRY_CUDA(L->alloc(&L->out_stage, static_cast<size_t>(T) * H * adt), "workspace");
+    MOE_TRY_CUDA(cudaStreamSynchronize(s), "create synchronise");
+  }
+  *out = L;
+  return MOE_OK;
+fail:
+  if (L) {
+    cudaStreamSynchronize(s);
+    L->free_all();
+    delete L;
+  }
+  g_create_error = why;
+  return st;
+}
+
+moe_status moe_layer_destroy(moe_layer* h) {
+  if (!h) return MOE_OK;
+  cudaDeviceSynchronize();
+  h->free_all();
+  delete h;
+  return MOE_OK;
+}
+
+static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out, void* stream,
+                               int32_t* ext_ids, float* ext_w, float* delta) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  const moe_layer_config& c = h->cfg;
+  if (!x || !out || T < 1 || T > c.max_tokens) {
+    h->last_error = "x/out must be non-NULL and 1 <= T <= max_tokens";
+    return MOE_ERR_INVALID_ARG;
+  }
+  const size_t adt = dt_size(c.act_dtype);
+  const size_t nbytes = static_cast<size_t>(T) * c.hidden * adt;
+  const char* xb = static_cast<const char*>(x);
+  const char* ob = static_cast<const char*>(out);
+  if (xb < ob + nbytes && ob < xb + nbytes) {
+    h->last_error = "x and out overlap";
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (h->path == MOE_PATH_GROUPED) {
+    h->last_error = "the grouped path is not available in this build";
+    return MOE_ERR_UNSUPPORTED;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int H = c.hidden, E = c.n_experts, k = c.top_k, F = c.expert_ffn, Lt = c.latent;
+  const int Fs = c.shared_ffn, kin = h->kin;
+  const bool gated = c.act == MOE_ACT_SWIGLU;
+  cudaError_t e;
+  auto mark = [&](int i) {
+    if (h->profiling) cudaEventRecord(h->ev[i], s);
+  };
+
+  // 1. dense matrices that read x
+  mark(0);
+  DenseInArgs di{};
+  int ns = 0;
+  auto seg1 = [&](const void* w, int dt, int rows, int row0) {
+    DenseSeg& S = di.seg[ns++];
+    S.part[0] = DensePart{w, dt, 0, H};
+    S.nparts = 1;
+    S.row0 = row0;
+    S.rows = rows;
+  };
+  seg1(h->router_w, c.router_dtype, E, 0);
+  if (Lt) seg1(h->fc1, c.act_dtype, Lt, h->off_fc1);
+  if (Fs && gated) seg1(h->sh_gate, c.act_dtype, Fs, h->off_shg);
+  if (Fs) seg1(h->sh_up, c.act_dtype, Fs, h->off_shu);
+  di.nseg = ns;
+  di.total_rows = h->r_in;
+  di.K = H;
+  di.x = x;
+  di.x_dt = c.act_dtype;
+  di.out = h->dense_in;
+  di.T = T;
+  const int tb_in = std::min(pow2_at_least(T, 8), dense_tb_cap(H));
+  const int grid_in = std::max(1, std::min(h->num_sms * 2, (h->r_in + 3) / 4));
+  if ((e = launch_dense_in(di, tb_in, grid_in, s)) != cudaSuccess) goto cuda_fail;
+
+  // 2. routing
+  mark(1);
+  {
+    RouteArgs ra{};
+    ra.logits = h->dense_in;
+    ra.r_in = h->r_in;
+    ra.bias = h->router_bias;
+    ra.E = E;
+    ra.k = k;
+    ra.T = T;
+    ra.router = c.router;
+    ra.renorm = c.renormalize;
+    ra.scale = c.routed_scale;
+    ra.ids = h->ids;
+    ra.w = h->wts;
+    ra.meta = h->meta;
+    ra.umax = h->umax;
+    ra.ext_ids = ext_ids;
+    ra.ext_w = ext_w;
+    ra.status = h->status;
+    k_route<<<1, MAX_E, 0, s>>>(ra);
+    if ((e = cudaGetLastError()) != cudaSuccess) goto cuda_fail;
+  }
+  // 3. expert up (+gate) with the activation, 4. expert down
+  {
+    const int pb_up = std::min(pow2_at_least(T, 8), expert_pb_cap(kin));
+    const int pb_dn = std::min(pow2_at_least(T, 8), expert_pb_cap(F));
+    const int grid_x = h->num_sms * 4;
+    ExpertArgs up{};
+    up.n_rows = F;
+    up.K = kin;
+    up.G = c.group_size;
+    up.q = h->up_q;
+    up.sb = h->up_sb;
+    up.q_gate = gated ? h->gate_q : nullptr;
+    up.sb_gate = gated ? h->gate_sb : nullptr;
+    up.s_dt = c.scale_dtype;
+    up.act = c.act;
+    up.meta = h->meta;
+    up.umax = h->umax;
+    up.k = k;
+    if (Lt) {
+      up.xin = h->dense_in;
+      up.xin_dt = DT_FP32;
+      up.xin_stride = h->r_in;
+      up.xin_off = h->off_fc1;
+    } else {
+      up.xin = x;
+      up.xin_dt = c.act_dtype;
+      up.xin_stride = H;
+      up.xin_off = 0;
+    }
+    up.xin_by_pair = 0;
+    up.out = h->hbuf;
+    mark(2);
+    if ((e = launch_expert(up, pb_up, grid_x, s)) != cudaSuccess) goto cuda_fail;
+    mark(3);
+
+    ExpertArgs dn = up;
+    dn.n_rows = kin;
+    dn.K = F;
+    dn.q = h->down_q;
+    dn.sb = h->down_sb;
+    dn.q_gate = nullptr;
+    dn.sb_gate = nullptr;
+    dn.act = -1;
+    dn.xin = h->hbuf;
+    dn.xin_dt = DT_FP32;
+    dn.xin_stride = F;
+    dn.xin_off = 0;
+    dn.xin_by_pair = 1;
+    dn.out = h->pexp;
+    if ((e = launch_expert(dn, pb_dn, grid_x, s)) != cudaSuccess) goto cuda_fail;
+  }
+  // 5. combine + fc2 + shared down + residual
+  {
+    DenseOutArgs dout{};
+    const int kout = (Lt ? Lt : 0) + Fs;
+    dout.nseg = 0;
+    if (kout) {
+      DenseSeg& S = dout.seg[0];
+      S.nparts = 0;
+      if (Lt) S.part[S.nparts++] = DensePart{h->fc2, c.act_dtype, 0, Lt};
+      if (Fs) S.part[S.nparts++] = DensePart{h->sh_down, c.act_dtype, Lt, Fs};
+      S.row0 = 0;
+      S.rows = H;
+      dout.nseg = 1;
+    }
+    dout.total_rows = H;
+    dout.K = kout;
+    dout.latent = Lt;
+    dout.shared = Fs;
+    dout.k = k;
+    dout.pexp = h->pexp;
+    dout.wts = h->wts;
+    dout.dense_in = h->dense_in;
+    dout.r_in = h->r_in;
+    dout.sh_g_off = h->off_shg;
+    dout.sh_u_off = h->off_shu;
+    dout.act = c.act;
+    dout.x = x;
+    dout.x_dt = c.act_dtype;
+    dout.out = out;
+    dout.delta = delta;
+    dout.T = T;
+    const int tb_out = kout ? std::min(pow2_at_least(T, 8), dense_tb_cap(kout)) : pow2_at_least(T, 8);
+    const int grid_out = std::max(1, std::min(h->num_sms * 2, (H + 3) / 4));
+    mark(4);
+    if ((e = launch_dense_out(dout, tb_out, grid_out, s)) != cudaSuccess) goto cuda_fail;
+    mark(5);
+    if (h->profiling) h->profiled = true;
+  }
+  (void)F;
+  return MOE_OK;
+cuda_fail:
+  h->last_error = std::string("launch failed: ") + cudaGetErrorString(e);
+  return MOE_ERR_CUDA;
+}
+
+moe_status moe_layer_forward(moe_layer* h, const void* x, int32_t T, void* out, void* stream) {
+  return forward_impl(h, x, T, out, stream, nullptr, nullptr, nullptr);
+}
+
+moe_status moe_layer_forward_ex(moe_layer* h, const void* x, int32_t T, void* out, void* stream,
+                                int32_t* topk_ids, float* topk_w, float* delta_f32) {
+  return forward_impl(h, x, T, out, stream, topk_ids, topk_w, delta_f32);
+}
+
+moe_status moe_layer_forward_host(moe_layer* h, const void* x_host, int32_t T, void* out_host,
+                                  void* stream) {
+  if (!h || !x_host || !out_host || T < 1 || T > h->cfg.max_tokens) {
+    if (h) h->last_error = "host buffers must be non-NULL and 1 <= T <= max_tokens";
+    return MOE_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t n = static_cast<size_t>(T) * h->cfg.hidden * dt_size(h->cfg.act_dtype);
+  cudaError_t e = cudaMemcpyAsync(h->x_stage, x_host, n, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) {
+    h->last_error = std::string("input copy: ") + cudaGetErrorString(e);
+    return MOE_ERR_CUDA;
+  }
+  moe_status st = forward_impl(h, h->x_stage, T, h->out_stage, stream, nullptr, nullptr, nullptr);
+  if (st != MOE_OK) return st;
+  e = cudaMemcpyAsync(out_host, h->out_stage, n, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    h->last_error = std::string("output copy: ") + cudaGetErrorString(e);
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_layer_set_path(moe_layer* h, int32_t path) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (path != MOE_PATH_AUTO && path != MOE_PATH_GEMV && path != MOE_PATH_GROUPED)
+    return MOE_ERR_INVALID_ARG;
+  h->path = path;
+  return MOE_OK;
+}
+
+moe_status moe_layer_device_status(moe_layer* h, void* stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, h->status, 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->status, 0, 4, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    h->last_error = std::string("status read: ") + cudaGetErrorString(e);
+    return MOE_ERR_CUDA;
+  }
+  if (v & STATUS_TIMEOUT) return MOE_ERR_TIMEOUT;
+  if (v & STATUS_NONFINITE) return MOE_ERR_NONFINITE;
+  return MOE_OK;
+}
+
+moe_status moe_layer_profile(moe_layer* h, int32_t enable) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (enable && !h->profiling) {
+    for (auto& e : h->ev) {
+      if (cudaEventCreate(&e) != cudaSuccess) {
+        h->free_events();
+        h->last_error = "event creation failed";
+        return MOE_ERR_CUDA;
+      }
+    }
+  } else if (!enable && h->profiling) {
+    cudaDeviceSynchronize();
+    h->free_events();
+  }
+  h->profiling = enable != 0;
+  h->profiled = false;
+  return MOE_OK;
+}
+
+moe_status moe_layer_stage_times(moe_layer* h, float* ms, int32_t n) {
+  if (!h || !ms || n < 0) return MOE_ERR_INVALID_ARG;
+  if (!h->profiling || !h->profiled) {
+    h->last_error = "no profiled forward";
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (cudaEventSynchronize(h->ev[MOE_NUM_STAGES]) != cudaSuccess) return MOE_ERR_CUDA;
+  for (int i = 0; i < n && i < MOE_NUM_STAGES; ++i) {
+    if (cudaEventElapsedTime(&ms[i], h->ev[i], h->ev[i + 1]) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+int64_t moe_layer_device_bytes(const moe_layer* h) { return h ? h->bytes : 0; }
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_TOPK_GT_E: return "MOE_ERR_TOPK_GT_E";
+    case MOE_ERR_LATENT_PROJ: return "MOE_ERR_LATENT_PROJ";
+    case MOE_ERR_SHAPE: return "MOE_ERR_SHAPE";
+    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
+    case MOE_ERR_OOM: return "MOE_ERR_OOM";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_NONFINITE: return "MOE_ERR_NONFINITE";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+const char* moe_layer_last_error(const moe_layer* h) {
+  return h ? h->last_error.c_str() : g_create_error.c_str();
+}
+
+int64_t moe_debug_live_allocations(void) { return g_live_allocs.load(); }
+
+void moe_debug_fail_allocation(int32_t n) { g_fail_countdown.store(n > 0 ? n : 0); }
+
+}  // extern "C"

@@ -1,0 +1,112 @@
+"""The C-ABI library on the host: it loads, exports every declared entry
+point, and refuses bad configs before touching a device (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quantized_moe_decode_gemv_gb300 as pkg
+from quantized_moe_decode_gemv_gb300 import _capi
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "moe_layer.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_capi.LIB_PATH):
+        pytest.fail("libmoe_gb300.so is not built; run __graft_entry__.build()")
+    return _capi.load_library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*[\w\s\*]+?\b(moe_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("moe_layer_create", "moe_layer_forward", "moe_layer_destroy"):
+        assert n in names
+    assert set(names) == set(_capi.SIGNATURES), set(names) ^ set(_capi.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert lib.moe_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for i, name in enumerate(_capi.STATUS_NAMES):
+        assert lib.moe_status_string(i).decode() == name
+
+
+def _cfg(**kw):
+    base = dict(hidden=512, n_experts=16, top_k=2, expert_ffn=256, latent=0, group_size=64,
+                shared_ffn=256, max_tokens=4, act="swiglu", router="softmax")
+    base.update(kw)
+    return pkg.MoEConfig(**base)
+
+
+FAKE = 0x1000  # non-NULL placeholder pointers: validation only checks presence
+
+
+def _w(**kw):
+    w = {n: FAKE for n in ("router_w", "gate_q", "up_q", "down_q", "gate_s", "gate_b", "up_s",
+                           "up_b", "down_s", "down_b", "sh_gate", "sh_up", "sh_down")}
+    w.update(kw)
+    return _capi.moe_layer_weights(**w)
+
+
+def _validate(lib, cfg, w=None):
+    c = cfg.to_c()
+    return lib.moe_layer_validate(ctypes.byref(c), ctypes.byref(w) if w is not None else None)
+
+
+CASES = [
+    ("valid", {}, {}, "MOE_OK"),
+    ("top_k above E", {"top_k": 17}, {}, "MOE_ERR_TOPK_GT_E"),
+    ("top_k zero", {"top_k": 0}, {}, "MOE_ERR_TOPK_GT_E"),
+    ("latent without fc1", {"latent": 256}, {"fc2_latent": FAKE}, "MOE_ERR_LATENT_PROJ"),
+    ("latent without fc2", {"latent": 256}, {"fc1_latent": FAKE}, "MOE_ERR_LATENT_PROJ"),
+    ("latent fp32", {"latent": 256, "act_dtype": "fp32"}, {"fc1_latent": FAKE, "fc2_latent": FAKE},
+     "MOE_ERR_LATENT_PROJ"),
+    ("latent given to non-latent layer", {}, {"fc1_latent": FAKE, "fc2_latent": FAKE}, "MOE_ERR_LATENT_PROJ"),
+    ("latent ok", {"latent": 256}, {"fc1_latent": FAKE, "fc2_latent": FAKE}, "MOE_OK"),
+    ("group 48", {"group_size": 48}, {}, "MOE_ERR_SHAPE"),
+    ("hidden not multiple of 64", {"hidden": 520}, {}, "MOE_ERR_SHAPE"),
+    ("ffn not multiple of group", {"expert_ffn": 192, "group_size": 128}, {}, "MOE_ERR_SHAPE"),
+    ("too many experts", {"n_experts": 2048}, {}, "MOE_ERR_UNSUPPORTED"),
+    ("top_k above 16", {"n_experts": 64, "top_k": 17}, {}, "MOE_ERR_UNSUPPORTED"),
+    ("bias with softmax", {"router_bias": True}, {"router_bias": FAKE}, "MOE_ERR_UNSUPPORTED"),
+    ("swiglu without gate", {}, {"gate_q": None}, "MOE_ERR_INVALID_ARG"),
+    ("relu2 with gate", {"act": "relu2"}, {"sh_gate": None}, "MOE_ERR_SHAPE"),
+    ("shared weights missing", {}, {"sh_down": None}, "MOE_ERR_UNSUPPORTED"),
+    ("shared weights without shared_ffn", {"shared_ffn": 0}, {}, "MOE_ERR_SHAPE"),
+    ("no router", {}, {"router_w": None}, "MOE_ERR_INVALID_ARG"),
+    ("zero max_tokens", {"max_tokens": 0}, {}, "MOE_ERR_INVALID_ARG"),
+]
+
+
+@pytest.mark.parametrize("name,ckw,wkw,want", CASES, ids=[c[0] for c in CASES])
+def test_validate_refusals(lib, name, ckw, wkw, want):
+    st = _validate(lib, _cfg(**ckw), _w(**wkw))
+    assert _capi.STATUS_NAMES[st] == want, (name, _capi.STATUS_NAMES[st],
+                                            lib.moe_layer_last_error(None))
+
+
+def test_create_refuses_before_any_allocation(lib):
+    """An invalid config is refused by create before any device call, and
+    nothing stays allocated."""
+    before = lib.moe_debug_live_allocations()
+    c = _cfg(top_k=40).to_c()
+    w = _w()
+    h = ctypes.c_void_p()
+    st = lib.moe_layer_create(ctypes.byref(c), ctypes.byref(w), None, ctypes.byref(h))
+    assert _capi.STATUS_NAMES[st] == "MOE_ERR_TOPK_GT_E"
+    assert h.value is None
+    assert lib.moe_debug_live_allocations() == before
+    assert b"top_k" in lib.moe_layer_last_error(None)

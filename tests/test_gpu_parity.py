@@ -1,0 +1,291 @@
+"""CUDA layer against the fp64 oracle, through the C ABI (GPU only).
+
+Inputs are seeded and margin-filtered (the k-th and (k+1)-th oracle selection
+keys differ by >= 1e-3), so the selected expert set is unambiguous in fp32 and
+must match exactly.  Full-size layers are compared on every row where the
+oracle takes seconds, and on sampled rows otherwise (the oracle is row
+independent, so a sampled row is checked exactly like a full pass).
+"""
+import numpy as np
+import pytest
+
+import moe_inputs as mi
+import oracle
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import quantized_moe_decode_gemv_gb300 as pkg
+    pkg.load_library()
+    torch.cuda.set_device(0)
+    yield
+    torch.cuda.synchronize()
+
+
+_HANDLES = {}
+
+
+def handle_for(name, max_tokens, seed=0, zipf=False, layer=None):
+    key = (name, seed, zipf, max_tokens)
+    if key not in _HANDLES:
+        lay = layer if layer is not None else gu.cached_layer(name, seed, zipf)
+        _HANDLES[key] = (lay, gu.build_layer(lay, max_tokens))
+    return _HANDLES[key]
+
+
+def teardown_module(module):
+    for _, h in _HANDLES.values():
+        h.close()
+    _HANDLES.clear()
+
+
+def _parity(name, T, rows=None, max_tokens=None, seed=0, zipf=False):
+    lay, h = handle_for(name, max_tokens or max(T, 16), seed, zipf)
+    x, redraws = gu.margin_x(lay, T, seed=seed + T)
+    got = gu.run_layer(h, x, lay.spec.act_dtype)
+    sel = list(range(T)) if rows is None else list(rows)
+    ref = oracle.oracle_forward(lay, x[sel])
+    rr = gu.check_parity(got, ref, rows=sel, what=f"{name} T={T}")
+    assert h.device_status() == 0
+    return rr
+
+
+# --- tiny layer (oracle in milliseconds): several tiles and ragged tails ------
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8, 13, 16])
+def test_tiny_parity(T):
+    _parity("tiny", T)
+
+
+# --- odd shapes covering every option of the config -------------------------
+
+ODD = {
+    # latent, softmax without renormalisation, SwiGLU, fp16, group 128, F not a power of 2
+    "odd_latent_fp16": mi.LayerSpec(name="odd_latent_fp16", hidden=1024, n_experts=40, top_k=6,
+                                    expert_ffn=384, latent=256, group_size=128, shared_ffn=320,
+                                    act="swiglu", router="softmax", renormalize=False,
+                                    routed_scale=1.5, act_dtype="fp16", scale_dtype="fp16",
+                                    router_dtype="fp16", weight_std=0.05),
+    # non-latent sigmoid without bias or shared expert, squared ReLU, fp32 router, group 32
+    "odd_relu2_noshared": mi.LayerSpec(name="odd_relu2_noshared", hidden=768, n_experts=33,
+                                       top_k=4, expert_ffn=192, latent=0, group_size=32,
+                                       shared_ffn=0, act="relu2", router="sigmoid",
+                                       renormalize=True, routed_scale=2.0, router_dtype="fp32",
+                                       weight_std=0.05),
+    # latent sigmoid with bias, no shared expert, k = E
+    "odd_k_eq_e": mi.LayerSpec(name="odd_k_eq_e", hidden=512, n_experts=8, top_k=8,
+                               expert_ffn=128, latent=128, group_size=64, shared_ffn=0,
+                               act="relu2", router="sigmoid", renormalize=True,
+                               routed_scale=2.5, router_bias=True, weight_std=0.05),
+    # a single expert (k = E = 1): the dense MLP special case
+    "odd_single": mi.LayerSpec(name="odd_single", hidden=256, n_experts=1, top_k=1,
+                               expert_ffn=128, latent=0, group_size=64, shared_ffn=64,
+                               act="swiglu", router="softmax", weight_std=0.05),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ODD))
+@pytest.mark.parametrize("T", [1, 7, 12])
+def test_odd_shapes(name, T):
+    spec = ODD[name]
+    lay = mi.make_layer(spec, 11)
+    h = gu.build_layer(lay, 12)
+    try:
+        x, _ = gu.margin_x(lay, T, seed=3)
+        got = gu.run_layer(h, x, spec.act_dtype)
+        ref = oracle.oracle_forward(lay, x)
+        gu.check_parity(got, ref, what=f"{name} T={T}")
+    finally:
+        h.close()
+
+
+# --- latent Bolt-shaped layer (E=496, k=9, latent 1024) at full size ---------
+
+@pytest.mark.parametrize("T", [1, 2, 9, 16])
+def test_latent_parity(T):
+    _parity("latent", T)
+
+
+# --- non-latent fp16 sigmoid top-8 layer (H=6144, E=256) at full size ---------
+
+@pytest.mark.parametrize("T,rows", [(1, None), (4, None), (32, [0, 13, 31])])
+def test_nonlatent_parity(T, rows):
+    _parity("nonlatent", T, rows=rows, max_tokens=32)
+
+
+# --- batched decode rows with Zipf-skewed expert load -------------------------
+
+@pytest.mark.parametrize("T,rows", [(32, [0, 31]), (64, [5, 63]), (256, [0, 128, 255])])
+def test_batched_zipf_parity(T, rows):
+    _parity("latent", T, rows=rows, max_tokens=256, zipf=True)
+
+
+# --- heterogeneous five-layer stack, residual stream carried -----------------
+
+@pytest.mark.parametrize("T", [2, 9, 16])
+def test_stack_parity(T):
+    layers = [mi.make_layer(s, i) for i, s in enumerate(mi.stack_specs())]
+    x, _ = gu.margin_x(layers[0], T, seed=40 + T, stack=layers)
+    # oracle follows its own residual stream, rounding each layer's output to
+    # the activation dtype as the GPU layer does
+    ref_in = x
+    handles = [gu.build_layer(l, 16) for l in layers]
+    try:
+        cur = gu.to_torch_x(x, "bf16")
+        for li, (lay, h) in enumerate(zip(layers, handles)):
+            out, ids, w, delta = h.forward_ex(cur)
+            torch.cuda.synchronize()
+            ref = oracle.oracle_forward(lay, ref_in)
+            assert np.array_equal(ids.cpu().numpy(), ref["ids"]), f"layer {li}"
+            np.testing.assert_allclose(w.cpu().numpy(), ref["w"], rtol=gu.W_RTOL, atol=gu.W_ATOL)
+            ref_in = mi._round_to_dtype(ref["out"], "bf16")
+            cur = out
+        final = cur.float().cpu().numpy().astype(np.float64)
+        want = ref["out"]
+        assert gu.rel_rms(final, want) <= gu.REL_RMS
+        assert gu.max_abs_frac(final, want) <= gu.MAX_ABS_FRAC
+    finally:
+        for h in handles:
+            h.close()
+
+
+# --- properties of the CUDA path ------------------------------------------------
+
+def test_row_invariance_bit_exact():
+    """Each row of a 16-row pass equals its own one-row pass, bit for bit."""
+    lay, h = handle_for("latent", 16)
+    x, _ = gu.margin_x(lay, 16, seed=77)
+    xt = gu.to_torch_x(x, "bf16")
+    full = h.forward(xt)
+    for t in range(16):
+        one = h.forward(xt[t:t + 1].contiguous())
+        torch.cuda.synchronize()
+        assert torch.equal(one.view(torch.int16), full[t:t + 1].view(torch.int16)), t
+
+
+def test_repeat_is_deterministic():
+    lay, h = handle_for("latent", 16)
+    x, _ = gu.margin_x(lay, 9, seed=78)
+    xt = gu.to_torch_x(x, "bf16")
+    a = h.forward(xt).clone()
+    b = h.forward(xt)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_host_buffer_forward_matches_device_forward():
+    lay, h = handle_for("latent", 16)
+    x, _ = gu.margin_x(lay, 4, seed=79)
+    xt = gu.to_torch_x(x, "bf16")
+    dev = h.forward(xt).cpu()
+    xh = xt.cpu().pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    h.forward_host(xh, oh)
+    assert torch.equal(dev.view(torch.int16), oh.view(torch.int16))
+
+
+def test_two_handles_on_two_streams_equal_solo():
+    lay = gu.cached_layer("tiny")
+    h1, h2 = gu.build_layer(lay, 16), gu.build_layer(lay, 16)
+    try:
+        x, _ = gu.margin_x(lay, 16, seed=80)
+        xt = gu.to_torch_x(x, "bf16")
+        solo = h1.forward(xt).clone()
+        s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+        torch.cuda.synchronize()
+        outs = []
+        for _ in range(8):
+            with torch.cuda.stream(s1):
+                a = h1.forward(xt)
+            with torch.cuda.stream(s2):
+                b = h2.forward(xt)
+            outs.append((a, b))
+        torch.cuda.synchronize()
+        for a, b in outs:
+            assert torch.equal(a.view(torch.int16), solo.view(torch.int16))
+            assert torch.equal(b.view(torch.int16), solo.view(torch.int16))
+    finally:
+        h1.close()
+        h2.close()
+
+
+def test_nonfinite_router_keys_rank_last_and_are_reported():
+    """A NaN selection bias makes that expert's key non-finite: it ranks below
+    every finite key (as in the oracle) and the device status reports it."""
+    spec = mi.LayerSpec(name="nan_bias", hidden=512, n_experts=16, top_k=3, expert_ffn=128,
+                        latent=0, group_size=64, shared_ffn=0, act="relu2", router="sigmoid",
+                        routed_scale=1.0, router_bias=True, weight_std=0.05)
+    lay = mi.make_layer(spec, 5)
+    lay.router_bias[[2, 7, 11]] = np.nan
+    h = gu.build_layer(lay, 4)
+    try:
+        x, _ = gu.margin_x(lay, 4, seed=81)
+        got = gu.run_layer(h, x, "bf16")
+        ref = oracle.oracle_forward(lay, x)
+        gu.check_parity(got, ref, what="nan bias")
+        assert not np.isin(got["ids"], [2, 7, 11]).any()
+        assert h.device_status() == 10  # MOE_ERR_NONFINITE
+        assert h.device_status() == 0   # cleared by the read
+    finally:
+        h.close()
+
+
+def test_forward_argument_errors():
+    import quantized_moe_decode_gemv_gb300 as pkg
+    lay, h = handle_for("tiny", 16)
+    xt = gu.to_torch_x(mi.make_x(lay.spec, 16, 0), "bf16")
+    with pytest.raises(pkg.MoEError, match="INVALID_ARG"):
+        pkg.moe_layer_forward(h.handle, xt, 0, torch.empty_like(xt))
+    with pytest.raises(pkg.MoEError, match="INVALID_ARG"):
+        pkg.moe_layer_forward(h.handle, xt, 17, torch.empty_like(xt))
+    with pytest.raises(pkg.MoEError, match="INVALID_ARG"):   # out overlaps x
+        pkg.moe_layer_forward(h.handle, xt, 8, xt[4:])
+    with pytest.raises(pkg.MoEError, match="UNSUPPORTED"):
+        h.set_path("grouped")
+        h.forward(xt)
+    h.set_path("auto")
+
+
+def test_refusals_and_allocation_failures_leak_nothing():
+    """Refused creates and creates whose n-th device allocation fails free
+    everything they allocated (the live-allocation count returns to its
+    starting value)."""
+    import quantized_moe_decode_gemv_gb300 as pkg
+    lib = pkg.load_library()
+    lay = gu.cached_layer("tiny")
+    cfg = pkg.MoEConfig.from_spec(lay.spec, max_tokens=4)
+    dev = pkg.upload_arrays(lay.arrays())
+    base = lib.moe_debug_live_allocations()
+    bad = pkg.MoEConfig.from_spec(lay.spec, max_tokens=4)
+    bad.top_k = 17
+    with pytest.raises(pkg.MoEError, match="TOPK_GT_E"):
+        pkg.moe_layer_create(bad, dev)
+    assert lib.moe_debug_live_allocations() == base
+    n_ok = 0
+    for n in range(1, 40):
+        lib.moe_debug_fail_allocation(n)
+        try:
+            hh = pkg.moe_layer_create(cfg, dev)
+        except pkg.MoEError as e:
+            assert e.status == 7  # MOE_ERR_OOM
+            assert lib.moe_debug_live_allocations() == base
+            continue
+        finally:
+            lib.moe_debug_fail_allocation(0)
+        pkg.moe_layer_destroy(hh)   # n beyond the number of allocations
+        n_ok = n
+        break
+    assert n_ok > 5
+    assert lib.moe_debug_live_allocations() == base
+
+
+def test_smoke_entry():
+    import __graft_entry__
+    __graft_entry__.smoke()
