@@ -174,6 +174,22 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
+def aggregate_replicas(local_ms: float, local_tokens: int, device=None):
+    """Whole-job throughput of independent replicas: every rank's tokens over
+    the slowest rank's time.  Returns (tokens/s, max ms, total tokens); a
+    no-op reduction when torch.distributed is not initialised."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return local_tokens / (local_ms / 1e3), local_ms, local_tokens
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    n = torch.tensor([float(local_tokens)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    max_ms, tokens = float(t.item()), int(n.item())
+    return tokens / (max_ms / 1e3), max_ms, tokens
+
+
 def run_reference(args):
     import moe_inputs as mi
     rank, world, _ = dist_env()
@@ -272,21 +288,21 @@ def run_ours(args):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        m = measure(torch, pkg, spec, h, args.T, args.steps, args.warmup, args.seed, flush, stream)
+        m = measure(torch, pkg, spec, h, args.T, args.steps, args.warmup, args.seed, flush, stream,
+                    profile=False)
     torch.cuda.synchronize()
-    total_ms = float(sum(m["step_ms"]))
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    tokens = args.steps * args.T * world
-    value = tokens / (total_ms / 1e3)
+    # per-kernel durations: a second pass with an event between every kernel
+    # (events serialise the kernels, so this pass has no inter-kernel overlap)
+    mp = measure(torch, pkg, spec, h, args.T, max(10, min(args.steps, 50)), 2, args.seed, flush,
+                 stream, profile=True)
+    value, total_ms, tokens = aggregate_replicas(float(sum(m["step_ms"])), args.steps * args.T,
+                                                 device=dev)
     bytes_steps = [layer_bytes(spec, args.T, u) for u in m["n_uniq"]]
     gbs = sum(bytes_steps) / (sum(m["step_ms"]) / 1e3) / 1e9
 
     # dominant kernel roofline (stage with the largest share of the step)
-    st = m["stage_ms"]
-    avg_uniq = float(np.mean(m["n_uniq"]))
+    st = mp["stage_ms"]
+    avg_uniq = float(np.mean(mp["n_uniq"]))
     sb = stage_bytes(spec, args.T, avg_uniq)
     dom = int(np.argmax(st))
     dom_name = STAGES[dom]
@@ -345,7 +361,9 @@ def run_ours(args):
             "mean_distinct_experts": float(np.mean(m["n_uniq"])),
             "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved,
                          "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                         "traffic": None},
+                         "traffic": None, "peak_source": peak_src,
+                         "timing": "per-kernel CUDA events, serialised pass"},
+            "profiled_step_ms": float(np.mean(mp["step_ms"])),
             "stages": stages,
             "also": also,
             "e2e": e2e,

@@ -49,7 +49,7 @@ import numpy as np
 __all__ = [
     "widen", "unpack_codes", "dequantize", "router_logits", "selection_keys",
     "topk_order", "route", "activation", "expert_output", "shared_output",
-    "oracle_forward", "routing_margin", "forward_rows",
+    "oracle_forward", "routing_margin", "forward_rows", "expert_cache",
 ]
 
 
@@ -181,12 +181,15 @@ def activation(spec, u: np.ndarray, g: Optional[np.ndarray]) -> np.ndarray:
 
 class _ExpertCache:
     """Dequantises each selected expert once per forward call (only selected
-    experts are ever dequantised)."""
+    experts are ever dequantised).  When shared across calls it keeps at most
+    ``max_bytes`` of dequantised matrices, evicting the oldest first."""
 
-    def __init__(self, layer):
+    def __init__(self, layer, max_bytes: int = 4 << 30):
         self.layer = layer
         self.spec = layer.spec
         self.mats: Dict[int, tuple] = {}
+        self.max_bytes = max_bytes
+        self.bytes = 0
 
     def get(self, e: int):
         if e not in self.mats:
@@ -195,8 +198,19 @@ class _ExpertCache:
             up = dequantize(L.up_q[e], L.up_s[e], L.up_b[e], G, sd)
             gate = dequantize(L.gate_q[e], L.gate_s[e], L.gate_b[e], G, sd) if sp.gated else None
             down = dequantize(L.down_q[e], L.down_s[e], L.down_b[e], G, sd)
+            size = up.nbytes + down.nbytes + (gate.nbytes if gate is not None else 0)
+            while self.mats and self.bytes + size > self.max_bytes:
+                old = next(iter(self.mats))
+                self.bytes -= sum(m.nbytes for m in self.mats.pop(old) if m is not None)
             self.mats[e] = (gate, up, down)
+            self.bytes += size
         return self.mats[e]
+
+
+def expert_cache(layer) -> _ExpertCache:
+    """A dequantised-expert cache that several ``oracle_forward`` calls on the
+    same layer may share (it only avoids repeating identical dequantisation)."""
+    return _ExpertCache(layer)
 
 
 def expert_output(cache: _ExpertCache, e: int, xin: np.ndarray) -> np.ndarray:
@@ -225,7 +239,7 @@ def shared_output(layer, x_row: np.ndarray) -> np.ndarray:
 # the layer
 # ---------------------------------------------------------------------------
 
-def oracle_forward(layer, x: np.ndarray) -> dict:
+def oracle_forward(layer, x: np.ndarray, cache: Optional[_ExpertCache] = None) -> dict:
     """Forward of the whole layer on ``x [T, H]`` (storage dtype), row by row,
     in the Bolt layer order (TensorFold #1038, "What's in it"):
 
@@ -243,7 +257,8 @@ def oracle_forward(layer, x: np.ndarray) -> dict:
     bias = None if layer.router_bias is None else np.asarray(layer.router_bias, np.float64)
     W1 = widen(layer.fc1, sp.act_dtype) if sp.latent else None
     W2 = widen(layer.fc2, sp.act_dtype) if sp.latent else None
-    cache = _ExpertCache(layer)
+    if cache is None or cache.layer is not layer:
+        cache = _ExpertCache(layer)
     k, Kin = sp.top_k, sp.k_in
     out = np.zeros((T, sp.hidden))
     ids_all = np.zeros((T, k), dtype=np.int64)

@@ -67,6 +67,22 @@ __device__ __forceinline__ uint32_t ldg_u32(const void* p) {
   return r;
 }
 
+// Programmatic dependent launch: wait for the preceding kernel of the stream
+// (a no-op when launched without the attribute) / let the next one launch.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// Asynchronous prefetch of [p, p + bytes) into L2 by the bulk-copy engine;
+// p 16-byte aligned, bytes a multiple of 16 (issued in pieces of <= 64 KB).
+__device__ __forceinline__ void prefetch_l2(const void* p, int64_t bytes) {
+  const char* c = static_cast<const char*>(p);
+  for (int64_t off = 0; off < bytes; off += 65536) {
+    const int64_t rem = bytes - off;
+    const uint32_t n = static_cast<uint32_t>(rem < 65536 ? rem : 65536);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c + off), "r"(n) : "memory");
+  }
+}
+
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 __device__ __forceinline__ float f16lo(uint32_t v) {
@@ -151,6 +167,225 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&v)[NV], int lane) {
 }
 
 // ---------------------------------------------------------------------------
+// routing arguments
+// ---------------------------------------------------------------------------
+
+// Route metadata (int32 buffer):
+//   [0]                      n_uniq
+//   [1, 1 + umax)            uniq_e[u]   distinct selected experts, ascending
+//   [1 + umax, 2 + 2 umax)   uniq_p0[u]  first position of u's pairs (u = n_uniq: total)
+//   [2 + 2 umax, ...)        pairs[i]    pair ids t*k + j grouped by expert, t ascending
+struct RouteArgs {
+  const float* logits;   // dense_in, row stride r_in, experts at columns [0, E)
+  int r_in;
+  const float* bias;     // [E] or null
+  int E, k, T;
+  int router, renorm;
+  float scale;
+  int* ids;              // [T*k]
+  float* w;              // [T*k]
+  int* meta;
+  int umax;
+  int* ext_ids;          // optional copies for the caller
+  float* ext_w;
+  int* status;
+  int mask_words;        // > 0: rank pairs with per-expert row bitmasks of this many
+                         // words in dynamic shared memory (E * mask_words words)
+};
+
+__device__ __forceinline__ bool key_better(float a, int ia, float b, int ib) {
+  return a > b || (a == b && ia < ib);
+}
+
+// Shared memory of route_block: two int arrays of MAX_E and 2 x 32 ints, plus
+// E * mask_words words of row bitmasks when A.mask_words > 0.
+constexpr int ROUTE_SMEM_BYTES = (2 * MAX_E + 64) * 4;
+
+// Routing of all T rows by one CTA (any block size that is a multiple of 32):
+// top-k per row by warp-shuffle selection, the combine weights, then the
+// distinct selected experts (ascending) with their (row, pick) pairs in row
+// order.  Logits are read with ld.global.cg, so this may run in the last CTA
+// of the kernel that produced them.
+__device__ void route_block(const RouteArgs& A, int* smem) {
+  int* s_cnt = smem;
+  int* s_scan_c = smem + MAX_E;
+  int* s_wsum_u = smem + 2 * MAX_E;
+  int* s_wsum_c = s_wsum_u + 32;
+  uint32_t* s_mask = reinterpret_cast<uint32_t*>(smem + 2 * MAX_E + 64);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = blockDim.x >> 5;
+  const int nthr = blockDim.x;
+  const int E = A.E, k = A.k;
+  const int nper = (E + 31) >> 5;
+
+  for (int t = warp; t < A.T; t += nwarp) {
+    const float* z = A.logits + static_cast<int64_t>(t) * A.r_in;
+    float key[32];
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = lane + 32 * i;
+      float kv = -INFINITY;
+      if (i < nper && e < E) {
+        const float zz = __ldcg(z + e);
+        kv = (A.router == ROUTER_SOFTMAX) ? zz : 1.0f / (1.0f + expf(-zz));
+        if (A.router == ROUTER_SIGMOID && A.bias) kv += A.bias[e];
+        if (!isfinite(kv)) { bad = true; kv = -INFINITY; }
+      }
+      key[i] = kv;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(A.status, STATUS_NONFINITE);
+    uint32_t taken = 0;
+    int my_id = -1;
+    for (int j = 0; j < k; ++j) {
+      float bk = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int e = lane + 32 * i;
+        if (i < nper && e < E && !((taken >> i) & 1u) && key_better(key[i], e, bk, bi)) {
+          bk = key[i]; bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (key_better(ok, oi, bk, bi)) { bk = ok; bi = oi; }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == j) my_id = bi;
+    }
+    // combine weights (lane j < k holds pick j)
+    const float zj = (lane < k) ? __ldcg(z + my_id) : 0.f;
+    float wv = 0.f;
+    if (A.router == ROUTER_SOFTMAX) {
+      const float m = __shfl_sync(0xffffffffu, zj, 0);   // largest selected logit
+      float den = 0.f;
+      if (A.renorm) {
+        const float ex = (lane < k) ? expf(zj - m) : 0.f;
+        den = ex;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        wv = ex / den;
+      } else {
+        float mm = -INFINITY;
+        for (int i = lane; i < E; i += 32) mm = fmaxf(mm, __ldcg(z + i));
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+        for (int i = lane; i < E; i += 32) den += expf(__ldcg(z + i) - mm);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        wv = (lane < k) ? expf(zj - mm) / den : 0.f;
+      }
+    } else {
+      const float sg = (lane < k) ? 1.0f / (1.0f + expf(-zj)) : 0.f;
+      wv = sg;
+      if (A.renorm) {
+        float den = sg;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        wv = sg / den;
+      }
+    }
+    wv *= A.scale;
+    if (lane < k) {
+      A.ids[t * k + lane] = my_id;
+      A.w[t * k + lane] = wv;
+      if (A.ext_ids) A.ext_ids[t * k + lane] = my_id;
+      if (A.ext_w) A.ext_w[t * k + lane] = wv;
+    }
+  }
+  // ---- distinct experts and their pairs ----
+  for (int e = tid; e < MAX_E; e += nthr) s_cnt[e] = 0;
+  __syncthreads();
+  const int P = A.T * k;
+  for (int p = tid; p < P; p += nthr) atomicAdd(&s_cnt[A.ids[p]], 1);
+  __syncthreads();
+  // exclusive scans over experts of (cnt > 0) and cnt; thread tid owns the
+  // experts [tid * ept, (tid + 1) * ept)
+  {
+    const int ept = MAX_E / nthr;
+    int lu = 0, lc = 0;
+    for (int i = 0; i < ept; ++i) {
+      const int e = tid * ept + i;
+      const int c = (e < E) ? s_cnt[e] : 0;
+      lu += (c > 0);
+      lc += c;
+    }
+    int iu = lu, ic = lc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, iu, o);
+      const int b = __shfl_up_sync(0xffffffffu, ic, o);
+      if (lane >= o) { iu += a; ic += b; }
+    }
+    if (lane == 31) { s_wsum_u[warp] = iu; s_wsum_c[warp] = ic; }
+    __syncthreads();
+    if (warp == 0) {
+      int a = (lane < nwarp) ? s_wsum_u[lane] : 0;
+      int b = (lane < nwarp) ? s_wsum_c[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, a, o);
+        const int y = __shfl_up_sync(0xffffffffu, b, o);
+        if (lane >= o) { a += x; b += y; }
+      }
+      s_wsum_u[lane] = a;  // inclusive prefix over warps
+      s_wsum_c[lane] = b;
+    }
+    __syncthreads();
+    int pu = (warp ? s_wsum_u[warp - 1] : 0) + iu - lu;
+    int pc = (warp ? s_wsum_c[warp - 1] : 0) + ic - lc;
+    int* uniq_e = A.meta + 1;
+    int* uniq_p0 = A.meta + 1 + A.umax;
+    for (int i = 0; i < ept; ++i) {
+      const int e = tid * ept + i;
+      const int c = (e < E) ? s_cnt[e] : 0;
+      s_scan_c[e] = pc;
+      if (c > 0) { uniq_e[pu] = e; uniq_p0[pu] = pc; ++pu; }
+      pc += c;
+    }
+    if (tid == nthr - 1) {
+      A.meta[0] = pu;
+      uniq_p0[pu] = pc;
+    }
+  }
+  __syncthreads();
+  int* pairs = A.meta + 2 + 2 * A.umax;
+  if (A.mask_words > 0) {
+    // rank of pair (t, j) among its expert's pairs = rows t' < t that chose
+    // the same expert (a row picks an expert at most once)
+    const int W = A.mask_words;
+    for (int i = tid; i < E * W; i += nthr) s_mask[i] = 0u;
+    __syncthreads();
+    for (int p = tid; p < P; p += nthr) {
+      const int t = p / k;
+      atomicOr(&s_mask[A.ids[p] * W + (t >> 5)], 1u << (t & 31));
+    }
+    __syncthreads();
+    for (int p = tid; p < P; p += nthr) {
+      const int e = A.ids[p], t = p / k;
+      const uint32_t* m = s_mask + e * W;
+      int rank = __popc(m[t >> 5] & ((1u << (t & 31)) - 1u));
+      for (int w = 0; w < (t >> 5); ++w) rank += __popc(m[w]);
+      pairs[s_scan_c[e] + rank] = p;
+    }
+  } else {
+    for (int p = tid; p < P; p += nthr) {
+      const int e = A.ids[p];
+      int rank = 0;
+      for (int q = 0; q < p; ++q) rank += (A.ids[q] == e);
+      pairs[s_scan_c[e] + rank] = p;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(1024) k_route(const RouteArgs A) {
+  extern __shared__ int route_smem[];
+  route_block(A, route_smem);
+}
+
+// ---------------------------------------------------------------------------
 // dense gemv (k_dense_in / k_dense_out)
 // ---------------------------------------------------------------------------
 
@@ -179,8 +414,19 @@ struct DenseInArgs {
   int K;             // staged vector length (hidden)
   const void* x;     // [T, K] act dtype
   int x_dt;
-  float* out;        // [T, total_rows] fp32
+  float* out;        // [T, out_ld] fp32, rows [0, total_rows)
+  int out_ld;
   int T;
+  // routing fused into the CTA that finishes the router rows last
+  int fuse_route;
+  int route_ctas;    // CTAs whose row range meets the router rows [0, E)
+  int* route_counter;
+  RouteArgs route;
+  // after routing, prefetch the distinct experts' up(+gate) weights into L2
+  int prefetch_up;
+  int64_t pf_budget;         // at most this many bytes
+  const uint32_t* pf_q; const uint32_t* pf_sb; const uint32_t* pf_q2; const uint32_t* pf_sb2;
+  int64_t pf_q_bytes, pf_sb_bytes;   // per expert
 };
 
 struct DenseOutArgs {
@@ -204,6 +450,7 @@ struct DenseOutArgs {
   void* out;         // [T, H] act dtype
   float* delta;      // [T, H] fp32 or null
   int T;
+  int prefetch;      // prefetch this CTA's weight rows into L2 before waiting
 };
 
 // Streams the rows [r_begin, r_end) of the segments against xs (staged
@@ -334,6 +581,8 @@ __global__ void __launch_bounds__(NT) k_dense_in(const DenseInArgs A) {
   float* xs = reinterpret_cast<float*>(smem4);
   float* red = xs + TB * A.K;
   const int K4 = A.K >> 2;
+  griddep_wait();
+  griddep_launch();
   int rb, re;
   cta_rows(A.total_rows, rb, re);
   for (int t0 = 0; t0 < A.T; t0 += TB) {
@@ -351,9 +600,38 @@ __global__ void __launch_bounds__(NT) k_dense_in(const DenseInArgs A) {
         float s = 0.f;
 #pragma unroll
         for (int w = 0; w < NW; ++w) s += red[o * NW + w];
-        A.out[static_cast<int64_t>(t0 + t) * A.total_rows + r0 + rl] = s;
+        A.out[static_cast<int64_t>(t0 + t) * A.out_ld + r0 + rl] = s;
       }
       __syncthreads();
+    }
+  }
+  if (A.fuse_route && static_cast<int>(blockIdx.x) < A.route_ctas) {
+    // the last CTA to finish router rows routes all T rows
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(A.route_counter, 1) == A.route_ctas - 1);
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      route_block(A.route, reinterpret_cast<int*>(smem4));
+      if (threadIdx.x == 0) *A.route_counter = 0;
+      if (A.prefetch_up) {
+        __syncthreads();
+        const int nu = A.route.meta[0];
+        const int64_t per = (A.pf_q_bytes + A.pf_sb_bytes) * (A.pf_q2 ? 2 : 1);
+        const int64_t cap = A.pf_budget / (per > 0 ? per : 1);
+        const int nmax = static_cast<int>(nu < cap ? nu : cap);
+        for (int u = threadIdx.x; u < nmax; u += blockDim.x) {
+          const int64_t e = A.route.meta[1 + u];
+          prefetch_l2(reinterpret_cast<const char*>(A.pf_q) + e * A.pf_q_bytes, A.pf_q_bytes);
+          prefetch_l2(reinterpret_cast<const char*>(A.pf_sb) + e * A.pf_sb_bytes, A.pf_sb_bytes);
+          if (A.pf_q2) {
+            prefetch_l2(reinterpret_cast<const char*>(A.pf_q2) + e * A.pf_q_bytes, A.pf_q_bytes);
+            prefetch_l2(reinterpret_cast<const char*>(A.pf_sb2) + e * A.pf_sb_bytes, A.pf_sb_bytes);
+          }
+        }
+      }
     }
   }
 }
@@ -368,6 +646,16 @@ __global__ void __launch_bounds__(NT) k_dense_out(const DenseOutArgs A) {
   const int Kin = L ? L : A.total_rows;
   int rb, re;
   cta_rows(A.total_rows, rb, re);
+  // the weights do not depend on this forward's earlier kernels: start them
+  // towards L2 while those finish
+  if (A.prefetch && A.nseg && threadIdx.x < A.seg[0].nparts && re > rb) {
+    const DensePart& P = A.seg[0].part[threadIdx.x];
+    const int esz = P.dt == DT_FP32 ? 4 : 2;
+    prefetch_l2(static_cast<const char*>(P.w) + static_cast<int64_t>(rb) * P.wk * esz,
+                static_cast<int64_t>(re - rb) * P.wk * esz);
+  }
+  griddep_wait();
+  griddep_launch();
   for (int t0 = 0; t0 < A.T; t0 += TB) {
     const int tb = min(TB, A.T - t0);
     if (t0) __syncthreads();
@@ -431,172 +719,6 @@ __global__ void __launch_bounds__(NT) k_dense_out(const DenseOutArgs A) {
 // routing: top-k, weights, distinct-expert lists
 // ---------------------------------------------------------------------------
 
-// Route metadata (int32 buffer):
-//   [0]                      n_uniq
-//   [1, 1 + umax)            uniq_e[u]   distinct selected experts, ascending
-//   [1 + umax, 2 + 2 umax)   uniq_p0[u]  first position of u's pairs (u = n_uniq: total)
-//   [2 + 2 umax, ...)        pairs[i]    pair ids t*k + j grouped by expert, t ascending
-struct RouteArgs {
-  const float* logits;   // dense_in, row stride r_in, experts at columns [0, E)
-  int r_in;
-  const float* bias;     // [E] or null
-  int E, k, T;
-  int router, renorm;
-  float scale;
-  int* ids;              // [T*k]
-  float* w;              // [T*k]
-  int* meta;
-  int umax;
-  int* ext_ids;          // optional copies for the caller
-  float* ext_w;
-  int* status;
-};
-
-__device__ __forceinline__ bool key_better(float a, int ia, float b, int ib) {
-  return a > b || (a == b && ia < ib);
-}
-
-__global__ void __launch_bounds__(1024) k_route(const RouteArgs A) {
-  __shared__ int s_cnt[MAX_E];
-  __shared__ int s_scan_c[MAX_E];
-  __shared__ int s_wsum_u[32], s_wsum_c[32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = blockDim.x >> 5;
-  const int E = A.E, k = A.k;
-  const int nper = (E + 31) >> 5;
-
-  for (int t = warp; t < A.T; t += nwarp) {
-    const float* z = A.logits + static_cast<int64_t>(t) * A.r_in;
-    float key[32];
-    bool bad = false;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int e = lane + 32 * i;
-      float kv = -INFINITY;
-      if (i < nper && e < E) {
-        const float zz = z[e];
-        kv = (A.router == ROUTER_SOFTMAX) ? zz : 1.0f / (1.0f + expf(-zz));
-        if (A.router == ROUTER_SIGMOID && A.bias) kv += A.bias[e];
-        if (!isfinite(kv)) { bad = true; kv = -INFINITY; }
-      }
-      key[i] = kv;
-    }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(A.status, STATUS_NONFINITE);
-    uint32_t taken = 0;
-    int my_id = -1;
-    for (int j = 0; j < k; ++j) {
-      float bk = -INFINITY;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int e = lane + 32 * i;
-        if (i < nper && e < E && !((taken >> i) & 1u) && key_better(key[i], e, bk, bi)) {
-          bk = key[i]; bi = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (key_better(ok, oi, bk, bi)) { bk = ok; bi = oi; }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == j) my_id = bi;
-    }
-    // combine weights (lane j < k holds pick j)
-    float zj = (lane < k) ? z[my_id] : 0.f;
-    float wv = 0.f;
-    if (A.router == ROUTER_SOFTMAX) {
-      float m = __shfl_sync(0xffffffffu, zj, 0);   // largest selected logit
-      float den = 0.f;
-      if (A.renorm) {
-        float ex = (lane < k) ? expf(zj - m) : 0.f;
-        den = ex;
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-        wv = ex / den;
-      } else {
-        float mm = -INFINITY;
-        for (int i = lane; i < E; i += 32) mm = fmaxf(mm, z[i]);
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
-        for (int i = lane; i < E; i += 32) den += expf(z[i] - mm);
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-        wv = (lane < k) ? expf(zj - mm) / den : 0.f;
-      }
-    } else {
-      const float s = (lane < k) ? 1.0f / (1.0f + expf(-zj)) : 0.f;
-      wv = s;
-      if (A.renorm) {
-        float den = s;
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-        wv = s / den;
-      }
-    }
-    wv *= A.scale;
-    if (lane < k) {
-      A.ids[t * k + lane] = my_id;
-      A.w[t * k + lane] = wv;
-      if (A.ext_ids) A.ext_ids[t * k + lane] = my_id;
-      if (A.ext_w) A.ext_w[t * k + lane] = wv;
-    }
-  }
-  // ---- distinct experts and their pairs ----
-  for (int e = tid; e < MAX_E; e += blockDim.x) s_cnt[e] = 0;
-  __syncthreads();
-  const int P = A.T * k;
-  for (int p = tid; p < P; p += blockDim.x) atomicAdd(&s_cnt[A.ids[p]], 1);
-  __syncthreads();
-  // exclusive scans over experts of (cnt > 0) and cnt; blockDim == MAX_E
-  {
-    const int e = tid;
-    int vu = (e < E && s_cnt[e] > 0) ? 1 : 0;
-    int vc = (e < E) ? s_cnt[e] : 0;
-    int iu = vu, ic = vc;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int a = __shfl_up_sync(0xffffffffu, iu, o);
-      const int b = __shfl_up_sync(0xffffffffu, ic, o);
-      if (lane >= o) { iu += a; ic += b; }
-    }
-    if (lane == 31) { s_wsum_u[warp] = iu; s_wsum_c[warp] = ic; }
-    __syncthreads();
-    if (warp == 0) {
-      int a = (lane < nwarp) ? s_wsum_u[lane] : 0;
-      int b = (lane < nwarp) ? s_wsum_c[lane] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int x = __shfl_up_sync(0xffffffffu, a, o);
-        const int y = __shfl_up_sync(0xffffffffu, b, o);
-        if (lane >= o) { a += x; b += y; }
-      }
-      s_wsum_u[lane] = a;  // inclusive warp prefix
-      s_wsum_c[lane] = b;
-    }
-    __syncthreads();
-    const int pu = (warp ? s_wsum_u[warp - 1] : 0) + iu - vu;
-    const int pc = (warp ? s_wsum_c[warp - 1] : 0) + ic - vc;
-    s_scan_c[e] = pc;
-    int* uniq_e = A.meta + 1;
-    int* uniq_p0 = A.meta + 1 + A.umax;
-    if (vu) { uniq_e[pu] = e; uniq_p0[pu] = pc; }
-    if (e == MAX_E - 1) {
-      const int nu = pu + vu;
-      A.meta[0] = nu;
-      uniq_p0[nu] = pc + vc;
-    }
-  }
-  __syncthreads();
-  int* pairs = A.meta + 2 + 2 * A.umax;
-  for (int p = tid; p < P; p += blockDim.x) {
-    const int e = A.ids[p];
-    int rank = 0;
-    for (int q = 0; q < p; ++q) rank += (A.ids[q] == e);
-    pairs[s_scan_c[e] + rank] = p;
-  }
-}
-
 // ---------------------------------------------------------------------------
 // int4 affine expert gemv (k_expert)
 // ---------------------------------------------------------------------------
@@ -621,6 +743,11 @@ struct ExpertArgs {
   int64_t xin_off;         // element offset of the first row
   int xin_by_pair;
   float* out;              // [T*k, n_rows]
+  int pre_wait_phase;      // 1: the route metadata is final at launch (the kernel
+                           // before this one waited for it): let the next kernel
+                           // launch, prefetch, then wait for the previous kernel.
+                           // 0: wait first (the metadata may still be written).
+  int prefetch;            // prefetch this CTA's weight rows into L2 (pre-wait phase)
 };
 
 __device__ __forceinline__ void sb_decode(uint32_t v, int dt, float& s, float& b) {
@@ -652,6 +779,8 @@ __global__ void __launch_bounds__(NT) k_expert(const ExpertArgs A) {
   const int K = A.K, K4 = K >> 2, nchunk = K >> 5;
   float* xsum = reinterpret_cast<float*>(smem4 + PB * K4);   // [PB][nchunk]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (!A.pre_wait_phase) griddep_wait();
+  griddep_launch();
   const int n_uniq = A.meta[0];
   const int* uniq_e = A.meta + 1;
   const int* uniq_p0 = A.meta + 1 + A.umax;
@@ -660,6 +789,19 @@ __global__ void __launch_bounds__(NT) k_expert(const ExpertArgs A) {
   const int64_t rb = blockIdx.x * total / gridDim.x, re = (blockIdx.x + 1) * total / gridDim.x;
   const int ngr = K / A.G;
   const bool gated = A.q_gate != nullptr;
+  if (A.pre_wait_phase && A.prefetch && threadIdx.x == 0) {
+    // route metadata is final here: it was written before the previous kernel began
+    for (int64_t r0 = rb; r0 < re;) {
+      const int u = static_cast<int>(r0 / A.n_rows);
+      const int64_t uend = min(re, static_cast<int64_t>(u + 1) * A.n_rows);
+      const int64_t e = uniq_e[u];
+      const int64_t n0 = r0 - static_cast<int64_t>(u) * A.n_rows, nr = uend - r0;
+      prefetch_l2(A.q + (e * A.n_rows + n0) * (K >> 3), nr * (K >> 1));
+      prefetch_l2(A.sb + (e * A.n_rows + n0) * ngr, nr * ngr * 4);
+      r0 = uend;
+    }
+  }
+  if (A.pre_wait_phase) griddep_wait();
   for (int64_t r0 = rb; r0 < re;) {
     const int u = static_cast<int>(r0 / A.n_rows);
     const int64_t uend = min(re, static_cast<int64_t>(u + 1) * A.n_rows);

@@ -12,6 +12,7 @@
 
 #include "moe_layer.h"
 #include "moe_kernels.cuh"
+#include "moe_umma.cuh"
 
 using namespace moe;
 
@@ -61,6 +62,8 @@ struct moe_layer {
   float* hbuf = nullptr;      // [Tmax*k, F]
   float* pexp = nullptr;      // [Tmax*k, Kin]
   int* status = nullptr;
+  int* route_counter = nullptr;
+  void* bout = nullptr;       // [Tmax, L + F_sh] 16-bit operand of the grouped output GEMM
   void* x_stage = nullptr;    // [Tmax, H] act dtype (host-buffer forward)
   void* out_stage = nullptr;
 
@@ -72,6 +75,10 @@ struct moe_layer {
   int r_in = 0, off_fc1 = 0, off_shg = 0, off_shu = 0;
   int umax = 0;
   int kin = 0;
+  int grouped_min_t = 64;
+  int use_pdl = 1;        // programmatic dependent launch between the gemv-path kernels
+  int prefetch = 7;       // bit 0: experts' up weights after routing; bit 1: down
+                          // weights; bit 2: output-projection weights
 
   cudaError_t alloc(void** p, size_t n) {
     *p = nullptr;
@@ -185,6 +192,23 @@ static int pow2_at_least(int t, int cap) {
 // launches
 // ---------------------------------------------------------------------------
 
+// Launch with the programmatic-stream-serialization attribute when pdl is set.
+template <typename Arg>
+static cudaError_t launch_ex(void (*kern)(Arg), int grid, int block, size_t smem, cudaStream_t s,
+                             bool pdl, const Arg& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
 template <int TB>
 static size_t dense_smem(int K) {
   return static_cast<size_t>(TB) * (4ull * K + 4ull * RED_ROWS * NW);
@@ -192,19 +216,20 @@ static size_t dense_smem(int K) {
 
 template <typename Args, int TB>
 static cudaError_t launch_dense_in_t(const Args& a, int grid, cudaStream_t s) {
-  k_dense_in<TB><<<grid, NT, dense_smem<TB>(a.K), s>>>(a);
+  size_t smem = dense_smem<TB>(a.K);
+  if (a.fuse_route)
+    smem = std::max<size_t>(smem, ROUTE_SMEM_BYTES + static_cast<size_t>(a.route.E) * a.route.mask_words * 4);
+  k_dense_in<TB><<<grid, NT, smem, s>>>(a);
   return cudaGetLastError();
 }
 template <typename Args, int TB>
-static cudaError_t launch_dense_out_t(const Args& a, int grid, cudaStream_t s) {
-  k_dense_out<TB><<<grid, NT, dense_smem<TB>(a.K), s>>>(a);
-  return cudaGetLastError();
+static cudaError_t launch_dense_out_t(const Args& a, int grid, cudaStream_t s, bool pdl) {
+  return launch_ex<Args>(k_dense_out<TB>, grid, NT, dense_smem<TB>(a.K), s, pdl, a);
 }
 template <int PB>
-static cudaError_t launch_expert_t(const ExpertArgs& a, int grid, cudaStream_t s) {
+static cudaError_t launch_expert_t(const ExpertArgs& a, int grid, cudaStream_t s, bool pdl) {
   const size_t smem = static_cast<size_t>(PB) * (4ull * a.K + 4ull * (a.K / 32));
-  k_expert<PB><<<grid, NT, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_ex<ExpertArgs>(k_expert<PB>, grid, NT, smem, s, pdl, a);
 }
 
 static cudaError_t launch_dense_in(const DenseInArgs& a, int tb, int grid, cudaStream_t s) {
@@ -215,20 +240,21 @@ static cudaError_t launch_dense_in(const DenseInArgs& a, int tb, int grid, cudaS
     default: return launch_dense_in_t<DenseInArgs, 8>(a, grid, s);
   }
 }
-static cudaError_t launch_dense_out(const DenseOutArgs& a, int tb, int grid, cudaStream_t s) {
+static cudaError_t launch_dense_out(const DenseOutArgs& a, int tb, int grid, cudaStream_t s,
+                                    bool pdl) {
   switch (tb) {
-    case 1: return launch_dense_out_t<DenseOutArgs, 1>(a, grid, s);
-    case 2: return launch_dense_out_t<DenseOutArgs, 2>(a, grid, s);
-    case 4: return launch_dense_out_t<DenseOutArgs, 4>(a, grid, s);
-    default: return launch_dense_out_t<DenseOutArgs, 8>(a, grid, s);
+    case 1: return launch_dense_out_t<DenseOutArgs, 1>(a, grid, s, pdl);
+    case 2: return launch_dense_out_t<DenseOutArgs, 2>(a, grid, s, pdl);
+    case 4: return launch_dense_out_t<DenseOutArgs, 4>(a, grid, s, pdl);
+    default: return launch_dense_out_t<DenseOutArgs, 8>(a, grid, s, pdl);
   }
 }
-static cudaError_t launch_expert(const ExpertArgs& a, int pb, int grid, cudaStream_t s) {
+static cudaError_t launch_expert(const ExpertArgs& a, int pb, int grid, cudaStream_t s, bool pdl) {
   switch (pb) {
-    case 1: return launch_expert_t<1>(a, grid, s);
-    case 2: return launch_expert_t<2>(a, grid, s);
-    case 4: return launch_expert_t<4>(a, grid, s);
-    default: return launch_expert_t<8>(a, grid, s);
+    case 1: return launch_expert_t<1>(a, grid, s, pdl);
+    case 2: return launch_expert_t<2>(a, grid, s, pdl);
+    case 4: return launch_expert_t<4>(a, grid, s, pdl);
+    default: return launch_expert_t<8>(a, grid, s, pdl);
   }
 }
 
@@ -242,6 +268,7 @@ static cudaError_t set_smem_attrs() {
   MOE_SMEM_ATTR(k_dense_in<8>) MOE_SMEM_ATTR(k_dense_out<1>) MOE_SMEM_ATTR(k_dense_out<2>)
   MOE_SMEM_ATTR(k_dense_out<4>) MOE_SMEM_ATTR(k_dense_out<8>) MOE_SMEM_ATTR(k_expert<1>)
   MOE_SMEM_ATTR(k_expert<2>) MOE_SMEM_ATTR(k_expert<4>) MOE_SMEM_ATTR(k_expert<8>)
+  MOE_SMEM_ATTR(k_umma) MOE_SMEM_ATTR(k_route)
 #undef MOE_SMEM_ATTR
   return e;
 }
@@ -318,6 +345,9 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   L->off_shu = E + Lt + (gated ? Fs : 0);
   L->r_in = L->off_shu + Fs;
   L->umax = std::min(E, T * k);
+  if (const char* env = std::getenv("MOE_GROUPED_MIN_T")) L->grouped_min_t = std::max(1, std::atoi(env));
+  if (const char* env = std::getenv("MOE_PDL")) L->use_pdl = std::atoi(env) != 0;
+  if (const char* env = std::getenv("MOE_PREFETCH")) L->prefetch = std::atoi(env);
   {
     const size_t adt = dt_size(c.act_dtype), rdt = dt_size(c.router_dtype);
     const size_t sdt = dt_size(c.scale_dtype);
@@ -385,6 +415,9 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->pexp), P * kin * 4), "workspace");
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->status), 4), "workspace");
     MOE_TRY_CUDA(cudaMemsetAsync(L->status, 0, 4, s), "status clear");
+    MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->route_counter), 4), "workspace");
+    MOE_TRY_CUDA(cudaMemsetAsync(L->route_counter, 0, 4, s), "counter clear");
+    MOE_TRY_CUDA(L->alloc(&L->bout, static_cast<size_t>(T) * (Lt + Fs + 64) * 2), "workspace");
     MOE_TRY_CUDA(L->alloc(&L->x_stage, static_cast<size_t>(T) * H * adt), "workspace");
     MOE_TRY_CUDA(L->alloc(&L->out_stage, static_cast<size_t>(T) * H * adt), "workspace");
     MOE_TRY_CUDA(cudaStreamSynchronize(s), "create synchronise");
@@ -409,6 +442,11 @@ moe_status moe_layer_destroy(moe_layer* h) {
   return MOE_OK;
 }
 
+static cudaError_t launch_umma(const UmmaArgs& a, int grid, cudaStream_t s) {
+  k_umma<<<grid, UM_THREADS, umma_smem_bytes(), s>>>(a);
+  return cudaGetLastError();
+}
+
 static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out, void* stream,
                                int32_t* ext_ids, float* ext_w, float* delta) {
   if (!h) return MOE_ERR_INVALID_ARG;
@@ -425,70 +463,136 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     h->last_error = "x and out overlap";
     return MOE_ERR_INVALID_ARG;
   }
-  if (h->path == MOE_PATH_GROUPED) {
-    h->last_error = "the grouped path is not available in this build";
-    return MOE_ERR_UNSUPPORTED;
-  }
+  const bool grouped =
+      h->path == MOE_PATH_GROUPED || (h->path == MOE_PATH_AUTO && T >= h->grouped_min_t);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int H = c.hidden, E = c.n_experts, k = c.top_k, F = c.expert_ffn, Lt = c.latent;
   const int Fs = c.shared_ffn, kin = h->kin;
   const bool gated = c.act == MOE_ACT_SWIGLU;
-  cudaError_t e;
+  const int kout = Lt + Fs;
+  const int mma_dt = c.act_dtype;
+  cudaError_t e = cudaSuccess;
   auto mark = [&](int i) {
     if (h->profiling) cudaEventRecord(h->ev[i], s);
   };
-
-  // 1. dense matrices that read x
-  mark(0);
-  DenseInArgs di{};
-  int ns = 0;
-  auto seg1 = [&](const void* w, int dt, int rows, int row0) {
-    DenseSeg& S = di.seg[ns++];
+  auto seg1 = [&](DenseSeg* segs, int& ns, const void* w, int dt, int rows, int row0) {
+    DenseSeg& S = segs[ns++];
     S.part[0] = DensePart{w, dt, 0, H};
     S.nparts = 1;
     S.row0 = row0;
     S.rows = rows;
   };
-  seg1(h->router_w, c.router_dtype, E, 0);
-  if (Lt) seg1(h->fc1, c.act_dtype, Lt, h->off_fc1);
-  if (Fs && gated) seg1(h->sh_gate, c.act_dtype, Fs, h->off_shg);
-  if (Fs) seg1(h->sh_up, c.act_dtype, Fs, h->off_shu);
-  di.nseg = ns;
-  di.total_rows = h->r_in;
-  di.K = H;
-  di.x = x;
-  di.x_dt = c.act_dtype;
-  di.out = h->dense_in;
-  di.T = T;
-  const int tb_in = std::min(pow2_at_least(T, 8), dense_tb_cap(H));
-  const int grid_in = std::max(1, std::min(h->num_sms * 2, (h->r_in + 3) / 4));
-  if ((e = launch_dense_in(di, tb_in, grid_in, s)) != cudaSuccess) goto cuda_fail;
 
-  // 2. routing
-  mark(1);
+  RouteArgs ra{};
+  ra.logits = h->dense_in;
+  ra.r_in = h->r_in;
+  ra.bias = h->router_bias;
+  ra.E = E;
+  ra.k = k;
+  ra.T = T;
+  ra.router = c.router;
+  ra.renorm = c.renormalize;
+  ra.scale = c.routed_scale;
+  ra.ids = h->ids;
+  ra.w = h->wts;
+  ra.meta = h->meta;
+  ra.umax = h->umax;
+  ra.ext_ids = ext_ids;
+  ra.ext_w = ext_w;
+  ra.status = h->status;
   {
-    RouteArgs ra{};
-    ra.logits = h->dense_in;
-    ra.r_in = h->r_in;
-    ra.bias = h->router_bias;
-    ra.E = E;
-    ra.k = k;
-    ra.T = T;
-    ra.router = c.router;
-    ra.renorm = c.renormalize;
-    ra.scale = c.routed_scale;
-    ra.ids = h->ids;
-    ra.w = h->wts;
-    ra.meta = h->meta;
-    ra.umax = h->umax;
-    ra.ext_ids = ext_ids;
-    ra.ext_w = ext_w;
-    ra.status = h->status;
-    k_route<<<1, MAX_E, 0, s>>>(ra);
+    const int P = T * k;
+    const int W = (T + 31) / 32;
+    ra.mask_words = (P > 256 && static_cast<int64_t>(E) * W * 4 <= 160 * 1024) ? W : 0;
+  }
+  const bool fuse_route = !grouped;
+  const bool pdl = h->use_pdl && !grouped && !h->profiling;
+
+  // 1. dense matrices that read x: router, fc1_latent_proj, shared gate/up
+  mark(0);
+  {
+    const bool router_on_tc = grouped && c.router_dtype == c.act_dtype;
+    DenseInArgs di{};
+    int ns = 0;
+    if (!grouped || !router_on_tc) {
+      // CUDA-core pass: everything (gemv path) or only the router (grouped path
+      // with a router dtype the tensor-core operands do not share)
+      seg1(di.seg, ns, h->router_w, c.router_dtype, E, 0);
+      if (!grouped) {
+        if (Lt) seg1(di.seg, ns, h->fc1, c.act_dtype, Lt, h->off_fc1);
+        if (Fs && gated) seg1(di.seg, ns, h->sh_gate, c.act_dtype, Fs, h->off_shg);
+        if (Fs) seg1(di.seg, ns, h->sh_up, c.act_dtype, Fs, h->off_shu);
+      }
+      di.nseg = ns;
+      di.total_rows = grouped ? E : h->r_in;
+      di.out_ld = h->r_in;
+      di.K = H;
+      di.x = x;
+      di.x_dt = c.act_dtype;
+      di.out = h->dense_in;
+      di.T = T;
+      const int tb_in = std::min(pow2_at_least(T, 8), dense_tb_cap(H));
+      const int grid_in = std::max(1, std::min(h->num_sms * 2, (di.total_rows + 3) / 4));
+      if (fuse_route) {
+        di.fuse_route = 1;
+        di.route = ra;
+        di.route_counter = h->route_counter;
+        int rc = 0;
+        while (rc < grid_in &&
+               static_cast<int64_t>(rc) * di.total_rows / grid_in < static_cast<int64_t>(E))
+          ++rc;
+        di.route_ctas = rc;
+        if (h->prefetch & 1) {
+          di.prefetch_up = 1;
+          di.pf_budget = 48ll << 20;
+          di.pf_q = h->up_q;
+          di.pf_sb = h->up_sb;
+          di.pf_q2 = gated ? h->gate_q : nullptr;
+          di.pf_sb2 = gated ? h->gate_sb : nullptr;
+          di.pf_q_bytes = static_cast<int64_t>(F) * kin / 2;
+          di.pf_sb_bytes = static_cast<int64_t>(F) * (kin / c.group_size) * 4;
+        }
+      }
+      if ((e = launch_dense_in(di, tb_in, grid_in, s)) != cudaSuccess) goto cuda_fail;
+    }
+    if (grouped) {
+      UmmaArgs ua{};
+      int n = 0;
+      const int col0 = router_on_tc ? 0 : E;
+      if (router_on_tc) seg1(ua.seg, n, h->router_w, c.router_dtype, E, 0);
+      if (Lt) seg1(ua.seg, n, h->fc1, c.act_dtype, Lt, h->off_fc1 - col0);
+      if (Fs && gated) seg1(ua.seg, n, h->sh_gate, c.act_dtype, Fs, h->off_shg - col0);
+      if (Fs) seg1(ua.seg, n, h->sh_up, c.act_dtype, Fs, h->off_shu - col0);
+      ua.nseg = n;
+      ua.n_rows = h->r_in - col0;
+      if (ua.n_rows > 0) {
+        ua.experts = 0;
+        ua.n_tokens = T;
+        ua.K = H;
+        ua.a_mode = UA_DENSE;
+        ua.mma_dt = mma_dt;
+        ua.b0 = x; ua.b0_dt = c.act_dtype; ua.b0_stride = H; ua.b0_off = 0; ua.b0_k = H;
+        ua.epi = UE_DENSE_IN;
+        ua.act = -1;
+        ua.out_f32 = h->dense_in;
+        ua.out_ld = h->r_in;
+        ua.out_col0 = col0;
+        ua.k = k;
+        ua.status = h->status;
+        if ((e = launch_umma(ua, h->num_sms, s)) != cudaSuccess) goto cuda_fail;
+      }
+    }
+  }
+
+  // 2. routing (fused into the dense pass on the gemv path)
+  mark(1);
+  if (!fuse_route) {
+    k_route<<<1, MAX_E, ROUTE_SMEM_BYTES + static_cast<size_t>(E) * ra.mask_words * 4, s>>>(ra);
     if ((e = cudaGetLastError()) != cudaSuccess) goto cuda_fail;
   }
+
   // 3. expert up (+gate) with the activation, 4. expert down
-  {
+  if (!grouped) {
     const int pb_up = std::min(pow2_at_least(T, 8), expert_pb_cap(kin));
     const int pb_dn = std::min(pow2_at_least(T, 8), expert_pb_cap(F));
     const int grid_x = h->num_sms * 4;
@@ -506,22 +610,17 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     up.umax = h->umax;
     up.k = k;
     if (Lt) {
-      up.xin = h->dense_in;
-      up.xin_dt = DT_FP32;
-      up.xin_stride = h->r_in;
-      up.xin_off = h->off_fc1;
+      up.xin = h->dense_in; up.xin_dt = DT_FP32; up.xin_stride = h->r_in; up.xin_off = h->off_fc1;
     } else {
-      up.xin = x;
-      up.xin_dt = c.act_dtype;
-      up.xin_stride = H;
-      up.xin_off = 0;
+      up.xin = x; up.xin_dt = c.act_dtype; up.xin_stride = H; up.xin_off = 0;
     }
     up.xin_by_pair = 0;
     up.out = h->hbuf;
+    up.pre_wait_phase = 0;
+    up.prefetch = 0;
     mark(2);
-    if ((e = launch_expert(up, pb_up, grid_x, s)) != cudaSuccess) goto cuda_fail;
+    if ((e = launch_expert(up, pb_up, grid_x, s, pdl)) != cudaSuccess) goto cuda_fail;
     mark(3);
-
     ExpertArgs dn = up;
     dn.n_rows = kin;
     dn.K = F;
@@ -530,18 +629,90 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     dn.q_gate = nullptr;
     dn.sb_gate = nullptr;
     dn.act = -1;
-    dn.xin = h->hbuf;
-    dn.xin_dt = DT_FP32;
-    dn.xin_stride = F;
-    dn.xin_off = 0;
+    dn.xin = h->hbuf; dn.xin_dt = DT_FP32; dn.xin_stride = F; dn.xin_off = 0;
     dn.xin_by_pair = 1;
     dn.out = h->pexp;
-    if ((e = launch_expert(dn, pb_dn, grid_x, s)) != cudaSuccess) goto cuda_fail;
+    dn.pre_wait_phase = 1;
+    dn.prefetch = (h->prefetch >> 1) & 1;
+    if ((e = launch_expert(dn, pb_dn, grid_x, s, pdl)) != cudaSuccess) goto cuda_fail;
+  } else {
+    UmmaArgs up{};
+    up.experts = 1;
+    up.meta = h->meta;
+    up.umax = h->umax;
+    up.n_rows = F;
+    up.K = kin;
+    up.a_mode = UA_INT4;
+    up.q = h->up_q;
+    up.sb = h->up_sb;
+    up.q2 = gated ? h->gate_q : nullptr;
+    up.sb2 = gated ? h->gate_sb : nullptr;
+    up.G = c.group_size;
+    up.s_dt = c.scale_dtype;
+    up.mma_dt = mma_dt;
+    if (Lt) {
+      up.b0 = h->dense_in; up.b0_dt = DT_FP32; up.b0_stride = h->r_in; up.b0_off = h->off_fc1;
+    } else {
+      up.b0 = x; up.b0_dt = c.act_dtype; up.b0_stride = H; up.b0_off = 0;
+    }
+    up.b0_k = kin;
+    up.by_pair = 0;
+    up.k = k;
+    up.epi = UE_ROWS;
+    up.act = c.act;
+    up.out_f32 = h->hbuf;
+    up.status = h->status;
+    mark(2);
+    if ((e = launch_umma(up, h->num_sms, s)) != cudaSuccess) goto cuda_fail;
+    mark(3);
+    UmmaArgs dn = up;
+    dn.n_rows = kin;
+    dn.K = F;
+    dn.q = h->down_q;
+    dn.sb = h->down_sb;
+    dn.q2 = nullptr;
+    dn.sb2 = nullptr;
+    dn.b0 = h->hbuf; dn.b0_dt = DT_FP32; dn.b0_stride = F; dn.b0_off = 0; dn.b0_k = F;
+    dn.by_pair = 1;
+    dn.act = -1;
+    dn.out_f32 = h->pexp;
+    if ((e = launch_umma(dn, h->num_sms, s)) != cudaSuccess) goto cuda_fail;
   }
+
   // 5. combine + fc2 + shared down + residual
-  {
+  mark(4);
+  if (grouped && kout) {
+    PrepOutArgs pa{};
+    pa.T = T; pa.L = Lt; pa.Fs = Fs; pa.k = k; pa.act = c.act; pa.mma_dt = mma_dt;
+    pa.pexp = h->pexp; pa.wts = h->wts; pa.dense_in = h->dense_in; pa.r_in = h->r_in;
+    pa.sh_g_off = h->off_shg; pa.sh_u_off = h->off_shu;
+    pa.bout = static_cast<unsigned short*>(h->bout);
+    const int64_t n = static_cast<int64_t>(T) * kout;
+    k_prep_out<<<static_cast<int>(std::min<int64_t>((n + 255) / 256, 4096)), 256, 0, s>>>(pa);
+    if ((e = cudaGetLastError()) != cudaSuccess) goto cuda_fail;
+    UmmaArgs ua{};
+    DenseSeg& S = ua.seg[0];
+    S.nparts = 0;
+    if (Lt) S.part[S.nparts++] = DensePart{h->fc2, c.act_dtype, 0, Lt};
+    if (Fs) S.part[S.nparts++] = DensePart{h->sh_down, c.act_dtype, Lt, Fs};
+    S.row0 = 0;
+    S.rows = H;
+    ua.nseg = 1;
+    ua.experts = 0;
+    ua.n_tokens = T;
+    ua.n_rows = H;
+    ua.K = kout;
+    ua.a_mode = UA_DENSE;
+    ua.mma_dt = mma_dt;
+    ua.b0 = h->bout; ua.b0_dt = mma_dt; ua.b0_stride = kout; ua.b0_off = 0; ua.b0_k = kout;
+    ua.k = k;
+    ua.epi = UE_OUT;
+    ua.x = x; ua.x_dt = c.act_dtype; ua.out = out; ua.delta = delta;
+    ua.pexp = h->pexp; ua.wts = h->wts; ua.add_combine = Lt ? 0 : 1;
+    ua.status = h->status;
+    if ((e = launch_umma(ua, h->num_sms, s)) != cudaSuccess) goto cuda_fail;
+  } else {
     DenseOutArgs dout{};
-    const int kout = (Lt ? Lt : 0) + Fs;
     dout.nseg = 0;
     if (kout) {
       DenseSeg& S = dout.seg[0];
@@ -569,14 +740,13 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     dout.out = out;
     dout.delta = delta;
     dout.T = T;
+    dout.prefetch = (h->prefetch >> 2) & 1;
     const int tb_out = kout ? std::min(pow2_at_least(T, 8), dense_tb_cap(kout)) : pow2_at_least(T, 8);
     const int grid_out = std::max(1, std::min(h->num_sms * 2, (H + 3) / 4));
-    mark(4);
-    if ((e = launch_dense_out(dout, tb_out, grid_out, s)) != cudaSuccess) goto cuda_fail;
-    mark(5);
-    if (h->profiling) h->profiled = true;
+    if ((e = launch_dense_out(dout, tb_out, grid_out, s, pdl)) != cudaSuccess) goto cuda_fail;
   }
-  (void)F;
+  mark(5);
+  if (h->profiling) h->profiled = true;
   return MOE_OK;
 cuda_fail:
   h->last_error = std::string("launch failed: ") + cudaGetErrorString(e);
@@ -620,6 +790,10 @@ moe_status moe_layer_set_path(moe_layer* h, int32_t path) {
   if (!h) return MOE_ERR_INVALID_ARG;
   if (path != MOE_PATH_AUTO && path != MOE_PATH_GEMV && path != MOE_PATH_GROUPED)
     return MOE_ERR_INVALID_ARG;
+  if (path == MOE_PATH_GROUPED && h->cfg.act_dtype == MOE_DTYPE_FP32) {
+    h->last_error = "the grouped path needs 16-bit activations";
+    return MOE_ERR_UNSUPPORTED;
+  }
   h->path = path;
   return MOE_OK;
 }

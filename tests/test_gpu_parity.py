@@ -51,7 +51,7 @@ def _parity(name, T, rows=None, max_tokens=None, seed=0, zipf=False):
     x, redraws = gu.margin_x(lay, T, seed=seed + T)
     got = gu.run_layer(h, x, lay.spec.act_dtype)
     sel = list(range(T)) if rows is None else list(rows)
-    ref = oracle.oracle_forward(lay, x[sel])
+    ref = gu.ora_forward(lay, x[sel])
     rr = gu.check_parity(got, ref, rows=sel, what=f"{name} T={T}")
     assert h.device_status() == 0
     return rr
@@ -100,7 +100,7 @@ def test_odd_shapes(name, T):
     try:
         x, _ = gu.margin_x(lay, T, seed=3)
         got = gu.run_layer(h, x, spec.act_dtype)
-        ref = oracle.oracle_forward(lay, x)
+        ref = gu.ora_forward(lay, x)
         gu.check_parity(got, ref, what=f"{name} T={T}")
     finally:
         h.close()
@@ -127,6 +127,44 @@ def test_batched_zipf_parity(T, rows):
     _parity("latent", T, rows=rows, max_tokens=256, zipf=True)
 
 
+# --- the tcgen05 grouped path (forced at small T, automatic from T = 64) ------
+
+@pytest.mark.parametrize("name,T", [("tiny", 1), ("tiny", 16), ("tiny", 37), ("latent", 4),
+                                    ("latent", 16), ("odd_latent_fp16", 12),
+                                    ("odd_relu2_noshared", 9)])
+def test_grouped_path_parity(name, T):
+    if name in ODD:
+        lay = mi.make_layer(ODD[name], 11)
+    else:
+        lay = gu.cached_layer(name)
+    h = gu.build_layer(lay, max(T, 16))
+    try:
+        h.set_path("grouped")
+        x, _ = gu.margin_x(lay, T, seed=90 + T)
+        got = gu.run_layer(h, x, lay.spec.act_dtype)
+        ref = gu.ora_forward(lay, x)
+        gu.check_parity(got, ref, what=f"grouped {name} T={T}")
+        assert h.device_status() == 0
+    finally:
+        h.close()
+
+
+def test_grouped_matches_gemv_path():
+    """Both expert paths on the same batch: identical expert choice, outputs
+    within the parity bound of each other."""
+    lay, h = handle_for("latent", 64, zipf=True)
+    x, _ = gu.margin_x(lay, 64, seed=95)
+    try:
+        h.set_path("gemv")
+        a = gu.run_layer(h, x, "bf16")
+        h.set_path("grouped")
+        b = gu.run_layer(h, x, "bf16")
+    finally:
+        h.set_path("auto")
+    assert np.array_equal(a["ids"], b["ids"])
+    assert gu.rel_rms(b["delta"], a["delta"]) <= gu.REL_RMS
+
+
 # --- heterogeneous five-layer stack, residual stream carried -----------------
 
 @pytest.mark.parametrize("T", [2, 9, 16])
@@ -142,7 +180,7 @@ def test_stack_parity(T):
         for li, (lay, h) in enumerate(zip(layers, handles)):
             out, ids, w, delta = h.forward_ex(cur)
             torch.cuda.synchronize()
-            ref = oracle.oracle_forward(lay, ref_in)
+            ref = gu.ora_forward(lay, ref_in)
             assert np.array_equal(ids.cpu().numpy(), ref["ids"]), f"layer {li}"
             np.testing.assert_allclose(w.cpu().numpy(), ref["w"], rtol=gu.W_RTOL, atol=gu.W_ATOL)
             ref_in = mi._round_to_dtype(ref["out"], "bf16")
@@ -168,6 +206,28 @@ def test_row_invariance_bit_exact():
         one = h.forward(xt[t:t + 1].contiguous())
         torch.cuda.synchronize()
         assert torch.equal(one.view(torch.int16), full[t:t + 1].view(torch.int16)), t
+
+
+def test_graph_replay_equals_eager():
+    """The forward is stream-capturable: a captured CUDA graph replays to the
+    same bits as the eager call."""
+    lay, h = handle_for("latent", 16)
+    x, _ = gu.margin_x(lay, 4, seed=82)
+    xt = gu.to_torch_x(x, "bf16")
+    out = torch.empty_like(xt)
+    eager = h.forward(xt).clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        h.forward(xt, out)          # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        h.forward(xt, out)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
 
 
 def test_repeat_is_deterministic():
@@ -228,7 +288,7 @@ def test_nonfinite_router_keys_rank_last_and_are_reported():
     try:
         x, _ = gu.margin_x(lay, 4, seed=81)
         got = gu.run_layer(h, x, "bf16")
-        ref = oracle.oracle_forward(lay, x)
+        ref = gu.ora_forward(lay, x)
         gu.check_parity(got, ref, what="nan bias")
         assert not np.isin(got["ids"], [2, 7, 11]).any()
         assert h.device_status() == 10  # MOE_ERR_NONFINITE
@@ -247,10 +307,8 @@ def test_forward_argument_errors():
         pkg.moe_layer_forward(h.handle, xt, 17, torch.empty_like(xt))
     with pytest.raises(pkg.MoEError, match="INVALID_ARG"):   # out overlaps x
         pkg.moe_layer_forward(h.handle, xt, 8, xt[4:])
-    with pytest.raises(pkg.MoEError, match="UNSUPPORTED"):
-        h.set_path("grouped")
-        h.forward(xt)
-    h.set_path("auto")
+    with pytest.raises(pkg.MoEError, match="INVALID_ARG"):   # unknown path id
+        pkg._capi._check(pkg.load_library().moe_layer_set_path(h.handle, 7), h.handle)
 
 
 def test_refusals_and_allocation_failures_leak_nothing():
