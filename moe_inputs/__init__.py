@@ -184,9 +184,18 @@ SPECS: Dict[str, LayerSpec] = {
 STACK_EXPERTS = (240, 304, 368, 432, 496)
 
 
+# Weight scale of the stacked layers.  A model puts a norm in front of every
+# MoE layer; this layer has none, and with N(0, 0.02) weights the squared-ReLU
+# shared expert grows the carried residual stream quadratically from layer to
+# layer (RMS 1 -> 3 -> 30 -> 3e3 ...).  At 0.008 each layer adds a delta of
+# RMS ~0.2 to a stream of RMS ~1, which stays bounded over the five layers.
+STACK_WEIGHT_STD = 0.008
+
+
 def stack_specs() -> List[LayerSpec]:
     """Five latent layers with the per-layer expert counts of the Bolt stack."""
-    return [SPECS["latent"].with_(name=f"latent_e{e}", n_experts=e) for e in STACK_EXPERTS]
+    return [SPECS["latent"].with_(name=f"latent_e{e}", n_experts=e, weight_std=STACK_WEIGHT_STD)
+            for e in STACK_EXPERTS]
 
 
 def spec_for(name: str) -> LayerSpec:

@@ -30,7 +30,7 @@ constexpr int UM_M = 128;       // weight rows per tile (MMA M)
 constexpr int UM_KC = 64;       // K elements per stage
 constexpr int UM_NMAX = 256;    // tokens per MMA (MMA N, multiple of 16)
 constexpr int UM_THREADS = 256;
-constexpr uint32_t UM_SPIN_LIMIT = 1u << 26;
+constexpr uint32_t UM_SPIN_LIMIT = 1u << 22;
 
 // canonical K-major no-swizzle layout of a [rows x 64] 16-bit tile:
 // core matrix (row / 8, k / 8) at (row / 8) * 1024 + (k / 8) * 128 bytes,

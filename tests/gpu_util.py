@@ -38,6 +38,8 @@ def margin_x(layer, T: int, seed: int = 0, min_margin: float = MIN_MARGIN, stack
     spec = layer.spec
     rng = np.random.Generator(np.random.PCG64(2_000_003 + seed))
     layers = stack if stack is not None else [layer]
+    routers = [(oracle.widen(l.router_w, l.spec.router_dtype),
+                None if l.router_bias is None else l.router_bias.astype(np.float64)) for l in layers]
     rows, redraws = [], 0
     while len(rows) < T:
         cand = mi.draw_x_rows(spec, 8, rng)
@@ -47,10 +49,9 @@ def margin_x(layer, T: int, seed: int = 0, min_margin: float = MIN_MARGIN, stack
             cur = row
             for li, lay in enumerate(layers):
                 sp = lay.spec
-                Wr = oracle.widen(lay.router_w, sp.router_dtype)
-                bias = None if lay.router_bias is None else lay.router_bias.astype(np.float64)
+                Wr, bias = routers[li]
                 z = Wr @ oracle.widen(cur, sp.act_dtype)[0]
-                if oracle.routing_margin(z, sp, bias) < min_margin:
+                if not oracle.routing_margin(z, sp, bias) >= min_margin:   # NaN fails too
                     ok = False
                     break
                 if li + 1 < len(layers):

@@ -115,7 +115,7 @@ def test_latent_parity(T):
 
 # --- non-latent fp16 sigmoid top-8 layer (H=6144, E=256) at full size ---------
 
-@pytest.mark.parametrize("T,rows", [(1, None), (4, None), (32, [0, 13, 31])])
+@pytest.mark.parametrize("T,rows", [(1, None), (4, [0, 3]), (32, [0, 31])])
 def test_nonlatent_parity(T, rows):
     _parity("nonlatent", T, rows=rows, max_tokens=32)
 
@@ -167,28 +167,43 @@ def test_grouped_matches_gemv_path():
 
 # --- heterogeneous five-layer stack, residual stream carried -----------------
 
-@pytest.mark.parametrize("T", [2, 9, 16])
-def test_stack_parity(T):
-    layers = [mi.make_layer(s, i) for i, s in enumerate(mi.stack_specs())]
-    x, _ = gu.margin_x(layers[0], T, seed=40 + T, stack=layers)
-    # oracle follows its own residual stream, rounding each layer's output to
-    # the activation dtype as the GPU layer does
-    ref_in = x
+_STACK = {}
+
+
+def stack_layers():
+    if "layers" not in _STACK:
+        _STACK["layers"] = [mi.make_layer(s, i) for i, s in enumerate(mi.stack_specs())]
+    return _STACK["layers"]
+
+
+@pytest.mark.parametrize("T,rows", [(2, None), (9, [0, 4, 8]), (16, [0, 7, 15])])
+def test_stack_parity(T, rows):
+    """Five stacked layers (E = 240..496), the output of each the input of the
+    next.  Checked rows are margin-filtered at every layer along the oracle's
+    own residual stream; the other rows are plain draws."""
+    layers = stack_layers()
+    sel = list(range(T)) if rows is None else rows
+    xs, _ = gu.margin_x(layers[0], len(sel), seed=40 + T, stack=layers)
+    x = mi.make_x(layers[0].spec, T, 50 + T)
+    x[sel] = xs
     handles = [gu.build_layer(l, 16) for l in layers]
     try:
         cur = gu.to_torch_x(x, "bf16")
+        ref_in = x[sel]
         for li, (lay, h) in enumerate(zip(layers, handles)):
             out, ids, w, delta = h.forward_ex(cur)
             torch.cuda.synchronize()
             ref = gu.ora_forward(lay, ref_in)
-            assert np.array_equal(ids.cpu().numpy(), ref["ids"]), f"layer {li}"
-            np.testing.assert_allclose(w.cpu().numpy(), ref["w"], rtol=gu.W_RTOL, atol=gu.W_ATOL)
+            assert np.array_equal(ids.cpu().numpy()[sel], ref["ids"]), f"layer {li}"
+            np.testing.assert_allclose(w.cpu().numpy()[sel], ref["w"], rtol=gu.W_RTOL,
+                                       atol=gu.W_ATOL)
             ref_in = mi._round_to_dtype(ref["out"], "bf16")
             cur = out
-        final = cur.float().cpu().numpy().astype(np.float64)
+        final = cur.float().cpu().numpy().astype(np.float64)[sel]
         want = ref["out"]
         assert gu.rel_rms(final, want) <= gu.REL_RMS
         assert gu.max_abs_frac(final, want) <= gu.MAX_ABS_FRAC
+        assert np.isfinite(final).all()
     finally:
         for h in handles:
             h.close()
