@@ -48,6 +48,12 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle sample budget")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--path", choices=["auto", "gemv", "grouped"], default="auto",
+                   help="routed-expert path (A/B); auto switches to grouped at T >= 64")
+    p.add_argument("--zipf", action="store_true", help="Zipf-skewed expert load (batched sweep)")
+    p.add_argument("--sweep", default="", help="comma-separated T values: time each and write "
+                   "one JSON line per T to --sweep-out (the main line is unchanged)")
+    p.add_argument("--sweep-out", default="sweep.jsonl")
     return p.parse_args()
 
 
@@ -276,10 +282,13 @@ def run_ours(args):
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
 
     spec = mi.SPECS["latent"]
-    layer = mi.make_layer(spec, args.seed + rank)
-    maxT = max(args.T, args.also_T or 1)
+    rb = mi.zipf_router_bias(spec.n_experts, args.seed + rank) if args.zipf else None
+    layer = mi.make_layer(spec, args.seed + rank, router_bias=rb)
+    sweep = [int(v) for v in args.sweep.split(",") if v.strip()]
+    maxT = max([args.T, args.also_T or 1] + sweep)
     cfg = pkg.MoEConfig.from_spec(spec, max_tokens=maxT)
     h = pkg.MoELayer(cfg, pkg.upload_arrays(layer.arrays(), device=dev))
+    h.set_path(args.path)
     torch.cuda.empty_cache()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream()
@@ -322,6 +331,27 @@ def run_ours(args):
                 "ms_per_step": t2 / len(m2["step_ms"]), "gbs": b2 / (t2 / 1e3) / 1e9,
                 "hbm_frac": b2 / (t2 / 1e3) / 1e9 / hbm_peak,
                 "mean_distinct_experts": float(np.mean(m2["n_uniq"]))}
+
+    # batched serving sweep (separate output file)
+    if sweep and rank == 0:
+        with open(args.sweep_out, "w") as f:
+            for T in sweep:
+                paths = ["gemv", "grouped"] if T >= 16 else ["gemv"]
+                for path in paths:
+                    h.set_path(path)
+                    ms = measure(torch, pkg, spec, h, T, max(20, args.steps // 4), 3,
+                                 args.seed + 7, flush, stream, profile=False)
+                    tt = sum(ms["step_ms"])
+                    bb = sum(layer_bytes(spec, T, u) for u in ms["n_uniq"])
+                    f.write(json.dumps({
+                        "T": T, "path": path, "zipf": bool(args.zipf),
+                        "tokens_per_s": len(ms["step_ms"]) * T / (tt / 1e3),
+                        "ms_per_step": tt / len(ms["step_ms"]),
+                        "gbs": bb / (tt / 1e3) / 1e9, "hbm_frac": bb / (tt / 1e3) / 1e9 / hbm_peak,
+                        "mean_distinct_experts": float(np.mean(ms["n_uniq"])),
+                        "expert_bytes_per_token": (float(np.mean(ms["n_uniq"])) *
+                                                   sum(expert_bytes(spec)) / T)}) + "\n")
+        h.set_path(args.path)
 
     # end to end through the host-buffer C-ABI call
     xs_host = [x.cpu().pin_memory() for x in m["xs"][:8]]

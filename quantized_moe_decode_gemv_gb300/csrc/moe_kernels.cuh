@@ -774,7 +774,7 @@ __device__ __forceinline__ float chunk_dot(const uint4 w, const float4* x8, int 
 }
 
 template <int PB>
-__global__ void __launch_bounds__(NT) k_expert(const ExpertArgs A) {
+__global__ void __launch_bounds__(NT, 2) k_expert(const ExpertArgs A) {
   extern __shared__ float4 smem4[];
   const int K = A.K, K4 = K >> 2, nchunk = K >> 5;
   float* xsum = reinterpret_cast<float*>(smem4 + PB * K4);   // [PB][nchunk]
@@ -833,52 +833,86 @@ __global__ void __launch_bounds__(NT) k_expert(const ExpertArgs A) {
         xsum[pp * nchunk + c] = s;
       }
       __syncthreads();
-      // rows of expert u in this CTA: one warp per row
-      for (int64_t r = r0 + warp; r < uend; r += NW) {
-        const int n = static_cast<int>(r - static_cast<int64_t>(u) * A.n_rows);
-        const int64_t rowq = (static_cast<int64_t>(e) * A.n_rows + n) * (K >> 3);
-        const int64_t rows = (static_cast<int64_t>(e) * A.n_rows + n) * ngr;
-        float acc[PB], accg[PB];
+      // rows of expert u in this CTA: one warp per row, RR rows per warp in
+      // flight (rows warp, warp + NW, ... of the CTA's range)
+      constexpr int RR = (PB <= 2) ? 4 : (PB <= 4 ? 2 : 1);
+      constexpr int NV = RR * PB * 2;   // up and gate partial sums
+      for (int64_t rbase = r0 + warp; rbase < uend; rbase += static_cast<int64_t>(NW) * RR) {
+        int nn[RR];
+        int64_t rowq[RR], rows[RR];
+        bool live[RR];
 #pragma unroll
-        for (int pp = 0; pp < PB; ++pp) { acc[pp] = 0.f; accg[pp] = 0.f; }
+        for (int j = 0; j < RR; ++j) {
+          const int64_t r = rbase + static_cast<int64_t>(NW) * j;
+          live[j] = r < uend;
+          nn[j] = static_cast<int>((live[j] ? r : rbase) - static_cast<int64_t>(u) * A.n_rows);
+          rowq[j] = (static_cast<int64_t>(e) * A.n_rows + nn[j]) * (K >> 3);
+          rows[j] = (static_cast<int64_t>(e) * A.n_rows + nn[j]) * ngr;
+        }
+        float acc[RR][PB], accg[RR][PB];
+#pragma unroll
+        for (int j = 0; j < RR; ++j)
+#pragma unroll
+          for (int pp = 0; pp < PB; ++pp) { acc[j][pp] = 0.f; accg[j][pp] = 0.f; }
         for (int c = lane; c < nchunk; c += 32) {
-          const uint4 w = ldg_stream(A.q + rowq + 4 * c);
           const int g = (c << 5) / A.G;
-          float s, b;
-          sb_decode(ldg_u32(A.sb + rows + g), A.s_dt, s, b);
-          const float s16 = 16.f * s, bb = b - s16;
-          uint4 wg = make_uint4(0u, 0u, 0u, 0u);
-          float sg16 = 0.f, bbg = 0.f;
-          if (gated) {
-            wg = ldg_stream(A.q_gate + rowq + 4 * c);
-            float sg, bg;
-            sb_decode(ldg_u32(A.sb_gate + rows + g), A.s_dt, sg, bg);
-            sg16 = 16.f * sg; bbg = bg - sg16;
+          uint4 w[RR], wg[RR];
+          uint32_t sbv[RR], sbg[RR];
+#pragma unroll
+          for (int j = 0; j < RR; ++j) {
+            if (live[j]) {
+              w[j] = ldg_stream(A.q + rowq[j] + 4 * c);
+              sbv[j] = ldg_u32(A.sb + rows[j] + g);
+              if (gated) {
+                wg[j] = ldg_stream(A.q_gate + rowq[j] + 4 * c);
+                sbg[j] = ldg_u32(A.sb_gate + rows[j] + g);
+              }
+            }
           }
 #pragma unroll
-          for (int pp = 0; pp < PB; ++pp) {
-            if (pp < np) {
-              const float4* x8 = smem4 + pp * K4 + 8 * c;
-              const float xs = xsum[pp * nchunk + c];
-              acc[pp] = fmaf(s16, chunk_dot(w, x8, c), fmaf(bb, xs, acc[pp]));
-              if (gated) accg[pp] = fmaf(sg16, chunk_dot(wg, x8, c), fmaf(bbg, xs, accg[pp]));
+          for (int j = 0; j < RR; ++j) {
+            if (!live[j]) continue;
+            float s, b;
+            sb_decode(sbv[j], A.s_dt, s, b);
+            const float s16 = 16.f * s, bb = b - s16;
+            float sg16 = 0.f, bbg = 0.f;
+            if (gated) {
+              float sg, bg;
+              sb_decode(sbg[j], A.s_dt, sg, bg);
+              sg16 = 16.f * sg; bbg = bg - sg16;
+            }
+#pragma unroll
+            for (int pp = 0; pp < PB; ++pp) {
+              if (pp < np) {
+                const float4* x8 = smem4 + pp * K4 + 8 * c;
+                const float xs = xsum[pp * nchunk + c];
+                acc[j][pp] = fmaf(s16, chunk_dot(w[j], x8, c), fmaf(bb, xs, acc[j][pp]));
+                if (gated)
+                  accg[j][pp] = fmaf(sg16, chunk_dot(wg[j], x8, c), fmaf(bbg, xs, accg[j][pp]));
+              }
             }
           }
         }
+        // warp reduce-scatter of all partial sums: value (j, pp, up|gate)
+        float v[NV];
 #pragma unroll
-        for (int pp = 0; pp < PB; ++pp) {
-          if (pp < np) {
-            float a = acc[pp], g = accg[pp];
+        for (int j = 0; j < RR; ++j)
 #pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) {
-              a += __shfl_xor_sync(0xffffffffu, a, o);
-              if (gated) g += __shfl_xor_sync(0xffffffffu, g, o);
-            }
-            if (lane == 0) {
-              const int pid = pairs[pc + pp];
-              const float v = (A.act >= 0) ? act_fn(A.act, g, a) : a;
-              A.out[static_cast<int64_t>(pid) * A.n_rows + n] = v;
-            }
+          for (int pp = 0; pp < PB; ++pp) {
+            v[(j * PB + pp) * 2] = acc[j][pp];
+            v[(j * PB + pp) * 2 + 1] = accg[j][pp];
+          }
+        const float tot = warp_reduce_scatter<NV>(v, lane);
+        constexpr int LPV = 32 / NV;
+        const int vi = lane / LPV;
+        const float other = __shfl_down_sync(0xffffffffu, tot, LPV);   // gate partner
+        if ((lane & (2 * LPV - 1)) == 0) {
+          const int j = (vi >> 1) / PB, pp = (vi >> 1) % PB;
+          if (live[j] && pp < np) {
+            const int pid = pairs[pc + pp];
+            const float a = tot, gv = other;
+            const float val = (A.act >= 0) ? act_fn(A.act, gv, a) : a;
+            A.out[static_cast<int64_t>(pid) * A.n_rows + nn[j]] = val;
           }
         }
       }

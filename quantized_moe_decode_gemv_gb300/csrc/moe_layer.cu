@@ -174,12 +174,12 @@ static moe_status validate_impl(const moe_layer_config* c, const moe_layer_weigh
 // dense staging rows per pass that fit shared memory for a staged width K
 static int dense_tb_cap(int K) {
   for (int tb = 8; tb >= 1; tb >>= 1)
-    if (static_cast<int64_t>(tb) * (4LL * K + 4LL * RED_ROWS * NW) <= kSmemMax) return tb;
+    if (static_cast<int64_t>(tb) * (4LL * K + 4LL * RED_ROWS * NW) <= kSmemMax - 2048) return tb;
   return 0;
 }
 static int expert_pb_cap(int K) {
   for (int pb = 8; pb >= 1; pb >>= 1)
-    if (static_cast<int64_t>(pb) * (4LL * K + 4LL * (K / 32)) <= kSmemMax) return pb;
+    if (static_cast<int64_t>(pb) * (4LL * K + 4LL * (K / 32)) <= kSmemMax - 2048) return pb;
   return 0;
 }
 static int pow2_at_least(int t, int cap) {
@@ -258,12 +258,22 @@ static cudaError_t launch_expert(const ExpertArgs& a, int pb, int grid, cudaStre
   }
 }
 
+// Allow each kernel the dynamic shared memory left beside its static shared
+// memory (227 KB per block in total).
+template <typename F>
+static cudaError_t set_smem_attr(F* fn) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(fn));
+  if (e != cudaSuccess) return e;
+  const int dyn = kSmemMax - static_cast<int>(fa.sharedSizeBytes);
+  return cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+}
+
 static cudaError_t set_smem_attrs() {
   cudaError_t e = cudaSuccess;
-#define MOE_SMEM_ATTR(fn)                                                              \
-  if (e == cudaSuccess)                                                                \
-    e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),                        \
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+#define MOE_SMEM_ATTR(fn) \
+  if (e == cudaSuccess) e = set_smem_attr(fn);
   MOE_SMEM_ATTR(k_dense_in<1>) MOE_SMEM_ATTR(k_dense_in<2>) MOE_SMEM_ATTR(k_dense_in<4>)
   MOE_SMEM_ATTR(k_dense_in<8>) MOE_SMEM_ATTR(k_dense_out<1>) MOE_SMEM_ATTR(k_dense_out<2>)
   MOE_SMEM_ATTR(k_dense_out<4>) MOE_SMEM_ATTR(k_dense_out<8>) MOE_SMEM_ATTR(k_expert<1>)
