@@ -72,14 +72,19 @@ __device__ __forceinline__ uint32_t ldg_u32(const void* p) {
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
 
-// Asynchronous prefetch of [p, p + bytes) into L2 by the bulk-copy engine;
-// p 16-byte aligned, bytes a multiple of 16 (issued in pieces of <= 64 KB).
+// Asynchronous prefetch of [p, p + bytes) into L2 by the bulk-copy engine.
+// The bulk prefetch needs a 16-byte aligned start and a size that is a
+// multiple of 16, so the range is widened to 16-byte bounds (every buffer the
+// library prefetches from is allocated with at least 256 bytes of padding).
 __device__ __forceinline__ void prefetch_l2(const void* p, int64_t bytes) {
-  const char* c = static_cast<const char*>(p);
-  for (int64_t off = 0; off < bytes; off += 65536) {
-    const int64_t rem = bytes - off;
+  if (bytes <= 0) return;
+  uint64_t a = reinterpret_cast<uint64_t>(p) & ~uint64_t(15);
+  const uint64_t e = (reinterpret_cast<uint64_t>(p) + static_cast<uint64_t>(bytes) + 15) &
+                     ~uint64_t(15);
+  for (; a < e; a += 65536) {
+    const uint64_t rem = e - a;
     const uint32_t n = static_cast<uint32_t>(rem < 65536 ? rem : 65536);
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c + off), "r"(n) : "memory");
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(n) : "memory");
   }
 }
 
