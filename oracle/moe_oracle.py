@@ -155,12 +155,17 @@ def route(z: np.ndarray, spec, bias: Optional[np.ndarray]):
 
 
 def routing_margin(z: np.ndarray, spec, bias: Optional[np.ndarray]) -> float:
-    """Gap between the k-th and (k+1)-th selection key of one row (inf if k=E)."""
+    """Gap between the k-th and (k+1)-th selection key of one row, in the
+    selection order of ``topk_order`` (non-finite keys rank last and count as
+    -inf); inf if k = E or the (k+1)-th key is non-finite."""
     keys = selection_keys(z, spec, bias)
     k = spec.top_k
     if k >= len(keys):
         return math.inf
-    srt = np.sort(keys)[::-1]
+    ranked = np.where(np.isfinite(keys), keys, -np.inf)
+    srt = np.sort(ranked)[::-1]
+    if srt[k] == -np.inf:
+        return math.inf if srt[k - 1] > -np.inf else 0.0
     return float(srt[k - 1] - srt[k])
 
 

@@ -263,6 +263,8 @@ class MoELayer:
     def _stream(self, stream):
         if stream is None:
             return self._torch.cuda.current_stream().cuda_stream
+        if hasattr(stream, "cuda_stream"):
+            return int(stream.cuda_stream)
         return int(stream)
 
     def forward(self, x, out=None, stream=None):
