@@ -77,8 +77,10 @@ struct moe_layer {
   int kin = 0;
   int grouped_min_t = 64;
   int use_pdl = 1;        // programmatic dependent launch between the gemv-path kernels
-  int prefetch = 7;       // bit 0: experts' up weights after routing; bit 1: down
-                          // weights; bit 2: output-projection weights
+  int expert_pb = 2;      // max token slots per pass of the gemv-path expert kernels
+  int prefetch = 6;       // bit 0: experts' up weights from the routing CTA (one SM's
+                          // bulk engine: slow, off by default); bit 1: down weights;
+                          // bit 2: output-projection weights
 
   cudaError_t alloc(void** p, size_t n) {
     *p = nullptr;
@@ -360,6 +362,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   if (const char* env = std::getenv("MOE_GROUPED_MIN_T")) L->grouped_min_t = std::max(1, std::atoi(env));
   if (const char* env = std::getenv("MOE_PDL")) L->use_pdl = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_PREFETCH")) L->prefetch = std::atoi(env);
+  if (const char* env = std::getenv("MOE_EXPERT_PB")) L->expert_pb = std::max(1, std::min(8, std::atoi(env)));
   {
     const size_t adt = dt_size(c.act_dtype), rdt = dt_size(c.router_dtype);
     const size_t sdt = dt_size(c.scale_dtype);
@@ -605,8 +608,10 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
 
   // 3. expert up (+gate) with the activation, 4. expert down
   if (!grouped) {
-    const int pb_up = std::min(pow2_at_least(T, 8), expert_pb_cap(kin));
-    const int pb_dn = std::min(pow2_at_least(T, 8), expert_pb_cap(F));
+    // token slots per pass: most distinct experts hold one or two of the
+    // batch's rows; experts with more loop over slot groups (L2 re-reads)
+    const int pb_up = std::min(pow2_at_least(T, h->expert_pb), expert_pb_cap(kin));
+    const int pb_dn = std::min(pow2_at_least(T, h->expert_pb), expert_pb_cap(F));
     const int grid_x = h->num_sms * 4;
     ExpertArgs up{};
     up.n_rows = F;
