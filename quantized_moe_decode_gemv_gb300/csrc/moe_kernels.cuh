@@ -39,7 +39,7 @@ namespace moe {
 constexpr int NT = 256;       // threads per CTA
 constexpr int NW = NT / 32;   // warps per CTA
 constexpr int RB = 4;         // dense rows per register batch
-constexpr int MAXC = 4;       // 16-byte chunks per thread per row per round
+constexpr int MAXC = 2;       // 16-byte chunks per thread per row per round
 constexpr int RED_ROWS = 64;  // dense rows per reduction round
 constexpr int MAX_E = 1024;   // routed experts served
 constexpr int MAX_K = 16;     // top-k served
@@ -53,17 +53,21 @@ enum : int { STATUS_NONFINITE = 1, STATUS_TIMEOUT = 2 };
 // small helpers
 // ---------------------------------------------------------------------------
 
+// Streaming loads of read-only weights.  Volatile so that the compiler keeps
+// them in program order and issues a batch of them before the first use
+// (a plain asm statement may be sunk next to its use, which serialises the
+// memory latency of every load).
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   uint4 r;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-      : "l"(p));
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
   return r;
 }
 
 __device__ __forceinline__ uint32_t ldg_u32(const void* p) {
   uint32_t r;
-  asm("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
   return r;
 }
 
@@ -211,7 +215,7 @@ constexpr int ROUTE_SMEM_BYTES = (2 * MAX_E + 64) * 4;
 // distinct selected experts (ascending) with their (row, pick) pairs in row
 // order.  Logits are read with ld.global.cg, so this may run in the last CTA
 // of the kernel that produced them.
-__device__ void route_block(const RouteArgs& A, int* smem) {
+static __device__ void route_block(const RouteArgs& A, int* smem) {
   int* s_cnt = smem;
   int* s_scan_c = smem + MAX_E;
   int* s_wsum_u = smem + 2 * MAX_E;
@@ -385,7 +389,7 @@ __device__ void route_block(const RouteArgs& A, int* smem) {
   }
 }
 
-__global__ void __launch_bounds__(1024) k_route(const RouteArgs A) {
+static __global__ void __launch_bounds__(1024) k_route(const RouteArgs A) {
   extern __shared__ int route_smem[];
   route_block(A, route_smem);
 }
@@ -580,8 +584,13 @@ __device__ __forceinline__ void cta_rows(int rows, int& b, int& e) {
   e = static_cast<int>((c + 1) * rows / g);
 }
 
+// CTAs per SM the dense kernels are compiled for: more resident warps keep
+// more weight loads in flight while other warps reduce.
 template <int TB>
-__global__ void __launch_bounds__(NT) k_dense_in(const DenseInArgs A) {
+constexpr int dense_min_blocks() { return TB <= 2 ? 4 : 2; }
+
+template <int TB>
+__global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_in(const DenseInArgs A) {
   extern __shared__ float4 smem4[];
   float* xs = reinterpret_cast<float*>(smem4);
   float* red = xs + TB * A.K;
@@ -642,7 +651,7 @@ __global__ void __launch_bounds__(NT) k_dense_in(const DenseInArgs A) {
 }
 
 template <int TB>
-__global__ void __launch_bounds__(NT) k_dense_out(const DenseOutArgs A) {
+__global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_out(const DenseOutArgs A) {
   extern __shared__ float4 smem4[];
   float* xs = reinterpret_cast<float*>(smem4);
   float* red = xs + TB * A.K;
@@ -778,8 +787,11 @@ __device__ __forceinline__ float chunk_dot(const uint4 w, const float4* x8, int 
   return s;
 }
 
-template <int PB>
-__global__ void __launch_bounds__(NT, 2) k_expert(const ExpertArgs A) {
+template <int PB, bool GATED>
+constexpr int expert_min_blocks() { return PB <= 2 ? (GATED ? 3 : 4) : 2; }
+
+template <int PB, bool GATED>
+__global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(const ExpertArgs A) {
   extern __shared__ float4 smem4[];
   const int K = A.K, K4 = K >> 2, nchunk = K >> 5;
   float* xsum = reinterpret_cast<float*>(smem4 + PB * K4);   // [PB][nchunk]
@@ -793,7 +805,7 @@ __global__ void __launch_bounds__(NT, 2) k_expert(const ExpertArgs A) {
   const int64_t total = static_cast<int64_t>(n_uniq) * A.n_rows;
   const int64_t rb = blockIdx.x * total / gridDim.x, re = (blockIdx.x + 1) * total / gridDim.x;
   const int ngr = K / A.G;
-  const bool gated = A.q_gate != nullptr;
+  constexpr bool gated = GATED;
   if (A.pre_wait_phase && A.prefetch && threadIdx.x == 0) {
     // route metadata is final here: it was written before the previous kernel began
     for (int64_t r0 = rb; r0 < re;) {
@@ -841,7 +853,7 @@ __global__ void __launch_bounds__(NT, 2) k_expert(const ExpertArgs A) {
       // rows of expert u in this CTA: one warp per row, RR rows per warp in
       // flight (rows warp, warp + NW, ... of the CTA's range)
       constexpr int RR = (PB <= 2) ? 4 : (PB <= 4 ? 2 : 1);
-      constexpr int NV = RR * PB * 2;   // up and gate partial sums
+      constexpr int NV = RR * PB * 2;   // up and gate partial sums (gate 0 when not gated)
       for (int64_t rbase = r0 + warp; rbase < uend; rbase += static_cast<int64_t>(NW) * RR) {
         int nn[RR];
         int64_t rowq[RR], rows[RR];
@@ -929,7 +941,7 @@ __global__ void __launch_bounds__(NT, 2) k_expert(const ExpertArgs A) {
 // ---------------------------------------------------------------------------
 // create-time re-layout: interleave a group's scale and bias into one word
 // ---------------------------------------------------------------------------
-__global__ void k_interleave_sb(const unsigned short* __restrict__ s,
+static __global__ void k_interleave_sb(const unsigned short* __restrict__ s,
                                 const unsigned short* __restrict__ b, uint32_t* __restrict__ out,
                                 int64_t n) {
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;

@@ -233,7 +233,8 @@ static cudaError_t launch_dense_out_t(const Args& a, int grid, cudaStream_t s, b
 template <int PB>
 static cudaError_t launch_expert_t(const ExpertArgs& a, int grid, cudaStream_t s, bool pdl) {
   const size_t smem = static_cast<size_t>(PB) * (4ull * a.K + 4ull * (a.K / 32));
-  return launch_ex<ExpertArgs>(k_expert<PB>, grid, NT, smem, s, pdl, a);
+  if (a.q_gate) return launch_ex<ExpertArgs>(k_expert<PB, true>, grid, NT, smem, s, pdl, a);
+  return launch_ex<ExpertArgs>(k_expert<PB, false>, grid, NT, smem, s, pdl, a);
 }
 
 static cudaError_t launch_dense_in(const DenseInArgs& a, int tb, int grid, cudaStream_t s) {
@@ -280,8 +281,11 @@ static cudaError_t set_smem_attrs() {
   if (e == cudaSuccess) e = set_smem_attr(fn);
   MOE_SMEM_ATTR(k_dense_in<1>) MOE_SMEM_ATTR(k_dense_in<2>) MOE_SMEM_ATTR(k_dense_in<4>)
   MOE_SMEM_ATTR(k_dense_in<8>) MOE_SMEM_ATTR(k_dense_out<1>) MOE_SMEM_ATTR(k_dense_out<2>)
-  MOE_SMEM_ATTR(k_dense_out<4>) MOE_SMEM_ATTR(k_dense_out<8>) MOE_SMEM_ATTR(k_expert<1>)
-  MOE_SMEM_ATTR(k_expert<2>) MOE_SMEM_ATTR(k_expert<4>) MOE_SMEM_ATTR(k_expert<8>)
+  MOE_SMEM_ATTR(k_dense_out<4>) MOE_SMEM_ATTR(k_dense_out<8>)
+  MOE_SMEM_ATTR((k_expert<1, false>)) MOE_SMEM_ATTR((k_expert<2, false>))
+  MOE_SMEM_ATTR((k_expert<4, false>)) MOE_SMEM_ATTR((k_expert<8, false>))
+  MOE_SMEM_ATTR((k_expert<1, true>)) MOE_SMEM_ATTR((k_expert<2, true>))
+  MOE_SMEM_ATTR((k_expert<4, true>)) MOE_SMEM_ATTR((k_expert<8, true>))
   MOE_SMEM_ATTR(k_umma) MOE_SMEM_ATTR(k_route)
 #undef MOE_SMEM_ATTR
   return e;
@@ -547,7 +551,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
       di.out = h->dense_in;
       di.T = T;
       const int tb_in = std::min(pow2_at_least(T, 8), dense_tb_cap(H));
-      const int grid_in = std::max(1, std::min(h->num_sms * 2, (di.total_rows + 3) / 4));
+      const int grid_in = std::max(1, std::min(h->num_sms * (tb_in <= 2 ? 4 : 2), (di.total_rows + 3) / 4));
       if (fuse_route) {
         di.fuse_route = 1;
         di.route = ra;
@@ -759,7 +763,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     dout.T = T;
     dout.prefetch = (h->prefetch >> 2) & 1;
     const int tb_out = kout ? std::min(pow2_at_least(T, 8), dense_tb_cap(kout)) : pow2_at_least(T, 8);
-    const int grid_out = std::max(1, std::min(h->num_sms * 2, (H + 3) / 4));
+    const int grid_out = std::max(1, std::min(h->num_sms * (tb_out <= 2 ? 4 : 2), (H + 3) / 4));
     if ((e = launch_dense_out(dout, tb_out, grid_out, s, pdl)) != cudaSuccess) goto cuda_fail;
   }
   mark(5);
