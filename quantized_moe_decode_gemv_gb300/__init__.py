@@ -7,5 +7,5 @@ arguments.  Importing a name that needs the library raises if it is missing.
 from ._capi import (  # noqa: F401
     MoEConfig, MoEError, MoELayer, load_library, moe_layer_create, moe_layer_destroy,
     moe_layer_device_status, moe_layer_forward, moe_layer_forward_ex, moe_layer_forward_host,
-    moe_layer_set_path, moe_layer_validate, torch_act_dtype, upload_arrays, SIGNATURES, LIB_PATH,
+    moe_layer_set_path, moe_layer_validate, moe_router_topk_noalloc, torch_act_dtype, upload_arrays, SIGNATURES, LIB_PATH,
 )

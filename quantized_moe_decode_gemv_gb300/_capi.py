@@ -81,6 +81,11 @@ SIGNATURES = {
     "moe_layer_destroy": (ctypes.c_int, [ctypes.c_void_p]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_layer_last_error": (ctypes.c_char_p, [ctypes.c_void_p]),
+    "moe_router_topk_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                               ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32,
+                                               ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                               ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
+                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "moe_debug_live_allocations": (ctypes.c_int64, []),
     "moe_debug_fail_allocation": (None, [ctypes.c_int32]),
 }
@@ -243,6 +248,18 @@ def moe_layer_set_path(handle: int, path: str) -> None:
 
 def moe_layer_device_status(handle: int, stream: int = 0) -> int:
     return load_library().moe_layer_device_status(handle, ctypes.c_void_p(stream))
+
+
+def moe_router_topk_noalloc(x, T: int, hidden: int, x_dtype: str, router_w, router_dtype: str,
+                            router_bias, n_experts: int, top_k: int, router: str,
+                            renormalize: bool, routed_scale: float, topk_ids, topk_w,
+                            stream: int = 0) -> None:
+    """Router gemv + top-k with no device allocation (see include/moe_layer.h)."""
+    lib = load_library()
+    _check(lib.moe_router_topk_noalloc(_ptr(x), T, hidden, DTYPE[x_dtype], _ptr(router_w),
+                                       DTYPE[router_dtype], _ptr(router_bias), n_experts, top_k,
+                                       ROUTER[router], int(bool(renormalize)), float(routed_scale),
+                                       _ptr(topk_ids), _ptr(topk_w), ctypes.c_void_p(stream)))
 
 
 def moe_layer_destroy(handle: int) -> None:
