@@ -176,6 +176,21 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&v)[NV], int lane) {
 }
 
 // ---------------------------------------------------------------------------
+// combine: the operand of the output projection, computed once per forward
+// ---------------------------------------------------------------------------
+
+// comb[t, :] = [ y_t = sum_j w[t, j] * pexp[t*k + j, :]  (latent layers; picks in
+//               order j = 0..k-1, fp32) | act(shared gate, shared up)[t, :] ]
+struct CombineArgs {
+  int T, L, Fs, k, act;
+  const float* pexp;      // [T*k, L]
+  const float* wts;       // [T*k]
+  const float* dense_in;  // [T, r_in]
+  int r_in, sh_g_off, sh_u_off;
+  float* comb;            // [T, L + Fs]
+};
+
+// ---------------------------------------------------------------------------
 // routing arguments
 // ---------------------------------------------------------------------------
 
@@ -391,6 +406,8 @@ static __device__ void route_block(const RouteArgs& A, int* smem) {
 
 static __global__ void __launch_bounds__(1024) k_route(const RouteArgs A) {
   extern __shared__ int route_smem[];
+  griddep_wait();
+  griddep_launch();
   route_block(A, route_smem);
 }
 
@@ -460,6 +477,7 @@ struct DenseOutArgs {
   float* delta;      // [T, H] fp32 or null
   int T;
   int prefetch;      // prefetch this CTA's weight rows into L2 before waiting
+  const float* staged;  // [T, K] fp32 staged vector computed once (k_combine), or null
 };
 
 // Streams the rows [r_begin, r_end) of the segments against xs (staged
@@ -677,7 +695,10 @@ __global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_out(const 
     for (int i = threadIdx.x; i < TB * K4; i += NT) {
       const int t = i / K4, f4 = i - t * K4;
       float v[4] = {0.f, 0.f, 0.f, 0.f};
-      if (t < tb) {
+      if (t < tb && A.staged) {
+        const float4 a = reinterpret_cast<const float4*>(A.staged)[static_cast<int64_t>(t0 + t) * K4 + f4];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+      } else if (t < tb) {
         const int tt = t0 + t;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -935,6 +956,31 @@ __global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(c
       }
     }
     r0 = uend;
+  }
+}
+
+static __global__ void __launch_bounds__(NT) k_combine(const CombineArgs A) {
+  // the output projection's pre-wait phase reads only weights: let it launch now
+  griddep_launch();
+  griddep_wait();
+  const int K = A.L + A.Fs;
+  const int64_t n = static_cast<int64_t>(A.T) * K;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(NT) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * NT) {
+    const int t = static_cast<int>(i / K), c = static_cast<int>(i - static_cast<int64_t>(t) * K);
+    float v;
+    if (c < A.L) {
+      v = 0.f;
+      for (int p = 0; p < A.k; ++p)
+        v = fmaf(A.wts[t * A.k + p], A.pexp[static_cast<int64_t>(t * A.k + p) * A.L + c], v);
+    } else {
+      const float* di = A.dense_in + static_cast<int64_t>(t) * A.r_in;
+      const int f = c - A.L;
+      const float u = di[A.sh_u_off + f];
+      const float g = (A.act == ACT_SWIGLU) ? di[A.sh_g_off + f] : 0.f;
+      v = act_fn(A.act, g, u);
+    }
+    A.comb[i] = v;
   }
 }
 

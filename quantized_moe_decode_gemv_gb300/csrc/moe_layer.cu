@@ -63,6 +63,7 @@ struct moe_layer {
   float* pexp = nullptr;      // [Tmax*k, Kin]
   int* status = nullptr;
   int* route_counter = nullptr;
+  float* comb = nullptr;      // [Tmax, L + F_sh] staged operand of the output projection
   void* bout = nullptr;       // [Tmax, L + F_sh] 16-bit operand of the grouped output GEMM
   void* x_stage = nullptr;    // [Tmax, H] act dtype (host-buffer forward)
   void* out_stage = nullptr;
@@ -78,6 +79,7 @@ struct moe_layer {
   int grouped_min_t = 64;
   int use_pdl = 1;        // programmatic dependent launch between the gemv-path kernels
   int expert_pb = 2;      // max token slots per pass of the gemv-path expert kernels
+  int fuse_route = 1;     // routing in the last router CTA of the dense pass (0: own kernel)
   int prefetch = 6;       // bit 0: experts' up weights from the routing CTA (one SM's
                           // bulk engine: slow, off by default); bit 1: down weights;
                           // bit 2: output-projection weights
@@ -367,6 +369,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   if (const char* env = std::getenv("MOE_PDL")) L->use_pdl = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_PREFETCH")) L->prefetch = std::atoi(env);
   if (const char* env = std::getenv("MOE_EXPERT_PB")) L->expert_pb = std::max(1, std::min(8, std::atoi(env)));
+  if (const char* env = std::getenv("MOE_FUSE_ROUTE")) L->fuse_route = std::atoi(env) != 0;
   {
     const size_t adt = dt_size(c.act_dtype), rdt = dt_size(c.router_dtype);
     const size_t sdt = dt_size(c.scale_dtype);
@@ -437,6 +440,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->route_counter), 4), "workspace");
     MOE_TRY_CUDA(cudaMemsetAsync(L->route_counter, 0, 4, s), "counter clear");
     MOE_TRY_CUDA(L->alloc(&L->bout, static_cast<size_t>(T) * (Lt + Fs + 64) * 2), "workspace");
+    MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->comb), static_cast<size_t>(T) * (Lt + Fs + 64) * 4), "workspace");
     MOE_TRY_CUDA(L->alloc(&L->x_stage, static_cast<size_t>(T) * H * adt), "workspace");
     MOE_TRY_CUDA(L->alloc(&L->out_stage, static_cast<size_t>(T) * H * adt), "workspace");
     MOE_TRY_CUDA(cudaStreamSynchronize(s), "create synchronise");
@@ -524,7 +528,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     const int W = (T + 31) / 32;
     ra.mask_words = (P > 256 && static_cast<int64_t>(E) * W * 4 <= 160 * 1024) ? W : 0;
   }
-  const bool fuse_route = !grouped;
+  const bool fuse_route = !grouped && h->fuse_route;
   const bool pdl = h->use_pdl && !grouped && !h->profiling;
 
   // 1. dense matrices that read x: router, fc1_latent_proj, shared gate/up
@@ -606,8 +610,10 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
   // 2. routing (fused into the dense pass on the gemv path)
   mark(1);
   if (!fuse_route) {
-    k_route<<<1, MAX_E, ROUTE_SMEM_BYTES + static_cast<size_t>(E) * ra.mask_words * 4, s>>>(ra);
-    if ((e = cudaGetLastError()) != cudaSuccess) goto cuda_fail;
+    if ((e = launch_ex<RouteArgs>(k_route, 1, MAX_E,
+                                  ROUTE_SMEM_BYTES + static_cast<size_t>(E) * ra.mask_words * 4, s,
+                                  pdl, ra)) != cudaSuccess)
+      goto cuda_fail;
   }
 
   // 3. expert up (+gate) with the activation, 4. expert down
@@ -762,6 +768,17 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     dout.delta = delta;
     dout.T = T;
     dout.prefetch = (h->prefetch >> 2) & 1;
+    if (kout) {
+      CombineArgs ca{};
+      ca.T = T; ca.L = Lt; ca.Fs = Fs; ca.k = k; ca.act = c.act;
+      ca.pexp = h->pexp; ca.wts = h->wts; ca.dense_in = h->dense_in; ca.r_in = h->r_in;
+      ca.sh_g_off = h->off_shg; ca.sh_u_off = h->off_shu;
+      ca.comb = h->comb;
+      const int64_t n = static_cast<int64_t>(T) * kout;
+      const int gc = static_cast<int>(std::min<int64_t>((n + NT - 1) / NT, h->num_sms * 4));
+      if ((e = launch_ex<CombineArgs>(k_combine, gc, NT, 0, s, pdl, ca)) != cudaSuccess) goto cuda_fail;
+      dout.staged = h->comb;
+    }
     const int tb_out = kout ? std::min(pow2_at_least(T, 8), dense_tb_cap(kout)) : pow2_at_least(T, 8);
     const int grid_out = std::max(1, std::min(h->num_sms * (tb_out <= 2 ? 4 : 2), (H + 3) / 4));
     if ((e = launch_dense_out(dout, tb_out, grid_out, s, pdl)) != cudaSuccess) goto cuda_fail;
