@@ -783,6 +783,7 @@ struct ExpertArgs {
                            // launch, prefetch, then wait for the previous kernel.
                            // 0: wait first (the metadata may still be written).
   int prefetch;            // prefetch this CTA's weight rows into L2 (pre-wait phase)
+  int cps;                 // CTAs per distinct-expert slot (grid = umax * cps)
 };
 
 __device__ __forceinline__ void sb_decode(uint32_t v, int dt, float& s, float& b) {
@@ -809,7 +810,7 @@ __device__ __forceinline__ float chunk_dot(const uint4 w, const float4* x8, int 
 }
 
 template <int PB, bool GATED>
-constexpr int expert_min_blocks() { return PB <= 2 ? (GATED ? 3 : 4) : 2; }
+constexpr int expert_min_blocks() { return PB <= 2 ? (GATED ? 2 : 3) : 2; }
 
 template <int PB, bool GATED>
 __global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(const ExpertArgs A) {
@@ -817,85 +818,108 @@ __global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(c
   const int K = A.K, K4 = K >> 2, nchunk = K >> 5;
   float* xsum = reinterpret_cast<float*>(smem4 + PB * K4);   // [PB][nchunk]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (!A.pre_wait_phase) griddep_wait();
-  griddep_launch();
-  const int n_uniq = A.meta[0];
+  const int ngr = K / A.G;
+  constexpr bool gated = GATED;
+  // rows of a weight matrix in flight per warp (rows warp, warp + NW, ...)
+  constexpr int RR = (PB <= 2) ? (GATED ? 2 : 4) : (PB <= 4 ? 2 : 1);
+  constexpr int NV = RR * PB * 2;   // up and gate partial sums (gate 0 when not gated)
+  // Static partition, independent of how many experts were selected: CTA
+  // blockIdx.x serves slot u (the u-th distinct selected expert) and rows
+  // [nb, ne) of its matrix; slots beyond the distinct count exit at once.
+  const int u = blockIdx.x / A.cps, part = blockIdx.x - u * A.cps;
+  const int nb = static_cast<int>(static_cast<int64_t>(part) * A.n_rows / A.cps);
+  const int ne = static_cast<int>(static_cast<int64_t>(part + 1) * A.n_rows / A.cps);
   const int* uniq_e = A.meta + 1;
   const int* uniq_p0 = A.meta + 1 + A.umax;
   const int* pairs = A.meta + 2 + 2 * A.umax;
-  const int64_t total = static_cast<int64_t>(n_uniq) * A.n_rows;
-  const int64_t rb = blockIdx.x * total / gridDim.x, re = (blockIdx.x + 1) * total / gridDim.x;
-  const int ngr = K / A.G;
-  constexpr bool gated = GATED;
+  if (!A.pre_wait_phase) griddep_wait();
+  griddep_launch();
+  if (u >= A.meta[0]) return;
+  const int64_t e = uniq_e[u];
   if (A.pre_wait_phase && A.prefetch && threadIdx.x == 0) {
-    // route metadata is final here: it was written before the previous kernel began
-    for (int64_t r0 = rb; r0 < re;) {
-      const int u = static_cast<int>(r0 / A.n_rows);
-      const int64_t uend = min(re, static_cast<int64_t>(u + 1) * A.n_rows);
-      const int64_t e = uniq_e[u];
-      const int64_t n0 = r0 - static_cast<int64_t>(u) * A.n_rows, nr = uend - r0;
-      prefetch_l2(A.q + (e * A.n_rows + n0) * (K >> 3), nr * (K >> 1));
-      prefetch_l2(A.sb + (e * A.n_rows + n0) * ngr, nr * ngr * 4);
-      r0 = uend;
-    }
+    // the route metadata was final before the previous kernel began
+    prefetch_l2(A.q + (e * A.n_rows + nb) * (K >> 3), static_cast<int64_t>(ne - nb) * (K >> 1));
+    prefetch_l2(A.sb + (e * A.n_rows + nb) * ngr, static_cast<int64_t>(ne - nb) * ngr * 4);
   }
   if (A.pre_wait_phase) griddep_wait();
-  for (int64_t r0 = rb; r0 < re;) {
-    const int u = static_cast<int>(r0 / A.n_rows);
-    const int64_t uend = min(re, static_cast<int64_t>(u + 1) * A.n_rows);
-    const int e = uniq_e[u];
-    const int pa = uniq_p0[u], pe = uniq_p0[u + 1];
-    for (int pc = pa; pc < pe; pc += PB) {
-      const int np = min(PB, pe - pc);
-      __syncthreads();
-      // stage the input rows of pairs [pc, pc + np), swizzled for 32-element chunks
-      for (int i = threadIdx.x; i < PB * K4; i += NT) {
-        const int pp = i / K4, f4 = i - pp * K4;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (pp < np) {
-          const int pid = pairs[pc + pp];
-          const int64_t row = A.xin_by_pair ? pid : (pid / A.k);
-          const int64_t base = A.xin_off + row * A.xin_stride + 4 * f4;
-          v.x = ld_any(A.xin, base, A.xin_dt); v.y = ld_any(A.xin, base + 1, A.xin_dt);
-          v.z = ld_any(A.xin, base + 2, A.xin_dt); v.w = ld_any(A.xin, base + 3, A.xin_dt);
+  const int pa = uniq_p0[u], pe = uniq_p0[u + 1];
+
+  // first row batch: issue its weight loads before staging the inputs, so
+  // their memory latency overlaps the staging
+  uint4 w0[RR], wg0[RR];
+  uint32_t sb0[RR], sbg0[RR];
+  {
+    const int c = lane;
+#pragma unroll
+    for (int j = 0; j < RR; ++j) {
+      const int n = nb + warp + NW * j;
+      if (n < ne && c < nchunk) {
+        const int64_t row = e * A.n_rows + n;
+        w0[j] = ldg_stream(A.q + row * (K >> 3) + 4 * c);
+        sb0[j] = ldg_u32(A.sb + row * ngr + (c << 5) / A.G);
+        if (gated) {
+          wg0[j] = ldg_stream(A.q_gate + row * (K >> 3) + 4 * c);
+          sbg0[j] = ldg_u32(A.sb_gate + row * ngr + (c << 5) / A.G);
         }
-        smem4[pp * K4 + swz(f4, 7)] = v;
       }
-      __syncthreads();
-      for (int i = threadIdx.x; i < PB * nchunk; i += NT) {
-        const int pp = i / nchunk, c = i - pp * nchunk;
-        const float4* x8 = smem4 + pp * K4 + 8 * c;
-        float s = 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) { const float4 a = x8[j]; s += (a.x + a.y) + (a.z + a.w); }
-        xsum[pp * nchunk + c] = s;
-      }
-      __syncthreads();
-      // rows of expert u in this CTA: one warp per row, RR rows per warp in
-      // flight (rows warp, warp + NW, ... of the CTA's range)
-      constexpr int RR = (PB <= 2) ? 4 : (PB <= 4 ? 2 : 1);
-      constexpr int NV = RR * PB * 2;   // up and gate partial sums (gate 0 when not gated)
-      for (int64_t rbase = r0 + warp; rbase < uend; rbase += static_cast<int64_t>(NW) * RR) {
-        int nn[RR];
-        int64_t rowq[RR], rows[RR];
-        bool live[RR];
-#pragma unroll
-        for (int j = 0; j < RR; ++j) {
-          const int64_t r = rbase + static_cast<int64_t>(NW) * j;
-          live[j] = r < uend;
-          nn[j] = static_cast<int>((live[j] ? r : rbase) - static_cast<int64_t>(u) * A.n_rows);
-          rowq[j] = (static_cast<int64_t>(e) * A.n_rows + nn[j]) * (K >> 3);
-          rows[j] = (static_cast<int64_t>(e) * A.n_rows + nn[j]) * ngr;
+    }
+  }
+  for (int pc = pa; pc < pe; pc += PB) {
+    const int np = min(PB, pe - pc);
+    if (pc != pa) __syncthreads();
+    // stage the input rows of pairs [pc, pc + np), swizzled for 32-element chunks
+    for (int i = threadIdx.x; i < PB * K4; i += NT) {
+      const int pp = i / K4, f4 = i - pp * K4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (pp < np) {
+        const int pid = pairs[pc + pp];
+        const int64_t row = A.xin_by_pair ? pid : (pid / A.k);
+        const int64_t base = A.xin_off + row * A.xin_stride + 4 * f4;
+        if (A.xin_dt == DT_FP32) {
+          v = *reinterpret_cast<const float4*>(static_cast<const float*>(A.xin) + base);
+        } else {
+          v.x = ld16(A.xin, base, A.xin_dt); v.y = ld16(A.xin, base + 1, A.xin_dt);
+          v.z = ld16(A.xin, base + 2, A.xin_dt); v.w = ld16(A.xin, base + 3, A.xin_dt);
         }
-        float acc[RR][PB], accg[RR][PB];
+      }
+      smem4[pp * K4 + swz(f4, 7)] = v;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < PB * nchunk; i += NT) {
+      const int pp = i / nchunk, c = i - pp * nchunk;
+      const float4* x8 = smem4 + pp * K4 + 8 * c;
+      float sx = 0.f;
 #pragma unroll
-        for (int j = 0; j < RR; ++j)
+      for (int j = 0; j < 8; ++j) { const float4 a = x8[j]; sx += (a.x + a.y) + (a.z + a.w); }
+      xsum[pp * nchunk + c] = sx;
+    }
+    __syncthreads();
+    for (int rbase = nb + warp; rbase < ne; rbase += NW * RR) {
+      const bool first = (pc == pa) && (rbase == nb + warp);
+      int nn[RR];
+      int64_t rowq[RR], rows[RR];
+      bool live[RR];
 #pragma unroll
-          for (int pp = 0; pp < PB; ++pp) { acc[j][pp] = 0.f; accg[j][pp] = 0.f; }
-        for (int c = lane; c < nchunk; c += 32) {
-          const int g = (c << 5) / A.G;
-          uint4 w[RR], wg[RR];
-          uint32_t sbv[RR], sbg[RR];
+      for (int j = 0; j < RR; ++j) {
+        const int n = rbase + NW * j;
+        live[j] = n < ne;
+        nn[j] = live[j] ? n : rbase;
+        rowq[j] = (e * A.n_rows + nn[j]) * (K >> 3);
+        rows[j] = (e * A.n_rows + nn[j]) * ngr;
+      }
+      float acc[RR][PB], accg[RR][PB];
+#pragma unroll
+      for (int j = 0; j < RR; ++j)
+#pragma unroll
+        for (int pp = 0; pp < PB; ++pp) { acc[j][pp] = 0.f; accg[j][pp] = 0.f; }
+      for (int c = lane; c < nchunk; c += 32) {
+        const int g = (c << 5) / A.G;
+        uint4 w[RR], wg[RR];
+        uint32_t sbv[RR], sbg[RR];
+        if (first && c == lane) {
+#pragma unroll
+          for (int j = 0; j < RR; ++j) { w[j] = w0[j]; sbv[j] = sb0[j]; wg[j] = wg0[j]; sbg[j] = sbg0[j]; }
+        } else {
 #pragma unroll
           for (int j = 0; j < RR; ++j) {
             if (live[j]) {
@@ -907,55 +931,53 @@ __global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(c
               }
             }
           }
-#pragma unroll
-          for (int j = 0; j < RR; ++j) {
-            if (!live[j]) continue;
-            float s, b;
-            sb_decode(sbv[j], A.s_dt, s, b);
-            const float s16 = 16.f * s, bb = b - s16;
-            float sg16 = 0.f, bbg = 0.f;
-            if (gated) {
-              float sg, bg;
-              sb_decode(sbg[j], A.s_dt, sg, bg);
-              sg16 = 16.f * sg; bbg = bg - sg16;
-            }
-#pragma unroll
-            for (int pp = 0; pp < PB; ++pp) {
-              if (pp < np) {
-                const float4* x8 = smem4 + pp * K4 + 8 * c;
-                const float xs = xsum[pp * nchunk + c];
-                acc[j][pp] = fmaf(s16, chunk_dot(w[j], x8, c), fmaf(bb, xs, acc[j][pp]));
-                if (gated)
-                  accg[j][pp] = fmaf(sg16, chunk_dot(wg[j], x8, c), fmaf(bbg, xs, accg[j][pp]));
-              }
-            }
-          }
         }
-        // warp reduce-scatter of all partial sums: value (j, pp, up|gate)
-        float v[NV];
 #pragma unroll
-        for (int j = 0; j < RR; ++j)
+        for (int j = 0; j < RR; ++j) {
+          if (!live[j]) continue;
+          float sc, bi;
+          sb_decode(sbv[j], A.s_dt, sc, bi);
+          const float s16 = 16.f * sc, bb = bi - s16;
+          float sg16 = 0.f, bbg = 0.f;
+          if (gated) {
+            float sg, bg;
+            sb_decode(sbg[j], A.s_dt, sg, bg);
+            sg16 = 16.f * sg; bbg = bg - sg16;
+          }
 #pragma unroll
           for (int pp = 0; pp < PB; ++pp) {
-            v[(j * PB + pp) * 2] = acc[j][pp];
-            v[(j * PB + pp) * 2 + 1] = accg[j][pp];
-          }
-        const float tot = warp_reduce_scatter<NV>(v, lane);
-        constexpr int LPV = 32 / NV;
-        const int vi = lane / LPV;
-        const float other = __shfl_down_sync(0xffffffffu, tot, LPV);   // gate partner
-        if ((lane & (2 * LPV - 1)) == 0) {
-          const int j = (vi >> 1) / PB, pp = (vi >> 1) % PB;
-          if (live[j] && pp < np) {
-            const int pid = pairs[pc + pp];
-            const float a = tot, gv = other;
-            const float val = (A.act >= 0) ? act_fn(A.act, gv, a) : a;
-            A.out[static_cast<int64_t>(pid) * A.n_rows + nn[j]] = val;
+            if (pp < np) {
+              const float4* x8 = smem4 + pp * K4 + 8 * c;
+              const float xs = xsum[pp * nchunk + c];
+              acc[j][pp] = fmaf(s16, chunk_dot(w[j], x8, c), fmaf(bb, xs, acc[j][pp]));
+              if (gated)
+                accg[j][pp] = fmaf(sg16, chunk_dot(wg[j], x8, c), fmaf(bbg, xs, accg[j][pp]));
+            }
           }
         }
       }
+      // warp reduce-scatter of all partial sums: value (j, pp, up|gate)
+      float v[NV];
+#pragma unroll
+      for (int j = 0; j < RR; ++j)
+#pragma unroll
+        for (int pp = 0; pp < PB; ++pp) {
+          v[(j * PB + pp) * 2] = acc[j][pp];
+          v[(j * PB + pp) * 2 + 1] = accg[j][pp];
+        }
+      const float tot = warp_reduce_scatter<NV>(v, lane);
+      constexpr int LPV = 32 / NV;
+      const int vi = lane / LPV;
+      const float other = __shfl_down_sync(0xffffffffu, tot, LPV);   // gate partner
+      if ((lane & (2 * LPV - 1)) == 0) {
+        const int j = (vi >> 1) / PB, pp = (vi >> 1) % PB;
+        if (live[j] && pp < np) {
+          const int pid = pairs[pc + pp];
+          const float val = (A.act >= 0) ? act_fn(A.act, other, tot) : tot;
+          A.out[static_cast<int64_t>(pid) * A.n_rows + nn[j]] = val;
+        }
+      }
     }
-    r0 = uend;
   }
 }
 

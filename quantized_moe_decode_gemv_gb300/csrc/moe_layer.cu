@@ -622,7 +622,6 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     // batch's rows; experts with more loop over slot groups (L2 re-reads)
     const int pb_up = std::min(pow2_at_least(T, h->expert_pb), expert_pb_cap(kin));
     const int pb_dn = std::min(pow2_at_least(T, h->expert_pb), expert_pb_cap(F));
-    const int grid_x = h->num_sms * 4;
     ExpertArgs up{};
     up.n_rows = F;
     up.K = kin;
@@ -645,8 +644,13 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     up.out = h->hbuf;
     up.pre_wait_phase = 0;
     up.prefetch = 0;
+    // CTAs per distinct-expert slot: about 4 resident CTAs per SM over all slots,
+    // at least 8 rows per CTA
+    const int target = h->num_sms * 4;
+    up.cps = std::max(1, std::min(std::max(1, F / 8), (target + h->umax - 1) / h->umax));
+    const int grid_up = h->umax * up.cps;
     mark(2);
-    if ((e = launch_expert(up, pb_up, grid_x, s, pdl)) != cudaSuccess) goto cuda_fail;
+    if ((e = launch_expert(up, pb_up, grid_up, s, pdl)) != cudaSuccess) goto cuda_fail;
     mark(3);
     ExpertArgs dn = up;
     dn.n_rows = kin;
@@ -661,7 +665,8 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     dn.out = h->pexp;
     dn.pre_wait_phase = 1;
     dn.prefetch = (h->prefetch >> 1) & 1;
-    if ((e = launch_expert(dn, pb_dn, grid_x, s, pdl)) != cudaSuccess) goto cuda_fail;
+    dn.cps = std::max(1, std::min(std::max(1, kin / 8), (target + h->umax - 1) / h->umax));
+    if ((e = launch_expert(dn, pb_dn, h->umax * dn.cps, s, pdl)) != cudaSuccess) goto cuda_fail;
   } else {
     UmmaArgs up{};
     up.experts = 1;
