@@ -243,40 +243,56 @@ static __device__ void route_block(const RouteArgs& A, int* smem) {
 
   for (int t = warp; t < A.T; t += nwarp) {
     const float* z = A.logits + static_cast<int64_t>(t) * A.r_in;
-    float key[32];
+    // 1. every lane keeps the best MAX_K of its keys (experts lane, lane + 32,
+    //    ...) in a list sorted best first; the insertion is branch-free and its
+    //    steps are independent of each other
+    float tk[MAX_K];
+    int ti[MAX_K];
+#pragma unroll
+    for (int s = 0; s < MAX_K; ++s) { tk[s] = -INFINITY; ti[s] = 0x7fffffff; }
     bool bad = false;
+    float zv[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const int e = lane + 32 * i;
-      float kv = -INFINITY;
+      zv[i] = (i < nper && e < E) ? __ldcg(z + e) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = lane + 32 * i;
       if (i < nper && e < E) {
-        const float zz = __ldcg(z + e);
-        kv = (A.router == ROUTER_SOFTMAX) ? zz : 1.0f / (1.0f + expf(-zz));
+        float kv = (A.router == ROUTER_SOFTMAX) ? zv[i] : 1.0f / (1.0f + expf(-zv[i]));
         if (A.router == ROUTER_SIGMOID && A.bias) kv += A.bias[e];
         if (!isfinite(kv)) { bad = true; kv = -INFINITY; }
+#pragma unroll
+        for (int s2 = MAX_K - 1; s2 > 0; --s2) {
+          const bool up = key_better(kv, e, tk[s2 - 1], ti[s2 - 1]);  // entry s2-1 moves down
+          const bool at = !up && key_better(kv, e, tk[s2], ti[s2]);   // the key lands at s2
+          tk[s2] = up ? tk[s2 - 1] : (at ? kv : tk[s2]);
+          ti[s2] = up ? ti[s2 - 1] : (at ? e : ti[s2]);
+        }
+        if (key_better(kv, e, tk[0], ti[0])) { tk[0] = kv; ti[0] = e; }
       }
-      key[i] = kv;
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(A.status, STATUS_NONFINITE);
-    uint32_t taken = 0;
+    // 2. k rounds of a warp argmax over the lanes' list heads; the winning
+    //    lane pops its head
     int my_id = -1;
     for (int j = 0; j < k; ++j) {
-      float bk = -INFINITY;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int e = lane + 32 * i;
-        if (i < nper && e < E && !((taken >> i) & 1u) && key_better(key[i], e, bk, bi)) {
-          bk = key[i]; bi = e;
-        }
-      }
+      float bk = tk[0];
+      int bi = ti[0];
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) {
         const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
         const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
         if (key_better(ok, oi, bk, bi)) { bk = ok; bi = oi; }
       }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (ti[0] == bi) {
+#pragma unroll
+        for (int s2 = 0; s2 < MAX_K - 1; ++s2) { tk[s2] = tk[s2 + 1]; ti[s2] = ti[s2 + 1]; }
+        tk[MAX_K - 1] = -INFINITY;
+        ti[MAX_K - 1] = 0x7fffffff;
+      }
       if (lane == j) my_id = bi;
     }
     // combine weights (lane j < k holds pick j)
@@ -404,7 +420,9 @@ static __device__ void route_block(const RouteArgs& A, int* smem) {
   }
 }
 
-static __global__ void __launch_bounds__(1024) k_route(const RouteArgs A) {
+constexpr int ROUTE_THREADS = 256;
+
+static __global__ void __launch_bounds__(ROUTE_THREADS) k_route(const RouteArgs A) {
   extern __shared__ int route_smem[];
   griddep_wait();
   griddep_launch();
@@ -480,101 +498,159 @@ struct DenseOutArgs {
   const float* staged;  // [T, K] fp32 staged vector computed once (k_combine), or null
 };
 
-// Streams the rows [r_begin, r_end) of the segments against xs (staged
-// [TB][K] swizzled fp32) and leaves per-(row, t) warp partials in red.
+// Rows of the dense weights per register batch: every thread keeps partial sums
+// for RB rows x TB token rows.
 template <int TB>
-__device__ __forceinline__ void dense_rows(const DenseSeg* segs, int nseg, int r_begin, int r_end,
-                                           const float4* xs4, int K4, float* red) {
+__host__ __device__ constexpr int dense_rb() { return TB <= 4 ? 4 : 2; }
+
+// One step of the dense streaming loop: rows [r, r + nb) of segment si, part
+// p, 16-byte chunks [cbase, cbase + MAXC * NT).
+struct DStep {
+  int r, nb, si, p, cbase;
+  bool valid;
+};
+
+__device__ __forceinline__ int dpart_chunks(const DensePart& P) {
+  return P.wk / (P.dt == DT_FP32 ? 4 : 8);
+}
+
+template <int RBN>
+__device__ __forceinline__ void dstep_first(const DenseSeg* segs, int r_begin, int r_end, DStep& st) {
+  st.si = 0; st.r = r_begin; st.p = 0; st.cbase = 0; st.nb = 0;
+  st.valid = r_begin < r_end;
+  if (st.valid) {
+    while (st.r >= segs[st.si].row0 + segs[st.si].rows) ++st.si;
+    st.nb = min(RBN, min(r_end, segs[st.si].row0 + segs[st.si].rows) - st.r);
+  }
+}
+
+template <int RBN>
+__device__ __forceinline__ void dstep_next(const DenseSeg* segs, int r_end, DStep& st) {
+  st.cbase += MAXC * NT;
+  if (st.cbase < dpart_chunks(segs[st.si].part[st.p])) return;
+  st.cbase = 0;
+  if (++st.p < segs[st.si].nparts) return;
+  st.p = 0;
+  st.r += st.nb;
+  if (st.r >= r_end) { st.valid = false; return; }
+  while (st.r >= segs[st.si].row0 + segs[st.si].rows) ++st.si;
+  st.nb = min(RBN, min(r_end, segs[st.si].row0 + segs[st.si].rows) - st.r);
+}
+
+template <int RBN>
+__device__ __forceinline__ void dstep_load(const DenseSeg* segs, const DStep& st, uint4 (&wv)[RBN][MAXC]) {
+  const DensePart& P = segs[st.si].part[st.p];
+  const int esz = P.dt == DT_FP32 ? 4 : 2;
+  const int nch = dpart_chunks(P);
+  const int64_t rstride = static_cast<int64_t>(P.wk) * esz;
+  const char* wbase = static_cast<const char*>(P.w) + static_cast<int64_t>(st.r - segs[st.si].row0) * rstride;
+#pragma unroll
+  for (int i = 0; i < RBN; ++i)
+#pragma unroll
+    for (int c = 0; c < MAXC; ++c) {
+      const int ci = st.cbase + c * NT + static_cast<int>(threadIdx.x);
+      if (i < st.nb && ci < nch)
+        wv[i][c] = ldg_stream(wbase + i * rstride + static_cast<int64_t>(ci) * 16);
+      else
+        wv[i][c] = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// Streams the rows [r_begin, r_end) of the segments against xs (staged
+// [TB][K] swizzled fp32) and leaves per-(row, t) warp partials in red.  The
+// loads of step s + 1 are issued before step s is computed (two register
+// buffers), so every warp keeps its next batch of weights in flight.
+// `stage` is called once after the first loads are issued (it stages xs and
+// ends with a barrier), so the first memory latency overlaps the staging.
+template <int TB, typename StageFn>
+__device__ __forceinline__ void dense_rows(const DenseSeg* segs, int r_begin, int r_end,
+                                           const float4* xs4, int K4, float* red, StageFn stage) {
+  constexpr int RBN = dense_rb<TB>();
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  int si = 0;
-  for (int r = r_begin; r < r_end;) {
-    while (r >= segs[si].row0 + segs[si].rows) ++si;
-    const DenseSeg& S = segs[si];
-    const int nb = min(RB, min(r_end, S.row0 + S.rows) - r);
-    float acc[RB][TB];
+  DStep cur;
+  dstep_first<RBN>(segs, r_begin, r_end, cur);
+  uint4 wcur[RBN][MAXC];
+  if (cur.valid) dstep_load<RBN>(segs, cur, wcur);
+  stage();
+  float acc[RBN][TB];
 #pragma unroll
-    for (int i = 0; i < RB; ++i)
+  for (int i = 0; i < RBN; ++i)
 #pragma unroll
-      for (int t = 0; t < TB; ++t) acc[i][t] = 0.0f;
-
-    for (int p = 0; p < S.nparts; ++p) {
-      const DensePart P = S.part[p];
-      const int epc = (P.dt == DT_FP32) ? 4 : 8;         // elements per 16-byte chunk
-      const int nch = P.wk / epc;
-      const char* wbase = static_cast<const char*>(P.w) +
-                          (static_cast<int64_t>(r - S.row0) * P.wk) * (P.dt == DT_FP32 ? 4 : 2);
-      const int64_t rstride = static_cast<int64_t>(P.wk) * (P.dt == DT_FP32 ? 4 : 2);
-      for (int cbase = 0; cbase < nch; cbase += MAXC * NT) {
-        uint4 wv[RB][MAXC];
+    for (int t = 0; t < TB; ++t) acc[i][t] = 0.0f;
+  while (cur.valid) {
+    DStep nxt = cur;
+    dstep_next<RBN>(segs, r_end, nxt);
+    uint4 wnxt[RBN][MAXC];
+    if (nxt.valid) dstep_load<RBN>(segs, nxt, wnxt);
+    // compute the current step
+    {
+      const DensePart& P = segs[cur.si].part[cur.p];
+      const int nch = dpart_chunks(P);
 #pragma unroll
-        for (int i = 0; i < RB; ++i)
+      for (int c = 0; c < MAXC; ++c) {
+        const int ci = cur.cbase + c * NT + tid;
+        if (ci >= nch) continue;
+        if (P.dt != DT_FP32) {
+          const int f4 = (P.k0 >> 2) + 2 * ci;
+          const int s0 = swz(f4, 1), s1 = swz(f4 + 1, 1);
 #pragma unroll
-          for (int c = 0; c < MAXC; ++c) {
-            const int ci = cbase + c * NT + tid;
-            if (i < nb && ci < nch)
-              wv[i][c] = ldg_stream(wbase + i * rstride + static_cast<int64_t>(ci) * 16);
-            else
-              wv[i][c] = make_uint4(0u, 0u, 0u, 0u);
-          }
+          for (int i = 0; i < RBN; ++i) {
+            if (i >= cur.nb) continue;
+            float wf[8];
+            cvt8(wcur[i][c], P.dt, wf);
 #pragma unroll
-        for (int c = 0; c < MAXC; ++c) {
-          const int ci = cbase + c * NT + tid;
-          if (ci >= nch) continue;
-          if (epc == 8) {
-            const int f4 = (P.k0 >> 2) + 2 * ci;
-            const int s0 = swz(f4, 1), s1 = swz(f4 + 1, 1);
-#pragma unroll
-            for (int i = 0; i < RB; ++i) {
-              if (i >= nb) continue;
-              float wf[8];
-              cvt8(wv[i][c], P.dt, wf);
-#pragma unroll
-              for (int t = 0; t < TB; ++t) {
-                const float4 a = xs4[t * K4 + s0];
-                const float4 b = xs4[t * K4 + s1];
-                float s = acc[i][t];
-                s = fmaf(wf[0], a.x, s); s = fmaf(wf[1], a.y, s);
-                s = fmaf(wf[2], a.z, s); s = fmaf(wf[3], a.w, s);
-                s = fmaf(wf[4], b.x, s); s = fmaf(wf[5], b.y, s);
-                s = fmaf(wf[6], b.z, s); s = fmaf(wf[7], b.w, s);
-                acc[i][t] = s;
-              }
+            for (int t = 0; t < TB; ++t) {
+              const float4 a = xs4[t * K4 + s0];
+              const float4 b = xs4[t * K4 + s1];
+              float sacc = acc[i][t];
+              sacc = fmaf(wf[0], a.x, sacc); sacc = fmaf(wf[1], a.y, sacc);
+              sacc = fmaf(wf[2], a.z, sacc); sacc = fmaf(wf[3], a.w, sacc);
+              sacc = fmaf(wf[4], b.x, sacc); sacc = fmaf(wf[5], b.y, sacc);
+              sacc = fmaf(wf[6], b.z, sacc); sacc = fmaf(wf[7], b.w, sacc);
+              acc[i][t] = sacc;
             }
-          } else {
-            const int s0 = swz((P.k0 >> 2) + ci, 1);
+          }
+        } else {
+          const int s0 = swz((P.k0 >> 2) + ci, 1);
 #pragma unroll
-            for (int i = 0; i < RB; ++i) {
-              if (i >= nb) continue;
-              const uint4 v = wv[i][c];
+          for (int i = 0; i < RBN; ++i) {
+            if (i >= cur.nb) continue;
+            const uint4 v = wcur[i][c];
 #pragma unroll
-              for (int t = 0; t < TB; ++t) {
-                const float4 a = xs4[t * K4 + s0];
-                float s = acc[i][t];
-                s = fmaf(__uint_as_float(v.x), a.x, s); s = fmaf(__uint_as_float(v.y), a.y, s);
-                s = fmaf(__uint_as_float(v.z), a.z, s); s = fmaf(__uint_as_float(v.w), a.w, s);
-                acc[i][t] = s;
-              }
+            for (int t = 0; t < TB; ++t) {
+              const float4 a = xs4[t * K4 + s0];
+              float sacc = acc[i][t];
+              sacc = fmaf(__uint_as_float(v.x), a.x, sacc); sacc = fmaf(__uint_as_float(v.y), a.y, sacc);
+              sacc = fmaf(__uint_as_float(v.z), a.z, sacc); sacc = fmaf(__uint_as_float(v.w), a.w, sacc);
+              acc[i][t] = sacc;
             }
           }
         }
       }
     }
-    // warp reduce-scatter of RB*TB values, then one partial per warp to smem
-    constexpr int NV = RB * TB;
-    float v[NV];
+    if (!nxt.valid || nxt.r != cur.r) {
+      // the rows of this batch are complete: warp reduce-scatter, one partial
+      // per warp to shared memory
+      constexpr int NV = RBN * TB;
+      float v[NV];
 #pragma unroll
-    for (int i = 0; i < RB; ++i)
+      for (int i = 0; i < RBN; ++i)
 #pragma unroll
-      for (int t = 0; t < TB; ++t) v[i * TB + t] = acc[i][t];
-    const float tot = warp_reduce_scatter<NV>(v, lane);
-    constexpr int LPV = 32 / NV;  // lanes per value
-    if ((lane & (LPV - 1)) == 0) {
-      const int vi = lane / LPV;
-      const int i = vi / TB, t = vi % TB;
-      if (i < nb) red[((r - r_begin + i) * TB + t) * NW + warp] = tot;
+        for (int t = 0; t < TB; ++t) { v[i * TB + t] = acc[i][t]; acc[i][t] = 0.0f; }
+      const float tot = warp_reduce_scatter<NV>(v, lane);
+      constexpr int LPV = 32 / NV;  // lanes per value
+      if ((lane & (LPV - 1)) == 0) {
+        const int vi = lane / LPV;
+        const int i = vi / TB, t = vi % TB;
+        if (i < cur.nb) red[((cur.r - r_begin + i) * TB + t) * NW + warp] = tot;
+      }
     }
-    r += nb;
+    cur = nxt;
+#pragma unroll
+    for (int i = 0; i < RBN; ++i)
+#pragma unroll
+      for (int c = 0; c < MAXC; ++c) wcur[i][c] = wnxt[i][c];
   }
 }
 
@@ -605,7 +681,7 @@ __device__ __forceinline__ void cta_rows(int rows, int& b, int& e) {
 // CTAs per SM the dense kernels are compiled for: more resident warps keep
 // more weight loads in flight while other warps reduce.
 template <int TB>
-constexpr int dense_min_blocks() { return TB <= 2 ? 4 : 2; }
+constexpr int dense_min_blocks() { return 2; }
 
 template <int TB>
 __global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_in(const DenseInArgs A) {
@@ -620,11 +696,13 @@ __global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_in(const D
   for (int t0 = 0; t0 < A.T; t0 += TB) {
     const int tb = min(TB, A.T - t0);
     if (t0) __syncthreads();
-    stage_x<TB>(xs, A.x, A.x_dt, A.K, t0, tb);
-    __syncthreads();
     for (int r0 = rb; r0 < re; r0 += RED_ROWS) {
       const int r1 = min(re, r0 + RED_ROWS);
-      dense_rows<TB>(A.seg, A.nseg, r0, r1, smem4, K4, red);
+      const bool first = r0 == rb;
+      dense_rows<TB>(A.seg, r0, r1, smem4, K4, red, [&]() {
+        if (first) stage_x<TB>(xs, A.x, A.x_dt, A.K, t0, tb);
+        __syncthreads();
+      });
       __syncthreads();
       for (int o = threadIdx.x; o < (r1 - r0) * TB; o += NT) {
         const int rl = o / TB, t = o % TB;
@@ -692,38 +770,43 @@ __global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_out(const 
     const int tb = min(TB, A.T - t0);
     if (t0) __syncthreads();
     // staged vector: [combined routed output y (latent only) | shared activation]
-    for (int i = threadIdx.x; i < TB * K4; i += NT) {
-      const int t = i / K4, f4 = i - t * K4;
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-      if (t < tb && A.staged) {
-        const float4 a = reinterpret_cast<const float4*>(A.staged)[static_cast<int64_t>(t0 + t) * K4 + f4];
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-      } else if (t < tb) {
-        const int tt = t0 + t;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int kk = 4 * f4 + j;
-          if (kk < L) {
-            float y = 0.f;
-            for (int p = 0; p < A.k; ++p)
-              y = fmaf(A.wts[tt * A.k + p],
-                       A.pexp[static_cast<int64_t>(tt * A.k + p) * Kin + kk], y);
-            v[j] = y;
-          } else {
-            const int f = kk - L;
-            const float* di = A.dense_in + static_cast<int64_t>(tt) * A.r_in;
-            const float u = di[A.sh_u_off + f];
-            const float g = (A.act == ACT_SWIGLU) ? di[A.sh_g_off + f] : 0.f;
-            v[j] = act_fn(A.act, g, u);
+    auto stage_body = [&]() {
+      for (int i = threadIdx.x; i < TB * K4; i += NT) {
+        const int t = i / K4, f4 = i - t * K4;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (t < tb && A.staged) {
+          const float4 a = reinterpret_cast<const float4*>(A.staged)[static_cast<int64_t>(t0 + t) * K4 + f4];
+          v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        } else if (t < tb) {
+          const int tt = t0 + t;
+  #pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int kk = 4 * f4 + j;
+            if (kk < L) {
+              float y = 0.f;
+              for (int p = 0; p < A.k; ++p)
+                y = fmaf(A.wts[tt * A.k + p],
+                         A.pexp[static_cast<int64_t>(tt * A.k + p) * Kin + kk], y);
+              v[j] = y;
+            } else {
+              const int f = kk - L;
+              const float* di = A.dense_in + static_cast<int64_t>(tt) * A.r_in;
+              const float u = di[A.sh_u_off + f];
+              const float g = (A.act == ACT_SWIGLU) ? di[A.sh_g_off + f] : 0.f;
+              v[j] = act_fn(A.act, g, u);
+            }
           }
         }
+        smem4[t * K4 + swz(f4, 1)] = make_float4(v[0], v[1], v[2], v[3]);
       }
-      smem4[t * K4 + swz(f4, 1)] = make_float4(v[0], v[1], v[2], v[3]);
-    }
-    __syncthreads();
+    };
     for (int r0 = rb; r0 < re; r0 += RED_ROWS) {
       const int r1 = min(re, r0 + RED_ROWS);
-      if (A.nseg) dense_rows<TB>(A.seg, A.nseg, r0, r1, smem4, K4, red);
+      const bool first = r0 == rb;
+      if (A.nseg) dense_rows<TB>(A.seg, r0, r1, smem4, K4, red, [&]() {
+        if (first) stage_body();
+        __syncthreads();
+      });
       __syncthreads();
       for (int o = threadIdx.x; o < (r1 - r0) * TB; o += NT) {
         const int rl = o / TB, t = o % TB;

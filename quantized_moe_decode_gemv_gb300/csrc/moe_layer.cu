@@ -555,7 +555,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
       di.out = h->dense_in;
       di.T = T;
       const int tb_in = std::min(pow2_at_least(T, 8), dense_tb_cap(H));
-      const int grid_in = std::max(1, std::min(h->num_sms * (tb_in <= 2 ? 4 : 2), (di.total_rows + 3) / 4));
+      const int grid_in = std::max(1, std::min(h->num_sms * 2, (di.total_rows + 3) / 4));
       if (fuse_route) {
         di.fuse_route = 1;
         di.route = ra;
@@ -610,7 +610,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
   // 2. routing (fused into the dense pass on the gemv path)
   mark(1);
   if (!fuse_route) {
-    if ((e = launch_ex<RouteArgs>(k_route, 1, MAX_E,
+    if ((e = launch_ex<RouteArgs>(k_route, 1, ROUTE_THREADS,
                                   ROUTE_SMEM_BYTES + static_cast<size_t>(E) * ra.mask_words * 4, s,
                                   pdl, ra)) != cudaSuccess)
       goto cuda_fail;
@@ -646,9 +646,11 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     up.prefetch = 0;
     // CTAs per distinct-expert slot: about 4 resident CTAs per SM over all slots,
     // at least 8 rows per CTA
+    // slots: at most min(E, T*k) distinct experts in this call
+    const int slots = std::min(E, T * k);
     const int target = h->num_sms * 4;
-    up.cps = std::max(1, std::min(std::max(1, F / 8), (target + h->umax - 1) / h->umax));
-    const int grid_up = h->umax * up.cps;
+    up.cps = std::max(1, std::min(std::max(1, F / 8), (target + slots - 1) / slots));
+    const int grid_up = slots * up.cps;
     mark(2);
     if ((e = launch_expert(up, pb_up, grid_up, s, pdl)) != cudaSuccess) goto cuda_fail;
     mark(3);
@@ -665,8 +667,8 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     dn.out = h->pexp;
     dn.pre_wait_phase = 1;
     dn.prefetch = (h->prefetch >> 1) & 1;
-    dn.cps = std::max(1, std::min(std::max(1, kin / 8), (target + h->umax - 1) / h->umax));
-    if ((e = launch_expert(dn, pb_dn, h->umax * dn.cps, s, pdl)) != cudaSuccess) goto cuda_fail;
+    dn.cps = std::max(1, std::min(std::max(1, kin / 8), (target + slots - 1) / slots));
+    if ((e = launch_expert(dn, pb_dn, slots * dn.cps, s, pdl)) != cudaSuccess) goto cuda_fail;
   } else {
     UmmaArgs up{};
     up.experts = 1;
@@ -785,7 +787,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
       dout.staged = h->comb;
     }
     const int tb_out = kout ? std::min(pow2_at_least(T, 8), dense_tb_cap(kout)) : pow2_at_least(T, 8);
-    const int grid_out = std::max(1, std::min(h->num_sms * (tb_out <= 2 ? 4 : 2), (H + 3) / 4));
+    const int grid_out = std::max(1, std::min(h->num_sms * 2, (H + 3) / 4));
     if ((e = launch_dense_out(dout, tb_out, grid_out, s, pdl)) != cudaSuccess) goto cuda_fail;
   }
   mark(5);
