@@ -215,7 +215,14 @@ struct RouteArgs {
   int* status;
   int mask_words;        // > 0: rank pairs with per-expert row bitmasks of this many
                          // words in dynamic shared memory (E * mask_words words)
+  int debug_times;       // print per-phase timestamps (diagnostics only)
 };
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ bool key_better(float a, int ia, float b, int ib) {
   return a > b || (a == b && ia < ib);
@@ -240,63 +247,76 @@ static __device__ void route_block(const RouteArgs& A, int* smem) {
   const int nthr = blockDim.x;
   const int E = A.E, k = A.k;
   const int nper = (E + 31) >> 5;
+  unsigned long long tp[8];
+  if (A.debug_times) tp[0] = global_ns();
 
   for (int t = warp; t < A.T; t += nwarp) {
     const float* z = A.logits + static_cast<int64_t>(t) * A.r_in;
     // 1. every lane keeps the best MAX_K of its keys (experts lane, lane + 32,
     //    ...) in a list sorted best first; the insertion is branch-free and its
     //    steps are independent of each other
-    float tk[MAX_K];
+    float tk[MAX_K], tz[MAX_K];
     int ti[MAX_K];
 #pragma unroll
-    for (int s = 0; s < MAX_K; ++s) { tk[s] = -INFINITY; ti[s] = 0x7fffffff; }
+    for (int s = 0; s < MAX_K; ++s) { tk[s] = -INFINITY; tz[s] = 0.f; ti[s] = 0x7fffffff; }
     bool bad = false;
-    float zv[32];
+    // loads first (logits and selection bias, 16 experts at a time), so none
+    // of them sits in the serial insertion chain below
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int e = lane + 32 * i;
-      zv[i] = (i < nper && e < E) ? __ldcg(z + e) : 0.f;
-    }
+    for (int hlf = 0; hlf < 2; ++hlf) {
+      if (hlf * 16 >= nper) break;
+      float zv[16], bv[16];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int e = lane + 32 * i;
-      if (i < nper && e < E) {
-        float kv = (A.router == ROUTER_SOFTMAX) ? zv[i] : 1.0f / (1.0f + expf(-zv[i]));
-        if (A.router == ROUTER_SIGMOID && A.bias) kv += A.bias[e];
-        if (!isfinite(kv)) { bad = true; kv = -INFINITY; }
+      for (int i = 0; i < 16; ++i) {
+        const int e = lane + 32 * (16 * hlf + i);
+        const bool ok = 16 * hlf + i < nper && e < E;
+        zv[i] = ok ? __ldcg(z + e) : 0.f;
+        bv[i] = (ok && A.bias) ? __ldg(A.bias + e) : 0.f;
+      }
 #pragma unroll
-        for (int s2 = MAX_K - 1; s2 > 0; --s2) {
-          const bool up = key_better(kv, e, tk[s2 - 1], ti[s2 - 1]);  // entry s2-1 moves down
-          const bool at = !up && key_better(kv, e, tk[s2], ti[s2]);   // the key lands at s2
-          tk[s2] = up ? tk[s2 - 1] : (at ? kv : tk[s2]);
-          ti[s2] = up ? ti[s2 - 1] : (at ? e : ti[s2]);
+      for (int i = 0; i < 16; ++i) {
+        const int e = lane + 32 * (16 * hlf + i);
+        if (16 * hlf + i < nper && e < E) {
+          float kv = (A.router == ROUTER_SOFTMAX) ? zv[i] : 1.0f / (1.0f + expf(-zv[i])) + bv[i];
+          if (!isfinite(kv)) { bad = true; kv = -INFINITY; }
+          const float zz = zv[i];
+#pragma unroll
+          for (int s2 = MAX_K - 1; s2 > 0; --s2) {
+            const bool up = key_better(kv, e, tk[s2 - 1], ti[s2 - 1]);  // entry s2-1 moves down
+            const bool at = !up && key_better(kv, e, tk[s2], ti[s2]);   // the key lands at s2
+            tk[s2] = up ? tk[s2 - 1] : (at ? kv : tk[s2]);
+            tz[s2] = up ? tz[s2 - 1] : (at ? zz : tz[s2]);
+            ti[s2] = up ? ti[s2 - 1] : (at ? e : ti[s2]);
+          }
+          if (key_better(kv, e, tk[0], ti[0])) { tk[0] = kv; tz[0] = zz; ti[0] = e; }
         }
-        if (key_better(kv, e, tk[0], ti[0])) { tk[0] = kv; ti[0] = e; }
       }
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(A.status, STATUS_NONFINITE);
     // 2. k rounds of a warp argmax over the lanes' list heads; the winning
-    //    lane pops its head
+    //    lane pops its head.  The winner's logit travels with it.
     int my_id = -1;
+    float my_z = 0.f;
     for (int j = 0; j < k; ++j) {
-      float bk = tk[0];
+      float bk = tk[0], bz = tz[0];
       int bi = ti[0];
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) {
         const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+        const float oz = __shfl_xor_sync(0xffffffffu, bz, o);
         const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (key_better(ok, oi, bk, bi)) { bk = ok; bi = oi; }
+        if (key_better(ok, oi, bk, bi)) { bk = ok; bi = oi; bz = oz; }
       }
       if (ti[0] == bi) {
 #pragma unroll
-        for (int s2 = 0; s2 < MAX_K - 1; ++s2) { tk[s2] = tk[s2 + 1]; ti[s2] = ti[s2 + 1]; }
+        for (int s2 = 0; s2 < MAX_K - 1; ++s2) { tk[s2] = tk[s2 + 1]; tz[s2] = tz[s2 + 1]; ti[s2] = ti[s2 + 1]; }
         tk[MAX_K - 1] = -INFINITY;
         ti[MAX_K - 1] = 0x7fffffff;
       }
-      if (lane == j) my_id = bi;
+      if (lane == j) { my_id = bi; my_z = bz; }
     }
     // combine weights (lane j < k holds pick j)
-    const float zj = (lane < k) ? __ldcg(z + my_id) : 0.f;
+    const float zj = (lane < k) ? my_z : 0.f;
     float wv = 0.f;
     if (A.router == ROUTER_SOFTMAX) {
       const float m = __shfl_sync(0xffffffffu, zj, 0);   // largest selected logit
@@ -336,11 +356,14 @@ static __device__ void route_block(const RouteArgs& A, int* smem) {
     }
   }
   // ---- distinct experts and their pairs ----
+  if (A.debug_times) tp[1] = global_ns();
   for (int e = tid; e < MAX_E; e += nthr) s_cnt[e] = 0;
   __syncthreads();
+  if (A.debug_times) tp[2] = global_ns();
   const int P = A.T * k;
   for (int p = tid; p < P; p += nthr) atomicAdd(&s_cnt[A.ids[p]], 1);
   __syncthreads();
+  if (A.debug_times) tp[3] = global_ns();
   // exclusive scans over experts of (cnt > 0) and cnt; thread tid owns the
   // experts [tid * ept, (tid + 1) * ept)
   {
@@ -391,6 +414,7 @@ static __device__ void route_block(const RouteArgs& A, int* smem) {
     }
   }
   __syncthreads();
+  if (A.debug_times) tp[4] = global_ns();
   int* pairs = A.meta + 2 + 2 * A.umax;
   if (A.mask_words > 0) {
     // rank of pair (t, j) among its expert's pairs = rows t' < t that chose
@@ -418,15 +442,25 @@ static __device__ void route_block(const RouteArgs& A, int* smem) {
       pairs[s_scan_c[e] + rank] = p;
     }
   }
+  if (A.debug_times && tid == 0) {
+    tp[5] = global_ns();
+    printf("route phases (ns): topk %llu zero %llu count %llu scan %llu pairs %llu\n",
+           tp[1] - tp[0], tp[2] - tp[1], tp[3] - tp[2], tp[4] - tp[3], tp[5] - tp[4]);
+  }
 }
 
 constexpr int ROUTE_THREADS = 256;
 
 static __global__ void __launch_bounds__(ROUTE_THREADS) k_route(const RouteArgs A) {
   extern __shared__ int route_smem[];
+  unsigned long long t0 = 0, t1 = 0;
+  if (A.debug_times) t0 = global_ns();
   griddep_wait();
+  if (A.debug_times) t1 = global_ns();
   griddep_launch();
   route_block(A, route_smem);
+  if (A.debug_times && threadIdx.x == 0)
+    printf("route kernel: wait %llu ns, total %llu ns\n", t1 - t0, global_ns() - t0);
 }
 
 // ---------------------------------------------------------------------------

@@ -80,6 +80,7 @@ struct moe_layer {
   int use_pdl = 1;        // programmatic dependent launch between the gemv-path kernels
   int expert_pb = 2;      // max token slots per pass of the gemv-path expert kernels
   int fuse_route = 1;     // routing in the last router CTA of the dense pass (0: own kernel)
+  int debug_route = 0;    // diagnostics: print routing phase times
   int prefetch = 6;       // bit 0: experts' up weights from the routing CTA (one SM's
                           // bulk engine: slow, off by default); bit 1: down weights;
                           // bit 2: output-projection weights
@@ -370,6 +371,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   if (const char* env = std::getenv("MOE_PREFETCH")) L->prefetch = std::atoi(env);
   if (const char* env = std::getenv("MOE_EXPERT_PB")) L->expert_pb = std::max(1, std::min(8, std::atoi(env)));
   if (const char* env = std::getenv("MOE_FUSE_ROUTE")) L->fuse_route = std::atoi(env) != 0;
+  if (const char* env = std::getenv("MOE_DEBUG_ROUTE")) L->debug_route = std::atoi(env) != 0;
   {
     const size_t adt = dt_size(c.act_dtype), rdt = dt_size(c.router_dtype);
     const size_t sdt = dt_size(c.scale_dtype);
@@ -523,6 +525,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
   ra.ext_ids = ext_ids;
   ra.ext_w = ext_w;
   ra.status = h->status;
+  ra.debug_times = h->debug_route;
   {
     const int P = T * k;
     const int W = (T + 31) / 32;
