@@ -252,70 +252,81 @@ static __device__ void route_block(const RouteArgs& A, int* smem) {
 
   for (int t = warp; t < A.T; t += nwarp) {
     const float* z = A.logits + static_cast<int64_t>(t) * A.r_in;
-    // 1. every lane keeps the best MAX_K of its keys (experts lane, lane + 32,
-    //    ...) in a list sorted best first; the insertion is branch-free and its
-    //    steps are independent of each other
-    float tk[MAX_K], tz[MAX_K];
-    int ti[MAX_K];
-#pragma unroll
-    for (int s = 0; s < MAX_K; ++s) { tk[s] = -INFINITY; tz[s] = 0.f; ti[s] = 0x7fffffff; }
+    // 1. load every key of the lane (experts lane, lane + 32, ...), all loads
+    //    first so none waits inside the selection below
+    float kv[32], sv[32];
     bool bad = false;
-    // loads first (logits and selection bias, 16 experts at a time), so none
-    // of them sits in the serial insertion chain below
 #pragma unroll
-    for (int hlf = 0; hlf < 2; ++hlf) {
-      if (hlf * 16 >= nper) break;
-      float zv[16], bv[16];
+    for (int i = 0; i < 32; ++i) {
+      const int e = lane + 32 * i;
+      const bool ok = i < nper && e < E;
+      sv[i] = ok ? __ldcg(z + e) : 0.f;
+      kv[i] = (ok && A.bias) ? __ldg(A.bias + e) : 0.f;
+    }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int e = lane + 32 * (16 * hlf + i);
-        const bool ok = 16 * hlf + i < nper && e < E;
-        zv[i] = ok ? __ldcg(z + e) : 0.f;
-        bv[i] = (ok && A.bias) ? __ldg(A.bias + e) : 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int e = lane + 32 * (16 * hlf + i);
-        if (16 * hlf + i < nper && e < E) {
-          float kv = (A.router == ROUTER_SOFTMAX) ? zv[i] : 1.0f / (1.0f + expf(-zv[i])) + bv[i];
-          if (!isfinite(kv)) { bad = true; kv = -INFINITY; }
-          const float zz = zv[i];
-#pragma unroll
-          for (int s2 = MAX_K - 1; s2 > 0; --s2) {
-            const bool up = key_better(kv, e, tk[s2 - 1], ti[s2 - 1]);  // entry s2-1 moves down
-            const bool at = !up && key_better(kv, e, tk[s2], ti[s2]);   // the key lands at s2
-            tk[s2] = up ? tk[s2 - 1] : (at ? kv : tk[s2]);
-            tz[s2] = up ? tz[s2 - 1] : (at ? zz : tz[s2]);
-            ti[s2] = up ? ti[s2 - 1] : (at ? e : ti[s2]);
-          }
-          if (key_better(kv, e, tk[0], ti[0])) { tk[0] = kv; tz[0] = zz; ti[0] = e; }
+    for (int i = 0; i < 32; ++i) {
+      const int e = lane + 32 * i;
+      if (i < nper && e < E) {
+        const float zz = sv[i];
+        float key;
+        if (A.router == ROUTER_SOFTMAX) {
+          key = zz;
+          sv[i] = zz;                         // softmax weights use the logit
+        } else {
+          const float sg = 1.0f / (1.0f + expf(-zz));
+          key = sg + kv[i];                   // selection key: score + bias
+          sv[i] = sg;                         // weight: score without bias
         }
+        if (!isfinite(key)) { bad = true; key = -INFINITY; }
+        kv[i] = key;
+      } else {
+        kv[i] = -INFINITY;
       }
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(A.status, STATUS_NONFINITE);
-    // 2. k rounds of a warp argmax over the lanes' list heads; the winning
-    //    lane pops its head.  The winner's logit travels with it.
+    // 2. k rounds: the lane's best remaining key by a pairwise tree, then a warp
+    //    argmax by butterfly; the owner lane retires that key
     int my_id = -1;
     float my_z = 0.f;
     for (int j = 0; j < k; ++j) {
-      float bk = tk[0], bz = tz[0];
-      int bi = ti[0];
+      float tkv[16];
+      int tix[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int e0 = lane + 32 * i, e1 = lane + 32 * (i + 16);
+        const bool b1 = (i + 16 < nper) && key_better(kv[i + 16], e1, kv[i], e0);
+        tkv[i] = b1 ? kv[i + 16] : kv[i];
+        tix[i] = (i < nper) ? (b1 ? e1 : e0) : 0x7fffffff;
+      }
+#pragma unroll
+      for (int w = 8; w >= 1; w >>= 1) {
+#pragma unroll
+        for (int i = 0; i < w; ++i) {
+          const bool b1 = key_better(tkv[i + w], tix[i + w], tkv[i], tix[i]);
+          tkv[i] = b1 ? tkv[i + w] : tkv[i];
+          tix[i] = b1 ? tix[i + w] : tix[i];
+        }
+      }
+      float bk = tkv[0];
+      int bi = tix[0];
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) {
         const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-        const float oz = __shfl_xor_sync(0xffffffffu, bz, o);
         const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (key_better(ok, oi, bk, bi)) { bk = ok; bi = oi; bz = oz; }
+        if (key_better(ok, oi, bk, bi)) { bk = ok; bi = oi; }
       }
-      if (ti[0] == bi) {
+      // the owner lane publishes the winner's weight input and retires the key
+      const int owner = bi & 31, slot = bi >> 5;
+      float wsel = 0.f;
 #pragma unroll
-        for (int s2 = 0; s2 < MAX_K - 1; ++s2) { tk[s2] = tk[s2 + 1]; tz[s2] = tz[s2 + 1]; ti[s2] = ti[s2 + 1]; }
-        tk[MAX_K - 1] = -INFINITY;
-        ti[MAX_K - 1] = 0x7fffffff;
+      for (int i = 0; i < 32; ++i) {
+        if (lane == owner && i == slot) { wsel = sv[i]; kv[i] = -INFINITY; }
       }
-      if (lane == j) { my_id = bi; my_z = bz; }
+      wsel = __shfl_sync(0xffffffffu, wsel, owner);
+      if (lane == j) { my_id = bi; my_z = wsel; }
     }
-    // combine weights (lane j < k holds pick j)
+    // combine weights (lane j < k holds pick j; my_z is its logit for softmax
+    // routing and its sigmoid score for sigmoid routing)
     const float zj = (lane < k) ? my_z : 0.f;
     float wv = 0.f;
     if (A.router == ROUTER_SOFTMAX) {
@@ -338,7 +349,7 @@ static __device__ void route_block(const RouteArgs& A, int* smem) {
         wv = (lane < k) ? expf(zj - mm) / den : 0.f;
       }
     } else {
-      const float sg = (lane < k) ? 1.0f / (1.0f + expf(-zj)) : 0.f;
+      const float sg = zj;
       wv = sg;
       if (A.renorm) {
         float den = sg;

@@ -64,6 +64,8 @@ struct moe_layer {
   int* status = nullptr;
   int* route_counter = nullptr;
   float* comb = nullptr;      // [Tmax, L + F_sh] staged operand of the output projection
+  void* xl16 = nullptr;       // [Tmax, L] 16-bit latent rows (grouped path B operand)
+  void* h16 = nullptr;        // [Tmax*k, F] 16-bit expert activations (grouped path)
   void* bout = nullptr;       // [Tmax, L + F_sh] 16-bit operand of the grouped output GEMM
   void* x_stage = nullptr;    // [Tmax, H] act dtype (host-buffer forward)
   void* out_stage = nullptr;
@@ -443,6 +445,8 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     MOE_TRY_CUDA(cudaMemsetAsync(L->route_counter, 0, 4, s), "counter clear");
     MOE_TRY_CUDA(L->alloc(&L->bout, static_cast<size_t>(T) * (Lt + Fs + 64) * 2), "workspace");
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->comb), static_cast<size_t>(T) * (Lt + Fs + 64) * 4), "workspace");
+    MOE_TRY_CUDA(L->alloc(&L->xl16, static_cast<size_t>(T) * (Lt + 64) * 2), "workspace");
+    MOE_TRY_CUDA(L->alloc(&L->h16, P * F * 2), "workspace");
     MOE_TRY_CUDA(L->alloc(&L->x_stage, static_cast<size_t>(T) * H * adt), "workspace");
     MOE_TRY_CUDA(L->alloc(&L->out_stage, static_cast<size_t>(T) * H * adt), "workspace");
     MOE_TRY_CUDA(cudaStreamSynchronize(s), "create synchronise");
@@ -467,8 +471,21 @@ moe_status moe_layer_destroy(moe_layer* h) {
   return MOE_OK;
 }
 
-static cudaError_t launch_umma(const UmmaArgs& a, int grid, cudaStream_t s) {
-  k_umma<<<grid, UM_THREADS, umma_smem_bytes(), s>>>(a);
+// Tokens per MMA and ring depth for a grouped launch, and its shared memory.
+static size_t umma_config(UmmaArgs& a, int T) {
+  const bool gated = a.a_mode == UA_INT4 && a.q2 != nullptr;
+  const int cap = a.a_mode == UA_DENSE ? 256 : 64;
+  a.n_tile = std::min(cap, (std::max(1, T) + 15) & ~15);
+  const size_t budget = 220 * 1024;
+  int st = UM_MAX_STAGES;
+  while (st > 2 && umma_plan(a.a_mode, gated, a.n_tile, st).total > budget) --st;
+  a.stages = st;
+  return umma_plan(a.a_mode, gated, a.n_tile, st).total;
+}
+
+static cudaError_t launch_umma(UmmaArgs& a, int T, int grid, cudaStream_t s) {
+  const size_t smem = umma_config(a, T);
+  k_umma<<<grid, UM_THREADS, smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -597,7 +614,13 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
         ua.K = H;
         ua.a_mode = UA_DENSE;
         ua.mma_dt = mma_dt;
-        ua.b0 = x; ua.b0_dt = c.act_dtype; ua.b0_stride = H; ua.b0_off = 0; ua.b0_k = H;
+        ua.b0 = x; ua.b0_stride = H; ua.b0_off = 0;
+        if (Lt) {   // 16-bit copy of the latent columns: the experts' B operand
+          ua.out16 = static_cast<unsigned short*>(h->xl16);
+          ua.out16_ld = Lt;
+          ua.c16_0 = h->off_fc1;
+          ua.c16_1 = h->off_fc1 + Lt;
+        }
         ua.epi = UE_DENSE_IN;
         ua.act = -1;
         ua.out_f32 = h->dense_in;
@@ -605,7 +628,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
         ua.out_col0 = col0;
         ua.k = k;
         ua.status = h->status;
-        if ((e = launch_umma(ua, h->num_sms, s)) != cudaSuccess) goto cuda_fail;
+        if ((e = launch_umma(ua, T, h->num_sms, s)) != cudaSuccess) goto cuda_fail;
       }
     }
   }
@@ -688,11 +711,11 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     up.s_dt = c.scale_dtype;
     up.mma_dt = mma_dt;
     if (Lt) {
-      up.b0 = h->dense_in; up.b0_dt = DT_FP32; up.b0_stride = h->r_in; up.b0_off = h->off_fc1;
+      up.b0 = h->xl16; up.b0_stride = Lt; up.b0_off = 0;
     } else {
-      up.b0 = x; up.b0_dt = c.act_dtype; up.b0_stride = H; up.b0_off = 0;
+      up.b0 = x; up.b0_stride = H; up.b0_off = 0;
     }
-    up.b0_k = kin;
+    up.out16 = static_cast<unsigned short*>(h->h16);   // the down GEMM's B operand
     up.by_pair = 0;
     up.k = k;
     up.epi = UE_ROWS;
@@ -700,7 +723,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     up.out_f32 = h->hbuf;
     up.status = h->status;
     mark(2);
-    if ((e = launch_umma(up, h->num_sms, s)) != cudaSuccess) goto cuda_fail;
+    if ((e = launch_umma(up, T, h->num_sms, s)) != cudaSuccess) goto cuda_fail;
     mark(3);
     UmmaArgs dn = up;
     dn.n_rows = kin;
@@ -709,11 +732,12 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     dn.sb = h->down_sb;
     dn.q2 = nullptr;
     dn.sb2 = nullptr;
-    dn.b0 = h->hbuf; dn.b0_dt = DT_FP32; dn.b0_stride = F; dn.b0_off = 0; dn.b0_k = F;
+    dn.b0 = h->h16; dn.b0_stride = F; dn.b0_off = 0;
+    dn.out16 = nullptr;
     dn.by_pair = 1;
     dn.act = -1;
     dn.out_f32 = h->pexp;
-    if ((e = launch_umma(dn, h->num_sms, s)) != cudaSuccess) goto cuda_fail;
+    if ((e = launch_umma(dn, T, h->num_sms, s)) != cudaSuccess) goto cuda_fail;
   }
 
   // 5. combine + fc2 + shared down + residual
@@ -741,13 +765,13 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     ua.K = kout;
     ua.a_mode = UA_DENSE;
     ua.mma_dt = mma_dt;
-    ua.b0 = h->bout; ua.b0_dt = mma_dt; ua.b0_stride = kout; ua.b0_off = 0; ua.b0_k = kout;
+    ua.b0 = h->bout; ua.b0_stride = kout; ua.b0_off = 0;
     ua.k = k;
     ua.epi = UE_OUT;
     ua.x = x; ua.x_dt = c.act_dtype; ua.out = out; ua.delta = delta;
     ua.pexp = h->pexp; ua.wts = h->wts; ua.add_combine = Lt ? 0 : 1;
     ua.status = h->status;
-    if ((e = launch_umma(ua, h->num_sms, s)) != cudaSuccess) goto cuda_fail;
+    if ((e = launch_umma(ua, T, h->num_sms, s)) != cudaSuccess) goto cuda_fail;
   } else {
     DenseOutArgs dout{};
     dout.nseg = 0;

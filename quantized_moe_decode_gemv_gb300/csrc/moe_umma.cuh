@@ -10,16 +10,16 @@
 //     D[128 x N] = A[128 x K] . B[N x K]^T          (swap-AB: weights are M,
 //                                                    tokens are N)
 //
-// with A = weights (int4 affine codes dequantised to 16-bit in shared memory,
-// or 16-bit dense rows), B = the tokens' activations rounded to the same
-// 16-bit type, fp32 accumulation in tensor memory (TMEM), and an epilogue that
-// reads TMEM with tcgen05.ld.  One thread issues tcgen05.mma; operands are
-// staged by all threads into the K-major, no-swizzle canonical layout
-// (8-row x 16-byte core matrices) and handed to the tensor core through
-// shared-memory descriptors; completion is signalled with tcgen05.commit on an
-// mbarrier.  Two stage buffers let the staging of K-chunk c+1 overlap the MMAs
-// of chunk c.  Every mbarrier wait is bounded: after the bound the kernel sets
-// the timeout bit of the status word, frees its TMEM and returns.
+// with fp32 accumulation in tensor memory (TMEM) and an epilogue that reads
+// TMEM with tcgen05.ld.  A is either 16-bit dense rows or int4 affine codes,
+// which are dequantised to 16 bits in shared memory; B is the tokens' 16-bit
+// activations.  Both are moved by cp.async into a ring of `stages` shared-memory
+// slots in the K-major, no-swizzle canonical layout (8-row x 16-byte core
+// matrices), so several K-chunks are in flight while the tensor core works on
+// an earlier one.  One thread issues tcgen05.mma through shared-memory
+// descriptors and signals completion with tcgen05.commit on an mbarrier.  Every
+// mbarrier wait is bounded: after the bound the kernel sets the timeout bit of
+// the status word, frees its TMEM and returns.
 #pragma once
 
 #include "moe_kernels.cuh"
@@ -28,8 +28,8 @@ namespace moe {
 
 constexpr int UM_M = 128;       // weight rows per tile (MMA M)
 constexpr int UM_KC = 64;       // K elements per stage
-constexpr int UM_NMAX = 256;    // tokens per MMA (MMA N, multiple of 16)
 constexpr int UM_THREADS = 256;
+constexpr int UM_MAX_STAGES = 8;
 constexpr uint32_t UM_SPIN_LIMIT = 1u << 22;
 
 // canonical K-major no-swizzle layout of a [rows x 64] 16-bit tile:
@@ -37,8 +37,9 @@ constexpr uint32_t UM_SPIN_LIMIT = 1u << 22;
 // element (row % 8, k % 8) at (row % 8) * 16 + (k % 8) * 2 inside it.
 constexpr uint32_t UM_LBO = 128;    // between core matrices along K
 constexpr uint32_t UM_SBO = 1024;   // between 8-row groups along M / N
-constexpr int UM_A_BYTES = UM_M * UM_KC * 2;        // 16 KB
-constexpr int UM_B_BYTES = UM_NMAX * UM_KC * 2;     // 32 KB
+constexpr int UM_A_BYTES = UM_M * UM_KC * 2;        // 16 KB (a 16-bit A tile)
+constexpr int UM_CODE_BYTES = UM_M * UM_KC / 2;     // 4 KB (int4 codes of an A tile)
+constexpr int UM_SB_BYTES = UM_M * 8;               // 1 KB (<= 2 scale/bias words per row)
 
 enum : int { UA_INT4 = 0, UA_DENSE = 1 };                  // A source
 enum : int { UE_ROWS = 0, UE_DENSE_IN = 1, UE_OUT = 2 };   // epilogue
@@ -59,22 +60,28 @@ struct UmmaArgs {
   const uint32_t* sb2;
   int G;
   int s_dt;
-  DenseSeg seg[4];          // dense: row segments (parts concatenated along K)
+  DenseSeg seg[4];          // dense: row segments (16-bit parts concatenated along K)
   int nseg;
   int mma_dt;               // DT_BF16 or DT_FP16: the 16-bit type of A and B
-  // ---- B: token n's activation row ----
+  // ---- B: token n's activation row, 16-bit (mma_dt) ----
   // experts mode: pair p = pairs[p0 + n]; source row = by_pair ? p : p / k
   // dense mode: source row = n
-  const void* b0; int b0_dt; int64_t b0_stride; int64_t b0_off; int b0_k;   // columns [0, b0_k)
-  const void* b1; int b1_dt; int64_t b1_stride; int64_t b1_off;             // columns [b0_k, K)
+  const void* b0; int64_t b0_stride; int64_t b0_off;
   int by_pair;
   int k;                    // top_k
+  // ---- pipeline (host-chosen) ----
+  int n_tile;               // tokens per MMA (multiple of 16, <= 256)
+  int stages;               // ring depth, 2..UM_MAX_STAGES
   // ---- epilogue ----
   int epi;
   int act;                  // UE_ROWS: activation applied (-1: none)
-  float* out_f32;           // UE_ROWS: [P, n_rows]; UE_DENSE_IN: [T, ld]
+  float* out_f32;           // UE_ROWS: [P, n_rows] (if out16 null); UE_DENSE_IN: [T, ld]
   int64_t out_ld;
   int out_col0;             // UE_DENSE_IN: first output column
+  unsigned short* out16;    // UE_ROWS: 16-bit [P, n_rows] instead of fp32;
+                            // UE_DENSE_IN: 16-bit copy of columns [c16_0, c16_1)
+  int64_t out16_ld;
+  int c16_0, c16_1;
   // UE_OUT: out[t, n] = x[t, n] + acc (+ combine of pexp for non-latent)
   const void* x; int x_dt; void* out; float* delta;
   const float* pexp; const float* wts; int add_combine;
@@ -158,6 +165,32 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16-byte asynchronous copy global -> shared; src_bytes = 0 writes zeros
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// wait until at most n of this thread's groups are pending (n = stages - 1)
+__device__ __forceinline__ void cp_async_wait(int n) {
+  switch (n) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+    case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
+  }
+}
+
 __device__ __forceinline__ uint32_t pack16(float a, float b, int dt) {
   if (dt == DT_BF16) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -170,6 +203,9 @@ __device__ __forceinline__ uint32_t pack16(float a, float b, int dt) {
 __device__ __forceinline__ uint32_t core_off(int row, int k) {
   return static_cast<uint32_t>((row >> 3) * UM_SBO + (k >> 3) * UM_LBO + (row & 7) * 16 + (k & 7) * 2);
 }
+
+// exact float of a 4-bit code: the bits of 2^23 + q, minus 2^23
+__device__ __forceinline__ float code_f(uint32_t q) { return __uint_as_float(0x4B000000u | q) - 8388608.0f; }
 
 // ---------------------------------------------------------------------------
 // the kernel
@@ -195,125 +231,41 @@ __device__ __forceinline__ UmmaGroup umma_group(const UmmaArgs& A, int g) {
   return G;
 }
 
-// source row of token n of the group
-__device__ __forceinline__ int64_t umma_token_row(const UmmaArgs& A, const UmmaGroup& G, int n,
-                                                  int* pid_out) {
-  if (!A.experts) {
-    *pid_out = n;
-    return n;
-  }
-  const int pid = A.meta[2 + 2 * A.umax + G.p0 + n];
-  *pid_out = pid;
-  return A.by_pair ? pid : pid / A.k;
-}
+// Shared-memory plan of one launch: `stages` ring slots of
+// [A (16-bit tile, or int4 codes + scale/bias words, x2 when gated) | B],
+// then (int4 only) two 16-bit A tiles (x2 when gated), the token table (256
+// ints), the mbarrier and the TMEM address.
+struct UmmaPlan {
+  uint32_t a_raw, b_bytes, stage, abuf, tok, total;
+};
 
-// Stage A rows [m0, m0 + 128) x K-chunk kc of matrix (q, sb) or of the dense
-// segments into sA.
-__device__ __forceinline__ void umma_stage_a(const UmmaArgs& A, const UmmaGroup& G, int m0, int kc,
-                                             const uint32_t* q, const uint32_t* sb, char* sA) {
-  const int k0 = kc * UM_KC;
-  if (A.a_mode == UA_INT4) {
-    // 128 rows x 2 halves of 32 codes: one 16-byte load per thread
-    const int t = threadIdx.x;
-    const int r = t >> 1, h = t & 1;
-    const int m = m0 + r;
-    if (m < A.n_rows) {
-      const int64_t row = static_cast<int64_t>(G.e) * A.n_rows + m;
-      const uint4 w = ldg_stream(q + row * (A.K >> 3) + (k0 >> 3) + 4 * h);
-      const int g = (k0 + 32 * h) / A.G;
-      float s, b;
-      sb_decode(ldg_u32(sb + row * (A.K / A.G) + g), A.s_dt, s, b);
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        // word i holds elements 32h + 8i .. +7 (one core-matrix row), nibble n -> element n
-        uint32_t pr[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float lo = fmaf(s, static_cast<float>((ws[i] >> (8 * j)) & 0xFu), b);
-          const float hi = fmaf(s, static_cast<float>((ws[i] >> (8 * j + 4)) & 0xFu), b);
-          pr[j] = pack16(lo, hi, A.mma_dt);
-        }
-        *reinterpret_cast<uint4*>(sA + core_off(r, 32 * h + 8 * i)) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        *reinterpret_cast<uint4*>(sA + core_off(r, 32 * h + 8 * i)) = make_uint4(0u, 0u, 0u, 0u);
-    }
-  } else {
-    // dense 16-bit rows: 128 rows x 8 chunks of 16 bytes = 1024 chunks, 4 per thread
-    for (int c = threadIdx.x; c < UM_M * (UM_KC / 8); c += UM_THREADS) {
-      const int r = c >> 3, j = c & 7;
-      const int m = m0 + r;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (m < A.n_rows) {
-        int si = 0;
-        while (m >= A.seg[si].row0 + A.seg[si].rows) ++si;
-        const DenseSeg& S = A.seg[si];
-        const int kk = k0 + 8 * j;
-        for (int p = 0; p < S.nparts; ++p) {
-          const DensePart& P = S.part[p];
-          if (kk >= P.k0 && kk < P.k0 + P.wk) {
-            const char* base = static_cast<const char*>(P.w) +
-                               (static_cast<int64_t>(m - S.row0) * P.wk + (kk - P.k0)) * 2;
-            v = ldg_stream(base);
-          }
-        }
-      }
-      *reinterpret_cast<uint4*>(sA + core_off(r, 8 * j)) = v;
-    }
-  }
-}
-
-// Stage B: tokens [n0, n0 + npad) of the group, K-chunk kc, as 16-bit.
-__device__ __forceinline__ void umma_stage_b(const UmmaArgs& A, const UmmaGroup& G, int n0,
-                                             int nvalid, int npad, int kc, char* sB) {
-  const int k0 = kc * UM_KC;
-  for (int c = threadIdx.x; c < npad * (UM_KC / 8); c += UM_THREADS) {
-    const int n = c >> 3, j = c & 7;
-    const int kk = k0 + 8 * j;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (n < nvalid) {
-      int pid;
-      const int64_t row = umma_token_row(A, G, n0 + n, &pid);
-      const void* src;
-      int dt;
-      int64_t e;
-      if (kk < A.b0_k) {
-        src = A.b0; dt = A.b0_dt; e = A.b0_off + row * A.b0_stride + kk;
-      } else {
-        src = A.b1; dt = A.b1_dt; e = A.b1_off + row * A.b1_stride + (kk - A.b0_k);
-      }
-      if (dt == A.mma_dt) {
-        v = *reinterpret_cast<const uint4*>(static_cast<const char*>(src) + e * 2);
-      } else {
-        float f[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = ld_any(src, e + i, dt);
-        v.x = pack16(f[0], f[1], A.mma_dt); v.y = pack16(f[2], f[3], A.mma_dt);
-        v.z = pack16(f[4], f[5], A.mma_dt); v.w = pack16(f[6], f[7], A.mma_dt);
-      }
-    }
-    *reinterpret_cast<uint4*>(sB + core_off(n, 8 * j)) = v;
-  }
-}
-
-constexpr size_t umma_smem_bytes() {
-  return 2 * (2 * static_cast<size_t>(UM_A_BYTES) + UM_B_BYTES) + 64;
+__host__ __device__ inline UmmaPlan umma_plan(int a_mode, bool gated, int n_tile, int stages) {
+  UmmaPlan p;
+  p.a_raw = a_mode == UA_DENSE ? static_cast<uint32_t>(UM_A_BYTES)
+                               : (gated ? 2u : 1u) * static_cast<uint32_t>(UM_CODE_BYTES + UM_SB_BYTES);
+  p.b_bytes = static_cast<uint32_t>(n_tile) * UM_KC * 2;
+  p.stage = p.a_raw + p.b_bytes;
+  p.abuf = static_cast<uint32_t>(stages) * p.stage;
+  const uint32_t abuf_bytes = a_mode == UA_DENSE ? 0u : 2u * (gated ? 2u : 1u) * UM_A_BYTES;
+  p.tok = p.abuf + abuf_bytes;
+  p.total = p.tok + 256 * 4 + 64;
+  return p;
 }
 
 __global__ void __launch_bounds__(UM_THREADS, 1) k_umma(const UmmaArgs A) {
   extern __shared__ __align__(1024) char um_smem[];
-  // layout: [2 stages][A (16 KB), A2 (16 KB), B (32 KB)] then 2 mbarriers + tmem holder
-  constexpr int STAGE = 2 * UM_A_BYTES + UM_B_BYTES;
-  char* base = um_smem;
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(base + 2 * STAGE);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base + 2 * STAGE + 16);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool gated = (A.a_mode == UA_INT4) && A.q2 != nullptr;
+  const UmmaPlan P = umma_plan(A.a_mode, gated, A.n_tile, A.stages);
+  char* base = um_smem;
+  int* tok_row = reinterpret_cast<int*>(base + P.tok);        // [n_tile] source rows
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(base + P.tok + 256 * 4);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base + P.tok + 256 * 4 + 16);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ncols = gated ? 512 : 256;
+  const int S = A.stages;
 
+  griddep_wait();
+  griddep_launch();
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_holder)),
@@ -322,75 +274,179 @@ __global__ void __launch_bounds__(UM_THREADS, 1) k_umma(const UmmaArgs A) {
   }
   if (tid == 0) {
     mbar_init(smem_u32(&mbar[0]), 1);
-    mbar_init(smem_u32(&mbar[1]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  uint32_t phase[2] = {0u, 0u};
-  uint32_t pending[2] = {0u, 0u};   // a commit on this stage not yet waited for
+  uint32_t commits = 0;      // tcgen05.commit operations issued so far (all waited in order)
   bool ok = true;
 
   const int n_groups = A.experts ? A.meta[0] : 1;
   const int mtiles = (A.n_rows + UM_M - 1) / UM_M;
   const int nkc = A.K / UM_KC;
+  const int ngr = A.K / A.G;
 
   for (int unit = blockIdx.x; ok && unit < n_groups * mtiles; unit += gridDim.x) {
     const int g = unit / mtiles, mt = unit - g * mtiles;
     const UmmaGroup G = umma_group(A, g);
     const int m0 = mt * UM_M;
-    for (int n0 = 0; ok && n0 < G.n; n0 += UM_NMAX) {
-      const int nvalid = min(UM_NMAX, G.n - n0);
+    for (int n0 = 0; ok && n0 < G.n; n0 += A.n_tile) {
+      const int nvalid = min(A.n_tile, G.n - n0);
       const int npad = (nvalid + 15) & ~15;
       const uint32_t idesc = umma_idesc(npad, A.mma_dt);
+      // token table: source row of every token of this tile
+      for (int n = tid; n < nvalid; n += UM_THREADS) {
+        int row = n0 + n;
+        if (A.experts) {
+          const int pid = A.meta[2 + 2 * A.umax + G.p0 + n0 + n];
+          row = A.by_pair ? pid : pid / A.k;
+        }
+        tok_row[n] = row;
+      }
+      __syncthreads();
+
+      // issue the copies of K-chunk kc into ring slot kc % S
+      auto issue = [&](int kc) {
+        char* slot = base + static_cast<size_t>(kc % S) * P.stage;
+        const uint32_t sa = smem_u32(slot), sbb = smem_u32(slot + P.a_raw);
+        const int k0 = kc * UM_KC;
+        if (A.a_mode == UA_DENSE) {
+          for (int c = tid; c < UM_M * 8; c += UM_THREADS) {
+            const int r = c >> 3, j = c & 7;
+            const int m = m0 + r, kk = k0 + 8 * j;
+            const void* src = A.b0;
+            uint32_t nbytes = 0;
+            if (m < A.n_rows) {
+              int si = 0;
+              while (m >= A.seg[si].row0 + A.seg[si].rows) ++si;
+              const DenseSeg& Sg = A.seg[si];
+              for (int p = 0; p < Sg.nparts; ++p) {
+                const DensePart& Pt = Sg.part[p];
+                if (kk >= Pt.k0 && kk < Pt.k0 + Pt.wk) {
+                  src = static_cast<const char*>(Pt.w) +
+                        (static_cast<int64_t>(m - Sg.row0) * Pt.wk + (kk - Pt.k0)) * 2;
+                  nbytes = 16;
+                }
+              }
+            }
+            cp_async16(sa + core_off(r, 8 * j), src, nbytes);
+          }
+        } else {
+          // codes: row r = tid / 2, 32 codes (16 bytes) per half
+          {
+            const int r = tid >> 1, hh = tid & 1;
+            const int m = min(m0 + r, A.n_rows - 1);
+            const int64_t row = static_cast<int64_t>(G.e) * A.n_rows + m;
+            const uint32_t nb = (m0 + r < A.n_rows) ? 16u : 0u;
+            cp_async16(sa + r * 32 + hh * 16, A.q + row * (A.K >> 3) + (k0 >> 3) + 4 * hh, nb);
+            if (gated)
+              cp_async16(sa + UM_CODE_BYTES + UM_SB_BYTES + r * 32 + hh * 16,
+                         A.q2 + row * (A.K >> 3) + (k0 >> 3) + 4 * hh, nb);
+          }
+          // scale/bias words of the chunk: one word per row (G >= 64), two (G = 32)
+          if (tid < UM_M) {
+            const int r = tid;
+            const int m = min(m0 + r, A.n_rows - 1);
+            const int64_t row = static_cast<int64_t>(G.e) * A.n_rows + m;
+            const int gw = k0 / A.G;
+            if (A.G == 32) {
+              cp_async8(sa + UM_CODE_BYTES + r * 8, A.sb + row * ngr + gw);
+              if (gated) cp_async8(sa + 2 * UM_CODE_BYTES + UM_SB_BYTES + r * 8, A.sb2 + row * ngr + gw);
+            } else {
+              cp_async4(sa + UM_CODE_BYTES + r * 8, A.sb + row * ngr + gw);
+              if (gated) cp_async4(sa + 2 * UM_CODE_BYTES + UM_SB_BYTES + r * 8, A.sb2 + row * ngr + gw);
+            }
+          }
+        }
+        // B: npad tokens x 8 chunks of 16 bytes
+        for (int c = tid; c < npad * 8; c += UM_THREADS) {
+          const int n = c >> 3, j = c & 7;
+          const void* src = A.b0;
+          uint32_t nbytes = 0;
+          if (n < nvalid) {
+            src = static_cast<const char*>(A.b0) +
+                  (A.b0_off + static_cast<int64_t>(tok_row[n]) * A.b0_stride + k0 + 8 * j) * 2;
+            nbytes = 16;
+          }
+          cp_async16(sbb + core_off(n, 8 * j), src, nbytes);
+        }
+      };
+
+      // dequantise the int4 codes of ring slot kc % S into A tile buffer kc & 1
+      auto dequant = [&](int kc) {
+        const char* slot = base + static_cast<size_t>(kc % S) * P.stage;
+        const int r = tid >> 1, hh = tid & 1;
+        for (int gsel = 0; gsel < (gated ? 2 : 1); ++gsel) {
+          const char* raw = slot + gsel * (UM_CODE_BYTES + UM_SB_BYTES);
+          char* dst = base + P.abuf + static_cast<size_t>((kc & 1) + 2 * gsel) * UM_A_BYTES;
+          const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 32 + hh * 16);
+          const uint32_t sbw = *reinterpret_cast<const uint32_t*>(
+              raw + UM_CODE_BYTES + r * 8 + ((A.G == 32) ? 4 * hh : 0));
+          float s, b;
+          sb_decode(sbw, A.s_dt, s, b);
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t pr[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float lo = fmaf(s, code_f((ws[i] >> (8 * j)) & 0xFu), b);
+              const float hi = fmaf(s, code_f((ws[i] >> (8 * j + 4)) & 0xFu), b);
+              pr[j] = pack16(lo, hi, A.mma_dt);
+            }
+            *reinterpret_cast<uint4*>(dst + core_off(r, 32 * hh + 8 * i)) =
+                make_uint4(pr[0], pr[1], pr[2], pr[3]);
+          }
+        }
+      };
+
+      for (int s = 0; s < S - 1; ++s) {
+        if (s < nkc) issue(s);
+        cp_async_commit();
+      }
       for (int kc = 0; kc < nkc; ++kc) {
-        const int st = kc & 1;
-        char* sA = base + st * STAGE;
-        char* sA2 = sA + UM_A_BYTES;
-        char* sB = sA + 2 * UM_A_BYTES;
-        // the MMAs that last read this stage must be done before overwriting it;
-        // thread 0 waits, the barrier makes the outcome uniform
-        if (pending[st]) {
+        if (kc > 0) {
+          // MMAs of chunk kc-1 done: its ring slot and A buffer (kc-1)&1 may be
+          // overwritten, and A buffer kc&1 (read by chunk kc-2) is free too
           bool w = true;
-          if (tid == 0) w = mbar_wait(smem_u32(&mbar[st]), phase[st]);
-          phase[st] ^= 1u;
-          pending[st] = 0u;
+          if (tid == 0) w = mbar_wait(smem_u32(&mbar[0]), (commits - 1) & 1u);
           if (!__syncthreads_and(w)) { ok = false; break; }
         }
-        umma_stage_a(A, G, m0, kc, A.q, A.sb, sA);
-        if (gated) umma_stage_a(A, G, m0, kc, A.q2, A.sb2, sA2);
-        umma_stage_b(A, G, n0, nvalid, npad, kc, sB);
+        if (kc + S - 1 < nkc) issue(kc + S - 1);
+        cp_async_commit();
+        cp_async_wait(S - 1);
+        __syncthreads();
+        if (A.a_mode == UA_INT4) dequant(kc);
         fence_proxy_async();
         __syncthreads();
         if (tid == 0) {
           tc_fence_after();
+          const char* slot = base + static_cast<size_t>(kc % S) * P.stage;
+          const uint32_t a_addr = A.a_mode == UA_DENSE
+                                      ? smem_u32(slot)
+                                      : smem_u32(base + P.abuf + static_cast<size_t>(kc & 1) * UM_A_BYTES);
+          const uint32_t b_addr = smem_u32(slot + P.a_raw);
 #pragma unroll
           for (int kk = 0; kk < UM_KC / 16; ++kk) {
-            const uint64_t ad = umma_desc(smem_u32(sA) + kk * 2 * UM_LBO);
-            const uint64_t bd = umma_desc(smem_u32(sB) + kk * 2 * UM_LBO);
+            const uint64_t ad = umma_desc(a_addr + kk * 2 * UM_LBO);
+            const uint64_t bd = umma_desc(b_addr + kk * 2 * UM_LBO);
             umma_f16(tmem, ad, bd, idesc, (kc | kk) ? 1u : 0u);
             if (gated) {
-              const uint64_t a2 = umma_desc(smem_u32(sA2) + kk * 2 * UM_LBO);
-              umma_f16(tmem + 256, a2, bd, idesc, (kc | kk) ? 1u : 0u);
+              const uint32_t a2 = smem_u32(base + P.abuf + static_cast<size_t>((kc & 1) + 2) * UM_A_BYTES);
+              umma_f16(tmem + 256, umma_desc(a2 + kk * 2 * UM_LBO), bd, idesc, (kc | kk) ? 1u : 0u);
             }
           }
-          umma_commit(smem_u32(&mbar[st]));
+          umma_commit(smem_u32(&mbar[0]));
         }
-        pending[st] = 1u;
+        ++commits;
       }
       if (!ok) break;
-      // wait for the last MMAs (both stages), then read the accumulators
+      cp_async_wait(0);
       {
         bool w = true;
-        for (int st = 0; st < 2; ++st) {
-          if (pending[st]) {
-            if (tid == 0 && w) w = mbar_wait(smem_u32(&mbar[st]), phase[st]);
-            phase[st] ^= 1u;
-            pending[st] = 0u;
-          }
-        }
+        if (tid == 0) w = mbar_wait(smem_u32(&mbar[0]), (commits - 1) & 1u);
         if (!__syncthreads_and(w)) { ok = false; break; }
       }
       tc_fence_after();
@@ -406,17 +462,20 @@ __global__ void __launch_bounds__(UM_THREADS, 1) k_umma(const UmmaArgs A) {
         for (int i = 0; i < 16; ++i) {
           const int n = c0 + i;
           if (n >= nvalid) break;
-          int pid;
-          const int64_t trow = umma_token_row(A, G, n0 + n, &pid);
-          (void)trow;
+          const int pid = A.experts ? A.meta[2 + 2 * A.umax + G.p0 + n0 + n] : n0 + n;
           float v = acc[i];
           if (A.epi == UE_ROWS) {
-            // gate accumulates in the second TMEM block; act(g, u)
             // A (q) is the up projection, A2 (q2) the gate: act(gate, up)
             if (A.act >= 0) v = gated ? act_fn(A.act, accg[i], v) : act_fn(A.act, 0.f, v);
-            A.out_f32[static_cast<int64_t>(pid) * A.n_rows + m] = v;
+            if (A.out16)
+              A.out16[static_cast<int64_t>(pid) * A.n_rows + m] = st16_bits(v, A.mma_dt);
+            else
+              A.out_f32[static_cast<int64_t>(pid) * A.n_rows + m] = v;
           } else if (A.epi == UE_DENSE_IN) {
-            A.out_f32[static_cast<int64_t>(pid) * A.out_ld + A.out_col0 + m] = v;
+            const int col = A.out_col0 + m;
+            A.out_f32[static_cast<int64_t>(pid) * A.out_ld + col] = v;
+            if (A.out16 && col >= A.c16_0 && col < A.c16_1)
+              A.out16[static_cast<int64_t>(pid) * A.out16_ld + (col - A.c16_0)] = st16_bits(v, A.mma_dt);
           } else {
             const int t = pid;
             if (A.add_combine) {
@@ -432,17 +491,17 @@ __global__ void __launch_bounds__(UM_THREADS, 1) k_umma(const UmmaArgs A) {
           }
         }
       }
-      // all TMEM reads done before the next unit's MMAs overwrite the accumulators
+      // all TMEM reads done before the next tile's MMAs overwrite the accumulators
       tc_fence_before();
       __syncthreads();
       tc_fence_after();
     }
   }
+  cp_async_wait(0);
   if (!ok && tid == 0) {
     atomicOr(A.status, STATUS_TIMEOUT);
     // bounded wait for MMAs still in flight before releasing TMEM
-    for (int st = 0; st < 2; ++st)
-      if (pending[st]) mbar_wait(smem_u32(&mbar[st]), phase[st]);
+    if (commits) mbar_wait(smem_u32(&mbar[0]), (commits - 1) & 1u);
   }
   tc_fence_before();
   __syncthreads();
@@ -451,10 +510,6 @@ __global__ void __launch_bounds__(UM_THREADS, 1) k_umma(const UmmaArgs A) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols));
   }
 }
-
-}  // namespace moe
-
-namespace moe {
 
 // Operand B of the grouped output projection: per token, [combined routed
 // output y (latent layers) | shared-expert activation], rounded to the MMA type.
@@ -468,6 +523,8 @@ struct PrepOutArgs {
 };
 
 __global__ void k_prep_out(const PrepOutArgs A) {
+  griddep_wait();
+  griddep_launch();
   const int K = A.L + A.Fs;
   const int64_t n = static_cast<int64_t>(A.T) * K;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
