@@ -230,141 +230,197 @@ __device__ __forceinline__ bool key_better(float a, int ia, float b, int ib) {
 
 // Shared memory of route_block: two int arrays of MAX_E and 2 x 32 ints, plus
 // E * mask_words words of row bitmasks when A.mask_words > 0.
-constexpr int ROUTE_SMEM_BYTES = (2 * MAX_E + 64) * 4;
+constexpr int ROUTE_CAND_WORDS = 32 * MAX_K * 3;   // per-warp candidate lists (32 warps max)
+constexpr int ROUTE_SMEM_BYTES = (2 * MAX_E + 64 + ROUTE_CAND_WORDS) * 4;
 
 // Routing of all T rows by one CTA (any block size that is a multiple of 32):
 // top-k per row by warp-shuffle selection, the combine weights, then the
 // distinct selected experts (ascending) with their (row, pick) pairs in row
 // order.  Logits are read with ld.global.cg, so this may run in the last CTA
 // of the kernel that produced them.
-static __device__ void route_block(const RouteArgs& A, int* smem) {
+
+// k rounds of selection over register-held keys: every round takes the lane's
+// best remaining key with a pairwise tree, then the warp's best by a
+// butterfly; the owner lane retires it.  Lane j ends with pick j (its expert
+// id and its weight input sv).  With ck != nullptr lanes j < k also write the
+// picks to ck/ci/cs[j] (a candidate list for a later merge).
+template <int NPL>
+__device__ __forceinline__ void topk_rounds(float (&kv)[NPL], const int (&ev)[NPL], const float (&sv)[NPL],
+                                            int k, int lane, int& my_id, float& my_z, float* ck,
+                                            int* ci, float* cs) {
+  for (int j = 0; j < k; ++j) {
+    float tk[NPL];
+    int tix[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) { tk[i] = kv[i]; tix[i] = ev[i]; }
+#pragma unroll
+    for (int w = NPL / 2; w >= 1; w >>= 1) {
+#pragma unroll
+      for (int i = 0; i < w; ++i) {
+        const bool b1 = key_better(tk[i + w], tix[i + w], tk[i], tix[i]);
+        tk[i] = b1 ? tk[i + w] : tk[i];
+        tix[i] = b1 ? tix[i + w] : tix[i];
+      }
+    }
+    float bk = tk[0];
+    int bi = tix[0];
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (key_better(ok, oi, bk, bi)) { bk = ok; bi = oi; }
+    }
+    // the owner lane retires the key and publishes its weight input
+    float ws = 0.f;
+    int owner = -1;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      if (ev[i] == bi) { ws = sv[i]; kv[i] = -INFINITY; owner = lane; }
+    }
+    owner = __reduce_max_sync(0xffffffffu, owner);
+    ws = __shfl_sync(0xffffffffu, ws, owner < 0 ? 0 : owner);
+    if (lane == j) { my_id = bi; my_z = ws; }
+    if (ck && lane == j) { ck[j] = bk; ci[j] = bi; cs[j] = ws; }
+  }
+}
+
+// Keys of one member warp: experts lane + 32 * (g + W * i), i < NPL.
+template <int NPL>
+__device__ __forceinline__ void route_member(const RouteArgs& A, const float* z, int W, int g, int lane,
+                                             int& my_id, float& my_z, float* ck, int* ci, float* cs,
+                                             bool& bad) {
+  float kv[NPL], sv[NPL];
+  int ev[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * (g + W * i);
+    const bool ok = e < A.E;
+    ev[i] = ok ? e : 0x7fffffff;
+    sv[i] = ok ? __ldcg(z + e) : 0.f;
+    kv[i] = (ok && A.bias) ? __ldg(A.bias + e) : 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    if (ev[i] < A.E) {
+      const float zz = sv[i];
+      float key;
+      if (A.router == ROUTER_SOFTMAX) {
+        key = zz;                          // softmax weights use the logit
+      } else {
+        const float sg = 1.0f / (1.0f + expf(-zz));
+        key = sg + kv[i];                  // selection key: score + bias
+        sv[i] = sg;                        // weight: score without bias
+      }
+      if (!isfinite(key)) { bad = true; key = -INFINITY; }
+      kv[i] = key;
+    } else {
+      kv[i] = -INFINITY;
+    }
+  }
+  topk_rounds<NPL>(kv, ev, sv, A.k, lane, my_id, my_z, ck, ci, cs);
+}
+
+static __device__ __noinline__ void route_block(const RouteArgs& A, int* smem) {
   int* s_cnt = smem;
   int* s_scan_c = smem + MAX_E;
   int* s_wsum_u = smem + 2 * MAX_E;
   int* s_wsum_c = s_wsum_u + 32;
-  uint32_t* s_mask = reinterpret_cast<uint32_t*>(smem + 2 * MAX_E + 64);
+  uint32_t* s_mask = reinterpret_cast<uint32_t*>(smem + 2 * MAX_E + 64 + ROUTE_CAND_WORDS);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = blockDim.x >> 5;
   const int nthr = blockDim.x;
   const int E = A.E, k = A.k;
-  const int nper = (E + 31) >> 5;
   unsigned long long tp[8];
   if (A.debug_times) tp[0] = global_ns();
 
-  for (int t = warp; t < A.T; t += nwarp) {
-    const float* z = A.logits + static_cast<int64_t>(t) * A.r_in;
-    // 1. load every key of the lane (experts lane, lane + 32, ...), all loads
-    //    first so none waits inside the selection below
-    float kv[32], sv[32];
-    bool bad = false;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int e = lane + 32 * i;
-      const bool ok = i < nper && e < E;
-      sv[i] = ok ? __ldcg(z + e) : 0.f;
-      kv[i] = (ok && A.bias) ? __ldg(A.bias + e) : 0.f;
-    }
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int e = lane + 32 * i;
-      if (i < nper && e < E) {
-        const float zz = sv[i];
-        float key;
-        if (A.router == ROUTER_SOFTMAX) {
-          key = zz;
-          sv[i] = zz;                         // softmax weights use the logit
-        } else {
-          const float sg = 1.0f / (1.0f + expf(-zz));
-          key = sg + kv[i];                   // selection key: score + bias
-          sv[i] = sg;                         // weight: score without bias
-        }
-        if (!isfinite(key)) { bad = true; key = -INFINITY; }
-        kv[i] = key;
-      } else {
-        kv[i] = -INFINITY;
-      }
-    }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(A.status, STATUS_NONFINITE);
-    // 2. k rounds: the lane's best remaining key by a pairwise tree, then a warp
-    //    argmax by butterfly; the owner lane retires that key
+  // W warps cooperate on one row (more when there are few rows), each with
+  // its slice of the experts; the first warp of the group merges their lists
+  float* cand_k = reinterpret_cast<float*>(smem + 2 * MAX_E + 64);
+  int* cand_i = reinterpret_cast<int*>(cand_k + 32 * MAX_K);
+  float* cand_s = reinterpret_cast<float*>(cand_i + 32 * MAX_K);
+  int W = E > 16 * 32 ? 2 : 1;            // at most 16 keys per lane
+  while (W < 8 && A.T * W * 2 <= nwarp) W *= 2;
+  const int npl = (E + 32 * W - 1) / (32 * W);
+  const int rows_per_pass = nwarp / W;
+  for (int tb = 0; tb < A.T; tb += rows_per_pass) {
+    const int t = tb + warp / W, g = warp % W;
+    const bool active = t < A.T;
+    const float* z = A.logits + static_cast<int64_t>(active ? t : 0) * A.r_in;
     int my_id = -1;
     float my_z = 0.f;
-    for (int j = 0; j < k; ++j) {
-      float tkv[16];
-      int tix[16];
+    bool bad = false;
+    float* ck = (W > 1) ? cand_k + warp * MAX_K : nullptr;
+    int* ci = cand_i + warp * MAX_K;
+    float* cs = cand_s + warp * MAX_K;
+    if (active) {
+      if (npl <= 1) route_member<1>(A, z, W, g, lane, my_id, my_z, ck, ci, cs, bad);
+      else if (npl <= 2) route_member<2>(A, z, W, g, lane, my_id, my_z, ck, ci, cs, bad);
+      else if (npl <= 4) route_member<4>(A, z, W, g, lane, my_id, my_z, ck, ci, cs, bad);
+      else if (npl <= 8) route_member<8>(A, z, W, g, lane, my_id, my_z, ck, ci, cs, bad);
+      else route_member<16>(A, z, W, g, lane, my_id, my_z, ck, ci, cs, bad);
+      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(A.status, STATUS_NONFINITE);
+    }
+    if (W > 1) {
+      __syncthreads();
+      if (active && g == 0) {
+        // merge the W lists of k picks held by warps warp .. warp + W - 1
+        float kv[4], sv[4];
+        int ev[4];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int e0 = lane + 32 * i, e1 = lane + 32 * (i + 16);
-        const bool b1 = (i + 16 < nper) && key_better(kv[i + 16], e1, kv[i], e0);
-        tkv[i] = b1 ? kv[i + 16] : kv[i];
-        tix[i] = (i < nper) ? (b1 ? e1 : e0) : 0x7fffffff;
+        for (int i = 0; i < 4; ++i) {
+          const int c = lane + 32 * i;            // candidate c of W * k
+          const int wl = c / k, jl = c - wl * k;
+          const bool ok = c < W * k;
+          kv[i] = ok ? cand_k[(warp + wl) * MAX_K + jl] : -INFINITY;
+          ev[i] = ok ? cand_i[(warp + wl) * MAX_K + jl] : 0x7fffffff;
+          sv[i] = ok ? cand_s[(warp + wl) * MAX_K + jl] : 0.f;
+        }
+        topk_rounds<4>(kv, ev, sv, k, lane, my_id, my_z, nullptr, nullptr, nullptr);
       }
-#pragma unroll
-      for (int w = 8; w >= 1; w >>= 1) {
-#pragma unroll
-        for (int i = 0; i < w; ++i) {
-          const bool b1 = key_better(tkv[i + w], tix[i + w], tkv[i], tix[i]);
-          tkv[i] = b1 ? tkv[i + w] : tkv[i];
-          tix[i] = b1 ? tix[i + w] : tix[i];
+    }
+    if (active && g == 0) {
+      // combine weights (lane j < k holds pick j; my_z is its logit for softmax
+      // routing and its sigmoid score for sigmoid routing)
+      const float zj = (lane < k) ? my_z : 0.f;
+      float wv = 0.f;
+      if (A.router == ROUTER_SOFTMAX) {
+        const float m = __shfl_sync(0xffffffffu, zj, 0);   // largest selected logit
+        float den = 0.f;
+        if (A.renorm) {
+          const float ex = (lane < k) ? expf(zj - m) : 0.f;
+          den = ex;
+  #pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+          wv = ex / den;
+        } else {
+          float mm = -INFINITY;
+          for (int i = lane; i < E; i += 32) mm = fmaxf(mm, __ldcg(z + i));
+  #pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+          for (int i = lane; i < E; i += 32) den += expf(__ldcg(z + i) - mm);
+  #pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+          wv = (lane < k) ? expf(zj - mm) / den : 0.f;
+        }
+      } else {
+        const float sg = zj;
+        wv = sg;
+        if (A.renorm) {
+          float den = sg;
+  #pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+          wv = sg / den;
         }
       }
-      float bk = tkv[0];
-      int bi = tix[0];
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (key_better(ok, oi, bk, bi)) { bk = ok; bi = oi; }
+      wv *= A.scale;
+      if (lane < k) {
+        A.ids[t * k + lane] = my_id;
+        A.w[t * k + lane] = wv;
+        if (A.ext_ids) A.ext_ids[t * k + lane] = my_id;
+        if (A.ext_w) A.ext_w[t * k + lane] = wv;
       }
-      // the owner lane publishes the winner's weight input and retires the key
-      const int owner = bi & 31, slot = bi >> 5;
-      float wsel = 0.f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        if (lane == owner && i == slot) { wsel = sv[i]; kv[i] = -INFINITY; }
-      }
-      wsel = __shfl_sync(0xffffffffu, wsel, owner);
-      if (lane == j) { my_id = bi; my_z = wsel; }
+  
     }
-    // combine weights (lane j < k holds pick j; my_z is its logit for softmax
-    // routing and its sigmoid score for sigmoid routing)
-    const float zj = (lane < k) ? my_z : 0.f;
-    float wv = 0.f;
-    if (A.router == ROUTER_SOFTMAX) {
-      const float m = __shfl_sync(0xffffffffu, zj, 0);   // largest selected logit
-      float den = 0.f;
-      if (A.renorm) {
-        const float ex = (lane < k) ? expf(zj - m) : 0.f;
-        den = ex;
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-        wv = ex / den;
-      } else {
-        float mm = -INFINITY;
-        for (int i = lane; i < E; i += 32) mm = fmaxf(mm, __ldcg(z + i));
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
-        for (int i = lane; i < E; i += 32) den += expf(__ldcg(z + i) - mm);
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-        wv = (lane < k) ? expf(zj - mm) / den : 0.f;
-      }
-    } else {
-      const float sg = zj;
-      wv = sg;
-      if (A.renorm) {
-        float den = sg;
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-        wv = sg / den;
-      }
-    }
-    wv *= A.scale;
-    if (lane < k) {
-      A.ids[t * k + lane] = my_id;
-      A.w[t * k + lane] = wv;
-      if (A.ext_ids) A.ext_ids[t * k + lane] = my_id;
-      if (A.ext_w) A.ext_w[t * k + lane] = wv;
-    }
+    if (W > 1) __syncthreads();
   }
   // ---- distinct experts and their pairs ----
   if (A.debug_times) tp[1] = global_ns();
