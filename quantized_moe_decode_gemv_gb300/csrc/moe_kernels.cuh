@@ -602,7 +602,7 @@ struct DenseOutArgs {
 // Rows of the dense weights per register batch: every thread keeps partial sums
 // for RB rows x TB token rows.
 template <int TB>
-__host__ __device__ constexpr int dense_rb() { return TB <= 4 ? 4 : 2; }
+__host__ __device__ constexpr int dense_rb() { return TB <= 2 ? 4 : 2; }
 
 // One step of the dense streaming loop: rows [r, r + nb) of segment si, part
 // p, 16-byte chunks [cbase, cbase + MAXC * NT).
@@ -669,63 +669,53 @@ __device__ __forceinline__ void dense_rows(const DenseSeg* segs, int r_begin, in
   constexpr int RBN = dense_rb<TB>();
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  DStep cur;
-  dstep_first<RBN>(segs, r_begin, r_end, cur);
-  uint4 wcur[RBN][MAXC];
-  if (cur.valid) dstep_load<RBN>(segs, cur, wcur);
-  stage();
   float acc[RBN][TB];
 #pragma unroll
   for (int i = 0; i < RBN; ++i)
 #pragma unroll
     for (int t = 0; t < TB; ++t) acc[i][t] = 0.0f;
-  while (cur.valid) {
-    DStep nxt = cur;
-    dstep_next<RBN>(segs, r_end, nxt);
-    uint4 wnxt[RBN][MAXC];
-    if (nxt.valid) dstep_load<RBN>(segs, nxt, wnxt);
-    // compute the current step
-    {
-      const DensePart& P = segs[cur.si].part[cur.p];
-      const int nch = dpart_chunks(P);
+
+  // compute one step from its loaded weights; reduce when its rows are done
+  auto compute = [&](const DStep& cur, const uint4 (&w)[RBN][MAXC], const DStep& nxt) {
+    const DensePart& P = segs[cur.si].part[cur.p];
+    const int nch = dpart_chunks(P);
 #pragma unroll
-      for (int c = 0; c < MAXC; ++c) {
-        const int ci = cur.cbase + c * NT + tid;
-        if (ci >= nch) continue;
-        if (P.dt != DT_FP32) {
-          const int f4 = (P.k0 >> 2) + 2 * ci;
-          const int s0 = swz(f4, 1), s1 = swz(f4 + 1, 1);
+    for (int c = 0; c < MAXC; ++c) {
+      const int ci = cur.cbase + c * NT + tid;
+      if (ci >= nch) continue;
+      if (P.dt != DT_FP32) {
+        const int f4 = (P.k0 >> 2) + 2 * ci;
+        const int s0 = swz(f4, 1), s1 = swz(f4 + 1, 1);
 #pragma unroll
-          for (int i = 0; i < RBN; ++i) {
-            if (i >= cur.nb) continue;
-            float wf[8];
-            cvt8(wcur[i][c], P.dt, wf);
+        for (int i = 0; i < RBN; ++i) {
+          if (i >= cur.nb) continue;
+          float wf[8];
+          cvt8(w[i][c], P.dt, wf);
 #pragma unroll
-            for (int t = 0; t < TB; ++t) {
-              const float4 a = xs4[t * K4 + s0];
-              const float4 b = xs4[t * K4 + s1];
-              float sacc = acc[i][t];
-              sacc = fmaf(wf[0], a.x, sacc); sacc = fmaf(wf[1], a.y, sacc);
-              sacc = fmaf(wf[2], a.z, sacc); sacc = fmaf(wf[3], a.w, sacc);
-              sacc = fmaf(wf[4], b.x, sacc); sacc = fmaf(wf[5], b.y, sacc);
-              sacc = fmaf(wf[6], b.z, sacc); sacc = fmaf(wf[7], b.w, sacc);
-              acc[i][t] = sacc;
-            }
+          for (int t = 0; t < TB; ++t) {
+            const float4 a = xs4[t * K4 + s0];
+            const float4 b = xs4[t * K4 + s1];
+            float sacc = acc[i][t];
+            sacc = fmaf(wf[0], a.x, sacc); sacc = fmaf(wf[1], a.y, sacc);
+            sacc = fmaf(wf[2], a.z, sacc); sacc = fmaf(wf[3], a.w, sacc);
+            sacc = fmaf(wf[4], b.x, sacc); sacc = fmaf(wf[5], b.y, sacc);
+            sacc = fmaf(wf[6], b.z, sacc); sacc = fmaf(wf[7], b.w, sacc);
+            acc[i][t] = sacc;
           }
-        } else {
-          const int s0 = swz((P.k0 >> 2) + ci, 1);
+        }
+      } else {
+        const int s0 = swz((P.k0 >> 2) + ci, 1);
 #pragma unroll
-          for (int i = 0; i < RBN; ++i) {
-            if (i >= cur.nb) continue;
-            const uint4 v = wcur[i][c];
+        for (int i = 0; i < RBN; ++i) {
+          if (i >= cur.nb) continue;
+          const uint4 v = w[i][c];
 #pragma unroll
-            for (int t = 0; t < TB; ++t) {
-              const float4 a = xs4[t * K4 + s0];
-              float sacc = acc[i][t];
-              sacc = fmaf(__uint_as_float(v.x), a.x, sacc); sacc = fmaf(__uint_as_float(v.y), a.y, sacc);
-              sacc = fmaf(__uint_as_float(v.z), a.z, sacc); sacc = fmaf(__uint_as_float(v.w), a.w, sacc);
-              acc[i][t] = sacc;
-            }
+          for (int t = 0; t < TB; ++t) {
+            const float4 a = xs4[t * K4 + s0];
+            float sacc = acc[i][t];
+            sacc = fmaf(__uint_as_float(v.x), a.x, sacc); sacc = fmaf(__uint_as_float(v.y), a.y, sacc);
+            sacc = fmaf(__uint_as_float(v.z), a.z, sacc); sacc = fmaf(__uint_as_float(v.w), a.w, sacc);
+            acc[i][t] = sacc;
           }
         }
       }
@@ -747,11 +737,25 @@ __device__ __forceinline__ void dense_rows(const DenseSeg* segs, int r_begin, in
         if (i < cur.nb) red[((cur.r - r_begin + i) * TB + t) * NW + warp] = tot;
       }
     }
-    cur = nxt;
-#pragma unroll
-    for (int i = 0; i < RBN; ++i)
-#pragma unroll
-      for (int c = 0; c < MAXC; ++c) wcur[i][c] = wnxt[i][c];
+  };
+
+  // two register buffers in ping-pong (no copies between them: a copy would
+  // wait for the loads in flight)
+  DStep sa, sb;
+  uint4 wa[RBN][MAXC], wb[RBN][MAXC];
+  dstep_first<RBN>(segs, r_begin, r_end, sa);
+  if (sa.valid) dstep_load<RBN>(segs, sa, wa);
+  stage();
+  while (sa.valid) {
+    sb = sa;
+    dstep_next<RBN>(segs, r_end, sb);
+    if (sb.valid) dstep_load<RBN>(segs, sb, wb);
+    compute(sa, wa, sb);
+    if (!sb.valid) break;
+    sa = sb;
+    dstep_next<RBN>(segs, r_end, sa);
+    if (sa.valid) dstep_load<RBN>(segs, sa, wa);
+    compute(sb, wb, sa);
   }
 }
 
@@ -793,7 +797,21 @@ __global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_in(const D
   griddep_wait();
   griddep_launch();
   int rb, re;
-  cta_rows(A.total_rows, rb, re);
+  if (A.fuse_route) {
+    // the first route_ctas CTAs take the router rows [0, E) (fewer rows each,
+    // so the routing starts early and overlaps the rest of the pass)
+    const int E = A.route.E, rc = A.route_ctas, c = blockIdx.x, g = gridDim.x;
+    if (c < rc) {
+      rb = static_cast<int>(static_cast<int64_t>(c) * E / rc);
+      re = static_cast<int>(static_cast<int64_t>(c + 1) * E / rc);
+    } else {
+      const int64_t rest = A.total_rows - E;
+      rb = E + static_cast<int>(static_cast<int64_t>(c - rc) * rest / (g - rc));
+      re = E + static_cast<int>(static_cast<int64_t>(c - rc + 1) * rest / (g - rc));
+    }
+  } else {
+    cta_rows(A.total_rows, rb, re);
+  }
   for (int t0 = 0; t0 < A.T; t0 += TB) {
     const int tb = min(TB, A.T - t0);
     if (t0) __syncthreads();

@@ -66,6 +66,7 @@ struct moe_layer {
   float* comb = nullptr;      // [Tmax, L + F_sh] staged operand of the output projection
   void* xl16 = nullptr;       // [Tmax, L] 16-bit latent rows (grouped path B operand)
   void* h16 = nullptr;        // [Tmax*k, F] 16-bit expert activations (grouped path)
+  float* part = nullptr;      // split-K partial sums of the grouped dense GEMMs
   void* bout = nullptr;       // [Tmax, L + F_sh] 16-bit operand of the grouped output GEMM
   void* x_stage = nullptr;    // [Tmax, H] act dtype (host-buffer forward)
   void* out_stage = nullptr;
@@ -447,6 +448,8 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->comb), static_cast<size_t>(T) * (Lt + Fs + 64) * 4), "workspace");
     MOE_TRY_CUDA(L->alloc(&L->xl16, static_cast<size_t>(T) * (Lt + 64) * 2), "workspace");
     MOE_TRY_CUDA(L->alloc(&L->h16, P * F * 2), "workspace");
+    MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->part),
+                          static_cast<size_t>(UM_MAX_KSPLIT) * T * std::max(L->r_in, H) * 4), "workspace");
     MOE_TRY_CUDA(L->alloc(&L->x_stage, static_cast<size_t>(T) * H * adt), "workspace");
     MOE_TRY_CUDA(L->alloc(&L->out_stage, static_cast<size_t>(T) * H * adt), "workspace");
     MOE_TRY_CUDA(cudaStreamSynchronize(s), "create synchronise");
@@ -478,15 +481,31 @@ static size_t umma_config(UmmaArgs& a, int T) {
   a.n_tile = std::min(cap, (std::max(1, T) + 15) & ~15);
   const size_t budget = 220 * 1024;
   int st = UM_MAX_STAGES;
-  while (st > 2 && umma_plan(a.a_mode, gated, a.n_tile, st).total > budget) --st;
+  while (st > 3 && umma_plan(a.a_mode, gated, a.n_tile, st).total > budget) --st;
   a.stages = st;
   return umma_plan(a.a_mode, gated, a.n_tile, st).total;
 }
 
-static cudaError_t launch_umma(UmmaArgs& a, int T, int grid, cudaStream_t s) {
+// A grouped launch; a dense matrix with fewer 128-row tiles than SMs splits K
+// over several CTAs and sums the partials in a second, deterministic pass.
+static cudaError_t launch_umma(moe_layer* h, UmmaArgs& a, int T, cudaStream_t s) {
   const size_t smem = umma_config(a, T);
-  k_umma<<<grid, UM_THREADS, smem, s>>>(a);
-  return cudaGetLastError();
+  a.ksplit = 1;
+  if (!a.experts) {
+    const int mtiles = (a.n_rows + UM_M - 1) / UM_M, nkc = a.K / UM_KC;
+    int ks = (h->num_sms + mtiles - 1) / mtiles;
+    ks = std::min(ks, std::min(std::max(1, nkc / 4), UM_MAX_KSPLIT));
+    a.ksplit = std::max(1, ks);
+    a.part = h->part;
+  }
+  k_umma<<<h->num_sms, UM_THREADS, smem, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess && a.ksplit > 1) {
+    const int64_t n = static_cast<int64_t>(T) * a.n_rows;
+    k_umma_reduce<<<static_cast<int>(std::min<int64_t>((n + 255) / 256, h->num_sms * 8)), 256, 0, s>>>(a);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out, void* stream,
@@ -580,10 +599,11 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
         di.fuse_route = 1;
         di.route = ra;
         di.route_counter = h->route_counter;
-        int rc = 0;
-        while (rc < grid_in &&
-               static_cast<int64_t>(rc) * di.total_rows / grid_in < static_cast<int64_t>(E))
-          ++rc;
+        // router rows get half the average rows per CTA
+        const double share = static_cast<double>(E) / di.total_rows;
+        int rc = static_cast<int>(grid_in * share * 2.0 + 0.5);
+        rc = std::max(1, std::min(rc, std::min(E, grid_in - 1)));
+        if (grid_in < 2) rc = 1;
         di.route_ctas = rc;
         if (h->prefetch & 1) {
           di.prefetch_up = 1;
@@ -628,7 +648,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
         ua.out_col0 = col0;
         ua.k = k;
         ua.status = h->status;
-        if ((e = launch_umma(ua, T, h->num_sms, s)) != cudaSuccess) goto cuda_fail;
+        if ((e = launch_umma(h, ua, T, s)) != cudaSuccess) goto cuda_fail;
       }
     }
   }
@@ -723,7 +743,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     up.out_f32 = h->hbuf;
     up.status = h->status;
     mark(2);
-    if ((e = launch_umma(up, T, h->num_sms, s)) != cudaSuccess) goto cuda_fail;
+    if ((e = launch_umma(h, up, T, s)) != cudaSuccess) goto cuda_fail;
     mark(3);
     UmmaArgs dn = up;
     dn.n_rows = kin;
@@ -737,7 +757,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     dn.by_pair = 1;
     dn.act = -1;
     dn.out_f32 = h->pexp;
-    if ((e = launch_umma(dn, T, h->num_sms, s)) != cudaSuccess) goto cuda_fail;
+    if ((e = launch_umma(h, dn, T, s)) != cudaSuccess) goto cuda_fail;
   }
 
   // 5. combine + fc2 + shared down + residual
@@ -771,7 +791,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     ua.x = x; ua.x_dt = c.act_dtype; ua.out = out; ua.delta = delta;
     ua.pexp = h->pexp; ua.wts = h->wts; ua.add_combine = Lt ? 0 : 1;
     ua.status = h->status;
-    if ((e = launch_umma(ua, T, h->num_sms, s)) != cudaSuccess) goto cuda_fail;
+    if ((e = launch_umma(h, ua, T, s)) != cudaSuccess) goto cuda_fail;
   } else {
     DenseOutArgs dout{};
     dout.nseg = 0;

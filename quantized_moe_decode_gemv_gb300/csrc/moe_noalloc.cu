@@ -156,9 +156,7 @@ extern "C" moe_status moe_router_topk_noalloc(const void* x, int32_t T, int32_t 
   ra.mask_words = P > 256 ? (T + 31) / 32 : 0;
   di.fuse_route = 1;
   di.route_counter = counter;
-  int rc = 0;
-  while (rc < grid && static_cast<int64_t>(rc) * n_experts / grid < n_experts) ++rc;
-  di.route_ctas = rc;
+  di.route_ctas = grid;   // every CTA holds router rows
   const size_t smem = std::max(na_dense_smem(tb, hidden),
                                ROUTE_SMEM_BYTES + static_cast<size_t>(n_experts) * ra.mask_words * 4);
   switch (tb) {

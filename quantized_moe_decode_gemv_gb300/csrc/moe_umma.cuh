@@ -30,6 +30,7 @@ constexpr int UM_M = 128;       // weight rows per tile (MMA M)
 constexpr int UM_KC = 64;       // K elements per stage
 constexpr int UM_THREADS = 256;
 constexpr int UM_MAX_STAGES = 8;
+constexpr int UM_MAX_KSPLIT = 8;
 constexpr uint32_t UM_SPIN_LIMIT = 1u << 22;
 
 // canonical K-major no-swizzle layout of a [rows x 64] 16-bit tile:
@@ -71,7 +72,9 @@ struct UmmaArgs {
   int k;                    // top_k
   // ---- pipeline (host-chosen) ----
   int n_tile;               // tokens per MMA (multiple of 16, <= 256)
-  int stages;               // ring depth, 2..UM_MAX_STAGES
+  int stages;               // ring depth, 3..UM_MAX_STAGES
+  int ksplit;               // dense mode: K split over this many units (partials in `part`)
+  float* part;              // [ksplit, n_tokens, n_rows] fp32 partial sums (ksplit > 1)
   // ---- epilogue ----
   int epi;
   int act;                  // UE_ROWS: activation applied (-1: none)
@@ -248,8 +251,38 @@ __host__ __device__ inline UmmaPlan umma_plan(int a_mode, bool gated, int n_tile
   p.abuf = static_cast<uint32_t>(stages) * p.stage;
   const uint32_t abuf_bytes = a_mode == UA_DENSE ? 0u : 2u * (gated ? 2u : 1u) * UM_A_BYTES;
   p.tok = p.abuf + abuf_bytes;
-  p.total = p.tok + 256 * 4 + 64;
+  p.total = p.tok + 256 * 4 + 64;   // token table, 2 mbarriers, TMEM address
   return p;
+}
+
+// Final value of output row m for token/pair `pid` from its accumulator.
+__device__ __forceinline__ void umma_epilogue(const UmmaArgs& A, int pid, int m, float v, float vg,
+                                              bool gated) {
+  if (A.epi == UE_ROWS) {
+    // A (q) is the up projection, A2 (q2) the gate: act(gate, up)
+    if (A.act >= 0) v = gated ? act_fn(A.act, vg, v) : act_fn(A.act, 0.f, v);
+    if (A.out16)
+      A.out16[static_cast<int64_t>(pid) * A.n_rows + m] = st16_bits(v, A.mma_dt);
+    else
+      A.out_f32[static_cast<int64_t>(pid) * A.n_rows + m] = v;
+  } else if (A.epi == UE_DENSE_IN) {
+    const int col = A.out_col0 + m;
+    A.out_f32[static_cast<int64_t>(pid) * A.out_ld + col] = v;
+    if (A.out16 && col >= A.c16_0 && col < A.c16_1)
+      A.out16[static_cast<int64_t>(pid) * A.out16_ld + (col - A.c16_0)] = st16_bits(v, A.mma_dt);
+  } else {
+    const int t = pid;
+    if (A.add_combine) {
+      float y = 0.f;
+      for (int p = 0; p < A.k; ++p)
+        y = fmaf(A.wts[t * A.k + p], A.pexp[static_cast<int64_t>(t * A.k + p) * A.n_rows + m], y);
+      v += y;
+    }
+    const int64_t e = static_cast<int64_t>(t) * A.n_rows + m;
+    const float xv = ld16(A.x, e, A.x_dt);
+    reinterpret_cast<unsigned short*>(A.out)[e] = st16_bits(xv + v, A.x_dt);
+    if (A.delta) A.delta[e] = v;
+  }
 }
 
 __global__ void __launch_bounds__(UM_THREADS, 1) k_umma(const UmmaArgs A) {
@@ -259,7 +292,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) k_umma(const UmmaArgs A) {
   char* base = um_smem;
   int* tok_row = reinterpret_cast<int*>(base + P.tok);        // [n_tile] source rows
   uint64_t* mbar = reinterpret_cast<uint64_t*>(base + P.tok + 256 * 4);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base + P.tok + 256 * 4 + 16);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base + P.tok + 256 * 4 + 32);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ncols = gated ? 512 : 256;
   const int S = A.stages;
@@ -274,13 +307,16 @@ __global__ void __launch_bounds__(UM_THREADS, 1) k_umma(const UmmaArgs A) {
   }
   if (tid == 0) {
     mbar_init(smem_u32(&mbar[0]), 1);
+    mbar_init(smem_u32(&mbar[1]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  uint32_t commits = 0;      // tcgen05.commit operations issued so far (all waited in order)
+  // tcgen05.commit operations issued so far on each mbarrier; chunk c of a
+  // tile commits on mbarrier c & 1, and every commit is waited for in order
+  uint32_t commits[2] = {0u, 0u}, waited[2] = {0u, 0u};
   bool ok = true;
 
   const int n_groups = A.experts ? A.meta[0] : 1;
@@ -288,8 +324,13 @@ __global__ void __launch_bounds__(UM_THREADS, 1) k_umma(const UmmaArgs A) {
   const int nkc = A.K / UM_KC;
   const int ngr = A.K / A.G;
 
-  for (int unit = blockIdx.x; ok && unit < n_groups * mtiles; unit += gridDim.x) {
-    const int g = unit / mtiles, mt = unit - g * mtiles;
+  const int nsplit = A.ksplit > 1 ? A.ksplit : 1;
+  for (int unit = blockIdx.x; ok && unit < n_groups * mtiles * nsplit; unit += gridDim.x) {
+    const int split = unit % nsplit;
+    const int gm = unit / nsplit;
+    const int g = gm / mtiles, mt = gm - g * mtiles;
+    const int kc_begin = static_cast<int>(static_cast<int64_t>(split) * nkc / nsplit);
+    const int nit = static_cast<int>(static_cast<int64_t>(split + 1) * nkc / nsplit) - kc_begin;
     const UmmaGroup G = umma_group(A, g);
     const int m0 = mt * UM_M;
     for (int n0 = 0; ok && n0 < G.n; n0 += A.n_tile) {
@@ -307,9 +348,9 @@ __global__ void __launch_bounds__(UM_THREADS, 1) k_umma(const UmmaArgs A) {
       }
       __syncthreads();
 
-      // issue the copies of K-chunk kc into ring slot kc % S
-      auto issue = [&](int kc) {
-        char* slot = base + static_cast<size_t>(kc % S) * P.stage;
+      // issue the copies of K-chunk kc (the tile's it-th) into ring slot it % S
+      auto issue = [&](int kc, int it) {
+        char* slot = base + static_cast<size_t>(it % S) * P.stage;
         const uint32_t sa = smem_u32(slot), sbb = smem_u32(slot + P.a_raw);
         const int k0 = kc * UM_KC;
         if (A.a_mode == UA_DENSE) {
@@ -374,13 +415,13 @@ __global__ void __launch_bounds__(UM_THREADS, 1) k_umma(const UmmaArgs A) {
         }
       };
 
-      // dequantise the int4 codes of ring slot kc % S into A tile buffer kc & 1
-      auto dequant = [&](int kc) {
-        const char* slot = base + static_cast<size_t>(kc % S) * P.stage;
+      // dequantise the int4 codes of ring slot it % S into A tile buffer it & 1
+      auto dequant = [&](int it) {
+        const char* slot = base + static_cast<size_t>(it % S) * P.stage;
         const int r = tid >> 1, hh = tid & 1;
         for (int gsel = 0; gsel < (gated ? 2 : 1); ++gsel) {
           const char* raw = slot + gsel * (UM_CODE_BYTES + UM_SB_BYTES);
-          char* dst = base + P.abuf + static_cast<size_t>((kc & 1) + 2 * gsel) * UM_A_BYTES;
+          char* dst = base + P.abuf + static_cast<size_t>((it & 1) + 2 * gsel) * UM_A_BYTES;
           const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 32 + hh * 16);
           const uint32_t sbw = *reinterpret_cast<const uint32_t*>(
               raw + UM_CODE_BYTES + r * 8 + ((A.G == 32) ? 4 * hh : 0));
@@ -402,51 +443,60 @@ __global__ void __launch_bounds__(UM_THREADS, 1) k_umma(const UmmaArgs A) {
         }
       };
 
-      for (int s = 0; s < S - 1; ++s) {
-        if (s < nkc) issue(s);
+      // Ring protocol, chunk kc in slot kc % S: the copies of chunks up to
+      // kc + S - 3 are in flight while chunk kc is computed.  Before a slot or
+      // an A buffer is reused, the MMAs of chunk kc - 2 (which read them) must
+      // be done -- two chunks back, so the tensor core's latency overlaps one
+      // chunk of staging.
+      auto wait_commit = [&](int b) -> bool {   // oldest unwaited commit on mbarrier b
+        bool w = true;
+        if (tid == 0) w = mbar_wait(smem_u32(&mbar[b]), waited[b] & 1u);
+        ++waited[b];
+        return w;
+      };
+      for (int s = 0; s < S - 2; ++s) {
+        if (s < nit) issue(kc_begin + s, s);
         cp_async_commit();
       }
-      for (int kc = 0; kc < nkc; ++kc) {
-        if (kc > 0) {
-          // MMAs of chunk kc-1 done: its ring slot and A buffer (kc-1)&1 may be
-          // overwritten, and A buffer kc&1 (read by chunk kc-2) is free too
-          bool w = true;
-          if (tid == 0) w = mbar_wait(smem_u32(&mbar[0]), (commits - 1) & 1u);
-          if (!__syncthreads_and(w)) { ok = false; break; }
-        }
-        if (kc + S - 1 < nkc) issue(kc + S - 1);
+      for (int it = 0; it < nit; ++it) {
+        const int kc = kc_begin + it;
+        bool w = true;
+        if (it >= 2) w = wait_commit(it & 1);       // chunk kc - 2 committed on mbarrier kc & 1
+        cp_async_wait(S - 3);                        // this thread's copies of chunk kc
+        if (!__syncthreads_and(w)) { ok = false; break; }
+        if (it + S - 2 < nit) issue(kc + S - 2, it + S - 2);   // into slot (it - 2) % S
         cp_async_commit();
-        cp_async_wait(S - 1);
-        __syncthreads();
-        if (A.a_mode == UA_INT4) dequant(kc);
+        if (A.a_mode == UA_INT4) dequant(it);
         fence_proxy_async();
         __syncthreads();
         if (tid == 0) {
           tc_fence_after();
-          const char* slot = base + static_cast<size_t>(kc % S) * P.stage;
+          const char* slot = base + static_cast<size_t>(it % S) * P.stage;
           const uint32_t a_addr = A.a_mode == UA_DENSE
                                       ? smem_u32(slot)
-                                      : smem_u32(base + P.abuf + static_cast<size_t>(kc & 1) * UM_A_BYTES);
+                                      : smem_u32(base + P.abuf + static_cast<size_t>(it & 1) * UM_A_BYTES);
           const uint32_t b_addr = smem_u32(slot + P.a_raw);
 #pragma unroll
           for (int kk = 0; kk < UM_KC / 16; ++kk) {
             const uint64_t ad = umma_desc(a_addr + kk * 2 * UM_LBO);
             const uint64_t bd = umma_desc(b_addr + kk * 2 * UM_LBO);
-            umma_f16(tmem, ad, bd, idesc, (kc | kk) ? 1u : 0u);
+            umma_f16(tmem, ad, bd, idesc, (it | kk) ? 1u : 0u);
             if (gated) {
-              const uint32_t a2 = smem_u32(base + P.abuf + static_cast<size_t>((kc & 1) + 2) * UM_A_BYTES);
-              umma_f16(tmem + 256, umma_desc(a2 + kk * 2 * UM_LBO), bd, idesc, (kc | kk) ? 1u : 0u);
+              const uint32_t a2 = smem_u32(base + P.abuf + static_cast<size_t>((it & 1) + 2) * UM_A_BYTES);
+              umma_f16(tmem + 256, umma_desc(a2 + kk * 2 * UM_LBO), bd, idesc, (it | kk) ? 1u : 0u);
             }
           }
-          umma_commit(smem_u32(&mbar[0]));
+          umma_commit(smem_u32(&mbar[it & 1]));
         }
-        ++commits;
+        ++commits[it & 1];
       }
       if (!ok) break;
       cp_async_wait(0);
       {
+        // the last (up to two) chunks' MMAs
         bool w = true;
-        if (tid == 0) w = mbar_wait(smem_u32(&mbar[0]), (commits - 1) & 1u);
+        for (int b = 0; b < 2; ++b)
+          while (waited[b] < commits[b]) w = wait_commit(b) && w;
         if (!__syncthreads_and(w)) { ok = false; break; }
       }
       tc_fence_after();
@@ -463,31 +513,10 @@ __global__ void __launch_bounds__(UM_THREADS, 1) k_umma(const UmmaArgs A) {
           const int n = c0 + i;
           if (n >= nvalid) break;
           const int pid = A.experts ? A.meta[2 + 2 * A.umax + G.p0 + n0 + n] : n0 + n;
-          float v = acc[i];
-          if (A.epi == UE_ROWS) {
-            // A (q) is the up projection, A2 (q2) the gate: act(gate, up)
-            if (A.act >= 0) v = gated ? act_fn(A.act, accg[i], v) : act_fn(A.act, 0.f, v);
-            if (A.out16)
-              A.out16[static_cast<int64_t>(pid) * A.n_rows + m] = st16_bits(v, A.mma_dt);
-            else
-              A.out_f32[static_cast<int64_t>(pid) * A.n_rows + m] = v;
-          } else if (A.epi == UE_DENSE_IN) {
-            const int col = A.out_col0 + m;
-            A.out_f32[static_cast<int64_t>(pid) * A.out_ld + col] = v;
-            if (A.out16 && col >= A.c16_0 && col < A.c16_1)
-              A.out16[static_cast<int64_t>(pid) * A.out16_ld + (col - A.c16_0)] = st16_bits(v, A.mma_dt);
+          if (A.ksplit > 1) {
+            A.part[(static_cast<int64_t>(split) * A.n_tokens + pid) * A.n_rows + m] = acc[i];
           } else {
-            const int t = pid;
-            if (A.add_combine) {
-              float y = 0.f;
-              for (int p = 0; p < A.k; ++p)
-                y = fmaf(A.wts[t * A.k + p], A.pexp[static_cast<int64_t>(t * A.k + p) * A.n_rows + m], y);
-              v += y;
-            }
-            const int64_t e = static_cast<int64_t>(t) * A.n_rows + m;
-            const float xv = ld16(A.x, e, A.x_dt);
-            reinterpret_cast<unsigned short*>(A.out)[e] = st16_bits(xv + v, A.x_dt);
-            if (A.delta) A.delta[e] = v;
+            umma_epilogue(A, pid, m, acc[i], gated ? accg[i] : 0.f, gated);
           }
         }
       }
@@ -500,14 +529,29 @@ __global__ void __launch_bounds__(UM_THREADS, 1) k_umma(const UmmaArgs A) {
   cp_async_wait(0);
   if (!ok && tid == 0) {
     atomicOr(A.status, STATUS_TIMEOUT);
-    // bounded wait for MMAs still in flight before releasing TMEM
-    if (commits) mbar_wait(smem_u32(&mbar[0]), (commits - 1) & 1u);
+    // bounded waits for MMAs still in flight before releasing TMEM
+    for (int b = 0; b < 2; ++b)
+      while (waited[b] < commits[b]) { mbar_wait(smem_u32(&mbar[b]), waited[b] & 1u); ++waited[b]; }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols));
+  }
+}
+
+// Sums the split-K partials of a dense grouped launch and applies its epilogue.
+__global__ void k_umma_reduce(const UmmaArgs A) {
+  griddep_wait();
+  griddep_launch();
+  const int64_t n = static_cast<int64_t>(A.n_tokens) * A.n_rows;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(i / A.n_rows), m = static_cast<int>(i - static_cast<int64_t>(t) * A.n_rows);
+    float v = 0.f;
+    for (int sp = 0; sp < A.ksplit; ++sp) v += A.part[static_cast<int64_t>(sp) * n + i];
+    umma_epilogue(A, t, m, v, 0.f, false);
   }
 }
 
