@@ -72,8 +72,22 @@ typedef enum moe_router {
 
 typedef enum moe_dtype { MOE_DTYPE_BF16 = 0, MOE_DTYPE_FP16 = 1, MOE_DTYPE_FP32 = 2 } moe_dtype;
 
-/* Path used for the routed experts.  AUTO picks the dequant-gemv path. */
-typedef enum moe_path { MOE_PATH_AUTO = 0, MOE_PATH_GEMV = 1, MOE_PATH_GROUPED = 2 } moe_path;
+/* Kernel schedule of a forward.
+ *   FUSED    one persistent cooperative kernel runs the whole layer; the
+ *            routing-independent shared-expert rows stream while the routed
+ *            chain (router -> top-k -> expert up -> expert down -> combine)
+ *            waits on its dependencies.  CUDA cores; for few token rows.
+ *   GEMV     the same arithmetic as five stream-ordered kernels.
+ *   GROUPED  row-grouped tcgen05 GEMMs for the experts and dense projections
+ *            (many token rows per forward).
+ *   AUTO     GROUPED when T >= 64 (MOE_GROUPED_MIN_T), else FUSED when
+ *            T <= MOE_FUSED_MAX_T (default 0: off), else GEMV. */
+typedef enum moe_path {
+  MOE_PATH_AUTO = 0,
+  MOE_PATH_GEMV = 1,
+  MOE_PATH_GROUPED = 2,
+  MOE_PATH_FUSED = 3
+} moe_path;
 
 typedef struct moe_layer_config {
   int32_t hidden;        /* H: width of x and out; multiple of 64 */
@@ -193,6 +207,14 @@ moe_status moe_layer_profile(moe_layer *h, int32_t enable);
  * stage durations in milliseconds to ms[] (host pointer).  Returns
  * MOE_ERR_INVALID_ARG if profiling is off or no forward was profiled. */
 moe_status moe_layer_stage_times(moe_layer *h, float *ms, int32_t n);
+
+/* Path (moe_path, never AUTO) a forward of T rows takes on this handle, or
+ * -1 for a NULL handle or T outside 1..max_tokens.  Pure host query. */
+int32_t moe_layer_path_for(const moe_layer *h, int32_t T);
+
+/* Kernel launches the handle's last forward made (0 before the first).
+ * Pure host query. */
+int32_t moe_layer_last_launch_count(const moe_layer *h);
 
 /* Bytes of device memory the handle owns (weights + workspace). */
 int64_t moe_layer_device_bytes(const moe_layer *h);

@@ -25,7 +25,7 @@ STATUS_NAMES = ["MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR
 ACT = {"swiglu": 0, "relu2": 1}
 ROUTER = {"softmax": 0, "sigmoid": 1}
 DTYPE = {"bf16": 0, "fp16": 1, "fp32": 2}
-PATH = {"auto": 0, "gemv": 1, "grouped": 2}
+PATH = {"auto": 0, "gemv": 1, "grouped": 2, "fused": 3}
 NUM_STAGES = 5
 STAGE_NAMES = ["dense_in", "route", "expert_up", "expert_down", "dense_out"]
 
@@ -77,6 +77,8 @@ SIGNATURES = {
     "moe_layer_profile": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
     "moe_layer_stage_times": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_float),
                                              ctypes.c_int32]),
+    "moe_layer_path_for": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_int32]),
+    "moe_layer_last_launch_count": (ctypes.c_int32, [ctypes.c_void_p]),
     "moe_layer_device_bytes": (ctypes.c_int64, [ctypes.c_void_p]),
     "moe_layer_destroy": (ctypes.c_int, [ctypes.c_void_p]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -328,6 +330,17 @@ class MoELayer:
 
     def device_bytes(self) -> int:
         return load_library().moe_layer_device_bytes(self.handle)
+
+    def path_for(self, T: int) -> str:
+        """The path ("fused", "gemv" or "grouped") a forward of T rows takes."""
+        v = load_library().moe_layer_path_for(self.handle, int(T))
+        if v < 0:
+            raise MoEError(f"no path for T={T}")
+        return {p: n for n, p in PATH.items()}[v]
+
+    def last_launch_count(self) -> int:
+        """Kernel launches of the last forward."""
+        return int(load_library().moe_layer_last_launch_count(self.handle))
 
     def close(self):
         if getattr(self, "handle", None):

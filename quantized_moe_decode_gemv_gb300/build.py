@@ -20,7 +20,10 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libmoe_gb300.so")
 
-SOURCES = ["moe_layer.cu", "moe_noalloc.cu"]
+# (source, object name, extra flags): the persistent kernel is compiled once per
+# staging width so that its instantiations build in parallel
+SOURCES = [("moe_layer.cu", "moe_layer", []), ("moe_noalloc.cu", "moe_noalloc", [])] + [
+    ("moe_fused.cu", f"moe_fused_tb{tb}", [f"-DFZ_TB={tb}"]) for tb in (1, 2, 4, 8)]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-warn-spills"]
@@ -44,10 +47,10 @@ def build(verbose: bool = False) -> str:
     os.makedirs(BUILD_DIR, exist_ok=True)
     nvcc = _nvcc()
     objs, cmds = [], []
-    for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
+    for src, name, extra in SOURCES:
+        obj = os.path.join(BUILD_DIR, name + ".o")
         objs.append(obj)
-        cmds.append([nvcc, *ARCH, *FLAGS, "-I", INCLUDE, "-I", CSRC, "-c",
+        cmds.append([nvcc, *ARCH, *FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-c",
                      os.path.join(CSRC, src), "-o", obj])
     with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, len(cmds))) as ex:
         logs = list(ex.map(_run, cmds))

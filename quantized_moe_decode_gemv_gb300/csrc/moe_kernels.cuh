@@ -33,6 +33,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
+#include <cstdio>
 
 namespace moe {
 
@@ -518,7 +519,7 @@ static __device__ __noinline__ void route_block(const RouteArgs& A, int* smem) {
 
 constexpr int ROUTE_THREADS = 256;
 
-static __global__ void __launch_bounds__(ROUTE_THREADS) k_route(const RouteArgs A) {
+static __global__ void __launch_bounds__(ROUTE_THREADS) k_route(const __grid_constant__ RouteArgs A) {
   extern __shared__ int route_smem[];
   unsigned long long t0 = 0, t1 = 0;
   if (A.debug_times) t0 = global_ns();
@@ -789,7 +790,7 @@ template <int TB>
 constexpr int dense_min_blocks() { return 2; }
 
 template <int TB>
-__global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_in(const DenseInArgs A) {
+__global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_in(const __grid_constant__ DenseInArgs A) {
   extern __shared__ float4 smem4[];
   float* xs = reinterpret_cast<float*>(smem4);
   float* red = xs + TB * A.K;
@@ -866,7 +867,7 @@ __global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_in(const D
 }
 
 template <int TB>
-__global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_out(const DenseOutArgs A) {
+__global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_out(const __grid_constant__ DenseOutArgs A) {
   extern __shared__ float4 smem4[];
   float* xs = reinterpret_cast<float*>(smem4);
   float* red = xs + TB * A.K;
@@ -1015,7 +1016,7 @@ template <int PB, bool GATED>
 constexpr int expert_min_blocks() { return PB <= 2 ? (GATED ? 2 : 3) : 2; }
 
 template <int PB, bool GATED>
-__global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(const ExpertArgs A) {
+__global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(const __grid_constant__ ExpertArgs A) {
   extern __shared__ float4 smem4[];
   const int K = A.K, K4 = K >> 2, nchunk = K >> 5;
   float* xsum = reinterpret_cast<float*>(smem4 + PB * K4);   // [PB][nchunk]
@@ -1078,7 +1079,12 @@ __global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(c
         const int64_t row = A.xin_by_pair ? pid : (pid / A.k);
         const int64_t base = A.xin_off + row * A.xin_stride + 4 * f4;
         if (A.xin_dt == DT_FP32) {
-          v = *reinterpret_cast<const float4*>(static_cast<const float*>(A.xin) + base);
+          const float* src = static_cast<const float*>(A.xin) + base;
+          if (((A.xin_off | A.xin_stride) & 3) == 0) {
+            v = *reinterpret_cast<const float4*>(src);
+          } else {   // latent columns of dense_in after a router width that is not a multiple of 4
+            v.x = src[0]; v.y = src[1]; v.z = src[2]; v.w = src[3];
+          }
         } else {
           v.x = ld16(A.xin, base, A.xin_dt); v.y = ld16(A.xin, base + 1, A.xin_dt);
           v.z = ld16(A.xin, base + 2, A.xin_dt); v.w = ld16(A.xin, base + 3, A.xin_dt);
@@ -1183,7 +1189,7 @@ __global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(c
   }
 }
 
-static __global__ void __launch_bounds__(NT) k_combine(const CombineArgs A) {
+static __global__ void __launch_bounds__(NT) k_combine(const __grid_constant__ CombineArgs A) {
   // the output projection's pre-wait phase reads only weights: let it launch now
   griddep_launch();
   griddep_wait();

@@ -13,6 +13,7 @@
 #include "moe_layer.h"
 #include "moe_kernels.cuh"
 #include "moe_umma.cuh"
+#include "moe_fused.cuh"
 
 using namespace moe;
 
@@ -68,6 +69,8 @@ struct moe_layer {
   void* h16 = nullptr;        // [Tmax*k, F] 16-bit expert activations (grouped path)
   float* part = nullptr;      // split-K partial sums of the grouped dense GEMMs
   void* bout = nullptr;       // [Tmax, L + F_sh] 16-bit operand of the grouped output GEMM
+  int* fsync = nullptr;       // FZ_WORDS phase counters of the persistent kernel
+  float* sdbuf = nullptr;     // [Tmax, H] shared-expert down output (persistent kernel)
   void* x_stage = nullptr;    // [Tmax, H] act dtype (host-buffer forward)
   void* out_stage = nullptr;
 
@@ -80,6 +83,11 @@ struct moe_layer {
   int umax = 0;
   int kin = 0;
   int grouped_min_t = 64;
+  int fused_max_t = 0;    // AUTO: the persistent kernel for T <= this (below grouped_min_t)
+  int fused_sd_mid = 2;   // persistent kernel: shared-down chunks between the expert up and down rows
+  FusedLaunchCache fused_grid[4][2];  // cooperative grid of k_fused<TB, ., gated>
+  int last_launches = 0;  // kernel launches of the last forward
+  unsigned long long* fz_trace = nullptr;   // diagnostics (MOE_FUSED_TRACE): phase stamps
   int use_pdl = 1;        // programmatic dependent launch between the gemv-path kernels
   int expert_pb = 2;      // max token slots per pass of the gemv-path expert kernels
   int fuse_route = 1;     // routing in the last router CTA of the dense pass (0: own kernel)
@@ -371,6 +379,9 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   L->umax = std::min(E, T * k);
   if (const char* env = std::getenv("MOE_GROUPED_MIN_T")) L->grouped_min_t = std::max(1, std::atoi(env));
   if (const char* env = std::getenv("MOE_PDL")) L->use_pdl = std::atoi(env) != 0;
+  if (const char* env = std::getenv("MOE_FUSED_MAX_T")) L->fused_max_t = std::atoi(env);
+  if (const char* env = std::getenv("MOE_SD_MID")) L->fused_sd_mid = std::max(0, std::atoi(env));
+  const bool want_trace = std::getenv("MOE_FUSED_TRACE") && std::atoi(std::getenv("MOE_FUSED_TRACE"));
   if (const char* env = std::getenv("MOE_PREFETCH")) L->prefetch = std::atoi(env);
   if (const char* env = std::getenv("MOE_EXPERT_PB")) L->expert_pb = std::max(1, std::min(8, std::atoi(env)));
   if (const char* env = std::getenv("MOE_FUSE_ROUTE")) L->fuse_route = std::atoi(env) != 0;
@@ -438,6 +449,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->ids), P * 4), "workspace");
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->wts), P * 4), "workspace");
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->meta), (2 + 2 * static_cast<size_t>(L->umax) + P) * 4), "workspace");
+    MOE_TRY_CUDA(cudaMemsetAsync(L->meta, 0, (2 + 2 * static_cast<size_t>(L->umax) + P) * 4, s), "workspace clear");
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->hbuf), P * F * 4), "workspace");
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->pexp), P * kin * 4), "workspace");
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->status), 4), "workspace");
@@ -450,6 +462,11 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     MOE_TRY_CUDA(L->alloc(&L->h16, P * F * 2), "workspace");
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->part),
                           static_cast<size_t>(UM_MAX_KSPLIT) * T * std::max(L->r_in, H) * 4), "workspace");
+    MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->fsync), FZ_WORDS * FZ_SYNC_STRIDE * 4), "workspace");
+    MOE_TRY_CUDA(cudaMemsetAsync(L->fsync, 0, FZ_WORDS * FZ_SYNC_STRIDE * 4, s), "counter clear");
+    if (want_trace)
+      MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->fz_trace), 4096 * FZ_TRACE * 8), "trace");
+    MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->sdbuf), static_cast<size_t>(T) * H * 4), "workspace");
     MOE_TRY_CUDA(L->alloc(&L->x_stage, static_cast<size_t>(T) * H * adt), "workspace");
     MOE_TRY_CUDA(L->alloc(&L->out_stage, static_cast<size_t>(T) * H * adt), "workspace");
     MOE_TRY_CUDA(cudaStreamSynchronize(s), "create synchronise");
@@ -488,7 +505,7 @@ static size_t umma_config(UmmaArgs& a, int T) {
 
 // A grouped launch; a dense matrix with fewer 128-row tiles than SMs splits K
 // over several CTAs and sums the partials in a second, deterministic pass.
-static cudaError_t launch_umma(moe_layer* h, UmmaArgs& a, int T, cudaStream_t s) {
+static cudaError_t launch_umma(moe_layer* h, UmmaArgs& a, int T, cudaStream_t s, int* nl) {
   const size_t smem = umma_config(a, T);
   a.ksplit = 1;
   if (!a.experts) {
@@ -500,13 +517,105 @@ static cudaError_t launch_umma(moe_layer* h, UmmaArgs& a, int T, cudaStream_t s)
   }
   k_umma<<<h->num_sms, UM_THREADS, smem, s>>>(a);
   cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) ++*nl;
   if (e == cudaSuccess && a.ksplit > 1) {
     const int64_t n = static_cast<int64_t>(T) * a.n_rows;
     k_umma_reduce<<<static_cast<int>(std::min<int64_t>((n + 255) / 256, h->num_sms * 8)), 256, 0, s>>>(a);
     e = cudaGetLastError();
+    if (e == cudaSuccess) ++*nl;
   }
   return e;
 }
+
+}  // extern "C"
+
+// Plan of a persistent-kernel launch: staged token rows per pass, ring slots
+// and slot size, and the shared memory of one CTA.
+struct FusedPlan {
+  int tb = 0, slots = 0, slot_bytes = 0;
+  size_t smem = 0;
+};
+
+static FusedPlan fused_plan(const moe_layer* h, int T, int mask_words) {
+  const moe_layer_config& c = h->cfg;
+  FusedPlan fp;
+  const int H = c.hidden, Fs = c.shared_ffn, L = c.latent, F = c.expert_ffn, kin = h->kin;
+  const int rd = dt_size(c.router_dtype), ad = dt_size(c.act_dtype);
+  // a slot holds at least one row of every dense matrix and of every expert matrix
+  int row = std::max(H * rd, H * ad);
+  if (Fs) row = std::max(row, Fs * ad);
+  if (L) row = std::max(row, L * ad);
+  const int gm = c.act == MOE_ACT_SWIGLU ? 2 : 1;
+  row = std::max(row, gm * (kin / 2 + (kin / c.group_size) * 4) + 32);
+  row = std::max(row, F / 2 + (F / c.group_size) * 4 + 16);
+  const int sb = std::max(16384, (row + 127) & ~127);
+  const size_t route = ROUTE_SMEM_BYTES + static_cast<size_t>(c.n_experts) * mask_words * 4;
+  for (int tb = pow2_at_least(T, 8); tb >= 1; tb >>= 1) {
+    const size_t base = fused_smem_bytes(tb, 0, sb, H, Fs, L, kin, F, route);
+    // two CTAs per SM when three or more slots fit beside the staging, else one
+    const size_t two = 112 * 1024, one = static_cast<size_t>(kSmemMax) - 2048;
+    size_t budget = (tb < 8 && base + 3ull * sb <= two) ? two : one;
+    if (base + 2ull * sb > budget) continue;
+    fp.tb = tb;
+    fp.slot_bytes = sb;
+    fp.slots = static_cast<int>(std::min<size_t>(FZ_MAX_SLOTS, (budget - base) / sb));
+    fp.smem = fused_smem_bytes(tb, fp.slots, sb, H, Fs, L, kin, F, route);
+    return fp;
+  }
+  return fp;
+}
+
+static cudaError_t launch_fused(moe_layer* h, const FusedArgs& a, int tb, size_t smem, bool gated,
+                                cudaStream_t s) {
+  switch (tb) {
+    case 1: return fused_launch_tb1(a, gated, smem, h->num_sms, &h->fused_grid[0][gated], s);
+    case 2: return fused_launch_tb2(a, gated, smem, h->num_sms, &h->fused_grid[1][gated], s);
+    case 4: return fused_launch_tb4(a, gated, smem, h->num_sms, &h->fused_grid[2][gated], s);
+    default: return fused_launch_tb8(a, gated, smem, h->num_sms, &h->fused_grid[3][gated], s);
+  }
+}
+
+// Diagnostics: per phase stamp, the min / median / max over CTAs of the time
+// since the earliest kernel start (microseconds).
+static void print_fused_trace(moe_layer* h, cudaStream_t s) {
+  const int G = 4096;
+  std::vector<unsigned long long> t(static_cast<size_t>(G) * FZ_TRACE);
+  if (cudaMemcpyAsync(t.data(), h->fz_trace, t.size() * 8, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return;
+  unsigned long long t0 = ~0ull;
+  int n = 0;
+  for (int c = 0; c < G; ++c)
+    if (t[static_cast<size_t>(c) * FZ_TRACE]) { t0 = std::min(t0, t[static_cast<size_t>(c) * FZ_TRACE]); n = c + 1; }
+  std::fprintf(stderr, "fused trace (%d CTAs, us since first start: min/med/max; CTA 0):\n", n);
+  for (int i = 0; i < 13; ++i) {
+    std::vector<double> v;
+    for (int c = 1; c < n; ++c)
+      if (t[static_cast<size_t>(c) * FZ_TRACE + i]) v.push_back((t[static_cast<size_t>(c) * FZ_TRACE + i] - t0) * 1e-3);
+    std::sort(v.begin(), v.end());
+    const double c0 = t[i] ? (t[i] - t0) * 1e-3 : -1.0;
+    if (v.empty())
+      std::fprintf(stderr, "  stamp %2d: -  (cta0 %.2f)\n", i, c0);
+    else
+      std::fprintf(stderr, "  stamp %2d: %7.2f %7.2f %7.2f  (cta0 %.2f)\n", i, v.front(), v[v.size() / 2],
+                   v.back(), c0);
+  }
+}
+
+// The path a forward of T rows takes (never AUTO).
+static int choose_path(const moe_layer* h, int T) {
+  if (h->path == MOE_PATH_GROUPED || (h->path == MOE_PATH_AUTO && T >= h->grouped_min_t))
+    return MOE_PATH_GROUPED;
+  if (h->path == MOE_PATH_FUSED || (h->path == MOE_PATH_AUTO && T <= h->fused_max_t)) {
+    const int P = T * h->cfg.top_k;
+    const int W = (T + 31) / 32;
+    const int mw = (P > 256 && static_cast<int64_t>(h->cfg.n_experts) * W * 4 <= 160 * 1024) ? W : 0;
+    if (fused_plan(h, T, mw).tb > 0) return MOE_PATH_FUSED;
+  }
+  return MOE_PATH_GEMV;
+}
+
+extern "C" {
 
 static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out, void* stream,
                                int32_t* ext_ids, float* ext_w, float* delta) {
@@ -524,8 +633,9 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     h->last_error = "x and out overlap";
     return MOE_ERR_INVALID_ARG;
   }
-  const bool grouped =
-      h->path == MOE_PATH_GROUPED || (h->path == MOE_PATH_AUTO && T >= h->grouped_min_t);
+  const int path = choose_path(h, T);
+  const bool grouped = path == MOE_PATH_GROUPED;
+  int nl = 0;   // kernel launches of this forward
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int H = c.hidden, E = c.n_experts, k = c.top_k, F = c.expert_ffn, Lt = c.latent;
   const int Fs = c.shared_ffn, kin = h->kin;
@@ -566,6 +676,86 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     const int P = T * k;
     const int W = (T + 31) / 32;
     ra.mask_words = (P > 256 && static_cast<int64_t>(E) * W * 4 <= 160 * 1024) ? W : 0;
+  }
+  const bool fused = path == MOE_PATH_FUSED;
+  const FusedPlan fzp = fused ? fused_plan(h, T, ra.mask_words) : FusedPlan{};
+  if (fused && fzp.tb > 0) {
+    // the whole layer as one persistent kernel
+    FusedArgs fa{};
+    fa.T = T;
+    fa.H = H; fa.E = E; fa.L = Lt; fa.Fs = Fs; fa.k = k;
+    fa.act = c.act;
+    fa.x = x;
+    fa.x_dt = c.act_dtype;
+    fa.router_w = h->router_w;
+    fa.router_dt = c.router_dtype;
+    fa.fc1 = h->fc1;
+    fa.sh_gate = h->sh_gate;
+    fa.sh_up = h->sh_up;
+    fa.sh_down = h->sh_down;
+    fa.fc2 = h->fc2;
+    fa.dense_in = h->dense_in;
+    fa.din_rows = h->r_in;
+    fa.off_fc1 = h->off_fc1;
+    fa.off_shg = h->off_shg;
+    fa.off_shu = h->off_shu;
+    fa.route = ra;
+    ExpertArgs& up = fa.up;
+    up.n_rows = F;
+    up.K = kin;
+    up.G = c.group_size;
+    up.q = h->up_q;
+    up.sb = h->up_sb;
+    up.q_gate = gated ? h->gate_q : nullptr;
+    up.sb_gate = gated ? h->gate_sb : nullptr;
+    up.s_dt = c.scale_dtype;
+    up.act = c.act;
+    up.meta = h->meta;
+    up.umax = h->umax;
+    up.k = k;
+    if (Lt) {
+      up.xin = h->dense_in; up.xin_dt = DT_FP32; up.xin_stride = h->r_in; up.xin_off = h->off_fc1;
+    } else {
+      up.xin = x; up.xin_dt = c.act_dtype; up.xin_stride = H; up.xin_off = 0;
+    }
+    up.xin_by_pair = 0;
+    up.out = h->hbuf;
+    ExpertArgs& dn = fa.dn;
+    dn = up;
+    dn.n_rows = kin;
+    dn.K = F;
+    dn.q = h->down_q;
+    dn.sb = h->down_sb;
+    dn.q_gate = nullptr;
+    dn.sb_gate = nullptr;
+    dn.act = -1;
+    dn.xin = h->hbuf; dn.xin_dt = DT_FP32; dn.xin_stride = F; dn.xin_off = 0;
+    dn.xin_by_pair = 1;
+    dn.out = h->pexp;
+    fa.sdbuf = h->sdbuf;
+    fa.pexp = h->pexp;
+    fa.wts = h->wts;
+    fa.ybuf = h->comb;
+    fa.out = out;
+    fa.delta = delta;
+    fa.sync = h->fsync;
+    fa.status = h->status;
+    fa.slots = fzp.slots;
+    fa.slot_bytes = fzp.slot_bytes;
+    fa.sd_mid = h->fused_sd_mid;
+    fa.trace = h->fz_trace;
+    if (h->fz_trace) cudaMemsetAsync(h->fz_trace, 0, 4096 * FZ_TRACE * 8, s);
+    mark(0);
+    e = launch_fused(h, fa, fzp.tb, fzp.smem, gated, s);
+    if (e != cudaSuccess) {
+      h->last_error = std::string("launch failed: ") + cudaGetErrorString(e);
+      return MOE_ERR_CUDA;
+    }
+    for (int i = 1; i <= MOE_NUM_STAGES; ++i) mark(i);
+    if (h->profiling) h->profiled = true;
+    h->last_launches = 1;
+    if (h->fz_trace) print_fused_trace(h, s);
+    return MOE_OK;
   }
   const bool fuse_route = !grouped && h->fuse_route;
   const bool pdl = h->use_pdl && !grouped && !h->profiling;
@@ -617,6 +807,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
         }
       }
       if ((e = launch_dense_in(di, tb_in, grid_in, s)) != cudaSuccess) goto cuda_fail;
+      ++nl;
     }
     if (grouped) {
       UmmaArgs ua{};
@@ -648,7 +839,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
         ua.out_col0 = col0;
         ua.k = k;
         ua.status = h->status;
-        if ((e = launch_umma(h, ua, T, s)) != cudaSuccess) goto cuda_fail;
+        if ((e = launch_umma(h, ua, T, s, &nl)) != cudaSuccess) goto cuda_fail;
       }
     }
   }
@@ -660,6 +851,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
                                   ROUTE_SMEM_BYTES + static_cast<size_t>(E) * ra.mask_words * 4, s,
                                   pdl, ra)) != cudaSuccess)
       goto cuda_fail;
+    ++nl;
   }
 
   // 3. expert up (+gate) with the activation, 4. expert down
@@ -699,6 +891,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     const int grid_up = slots * up.cps;
     mark(2);
     if ((e = launch_expert(up, pb_up, grid_up, s, pdl)) != cudaSuccess) goto cuda_fail;
+    ++nl;
     mark(3);
     ExpertArgs dn = up;
     dn.n_rows = kin;
@@ -715,6 +908,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     dn.prefetch = (h->prefetch >> 1) & 1;
     dn.cps = std::max(1, std::min(std::max(1, kin / 8), (target + slots - 1) / slots));
     if ((e = launch_expert(dn, pb_dn, slots * dn.cps, s, pdl)) != cudaSuccess) goto cuda_fail;
+    ++nl;
   } else {
     UmmaArgs up{};
     up.experts = 1;
@@ -743,7 +937,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     up.out_f32 = h->hbuf;
     up.status = h->status;
     mark(2);
-    if ((e = launch_umma(h, up, T, s)) != cudaSuccess) goto cuda_fail;
+    if ((e = launch_umma(h, up, T, s, &nl)) != cudaSuccess) goto cuda_fail;
     mark(3);
     UmmaArgs dn = up;
     dn.n_rows = kin;
@@ -757,7 +951,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     dn.by_pair = 1;
     dn.act = -1;
     dn.out_f32 = h->pexp;
-    if ((e = launch_umma(h, dn, T, s)) != cudaSuccess) goto cuda_fail;
+    if ((e = launch_umma(h, dn, T, s, &nl)) != cudaSuccess) goto cuda_fail;
   }
 
   // 5. combine + fc2 + shared down + residual
@@ -771,6 +965,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     const int64_t n = static_cast<int64_t>(T) * kout;
     k_prep_out<<<static_cast<int>(std::min<int64_t>((n + 255) / 256, 4096)), 256, 0, s>>>(pa);
     if ((e = cudaGetLastError()) != cudaSuccess) goto cuda_fail;
+    ++nl;
     UmmaArgs ua{};
     DenseSeg& S = ua.seg[0];
     S.nparts = 0;
@@ -791,7 +986,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     ua.x = x; ua.x_dt = c.act_dtype; ua.out = out; ua.delta = delta;
     ua.pexp = h->pexp; ua.wts = h->wts; ua.add_combine = Lt ? 0 : 1;
     ua.status = h->status;
-    if ((e = launch_umma(h, ua, T, s)) != cudaSuccess) goto cuda_fail;
+    if ((e = launch_umma(h, ua, T, s, &nl)) != cudaSuccess) goto cuda_fail;
   } else {
     DenseOutArgs dout{};
     dout.nseg = 0;
@@ -831,14 +1026,17 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
       const int64_t n = static_cast<int64_t>(T) * kout;
       const int gc = static_cast<int>(std::min<int64_t>((n + NT - 1) / NT, h->num_sms * 4));
       if ((e = launch_ex<CombineArgs>(k_combine, gc, NT, 0, s, pdl, ca)) != cudaSuccess) goto cuda_fail;
+      ++nl;
       dout.staged = h->comb;
     }
     const int tb_out = kout ? std::min(pow2_at_least(T, 8), dense_tb_cap(kout)) : pow2_at_least(T, 8);
     const int grid_out = std::max(1, std::min(h->num_sms * 2, (H + 3) / 4));
     if ((e = launch_dense_out(dout, tb_out, grid_out, s, pdl)) != cudaSuccess) goto cuda_fail;
+    ++nl;
   }
   mark(5);
   if (h->profiling) h->profiled = true;
+  h->last_launches = nl;
   return MOE_OK;
 cuda_fail:
   h->last_error = std::string("launch failed: ") + cudaGetErrorString(e);
@@ -880,7 +1078,8 @@ moe_status moe_layer_forward_host(moe_layer* h, const void* x_host, int32_t T, v
 
 moe_status moe_layer_set_path(moe_layer* h, int32_t path) {
   if (!h) return MOE_ERR_INVALID_ARG;
-  if (path != MOE_PATH_AUTO && path != MOE_PATH_GEMV && path != MOE_PATH_GROUPED)
+  if (path != MOE_PATH_AUTO && path != MOE_PATH_GEMV && path != MOE_PATH_GROUPED &&
+      path != MOE_PATH_FUSED)
     return MOE_ERR_INVALID_ARG;
   if (path == MOE_PATH_GROUPED && h->cfg.act_dtype == MOE_DTYPE_FP32) {
     h->last_error = "the grouped path needs 16-bit activations";
@@ -939,6 +1138,13 @@ moe_status moe_layer_stage_times(moe_layer* h, float* ms, int32_t n) {
 }
 
 int64_t moe_layer_device_bytes(const moe_layer* h) { return h ? h->bytes : 0; }
+
+int32_t moe_layer_path_for(const moe_layer* h, int32_t T) {
+  if (!h || T < 1 || T > h->cfg.max_tokens) return -1;
+  return choose_path(h, T);
+}
+
+int32_t moe_layer_last_launch_count(const moe_layer* h) { return h ? h->last_launches : 0; }
 
 const char* moe_status_string(moe_status s) {
   switch (s) {

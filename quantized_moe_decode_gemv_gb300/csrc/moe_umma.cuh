@@ -285,7 +285,7 @@ __device__ __forceinline__ void umma_epilogue(const UmmaArgs& A, int pid, int m,
   }
 }
 
-__global__ void __launch_bounds__(UM_THREADS, 1) k_umma(const UmmaArgs A) {
+__global__ void __launch_bounds__(UM_THREADS, 1) k_umma(const __grid_constant__ UmmaArgs A) {
   extern __shared__ __align__(1024) char um_smem[];
   const bool gated = (A.a_mode == UA_INT4) && A.q2 != nullptr;
   const UmmaPlan P = umma_plan(A.a_mode, gated, A.n_tile, A.stages);
@@ -542,7 +542,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) k_umma(const UmmaArgs A) {
 }
 
 // Sums the split-K partials of a dense grouped launch and applies its epilogue.
-__global__ void k_umma_reduce(const UmmaArgs A) {
+__global__ void k_umma_reduce(const __grid_constant__ UmmaArgs A) {
   griddep_wait();
   griddep_launch();
   const int64_t n = static_cast<int64_t>(A.n_tokens) * A.n_rows;
@@ -566,7 +566,7 @@ struct PrepOutArgs {
   unsigned short* bout;    // [T, L + Fs]
 };
 
-__global__ void k_prep_out(const PrepOutArgs A) {
+__global__ void k_prep_out(const __grid_constant__ PrepOutArgs A) {
   griddep_wait();
   griddep_launch();
   const int K = A.L + A.Fs;

@@ -46,22 +46,33 @@ def teardown_module(module):
     _HANDLES.clear()
 
 
-def _parity(name, T, rows=None, max_tokens=None, seed=0, zipf=False):
+def _parity(name, T, rows=None, max_tokens=None, seed=0, zipf=False, paths=("auto",)):
+    """Every path in `paths` against one oracle result of the same inputs."""
     lay, h = handle_for(name, max_tokens or max(T, 16), seed, zipf)
     x, redraws = gu.margin_x(lay, T, seed=seed + T)
-    got = gu.run_layer(h, x, lay.spec.act_dtype)
     sel = list(range(T)) if rows is None else list(rows)
     ref = gu.ora_forward(lay, x[sel])
-    rr = gu.check_parity(got, ref, rows=sel, what=f"{name} T={T}")
-    assert h.device_status() == 0
+    rr = None
+    try:
+        for path in paths:
+            h.set_path(path)
+            got = gu.run_layer(h, x, lay.spec.act_dtype)
+            rr = gu.check_parity(got, ref, rows=sel, what=f"{name} T={T} path={path}")
+            assert h.device_status() == 0
+    finally:
+        h.set_path("auto")
     return rr
+
+
+# the two CUDA-core schedules: one persistent kernel, and five stream-ordered kernels
+SMALL_T_PATHS = ("fused", "gemv")
 
 
 # --- tiny layer (oracle in milliseconds): several tiles and ragged tails ------
 
 @pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8, 13, 16])
 def test_tiny_parity(T):
-    _parity("tiny", T)
+    _parity("tiny", T, paths=SMALL_T_PATHS)
 
 
 # --- odd shapes covering every option of the config -------------------------
@@ -99,9 +110,12 @@ def test_odd_shapes(name, T):
     h = gu.build_layer(lay, 12)
     try:
         x, _ = gu.margin_x(lay, T, seed=3)
-        got = gu.run_layer(h, x, spec.act_dtype)
         ref = gu.ora_forward(lay, x)
-        gu.check_parity(got, ref, what=f"{name} T={T}")
+        for path in SMALL_T_PATHS:
+            h.set_path(path)
+            got = gu.run_layer(h, x, spec.act_dtype)
+            gu.check_parity(got, ref, what=f"{name} T={T} path={path}")
+            assert h.device_status() == 0
     finally:
         h.close()
 
@@ -110,21 +124,22 @@ def test_odd_shapes(name, T):
 
 @pytest.mark.parametrize("T", [1, 2, 9, 16])
 def test_latent_parity(T):
-    _parity("latent", T)
+    _parity("latent", T, paths=SMALL_T_PATHS)
 
 
 # --- non-latent fp16 sigmoid top-8 layer (H=6144, E=256) at full size ---------
 
 @pytest.mark.parametrize("T,rows", [(1, None), (4, [0, 3]), (32, [0, 31])])
 def test_nonlatent_parity(T, rows):
-    _parity("nonlatent", T, rows=rows, max_tokens=32)
+    _parity("nonlatent", T, rows=rows, max_tokens=32, paths=SMALL_T_PATHS)
 
 
 # --- batched decode rows with Zipf-skewed expert load -------------------------
 
 @pytest.mark.parametrize("T,rows", [(32, [0, 31]), (64, [5, 63]), (256, [0, 128, 255])])
 def test_batched_zipf_parity(T, rows):
-    _parity("latent", T, rows=rows, max_tokens=256, zipf=True)
+    _parity("latent", T, rows=rows, max_tokens=256, zipf=True,
+            paths=SMALL_T_PATHS + ("auto",) if T < 64 else ("auto",))
 
 
 # --- the tcgen05 grouped path (forced at small T, automatic from T = 64) ------
@@ -210,6 +225,29 @@ def test_stack_parity(T, rows):
 
 
 # --- properties of the CUDA path ------------------------------------------------
+
+def test_path_selection_and_launch_counts():
+    """AUTO takes the grouped tcgen05 path from 64 rows; a forced path is
+    honoured, and the persistent kernel is one launch per forward."""
+    lay, h = handle_for("latent", 256, zipf=True)
+    x = gu.to_torch_x(mi.make_x(lay.spec, 64, 5), "bf16")
+    assert [h.path_for(T) for T in (64, 256)] == ["grouped"] * 2
+    assert h.path_for(1) in ("fused", "gemv")
+    try:
+        h.set_path("gemv")
+        assert h.path_for(1) == "gemv"
+        h.forward(x[:1].contiguous())
+        assert h.last_launch_count() >= 4
+        h.set_path("fused")
+        assert h.path_for(64) == "fused"
+        h.forward(x)
+        assert h.last_launch_count() == 1
+        h.set_path("grouped")
+        assert h.path_for(1) == "grouped"
+    finally:
+        h.set_path("auto")
+    torch.cuda.synchronize()
+    assert h.device_status() == 0
 
 def test_row_invariance_bit_exact():
     """Each row of a 16-row pass equals its own one-row pass, bit for bit."""
