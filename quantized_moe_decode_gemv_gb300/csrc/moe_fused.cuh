@@ -8,35 +8,37 @@
 // every CTA resident and lets the routing-independent streams run while the
 // routed chain waits on its dependencies.
 //
-// Work of one CTA, in consumption order (the "phases"):
-//   ROUTER, FC1, SHIN  its rows of the router, fc1_latent_proj and shared
-//                      gate/up matrices (every CTA but CTA 0) -> dense_in
-//   route              CTA 0: top-k selection once every router row is done
-//   SD                 its rows of the shared-expert down matrix -> sdbuf
-//   UP                 its share of the selected experts' up(+gate) rows,
-//                      activation fused -> hbuf
-//   DN                 its share of the selected experts' down rows -> pexp
-//   combine            its slice of y = sum_j w_j * down_j (latent layers)
-//   OUT                its rows of fc2_latent_proj . y + sdbuf + residual
-//                      (latent), or combine + sdbuf + residual (non-latent)
+// A CTA works through a list of segments, each a contiguous range of rows of
+// one matrix with its dependency (a counter to wait for), the vector it reads
+// (staged in shared memory) and the counter it signals when done:
+//   router rows, fc1_latent_proj rows, shared gate/up rows -> dense_in
+//                      (every CTA but CTA 0, which routes once the router rows
+//                      are done and publishes the distinct-expert lists)
+//   shared-down rows (first part)        -> sdbuf, while the routing finishes
+//   expert up(+gate) rows, activation    -> hbuf  (one segment per distinct
+//                      expert and group of its token rows in this CTA's share)
+//   shared-down rows (second part)       -> sdbuf, over the up/down barrier
+//   expert down rows                     -> pexp
+//   shared-down rows (rest)              -> sdbuf
+//   combine y = sum_j w_j * down_j (pick order), then fc2_latent_proj . y
+//   + sdbuf + residual -> out (latent); or the combine + sdbuf + residual
 //
-// Weights move by bulk copies (cp.async.bulk, completion on an mbarrier) into
-// a ring of shared-memory slots, a chunk of whole rows per slot.  Thread 0 is
-// the producer: it keeps the ring full, and its issue order decides where the
-// shared-expert down rows (SD) go: first while the routing is not yet
-// published, then a few between the expert up and down rows (to cover that
-// barrier), the rest before fc2.  All 256 threads consume the chunks in issue
-// order with one compact executor for dense rows and one for int4 expert rows,
-// so the code of every phase stays small and warm in the instruction cache.
+// Weights move by bulk copies (cp.async.bulk, completion on an mbarrier):
+// every warp owns a small ring of shared-memory slots and streams its own
+// rows of each segment, lane 0 issuing up to `depth` chunks ahead, across
+// segment boundaries whenever the next segment is known.  A warp reduces its
+// rows on its own (shuffles), so the 256 threads of a CTA meet only at segment
+// boundaries.  One compact executor for dense rows and one for int4 expert
+// rows serve every segment, so the code stays warm in the instruction cache.
 //
-// Dependencies between CTAs are counters in global memory: a CTA signals a
-// phase after a CTA barrier, a gpu-scope fence and an atomic add; a waiting
-// CTA's thread 0 spins on an acquire load (bounded: after FZ_SPIN_LIMIT polls
-// the kernel sets the timeout bit of the status word and stops computing, but
+// Dependencies between CTAs are counters in global memory: a CTA signals
+// after a CTA barrier, a gpu-scope fence and an atomic add; a waiting CTA's
+// thread 0 spins on an acquire load (bounded: after FZ_SPIN_LIMIT polls the
+// kernel sets the timeout bit of the status word and stops computing, but
 // still signals and drains its copies, so no other CTA waits longer).  The
 // launch is cooperative, so every CTA is resident and the waits end.  The last
 // CTA to finish resets the counters for the next launch.  Every output element
-// is computed by exactly one CTA in a fixed order, so results are
+// is computed by exactly one warp in a fixed order, so results are
 // deterministic and do not depend on the other rows of the batch.
 #pragma once
 
@@ -45,8 +47,8 @@
 namespace moe {
 
 constexpr uint32_t FZ_SPIN_LIMIT = 1u << 20;
-constexpr int FZ_MAX_SLOTS = 8;
-constexpr int FZ_MAX_JOBS = 12;     // per phase
+constexpr int FZ_MAX_DEPTH = 4;     // slots per warp ring
+constexpr int FZ_MAX_SEGS = 32;     // segments per CTA (at most 8 dense + 2 x 9 expert)
 constexpr int FZ_SYNC_STRIDE = 32;  // ints between counters (one 128-byte line each)
 
 // counters (index * FZ_SYNC_STRIDE)
@@ -63,8 +65,10 @@ enum : int {
   FZ_WORDS = 9
 };
 
-// phases
-enum : int { PH_ROUTER = 0, PH_FC1, PH_SHIN, PH_SD, PH_UP, PH_DN, PH_OUT, PH_N };
+// segment kinds, staged vectors and epilogues
+enum : int { SK_DENSE = 0, SK_UP = 1, SK_DN = 2 };
+enum : int { ST_X = 0, ST_SH = 1, ST_Y = 2, ST_EXP = 3 };
+enum : int { EP_DIN = 0, EP_SD = 1, EP_OUT = 2 };
 
 struct FusedArgs {
   int T;
@@ -93,10 +97,11 @@ struct FusedArgs {
   float* delta;
   int* sync;         // FZ_WORDS counters, FZ_SYNC_STRIDE ints apart, zero at launch
   int* status;
-  // ring
-  int slots;         // S
-  int slot_bytes;
-  int sd_mid;        // SD chunks issued between the expert up and down rows
+  // per-warp rings and the placement of the shared-down rows
+  int depth;         // slots per warp ring (<= FZ_MAX_DEPTH)
+  int chunk_bytes;   // slot size (multiple of 128)
+  int sd_pre, sd_mid;   // percent of this CTA's shared-down rows before the expert
+                        // up rows, and between the expert up and down rows
   unsigned long long* trace;   // diagnostics: [grid][FZ_TRACE] globaltimer stamps, or null
 };
 
@@ -173,40 +178,46 @@ __device__ __forceinline__ void span(int64_t n, int c, int g, int64_t& b, int64_
 }
 
 // ---------------------------------------------------------------------------
-// jobs and chunks
+// segments
 // ---------------------------------------------------------------------------
 
-// Dense job: rows [row0, row0 + nrows) of one matrix, R rows per chunk.
-// Expert job: rows [row0, row0 + nrows) of distinct-expert slot u (expert e),
-// all pairs [pa, pa + np) of the slot in groups of PB; chunk = (group, R rows).
-struct FzJob {
-  const char* w;    // dense: matrix; expert: codes of expert e
-  const char* w2;   // expert: gate codes of expert e (gated up), else null
-  const char* sb;   // expert: scale/bias words of expert e
+// A segment runs in nsub sub-rounds, each with its own staged vector: the
+// token-row passes of a dense segment, the groups of PB token pairs of an
+// expert segment.
+struct FzSeg {
+  int kind, stage, nsub;
+  int wait_ctr, wait_tgt;   // counter to wait for before the segment (-1: none)
+  int sig;                  // counter to signal after it (-1: none)
+  int row0, nrows;          // the CTA's rows of the matrix (dense) or of the expert (experts)
+  // dense
+  const char* w;
+  int dt, esz, K, col0, epi;
+  // experts: codes and scale/bias words of expert e (gate: q2/sb2), token pairs [pa, pa + np)
+  const char* q;
+  const char* sb;
+  const char* q2;
   const char* sb2;
-  int row0, nrows, R;
-  int col;          // dense: output column of row0; expert: slot u
-  int pa, np;       // expert pairs
-  int nchunks, first;
+  int pa, np, R;            // all token pairs of the slot; R rows per chunk
 };
 
-struct FzPhase {
-  int njobs, nchunks, passes;   // nchunks per pass
-  int ready;                    // job table built
-  int K, dt;                    // reduction width, weight dtype (dense)
-  FzJob job[FZ_MAX_JOBS];
-};
-
-// Shared bookkeeping of a CTA (dynamic shared memory, after the ring).
 struct FzShared {
-  FzPhase ph[PH_N];
-  int slot_phase[FZ_MAX_SLOTS];
-  int slot_idx[FZ_MAX_SLOTS];
-  int issued;        // chunks issued (written by thread 0)
-  int done_all;      // producer has nothing left
-  int routed;        // thread 0's last view of the routing flag
-  int pid[8];        // expert staging: pair ids of the staged group
+  FzSeg seg[FZ_MAX_SEGS];
+  volatile int nsegs;       // segments known so far (grows once, after the routing)
+  int pid[8];               // expert staging: pair ids of the staged group
 };
+
+// Warp w's rows [r0, r1) of the CTA's rows of segment S, and its chunks per sub-round.
+__device__ __forceinline__ void fz_warp_rows(const FzSeg& S, int w, int& r0, int& r1) {
+  r0 = S.row0 + S.nrows * w / NW;
+  r1 = S.row0 + S.nrows * (w + 1) / NW;
+}
+__device__ __forceinline__ int fz_sub_chunks(const FzSeg& S, int w, int CH) {
+  int r0, r1;
+  fz_warp_rows(S, w, r0, r1);
+  if (r1 <= r0) return 0;
+  if (S.kind == SK_DENSE) return (r1 - r0) * ((S.K * S.esz + CH - 1) / CH);
+  return (r1 - r0 + S.R - 1) / S.R;
+}
 
 // ---------------------------------------------------------------------------
 // staging (all threads)
@@ -219,30 +230,45 @@ template <int TB>
 __device__ __forceinline__ void fz_stage_dense(const FusedArgs& A, int kind, int t0, int tb, int K,
                                                float4* xs4) {
   const int K4 = K >> 2;
-  for (int i = threadIdx.x; i < TB * K4; i += NT) {
-    const int t = i / K4, f4 = i - t * K4;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (t < tb) {
+  const bool al = ((A.din_rows | A.off_shu | A.off_shg) & 3) == 0;
+  // four items per thread per round, loads first, so their latencies overlap
+  for (int i0 = threadIdx.x; i0 < TB * K4; i0 += 4 * NT) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * NT;
+      const int t = i / K4, f4 = i - t * K4;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i >= TB * K4 || t >= tb) continue;
       const int64_t tt = t0 + t;
       if (kind == 0) {
-        const int64_t e = tt * A.H + 4 * f4;
-        v.x = ld16(A.x, e, A.x_dt); v.y = ld16(A.x, e + 1, A.x_dt);
-        v.z = ld16(A.x, e + 2, A.x_dt); v.w = ld16(A.x, e + 3, A.x_dt);
+        const uint2 h = *reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(A.x) + tt * A.H + 4 * f4);
+        if (A.x_dt == DT_BF16) v[u] = make_float4(bf16lo(h.x), bf16hi(h.x), bf16lo(h.y), bf16hi(h.y));
+        else v[u] = make_float4(f16lo(h.x), f16hi(h.x), f16lo(h.y), f16hi(h.y));
       } else if (kind == 1) {
-        // the shared columns start at any column of dense_in: scalar loads
         const float* du = A.dense_in + tt * A.din_rows + A.off_shu + 4 * f4;
         const float* dg = A.dense_in + tt * A.din_rows + A.off_shg + 4 * f4;
-        const bool gl = A.act == ACT_SWIGLU;
-        const float u0 = __ldcg(du), u1 = __ldcg(du + 1), u2 = __ldcg(du + 2), u3 = __ldcg(du + 3);
-        float g0 = 0.f, g1 = 0.f, g2 = 0.f, g3 = 0.f;
-        if (gl) { g0 = __ldcg(dg); g1 = __ldcg(dg + 1); g2 = __ldcg(dg + 2); g3 = __ldcg(dg + 3); }
-        v = make_float4(act_fn(A.act, g0, u0), act_fn(A.act, g1, u1), act_fn(A.act, g2, u2),
-                        act_fn(A.act, g3, u3));
+        float4 uu, gg = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (al) {
+          uu = __ldcg(reinterpret_cast<const float4*>(du));
+          if (A.act == ACT_SWIGLU) gg = __ldcg(reinterpret_cast<const float4*>(dg));
+        } else {   // the shared columns start at a column that is not a multiple of 4
+          uu = make_float4(__ldcg(du), __ldcg(du + 1), __ldcg(du + 2), __ldcg(du + 3));
+          if (A.act == ACT_SWIGLU) gg = make_float4(__ldcg(dg), __ldcg(dg + 1), __ldcg(dg + 2), __ldcg(dg + 3));
+        }
+        v[u] = make_float4(act_fn(A.act, gg.x, uu.x), act_fn(A.act, gg.y, uu.y), act_fn(A.act, gg.z, uu.z),
+                           act_fn(A.act, gg.w, uu.w));
       } else {
-        v = __ldcg(reinterpret_cast<const float4*>(A.ybuf + tt * A.L) + f4);
+        v[u] = __ldcg(reinterpret_cast<const float4*>(A.ybuf + tt * A.L) + f4);
       }
     }
-    xs4[t * K4 + swz(f4, 1)] = v;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * NT;
+      if (i >= TB * K4) break;
+      const int t = i / K4, f4 = i - t * K4;
+      xs4[t * K4 + swz(f4, 1)] = v[u];
+    }
   }
 }
 
@@ -289,108 +315,91 @@ __device__ __forceinline__ void fz_stage_expert(const ExpertArgs& X, int pa, int
 }
 
 // ---------------------------------------------------------------------------
-// executors (one copy each, shared by every phase)
+// executors (one copy each, shared by every segment)
 // ---------------------------------------------------------------------------
 
-// Epilogue of a dense chunk.
-struct FzEpi {
-  int mode;          // 0: store fp32 to out[t * ld + col]; 1: final output row
-  float* out;
-  int64_t ld;
-};
-
-// Rows [0, n) of a chunk of R rows (K elements of dtype dt each) in shared
-// memory against TB staged token rows; v(t, r) goes to the epilogue for token
-// row t0 + t (t < tb) and output column col + r.  R in {1, 2, 4, 8}: 8 / R
-// warps share a row, each a contiguous K slice.
+// Bytes [boff, boff + nb) of row r of a dense matrix, in a slot, against TB
+// staged token rows: partial sums into acc; on the row's last chunk the warp
+// reduces them and writes the epilogue.
 template <int TB>
-__device__ __noinline__ void fz_dense_chunk(const FusedArgs& A, const char* slot, int n, int R, int K,
-                                            int dt, const float4* xs4, float* red, int t0, int tb,
-                                            int col, FzEpi ep) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int wpr = NW / R;
-  const int rl = warp / wpr, q = warp - rl * wpr;
-  const int K4 = K >> 2;
-  float acc[TB];
+__device__ __noinline__ void fz_dense_piece(const FusedArgs& A, const FzSeg& S, const char* slot, int r,
+                                            int boff, int nb, bool last, const float4* xs4, int t0,
+                                            int tb, float (&acc)[TB]) {
+  const int lane = threadIdx.x & 31;
+  const int K4 = S.K >> 2;
+  const int np16 = nb >> 4;
+  if (S.esz == 2) {
+    const int f0 = boff >> 3;   // float4 index of the chunk's first element
+    const int dt = S.dt;
+    for (int p = lane; p < np16; p += 32) {
+      float wf[8];
+      cvt8(reinterpret_cast<const uint4*>(slot)[p], dt, wf);
+      const int s0 = swz(f0 + 2 * p, 1), s1 = swz(f0 + 2 * p + 1, 1);
 #pragma unroll
-  for (int t = 0; t < TB; ++t) acc[t] = 0.f;
-  if (rl < n) {
-    if (dt != DT_FP32) {
-      const int pieces = K >> 3, per = pieces / wpr;   // 8 elements per piece
-      const uint4* wr = reinterpret_cast<const uint4*>(slot + static_cast<int64_t>(rl) * K * 2);
-#pragma unroll 2
-      for (int p = q * per + lane; p < (q + 1) * per; p += 32) {
-        float wf[8];
-        cvt8(wr[p], dt, wf);
-        const int s0 = swz(2 * p, 1), s1 = swz(2 * p + 1, 1);
-#pragma unroll
-        for (int t = 0; t < TB; ++t) {
-          const float4 a = xs4[t * K4 + s0], b = xs4[t * K4 + s1];
-          float s = acc[t];
-          s = fmaf(wf[0], a.x, s); s = fmaf(wf[1], a.y, s); s = fmaf(wf[2], a.z, s); s = fmaf(wf[3], a.w, s);
-          s = fmaf(wf[4], b.x, s); s = fmaf(wf[5], b.y, s); s = fmaf(wf[6], b.z, s); s = fmaf(wf[7], b.w, s);
-          acc[t] = s;
-        }
+      for (int t = 0; t < TB; ++t) {
+        const float4 a = xs4[t * K4 + s0], b = xs4[t * K4 + s1];
+        float s = acc[t];
+        s = fmaf(wf[0], a.x, s); s = fmaf(wf[1], a.y, s); s = fmaf(wf[2], a.z, s); s = fmaf(wf[3], a.w, s);
+        s = fmaf(wf[4], b.x, s); s = fmaf(wf[5], b.y, s); s = fmaf(wf[6], b.z, s); s = fmaf(wf[7], b.w, s);
+        acc[t] = s;
       }
-    } else {
-      const int pieces = K >> 2, per = pieces / wpr;   // 4 elements per piece
-      const float4* wr = reinterpret_cast<const float4*>(slot + static_cast<int64_t>(rl) * K * 4);
-#pragma unroll 2
-      for (int p = q * per + lane; p < (q + 1) * per; p += 32) {
-        const float4 w = wr[p];
-        const int s0 = swz(p, 1);
+    }
+  } else {
+    const int f0 = boff >> 4;
+    for (int p = lane; p < np16; p += 32) {
+      const float4 w = reinterpret_cast<const float4*>(slot)[p];
+      const int s0 = swz(f0 + p, 1);
 #pragma unroll
-        for (int t = 0; t < TB; ++t) {
-          const float4 a = xs4[t * K4 + s0];
-          float s = acc[t];
-          s = fmaf(w.x, a.x, s); s = fmaf(w.y, a.y, s); s = fmaf(w.z, a.z, s); s = fmaf(w.w, a.w, s);
-          acc[t] = s;
-        }
+      for (int t = 0; t < TB; ++t) {
+        const float4 a = xs4[t * K4 + s0];
+        float s = acc[t];
+        s = fmaf(w.x, a.x, s); s = fmaf(w.y, a.y, s); s = fmaf(w.z, a.z, s); s = fmaf(w.w, a.w, s);
+        acc[t] = s;
       }
     }
   }
+  if (!last) return;
   const float tot = warp_reduce_scatter<TB>(acc, lane);
+#pragma unroll
+  for (int t = 0; t < TB; ++t) acc[t] = 0.f;
   constexpr int LPV = 32 / TB;
-  if ((lane & (LPV - 1)) == 0) red[warp * TB + lane / LPV] = tot;
-  __syncthreads();
-  for (int o = threadIdx.x; o < n * TB; o += NT) {
-    const int r = o / TB, t = o - r * TB;
-    if (t >= tb) continue;
-    float s = 0.f;
-    for (int qq = 0; qq < wpr; ++qq) s += red[(r * wpr + qq) * TB + t];
-    const int tt = t0 + t, cc = col + r;
-    if (ep.mode == 0) {
-      ep.out[tt * ep.ld + cc] = s;
-    } else {
-      const int64_t e = static_cast<int64_t>(tt) * A.H + cc;
-      if (A.Fs) s += __ldcg(A.sdbuf + e);
-      const float xv = ld16(A.x, e, A.x_dt);
-      reinterpret_cast<unsigned short*>(A.out)[e] = st16_bits(xv + s, A.x_dt);
-      if (A.delta) A.delta[e] = s;
-    }
+  const int t = lane / LPV;
+  if ((lane & (LPV - 1)) != 0 || t >= tb) return;
+  const int tt = t0 + t;
+  const int cc = S.col0 + (r - S.row0);
+  if (S.epi == EP_DIN) {
+    A.dense_in[static_cast<int64_t>(tt) * A.din_rows + cc] = tot;
+  } else if (S.epi == EP_SD) {
+    A.sdbuf[static_cast<int64_t>(tt) * A.H + cc] = tot;
+  } else {
+    const int64_t e = static_cast<int64_t>(tt) * A.H + cc;
+    float v = tot;
+    if (A.Fs) v += __ldcg(A.sdbuf + e);
+    const float xv = ld16(A.x, e, A.x_dt);
+    reinterpret_cast<unsigned short*>(A.out)[e] = st16_bits(xv + v, A.x_dt);
+    if (A.delta) A.delta[e] = v;
   }
 }
 
-// Rows [0, n) of a chunk of int4 expert rows in shared memory: codes
-// [n][K/2 bytes], then scale/bias words [n][K/G] at sb (and the gate's at
-// q2/sb2), against the np staged pair rows.  Warp w takes rows w, w + 8, ...;
-// a lane takes 32-code pieces lane, lane + 32, ...
+// Rows [r, r + n) of an expert segment in a slot: codes [n][K/2 bytes], the
+// scale/bias words at sb (and the gate's at q2 / sb2), against the np staged
+// token rows of the segment.  One warp; a lane takes 32-code pieces.
 template <int PB, bool GATED>
-__device__ __noinline__ void fz_expert_chunk(const ExpertArgs& X, const char* q, const uint32_t* sb,
-                                             const char* q2, const uint32_t* sb2, int n, int row0,
-                                             const float4* xs4, const int* pid_s, int np) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__device__ __noinline__ void fz_expert_rows(const ExpertArgs& X, const char* q, const uint32_t* sb,
+                                            const char* q2, const uint32_t* sb2, int n, int r,
+                                            const float4* xs4, const int* pid_s, int np) {
+  const int lane = threadIdx.x & 31;
   const int K = X.K, K4 = K >> 2, nchunk = K >> 5, ngr = K / X.G;
   const float* xsum = reinterpret_cast<const float*>(xs4 + PB * K4);
   constexpr int NV = 2 * PB;
   constexpr int LPV = 32 / NV;
 #pragma unroll 1
-  for (int r = warp; r < n; r += NW) {
+  for (int i = 0; i < n; ++i) {
     float acc[PB], accg[PB];
 #pragma unroll
     for (int pp = 0; pp < PB; ++pp) { acc[pp] = 0.f; accg[pp] = 0.f; }
-    const uint4* qr = reinterpret_cast<const uint4*>(q + static_cast<int64_t>(r) * (K >> 1));
-    const uint32_t* sr = sb + r * ngr;
+    const uint4* qr = reinterpret_cast<const uint4*>(q + static_cast<int64_t>(i) * (K >> 1));
+    const uint32_t* sr = sb + i * ngr;
 #pragma unroll 1
     for (int cc = lane; cc < nchunk; cc += 32) {
       const uint4 w = qr[cc];
@@ -400,9 +409,9 @@ __device__ __noinline__ void fz_expert_chunk(const ExpertArgs& X, const char* q,
       uint4 wg = make_uint4(0u, 0u, 0u, 0u);
       float sg16 = 0.f, bbg = 0.f;
       if (GATED) {
-        wg = reinterpret_cast<const uint4*>(q2 + static_cast<int64_t>(r) * (K >> 1))[cc];
+        wg = reinterpret_cast<const uint4*>(q2 + static_cast<int64_t>(i) * (K >> 1))[cc];
         float sg, bg;
-        sb_decode(sb2[r * ngr + (cc << 5) / X.G], X.s_dt, sg, bg);
+        sb_decode(sb2[i * ngr + (cc << 5) / X.G], X.s_dt, sg, bg);
         sg16 = 16.f * sg;
         bbg = bg - sg16;
       }
@@ -425,7 +434,7 @@ __device__ __noinline__ void fz_expert_chunk(const ExpertArgs& X, const char* q,
       const int pp = (lane / LPV) >> 1;
       if (pp < np) {
         const float val = (X.act >= 0) ? act_fn(X.act, other, tot) : tot;
-        X.out[static_cast<int64_t>(pid_s[pp]) * X.n_rows + row0 + r] = val;
+        X.out[static_cast<int64_t>(pid_s[pp]) * X.n_rows + r + i] = val;
       }
     }
   }
@@ -435,91 +444,148 @@ __device__ __noinline__ void fz_expert_chunk(const ExpertArgs& X, const char* q,
 // the kernel
 // ---------------------------------------------------------------------------
 
+// Geometry of chunk ci (within a sub-round) of warp w in segment S: dense ->
+// row, byte offset and bytes; expert -> first row and rows.
+struct FzChunk {
+  int r, boff, nb, n;
+  bool last;   // dense: the row's last chunk
+};
+__device__ __forceinline__ FzChunk fz_chunk(const FzSeg& S, int w, int ci, int CH) {
+  int r0, r1;
+  fz_warp_rows(S, w, r0, r1);
+  FzChunk C;
+  if (S.kind == SK_DENSE) {
+    const int rb = S.K * S.esz, per = (rb + CH - 1) / CH;
+    const int ri = ci / per, k = ci - ri * per;
+    C.r = r0 + ri;
+    C.boff = k * CH;
+    C.nb = min(CH, rb - C.boff);
+    C.n = 1;
+    C.last = k == per - 1;
+  } else {
+    C.r = r0 + ci * S.R;
+    C.n = min(S.R, r1 - C.r);
+    C.boff = 0;
+    C.nb = 0;
+    C.last = true;
+  }
+  return C;
+}
+
 template <int TB, int PB, bool GATED>
 __global__ void __launch_bounds__(NT, TB >= 8 ? 1 : 2) k_fused(const __grid_constant__ FusedArgs A) {
   extern __shared__ __align__(128) char fz_smem_raw[];
   const int c = blockIdx.x, G = gridDim.x;
-  const int S = A.slots;
-  const int SB = A.slot_bytes;
-  char* ring = fz_smem_raw;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(ring + static_cast<size_t>(S) * SB);
-  FzShared* sh = reinterpret_cast<FzShared*>(bar + FZ_MAX_SLOTS);
-  float* red = reinterpret_cast<float*>(reinterpret_cast<char*>(sh) + ((sizeof(FzShared) + 15) & ~size_t(15)));
-  float4* xs4 = reinterpret_cast<float4*>(red + NW * 8);   // staged vectors / route scratch
+  const int D = A.depth, CH = A.chunk_bytes;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  char* rings = fz_smem_raw;                                             // [NW][D][CH]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rings + static_cast<size_t>(NW) * D * CH);   // [NW][FZ_MAX_DEPTH]
+  FzShared* sh = reinterpret_cast<FzShared*>(bars + NW * FZ_MAX_DEPTH);
+  float4* xs4 = reinterpret_cast<float4*>(reinterpret_cast<char*>(sh) + ((sizeof(FzShared) + 15) & ~size_t(15)));
+  char* ring = rings + static_cast<size_t>(warp) * D * CH;
+  uint64_t* bar = bars + warp * FZ_MAX_DEPTH;
   int* sync = A.sync;
   const int T = A.T;
-  const int tid = threadIdx.x;
   bool ok = true;
   auto stamp = [&](int i) {
     if (A.trace && tid == 0) A.trace[c * FZ_TRACE + i] = global_ns();
   };
+  // diagnostics: CTA 1's warp 7 (which holds router row 0) at points of the first segment
+  auto dstamp = [&](int i) {
+    if (A.trace && c == 1 && tid == 224) A.trace[FZ_TRACE + 13 + i] = global_ns();
+  };
   stamp(0);
-
-  // ---- job tables of the routing-independent phases (thread 0) ----
   const int passes = (T + TB - 1) / TB;
-  const bool din_cta = c > 0;
+
+  // ---- the static segments (thread 0) ----
   if (tid == 0) {
-    for (int s = 0; s < FZ_MAX_SLOTS; ++s) fz_mbar_init(bar + s, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    auto dense_job = [&](FzPhase& P, const void* w, int dt, int K, int rows, int cc, int gg, int col0) {
-      int64_t b, e;
-      span(rows, cc, gg, b, e);
-      if (e <= b) return;
-      const int rb = K * (dt == DT_FP32 ? 4 : 2);
-      int R = 8;
-      while (R > 1 && R * rb > SB) R >>= 1;
-      FzJob& J = P.job[P.njobs++];
-      J.w = static_cast<const char*>(w);
-      J.w2 = nullptr; J.sb = nullptr; J.sb2 = nullptr;
-      J.row0 = static_cast<int>(b);
-      J.nrows = static_cast<int>(e - b);
-      J.R = R;
-      J.col = col0 + static_cast<int>(b);
-      J.pa = 0; J.np = 0;
-      J.nchunks = (J.nrows + R - 1) / R;
-      J.first = P.nchunks;
-      P.nchunks += J.nchunks;
+    int ns = 0;
+    auto dense = [&](const void* w, int dt, int K, int64_t rb, int64_t re, int col0, int epi, int stage,
+                     int wctr, int wtgt, int sig) {
+      FzSeg& S = sh->seg[ns++];
+      S.kind = SK_DENSE; S.stage = stage; S.nsub = passes;
+      S.wait_ctr = wctr; S.wait_tgt = wtgt; S.sig = sig;
+      S.row0 = static_cast<int>(rb); S.nrows = static_cast<int>(re - rb);
+      S.w = static_cast<const char*>(w); S.dt = dt; S.esz = dt == DT_FP32 ? 4 : 2; S.K = K;
+      S.col0 = col0 + static_cast<int>(rb); S.epi = epi;
+      S.q = S.sb = S.q2 = S.sb2 = nullptr; S.pa = 0; S.np = 0; S.R = 1;
     };
-    for (int p = 0; p < PH_N; ++p) {
-      FzPhase& P = sh->ph[p];
-      P.njobs = 0; P.nchunks = 0; P.passes = 1; P.ready = 0; P.K = A.H; P.dt = A.x_dt;
+    if (c > 0) {
+      // CTA 0 routes; the others share the rows that read x
+      const int gd = G - 1, cd = c - 1;
+      int64_t b, e;
+      span(A.E, cd, gd, b, e);
+      dense(A.router_w, A.router_dt, A.H, b, e, 0, EP_DIN, ST_X, -1, 0, FZ_ROUTER);
+      span(A.L, cd, gd, b, e);
+      dense(A.fc1, A.x_dt, A.H, b, e, A.off_fc1, EP_DIN, ST_X, -1, 0, FZ_FC1);
+      span(A.Fs, cd, gd, b, e);
+      if (A.act == ACT_SWIGLU) dense(A.sh_gate, A.x_dt, A.H, b, e, A.off_shg, EP_DIN, ST_X, -1, 0, -1);
+      dense(A.sh_up, A.x_dt, A.H, b, e, A.off_shu, EP_DIN, ST_X, -1, 0, FZ_DIN);
     }
-    const int gd = G - 1, cd = c - 1;
-    if (din_cta) {
-      FzPhase& P0 = sh->ph[PH_ROUTER];
-      P0.dt = A.router_dt; P0.passes = passes;
-      dense_job(P0, A.router_w, A.router_dt, A.H, A.E, cd, gd, 0);
-      FzPhase& P1 = sh->ph[PH_FC1];
-      P1.passes = passes;
-      if (A.L) dense_job(P1, A.fc1, A.x_dt, A.H, A.L, cd, gd, A.off_fc1);
-      FzPhase& P2 = sh->ph[PH_SHIN];
-      P2.passes = passes;
-      if (A.Fs) {
-        if (A.act == ACT_SWIGLU) dense_job(P2, A.sh_gate, A.x_dt, A.H, A.Fs, cd, gd, A.off_shg);
-        dense_job(P2, A.sh_up, A.x_dt, A.H, A.Fs, cd, gd, A.off_shu);
-      }
+    // the first part of this CTA's shared-down rows
+    if (A.Fs) {
+      int64_t b, e;
+      span(A.H, c, G, b, e);
+      const int64_t n1 = (e - b) * A.sd_pre / 100;
+      dense(A.sh_down, A.x_dt, A.Fs, b, b + n1, 0, EP_SD, ST_SH, FZ_DIN, G - 1, -1);
     }
-    sh->ph[PH_ROUTER].ready = sh->ph[PH_FC1].ready = sh->ph[PH_SHIN].ready = 1;
-    FzPhase& Ps = sh->ph[PH_SD];
-    Ps.K = A.Fs; Ps.passes = passes;
-    if (A.Fs) dense_job(Ps, A.sh_down, A.x_dt, A.Fs, A.H, c, G, 0);
-    Ps.ready = 1;
-    FzPhase& Po = sh->ph[PH_OUT];
-    Po.K = A.L; Po.passes = passes;
-    if (A.L) dense_job(Po, A.fc2, A.x_dt, A.L, A.H, c, G, 0);
-    Po.ready = 1;
-    sh->issued = 0;
-    sh->done_all = 0;
-    sh->routed = 0;
-    // phases without rows are complete at once
-    if (din_cta) {
-      if (sh->ph[PH_ROUTER].nchunks == 0) fz_post(sync + FZ_ROUTER * FZ_SYNC_STRIDE);
-      if (sh->ph[PH_FC1].nchunks == 0) fz_post(sync + FZ_FC1 * FZ_SYNC_STRIDE);
-      if (sh->ph[PH_SHIN].nchunks == 0) fz_post(sync + FZ_DIN * FZ_SYNC_STRIDE);
-    }
-    if (sh->ph[PH_SD].nchunks == 0) fz_post(sync + FZ_SD * FZ_SYNC_STRIDE);
+    sh->nsegs = ns;
+    for (int w = 0; w < NW; ++w)
+      for (int d = 0; d < FZ_MAX_DEPTH; ++d) fz_mbar_init(bars + w * FZ_MAX_DEPTH + d, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  dstamp(0);
+
+  // ---- per-warp ring: lane 0 issues chunks in segment order ----
+  int p_seg = 0, p_ci = 0;          // producer cursor (lane 0)
+  uint32_t issued = 0, consumed = 0;
+  // The router rows go first and alone: the routing (on the critical path)
+  // then does not wait behind every other warp's first chunks.
+  int seg_limit = c > 0 ? 1 : FZ_MAX_SEGS;
+  auto produce = [&]() {
+    if (lane != 0) return;
+    const int nk = min(static_cast<int>(sh->nsegs), seg_limit);
+    while (issued - consumed < static_cast<uint32_t>(D) && p_seg < nk) {
+      const FzSeg& S = sh->seg[p_seg];
+      const int per = fz_sub_chunks(S, warp, CH);
+      if (p_ci >= per * S.nsub) { ++p_seg; p_ci = 0; continue; }
+      const FzChunk C = fz_chunk(S, warp, p_ci % per, CH);
+      const int sl = issued % D;
+      char* dst = ring + static_cast<size_t>(sl) * CH;
+      uint64_t* b = bar + sl;
+      if (S.kind == SK_DENSE) {
+        fz_expect_tx(b, C.nb);
+        fz_bulk(dst, S.w + static_cast<int64_t>(C.r) * S.K * S.esz + C.boff, C.nb, b);
+      } else {
+        const ExpertArgs& X = S.kind == SK_UP ? A.up : A.dn;
+        const int ngr = X.K / X.G;
+        const uint32_t qb = static_cast<uint32_t>(C.n) * (X.K / 2);
+        const uint64_t sa = reinterpret_cast<uint64_t>(S.sb + static_cast<int64_t>(C.r) * ngr * 4);
+        const uint64_t sa0 = sa & ~uint64_t(15);
+        const uint32_t sbb = static_cast<uint32_t>((sa + static_cast<uint64_t>(C.n) * ngr * 4 - sa0 + 15) & ~uint64_t(15));
+        uint32_t tx = qb + sbb, sbb2 = 0;
+        uint64_t sa2_0 = 0;
+        if (S.q2) {
+          const uint64_t sa2 = reinterpret_cast<uint64_t>(S.sb2 + static_cast<int64_t>(C.r) * ngr * 4);
+          sa2_0 = sa2 & ~uint64_t(15);
+          sbb2 = static_cast<uint32_t>((sa2 + static_cast<uint64_t>(C.n) * ngr * 4 - sa2_0 + 15) & ~uint64_t(15));
+          tx += qb + sbb2;
+        }
+        fz_expect_tx(b, tx);
+        fz_bulk(dst, S.q + static_cast<int64_t>(C.r) * (X.K / 2), qb, b);
+        fz_bulk(dst + qb, reinterpret_cast<const void*>(sa0), sbb, b);
+        if (S.q2) {
+          fz_bulk(dst + qb + sbb, S.q2 + static_cast<int64_t>(C.r) * (X.K / 2), qb, b);
+          fz_bulk(dst + 2 * qb + sbb, reinterpret_cast<const void*>(sa2_0), sbb2, b);
+        }
+      }
+      ++issued;
+      ++p_ci;
+    }
+  };
+  produce();
+  dstamp(1);
 
   // ---- routing (CTA 0) ----
   if (c == 0) {
@@ -528,7 +594,7 @@ __global__ void __launch_bounds__(NT, TB >= 8 ? 1 : 2) k_fused(const __grid_cons
     if (ok)
       route_block(A.route, reinterpret_cast<int*>(xs4));
     else if (tid == 0)
-      A.route.meta[0] = 0;   // no routing: the expert phases find no work
+      A.route.meta[0] = 0;   // no routing: the expert segments find no work
     __syncthreads();
     if (tid == 0) {
       __threadfence();
@@ -537,149 +603,93 @@ __global__ void __launch_bounds__(NT, TB >= 8 ? 1 : 2) k_fused(const __grid_cons
     stamp(2);
   }
 
-  // ---- producer (thread 0): the next chunk in issue order ----
-  // steps: 0 ROUTER, 1 FC1, 2 SHIN, 3 SD until routed, 4 UP, 5 SD (sd_mid), 6 DN,
-  // 7 SD rest, 8 OUT, 9 done
-  int step = 0, sd_mid_left = A.sd_mid;
-  int cur[PH_N];
-  for (int p = 0; p < PH_N; ++p) cur[p] = 0;
-
-  // expert job tables from the route metadata (thread 0; after the routing flag)
-  auto build_expert = [&](int ph, const ExpertArgs& X, bool gated_up) {
-    FzPhase& P = sh->ph[ph];
-    P.njobs = 0; P.nchunks = 0; P.passes = 1; P.K = X.K;
-    const int nu = min(max(__ldcg(X.meta), 0), X.umax);
-    const int ngr = X.K / X.G;
-    const int rowb = (gated_up ? 2 : 1) * (X.K / 2 + ngr * 4);
-    int R = (SB - (gated_up ? 32 : 16)) / rowb;
-    R = max(1, min(R, 32));
-    int64_t b, e;
-    span(static_cast<int64_t>(nu) * X.n_rows, c, G, b, e);
-    while (b < e && P.njobs < FZ_MAX_JOBS) {
-      const int u = static_cast<int>(b / X.n_rows);
-      const int n0 = static_cast<int>(b - static_cast<int64_t>(u) * X.n_rows);
-      const int n1 = static_cast<int>(min(static_cast<int64_t>(X.n_rows), n0 + (e - b)));
-      const int64_t ex = __ldcg(X.meta + 1 + u);
-      const int pa = __ldcg(X.meta + 1 + X.umax + u), pe = __ldcg(X.meta + 2 + X.umax + u);
-      FzJob& J = P.job[P.njobs++];
-      J.w = reinterpret_cast<const char*>(X.q) + ex * X.n_rows * (X.K / 2);
-      J.sb = reinterpret_cast<const char*>(X.sb) + ex * X.n_rows * ngr * 4;
-      J.w2 = gated_up ? reinterpret_cast<const char*>(X.q_gate) + ex * X.n_rows * (X.K / 2) : nullptr;
-      J.sb2 = gated_up ? reinterpret_cast<const char*>(X.sb_gate) + ex * X.n_rows * ngr * 4 : nullptr;
-      J.row0 = n0;
-      J.nrows = n1 - n0;
-      J.R = R;
-      J.col = u;
-      J.pa = pa;
-      J.np = max(0, pe - pa);
-      const int groups = (J.np + PB - 1) / PB;
-      J.nchunks = groups * ((J.nrows + R - 1) / R);
-      J.first = P.nchunks;
-      P.nchunks += J.nchunks;
-      b += n1 - n0;
-    }
-    if (b < e) atomicOr(A.status, STATUS_TIMEOUT);   // job table overflow (not expected)
-    P.ready = 1;
-  };
-
-  // chunk i of a phase: job j, pass (dense) and chunk lc within the job
-  auto locate = [&](const FzPhase& P, int i, int& j, int& pass, int& lc) {
-    pass = i / max(P.nchunks, 1);
-    const int ci = i - pass * P.nchunks;
-    j = 0;
-    while (j + 1 < P.njobs && ci >= P.job[j + 1].first) ++j;
-    lc = ci - P.job[j].first;
-  };
-
-  auto issue = [&](int p, int i) {
-    const int seq = sh->issued;
-    const int s = seq % S;
-    const FzPhase& P = sh->ph[p];
-    int j, pass, lc;
-    locate(P, i, j, pass, lc);
-    const FzJob& J = P.job[j];
-    char* dst = ring + static_cast<size_t>(s) * SB;
-    sh->slot_phase[s] = p;
-    sh->slot_idx[s] = i;
-    if (p == PH_UP || p == PH_DN) {
-      const ExpertArgs& X = (p == PH_UP) ? A.up : A.dn;
-      const int nrc = (J.nrows + J.R - 1) / J.R;
-      const int rc = lc % nrc;
-      const int r = J.row0 + rc * J.R, n = min(J.R, J.row0 + J.nrows - r);
+  // the segments after the routing (thread 0, after the routing flag)
+  auto build_rest = [&]() {
+    int ns = sh->nsegs;
+    auto add = [&]() -> FzSeg* {
+      if (ns >= FZ_MAX_SEGS) { atomicOr(A.status, STATUS_TIMEOUT); return nullptr; }   // not reachable
+      return &sh->seg[ns++];
+    };
+    auto experts = [&](int kind, const ExpertArgs& X, bool gated_up, int wctr, int wtgt, int sig) {
+      const int nu = min(max(__ldcg(X.meta), 0), X.umax);
       const int ngr = X.K / X.G;
-      const uint32_t qb = static_cast<uint32_t>(n) * (X.K / 2);
-      const uint64_t sa = reinterpret_cast<uint64_t>(J.sb + static_cast<int64_t>(r) * ngr * 4);
-      const uint64_t sa0 = sa & ~uint64_t(15);
-      const uint32_t sbb = static_cast<uint32_t>((sa + static_cast<uint64_t>(n) * ngr * 4 - sa0 + 15) & ~uint64_t(15));
-      uint32_t tx = qb + sbb;
-      uint32_t sbb2 = 0;
-      uint64_t sa2_0 = 0;
-      if (J.w2) {
-        const uint64_t sa2 = reinterpret_cast<uint64_t>(J.sb2 + static_cast<int64_t>(r) * ngr * 4);
-        sa2_0 = sa2 & ~uint64_t(15);
-        sbb2 = static_cast<uint32_t>((sa2 + static_cast<uint64_t>(n) * ngr * 4 - sa2_0 + 15) & ~uint64_t(15));
-        tx += qb + sbb2;
+      const int rowb = (gated_up ? 2 : 1) * (X.K / 2 + ngr * 4);
+      const int R = max(1, min(32, (CH - (gated_up ? 32 : 16)) / rowb));
+      int64_t b, e;
+      span(static_cast<int64_t>(nu) * X.n_rows, c, G, b, e);
+      FzSeg* last = nullptr;
+      while (b < e) {
+        const int u = static_cast<int>(b / X.n_rows);
+        const int n0 = static_cast<int>(b - static_cast<int64_t>(u) * X.n_rows);
+        const int n1 = static_cast<int>(min(static_cast<int64_t>(X.n_rows), n0 + (e - b)));
+        const int64_t ex = __ldcg(X.meta + 1 + u);
+        const int pa = __ldcg(X.meta + 1 + X.umax + u), pe = __ldcg(X.meta + 2 + X.umax + u);
+        FzSeg* S = add();
+        if (!S) break;
+        S->kind = kind; S->stage = ST_EXP; S->nsub = max(1, (pe - pa + PB - 1) / PB);
+        S->wait_ctr = wctr; S->wait_tgt = wtgt; S->sig = -1;
+        S->row0 = n0; S->nrows = pe > pa ? n1 - n0 : 0;
+        S->w = nullptr; S->dt = 0; S->esz = 0; S->K = X.K; S->col0 = u; S->epi = 0;
+        S->q = reinterpret_cast<const char*>(X.q) + ex * X.n_rows * (X.K / 2);
+        S->sb = reinterpret_cast<const char*>(X.sb) + ex * X.n_rows * ngr * 4;
+        S->q2 = gated_up ? reinterpret_cast<const char*>(X.q_gate) + ex * X.n_rows * (X.K / 2) : nullptr;
+        S->sb2 = gated_up ? reinterpret_cast<const char*>(X.sb_gate) + ex * X.n_rows * ngr * 4 : nullptr;
+        S->pa = pa; S->np = max(0, pe - pa); S->R = R;
+        last = S;
+        b += n1 - n0;
       }
-      fz_expect_tx(bar + s, tx);
-      fz_bulk(dst, J.w + static_cast<int64_t>(r) * (X.K / 2), qb, bar + s);
-      fz_bulk(dst + qb, reinterpret_cast<const void*>(sa0), sbb, bar + s);
-      if (J.w2) {
-        fz_bulk(dst + qb + sbb, J.w2 + static_cast<int64_t>(r) * (X.K / 2), qb, bar + s);
-        fz_bulk(dst + 2 * qb + sbb, reinterpret_cast<const void*>(sa2_0), sbb2, bar + s);
+      if (!last) {
+        // no rows here: an empty segment carries the signal
+        last = add();
+        if (!last) return;
+        last->kind = kind; last->stage = -1; last->nsub = 1; last->wait_ctr = -1; last->wait_tgt = 0;
+        last->row0 = 0; last->nrows = 0; last->w = nullptr; last->dt = 0; last->esz = 0; last->K = X.K;
+        last->col0 = 0; last->epi = 0; last->q = last->sb = last->q2 = last->sb2 = nullptr;
+        last->pa = 0; last->np = 0; last->R = 1;
       }
-    } else {
-      const int esz = P.dt == DT_FP32 ? 4 : 2;
-      const int r = J.row0 + lc * J.R, n = min(J.R, J.row0 + J.nrows - r);
-      const uint32_t bytes = static_cast<uint32_t>(n) * P.K * esz;
-      fz_expect_tx(bar + s, bytes);
-      fz_bulk(dst, J.w + static_cast<int64_t>(r) * P.K * esz, bytes, bar + s);
+      last->sig = sig;
+    };
+    auto sdpart = [&](int pct0, int pct1, int sig) {
+      int64_t b, e;
+      span(A.H, c, G, b, e);
+      const int64_t n = e - b;
+      FzSeg* S = add();
+      if (!S) return;
+      S->kind = SK_DENSE; S->stage = ST_SH; S->nsub = passes;
+      S->wait_ctr = FZ_DIN; S->wait_tgt = G - 1; S->sig = sig;
+      S->row0 = static_cast<int>(b + n * pct0 / 100); S->nrows = static_cast<int>(n * pct1 / 100 - n * pct0 / 100);
+      S->w = static_cast<const char*>(A.sh_down); S->dt = A.x_dt; S->esz = 2; S->K = A.Fs;
+      S->col0 = S->row0; S->epi = EP_SD;
+      S->q = S->sb = S->q2 = S->sb2 = nullptr; S->pa = 0; S->np = 0; S->R = 1;
+    };
+    experts(SK_UP, A.up, GATED, A.L ? FZ_FC1 : -1, G - 1, FZ_UP);
+    const int pre = A.sd_pre, mid = min(100, A.sd_pre + A.sd_mid);
+    if (A.Fs) sdpart(pre, mid, -1);
+    experts(SK_DN, A.dn, false, FZ_UP, G, FZ_DN);
+    if (A.Fs) sdpart(mid, 100, FZ_SD);
+    if (A.L) {
+      int64_t b, e;
+      span(A.H, c, G, b, e);
+      FzSeg* S = add();
+      if (S) {
+        S->kind = SK_DENSE; S->stage = ST_Y; S->nsub = passes;
+        S->wait_ctr = FZ_COMB; S->wait_tgt = G; S->sig = -1;
+        S->row0 = static_cast<int>(b); S->nrows = static_cast<int>(e - b);
+        S->w = static_cast<const char*>(A.fc2); S->dt = A.x_dt; S->esz = 2; S->K = A.L;
+        S->col0 = S->row0; S->epi = EP_OUT;
+        S->q = S->sb = S->q2 = S->sb2 = nullptr; S->pa = 0; S->np = 0; S->R = 1;
+      }
     }
-    sh->issued = seq + 1;
+    __threadfence_block();
+    sh->nsegs = ns;
   };
 
-  // thread 0: issue while a slot is free and the next chunk is known
-  auto produce = [&](int consumed) {
-    // one poll of the routing flag per call while the issue order waits on it
-    if ((step == 3 || step == 4) && !sh->routed && ld_acquire(sync + FZ_ROUTED * FZ_SYNC_STRIDE) >= 1)
-      sh->routed = 1;
-    if (sh->routed && !sh->ph[PH_UP].ready) {
-      build_expert(PH_UP, A.up, GATED);
-      build_expert(PH_DN, A.dn, false);
-      if (sh->ph[PH_UP].nchunks == 0) fz_post(sync + FZ_UP * FZ_SYNC_STRIDE);
-      if (sh->ph[PH_DN].nchunks == 0) fz_post(sync + FZ_DN * FZ_SYNC_STRIDE);
-    }
-    while (sh->issued - consumed < S && step < 9) {
-      if (step == 3) {
-        const FzPhase& Ps = sh->ph[PH_SD];
-        if (sh->routed) { ++step; continue; }
-        if (cur[PH_SD] < Ps.nchunks * Ps.passes) { issue(PH_SD, cur[PH_SD]++); continue; }
-        break;   // nothing to issue until the routing is published
-      }
-      if (step == 4 && !sh->routed) break;
-      const int p = step == 0 ? PH_ROUTER : step == 1 ? PH_FC1 : step == 2 ? PH_SHIN
-                  : step == 4 ? PH_UP : step == 6 ? PH_DN : step == 8 ? PH_OUT : PH_SD;
-      const FzPhase& P = sh->ph[p];
-      const int total = P.nchunks * P.passes;
-      if (step == 5) {
-        if (sd_mid_left > 0 && cur[PH_SD] < total) { --sd_mid_left; issue(PH_SD, cur[PH_SD]++); continue; }
-        ++step;
-        continue;
-      }
-      if (cur[p] < total) { issue(p, cur[p]++); continue; }
-      ++step;
-    }
-    sh->done_all = step >= 9;
-  };
-
-  // ---- consumer loop (all threads) ----
-  int consumed = 0;
-  int done_cnt[PH_N];
-  for (int p = 0; p < PH_N; ++p) done_cnt[p] = 0;
-  int staged = -1;          // what xs holds: kind * 65536 + pass (dense), 0x40000 + job (expert)
-  uint32_t waited = 0;      // dependency waits already satisfied (bit per counter)
+  // ---- consume the segments ----
+  uint32_t waited = 0;      // counters already waited for (bit per counter)
+  int staged = -1;          // what the staging area holds
   bool comb_done = false;
   auto need = [&](int ctr, int target) {
-    if (waited & (1u << ctr)) return;
+    if (ctr < 0 || (waited & (1u << ctr))) return;
     ok = fz_wait(sync + ctr * FZ_SYNC_STRIDE, target, A.status, ok);
     waited |= 1u << ctr;
   };
@@ -700,91 +710,100 @@ __global__ void __launch_bounds__(NT, TB >= 8 ? 1 : 2) k_fused(const __grid_cons
     comb_done = true;
   };
 
-  while (true) {
-    if (tid == 0) produce(consumed);
-    __syncthreads();
-    if (consumed == sh->issued) {
-      if (sh->done_all || !ok) break;
-      // the ring is empty and the next chunks need the routing
+  bool rest_built = false;
+  for (int si = 0;; ++si) {
+    if (si == sh->nsegs) {
+      if (rest_built) break;
+      // the remaining segments need the routing
       need(FZ_ROUTED, 1);
+      if (tid == 0 && ok) build_rest();
+      __syncthreads();
+      rest_built = true;
       if (!ok) break;
-      continue;
+      produce();
+      if (si == sh->nsegs) break;
     }
-    const int s = consumed % S;
-    const int p = sh->slot_phase[s], i = sh->slot_idx[s];
-    const FzPhase& P = sh->ph[p];
-    int j, pass, lc;
-    locate(P, i, j, pass, lc);
-    const FzJob& J = P.job[j];
-    // dependencies of the phase
-    if (p == PH_SD) need(FZ_DIN, G - 1);
-    if (p == PH_UP && A.L) need(FZ_FC1, G - 1);
-    if (p == PH_DN) need(FZ_UP, G);
-    if (p == PH_OUT) {
-      if (!comb_done) combine();
-      need(FZ_COMB, G);
-      need(FZ_SD, G);
+    const FzSeg& S = sh->seg[si];
+    if (si == 0 || sh->seg[si - 1].kind != S.kind) {
+      if (S.kind == SK_UP) stamp(4);
+      if (S.kind == SK_DN) stamp(7);
     }
-    const bool wok = __syncthreads_and(tid != 0 || fz_mbar_wait(bar + s, (consumed / S) & 1)) != 0;
-    if (!wok && tid == 0) atomicOr(A.status, STATUS_TIMEOUT);
-    ok = ok && wok;
-    const char* slot = ring + static_cast<size_t>(s) * SB;
-    if (p == PH_UP || p == PH_DN) {
-      const ExpertArgs& X = (p == PH_UP) ? A.up : A.dn;
-      const int nrc = (J.nrows + J.R - 1) / J.R;
-      const int g = lc / nrc, rc = lc - g * nrc;
-      const int r = J.row0 + rc * J.R, n = min(J.R, J.row0 + J.nrows - r);
-      const int pa = J.pa + g * PB, np = min(PB, J.np - g * PB);
-      const int tag = 0x40000 + (p << 12) + (j << 6) + g;
-      if (ok && staged != tag) {
-        fz_stage_expert<PB>(X, pa, np, xs4, sh->pid);
-        staged = tag;
+    // dependencies
+    if (S.stage == ST_Y && !comb_done) combine();
+    if (S.stage == ST_Y && A.Fs) need(FZ_SD, G);
+    need(S.wait_ctr, S.wait_tgt);
+    const int per = fz_sub_chunks(S, warp, CH);
+    for (int sub = 0; sub < S.nsub; ++sub) {
+      // the staged vector of the sub-round
+      const int t0 = sub * TB;
+      const int pa = S.pa + sub * PB, np = min(PB, S.np - sub * PB);
+      if (S.stage >= 0) {
+        const int tag = S.stage == ST_EXP ? (0x40000 + si * 256 + sub) : (S.stage * 256 + sub);
+        if (tag != staged) {
+          __syncthreads();   // every warp is done with the previous vector
+          if (S.stage == ST_EXP) {
+            fz_stage_expert<PB>(S.kind == SK_UP ? A.up : A.dn, pa, np, xs4, sh->pid);
+          } else {
+            fz_stage_dense<TB>(A, S.stage == ST_X ? 0 : S.stage == ST_SH ? 1 : 2, t0, min(TB, T - t0), S.K,
+                               xs4);
+            __syncthreads();
+          }
+          staged = tag;
+        }
       }
-      const int ngr = X.K / X.G;
-      const uint32_t qb = static_cast<uint32_t>(n) * (X.K / 2);
-      const uint64_t sa = reinterpret_cast<uint64_t>(J.sb + static_cast<int64_t>(r) * ngr * 4);
-      const uint32_t off = static_cast<uint32_t>(sa & 15);
-      const uint32_t sbb = static_cast<uint32_t>((off + static_cast<uint64_t>(n) * ngr * 4 + 15) & ~uint64_t(15));
-      const uint32_t* sbp = reinterpret_cast<const uint32_t*>(slot + qb + off);
-      const char* q2 = nullptr;
-      const uint32_t* sb2p = nullptr;
-      if (J.w2) {
-        const uint64_t sa2 = reinterpret_cast<uint64_t>(J.sb2 + static_cast<int64_t>(r) * ngr * 4);
-        q2 = slot + qb + sbb;
-        sb2p = reinterpret_cast<const uint32_t*>(slot + 2 * qb + sbb + (sa2 & 15));
+      if (si == 0) dstamp(2);
+      // this warp's chunks of the sub-round
+      float acc[TB];
+#pragma unroll
+      for (int t = 0; t < TB; ++t) acc[t] = 0.f;
+      for (int ci = 0; ci < per; ++ci) {
+        const int sl = consumed % D;
+        // (a copy that never lands only skips this warp's work: control flow
+        // stays uniform, the status word records it)
+        const bool wok = fz_mbar_wait(bar + sl, (consumed / D) & 1);
+        if (si == 0) dstamp(3 + 2 * min(ci, 2));
+        if (!wok && lane == 0) atomicOr(A.status, STATUS_TIMEOUT);
+        const char* slot = ring + static_cast<size_t>(sl) * CH;
+        const FzChunk C = fz_chunk(S, warp, ci, CH);
+        if (ok && wok) {
+          if (S.kind == SK_DENSE) {
+            fz_dense_piece<TB>(A, S, slot, C.r, C.boff, C.nb, C.last, xs4, t0, min(TB, T - t0), acc);
+          } else {
+            const ExpertArgs& X = S.kind == SK_UP ? A.up : A.dn;
+            const int ngr = X.K / X.G;
+            const uint32_t qb = static_cast<uint32_t>(C.n) * (X.K / 2);
+            const uint64_t sa = reinterpret_cast<uint64_t>(S.sb + static_cast<int64_t>(C.r) * ngr * 4);
+            const uint32_t off = static_cast<uint32_t>(sa & 15);
+            const uint32_t sbb = static_cast<uint32_t>((off + static_cast<uint64_t>(C.n) * ngr * 4 + 15) & ~uint64_t(15));
+            const uint32_t* sbp = reinterpret_cast<const uint32_t*>(slot + qb + off);
+            if (S.kind == SK_UP && S.q2) {
+              const uint64_t sa2 = reinterpret_cast<uint64_t>(S.sb2 + static_cast<int64_t>(C.r) * ngr * 4);
+              fz_expert_rows<PB, GATED>(X, slot, sbp, slot + qb + sbb,
+                                        reinterpret_cast<const uint32_t*>(slot + 2 * qb + sbb + (sa2 & 15)),
+                                        C.n, C.r, xs4, sh->pid, np);
+            } else {
+              fz_expert_rows<PB, false>(X, slot, sbp, nullptr, nullptr, C.n, C.r, xs4, sh->pid, np);
+            }
+          }
+        }
+        __syncwarp();   // every lane is done with the slot
+        if (si == 0) dstamp(4 + 2 * min(ci, 2));
+        ++consumed;
+        produce();
       }
-      if (ok) {
-        if (p == PH_UP)
-          fz_expert_chunk<PB, GATED>(X, slot, sbp, q2, sb2p, n, r, xs4, sh->pid, np);
-        else
-          fz_expert_chunk<PB, false>(X, slot, sbp, nullptr, nullptr, n, r, xs4, sh->pid, np);
-      }
-    } else {
-      const int kind = (p == PH_SD) ? 1 : (p == PH_OUT) ? 2 : 0;
-      const int t0 = pass * TB, tb = min(TB, T - t0);
-      const int tag = kind * 65536 + pass;
-      if (ok && staged != tag) {
-        fz_stage_dense<TB>(A, kind, t0, tb, P.K, xs4);
-        __syncthreads();
-        staged = tag;
-      }
-      const int r = J.row0 + lc * J.R, n = min(J.R, J.row0 + J.nrows - r);
-      FzEpi ep;
-      ep.mode = (p == PH_OUT) ? 1 : 0;
-      ep.out = (p == PH_SD) ? A.sdbuf : A.dense_in;
-      ep.ld = (p == PH_SD) ? A.H : A.din_rows;
-      if (ok) fz_dense_chunk<TB>(A, slot, n, J.R, P.K, P.dt, xs4, red, t0, tb, J.col + (r - J.row0), ep);
     }
-    __syncthreads();   // the slot, the staging and the reduction area are free again
-    ++consumed;
-    if (++done_cnt[p] == P.nchunks * P.passes) {
-      const int sg = p == PH_ROUTER ? FZ_ROUTER : p == PH_FC1 ? FZ_FC1 : p == PH_SHIN ? FZ_DIN
-                   : p == PH_SD ? FZ_SD : p == PH_UP ? FZ_UP : p == PH_DN ? FZ_DN : -1;
-      if (sg >= 0 && tid == 0) fz_post(sync + sg * FZ_SYNC_STRIDE);
-      if (p == PH_SHIN) stamp(3);
-      if (p == PH_UP) stamp(5);
-      if (p == PH_DN) stamp(8);
-      if (p == PH_SD) stamp(9);
+    if (si == 0 && seg_limit == 1) {
+      seg_limit = FZ_MAX_SEGS;
+      produce();
+    }
+    if (S.sig >= 0) {
+      __syncthreads();
+      if (si == 0) dstamp(9);
+      if (tid == 0) fz_post(sync + S.sig * FZ_SYNC_STRIDE);
+      if (S.sig == FZ_DIN) stamp(3);
+      if (S.sig == FZ_UP) stamp(5);
+      if (S.sig == FZ_DN) stamp(8);
+      if (S.sig == FZ_SD) stamp(9);
     }
   }
   stamp(10);
@@ -794,7 +813,7 @@ __global__ void __launch_bounds__(NT, TB >= 8 ? 1 : 2) k_fused(const __grid_cons
     if (!comb_done) combine();
   } else {
     need(FZ_DN, G);
-    need(FZ_SD, G);
+    if (A.Fs) need(FZ_SD, G);
     int64_t b, e;
     span(static_cast<int64_t>(T) * A.H, c, G, b, e);
     for (int64_t i = b + tid; ok && i < e; i += NT) {
@@ -839,11 +858,11 @@ cudaError_t fused_launch_tb8(const FusedArgs& a, bool gated, size_t smem, int nu
                              FusedLaunchCache* cache, cudaStream_t s);
 
 // Token-pair slots per staging group of k_fused<TB, .>.
-__host__ __device__ constexpr int fused_pb(int tb) { return tb <= 1 ? 1 : 2; }
+__host__ __device__ constexpr int fused_pb(int tb) { return tb <= 1 ? 1 : (tb <= 4 ? 2 : 4); }
 
-// Shared memory of k_fused<TB, PB>: ring, barriers, bookkeeping, reduction
-// area, then the largest staged vector (or the routing block's scratch).
-inline size_t fused_smem_bytes(int tb, int slots, int slot_bytes, int H, int Fs, int L, int kin, int F,
+// Shared memory of k_fused<TB, PB>: warp rings, their barriers, the segment
+// list, then the largest staged vector (or the routing block's scratch).
+inline size_t fused_smem_bytes(int tb, int depth, int chunk_bytes, int H, int Fs, int L, int kin, int F,
                                size_t route_bytes) {
   const int pb = fused_pb(tb);
   const int mx = H > Fs ? (H > L ? H : L) : (Fs > L ? Fs : L);
@@ -853,8 +872,8 @@ inline size_t fused_smem_bytes(int tb, int slots, int slot_bytes, int H, int Fs,
   st = st > e1 ? st : e1;
   st = st > e2 ? st : e2;
   st = st > route_bytes ? st : route_bytes;
-  return static_cast<size_t>(slots) * slot_bytes + FZ_MAX_SLOTS * 8 + ((sizeof(FzShared) + 15) & ~size_t(15)) +
-         NW * 8 * 4 + st;
+  return static_cast<size_t>(NW) * depth * chunk_bytes + NW * FZ_MAX_DEPTH * 8 +
+         ((sizeof(FzShared) + 15) & ~size_t(15)) + st;
 }
 
 }  // namespace moe

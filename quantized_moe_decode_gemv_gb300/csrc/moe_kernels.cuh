@@ -229,6 +229,15 @@ __device__ __forceinline__ bool key_better(float a, int ia, float b, int ib) {
   return a > b || (a == b && ia < ib);
 }
 
+// Signed integers in the order of the floats (for keys without NaN and -0).
+__device__ __forceinline__ int ordered_bits(float f) {
+  const int b = __float_as_int(f);
+  return b >= 0 ? b : (b ^ 0x7fffffff);
+}
+__device__ __forceinline__ float from_ordered_bits(int b) {
+  return __int_as_float(b >= 0 ? b : (b ^ 0x7fffffff));
+}
+
 // Shared memory of route_block: two int arrays of MAX_E and 2 x 32 ints, plus
 // E * mask_words words of row bitmasks when A.mask_words > 0.
 constexpr int ROUTE_CAND_WORDS = 32 * MAX_K * 3;   // per-warp candidate lists (32 warps max)
@@ -263,14 +272,14 @@ __device__ __forceinline__ void topk_rounds(float (&kv)[NPL], const int (&ev)[NP
         tix[i] = b1 ? tix[i + w] : tix[i];
       }
     }
-    float bk = tk[0];
-    int bi = tix[0];
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (key_better(ok, oi, bk, bi)) { bk = ok; bi = oi; }
-    }
+    // warp best: the largest key by an integer max over order-preserving
+    // bits (keys carry no -0 and no NaN), then the smallest expert id among
+    // the lanes that hold it
+    const int ik = ordered_bits(tk[0]);
+    const int mx = __reduce_max_sync(0xffffffffu, ik);
+    const int bi = static_cast<int>(__reduce_min_sync(
+        0xffffffffu, ik == mx ? static_cast<unsigned>(tix[0]) : 0xffffffffu));
+    const float bk = from_ordered_bits(mx);
     // the owner lane retires the key and publishes its weight input
     float ws = 0.f;
     int owner = -1;
@@ -313,7 +322,7 @@ __device__ __forceinline__ void route_member(const RouteArgs& A, const float* z,
         sv[i] = sg;                        // weight: score without bias
       }
       if (!isfinite(key)) { bad = true; key = -INFINITY; }
-      kv[i] = key;
+      kv[i] = key + 0.0f;   // -0 -> +0: equal keys compare equal as integers too
     } else {
       kv[i] = -INFINITY;
     }
@@ -425,6 +434,38 @@ static __device__ __noinline__ void route_block(const RouteArgs& A, int* smem) {
   }
   // ---- distinct experts and their pairs ----
   if (A.debug_times) tp[1] = global_ns();
+  if (A.T * k <= 32) {
+    // few pairs: one warp sorts them by (expert, pair) with a bitonic network;
+    // the first pair of each expert opens its group
+    __syncthreads();
+    if (warp == 0) {
+      const int P = A.T * k;
+      int v = lane < P ? ((A.ids[lane] << 5) | lane) : 0x7fffffff;
+#pragma unroll
+      for (int k2 = 2; k2 <= 32; k2 <<= 1) {
+#pragma unroll
+        for (int j = k2 >> 1; j > 0; j >>= 1) {
+          const int o = __shfl_xor_sync(0xffffffffu, v, j);
+          const bool asc = (lane & k2) == 0, low = (lane & j) == 0;
+          v = (low == asc) ? min(v, o) : max(v, o);
+        }
+      }
+      const bool valid = lane < P;
+      const int prev = __shfl_up_sync(0xffffffffu, v, 1);
+      const bool open = valid && (lane == 0 || (prev >> 5) != (v >> 5));
+      const unsigned om = __ballot_sync(0xffffffffu, open);
+      const int u = __popc(om & ((2u << lane) - 1u)) - 1;
+      int* uniq_e = A.meta + 1;
+      int* uniq_p0 = A.meta + 1 + A.umax;
+      int* pairs = A.meta + 2 + 2 * A.umax;
+      if (open) { uniq_e[u] = v >> 5; uniq_p0[u] = lane; }
+      if (valid) pairs[lane] = v & 31;
+      if (lane == 0) { A.meta[0] = __popc(om); uniq_p0[__popc(om)] = P; }
+    }
+    if (A.debug_times && tid == 0)
+      printf("route phases (ns): topk %llu list %llu\n", tp[1] - tp[0], global_ns() - tp[1]);
+    return;
+  }
   for (int e = tid; e < MAX_E; e += nthr) s_cnt[e] = 0;
   __syncthreads();
   if (A.debug_times) tp[2] = global_ns();

@@ -84,7 +84,10 @@ struct moe_layer {
   int kin = 0;
   int grouped_min_t = 64;
   int fused_max_t = 0;    // AUTO: the persistent kernel for T <= this (below grouped_min_t)
-  int fused_sd_mid = 2;   // persistent kernel: shared-down chunks between the expert up and down rows
+  int fused_sd_pre = 60;  // persistent kernel: percent of a CTA's shared-down rows before the experts,
+  int fused_sd_mid = 20;  // and between the expert up and down rows
+  int fused_depth = 4;    // slots per warp ring (at most)
+  int fused_chunk = 4096; // slot bytes (at least)
   FusedLaunchCache fused_grid[4][2];  // cooperative grid of k_fused<TB, ., gated>
   int last_launches = 0;  // kernel launches of the last forward
   unsigned long long* fz_trace = nullptr;   // diagnostics (MOE_FUSED_TRACE): phase stamps
@@ -380,7 +383,10 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   if (const char* env = std::getenv("MOE_GROUPED_MIN_T")) L->grouped_min_t = std::max(1, std::atoi(env));
   if (const char* env = std::getenv("MOE_PDL")) L->use_pdl = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_FUSED_MAX_T")) L->fused_max_t = std::atoi(env);
-  if (const char* env = std::getenv("MOE_SD_MID")) L->fused_sd_mid = std::max(0, std::atoi(env));
+  if (const char* env = std::getenv("MOE_SD_PRE")) L->fused_sd_pre = std::max(0, std::min(100, std::atoi(env)));
+  if (const char* env = std::getenv("MOE_SD_MID")) L->fused_sd_mid = std::max(0, std::min(100, std::atoi(env)));
+  if (const char* env = std::getenv("MOE_FZ_DEPTH")) L->fused_depth = std::max(2, std::atoi(env));
+  if (const char* env = std::getenv("MOE_FZ_CHUNK")) L->fused_chunk = std::max(1024, std::atoi(env)) & ~127;
   const bool want_trace = std::getenv("MOE_FUSED_TRACE") && std::atoi(std::getenv("MOE_FUSED_TRACE"));
   if (const char* env = std::getenv("MOE_PREFETCH")) L->prefetch = std::atoi(env);
   if (const char* env = std::getenv("MOE_EXPERT_PB")) L->expert_pb = std::max(1, std::min(8, std::atoi(env)));
@@ -529,38 +535,40 @@ static cudaError_t launch_umma(moe_layer* h, UmmaArgs& a, int T, cudaStream_t s,
 
 }  // extern "C"
 
-// Plan of a persistent-kernel launch: staged token rows per pass, ring slots
-// and slot size, and the shared memory of one CTA.
+// Plan of a persistent-kernel launch: staged token rows per pass, per-warp
+// ring depth and slot size, and the shared memory of one CTA.
 struct FusedPlan {
-  int tb = 0, slots = 0, slot_bytes = 0;
+  int tb = 0, depth = 0, chunk = 0;
   size_t smem = 0;
 };
 
 static FusedPlan fused_plan(const moe_layer* h, int T, int mask_words) {
   const moe_layer_config& c = h->cfg;
   FusedPlan fp;
+  if (T > 32) return fp;   // the segment list is sized for up to 32 token rows
   const int H = c.hidden, Fs = c.shared_ffn, L = c.latent, F = c.expert_ffn, kin = h->kin;
-  const int rd = dt_size(c.router_dtype), ad = dt_size(c.act_dtype);
-  // a slot holds at least one row of every dense matrix and of every expert matrix
-  int row = std::max(H * rd, H * ad);
-  if (Fs) row = std::max(row, Fs * ad);
-  if (L) row = std::max(row, L * ad);
+  // a slot holds at least one expert row (dense rows are split over slots)
   const int gm = c.act == MOE_ACT_SWIGLU ? 2 : 1;
-  row = std::max(row, gm * (kin / 2 + (kin / c.group_size) * 4) + 32);
-  row = std::max(row, F / 2 + (F / c.group_size) * 4 + 16);
-  const int sb = std::max(16384, (row + 127) & ~127);
+  int row = std::max(gm * (kin / 2 + (kin / c.group_size) * 4) + 32, F / 2 + (F / c.group_size) * 4 + 16);
+  const int chunk = std::max(h->fused_chunk, (row + 127) & ~127);
   const size_t route = ROUTE_SMEM_BYTES + static_cast<size_t>(c.n_experts) * mask_words * 4;
   for (int tb = pow2_at_least(T, 8); tb >= 1; tb >>= 1) {
-    const size_t base = fused_smem_bytes(tb, 0, sb, H, Fs, L, kin, F, route);
-    // two CTAs per SM when three or more slots fit beside the staging, else one
+    // two CTAs per SM when a ring of depth 2 fits, else one CTA with deeper rings
     const size_t two = 112 * 1024, one = static_cast<size_t>(kSmemMax) - 2048;
-    size_t budget = (tb < 8 && base + 3ull * sb <= two) ? two : one;
-    if (base + 2ull * sb > budget) continue;
-    fp.tb = tb;
-    fp.slot_bytes = sb;
-    fp.slots = static_cast<int>(std::min<size_t>(FZ_MAX_SLOTS, (budget - base) / sb));
-    fp.smem = fused_smem_bytes(tb, fp.slots, sb, H, Fs, L, kin, F, route);
-    return fp;
+    for (int pass = 0; pass < 2; ++pass) {
+      const size_t budget = pass == 0 ? two : one;
+      if (pass == 0 && tb >= 8) continue;   // TB = 8 is compiled for one CTA per SM
+      for (int d = std::min(h->fused_depth, FZ_MAX_DEPTH); d >= 2; --d) {
+        const size_t sm = fused_smem_bytes(tb, d, chunk, H, Fs, L, kin, F, route);
+        if (sm <= budget) {
+          fp.tb = tb;
+          fp.depth = d;
+          fp.chunk = chunk;
+          fp.smem = sm;
+          return fp;
+        }
+      }
+    }
   }
   return fp;
 }
@@ -600,6 +608,10 @@ static void print_fused_trace(moe_layer* h, cudaStream_t s) {
       std::fprintf(stderr, "  stamp %2d: %7.2f %7.2f %7.2f  (cta0 %.2f)\n", i, v.front(), v[v.size() / 2],
                    v.back(), c0);
   }
+  std::fprintf(stderr, "  CTA 1 detail:");
+  for (int i = 13; i < 25; ++i)
+    std::fprintf(stderr, " %.2f", t[FZ_TRACE + i] ? (t[FZ_TRACE + i] - t0) * 1e-3 : -1.0);
+  std::fprintf(stderr, "\n");
 }
 
 // The path a forward of T rows takes (never AUTO).
@@ -740,8 +752,9 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     fa.delta = delta;
     fa.sync = h->fsync;
     fa.status = h->status;
-    fa.slots = fzp.slots;
-    fa.slot_bytes = fzp.slot_bytes;
+    fa.depth = fzp.depth;
+    fa.chunk_bytes = fzp.chunk;
+    fa.sd_pre = h->fused_sd_pre;
     fa.sd_mid = h->fused_sd_mid;
     fa.trace = h->fz_trace;
     if (h->fz_trace) cudaMemsetAsync(h->fz_trace, 0, 4096 * FZ_TRACE * 8, s);

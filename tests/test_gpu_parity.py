@@ -239,8 +239,9 @@ def test_path_selection_and_launch_counts():
         h.forward(x[:1].contiguous())
         assert h.last_launch_count() >= 4
         h.set_path("fused")
-        assert h.path_for(64) == "fused"
-        h.forward(x)
+        assert h.path_for(32) == "fused"
+        assert h.path_for(33) == "gemv"   # the persistent kernel serves up to 32 rows
+        h.forward(x[:32].contiguous())
         assert h.last_launch_count() == 1
         h.set_path("grouped")
         assert h.path_for(1) == "grouped"
