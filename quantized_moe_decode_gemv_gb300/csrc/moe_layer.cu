@@ -93,6 +93,7 @@ struct moe_layer {
   unsigned long long* fz_trace = nullptr;   // diagnostics (MOE_FUSED_TRACE): phase stamps
   int use_pdl = 1;        // programmatic dependent launch between the gemv-path kernels
   int expert_pb = 2;      // max token slots per pass of the gemv-path expert kernels
+  int expert_target = 4;  // gemv-path expert kernels: CTAs per SM the grid is sized for
   int fuse_route = 1;     // routing in the last router CTA of the dense pass (0: own kernel)
   int debug_route = 0;    // diagnostics: print routing phase times
   int prefetch = 6;       // bit 0: experts' up weights from the routing CTA (one SM's
@@ -390,6 +391,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   const bool want_trace = std::getenv("MOE_FUSED_TRACE") && std::atoi(std::getenv("MOE_FUSED_TRACE"));
   if (const char* env = std::getenv("MOE_PREFETCH")) L->prefetch = std::atoi(env);
   if (const char* env = std::getenv("MOE_EXPERT_PB")) L->expert_pb = std::max(1, std::min(8, std::atoi(env)));
+  if (const char* env = std::getenv("MOE_EXPERT_TARGET")) L->expert_target = std::max(1, std::min(16, std::atoi(env)));
   if (const char* env = std::getenv("MOE_FUSE_ROUTE")) L->fuse_route = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_DEBUG_ROUTE")) L->debug_route = std::atoi(env) != 0;
   {
@@ -899,7 +901,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     // at least 8 rows per CTA
     // slots: at most min(E, T*k) distinct experts in this call
     const int slots = std::min(E, T * k);
-    const int target = h->num_sms * 4;
+    const int target = h->num_sms * h->expert_target;
     up.cps = std::max(1, std::min(std::max(1, F / 8), (target + slots - 1) / slots));
     const int grid_up = slots * up.cps;
     mark(2);
