@@ -94,6 +94,7 @@ struct moe_layer {
   int use_pdl = 1;        // programmatic dependent launch between the gemv-path kernels
   int expert_pb = 2;      // max token slots per pass of the gemv-path expert kernels
   int expert_target = 4;  // gemv-path expert kernels: CTAs per SM the grid is sized for
+  int umma_ctas = 2;      // grouped path: resident CTAs per SM (2 when the TMEM columns allow)
   int fuse_route = 1;     // routing in the last router CTA of the dense pass (0: own kernel)
   int debug_route = 0;    // diagnostics: print routing phase times
   int prefetch = 6;       // bit 0: experts' up weights from the routing CTA (one SM's
@@ -392,6 +393,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   if (const char* env = std::getenv("MOE_PREFETCH")) L->prefetch = std::atoi(env);
   if (const char* env = std::getenv("MOE_EXPERT_PB")) L->expert_pb = std::max(1, std::min(8, std::atoi(env)));
   if (const char* env = std::getenv("MOE_EXPERT_TARGET")) L->expert_target = std::max(1, std::min(16, std::atoi(env)));
+  if (const char* env = std::getenv("MOE_UMMA_CTAS")) L->umma_ctas = std::max(1, std::min(2, std::atoi(env)));
   if (const char* env = std::getenv("MOE_FUSE_ROUTE")) L->fuse_route = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_DEBUG_ROUTE")) L->debug_route = std::atoi(env) != 0;
   {
@@ -500,11 +502,10 @@ moe_status moe_layer_destroy(moe_layer* h) {
 }
 
 // Tokens per MMA and ring depth for a grouped launch, and its shared memory.
-static size_t umma_config(UmmaArgs& a, int T) {
+static size_t umma_config(UmmaArgs& a, int T, size_t budget) {
   const bool gated = a.a_mode == UA_INT4 && a.q2 != nullptr;
   const int cap = a.a_mode == UA_DENSE ? 256 : 64;
   a.n_tile = std::min(cap, (std::max(1, T) + 15) & ~15);
-  const size_t budget = 220 * 1024;
   int st = UM_MAX_STAGES;
   while (st > 3 && umma_plan(a.a_mode, gated, a.n_tile, st).total > budget) --st;
   a.stages = st;
@@ -514,16 +515,20 @@ static size_t umma_config(UmmaArgs& a, int T) {
 // A grouped launch; a dense matrix with fewer 128-row tiles than SMs splits K
 // over several CTAs and sums the partials in a second, deterministic pass.
 static cudaError_t launch_umma(moe_layer* h, UmmaArgs& a, int T, cudaStream_t s, int* nl) {
-  const size_t smem = umma_config(a, T);
+  // two CTAs per SM when the accumulators fit twice in TMEM (256 columns each:
+  // not gated), so that one CTA's copies and dequantisation overlap the other's
+  const bool gated = a.a_mode == UA_INT4 && a.q2 != nullptr;
+  const int per_sm = (h->umma_ctas >= 2 && !gated) ? 2 : 1;
+  const size_t smem = umma_config(a, T, per_sm == 2 ? 110 * 1024 : 220 * 1024);
   a.ksplit = 1;
   if (!a.experts) {
     const int mtiles = (a.n_rows + UM_M - 1) / UM_M, nkc = a.K / UM_KC;
-    int ks = (h->num_sms + mtiles - 1) / mtiles;
+    int ks = (h->num_sms * per_sm + mtiles - 1) / mtiles;
     ks = std::min(ks, std::min(std::max(1, nkc / 4), UM_MAX_KSPLIT));
     a.ksplit = std::max(1, ks);
     a.part = h->part;
   }
-  k_umma<<<h->num_sms, UM_THREADS, smem, s>>>(a);
+  k_umma<<<h->num_sms * per_sm, UM_THREADS, smem, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) ++*nl;
   if (e == cudaSuccess && a.ksplit > 1) {

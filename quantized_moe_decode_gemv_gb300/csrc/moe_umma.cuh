@@ -285,7 +285,7 @@ __device__ __forceinline__ void umma_epilogue(const UmmaArgs& A, int pid, int m,
   }
 }
 
-__global__ void __launch_bounds__(UM_THREADS, 1) k_umma(const __grid_constant__ UmmaArgs A) {
+__global__ void __launch_bounds__(UM_THREADS, 2) k_umma(const __grid_constant__ UmmaArgs A) {
   extern __shared__ __align__(1024) char um_smem[];
   const bool gated = (A.a_mode == UA_INT4) && A.q2 != nullptr;
   const UmmaPlan P = umma_plan(A.a_mode, gated, A.n_tile, A.stages);
