@@ -80,7 +80,7 @@ typedef enum moe_dtype { MOE_DTYPE_BF16 = 0, MOE_DTYPE_FP16 = 1, MOE_DTYPE_FP32 
  *   GEMV     the same arithmetic as five stream-ordered kernels.
  *   GROUPED  row-grouped tcgen05 GEMMs for the experts and dense projections
  *            (many token rows per forward).
- *   AUTO     GROUPED when T >= 64 (MOE_GROUPED_MIN_T), else FUSED when
+ *   AUTO     GROUPED when T >= 16 (MOE_GROUPED_MIN_T), else FUSED when
  *            T <= MOE_FUSED_MAX_T (default 0: off), else GEMV. */
 typedef enum moe_path {
   MOE_PATH_AUTO = 0,

@@ -558,7 +558,9 @@ static __device__ __noinline__ void route_block(const RouteArgs& A, int* smem) {
   }
 }
 
-constexpr int ROUTE_THREADS = 256;
+// The routing kernel of the grouped path: one warp per row for up to 16 rows
+// (route_block adapts to the block size; ~90 registers a thread).
+constexpr int ROUTE_THREADS = 512;
 
 static __global__ void __launch_bounds__(ROUTE_THREADS) k_route(const __grid_constant__ RouteArgs A) {
   extern __shared__ int route_smem[];

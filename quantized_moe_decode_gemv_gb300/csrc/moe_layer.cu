@@ -13,6 +13,7 @@
 #include "moe_layer.h"
 #include "moe_kernels.cuh"
 #include "moe_umma.cuh"
+#include "moe_umma2.cuh"
 #include "moe_fused.cuh"
 
 using namespace moe;
@@ -82,7 +83,7 @@ struct moe_layer {
   int r_in = 0, off_fc1 = 0, off_shg = 0, off_shu = 0;
   int umax = 0;
   int kin = 0;
-  int grouped_min_t = 64;
+  int grouped_min_t = 16;
   int fused_max_t = 0;    // AUTO: the persistent kernel for T <= this (below grouped_min_t)
   int fused_sd_pre = 60;  // persistent kernel: percent of a CTA's shared-down rows before the experts,
   int fused_sd_mid = 20;  // and between the expert up and down rows
@@ -95,6 +96,8 @@ struct moe_layer {
   int expert_pb = 2;      // max token slots per pass of the gemv-path expert kernels
   int expert_target = 4;  // gemv-path expert kernels: CTAs per SM the grid is sized for
   int umma_ctas = 2;      // grouped path: resident CTAs per SM (2 when the TMEM columns allow)
+  int umma_v = 0;         // grouped path GEMM: 1 = k_umma, 2 = warp-specialised roles (k_umma2),
+                          // 0 = k_umma2 up to 128 token rows, k_umma above
   int fuse_route = 1;     // routing in the last router CTA of the dense pass (0: own kernel)
   int debug_route = 0;    // diagnostics: print routing phase times
   int prefetch = 6;       // bit 0: experts' up weights from the routing CTA (one SM's
@@ -305,7 +308,7 @@ static cudaError_t set_smem_attrs() {
   MOE_SMEM_ATTR((k_expert<4, false>)) MOE_SMEM_ATTR((k_expert<8, false>))
   MOE_SMEM_ATTR((k_expert<1, true>)) MOE_SMEM_ATTR((k_expert<2, true>))
   MOE_SMEM_ATTR((k_expert<4, true>)) MOE_SMEM_ATTR((k_expert<8, true>))
-  MOE_SMEM_ATTR(k_umma) MOE_SMEM_ATTR(k_route)
+  MOE_SMEM_ATTR(k_umma) MOE_SMEM_ATTR(k_umma2) MOE_SMEM_ATTR(k_route)
 #undef MOE_SMEM_ATTR
   return e;
 }
@@ -394,6 +397,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   if (const char* env = std::getenv("MOE_EXPERT_PB")) L->expert_pb = std::max(1, std::min(8, std::atoi(env)));
   if (const char* env = std::getenv("MOE_EXPERT_TARGET")) L->expert_target = std::max(1, std::min(16, std::atoi(env)));
   if (const char* env = std::getenv("MOE_UMMA_CTAS")) L->umma_ctas = std::max(1, std::min(2, std::atoi(env)));
+  if (const char* env = std::getenv("MOE_UMMA_V")) L->umma_v = std::max(0, std::min(2, std::atoi(env)));
   if (const char* env = std::getenv("MOE_FUSE_ROUTE")) L->fuse_route = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_DEBUG_ROUTE")) L->debug_route = std::atoi(env) != 0;
   {
@@ -528,7 +532,10 @@ static cudaError_t launch_umma(moe_layer* h, UmmaArgs& a, int T, cudaStream_t s,
     a.ksplit = std::max(1, ks);
     a.part = h->part;
   }
-  k_umma<<<h->num_sms * per_sm, UM_THREADS, smem, s>>>(a);
+  if (h->umma_v == 2 || (h->umma_v == 0 && T <= 128))
+    k_umma2<<<h->num_sms * per_sm, UM_THREADS, smem, s>>>(a);
+  else
+    k_umma<<<h->num_sms * per_sm, UM_THREADS, smem, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) ++*nl;
   if (e == cudaSuccess && a.ksplit > 1) {

@@ -144,10 +144,14 @@ def test_batched_zipf_parity(T, rows):
 
 # --- the tcgen05 grouped path (forced at small T, automatic from T = 64) ------
 
+@pytest.mark.parametrize("gemm", ["k_umma", "k_umma2"])
 @pytest.mark.parametrize("name,T", [("tiny", 1), ("tiny", 16), ("tiny", 37), ("latent", 4),
                                     ("latent", 16), ("odd_latent_fp16", 12),
                                     ("odd_relu2_noshared", 9)])
-def test_grouped_path_parity(name, T):
+def test_grouped_path_parity(name, T, gemm, monkeypatch):
+    """Both grouped GEMM kernels (one CTA-synchronised K loop; warp-specialised
+    producer / dequant / MMA roles), selected at create time."""
+    monkeypatch.setenv("MOE_UMMA_V", "2" if gemm == "k_umma2" else "1")
     if name in ODD:
         lay = mi.make_layer(ODD[name], 11)
     else:
@@ -210,8 +214,14 @@ def test_stack_parity(T, rows):
             torch.cuda.synchronize()
             ref = gu.ora_forward(lay, ref_in)
             assert np.array_equal(ids.cpu().numpy()[sel], ref["ids"]), f"layer {li}"
-            np.testing.assert_allclose(w.cpu().numpy()[sel], ref["w"], rtol=gu.W_RTOL,
-                                       atol=gu.W_ATOL)
+            # Layer 0 sees the same input on both sides: the weights match to the
+            # fp32 routing bound.  A later layer's GPU input is the GPU's previous
+            # output, within the parity bound (rel. RMS <= 1e-2) of the oracle's;
+            # a relative input error e moves a logit by about e * |z| and a
+            # sigmoid weight by at most e * |z| / 4 of its unit scale, so those
+            # layers are held to the parity bound itself.
+            rtol, atol = (gu.W_RTOL, gu.W_ATOL) if li == 0 else (gu.REL_RMS, gu.REL_RMS * 0.1)
+            np.testing.assert_allclose(w.cpu().numpy()[sel], ref["w"], rtol=rtol, atol=atol)
             ref_in = mi._round_to_dtype(ref["out"], "bf16")
             cur = out
         final = cur.float().cpu().numpy().astype(np.float64)[sel]
@@ -250,16 +260,22 @@ def test_path_selection_and_launch_counts():
     torch.cuda.synchronize()
     assert h.device_status() == 0
 
-def test_row_invariance_bit_exact():
-    """Each row of a 16-row pass equals its own one-row pass, bit for bit."""
+@pytest.mark.parametrize("path", ["gemv", "grouped", "fused"])
+def test_row_invariance_bit_exact(path):
+    """On one path, each row of a 16-row pass equals its own one-row pass, bit
+    for bit (no reduction order depends on the other rows of the batch)."""
     lay, h = handle_for("latent", 16)
     x, _ = gu.margin_x(lay, 16, seed=77)
     xt = gu.to_torch_x(x, "bf16")
-    full = h.forward(xt)
-    for t in range(16):
-        one = h.forward(xt[t:t + 1].contiguous())
-        torch.cuda.synchronize()
-        assert torch.equal(one.view(torch.int16), full[t:t + 1].view(torch.int16)), t
+    try:
+        h.set_path(path)
+        full = h.forward(xt).clone()
+        for t in range(16):
+            one = h.forward(xt[t:t + 1].contiguous())
+            torch.cuda.synchronize()
+            assert torch.equal(one.view(torch.int16), full[t:t + 1].view(torch.int16)), (path, t)
+    finally:
+        h.set_path("auto")
 
 
 def test_graph_replay_equals_eager():
