@@ -55,16 +55,26 @@ KERNEL_OF_STAGE = {"dense_in": "k_dense_in", "route": "k_route", "expert_up": "k
                    "expert_down": "k_expert", "dense_out": "k_dense_out", "k_fused": "k_fused"}
 
 
-def kernel_source_hash():
-    """sha256 over the CUDA sources, so that DRAM traffic captured by ncu is
-    only reported for the kernels it was captured from."""
+# the sources that define each kernel and its launch
+KERNEL_SOURCES = {
+    "k_dense_in": ["moe_kernels.cuh", "moe_layer.cu"],
+    "k_dense_out": ["moe_kernels.cuh", "moe_layer.cu"],
+    "k_expert": ["moe_kernels.cuh", "moe_layer.cu"],
+    "k_route": ["moe_kernels.cuh", "moe_layer.cu"],
+    "k_umma": ["moe_kernels.cuh", "moe_umma.cuh", "moe_umma2.cuh", "moe_layer.cu"],
+    "k_fused": ["moe_kernels.cuh", "moe_fused.cuh", "moe_fused.cu", "moe_layer.cu"],
+}
+
+
+def kernel_source_hash(kernel):
+    """sha256 over the CUDA sources of a kernel, so that DRAM traffic captured
+    by ncu is only reported for the code it was captured from."""
     import hashlib
     d = os.path.join(ROOT, "quantized_moe_decode_gemv_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(d, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in KERNEL_SOURCES.get(kernel, sorted(os.listdir(d))):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()
 
 
@@ -75,11 +85,10 @@ def captured_traffic(kernel, T):
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p))
-    if d.get("source_sha256") != kernel_source_hash():
+    d = json.load(open(p)).get("kernels", {}).get(f"{kernel}@T{T}")
+    if not d or d.get("source_sha256") != kernel_source_hash(kernel):
         return None
-    v = d.get("per_launch_bytes", {}).get(f"{kernel}@T{T}")
-    return float(v) if v is not None else None
+    return float(d["dram_bytes_per_launch"])
 
 
 def parse_args():

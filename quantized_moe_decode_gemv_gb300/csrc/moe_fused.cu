@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "moe_fused.cuh"
 
@@ -54,6 +55,13 @@ cudaError_t launch(const FusedArgs& a, size_t smem, int num_sms, FusedLaunchCach
 #define FZ_CAT(a, b) FZ_CAT2(a, b)
 cudaError_t FZ_CAT(fused_launch_tb, FZ_TB)(const FusedArgs& a, bool gated, size_t smem, int num_sms,
                                            FusedLaunchCache* cache, cudaStream_t s) {
+  // MOE_DEBUG_STALL (tests of failure detection): make CTA 0's first wait run out
+  const char* stall = std::getenv("MOE_DEBUG_STALL");
+  if (stall && std::atoi(stall)) {
+    FusedArgs b = a;
+    b.debug_stall = 1;
+    return gated ? launch<true>(b, smem, num_sms, cache, s) : launch<false>(b, smem, num_sms, cache, s);
+  }
   return gated ? launch<true>(a, smem, num_sms, cache, s) : launch<false>(a, smem, num_sms, cache, s);
 }
 

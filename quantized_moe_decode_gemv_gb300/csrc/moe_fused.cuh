@@ -103,6 +103,7 @@ struct FusedArgs {
   int sd_pre, sd_mid;   // percent of this CTA's shared-down rows before the expert
                         // up rows, and between the expert up and down rows
   unsigned long long* trace;   // diagnostics: [grid][FZ_TRACE] globaltimer stamps, or null
+  int debug_stall;   // failure-detection test: CTA 0 first waits on a counter nothing sets
 };
 
 constexpr int FZ_TRACE = 32;
@@ -152,11 +153,12 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
 
 // CTA-wide wait until *p >= target; false (and the timeout bit set) if the
 // bound ran out.  `ok` false skips the wait.
-__device__ __forceinline__ bool fz_wait(const int* p, int target, int* status, bool ok) {
+__device__ __forceinline__ bool fz_wait(const int* p, int target, int* status, bool ok,
+                                        uint32_t limit = FZ_SPIN_LIMIT) {
   bool w = true;
   if (threadIdx.x == 0 && ok) {
     w = false;
-    for (uint32_t i = 0; i < FZ_SPIN_LIMIT; ++i) {
+    for (uint32_t i = 0; i < limit; ++i) {
       if (ld_acquire(p) >= target) { w = true; break; }
       __nanosleep(32);
     }
@@ -589,6 +591,9 @@ __global__ void __launch_bounds__(NT, TB >= 8 ? 1 : 2) k_fused(const __grid_cons
 
   // ---- routing (CTA 0) ----
   if (c == 0) {
+    // failure-detection test: a short wait on a word that nothing sets runs
+    // out, the timeout is recorded and the launch completes without routing
+    if (A.debug_stall) ok = fz_wait(sync + FZ_EXIT * FZ_SYNC_STRIDE + 8, 1, A.status, ok, 1u << 12);
     ok = fz_wait(sync + FZ_ROUTER * FZ_SYNC_STRIDE, G - 1, A.status, ok);
     stamp(1);
     if (ok)
