@@ -1030,6 +1030,7 @@ struct ExpertArgs {
                            // 0: wait first (the metadata may still be written).
   int prefetch;            // prefetch this CTA's weight rows into L2 (pre-wait phase)
   int cps;                 // CTAs per distinct-expert slot (grid = umax * cps)
+  int max_pairs;           // > 0: slots with more token pairs are left to the grouped GEMM
 };
 
 __device__ __forceinline__ void sb_decode(uint32_t v, int dt, float& s, float& b) {
@@ -1081,6 +1082,7 @@ __global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(c
   if (!A.pre_wait_phase) griddep_wait();
   griddep_launch();
   if (u >= A.meta[0]) return;
+  if (A.max_pairs > 0 && uniq_p0[u + 1] - uniq_p0[u] > A.max_pairs) return;
   const int64_t e = uniq_e[u];
   if (A.pre_wait_phase && A.prefetch && threadIdx.x == 0) {
     // the route metadata was final before the previous kernel began

@@ -84,6 +84,8 @@ struct moe_layer {
   int umax = 0;
   int kin = 0;
   int grouped_min_t = 16;
+  int combine_min_t = 1;  // gemv path: the combine as its own kernel from this T
+  int expert_split = 0;   // AUTO's grouped path: light experts on the int4 gemv kernel
   int fused_max_t = 0;    // AUTO: the persistent kernel for T <= this (below grouped_min_t)
   int fused_sd_pre = 60;  // persistent kernel: percent of a CTA's shared-down rows before the experts,
   int fused_sd_mid = 20;  // and between the expert up and down rows
@@ -386,6 +388,8 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   L->r_in = L->off_shu + Fs;
   L->umax = std::min(E, T * k);
   if (const char* env = std::getenv("MOE_GROUPED_MIN_T")) L->grouped_min_t = std::max(1, std::atoi(env));
+  if (const char* env = std::getenv("MOE_COMBINE_MIN_T")) L->combine_min_t = std::max(1, std::atoi(env));
+  if (const char* env = std::getenv("MOE_EXPERT_SPLIT")) L->expert_split = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_PDL")) L->use_pdl = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_FUSED_MAX_T")) L->fused_max_t = std::atoi(env);
   if (const char* env = std::getenv("MOE_SD_PRE")) L->fused_sd_pre = std::max(0, std::min(100, std::atoi(env)));
@@ -661,6 +665,14 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
   }
   const int path = choose_path(h, T);
   const bool grouped = path == MOE_PATH_GROUPED;
+  // With expert_split (MOE_EXPERT_SPLIT=1), AUTO's grouped path splits the
+  // routed experts by load: an expert with at most `expert_pb` token pairs in
+  // this batch goes to the int4 gemv kernel (one pass over its rows), a busier
+  // one to the tcgen05 grouped GEMM; both launch and each skips the other's
+  // experts.  Forced GROUPED runs every expert on the tensor cores.
+  const bool split_experts = grouped && h->path != MOE_PATH_GROUPED && h->expert_split;
+  const bool experts_gemv = !grouped || split_experts;
+  const bool experts_tc = grouped;
   int nl = 0;   // kernel launches of this forward
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int H = c.hidden, E = c.n_experts, k = c.top_k, F = c.expert_ffn, Lt = c.latent;
@@ -882,103 +894,115 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
   }
 
   // 3. expert up (+gate) with the activation, 4. expert down
-  if (!grouped) {
+  {
+    // token slots per pass of the gemv kernel; with the split, an expert with
+    // at most pb_split pairs is the gemv kernel's, a busier one the GEMM's
+    const int pb_split = std::min(std::min(pow2_at_least(T, h->expert_pb), expert_pb_cap(kin)),
+                                  expert_pb_cap(F));
     // token slots per pass: most distinct experts hold one or two of the
     // batch's rows; experts with more loop over slot groups (L2 re-reads)
     const int pb_up = std::min(pow2_at_least(T, h->expert_pb), expert_pb_cap(kin));
     const int pb_dn = std::min(pow2_at_least(T, h->expert_pb), expert_pb_cap(F));
-    ExpertArgs up{};
-    up.n_rows = F;
-    up.K = kin;
-    up.G = c.group_size;
-    up.q = h->up_q;
-    up.sb = h->up_sb;
-    up.q_gate = gated ? h->gate_q : nullptr;
-    up.sb_gate = gated ? h->gate_sb : nullptr;
-    up.s_dt = c.scale_dtype;
-    up.act = c.act;
-    up.meta = h->meta;
-    up.umax = h->umax;
-    up.k = k;
-    if (Lt) {
-      up.xin = h->dense_in; up.xin_dt = DT_FP32; up.xin_stride = h->r_in; up.xin_off = h->off_fc1;
-    } else {
-      up.xin = x; up.xin_dt = c.act_dtype; up.xin_stride = H; up.xin_off = 0;
-    }
-    up.xin_by_pair = 0;
-    up.out = h->hbuf;
-    up.pre_wait_phase = 0;
-    up.prefetch = 0;
-    // CTAs per distinct-expert slot: about 4 resident CTAs per SM over all slots,
-    // at least 8 rows per CTA
-    // slots: at most min(E, T*k) distinct experts in this call
+    // CTAs per distinct-expert slot: about expert_target resident CTAs per SM
+    // over all slots (at most min(E, T*k) distinct experts), at least 8 rows each
     const int slots = std::min(E, T * k);
     const int target = h->num_sms * h->expert_target;
-    up.cps = std::max(1, std::min(std::max(1, F / 8), (target + slots - 1) / slots));
-    const int grid_up = slots * up.cps;
+    ExpertArgs up{};
+    UmmaArgs uup{};
     mark(2);
-    if ((e = launch_expert(up, pb_up, grid_up, s, pdl)) != cudaSuccess) goto cuda_fail;
-    ++nl;
-    mark(3);
-    ExpertArgs dn = up;
-    dn.n_rows = kin;
-    dn.K = F;
-    dn.q = h->down_q;
-    dn.sb = h->down_sb;
-    dn.q_gate = nullptr;
-    dn.sb_gate = nullptr;
-    dn.act = -1;
-    dn.xin = h->hbuf; dn.xin_dt = DT_FP32; dn.xin_stride = F; dn.xin_off = 0;
-    dn.xin_by_pair = 1;
-    dn.out = h->pexp;
-    dn.pre_wait_phase = 1;
-    dn.prefetch = (h->prefetch >> 1) & 1;
-    dn.cps = std::max(1, std::min(std::max(1, kin / 8), (target + slots - 1) / slots));
-    if ((e = launch_expert(dn, pb_dn, slots * dn.cps, s, pdl)) != cudaSuccess) goto cuda_fail;
-    ++nl;
-  } else {
-    UmmaArgs up{};
-    up.experts = 1;
-    up.meta = h->meta;
-    up.umax = h->umax;
-    up.n_rows = F;
-    up.K = kin;
-    up.a_mode = UA_INT4;
-    up.q = h->up_q;
-    up.sb = h->up_sb;
-    up.q2 = gated ? h->gate_q : nullptr;
-    up.sb2 = gated ? h->gate_sb : nullptr;
-    up.G = c.group_size;
-    up.s_dt = c.scale_dtype;
-    up.mma_dt = mma_dt;
-    if (Lt) {
-      up.b0 = h->xl16; up.b0_stride = Lt; up.b0_off = 0;
-    } else {
-      up.b0 = x; up.b0_stride = H; up.b0_off = 0;
+    if (experts_gemv) {
+      up.n_rows = F;
+      up.K = kin;
+      up.G = c.group_size;
+      up.q = h->up_q;
+      up.sb = h->up_sb;
+      up.q_gate = gated ? h->gate_q : nullptr;
+      up.sb_gate = gated ? h->gate_sb : nullptr;
+      up.s_dt = c.scale_dtype;
+      up.act = c.act;
+      up.meta = h->meta;
+      up.umax = h->umax;
+      up.k = k;
+      if (Lt) {
+        up.xin = h->dense_in; up.xin_dt = DT_FP32; up.xin_stride = h->r_in; up.xin_off = h->off_fc1;
+      } else {
+        up.xin = x; up.xin_dt = c.act_dtype; up.xin_stride = H; up.xin_off = 0;
+      }
+      up.xin_by_pair = 0;
+      up.out = h->hbuf;
+      up.pre_wait_phase = 0;
+      up.prefetch = 0;
+      up.max_pairs = split_experts ? pb_split : 0;
+      up.cps = std::max(1, std::min(std::max(1, F / 8), (target + slots - 1) / slots));
+      const int grid_up = slots * up.cps;
+      if ((e = launch_expert(up, pb_up, grid_up, s, pdl)) != cudaSuccess) goto cuda_fail;
+      ++nl;
+
     }
-    up.out16 = static_cast<unsigned short*>(h->h16);   // the down GEMM's B operand
-    up.by_pair = 0;
-    up.k = k;
-    up.epi = UE_ROWS;
-    up.act = c.act;
-    up.out_f32 = h->hbuf;
-    up.status = h->status;
-    mark(2);
-    if ((e = launch_umma(h, up, T, s, &nl)) != cudaSuccess) goto cuda_fail;
+    if (experts_tc) {
+      uup.experts = 1;
+      uup.min_pairs = split_experts ? pb_split + 1 : 0;
+      uup.meta = h->meta;
+      uup.umax = h->umax;
+      uup.n_rows = F;
+      uup.K = kin;
+      uup.a_mode = UA_INT4;
+      uup.q = h->up_q;
+      uup.sb = h->up_sb;
+      uup.q2 = gated ? h->gate_q : nullptr;
+      uup.sb2 = gated ? h->gate_sb : nullptr;
+      uup.G = c.group_size;
+      uup.s_dt = c.scale_dtype;
+      uup.mma_dt = mma_dt;
+      if (Lt) {
+        uup.b0 = h->xl16; uup.b0_stride = Lt; uup.b0_off = 0;
+      } else {
+        uup.b0 = x; uup.b0_stride = H; uup.b0_off = 0;
+      }
+      uup.out16 = static_cast<unsigned short*>(h->h16);   // the down GEMM's B operand
+      uup.by_pair = 0;
+      uup.k = k;
+      uup.epi = UE_ROWS;
+      uup.act = c.act;
+      uup.out_f32 = h->hbuf;
+      uup.status = h->status;
+      if ((e = launch_umma(h, uup, T, s, &nl)) != cudaSuccess) goto cuda_fail;
+
+    }
     mark(3);
-    UmmaArgs dn = up;
-    dn.n_rows = kin;
-    dn.K = F;
-    dn.q = h->down_q;
-    dn.sb = h->down_sb;
-    dn.q2 = nullptr;
-    dn.sb2 = nullptr;
-    dn.b0 = h->h16; dn.b0_stride = F; dn.b0_off = 0;
-    dn.out16 = nullptr;
-    dn.by_pair = 1;
-    dn.act = -1;
-    dn.out_f32 = h->pexp;
-    if ((e = launch_umma(h, dn, T, s, &nl)) != cudaSuccess) goto cuda_fail;
+    if (experts_gemv) {
+      ExpertArgs dn = up;
+      dn.n_rows = kin;
+      dn.K = F;
+      dn.q = h->down_q;
+      dn.sb = h->down_sb;
+      dn.q_gate = nullptr;
+      dn.sb_gate = nullptr;
+      dn.act = -1;
+      dn.xin = h->hbuf; dn.xin_dt = DT_FP32; dn.xin_stride = F; dn.xin_off = 0;
+      dn.xin_by_pair = 1;
+      dn.out = h->pexp;
+      dn.pre_wait_phase = 1;
+      dn.prefetch = (h->prefetch >> 1) & 1;
+      dn.cps = std::max(1, std::min(std::max(1, kin / 8), (target + slots - 1) / slots));
+      if ((e = launch_expert(dn, pb_dn, slots * dn.cps, s, pdl)) != cudaSuccess) goto cuda_fail;
+      ++nl;
+    }
+    if (experts_tc) {
+      UmmaArgs udn = uup;
+      udn.n_rows = kin;
+      udn.K = F;
+      udn.q = h->down_q;
+      udn.sb = h->down_sb;
+      udn.q2 = nullptr;
+      udn.sb2 = nullptr;
+      udn.b0 = h->h16; udn.b0_stride = F; udn.b0_off = 0;
+      udn.out16 = nullptr;
+      udn.by_pair = 1;
+      udn.act = -1;
+      udn.out_f32 = h->pexp;
+      if ((e = launch_umma(h, udn, T, s, &nl)) != cudaSuccess) goto cuda_fail;
+    }
   }
 
   // 5. combine + fc2 + shared down + residual
@@ -1044,7 +1068,9 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     dout.delta = delta;
     dout.T = T;
     dout.prefetch = (h->prefetch >> 2) & 1;
-    if (kout) {
+    if (kout && T >= h->combine_min_t) {
+      // the output projection's operand once per forward; below combine_min_t
+      // rows every dense_out CTA stages it itself (one launch fewer)
       CombineArgs ca{};
       ca.T = T; ca.L = Lt; ca.Fs = Fs; ca.k = k; ca.act = c.act;
       ca.pexp = h->pexp; ca.wts = h->wts; ca.dense_in = h->dense_in; ca.r_in = h->r_in;

@@ -89,6 +89,7 @@ struct UmmaArgs {
   const void* x; int x_dt; void* out; float* delta;
   const float* pexp; const float* wts; int add_combine;
   int* status;
+  int min_pairs;            // experts mode: groups with fewer token pairs are left to the gemv kernel
 };
 
 // ---------------------------------------------------------------------------
@@ -226,6 +227,7 @@ __device__ __forceinline__ UmmaGroup umma_group(const UmmaArgs& A, int g) {
     G.e = A.meta[1 + g];
     G.p0 = A.meta[1 + A.umax + g];
     G.n = A.meta[1 + A.umax + g + 1] - G.p0;
+    if (G.n < A.min_pairs) G.n = 0;   // served by the int4 gemv kernel
   } else {
     G.e = 0;
     G.p0 = 0;
