@@ -109,6 +109,11 @@ def parse_args():
     p.add_argument("--sweep", default="", help="comma-separated T values: time each and write "
                    "one JSON line per T to --sweep-out (the main line is unchanged)")
     p.add_argument("--sweep-out", default="sweep.jsonl")
+    p.add_argument("--stack", action="store_true",
+                   help="also time the five-layer heterogeneous stack (E = 240..496) at --stack-T "
+                        "rows, layers round-robin with the residual carried; one JSON line per T "
+                        "appended to --sweep-out")
+    p.add_argument("--stack-T", default="2,9,16")
     return p.parse_args()
 
 
@@ -424,6 +429,39 @@ def run_ours(args):
                                                    sum(expert_bytes(spec)) / T)}) + "\n")
         h.set_path(args.path)
 
+    # the heterogeneous five-layer stack, run like a model (layers round-robin)
+    if args.stack and rank == 0:
+        specs = mi.stack_specs()
+        stack_T = [int(v) for v in args.stack_T.split(",") if v.strip()]
+        layers = [mi.make_layer(sp, i) for i, sp in enumerate(specs)]
+        hs = [pkg.MoELayer(pkg.MoEConfig.from_spec(sp, max_tokens=max(stack_T)),
+                           pkg.upload_arrays(l.arrays(), device=dev)) for sp, l in zip(specs, layers)]
+        with open(args.sweep_out, "a") as f:
+            for T in stack_T:
+                xs = [torch.from_numpy(mi.make_x(specs[0], T, 900 + i).view(np.int16)).cuda()
+                      .view(torch.bfloat16) for i in range(8)]
+                evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                       for _ in range(args.steps)]
+                with torch.cuda.stream(stream):
+                    for i in range(args.warmup + args.steps):
+                        flush.zero_()
+                        if i >= args.warmup:
+                            evs[i - args.warmup][0].record(stream)
+                        cur = xs[i % 8]
+                        for hh in hs:
+                            cur = hh.forward(cur, stream=stream)
+                        if i >= args.warmup:
+                            evs[i - args.warmup][1].record(stream)
+                    stream.synchronize()
+                ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+                f.write(json.dumps({
+                    "stack_experts": [sp.n_experts for sp in specs], "T": T,
+                    "paths": [hh.path_for(T) for hh in hs],
+                    "ms_per_stack_step": ms, "tokens_per_s": T / (ms / 1e3),
+                    "layer_forwards_per_s": len(hs) / (ms / 1e3)}) + "\n")
+        for hh in hs:
+            hh.close()
+
     # end to end through the host-buffer C-ABI call
     xs_host = [x.cpu().pin_memory() for x in m["xs"][:8]]
     out_host = torch.empty_like(xs_host[0]).pin_memory()
@@ -452,6 +490,7 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "ms_p10_p50_p90": [float(np.percentile(m["step_ms"], q)) for q in (10, 50, 90)],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded random weights and activations)",
             "config": {"workload": WORKLOAD, "T": args.T, "parallelism": "replicas" if world > 1 else "single",
