@@ -145,6 +145,16 @@ def stage_bytes(spec, T, n_uniq):
             "expert_down": n_uniq * dn_b, "dense_out": dout}
 
 
+def layer_flops(spec, T):
+    """Multiply-add flops of one forward of T rows (2 per MAC): router, latent
+    projections, shared expert, and k routed experts per row."""
+    H, E, L, Fs, k = spec.hidden, spec.n_experts, spec.latent, spec.shared_ffn, spec.top_k
+    n_in = 2 if spec.gated else 1
+    dense = E * H + 2 * L * H + (n_in + 1) * Fs * H
+    experts = k * (n_in + 1) * spec.expert_ffn * spec.k_in
+    return 2 * T * (dense + experts)
+
+
 def layer_bytes(spec, T, n_uniq):
     b = stage_bytes(spec, T, n_uniq)
     return b["dense_in"] + b["expert_up"] + b["expert_down"] + b["dense_out"] - T * spec.hidden * 2
@@ -339,6 +349,7 @@ def run_ours(args):
     if os.path.exists(pp):
         peaks = json.load(open(pp))
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    tc_peak = peaks.get("bf16_tflops", 1900.0)
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
 
     spec = mi.SPECS["latent"]
@@ -412,7 +423,9 @@ def run_ours(args):
     if sweep and rank == 0:
         with open(args.sweep_out, "w") as f:
             for T in sweep:
-                paths = ["fused", "gemv", "grouped"] if T >= 16 else ["fused", "gemv"]
+                # beyond 256 rows (prefill) only the grouped path is timed
+                paths = (["grouped"] if T > 256 else
+                         ["fused", "gemv", "grouped"] if T >= 16 else ["fused", "gemv"])
                 for path in paths:
                     h.set_path(path)
                     ms = measure(torch, pkg, spec, h, T, max(20, args.steps // 4), 3,
@@ -426,7 +439,10 @@ def run_ours(args):
                         "gbs": bb / (tt / 1e3) / 1e9, "hbm_frac": bb / (tt / 1e3) / 1e9 / hbm_peak,
                         "mean_distinct_experts": float(np.mean(ms["n_uniq"])),
                         "expert_bytes_per_token": (float(np.mean(ms["n_uniq"])) *
-                                                   sum(expert_bytes(spec)) / T)}) + "\n")
+                                                   sum(expert_bytes(spec)) / T),
+                        "tflops": layer_flops(spec, T) / (tt / len(ms["step_ms"]) / 1e3) / 1e12,
+                        "tensor_frac": (layer_flops(spec, T) / (tt / len(ms["step_ms"]) / 1e3) / 1e12
+                                        / tc_peak)}) + "\n")
         h.set_path(args.path)
 
     # the heterogeneous five-layer stack, run like a model (layers round-robin)

@@ -217,6 +217,7 @@ struct RouteArgs {
   int mask_words;        // > 0: rank pairs with per-expert row bitmasks of this many
                          // words in dynamic shared memory (E * mask_words words)
   int debug_times;       // print per-phase timestamps (diagnostics only)
+  int topk_only;         // 1: ids and weights only (the lists come from k_route_lists)
 };
 
 __device__ __forceinline__ unsigned long long global_ns() {
@@ -432,6 +433,7 @@ static __device__ __noinline__ void route_block(const RouteArgs& A, int* smem) {
     }
     if (W > 1) __syncthreads();
   }
+  if (A.topk_only) return;
   // ---- distinct experts and their pairs ----
   if (A.debug_times) tp[1] = global_ns();
   if (A.T * k <= 32) {
@@ -561,6 +563,114 @@ static __device__ __noinline__ void route_block(const RouteArgs& A, int* smem) {
 // The routing kernel of the grouped path: one warp per row for up to 16 rows
 // (route_block adapts to the block size; ~90 registers a thread).
 constexpr int ROUTE_THREADS = 512;
+
+// Routing of many rows (prefill): k_route_rows selects the top-k of
+// ROUTE_ROWS_PER_CTA rows per CTA (ids and weights only), then one CTA of
+// k_route_lists builds the distinct-expert lists.  A pair's place among its
+// expert's pairs (row order) comes from per-expert row bitmasks: the number of
+// earlier rows that chose the expert is a popcount prefix over the bitmask.
+constexpr int ROUTE_ROWS_PER_CTA = 16;
+constexpr int ROUTE_SMALL_T = 64;   // up to this many rows one k_route CTA does both
+constexpr int LIST_THREADS = 1024;
+static_assert(LIST_THREADS == MAX_E, "k_route_lists scans one expert per thread");
+
+struct ListArgs {
+  const int* ids;   // [T*k]
+  int T, k, E, umax;
+  int* meta;
+  uint32_t* mask;   // [E][W] bit t of word t/32: row t chose the expert
+  int* pref;        // [E][W] set bits in the expert's words before word w
+  int W;            // (T + 31) / 32
+};
+
+static __global__ void __launch_bounds__(LIST_THREADS) k_route_lists(const __grid_constant__ ListArgs A) {
+  __shared__ int s_cnt[MAX_E];
+  __shared__ int s_base[MAX_E];
+  __shared__ int s_wu[32], s_wc[32];
+  griddep_wait();
+  griddep_launch();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
+  const int P = A.T * A.k, E = A.E, W = A.W;
+  for (int64_t i = tid; i < static_cast<int64_t>(E) * W; i += nthr) A.mask[i] = 0u;
+  __syncthreads();
+  for (int p = tid; p < P; p += nthr) {
+    const int e = A.ids[p], t = p / A.k;
+    atomicOr(&A.mask[static_cast<int64_t>(e) * W + (t >> 5)], 1u << (t & 31));
+  }
+  __syncthreads();
+  for (int e = tid; e < MAX_E; e += nthr) {
+    int acc = 0;
+    if (e < E) {
+      for (int w = 0; w < W; ++w) {
+        A.pref[static_cast<int64_t>(e) * W + w] = acc;
+        acc += __popc(__ldcg(&A.mask[static_cast<int64_t>(e) * W + w]));
+      }
+    }
+    s_cnt[e] = acc;
+  }
+  __syncthreads();
+  // exclusive scans over experts (one expert per thread) of (count > 0) and count
+  {
+    const int e = tid;   // LIST_THREADS == MAX_E
+    const int c = s_cnt[e];
+    int iu = c > 0 ? 1 : 0, ic = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, iu, o);
+      const int b = __shfl_up_sync(0xffffffffu, ic, o);
+      if (lane >= o) { iu += a; ic += b; }
+    }
+    if (lane == 31) { s_wu[warp] = iu; s_wc[warp] = ic; }
+    __syncthreads();
+    if (warp == 0) {
+      int a = s_wu[lane], b = s_wc[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, a, o);
+        const int y = __shfl_up_sync(0xffffffffu, b, o);
+        if (lane >= o) { a += x; b += y; }
+      }
+      s_wu[lane] = a;
+      s_wc[lane] = b;
+    }
+    __syncthreads();
+    const int pu = (warp ? s_wu[warp - 1] : 0) + iu - (c > 0 ? 1 : 0);
+    const int pc = (warp ? s_wc[warp - 1] : 0) + ic - c;
+    s_base[e] = pc;
+    int* uniq_e = A.meta + 1;
+    int* uniq_p0 = A.meta + 1 + A.umax;
+    if (c > 0) { uniq_e[pu] = e; uniq_p0[pu] = pc; }
+    if (e == MAX_E - 1) {
+      A.meta[0] = pu + (c > 0 ? 1 : 0);
+      uniq_p0[pu + (c > 0 ? 1 : 0)] = P;
+    }
+  }
+  __syncthreads();
+  int* pairs = A.meta + 2 + 2 * A.umax;
+  for (int p = tid; p < P; p += nthr) {
+    const int e = A.ids[p], t = p / A.k, w = t >> 5;
+    const int64_t o = static_cast<int64_t>(e) * W + w;
+    const int r = __ldcg(&A.pref[o]) + __popc(__ldcg(&A.mask[o]) & ((1u << (t & 31)) - 1u));
+    pairs[s_base[e] + r] = p;
+  }
+}
+
+static __global__ void __launch_bounds__(ROUTE_THREADS) k_route_rows(const __grid_constant__ RouteArgs A) {
+  extern __shared__ int route_smem[];
+  griddep_wait();
+  griddep_launch();
+  RouteArgs B = A;
+  const int t0 = blockIdx.x * ROUTE_ROWS_PER_CTA;
+  B.T = min(ROUTE_ROWS_PER_CTA, A.T - t0);
+  B.logits = A.logits + static_cast<int64_t>(t0) * A.r_in;
+  B.ids = A.ids + t0 * A.k;
+  B.w = A.w + t0 * A.k;
+  if (A.ext_ids) B.ext_ids = A.ext_ids + t0 * A.k;
+  if (A.ext_w) B.ext_w = A.ext_w + t0 * A.k;
+  B.topk_only = 1;
+  B.mask_words = 0;
+  route_block(B, route_smem);
+}
 
 static __global__ void __launch_bounds__(ROUTE_THREADS) k_route(const __grid_constant__ RouteArgs A) {
   extern __shared__ int route_smem[];

@@ -70,6 +70,8 @@ struct moe_layer {
   void* h16 = nullptr;        // [Tmax*k, F] 16-bit expert activations (grouped path)
   float* part = nullptr;      // split-K partial sums of the grouped dense GEMMs
   void* bout = nullptr;       // [Tmax, L + F_sh] 16-bit operand of the grouped output GEMM
+  uint32_t* rmask = nullptr;  // [E, (Tmax+31)/32] routing row bitmasks (Tmax > ROUTE_SMALL_T)
+  int* rpref = nullptr;       // [E, (Tmax+31)/32] their popcount prefixes
   int* fsync = nullptr;       // FZ_WORDS phase counters of the persistent kernel
   float* sdbuf = nullptr;     // [Tmax, H] shared-expert down output (persistent kernel)
   void* x_stage = nullptr;    // [Tmax, H] act dtype (host-buffer forward)
@@ -310,7 +312,7 @@ static cudaError_t set_smem_attrs() {
   MOE_SMEM_ATTR((k_expert<4, false>)) MOE_SMEM_ATTR((k_expert<8, false>))
   MOE_SMEM_ATTR((k_expert<1, true>)) MOE_SMEM_ATTR((k_expert<2, true>))
   MOE_SMEM_ATTR((k_expert<4, true>)) MOE_SMEM_ATTR((k_expert<8, true>))
-  MOE_SMEM_ATTR(k_umma) MOE_SMEM_ATTR(k_umma2) MOE_SMEM_ATTR(k_route)
+  MOE_SMEM_ATTR(k_umma) MOE_SMEM_ATTR(k_umma2) MOE_SMEM_ATTR(k_route) MOE_SMEM_ATTR(k_route_rows)
 #undef MOE_SMEM_ATTR
   return e;
 }
@@ -479,7 +481,13 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     MOE_TRY_CUDA(L->alloc(&L->xl16, static_cast<size_t>(T) * (Lt + 64) * 2), "workspace");
     MOE_TRY_CUDA(L->alloc(&L->h16, P * F * 2), "workspace");
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->part),
-                          static_cast<size_t>(UM_MAX_KSPLIT) * T * std::max(L->r_in, H) * 4), "workspace");
+                          static_cast<size_t>(UM_MAX_KSPLIT) * std::min(T, UM_KSPLIT_MAX_T) *
+                              std::max(L->r_in, H) * 4), "workspace");
+    if (T > ROUTE_SMALL_T) {
+      const size_t nw = static_cast<size_t>(E) * ((T + 31) / 32);
+      MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->rmask), nw * 4), "workspace");
+      MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->rpref), nw * 4), "workspace");
+    }
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->fsync), FZ_WORDS * FZ_SYNC_STRIDE * 4), "workspace");
     MOE_TRY_CUDA(cudaMemsetAsync(L->fsync, 0, FZ_WORDS * FZ_SYNC_STRIDE * 4, s), "counter clear");
     if (want_trace)
@@ -529,7 +537,7 @@ static cudaError_t launch_umma(moe_layer* h, UmmaArgs& a, int T, cudaStream_t s,
   const int per_sm = (h->umma_ctas >= 2 && !gated) ? 2 : 1;
   const size_t smem = umma_config(a, T, per_sm == 2 ? 110 * 1024 : 220 * 1024);
   a.ksplit = 1;
-  if (!a.experts) {
+  if (!a.experts && T <= UM_KSPLIT_MAX_T) {
     const int mtiles = (a.n_rows + UM_M - 1) / UM_M, nkc = a.K / UM_KC;
     int ks = (h->num_sms * per_sm + mtiles - 1) / mtiles;
     ks = std::min(ks, std::min(std::max(1, nkc / 4), UM_MAX_KSPLIT));
@@ -796,7 +804,8 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     if (h->fz_trace) print_fused_trace(h, s);
     return MOE_OK;
   }
-  const bool fuse_route = !grouped && h->fuse_route;
+  const bool big_route = T > ROUTE_SMALL_T;
+  const bool fuse_route = !grouped && h->fuse_route && !big_route;
   const bool pdl = h->use_pdl && !grouped && !h->profiling;
 
   // 1. dense matrices that read x: router, fc1_latent_proj, shared gate/up
@@ -885,7 +894,28 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
 
   // 2. routing (fused into the dense pass on the gemv path)
   mark(1);
-  if (!fuse_route) {
+  if (big_route) {
+    // many rows: top-k over row blocks in parallel, then the lists in one CTA
+    RouteArgs rr = ra;
+    rr.mask_words = 0;
+    if ((e = launch_ex<RouteArgs>(k_route_rows, (T + ROUTE_ROWS_PER_CTA - 1) / ROUTE_ROWS_PER_CTA,
+                                  ROUTE_THREADS, ROUTE_SMEM_BYTES, s, pdl, rr)) != cudaSuccess)
+      goto cuda_fail;
+    ++nl;
+    ListArgs la{};
+    la.ids = h->ids;
+    la.T = T;
+    la.k = k;
+    la.E = E;
+    la.umax = h->umax;
+    la.meta = h->meta;
+    la.mask = h->rmask;
+    la.pref = h->rpref;
+    la.W = (T + 31) / 32;
+    if ((e = launch_ex<ListArgs>(k_route_lists, 1, LIST_THREADS, 0, s, pdl, la)) != cudaSuccess)
+      goto cuda_fail;
+    ++nl;
+  } else if (!fuse_route) {
     if ((e = launch_ex<RouteArgs>(k_route, 1, ROUTE_THREADS,
                                   ROUTE_SMEM_BYTES + static_cast<size_t>(E) * ra.mask_words * 4, s,
                                   pdl, ra)) != cudaSuccess)

@@ -32,6 +32,7 @@ constexpr int UM_THREADS = 256;
 constexpr int UM_MAX_STAGES = 8;
 constexpr int UM_MAX_KSPLIT = 8;
 constexpr uint32_t UM_SPIN_LIMIT = 1u << 22;
+constexpr int UM_KSPLIT_MAX_T = 256;   // dense GEMMs split K only up to this many token rows
 
 // canonical K-major no-swizzle layout of a [rows x 64] 16-bit tile:
 // core matrix (row / 8, k / 8) at (row / 8) * 1024 + (k / 8) * 128 bytes,

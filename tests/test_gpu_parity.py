@@ -142,6 +142,16 @@ def test_batched_zipf_parity(T, rows):
             paths=SMALL_T_PATHS + ("auto",) if T < 64 else ("auto",))
 
 
+# --- prefill-sized batches: the routing over row blocks, then one list CTA ----
+
+@pytest.mark.parametrize("T,rows", [(65, [0, 64]), (512, [0, 255, 511]), (2048, [0, 1023, 2047])])
+def test_prefill_parity(T, rows):
+    """Above 64 rows the top-k runs over 16-row blocks in parallel and one CTA
+    builds the distinct-expert lists from per-expert row bitmasks; the
+    grouped tcgen05 path takes every projection."""
+    _parity("latent", T, rows=rows, max_tokens=2048, zipf=True)
+
+
 # --- the tcgen05 grouped path (forced at small T, automatic from T = 64) ------
 
 @pytest.mark.parametrize("gemm", ["k_umma", "k_umma2"])
