@@ -1,6 +1,7 @@
 // Host side of the quantized MoE decode layer: validation, create/destroy,
 // forward orchestration and the C ABI declared in include/moe_layer.h.
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>   // PFN_cuTensorMapEncodeTiled
 
 #include <algorithm>
 #include <atomic>
@@ -96,12 +97,17 @@ struct moe_layer {
   FusedLaunchCache fused_grid[4][2];  // cooperative grid of k_fused<TB, ., gated>
   int last_launches = 0;  // kernel launches of the last forward
   unsigned long long* fz_trace = nullptr;   // diagnostics (MOE_FUSED_TRACE): phase stamps
+  unsigned long long* um_trace = nullptr;   // diagnostics (MOE_UMMA_TRACE): grouped GEMM role stamps
+  int um_trace_n = 0;                       // grouped launches stamped in this forward
   int use_pdl = 1;        // programmatic dependent launch between the gemv-path kernels
   int expert_pb = 2;      // max token slots per pass of the gemv-path expert kernels
   int expert_target = 4;  // gemv-path expert kernels: CTAs per SM the grid is sized for
   int umma_ctas = 2;      // grouped path: resident CTAs per SM (2 when the TMEM columns allow)
-  int umma_v = 0;         // grouped path GEMM: 1 = k_umma, 2 = warp-specialised roles (k_umma2),
-                          // 0 = k_umma2 up to 128 token rows, k_umma above
+  int umma_v = 0;         // grouped path GEMM: 1 = k_umma (CTA-synchronised K loop),
+                          // 0 or 2 = k_umma2 (warp-specialised roles, tensor copies)
+  int umma_abufs = 3;         // grouped path (k_umma2, int4): dequantised A tiles in the ring
+  int umma_tma = 1;           // grouped path (k_umma2): A operand by tensor copies when the layout allows
+  int umma_ntile_int4 = 128;  // grouped path: max tokens per MMA tile with int4 (dequantised) A
   int fuse_route = 1;     // routing in the last router CTA of the dense pass (0: own kernel)
   int debug_route = 0;    // diagnostics: print routing phase times
   int prefetch = 6;       // bit 0: experts' up weights from the routing CTA (one SM's
@@ -404,6 +410,11 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   if (const char* env = std::getenv("MOE_EXPERT_TARGET")) L->expert_target = std::max(1, std::min(16, std::atoi(env)));
   if (const char* env = std::getenv("MOE_UMMA_CTAS")) L->umma_ctas = std::max(1, std::min(2, std::atoi(env)));
   if (const char* env = std::getenv("MOE_UMMA_V")) L->umma_v = std::max(0, std::min(2, std::atoi(env)));
+  if (const char* env = std::getenv("MOE_UMMA_ABUFS"))
+    L->umma_abufs = std::max(2, std::min(UM_MAX_ABUFS, std::atoi(env)));
+  if (const char* env = std::getenv("MOE_UMMA_TMA")) L->umma_tma = std::atoi(env) != 0;
+  if (const char* env = std::getenv("MOE_UMMA_NTILE"))
+    L->umma_ntile_int4 = std::max(16, std::min(128, std::atoi(env))) & ~15;
   if (const char* env = std::getenv("MOE_FUSE_ROUTE")) L->fuse_route = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_DEBUG_ROUTE")) L->debug_route = std::atoi(env) != 0;
   {
@@ -492,6 +503,10 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     MOE_TRY_CUDA(cudaMemsetAsync(L->fsync, 0, FZ_WORDS * FZ_SYNC_STRIDE * 4, s), "counter clear");
     if (want_trace)
       MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->fz_trace), 4096 * FZ_TRACE * 8), "trace");
+    if (std::getenv("MOE_UMMA_TRACE") && std::atoi(std::getenv("MOE_UMMA_TRACE"))) {
+      MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->um_trace), 4 * UM_TRACE_WORDS * 8), "trace");
+      MOE_TRY_CUDA(cudaMemsetAsync(L->um_trace, 0, 4 * UM_TRACE_WORDS * 8, s), "trace");
+    }
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->sdbuf), static_cast<size_t>(T) * H * 4), "workspace");
     MOE_TRY_CUDA(L->alloc(&L->x_stage, static_cast<size_t>(T) * H * adt), "workspace");
     MOE_TRY_CUDA(L->alloc(&L->out_stage, static_cast<size_t>(T) * H * adt), "workspace");
@@ -517,15 +532,74 @@ moe_status moe_layer_destroy(moe_layer* h) {
   return MOE_OK;
 }
 
+// The driver's tensor-map encoder (looked up once through the runtime).
+static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// Tensor maps of a grouped launch's A operand (layouts in UmmaArgs::tm).
+// False -- A then goes by cp.async -- when the encoder is missing or a matrix
+// breaks the copy engine's rules: 16-byte aligned bases and row strides,
+// dense parts in whole 64-column chunks.
+static bool umma_tensor_maps(UmmaArgs& a, int n_experts) {
+  const auto enc = tmap_encoder();
+  if (!enc) return false;
+  const cuuint32_t unit[3] = {1, 1, 1};
+  if (a.a_mode == UA_DENSE) {
+    if (a.nseg < 1 || a.nseg > 4) return false;
+    for (int si = 0; si < a.nseg; ++si) {
+      const DenseSeg& S = a.seg[si];
+      if (S.nparts < 1 || S.nparts > 2) return false;
+      if (S.part[0].k0 != 0 || (S.nparts == 2 && S.part[1].k0 != S.part[0].wk)) return false;
+      for (int p = 0; p < S.nparts; ++p) {
+        const DensePart& Pt = S.part[p];
+        if (Pt.wk % UM_KC || reinterpret_cast<uintptr_t>(Pt.w) % 16) return false;
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(Pt.wk), static_cast<cuuint64_t>(S.rows)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(Pt.wk) * 2};
+        const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(UM_M)};
+        if (enc(&a.tm[2 * si + p], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(Pt.w), dims, strides,
+                box, unit, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+          return false;
+      }
+    }
+    return true;
+  }
+  const cuuint64_t words = static_cast<cuuint64_t>(a.K / 8);
+  const cuuint64_t dims[3] = {words, static_cast<cuuint64_t>(a.n_rows), static_cast<cuuint64_t>(n_experts)};
+  const cuuint64_t strides[2] = {words * 4, words * 4 * static_cast<cuuint64_t>(a.n_rows)};
+  const cuuint32_t box[3] = {8, 128, 1};
+  const uint32_t* qs[2] = {a.q, a.q2};
+  for (int i = 0; i < (a.q2 ? 2 : 1); ++i) {
+    if (reinterpret_cast<uintptr_t>(qs[i]) % 16) return false;
+    if (enc(&a.tm[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(qs[i]), dims, strides, box, unit,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  return true;
+}
+
 // Tokens per MMA and ring depth for a grouped launch, and its shared memory.
-static size_t umma_config(UmmaArgs& a, int T, size_t budget) {
+static size_t umma_config(UmmaArgs& a, int T, size_t budget, int int4_cap) {
   const bool gated = a.a_mode == UA_INT4 && a.q2 != nullptr;
-  const int cap = a.a_mode == UA_DENSE ? 256 : 64;
+  const int cap = a.a_mode == UA_DENSE ? 256 : int4_cap;
   a.n_tile = std::min(cap, (std::max(1, T) + 15) & ~15);
   int st = UM_MAX_STAGES;
-  while (st > 3 && umma_plan(a.a_mode, gated, a.n_tile, st).total > budget) --st;
+  while (st > 3 && umma_plan(a.a_mode, gated, a.n_tile, st, a.abufs).total > budget) --st;
   a.stages = st;
-  return umma_plan(a.a_mode, gated, a.n_tile, st).total;
+  return umma_plan(a.a_mode, gated, a.n_tile, st, a.abufs).total;
 }
 
 // A grouped launch; a dense matrix with fewer 128-row tiles than SMs splits K
@@ -534,8 +608,26 @@ static cudaError_t launch_umma(moe_layer* h, UmmaArgs& a, int T, cudaStream_t s,
   // two CTAs per SM when the accumulators fit twice in TMEM (256 columns each:
   // not gated), so that one CTA's copies and dequantisation overlap the other's
   const bool gated = a.a_mode == UA_INT4 && a.q2 != nullptr;
-  const int per_sm = (h->umma_ctas >= 2 && !gated) ? 2 : 1;
-  const size_t smem = umma_config(a, T, per_sm == 2 ? 110 * 1024 : 220 * 1024);
+  const bool v2 = h->umma_v != 1;
+  int per_sm = (h->umma_ctas >= 2 && !gated) ? 2 : 1;
+  a.abufs = 2;
+  size_t smem = umma_config(a, T, per_sm == 2 ? 110 * 1024 : 220 * 1024, h->umma_ntile_int4);
+  if (per_sm == 2 && smem > 110 * 1024) {   // a wide token tile: one CTA per SM
+    per_sm = 1;
+    smem = umma_config(a, T, 220 * 1024, h->umma_ntile_int4);
+  }
+  if (v2 && a.a_mode == UA_INT4 && h->umma_abufs > 2) {
+    // more dequantised A tiles in the ring, while it keeps at least 4 stages
+    const int keep = a.stages;
+    a.abufs = h->umma_abufs;
+    const size_t sm = umma_config(a, T, per_sm == 2 ? 110 * 1024 : 220 * 1024, h->umma_ntile_int4);
+    if (a.stages >= 4 && sm <= static_cast<size_t>(per_sm == 2 ? 110 * 1024 : 220 * 1024)) {
+      smem = sm;
+    } else {
+      a.abufs = 2;
+      a.stages = keep;
+    }
+  }
   a.ksplit = 1;
   if (!a.experts && T <= UM_KSPLIT_MAX_T) {
     const int mtiles = (a.n_rows + UM_M - 1) / UM_M, nkc = a.K / UM_KC;
@@ -544,10 +636,14 @@ static cudaError_t launch_umma(moe_layer* h, UmmaArgs& a, int T, cudaStream_t s,
     a.ksplit = std::max(1, ks);
     a.part = h->part;
   }
-  if (h->umma_v == 2 || (h->umma_v == 0 && T <= 128))
+  a.trace = nullptr;
+  if (v2) {
+    a.tma_a = (h->umma_tma && umma_tensor_maps(a, h->cfg.n_experts)) ? 1 : 0;
+    if (h->um_trace && h->um_trace_n < 4) a.trace = h->um_trace + static_cast<size_t>(h->um_trace_n++) * UM_TRACE_WORDS;
     k_umma2<<<h->num_sms * per_sm, UM_THREADS, smem, s>>>(a);
-  else
+  } else {
     k_umma<<<h->num_sms * per_sm, UM_THREADS, smem, s>>>(a);
+  }
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) ++*nl;
   if (e == cudaSuccess && a.ksplit > 1) {
@@ -606,6 +702,35 @@ static cudaError_t launch_fused(moe_layer* h, const FusedArgs& a, int tb, size_t
     case 2: return fused_launch_tb2(a, gated, smem, h->num_sms, &h->fused_grid[1][gated], s);
     case 4: return fused_launch_tb4(a, gated, smem, h->num_sms, &h->fused_grid[2][gated], s);
     default: return fused_launch_tb8(a, gated, smem, h->num_sms, &h->fused_grid[3][gated], s);
+  }
+}
+
+// Diagnostics: CTA 0's role stamps per chunk of each grouped launch of the last
+// forward, in microseconds since the CTA started (producer issue start / issue
+// end / copies landed, dequant start / done, MMA start / issued, epilogue).
+static void print_umma_trace(moe_layer* h, cudaStream_t s) {
+  std::vector<unsigned long long> t(static_cast<size_t>(4) * UM_TRACE_WORDS);
+  const bool got = cudaMemcpyAsync(t.data(), h->um_trace, t.size() * 8, cudaMemcpyDeviceToHost, s) == cudaSuccess &&
+                   cudaStreamSynchronize(s) == cudaSuccess;
+  cudaMemsetAsync(h->um_trace, 0, t.size() * 8, s);
+  const int n = h->um_trace_n;
+  h->um_trace_n = 0;
+  if (!got) return;
+  for (int l = 0; l < n; ++l) {
+    const unsigned long long* L = t.data() + static_cast<size_t>(l) * UM_TRACE_WORDS;
+    const unsigned long long t0 = L[UM_TRACE_CHUNKS * UM_TRACE_STAMPS];
+    std::fprintf(stderr,
+                 "umma trace launch %d: chunk: p_begin p_slot p_A p_sb p_B d_landed d_buf d_done m_start m_issued "
+                 "epi p95_B\n",
+                 l);
+    for (int c = 0; c < UM_TRACE_CHUNKS; ++c) {
+      const unsigned long long* R = L + static_cast<size_t>(c) * UM_TRACE_STAMPS;
+      if (!R[0] && !R[8]) continue;
+      std::fprintf(stderr, "  %3d:", c);
+      for (int k = 0; k < UM_TRACE_STAMPS; ++k)
+        std::fprintf(stderr, " %7.2f", R[k] ? (static_cast<double>(R[k]) - static_cast<double>(t0)) * 1e-3 : -1.0);
+      std::fprintf(stderr, "\n");
+    }
   }
 }
 
@@ -1120,6 +1245,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
   mark(5);
   if (h->profiling) h->profiled = true;
   h->last_launches = nl;
+  if (h->um_trace) print_umma_trace(h, s);
   return MOE_OK;
 cuda_fail:
   h->last_error = std::string("launch failed: ") + cudaGetErrorString(e);

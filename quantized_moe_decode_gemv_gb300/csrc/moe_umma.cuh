@@ -22,6 +22,8 @@
 // the status word, frees its TMEM and returns.
 #pragma once
 
+#include <cuda.h>   // CUtensorMap (the layout only; maps are encoded on the host)
+
 #include "moe_kernels.cuh"
 
 namespace moe {
@@ -31,6 +33,7 @@ constexpr int UM_KC = 64;       // K elements per stage
 constexpr int UM_THREADS = 256;
 constexpr int UM_MAX_STAGES = 8;
 constexpr int UM_MAX_KSPLIT = 8;
+constexpr int UM_MAX_ABUFS = 4;
 constexpr uint32_t UM_SPIN_LIMIT = 1u << 22;
 constexpr int UM_KSPLIT_MAX_T = 256;   // dense GEMMs split K only up to this many token rows
 
@@ -74,6 +77,7 @@ struct UmmaArgs {
   // ---- pipeline (host-chosen) ----
   int n_tile;               // tokens per MMA (multiple of 16, <= 256)
   int stages;               // ring depth, 3..UM_MAX_STAGES
+  int abufs;                // int4 (k_umma2): dequantised A tiles in the ring, 2..UM_MAX_ABUFS (k_umma: 2)
   int ksplit;               // dense mode: K split over this many units (partials in `part`)
   float* part;              // [ksplit, n_tokens, n_rows] fp32 partial sums (ksplit > 1)
   // ---- epilogue ----
@@ -91,7 +95,19 @@ struct UmmaArgs {
   const float* pexp; const float* wts; int add_combine;
   int* status;
   int min_pairs;            // experts mode: groups with fewer token pairs are left to the gemv kernel
+  unsigned long long* trace;   // diagnostics: CTA 0's per-chunk role stamps (k_umma2), or null
+  // ---- A by tensor copies (k_umma2; host-encoded maps, tma_a = 0: A by cp.async) ----
+  // dense: map [2 * seg + part] over that part's [rows, wk] 16-bit matrix, boxes of
+  //        8 rows x 64 columns with the 128-byte swizzle (one box per 8-row group);
+  // int4:  map [0] over the codes [E, n_rows, K/8] words, boxes of 128 rows x 8
+  //        words (one per chunk), map [1] the gate's codes.
+  int tma_a;
+  CUtensorMap tm[8];
 };
+
+constexpr int UM_TRACE_CHUNKS = 128;                        // chunks stamped per launch
+constexpr int UM_TRACE_STAMPS = 12;                         // stamps a chunk
+constexpr int UM_TRACE_WORDS = UM_TRACE_CHUNKS * UM_TRACE_STAMPS + 8;   // then the start
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -121,6 +137,40 @@ __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t a, uint64_t b
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+// Descriptor of a K-major tile written with the 128-byte swizzle (8-row
+// groups 1024 bytes apart; the tile starts on a 1024-byte boundary, and a
+// K step inside the 128-byte row advances the start address).
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (1ull << 16) |                                   // leading offset (unused when swizzled)
+         (static_cast<uint64_t>(1024 >> 4) << 32) |       // 8-row group stride
+         (1ull << 46) |                                   // descriptor version for tcgen05
+         (2ull << 61);                                    // layout: 128-byte swizzle
+}
+
+// Tensor copies global -> shared, completing on an mbarrier (transaction bytes).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(mbar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(mbar)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
+}
+// Arrive on the mbarrier once this thread's earlier cp.async copies have landed
+// (the arrival is one of the barrier's expected count).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t mbar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(mbar) : "memory");
 }
 
 __device__ __forceinline__ void umma_commit(uint32_t mbar) {
@@ -237,24 +287,92 @@ __device__ __forceinline__ UmmaGroup umma_group(const UmmaArgs& A, int g) {
   return G;
 }
 
+// Work units of a launch.  A unit is one 128-row tile of A against one tile
+// of up to n_tile tokens of one group (and one part of K when K is split), so
+// that a group with many tokens -- a dense matrix, or an expert that takes a
+// large share of a batch -- spreads over many CTAs instead of walking its
+// token tiles inside one.  Units are numbered by group, then A tile, then
+// token tile: CTAs running side by side read the same A tile.
+constexpr int UM_MAX_GROUPS = 4 * UM_THREADS;
+static_assert(UM_MAX_GROUPS >= MAX_E, "one prefix entry per routed expert");
+
+// pref[g] = token tiles of the groups before g, for g = 0..n_groups (block
+// scan: 4 groups per thread; wsum holds the 8 warp totals).  Ends with a CTA
+// barrier; every thread of the CTA calls it.
+__device__ __forceinline__ void umma_tile_prefix(const UmmaArgs& A, int n_groups, int* pref, int* wsum) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int cnt[4], sum = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int g = 4 * tid + i;
+    cnt[i] = g < n_groups ? (umma_group(A, g).n + A.n_tile - 1) / A.n_tile : 0;
+    sum += cnt[i];
+  }
+  int inc = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) wsum[warp] = inc;
+  __syncthreads();
+  int run = inc - sum;
+  for (int w = 0; w < warp; ++w) run += wsum[w];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    pref[4 * tid + i] = run;
+    run += cnt[i];
+  }
+  if (tid == UM_THREADS - 1) pref[UM_MAX_GROUPS] = run;
+  __syncthreads();
+}
+
+struct UmmaUnit {
+  int g, mt, nt, split;
+};
+
+// Unit u (< pref[n_groups] * mtiles * nsplit) -> its group, A tile, token tile and K part.
+__device__ __forceinline__ UmmaUnit umma_unit(const int* pref, int n_groups, int mtiles, int nsplit, int u) {
+  UmmaUnit U;
+  U.split = u % nsplit;
+  const int r = u / nsplit;
+  // the last group whose first unit is at or before r (it has units: r is valid)
+  int lo = 0, hi = n_groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pref[mid] * mtiles <= r) lo = mid;
+    else hi = mid - 1;
+  }
+  U.g = lo;
+  const int ntg = pref[lo + 1] - pref[lo];
+  const int local = r - pref[lo] * mtiles;
+  U.mt = local / ntg;
+  U.nt = local - U.mt * ntg;
+  return U;
+}
+
 // Shared-memory plan of one launch: `stages` ring slots of
 // [A (16-bit tile, or int4 codes + scale/bias words, x2 when gated) | B],
 // then (int4 only) two 16-bit A tiles (x2 when gated), the token table (256
-// ints), the mbarrier and the TMEM address.
+// ints), the mbarriers, the TMEM address and the unit prefix.
 struct UmmaPlan {
-  uint32_t a_raw, b_bytes, stage, abuf, tok, total;
+  uint32_t a_raw, b_bytes, stage, abuf, tok, pref, total;
 };
 
-__host__ __device__ inline UmmaPlan umma_plan(int a_mode, bool gated, int n_tile, int stages) {
+__host__ __device__ inline UmmaPlan umma_plan(int a_mode, bool gated, int n_tile, int stages, int abufs = 2) {
   UmmaPlan p;
   p.a_raw = a_mode == UA_DENSE ? static_cast<uint32_t>(UM_A_BYTES)
                                : (gated ? 2u : 1u) * static_cast<uint32_t>(UM_CODE_BYTES + UM_SB_BYTES);
   p.b_bytes = static_cast<uint32_t>(n_tile) * UM_KC * 2;
   p.stage = p.a_raw + p.b_bytes;
   p.abuf = static_cast<uint32_t>(stages) * p.stage;
-  const uint32_t abuf_bytes = a_mode == UA_DENSE ? 0u : 2u * (gated ? 2u : 1u) * UM_A_BYTES;
+  const uint32_t abuf_bytes =
+      a_mode == UA_DENSE ? 0u : static_cast<uint32_t>(abufs) * (gated ? 2u : 1u) * UM_A_BYTES;
   p.tok = p.abuf + abuf_bytes;
-  p.total = p.tok + 256 * 4 + 64;   // token table, 2 mbarriers, TMEM address
+  p.pref = p.tok + 2048;            // token table, mbarriers, TMEM address
+  // unit prefix and warp totals, then room to put the plan on a 1024-byte
+  // boundary (swizzled tiles)
+  p.total = p.pref + (UM_MAX_GROUPS + 1 + 15) * 4 + 1024;
   return p;
 }
 
@@ -328,15 +446,18 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma(const __grid_constant__ 
   const int ngr = A.K / A.G;
 
   const int nsplit = A.ksplit > 1 ? A.ksplit : 1;
-  for (int unit = blockIdx.x; ok && unit < n_groups * mtiles * nsplit; unit += gridDim.x) {
-    const int split = unit % nsplit;
-    const int gm = unit / nsplit;
-    const int g = gm / mtiles, mt = gm - g * mtiles;
+  int* pref = reinterpret_cast<int*>(base + P.pref);
+  umma_tile_prefix(A, n_groups, pref, pref + UM_MAX_GROUPS + 1);
+  const int nunits = pref[n_groups] * mtiles * nsplit;
+  for (int unit = blockIdx.x; ok && unit < nunits; unit += gridDim.x) {
+    const UmmaUnit U = umma_unit(pref, n_groups, mtiles, nsplit, unit);
+    const int split = U.split;
     const int kc_begin = static_cast<int>(static_cast<int64_t>(split) * nkc / nsplit);
     const int nit = static_cast<int>(static_cast<int64_t>(split + 1) * nkc / nsplit) - kc_begin;
-    const UmmaGroup G = umma_group(A, g);
-    const int m0 = mt * UM_M;
-    for (int n0 = 0; ok && n0 < G.n; n0 += A.n_tile) {
+    const UmmaGroup G = umma_group(A, U.g);
+    const int m0 = U.mt * UM_M;
+    const int n_first = U.nt * A.n_tile, n_end = min(G.n, n_first + A.n_tile);
+    for (int n0 = n_first; ok && n0 < n_end; n0 += A.n_tile) {
       const int nvalid = min(A.n_tile, G.n - n0);
       const int npad = (nvalid + 15) & ~15;
       const uint32_t idesc = umma_idesc(npad, A.mma_dt);

@@ -6,6 +6,8 @@ must match exactly.  Full-size layers are compared on every row where the
 oracle takes seconds, and on sampled rows otherwise (the oracle is row
 independent, so a sampled row is checked exactly like a full pass).
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -32,8 +34,12 @@ def _cuda():
 _HANDLES = {}
 
 
+# create-time knobs a cached handle was built under
+KNOBS = ("MOE_UMMA_V", "MOE_UMMA_TMA", "MOE_UMMA_ABUFS", "MOE_UMMA_NTILE")
+
+
 def handle_for(name, max_tokens, seed=0, zipf=False, layer=None):
-    key = (name, seed, zipf, max_tokens)
+    key = (name, seed, zipf, max_tokens) + tuple(os.environ.get(k) for k in KNOBS)
     if key not in _HANDLES:
         lay = layer if layer is not None else gu.cached_layer(name, seed, zipf)
         _HANDLES[key] = (lay, gu.build_layer(lay, max_tokens))
@@ -144,24 +150,38 @@ def test_batched_zipf_parity(T, rows):
 
 # --- prefill-sized batches: the routing over row blocks, then one list CTA ----
 
-@pytest.mark.parametrize("T,rows", [(65, [0, 64]), (512, [0, 255, 511]), (2048, [0, 1023, 2047])])
-def test_prefill_parity(T, rows):
+@pytest.mark.parametrize("T,rows,gemm", [(65, [0, 64], "k_umma2"), (512, [0, 255, 511], "k_umma2"),
+                                         (512, [0, 255, 511], "k_umma"),
+                                         (2048, [0, 1023, 2047], "k_umma2")])
+def test_prefill_parity(T, rows, gemm, monkeypatch):
     """Above 64 rows the top-k runs over 16-row blocks in parallel and one CTA
     builds the distinct-expert lists from per-expert row bitmasks; the
-    grouped tcgen05 path takes every projection."""
+    grouped tcgen05 path takes every projection (token tiles of a dense
+    matrix or of a busy expert spread over CTAs)."""
+    for k, v in GEMM_ENV[gemm].items():
+        monkeypatch.setenv(k, v)
     _parity("latent", T, rows=rows, max_tokens=2048, zipf=True)
 
 
 # --- the tcgen05 grouped path (forced at small T, automatic from T = 64) ------
 
-@pytest.mark.parametrize("gemm", ["k_umma", "k_umma2"])
+# grouped GEMM variants, selected at create time: the CTA-synchronised K loop
+# (k_umma); the warp-specialised roles (k_umma2) with A by tensor copies and
+# three dequantised A tiles (default), with A by cp.async, with two A tiles
+GEMM_ENV = {"k_umma": {"MOE_UMMA_V": "1"},
+            "k_umma2": {"MOE_UMMA_V": "2"},
+            "k_umma2_cpasync": {"MOE_UMMA_V": "2", "MOE_UMMA_TMA": "0"},
+            "k_umma2_2buf": {"MOE_UMMA_V": "2", "MOE_UMMA_ABUFS": "2"}}
+
+
+@pytest.mark.parametrize("gemm", list(GEMM_ENV))
 @pytest.mark.parametrize("name,T", [("tiny", 1), ("tiny", 16), ("tiny", 37), ("latent", 4),
                                     ("latent", 16), ("odd_latent_fp16", 12),
                                     ("odd_relu2_noshared", 9)])
 def test_grouped_path_parity(name, T, gemm, monkeypatch):
-    """Both grouped GEMM kernels (one CTA-synchronised K loop; warp-specialised
-    producer / dequant / MMA roles), selected at create time."""
-    monkeypatch.setenv("MOE_UMMA_V", "2" if gemm == "k_umma2" else "1")
+    """Every grouped GEMM variant on the tiny, latent and odd layers."""
+    for k, v in GEMM_ENV[gemm].items():
+        monkeypatch.setenv(k, v)
     if name in ODD:
         lay = mi.make_layer(ODD[name], 11)
     else:
