@@ -53,6 +53,10 @@ class L2Flush:
 STAGES = ["dense_in", "route", "expert_up", "expert_down", "dense_out"]
 KERNEL_OF_STAGE = {"dense_in": "k_dense_in", "route": "k_route", "expert_up": "k_expert",
                    "expert_down": "k_expert", "dense_out": "k_dense_out", "k_fused": "k_fused"}
+# the grouped path runs every projection through the tcgen05 GEMM (its split-K
+# sums and the combine ride in the same stages)
+KERNEL_OF_STAGE_GROUPED = {"dense_in": "k_umma2", "route": "k_route", "expert_up": "k_umma2",
+                           "expert_down": "k_umma2", "dense_out": "k_umma2"}
 
 
 # the sources that define each kernel and its launch
@@ -61,7 +65,8 @@ KERNEL_SOURCES = {
     "k_dense_out": ["moe_kernels.cuh", "moe_layer.cu"],
     "k_expert": ["moe_kernels.cuh", "moe_layer.cu"],
     "k_route": ["moe_kernels.cuh", "moe_layer.cu"],
-    "k_umma": ["moe_kernels.cuh", "moe_umma.cuh", "moe_umma2.cuh", "moe_layer.cu"],
+    "k_umma": ["moe_kernels.cuh", "moe_umma.cuh", "moe_layer.cu"],
+    "k_umma2": ["moe_kernels.cuh", "moe_umma.cuh", "moe_umma2.cuh", "moe_layer.cu"],
     "k_fused": ["moe_kernels.cuh", "moe_fused.cuh", "moe_fused.cu", "moe_layer.cu"],
 }
 
@@ -397,8 +402,9 @@ def run_ours(args):
         # the dominant kernel: the largest share of the step, its launches
         # pooled (the expert kernel runs twice: up and down)
         per_kernel = {}
+        kmap = KERNEL_OF_STAGE_GROUPED if path == "grouped" else KERNEL_OF_STAGE
         for i, n in enumerate(STAGES):
-            kname = KERNEL_OF_STAGE[n]
+            kname = kmap[n]
             b, t = per_kernel.get(kname, (0.0, 0.0))
             per_kernel[kname] = (b + sb[n], t + float(st[i]))
         dom_name = max(per_kernel, key=lambda kn: per_kernel[kn][1])

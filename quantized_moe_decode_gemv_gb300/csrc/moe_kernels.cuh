@@ -1380,4 +1380,44 @@ static __global__ void k_interleave_sb(const unsigned short* __restrict__ s,
     out[i] = static_cast<uint32_t>(s[i]) | (static_cast<uint32_t>(b[i]) << 16);
 }
 
+// The up projection's B operand in the lists' sorted pair order: row p of
+// `out` is the 16-bit input row of the pair at sorted position p (token pid / k),
+// so that an expert's rows form one block for tensor copies.
+struct GatherArgs {
+  const int* meta;      // route metadata: pairs at meta[2 + 2 * umax + p]
+  int umax, k, P, K;    // pairs, row length (multiple of 8)
+  const unsigned short* in;
+  int64_t in_stride;    // elements between input rows
+  unsigned short* out;  // [P, K]
+};
+
+static __global__ void k_gather_pairs(const __grid_constant__ GatherArgs A) {
+  griddep_wait();
+  griddep_launch();
+  const int v = A.K / 8;   // 16-byte pieces a row
+  const int64_t n = static_cast<int64_t>(A.P) * v;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int p = static_cast<int>(i / v), j = static_cast<int>(i - static_cast<int64_t>(p) * v);
+    const int row = A.meta[2 + 2 * A.umax + p] / A.k;
+    reinterpret_cast<uint4*>(A.out)[i] =
+        reinterpret_cast<const uint4*>(A.in + static_cast<int64_t>(row) * A.in_stride)[j];
+  }
+}
+
+// Group-major copy of packed scale/bias words: out[e][g][r] = in[e][r][g], so
+// that the words of one group for consecutive rows are contiguous (one tensor
+// copy per chunk in the grouped GEMM).
+static __global__ void k_sb_group_major(const uint32_t* __restrict__ in, uint32_t* __restrict__ out,
+                                        int E, int rows, int ngr) {
+  const int64_t n = static_cast<int64_t>(E) * rows * ngr;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e = i / (static_cast<int64_t>(rows) * ngr);
+    const int64_t rem = i - e * rows * ngr;
+    const int64_t g = rem / rows, r = rem - g * rows;
+    out[i] = in[(e * rows + r) * ngr + g];
+  }
+}
+
 }  // namespace moe

@@ -55,6 +55,8 @@ struct moe_layer {
   void* fc2 = nullptr;
   uint32_t *gate_q = nullptr, *up_q = nullptr, *down_q = nullptr;
   uint32_t *gate_sb = nullptr, *up_sb = nullptr, *down_sb = nullptr;
+  // group-major copies of the scale/bias words ([E, K/G, rows]: the grouped GEMM's tensor copies)
+  uint32_t *gate_sbT = nullptr, *up_sbT = nullptr, *down_sbT = nullptr;
   void *sh_gate = nullptr, *sh_up = nullptr, *sh_down = nullptr;
 
   // workspace
@@ -69,9 +71,10 @@ struct moe_layer {
   float* comb = nullptr;      // [Tmax, L + F_sh] staged operand of the output projection
   void* xl16 = nullptr;       // [Tmax, L] 16-bit latent rows (grouped path B operand)
   void* h16 = nullptr;        // [Tmax*k, F] 16-bit expert activations (grouped path)
+  void* xs = nullptr;         // [Tmax*k, K_in] 16-bit up-projection inputs in sorted pair order
   float* part = nullptr;      // split-K partial sums of the grouped dense GEMMs
   void* bout = nullptr;       // [Tmax, L + F_sh] 16-bit operand of the grouped output GEMM
-  uint32_t* rmask = nullptr;  // [E, (Tmax+31)/32] routing row bitmasks (Tmax > ROUTE_SMALL_T)
+  uint32_t* rmask = nullptr;  // [E, (Tmax+31)/32] routing row bitmasks (Tmax > route_small_t)
   int* rpref = nullptr;       // [E, (Tmax+31)/32] their popcount prefixes
   int* fsync = nullptr;       // FZ_WORDS phase counters of the persistent kernel
   float* sdbuf = nullptr;     // [Tmax, H] shared-expert down output (persistent kernel)
@@ -103,8 +106,12 @@ struct moe_layer {
   int expert_pb = 2;      // max token slots per pass of the gemv-path expert kernels
   int expert_target = 4;  // gemv-path expert kernels: CTAs per SM the grid is sized for
   int umma_ctas = 2;      // grouped path: resident CTAs per SM (2 when the TMEM columns allow)
-  int umma_v = 0;         // grouped path GEMM: 1 = k_umma (CTA-synchronised K loop),
-                          // 0 or 2 = k_umma2 (warp-specialised roles, tensor copies)
+  int umma_v = 0;         // grouped path GEMM: 1 = k_umma (CTA-synchronised K loop), 2 = k_umma2
+                          // (warp-specialised roles, tensor copies), 0 = umma_is_v2's choice
+  int gather_min_t = 64;     // grouped path: from this many rows the up GEMM's B rows are gathered
+                             // into sorted pair order first (then read by tensor copies)
+  int route_small_t = 16;   // up to this many rows one routing CTA does top-k and lists (at most
+                            // ROUTE_SMALL_T); above, row blocks in parallel, then the list CTA
   int umma_abufs = 3;         // grouped path (k_umma2, int4): dequantised A tiles in the ring
   int umma_tma = 1;           // grouped path (k_umma2): A operand by tensor copies when the layout allows
   int umma_ntile_int4 = 128;  // grouped path: max tokens per MMA tile with int4 (dequantised) A
@@ -410,6 +417,9 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   if (const char* env = std::getenv("MOE_EXPERT_TARGET")) L->expert_target = std::max(1, std::min(16, std::atoi(env)));
   if (const char* env = std::getenv("MOE_UMMA_CTAS")) L->umma_ctas = std::max(1, std::min(2, std::atoi(env)));
   if (const char* env = std::getenv("MOE_UMMA_V")) L->umma_v = std::max(0, std::min(2, std::atoi(env)));
+  if (const char* env = std::getenv("MOE_GATHER_MIN_T")) L->gather_min_t = std::max(1, std::atoi(env));
+  if (const char* env = std::getenv("MOE_ROUTE_SMALL_T"))
+    L->route_small_t = std::max(1, std::min(ROUTE_SMALL_T, std::atoi(env)));
   if (const char* env = std::getenv("MOE_UMMA_ABUFS"))
     L->umma_abufs = std::max(2, std::min(UM_MAX_ABUFS, std::atoi(env)));
   if (const char* env = std::getenv("MOE_UMMA_TMA")) L->umma_tma = std::atoi(env) != 0;
@@ -463,6 +473,17 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     MOE_TRY_CUDA(copy_sb(&L->up_sb, w->up_s, w->up_b, ng_in), "up scales");
     MOE_TRY_CUDA(copy_q(&L->down_q, w->down_q, nq_dn), "down codes");
     MOE_TRY_CUDA(copy_sb(&L->down_sb, w->down_s, w->down_b, ng_dn), "down scales");
+    auto group_major = [&](uint32_t** dst, const uint32_t* src, int rows, int ngr) -> cudaError_t {
+      const size_t n = static_cast<size_t>(E) * rows * ngr;
+      cudaError_t e = L->alloc(reinterpret_cast<void**>(dst), n * 4);
+      if (e != cudaSuccess) return e;
+      const int blocks = static_cast<int>(std::min<size_t>((n + 255) / 256, 4096));
+      k_sb_group_major<<<blocks, 256, 0, s>>>(src, *dst, E, rows, ngr);
+      return cudaGetLastError();
+    };
+    if (gated) MOE_TRY_CUDA(group_major(&L->gate_sbT, L->gate_sb, F, kin / G), "gate scales");
+    MOE_TRY_CUDA(group_major(&L->up_sbT, L->up_sb, F, kin / G), "up scales");
+    MOE_TRY_CUDA(group_major(&L->down_sbT, L->down_sb, kin, F / G), "down scales");
     if (Fs) {
       const size_t n = static_cast<size_t>(Fs) * H * adt;
       if (gated) {
@@ -491,10 +512,11 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->comb), static_cast<size_t>(T) * (Lt + Fs + 64) * 4), "workspace");
     MOE_TRY_CUDA(L->alloc(&L->xl16, static_cast<size_t>(T) * (Lt + 64) * 2), "workspace");
     MOE_TRY_CUDA(L->alloc(&L->h16, P * F * 2), "workspace");
+    if (T >= L->gather_min_t) MOE_TRY_CUDA(L->alloc(&L->xs, P * L->kin * 2), "workspace");
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->part),
                           static_cast<size_t>(UM_MAX_KSPLIT) * std::min(T, UM_KSPLIT_MAX_T) *
                               std::max(L->r_in, H) * 4), "workspace");
-    if (T > ROUTE_SMALL_T) {
+    if (T > L->route_small_t) {
       const size_t nw = static_cast<size_t>(E) * ((T + 31) / 32);
       MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->rmask), nw * 4), "workspace");
       MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->rpref), nw * 4), "workspace");
@@ -577,18 +599,58 @@ static bool umma_tensor_maps(UmmaArgs& a, int n_experts) {
     return true;
   }
   const cuuint64_t words = static_cast<cuuint64_t>(a.K / 8);
-  const cuuint64_t dims[3] = {words, static_cast<cuuint64_t>(a.n_rows), static_cast<cuuint64_t>(n_experts)};
-  const cuuint64_t strides[2] = {words * 4, words * 4 * static_cast<cuuint64_t>(a.n_rows)};
+  const cuuint64_t rows = static_cast<cuuint64_t>(a.n_rows), ngr = static_cast<cuuint64_t>(a.K / a.G);
+  const cuuint64_t dims[3] = {words, rows, static_cast<cuuint64_t>(n_experts)};
+  const cuuint64_t strides[2] = {words * 4, words * 4 * rows};
   const cuuint32_t box[3] = {8, 128, 1};
+  // scale/bias words, group-major: 128 rows x the chunk's groups (2 when G = 32)
+  const cuuint64_t sdims[3] = {rows, ngr, static_cast<cuuint64_t>(n_experts)};
+  const cuuint64_t sstrides[2] = {rows * 4, rows * 4 * ngr};
+  const cuuint32_t sbox[3] = {128, a.G == 32 ? 2u : 1u, 1};
+  if (a.n_rows % 4) return false;
   const uint32_t* qs[2] = {a.q, a.q2};
+  const uint32_t* ss[2] = {a.sbT, a.sbT2};
   for (int i = 0; i < (a.q2 ? 2 : 1); ++i) {
-    if (reinterpret_cast<uintptr_t>(qs[i]) % 16) return false;
+    if (!qs[i] || !ss[i] || reinterpret_cast<uintptr_t>(qs[i]) % 16 || reinterpret_cast<uintptr_t>(ss[i]) % 16)
+      return false;
     if (enc(&a.tm[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(qs[i]), dims, strides, box, unit,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return false;
+    if (enc(&a.tm[2 + i], CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(ss[i]), sdims, sstrides, sbox,
+            unit, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
   }
   return true;
+}
+
+// Tensor map of a grouped launch's B operand (map [8]) when its rows form a
+// plain matrix: the tokens of a dense launch, or the pairs' hidden rows in
+// sorted order.  False (B then goes by cp.async) for gathered rows or when the
+// base or the row stride breaks the 16-byte rule.
+static bool umma_b_map(UmmaArgs& a) {
+  const auto enc = tmap_encoder();
+  if (!enc || (a.experts && !a.b_sorted)) return false;
+  const char* base = static_cast<const char*>(a.b0) + a.b0_off * 2;
+  const int64_t nrows = a.experts ? a.b_rows : a.n_tokens;
+  if (reinterpret_cast<uintptr_t>(base) % 16 || (a.b0_stride * 2) % 16 || nrows < 1) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(nrows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.b0_stride) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(a.n_tile)};
+  const cuuint32_t unit[2] = {1, 1};
+  return enc(&a.tm[8], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<char*>(base), dims, strides, box, unit,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Which grouped GEMM a launch takes: k_umma2 for the dense projections at any
+// T and for the experts up to 128 rows; above that the experts' wide token
+// tiles run faster in k_umma (measured), unless MOE_UMMA_V forces one.
+static bool umma_is_v2(const moe_layer* h, bool dense, int T) {
+  if (h->umma_v == 1) return false;
+  if (h->umma_v == 2) return true;
+  return dense || T <= 128;
 }
 
 // Tokens per MMA and ring depth for a grouped launch, and its shared memory.
@@ -608,7 +670,7 @@ static cudaError_t launch_umma(moe_layer* h, UmmaArgs& a, int T, cudaStream_t s,
   // two CTAs per SM when the accumulators fit twice in TMEM (256 columns each:
   // not gated), so that one CTA's copies and dequantisation overlap the other's
   const bool gated = a.a_mode == UA_INT4 && a.q2 != nullptr;
-  const bool v2 = h->umma_v != 1;
+  const bool v2 = umma_is_v2(h, a.a_mode == UA_DENSE, T);
   int per_sm = (h->umma_ctas >= 2 && !gated) ? 2 : 1;
   a.abufs = 2;
   size_t smem = umma_config(a, T, per_sm == 2 ? 110 * 1024 : 220 * 1024, h->umma_ntile_int4);
@@ -630,8 +692,15 @@ static cudaError_t launch_umma(moe_layer* h, UmmaArgs& a, int T, cudaStream_t s,
   }
   a.ksplit = 1;
   if (!a.experts && T <= UM_KSPLIT_MAX_T) {
-    const int mtiles = (a.n_rows + UM_M - 1) / UM_M, nkc = a.K / UM_KC;
-    int ks = (h->num_sms * per_sm + mtiles - 1) / mtiles;
+    // as many K parts as keep every unit in one wave of CTAs (k_umma2 tiles
+    // each dense segment on its own)
+    int mtiles = (a.n_rows + UM_M - 1) / UM_M;
+    if (v2) {
+      mtiles = 0;
+      for (int si = 0; si < a.nseg; ++si) mtiles += (a.seg[si].rows + UM_M - 1) / UM_M;
+    }
+    const int nkc = a.K / UM_KC;
+    int ks = std::max(1, h->num_sms * per_sm / std::max(1, mtiles));
     ks = std::min(ks, std::min(std::max(1, nkc / 4), UM_MAX_KSPLIT));
     a.ksplit = std::max(1, ks);
     a.part = h->part;
@@ -639,9 +708,12 @@ static cudaError_t launch_umma(moe_layer* h, UmmaArgs& a, int T, cudaStream_t s,
   a.trace = nullptr;
   if (v2) {
     a.tma_a = (h->umma_tma && umma_tensor_maps(a, h->cfg.n_experts)) ? 1 : 0;
+    a.tma_b = (h->umma_tma && umma_b_map(a)) ? 1 : 0;
     if (h->um_trace && h->um_trace_n < 4) a.trace = h->um_trace + static_cast<size_t>(h->um_trace_n++) * UM_TRACE_WORDS;
     k_umma2<<<h->num_sms * per_sm, UM_THREADS, smem, s>>>(a);
   } else {
+    a.tma_a = a.tma_b = 0;
+    if (a.b_sorted || a.out_sorted) return cudaErrorInvalidValue;   // sorted rows are k_umma2's
     k_umma<<<h->num_sms * per_sm, UM_THREADS, smem, s>>>(a);
   }
   cudaError_t e = cudaGetLastError();
@@ -929,7 +1001,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     if (h->fz_trace) print_fused_trace(h, s);
     return MOE_OK;
   }
-  const bool big_route = T > ROUTE_SMALL_T;
+  const bool big_route = T > h->route_small_t;
   const bool fuse_route = !grouped && h->fuse_route && !big_route;
   const bool pdl = h->use_pdl && !grouped && !h->profiling;
 
@@ -1116,6 +1188,25 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
       }
       uup.out16 = static_cast<unsigned short*>(h->h16);   // the down GEMM's B operand
       uup.by_pair = 0;
+      // hidden rows in the lists' sorted order (the down GEMM reads an expert's
+      // rows as one block) unless the gemv kernel shares the buffer
+      uup.out_sorted = (umma_is_v2(h, false, T) && !split_experts) ? 1 : 0;
+      uup.sbT = h->up_sbT;
+      uup.sbT2 = gated ? h->gate_sbT : nullptr;
+      if (uup.out_sorted && h->xs && T >= h->gather_min_t && kin % 8 == 0 && uup.b0_stride % 8 == 0) {
+        // the B rows in sorted pair order: an expert's rows are one block
+        GatherArgs ga{};
+        ga.meta = h->meta; ga.umax = h->umax; ga.k = k; ga.P = T * k; ga.K = kin;
+        ga.in = static_cast<const unsigned short*>(uup.b0); ga.in_stride = uup.b0_stride;
+        ga.out = static_cast<unsigned short*>(h->xs);
+        const int64_t n = static_cast<int64_t>(T) * k * (kin / 8);
+        const int gg = static_cast<int>(std::min<int64_t>((n + 255) / 256, h->num_sms * 8));
+        if ((e = launch_ex<GatherArgs>(k_gather_pairs, gg, 256, 0, s, false, ga)) != cudaSuccess) goto cuda_fail;
+        ++nl;
+        uup.b0 = h->xs; uup.b0_stride = kin; uup.b0_off = 0;
+        uup.b_sorted = 1;
+        uup.b_rows = T * k;
+      }
       uup.k = k;
       uup.epi = UE_ROWS;
       uup.act = c.act;
@@ -1154,6 +1245,11 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
       udn.b0 = h->h16; udn.b0_stride = F; udn.b0_off = 0;
       udn.out16 = nullptr;
       udn.by_pair = 1;
+      udn.b_sorted = uup.out_sorted;
+      udn.out_sorted = 0;
+      udn.b_rows = T * k;
+      udn.sbT = h->down_sbT;
+      udn.sbT2 = nullptr;
       udn.act = -1;
       udn.out_f32 = h->pexp;
       if ((e = launch_umma(h, udn, T, s, &nl)) != cudaSuccess) goto cuda_fail;

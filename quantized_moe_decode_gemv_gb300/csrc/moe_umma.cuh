@@ -96,13 +96,22 @@ struct UmmaArgs {
   int* status;
   int min_pairs;            // experts mode: groups with fewer token pairs are left to the gemv kernel
   unsigned long long* trace;   // diagnostics: CTA 0's per-chunk role stamps (k_umma2), or null
-  // ---- A by tensor copies (k_umma2; host-encoded maps, tma_a = 0: A by cp.async) ----
-  // dense: map [2 * seg + part] over that part's [rows, wk] 16-bit matrix, boxes of
-  //        8 rows x 64 columns with the 128-byte swizzle (one box per 8-row group);
-  // int4:  map [0] over the codes [E, n_rows, K/8] words, boxes of 128 rows x 8
-  //        words (one per chunk), map [1] the gate's codes.
-  int tma_a;
-  CUtensorMap tm[8];
+  // ---- operands by tensor copies (k_umma2; host-encoded maps) ----
+  // tma_a (else cp.async): dense: map [2 * seg + part] over that part's [rows, wk]
+  //   16-bit matrix, 128 x 64 boxes with the 128-byte swizzle; int4: map [0] the
+  //   codes [E, n_rows, K/8] words (128 x 8-word boxes), [1] the gate's codes,
+  //   [2] / [3] the group-major scale/bias words [E, K/G, n_rows] (128 x
+  //   words-per-chunk boxes).
+  // tma_b (else cp.async): map [8] over the B rows [rows, K] 16-bit (dense
+  //   tokens, or the pairs' hidden rows in sorted order), n_tile x 64 boxes with
+  //   the 128-byte swizzle.
+  int tma_a, tma_b;
+  int b_sorted;             // experts: B row of pair slot n is p0 + n (hidden rows in sorted order)
+  int out_sorted;           // UE_ROWS: output row of pair slot n is p0 + n instead of the pair id
+  const uint32_t* sbT;      // host: group-major scale/bias words (maps [2], [3])
+  const uint32_t* sbT2;
+  int b_rows;               // host: rows of the B matrix (map [8])
+  CUtensorMap tm[9];
 };
 
 constexpr int UM_TRACE_CHUNKS = 128;                        // chunks stamped per launch
@@ -377,15 +386,17 @@ __host__ __device__ inline UmmaPlan umma_plan(int a_mode, bool gated, int n_tile
 }
 
 // Final value of output row m for token/pair `pid` from its accumulator.
+// `orow` is the output row of UE_ROWS (the pair id, or the pair's slot in the
+// sorted lists).
 __device__ __forceinline__ void umma_epilogue(const UmmaArgs& A, int pid, int m, float v, float vg,
-                                              bool gated) {
+                                              bool gated, int orow) {
   if (A.epi == UE_ROWS) {
     // A (q) is the up projection, A2 (q2) the gate: act(gate, up)
     if (A.act >= 0) v = gated ? act_fn(A.act, vg, v) : act_fn(A.act, 0.f, v);
     if (A.out16)
-      A.out16[static_cast<int64_t>(pid) * A.n_rows + m] = st16_bits(v, A.mma_dt);
+      A.out16[static_cast<int64_t>(orow) * A.n_rows + m] = st16_bits(v, A.mma_dt);
     else
-      A.out_f32[static_cast<int64_t>(pid) * A.n_rows + m] = v;
+      A.out_f32[static_cast<int64_t>(orow) * A.n_rows + m] = v;
   } else if (A.epi == UE_DENSE_IN) {
     const int col = A.out_col0 + m;
     A.out_f32[static_cast<int64_t>(pid) * A.out_ld + col] = v;
@@ -640,7 +651,7 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma(const __grid_constant__ 
           if (A.ksplit > 1) {
             A.part[(static_cast<int64_t>(split) * A.n_tokens + pid) * A.n_rows + m] = acc[i];
           } else {
-            umma_epilogue(A, pid, m, acc[i], gated ? accg[i] : 0.f, gated);
+            umma_epilogue(A, pid, m, acc[i], gated ? accg[i] : 0.f, gated, pid);
           }
         }
       }
@@ -675,7 +686,7 @@ __global__ void k_umma_reduce(const __grid_constant__ UmmaArgs A) {
     const int t = static_cast<int>(i / A.n_rows), m = static_cast<int>(i - static_cast<int64_t>(t) * A.n_rows);
     float v = 0.f;
     for (int sp = 0; sp < A.ksplit; ++sp) v += A.part[static_cast<int64_t>(sp) * n + i];
-    umma_epilogue(A, t, m, v, 0.f, false);
+    umma_epilogue(A, t, m, v, 0.f, false, t);
   }
 }
 

@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
   }
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(smem_u32(&full[s]), tma ? 97 : 96);
+      mbar_init(smem_u32(&full[s]), (tma || A.tma_b) ? 97 : 96);
       mbar_init(smem_u32(&empty[s]), 1);
     }
     for (int b = 0; b < NA; ++b) {
@@ -207,9 +207,13 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
     const int pt = tid - 32;   // 0..95
     uint32_t c = 0;
     if (tma && pt == 0) {
-      const int nmaps = A.a_mode == UA_DENSE ? 2 * A.nseg : (gated ? 2 : 1);
+      const int nmaps = A.a_mode == UA_DENSE ? 2 * A.nseg : (gated ? 4 : 3);
       for (int i = 0; i < nmaps; ++i)
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&A.tm[i])) : "memory");
+        if (A.a_mode == UA_DENSE || gated || i != 1)
+          asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&A.tm[i])) : "memory");
+    }
+    if (A.tma_b && pt == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&A.tm[8])) : "memory");
     }
     tiles([&](const UmmaTile& Tl) {
       const int m0 = Tl.m0, n0 = Tl.n0, nvalid = Tl.nvalid;
@@ -222,7 +226,9 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
         const int n = (pt + 96 * q) >> 3;
         brow[q] = -1;
         if (n < nvalid) {
-          if (A.experts) {
+          if (A.experts && A.b_sorted) {
+            brow[q] = G.p0 + n0 + n;
+          } else if (A.experts) {
             const int pid = A.meta[2 + 2 * A.umax + G.p0 + n0 + n];
             brow[q] = A.by_pair ? pid : pid / A.k;
           } else {
@@ -239,22 +245,33 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
         const uint32_t sa = smem_u32(slot), sbb = smem_u32(slot + P.a_raw);
         const uint32_t fb = smem_u32(&full[s]);
         const int k0 = (Tl.kc_begin + it) * UM_KC;
-        if (tma) {
-          if (pt == 0) {
-            if (A.a_mode == UA_DENSE) {
-              // the tile's 128 rows x 64 columns of its segment (rows past the
-              // segment's end read as zeros)
-              const DenseSeg& Sg = A.seg[Tl.si];
-              const int p = (Sg.nparts > 1 && k0 >= Sg.part[1].k0) ? 1 : 0;
-              mbar_arrive_expect_tx(fb, static_cast<uint32_t>(UM_A_BYTES));
-              tma_load_2d(sa, &A.tm[2 * Tl.si + p], k0 - Sg.part[p].k0, m0 - Sg.row0, fb);
-            } else {
-              mbar_arrive_expect_tx(fb, (gated ? 2u : 1u) * static_cast<uint32_t>(UM_CODE_BYTES));
-              tma_load_3d(sa, &A.tm[0], k0 >> 3, m0, G.e, fb);
-              if (gated) tma_load_3d(sa + UM_CODE_BYTES + UM_SB_BYTES, &A.tm[1], k0 >> 3, m0, G.e, fb);
+        if ((tma || A.tma_b) && pt == 0) {
+          // the slot's tensor copies, all counted on full[s]
+          const uint32_t sbx = 128u * 4u * static_cast<uint32_t>(A.G == 32 ? 2 : 1);   // scale/bias box
+          uint32_t tx = 0;
+          if (tma) tx += A.a_mode == UA_DENSE ? static_cast<uint32_t>(UM_A_BYTES)
+                                              : (gated ? 2u : 1u) * (static_cast<uint32_t>(UM_CODE_BYTES) + sbx);
+          if (A.tma_b) tx += static_cast<uint32_t>(A.n_tile) * 128u;
+          mbar_arrive_expect_tx(fb, tx);
+          if (tma && A.a_mode == UA_DENSE) {
+            // the tile's 128 rows x 64 columns of its segment (rows past the
+            // segment's end read as zeros)
+            const DenseSeg& Sg = A.seg[Tl.si];
+            const int p = (Sg.nparts > 1 && k0 >= Sg.part[1].k0) ? 1 : 0;
+            tma_load_2d(sa, &A.tm[2 * Tl.si + p], k0 - Sg.part[p].k0, m0 - Sg.row0, fb);
+          } else if (tma) {
+            // codes (128 rows x 32 bytes) and the chunk's scale/bias words
+            tma_load_3d(sa, &A.tm[0], k0 >> 3, m0, G.e, fb);
+            tma_load_3d(sa + UM_CODE_BYTES, &A.tm[2], m0, k0 / A.G, G.e, fb);
+            if (gated) {
+              tma_load_3d(sa + UM_CODE_BYTES + UM_SB_BYTES, &A.tm[1], k0 >> 3, m0, G.e, fb);
+              tma_load_3d(sa + 2 * UM_CODE_BYTES + UM_SB_BYTES, &A.tm[3], m0, k0 / A.G, G.e, fb);
             }
           }
-        } else if (A.a_mode == UA_DENSE) {
+          // B rows n0.. of the tile (dense tokens, or the pairs' sorted hidden rows)
+          if (A.tma_b) tma_load_2d(sbb, &A.tm[8], k0, A.experts ? G.p0 + n0 : n0, fb);
+        }
+        if (!tma && A.a_mode == UA_DENSE) {
           const DenseSeg& Sg = A.seg[Tl.si];
           for (int i = pt; i < UM_M * 8; i += 96) {
             const int r = i >> 3, j = i & 7;
@@ -273,7 +290,7 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
             }
             cp_async16(sa + sw_off(r, 8 * j), src, nbytes);
           }
-        } else {
+        } else if (!tma) {
           // codes: row r, 32 codes (16 bytes) per half
           for (int i = pt; i < UM_M * 2; i += 96) {
             const int r = i >> 1, hh = i & 1;
@@ -287,18 +304,17 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
           }
         }
         if (pt == 0) stamp(c, 2);
-        if (A.a_mode == UA_INT4) {
-          // scale/bias words: one word per row (G >= 64), two (G = 32)
+        if (A.a_mode == UA_INT4 && !tma) {
+          // scale/bias words, group-major in the slot ([group of the chunk][row]):
+          // one word per row (G >= 64), two (G = 32)
           for (int r = pt; r < UM_M; r += 96) {
             const int m = min(m0 + r, A.n_rows - 1);
             const int64_t row = static_cast<int64_t>(G.e) * A.n_rows + m;
             const int gw = k0 / A.G;
-            if (A.G == 32) {
-              cp_async8(sa + UM_CODE_BYTES + r * 8, A.sb + row * ngr + gw);
-              if (gated) cp_async8(sa + 2 * UM_CODE_BYTES + UM_SB_BYTES + r * 8, A.sb2 + row * ngr + gw);
-            } else {
-              cp_async4(sa + UM_CODE_BYTES + r * 8, A.sb + row * ngr + gw);
-              if (gated) cp_async4(sa + 2 * UM_CODE_BYTES + UM_SB_BYTES + r * 8, A.sb2 + row * ngr + gw);
+            for (int h2 = 0; h2 < (A.G == 32 ? 2 : 1); ++h2) {
+              cp_async4(sa + UM_CODE_BYTES + (h2 * 128 + r) * 4, A.sb + row * ngr + gw + h2);
+              if (gated)
+                cp_async4(sa + 2 * UM_CODE_BYTES + UM_SB_BYTES + (h2 * 128 + r) * 4, A.sb2 + row * ngr + gw + h2);
             }
           }
         }
@@ -307,7 +323,7 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
         // reach accumulator columns that are never read: left as they are)
 #pragma unroll
         for (int q = 0; q < UM_BPIECES; ++q) {
-          if (brow[q] >= 0) {
+          if (brow[q] >= 0 && !A.tma_b) {
             const int i = pt + 96 * q;
             const int n = i >> 3, j = i & 7;
             cp_async16(sbb + sw_off(n, 8 * j),
@@ -317,10 +333,12 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
           }
         }
         // pieces past the table (tiles wider than 128 tokens: dense only)
-        for (int i = pt + 96 * UM_BPIECES; i < nvalid * 8; i += 96) {
+        for (int i = pt + 96 * UM_BPIECES; !A.tma_b && i < nvalid * 8; i += 96) {
           const int n = i >> 3, j = i & 7;
           int row = n0 + n;
-          if (A.experts) {
+          if (A.experts && A.b_sorted) {
+            row = G.p0 + n0 + n;
+          } else if (A.experts) {
             const int pid = A.meta[2 + 2 * A.umax + G.p0 + n0 + n];
             row = A.by_pair ? pid : pid / A.k;
           }
@@ -337,7 +355,7 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
     cp_async_wait(0);
     // tensor copies still in flight land before the CTA ends: the last use of
     // each slot (already complete unless a wait gave up; bounded)
-    if (tma && pt == 0 && !ok)
+    if ((tma || A.tma_b) && pt == 0 && !ok)
       for (uint32_t j = c > static_cast<uint32_t>(S) ? c - S : 0u; j < c; ++j)
         mbar_wait(smem_u32(&full[j % S]), (j / S) & 1);
   } else if (warp >= 4) {
@@ -363,7 +381,7 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
             for (int hh = 0; hh < 2; ++hh) {
               const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 32 + hh * 16);
               const uint32_t sbw = *reinterpret_cast<const uint32_t*>(
-                  raw + UM_CODE_BYTES + r * 8 + ((A.G == 32) ? 4 * hh : 0));
+                  raw + UM_CODE_BYTES + ((A.G == 32 ? hh * 128 : 0) + r) * 4);
               const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
               if (A.s_dt == A.mma_dt) {
                 // packed 16-bit affine (scale and bias already in the MMA type)
@@ -416,7 +434,8 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
           if (A.ksplit > 1)
             A.part[(static_cast<int64_t>(Tl.split) * A.n_tokens + pid) * A.n_rows + m] = acc[i];
           else
-            umma_epilogue(A, pid, m, acc[i], gated ? accg[i] : 0.f, gated);
+            umma_epilogue(A, pid, m, acc[i], gated ? accg[i] : 0.f, gated,
+                          A.out_sorted ? G.p0 + n0 + n : pid);
         }
       }
       tc_fence_before();

@@ -229,7 +229,16 @@ def stack_layers():
 def test_stack_parity(T, rows):
     """Five stacked layers (E = 240..496), the output of each the input of the
     next.  Checked rows are margin-filtered at every layer along the oracle's
-    own residual stream; the other rows are plain draws."""
+    own residual stream; the other rows are plain draws.
+
+    The free-running output is compared with the oracle's own stream: its
+    error is the sum of five layers' errors carried along the residual path,
+    so its max-abs bound is five single-layer bounds (relative RMS stays at
+    the single-layer bound).  Re-running the oracle on the GPU's input to each
+    layer is no test here: with relu^2 experts and no normalisation the
+    synthetic stream grows about quadratically per layer, the later routers'
+    logits saturate, and a 1e-4 relative change of the input already moves
+    the oracle's own expert choice."""
     layers = stack_layers()
     sel = list(range(T)) if rows is None else rows
     xs, _ = gu.margin_x(layers[0], len(sel), seed=40 + T, stack=layers)
@@ -257,7 +266,7 @@ def test_stack_parity(T, rows):
         final = cur.float().cpu().numpy().astype(np.float64)[sel]
         want = ref["out"]
         assert gu.rel_rms(final, want) <= gu.REL_RMS
-        assert gu.max_abs_frac(final, want) <= gu.MAX_ABS_FRAC
+        assert gu.max_abs_frac(final, want) <= len(layers) * gu.MAX_ABS_FRAC
         assert np.isfinite(final).all()
     finally:
         for h in handles:
@@ -427,7 +436,7 @@ def test_refusals_and_allocation_failures_leak_nothing():
         pkg.moe_layer_create(bad, dev)
     assert lib.moe_debug_live_allocations() == base
     n_ok = 0
-    for n in range(1, 40):
+    for n in range(1, 80):
         lib.moe_debug_fail_allocation(n)
         try:
             hh = pkg.moe_layer_create(cfg, dev)
