@@ -83,14 +83,15 @@ def kernel_source_hash(kernel):
     return h.hexdigest()
 
 
-def captured_traffic(kernel, T):
+def captured_traffic(kernel, T, zipf=False):
     """DRAM bytes (read + write) per launch of a kernel from the committed ncu
-    summary profiles/traffic.json, or None when there is none for this kernel
-    and T or the kernels changed since the capture."""
+    summary profiles/traffic.json, or None when there is none for this kernel,
+    T and load (uniform, or Zipf-skewed: key suffix "z") or the kernels changed
+    since the capture."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p)).get("kernels", {}).get(f"{kernel}@T{T}")
+    d = json.load(open(p)).get("kernels", {}).get(f"{kernel}@T{T}{'z' if zipf else ''}")
     if not d or d.get("source_sha256") != kernel_source_hash(kernel):
         return None
     return float(d["dram_bytes_per_launch"])
@@ -523,7 +524,7 @@ def run_ours(args):
             "mean_distinct_experts": float(np.mean(m["n_uniq"])),
             "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved,
                          "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                         "traffic": captured_traffic(dom_name, args.T), "peak_source": peak_src,
+                         "traffic": captured_traffic(dom_name, args.T, args.zipf), "peak_source": peak_src,
                          "timing": "CUDA events around each kernel on its stream (profiled pass)"},
             "profiled_step_ms": float(np.mean(mp["step_ms"])),
             "stages": stages,
