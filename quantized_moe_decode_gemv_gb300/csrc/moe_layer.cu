@@ -108,10 +108,13 @@ struct moe_layer {
   int umma_ctas = 2;      // grouped path: resident CTAs per SM (2 when the TMEM columns allow)
   int umma_v = 0;         // grouped path GEMM: 1 = k_umma (CTA-synchronised K loop), 2 = k_umma2
                           // (warp-specialised roles, tensor copies), 0 = umma_is_v2's choice
-  int gather_min_t = 64;     // grouped path: from this many rows the up GEMM's B rows are gathered
+  int gather_min_t = 1;     // grouped path: from this many rows the up GEMM's B rows are gathered
                              // into sorted pair order first (then read by tensor copies)
   int route_small_t = 16;   // up to this many rows one routing CTA does top-k and lists (at most
                             // ROUTE_SMALL_T); above, row blocks in parallel, then the list CTA
+  int umma_sub = 2;            // grouped path (k_umma2, int4, all tensor copies): chunks per ring slot
+  int umma_sleep_ns = 64;     // grouped path (k_umma2): sleep between mbarrier polls (waiting
+                              // warps leave the issue slots to the working ones)
   int umma_abufs = 3;         // grouped path (k_umma2, int4): dequantised A tiles in the ring
   int umma_tma = 1;           // grouped path (k_umma2): A operand by tensor copies when the layout allows
   int umma_ntile_int4 = 128;  // grouped path: max tokens per MMA tile with int4 (dequantised) A
@@ -420,6 +423,8 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   if (const char* env = std::getenv("MOE_GATHER_MIN_T")) L->gather_min_t = std::max(1, std::atoi(env));
   if (const char* env = std::getenv("MOE_ROUTE_SMALL_T"))
     L->route_small_t = std::max(1, std::min(ROUTE_SMALL_T, std::atoi(env)));
+  if (const char* env = std::getenv("MOE_UMMA_SUB")) L->umma_sub = std::max(1, std::min(2, std::atoi(env)));
+  if (const char* env = std::getenv("MOE_UMMA_SLEEP")) L->umma_sleep_ns = std::max(0, std::min(2000, std::atoi(env)));
   if (const char* env = std::getenv("MOE_UMMA_ABUFS"))
     L->umma_abufs = std::max(2, std::min(UM_MAX_ABUFS, std::atoi(env)));
   if (const char* env = std::getenv("MOE_UMMA_TMA")) L->umma_tma = std::atoi(env) != 0;
@@ -602,11 +607,12 @@ static bool umma_tensor_maps(UmmaArgs& a, int n_experts) {
   const cuuint64_t rows = static_cast<cuuint64_t>(a.n_rows), ngr = static_cast<cuuint64_t>(a.K / a.G);
   const cuuint64_t dims[3] = {words, rows, static_cast<cuuint64_t>(n_experts)};
   const cuuint64_t strides[2] = {words * 4, words * 4 * rows};
-  const cuuint32_t box[3] = {8, 128, 1};
-  // scale/bias words, group-major: 128 rows x the chunk's groups (2 when G = 32)
+  const int sub = a.sub > 1 ? 2 : 1;   // 64-column chunks per ring slot
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(8 * sub), 128, 1};
+  // scale/bias words, group-major: 128 rows x the slot's groups
   const cuuint64_t sdims[3] = {rows, ngr, static_cast<cuuint64_t>(n_experts)};
   const cuuint64_t sstrides[2] = {rows * 4, rows * 4 * ngr};
-  const cuuint32_t sbox[3] = {128, a.G == 32 ? 2u : 1u, 1};
+  const cuuint32_t sbox[3] = {128, static_cast<cuuint32_t>(std::max(1, sub * UM_KC / a.G)), 1};
   if (a.n_rows % 4) return false;
   const uint32_t* qs[2] = {a.q, a.q2};
   const uint32_t* ss[2] = {a.sbT, a.sbT2};
@@ -658,10 +664,11 @@ static size_t umma_config(UmmaArgs& a, int T, size_t budget, int int4_cap) {
   const bool gated = a.a_mode == UA_INT4 && a.q2 != nullptr;
   const int cap = a.a_mode == UA_DENSE ? 256 : int4_cap;
   a.n_tile = std::min(cap, (std::max(1, T) + 15) & ~15);
+  const int sub = a.sub > 1 ? 2 : 1;
   int st = UM_MAX_STAGES;
-  while (st > 3 && umma_plan(a.a_mode, gated, a.n_tile, st, a.abufs).total > budget) --st;
+  while (st > 3 && umma_plan(a.a_mode, gated, a.n_tile, st, a.abufs, sub, a.G).total > budget) --st;
   a.stages = st;
-  return umma_plan(a.a_mode, gated, a.n_tile, st, a.abufs).total;
+  return umma_plan(a.a_mode, gated, a.n_tile, st, a.abufs, sub, a.G).total;
 }
 
 // A grouped launch; a dense matrix with fewer 128-row tiles than SMs splits K
@@ -671,25 +678,37 @@ static cudaError_t launch_umma(moe_layer* h, UmmaArgs& a, int T, cudaStream_t s,
   // not gated), so that one CTA's copies and dequantisation overlap the other's
   const bool gated = a.a_mode == UA_INT4 && a.q2 != nullptr;
   const bool v2 = umma_is_v2(h, a.a_mode == UA_DENSE, T);
-  int per_sm = (h->umma_ctas >= 2 && !gated) ? 2 : 1;
-  a.abufs = 2;
-  size_t smem = umma_config(a, T, per_sm == 2 ? 110 * 1024 : 220 * 1024, h->umma_ntile_int4);
-  if (per_sm == 2 && smem > 110 * 1024) {   // a wide token tile: one CTA per SM
-    per_sm = 1;
-    smem = umma_config(a, T, 220 * 1024, h->umma_ntile_int4);
-  }
-  if (v2 && a.a_mode == UA_INT4 && h->umma_abufs > 2) {
-    // more dequantised A tiles in the ring, while it keeps at least 4 stages
-    const int keep = a.stages;
-    a.abufs = h->umma_abufs;
-    const size_t sm = umma_config(a, T, per_sm == 2 ? 110 * 1024 : 220 * 1024, h->umma_ntile_int4);
-    if (a.stages >= 4 && sm <= static_cast<size_t>(per_sm == 2 ? 110 * 1024 : 220 * 1024)) {
-      smem = sm;
-    } else {
-      a.abufs = 2;
-      a.stages = keep;
+  int per_sm = 1;
+  size_t smem = 0;
+  // tokens per tile, ring depth, A tiles and CTAs per SM for `sub` chunks per slot
+  auto configure = [&](int sub) {
+    a.sub = sub;
+    per_sm = (h->umma_ctas >= 2 && !gated) ? 2 : 1;
+    a.abufs = 2;
+    smem = umma_config(a, T, per_sm == 2 ? 110 * 1024 : 220 * 1024, h->umma_ntile_int4);
+    if (per_sm == 2 && smem > 110 * 1024) {   // a wide token tile: one CTA per SM
+      per_sm = 1;
+      smem = umma_config(a, T, 220 * 1024, h->umma_ntile_int4);
     }
-  }
+    if (v2 && a.a_mode == UA_INT4 && h->umma_abufs > 2) {
+      // more dequantised A tiles in the ring, while it keeps at least 4 stages
+      const int keep = a.stages;
+      a.abufs = h->umma_abufs;
+      const size_t sm = umma_config(a, T, per_sm == 2 ? 110 * 1024 : 220 * 1024, h->umma_ntile_int4);
+      if (a.stages >= 4 && sm <= static_cast<size_t>(per_sm == 2 ? 110 * 1024 : 220 * 1024)) {
+        smem = sm;
+      } else {
+        a.abufs = 2;
+        a.stages = keep;
+      }
+    }
+  };
+  // two chunks per ring slot for int4 when every operand can go by tensor
+  // copies (half the copy issues and slot handshakes per byte), unless the
+  // wider slots would cost the second CTA per SM (measured: slower)
+  const bool want2 = v2 && a.a_mode == UA_INT4 && h->umma_tma && h->umma_sub > 1;
+  configure(want2 ? 2 : 1);
+  if (want2 && per_sm == 1 && h->umma_ctas >= 2 && !gated) configure(1);
   a.ksplit = 1;
   if (!a.experts && T <= UM_KSPLIT_MAX_T) {
     // as many K parts as keep every unit in one wave of CTAs (k_umma2 tiles
@@ -709,6 +728,12 @@ static cudaError_t launch_umma(moe_layer* h, UmmaArgs& a, int T, cudaStream_t s,
   if (v2) {
     a.tma_a = (h->umma_tma && umma_tensor_maps(a, h->cfg.n_experts)) ? 1 : 0;
     a.tma_b = (h->umma_tma && umma_b_map(a)) ? 1 : 0;
+    if (a.sub > 1 && !(a.tma_a && a.tma_b)) {   // a map was ruled out: one chunk per slot
+      configure(1);
+      a.tma_a = (h->umma_tma && umma_tensor_maps(a, h->cfg.n_experts)) ? 1 : 0;
+      a.tma_b = (h->umma_tma && umma_b_map(a)) ? 1 : 0;
+    }
+    a.wait_sleep_ns = h->umma_sleep_ns;
     if (h->um_trace && h->um_trace_n < 4) a.trace = h->um_trace + static_cast<size_t>(h->um_trace_n++) * UM_TRACE_WORDS;
     k_umma2<<<h->num_sms * per_sm, UM_THREADS, smem, s>>>(a);
   } else {
@@ -778,8 +803,7 @@ static cudaError_t launch_fused(moe_layer* h, const FusedArgs& a, int tb, size_t
 }
 
 // Diagnostics: CTA 0's role stamps per chunk of each grouped launch of the last
-// forward, in microseconds since the CTA started (producer issue start / issue
-// end / copies landed, dequant start / done, MMA start / issued, epilogue).
+// forward, in microseconds since the CTA started (SM cycles at 2070 MHz).
 static void print_umma_trace(moe_layer* h, cudaStream_t s) {
   std::vector<unsigned long long> t(static_cast<size_t>(4) * UM_TRACE_WORDS);
   const bool got = cudaMemcpyAsync(t.data(), h->um_trace, t.size() * 8, cudaMemcpyDeviceToHost, s) == cudaSuccess &&
@@ -792,15 +816,15 @@ static void print_umma_trace(moe_layer* h, cudaStream_t s) {
     const unsigned long long* L = t.data() + static_cast<size_t>(l) * UM_TRACE_WORDS;
     const unsigned long long t0 = L[UM_TRACE_CHUNKS * UM_TRACE_STAMPS];
     std::fprintf(stderr,
-                 "umma trace launch %d: chunk: p_begin p_slot p_A p_sb p_B d_landed d_buf d_done m_start m_issued "
-                 "epi p95_B\n",
+                 "umma trace launch %d: chunk: p_begin p_slot p_tx p_tma1 p_tma p_landed d_buf d_done m_start "
+                 "m_issued p_arrived p_cpasync\n",
                  l);
     for (int c = 0; c < UM_TRACE_CHUNKS; ++c) {
       const unsigned long long* R = L + static_cast<size_t>(c) * UM_TRACE_STAMPS;
       if (!R[0] && !R[8]) continue;
       std::fprintf(stderr, "  %3d:", c);
       for (int k = 0; k < UM_TRACE_STAMPS; ++k)
-        std::fprintf(stderr, " %7.2f", R[k] ? (static_cast<double>(R[k]) - static_cast<double>(t0)) * 1e-3 : -1.0);
+        std::fprintf(stderr, " %7.3f", R[k] ? (static_cast<double>(R[k]) - static_cast<double>(t0)) / 2070.0 : -1.0);
       std::fprintf(stderr, "\n");
     }
   }

@@ -106,6 +106,8 @@ struct UmmaArgs {
   //   tokens, or the pairs' hidden rows in sorted order), n_tile x 64 boxes with
   //   the 128-byte swizzle.
   int tma_a, tma_b;
+  int wait_sleep_ns;        // k_umma2: sleep between mbarrier polls (0: poll back to back)
+  int sub;                  // k_umma2: 64-column chunks per ring slot (2: int4 with every operand by tensor copies)
   int b_sorted;             // experts: B row of pair slot n is p0 + n (hidden rows in sorted order)
   int out_sorted;           // UE_ROWS: output row of pair slot n is p0 + n instead of the pair id
   const uint32_t* sbT;      // host: group-major scale/bias words (maps [2], [3])
@@ -202,6 +204,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
         : "r"(mbar), "r"(parity)
         : "memory");
     if (done) return true;
+  }
+  return false;
+}
+
+// Bounded wait that sleeps `ns` between polls (0: poll back to back), so that
+// waiting warps leave the issue slots to the working ones; false on timeout.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t mbar, uint32_t parity, int ns) {
+  if (ns <= 0) return mbar_wait(mbar, parity);
+  for (uint32_t i = 0; i < UM_SPIN_LIMIT; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(done)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    __nanosleep(static_cast<unsigned>(ns));
   }
   return false;
 }
@@ -365,14 +385,22 @@ __device__ __forceinline__ UmmaUnit umma_unit(const int* pref, int n_groups, int
 // then (int4 only) two 16-bit A tiles (x2 when gated), the token table (256
 // ints), the mbarriers, the TMEM address and the unit prefix.
 struct UmmaPlan {
-  uint32_t a_raw, b_bytes, stage, abuf, tok, pref, total;
+  uint32_t code_bytes, sb_bytes, sb_box;   // int4, per matrix and slot: codes, scale/bias region, its copy
+  uint32_t a_raw, b_tile, b_bytes, stage, abuf, tok, pref, total;
 };
 
-__host__ __device__ inline UmmaPlan umma_plan(int a_mode, bool gated, int n_tile, int stages, int abufs = 2) {
+// A ring slot holds `sub` consecutive 64-column chunks (k_umma2 with every
+// operand by tensor copies: 2 for int4; else 1), G the int4 group size.
+__host__ __device__ inline UmmaPlan umma_plan(int a_mode, bool gated, int n_tile, int stages, int abufs = 2,
+                                              int sub = 1, int G = 64) {
   UmmaPlan p;
-  p.a_raw = a_mode == UA_DENSE ? static_cast<uint32_t>(UM_A_BYTES)
-                               : (gated ? 2u : 1u) * static_cast<uint32_t>(UM_CODE_BYTES + UM_SB_BYTES);
-  p.b_bytes = static_cast<uint32_t>(n_tile) * UM_KC * 2;
+  const uint32_t groups = static_cast<uint32_t>(sub * UM_KC / G > 0 ? sub * UM_KC / G : 1);
+  p.code_bytes = static_cast<uint32_t>(UM_CODE_BYTES * sub);
+  p.sb_box = 128u * 4u * groups;
+  p.sb_bytes = p.sb_box > static_cast<uint32_t>(UM_SB_BYTES) ? p.sb_box : static_cast<uint32_t>(UM_SB_BYTES);
+  p.a_raw = a_mode == UA_DENSE ? static_cast<uint32_t>(UM_A_BYTES) : (gated ? 2u : 1u) * (p.code_bytes + p.sb_bytes);
+  p.b_tile = static_cast<uint32_t>(n_tile) * UM_KC * 2;
+  p.b_bytes = p.b_tile * static_cast<uint32_t>(sub);
   p.stage = p.a_raw + p.b_bytes;
   p.abuf = static_cast<uint32_t>(stages) * p.stage;
   const uint32_t abuf_bytes =

@@ -92,11 +92,15 @@ __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
 __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__ UmmaArgs A) {
   extern __shared__ __align__(1024) char um_smem[];
   const bool gated = (A.a_mode == UA_INT4) && A.q2 != nullptr;
-  const UmmaPlan P = umma_plan(A.a_mode, gated, A.n_tile, A.stages, A.abufs);
+  const int SUB = A.sub > 1 ? 2 : 1;   // 64-column chunks per ring slot
+  const UmmaPlan P = umma_plan(A.a_mode, gated, A.n_tile, A.stages, A.abufs, SUB, A.G);
+  const uint32_t CB = P.code_bytes, SBB = P.sb_bytes;
   const int NA = A.abufs;   // dequantised A tiles: chunk c uses buffer c % NA
   // the plan starts on a 1024-byte boundary (swizzled tiles; the plan has the room)
   char* base = um_smem + ((1024u - (smem_u32(um_smem) & 1023u)) & 1023u);
   const bool tma = A.tma_a != 0;
+  // every operand by tensor copies: thread 0 alone produces (no cp.async arrivals)
+  const bool all_tma = tma && A.tma_b != 0;
   const int S = A.stages;
   // barriers and the tensor-memory address in the plan's token-table area
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + P.tok);
@@ -110,15 +114,17 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drainb + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ncols = gated ? 512 : 256;
-  // diagnostics: role stamps of CTA 0 -- producer 0 (before the slot wait),
-  // 1 (slot free), 2 (A issued), 3 (scale/bias issued), 4 (B issued, arrived),
-  // 11 (B issued by the last producer thread); dequant 5 (copies landed),
-  // 6 (A buffer free), 7 (done); MMA 8 (start), 9 (issued); epilogue 10
+  // diagnostics: role stamps of CTA 0 -- producer thread 0: 0 (before the slot
+  // wait), 1 (slot free), 2 (transaction bytes announced), 3 (first tensor
+  // copy issued), 4 (all tensor copies issued), 11 (cp.async copies issued),
+  // 10 (cp.async arrival done); dequant 5 (copies landed), 6 (A buffer free),
+  // 7 (done); MMA 8 (start), 9 (issued)
   unsigned long long* const trace = (A.trace && blockIdx.x == 0) ? A.trace : nullptr;
+  // (SM cycle counter: exact within the CTA)
   auto stamp = [&](uint32_t chunk, int k) {
-    if (trace && chunk < static_cast<uint32_t>(UM_TRACE_CHUNKS)) trace[chunk * UM_TRACE_STAMPS + k] = global_ns();
+    if (trace && chunk < static_cast<uint32_t>(UM_TRACE_CHUNKS)) trace[chunk * UM_TRACE_STAMPS + k] = clock64();
   };
-  if (trace && tid == 0) trace[UM_TRACE_CHUNKS * UM_TRACE_STAMPS] = global_ns();
+  if (trace && tid == 0) trace[UM_TRACE_CHUNKS * UM_TRACE_STAMPS] = clock64();
 
   griddep_wait();
   griddep_launch();
@@ -130,7 +136,7 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
   }
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(smem_u32(&full[s]), (tma || A.tma_b) ? 97 : 96);
+      mbar_init(smem_u32(&full[s]), all_tma ? 1 : ((tma || A.tma_b) ? 97 : 96));
       mbar_init(smem_u32(&empty[s]), 1);
     }
     for (int b = 0; b < NA; ++b) {
@@ -191,7 +197,7 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
   };
   auto wait = [&](uint64_t* b, uint32_t parity) -> bool {
     if (!ok) return false;
-    if (!mbar_wait(smem_u32(b), parity)) {
+    if (!mbar_wait_sleep(smem_u32(b), parity, A.wait_sleep_ns)) {
       ok = false;
       atomicOr(A.status, STATUS_TIMEOUT);
     }
@@ -215,6 +221,7 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
     if (A.tma_b && pt == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&A.tm[8])) : "memory");
     }
+    if (all_tma && pt != 0) ok = false;   // nothing to copy for the other producers (local flag only)
     tiles([&](const UmmaTile& Tl) {
       const int m0 = Tl.m0, n0 = Tl.n0, nvalid = Tl.nvalid;
       const UmmaGroup& G = Tl.G;
@@ -225,7 +232,7 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
       for (int q = 0; q < UM_BPIECES; ++q) {
         const int n = (pt + 96 * q) >> 3;
         brow[q] = -1;
-        if (n < nvalid) {
+        if (n < nvalid && !A.tma_b) {
           if (A.experts && A.b_sorted) {
             brow[q] = G.p0 + n0 + n;
           } else if (A.experts) {
@@ -236,7 +243,9 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
           }
         }
       }
-      for (int it = 0; ok && it < Tl.nit; ++it) {
+      // slot i holds chunks SUB * i .. (a tile's last slot may hold fewer: the
+      // copies past K read as zeros and no MMA reads them)
+      for (int it = 0; ok && it < Tl.nit; it += SUB) {
         const int s = c % S;
         if (pt == 0) stamp(c, 0);
         if (c >= static_cast<uint32_t>(S) && !wait(&empty[s], ((c / S) - 1) & 1)) return;
@@ -247,29 +256,35 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
         const int k0 = (Tl.kc_begin + it) * UM_KC;
         if ((tma || A.tma_b) && pt == 0) {
           // the slot's tensor copies, all counted on full[s]
-          const uint32_t sbx = 128u * 4u * static_cast<uint32_t>(A.G == 32 ? 2 : 1);   // scale/bias box
           uint32_t tx = 0;
           if (tma) tx += A.a_mode == UA_DENSE ? static_cast<uint32_t>(UM_A_BYTES)
-                                              : (gated ? 2u : 1u) * (static_cast<uint32_t>(UM_CODE_BYTES) + sbx);
-          if (A.tma_b) tx += static_cast<uint32_t>(A.n_tile) * 128u;
+                                              : (gated ? 2u : 1u) * (CB + P.sb_box);
+          if (A.tma_b) tx += P.b_bytes;
           mbar_arrive_expect_tx(fb, tx);
+          stamp(c, 2);
           if (tma && A.a_mode == UA_DENSE) {
             // the tile's 128 rows x 64 columns of its segment (rows past the
             // segment's end read as zeros)
             const DenseSeg& Sg = A.seg[Tl.si];
             const int p = (Sg.nparts > 1 && k0 >= Sg.part[1].k0) ? 1 : 0;
             tma_load_2d(sa, &A.tm[2 * Tl.si + p], k0 - Sg.part[p].k0, m0 - Sg.row0, fb);
+            stamp(c, 3);
           } else if (tma) {
             // codes (128 rows x 32 bytes) and the chunk's scale/bias words
             tma_load_3d(sa, &A.tm[0], k0 >> 3, m0, G.e, fb);
-            tma_load_3d(sa + UM_CODE_BYTES, &A.tm[2], m0, k0 / A.G, G.e, fb);
+            stamp(c, 3);
+            tma_load_3d(sa + CB, &A.tm[2], m0, k0 / A.G, G.e, fb);
             if (gated) {
-              tma_load_3d(sa + UM_CODE_BYTES + UM_SB_BYTES, &A.tm[1], k0 >> 3, m0, G.e, fb);
-              tma_load_3d(sa + 2 * UM_CODE_BYTES + UM_SB_BYTES, &A.tm[3], m0, k0 / A.G, G.e, fb);
+              tma_load_3d(sa + CB + SBB, &A.tm[1], k0 >> 3, m0, G.e, fb);
+              tma_load_3d(sa + 2 * CB + SBB, &A.tm[3], m0, k0 / A.G, G.e, fb);
             }
           }
-          // B rows n0.. of the tile (dense tokens, or the pairs' sorted hidden rows)
-          if (A.tma_b) tma_load_2d(sbb, &A.tm[8], k0, A.experts ? G.p0 + n0 : n0, fb);
+          // B rows n0.. of the tile (dense tokens, or the pairs' sorted hidden
+          // rows), one 64-column tile per chunk of the slot
+          if (A.tma_b)
+            for (int j = 0; j < SUB; ++j)
+              tma_load_2d(sbb + j * P.b_tile, &A.tm[8], k0 + j * UM_KC, A.experts ? G.p0 + n0 : n0, fb);
+          stamp(c, 4);
         }
         if (!tma && A.a_mode == UA_DENSE) {
           const DenseSeg& Sg = A.seg[Tl.si];
@@ -299,11 +314,10 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
             const uint32_t nb = (m0 + r < A.n_rows) ? 16u : 0u;
             cp_async16(sa + r * 32 + hh * 16, A.q + row * (A.K >> 3) + (k0 >> 3) + 4 * hh, nb);
             if (gated)
-              cp_async16(sa + UM_CODE_BYTES + UM_SB_BYTES + r * 32 + hh * 16,
+              cp_async16(sa + CB + SBB + r * 32 + hh * 16,
                          A.q2 + row * (A.K >> 3) + (k0 >> 3) + 4 * hh, nb);
           }
         }
-        if (pt == 0) stamp(c, 2);
         if (A.a_mode == UA_INT4 && !tma) {
           // scale/bias words, group-major in the slot ([group of the chunk][row]):
           // one word per row (G >= 64), two (G = 32)
@@ -312,13 +326,12 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
             const int64_t row = static_cast<int64_t>(G.e) * A.n_rows + m;
             const int gw = k0 / A.G;
             for (int h2 = 0; h2 < (A.G == 32 ? 2 : 1); ++h2) {
-              cp_async4(sa + UM_CODE_BYTES + (h2 * 128 + r) * 4, A.sb + row * ngr + gw + h2);
+              cp_async4(sa + CB + (h2 * 128 + r) * 4, A.sb + row * ngr + gw + h2);
               if (gated)
-                cp_async4(sa + 2 * UM_CODE_BYTES + UM_SB_BYTES + (h2 * 128 + r) * 4, A.sb2 + row * ngr + gw + h2);
+                cp_async4(sa + 2 * CB + SBB + (h2 * 128 + r) * 4, A.sb2 + row * ngr + gw + h2);
             }
           }
         }
-        if (pt == 0) stamp(c, 3);
         // B: the tile's valid tokens x 8 pieces of 16 bytes (padding rows only
         // reach accumulator columns that are never read: left as they are)
 #pragma unroll
@@ -346,9 +359,9 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
                      static_cast<const char*>(A.b0) + (A.b0_off + static_cast<int64_t>(row) * A.b0_stride + k0 + 8 * j) * 2,
                      16u);
         }
-        cp_async_mbar_arrive(fb);
-        if (pt == 0) stamp(c, 4);
-        if (pt == 95) stamp(c, 11);
+        if (pt == 0) stamp(c, 11);
+        if (!all_tma) cp_async_mbar_arrive(fb);
+        if (pt == 0) stamp(c, 10);
         ++c;
       }
     });
@@ -361,13 +374,14 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
   } else if (warp >= 4) {
     // ---------------- dequant and epilogue ----------------
     const int dt = tid - 128;   // 0..127: row of the A tile
-    uint32_t c = 0, t = 0;
+    uint32_t c = 0, q = 0, t = 0;   // chunks, ring slots, tiles
     tiles([&](const UmmaTile& Tl) {
       const int n0 = Tl.n0, nvalid = Tl.nvalid, npad = Tl.npad;
       const UmmaGroup& G = Tl.G;
       for (int it = 0; ok && it < Tl.nit; ++it) {
-        const int s = c % S, b = c % NA;
-        if (!wait(&full[s], (c / S) & 1)) return;
+        const int j = it % SUB;   // chunk within the slot
+        const int s = q % S, b = c % NA;
+        if (j == 0 && !wait(&full[s], (q / S) & 1)) return;
         if (dt == 0) stamp(c, 5);
         if (c >= static_cast<uint32_t>(NA) && !wait(&dempty[b], ((c / NA) - 1) & 1)) return;
         if (dt == 0) stamp(c, 6);
@@ -375,13 +389,14 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
           const char* slot = base + static_cast<size_t>(s) * P.stage;
           const int r = dt;
           for (int gsel = 0; gsel < (gated ? 2 : 1); ++gsel) {
-            const char* raw = slot + gsel * (UM_CODE_BYTES + UM_SB_BYTES);
+            const char* raw = slot + gsel * (CB + SBB);
             char* dst = base + P.abuf + static_cast<size_t>(b + NA * gsel) * UM_A_BYTES;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-              const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 32 + hh * 16);
-              const uint32_t sbw = *reinterpret_cast<const uint32_t*>(
-                  raw + UM_CODE_BYTES + ((A.G == 32 ? hh * 128 : 0) + r) * 4);
+              // codes: row r's 32 * SUB bytes; scale/bias: the slot's groups x 128 rows
+              const uint4 w = *reinterpret_cast<const uint4*>(raw + r * (32 * SUB) + 32 * j + hh * 16);
+              const int grp = (UM_KC * j + 32 * hh) / A.G;
+              const uint32_t sbw = *reinterpret_cast<const uint32_t*>(raw + CB + (grp * 128 + r) * 4);
               const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
               if (A.s_dt == A.mma_dt) {
                 // packed 16-bit affine (scale and bias already in the MMA type)
@@ -414,10 +429,10 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
         mbar_arrive(smem_u32(&dfull[b]));
         if (dt == 0) stamp(c, 7);
         ++c;
+        if (j == SUB - 1 || it == Tl.nit - 1) ++q;
       }
       // the tile's accumulators -> epilogue (rows 32 * (warp % 4) + lane)
       if (!wait(accb, t & 1)) return;
-      if (dt == 0) stamp(c - 1, 10);
       tc_fence_after();
       const int q4 = warp & 3;
       const int m = Tl.m0 + 32 * q4 + lane;
@@ -444,14 +459,15 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
     });
   } else if (lane == 0) {
     // ---------------- MMA issuer (warp 0, lane 0) ----------------
-    uint32_t c = 0, t = 0;
+    uint32_t c = 0, q = 0, t = 0;   // chunks, ring slots, tiles
     tiles([&](const UmmaTile& Tl) {
       const int nit = Tl.nit;
       if (t > 0 && !wait(epib, (t - 1) & 1)) return;   // the previous tile's accumulators were read
       tc_fence_after();
       const uint32_t idesc = umma_idesc(Tl.npad, A.mma_dt);
       for (int it = 0; ok && it < nit; ++it) {
-        const int s = c % S, b = c % NA;
+        const int j = it % SUB;
+        const int s = q % S, b = c % NA;
         if (!wait(&dfull[b], (c / NA) & 1)) return;
         stamp(c, 8);
         fence_proxy_async();
@@ -459,7 +475,7 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
         const char* slot = base + static_cast<size_t>(s) * P.stage;
         const uint32_t a_addr = A.a_mode == UA_DENSE ? smem_u32(slot)
                                                      : smem_u32(base + P.abuf + static_cast<size_t>(b) * UM_A_BYTES);
-        const uint32_t b_addr = smem_u32(slot + P.a_raw);
+        const uint32_t b_addr = smem_u32(slot + P.a_raw + j * P.b_tile);
 #pragma unroll
         for (int kk = 0; kk < UM_KC / 16; ++kk) {
           const uint64_t ad = umma_desc_sw128(a_addr + kk * 32);
@@ -470,7 +486,10 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
             umma_f16(tmem + 256, umma_desc_sw128(a2 + kk * 32), bd, idesc, (it | kk) ? 1u : 0u);
           }
         }
-        umma_commit(smem_u32(&empty[s]));
+        if (j == SUB - 1 || it == nit - 1) {   // the slot's last chunk: it may be refilled
+          umma_commit(smem_u32(&empty[s]));
+          ++q;
+        }
         umma_commit(smem_u32(&dempty[b]));
         if (it == nit - 1) umma_commit(smem_u32(accb));
         stamp(c, 9);

@@ -35,7 +35,8 @@ _HANDLES = {}
 
 
 # create-time knobs a cached handle was built under
-KNOBS = ("MOE_UMMA_V", "MOE_UMMA_TMA", "MOE_UMMA_ABUFS", "MOE_UMMA_NTILE")
+KNOBS = ("MOE_UMMA_V", "MOE_UMMA_TMA", "MOE_UMMA_ABUFS", "MOE_UMMA_NTILE", "MOE_UMMA_SUB",
+         "MOE_UMMA_SLEEP", "MOE_GATHER_MIN_T")
 
 
 def handle_for(name, max_tokens, seed=0, zipf=False, layer=None):
@@ -166,12 +167,16 @@ def test_prefill_parity(T, rows, gemm, monkeypatch):
 # --- the tcgen05 grouped path (forced at small T, automatic from T = 64) ------
 
 # grouped GEMM variants, selected at create time: the CTA-synchronised K loop
-# (k_umma); the warp-specialised roles (k_umma2) with A by tensor copies and
-# three dequantised A tiles (default), with A by cp.async, with two A tiles
+# (k_umma); the warp-specialised roles (k_umma2) with every operand by tensor
+# copies, two chunks per ring slot and three dequantised A tiles (default),
+# with every operand by cp.async, with two A tiles, with one chunk per slot
+# and back-to-back polls, with the up GEMM's B rows gathered by cp.async
 GEMM_ENV = {"k_umma": {"MOE_UMMA_V": "1"},
             "k_umma2": {"MOE_UMMA_V": "2"},
             "k_umma2_cpasync": {"MOE_UMMA_V": "2", "MOE_UMMA_TMA": "0"},
-            "k_umma2_2buf": {"MOE_UMMA_V": "2", "MOE_UMMA_ABUFS": "2"}}
+            "k_umma2_2buf": {"MOE_UMMA_V": "2", "MOE_UMMA_ABUFS": "2"},
+            "k_umma2_slot1": {"MOE_UMMA_V": "2", "MOE_UMMA_SUB": "1", "MOE_UMMA_SLEEP": "0"},
+            "k_umma2_nogather": {"MOE_UMMA_V": "2", "MOE_GATHER_MIN_T": "100000"}}
 
 
 @pytest.mark.parametrize("gemm", list(GEMM_ENV))
