@@ -218,6 +218,7 @@ struct RouteArgs {
                          // words in dynamic shared memory (E * mask_words words)
   int debug_times;       // print per-phase timestamps (diagnostics only)
   int topk_only;         // 1: ids and weights only (the lists come from k_route_lists)
+  int rows_per_cta;      // k_route_rows: rows of one CTA (fewer rows: more warps per row)
 };
 
 __device__ __forceinline__ unsigned long long global_ns() {
@@ -660,8 +661,9 @@ static __global__ void __launch_bounds__(ROUTE_THREADS) k_route_rows(const __gri
   griddep_wait();
   griddep_launch();
   RouteArgs B = A;
-  const int t0 = blockIdx.x * ROUTE_ROWS_PER_CTA;
-  B.T = min(ROUTE_ROWS_PER_CTA, A.T - t0);
+  const int rpc = A.rows_per_cta > 0 ? A.rows_per_cta : ROUTE_ROWS_PER_CTA;
+  const int t0 = blockIdx.x * rpc;
+  B.T = min(rpc, A.T - t0);
   B.logits = A.logits + static_cast<int64_t>(t0) * A.r_in;
   B.ids = A.ids + t0 * A.k;
   B.w = A.w + t0 * A.k;

@@ -110,7 +110,9 @@ struct moe_layer {
                           // (warp-specialised roles, tensor copies), 0 = umma_is_v2's choice
   int gather_min_t = 1;     // grouped path: from this many rows the up GEMM's B rows are gathered
                              // into sorted pair order first (then read by tensor copies)
-  int route_small_t = 16;   // up to this many rows one routing CTA does top-k and lists (at most
+  int route_rpc = 2;         // rows per routing CTA up to route_rpc_max_t rows (else 16)
+  int route_rpc_max_t = 256;
+  int route_small_t = 8;   // up to this many rows one routing CTA does top-k and lists (at most
                             // ROUTE_SMALL_T); above, row blocks in parallel, then the list CTA
   int umma_sub = 2;            // grouped path (k_umma2, int4, all tensor copies): chunks per ring slot
   int umma_sleep_ns = 64;     // grouped path (k_umma2): sleep between mbarrier polls (waiting
@@ -421,6 +423,8 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   if (const char* env = std::getenv("MOE_UMMA_CTAS")) L->umma_ctas = std::max(1, std::min(2, std::atoi(env)));
   if (const char* env = std::getenv("MOE_UMMA_V")) L->umma_v = std::max(0, std::min(2, std::atoi(env)));
   if (const char* env = std::getenv("MOE_GATHER_MIN_T")) L->gather_min_t = std::max(1, std::atoi(env));
+  if (const char* env = std::getenv("MOE_ROUTE_RPC"))
+    L->route_rpc = std::max(1, std::min(ROUTE_ROWS_PER_CTA, std::atoi(env)));
   if (const char* env = std::getenv("MOE_ROUTE_SMALL_T"))
     L->route_small_t = std::max(1, std::min(ROUTE_SMALL_T, std::atoi(env)));
   if (const char* env = std::getenv("MOE_UMMA_SUB")) L->umma_sub = std::max(1, std::min(2, std::atoi(env)));
@@ -1119,7 +1123,9 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     // many rows: top-k over row blocks in parallel, then the lists in one CTA
     RouteArgs rr = ra;
     rr.mask_words = 0;
-    if ((e = launch_ex<RouteArgs>(k_route_rows, (T + ROUTE_ROWS_PER_CTA - 1) / ROUTE_ROWS_PER_CTA,
+    // few rows per CTA while the grid stays small: four warps share a row's keys
+    rr.rows_per_cta = T <= h->route_rpc_max_t ? h->route_rpc : ROUTE_ROWS_PER_CTA;
+    if ((e = launch_ex<RouteArgs>(k_route_rows, (T + rr.rows_per_cta - 1) / rr.rows_per_cta,
                                   ROUTE_THREADS, ROUTE_SMEM_BYTES, s, pdl, rr)) != cudaSuccess)
       goto cuda_fail;
     ++nl;
