@@ -71,15 +71,41 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text):
+    """C/C++ source without its comments and blank lines (string literals kept)."""
+    import re
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"':                                   # string literal
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = [ln.rstrip() for ln in "".join(out).splitlines()]
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
 def kernel_source_hash(kernel):
-    """sha256 over the CUDA sources of a kernel, so that DRAM traffic captured
-    by ncu is only reported for the code it was captured from."""
+    """sha256 over the code (comments stripped) of a kernel's CUDA sources, so
+    that DRAM traffic captured by ncu is only reported for the code it was
+    captured from."""
     import hashlib
     d = os.path.join(ROOT, "quantized_moe_decode_gemv_gb300", "csrc")
     h = hashlib.sha256()
     for name in KERNEL_SOURCES.get(kernel, sorted(os.listdir(d))):
-        with open(os.path.join(d, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        with open(os.path.join(d, name), encoding="utf-8") as f:
+            h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()
 
 

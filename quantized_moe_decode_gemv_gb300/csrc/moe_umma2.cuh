@@ -1,35 +1,38 @@
 // Row-grouped GEMM on tcgen05 with warp-specialised roles (k_umma2).
 //
-// Same contraction, operands, shared-memory layouts and epilogue as k_umma
-// (moe_umma.cuh), but the three jobs of a K-chunk run in different warps and
-// meet on mbarriers instead of CTA barriers, so copies, int4 dequantisation
-// and tensor-core MMAs of different chunks overlap:
+// The contraction and epilogue of k_umma (moe_umma.cuh), with the three jobs
+// of a 64-column K-chunk in different warps that meet on mbarriers, so that
+// copies, int4 dequantisation and tensor-core MMAs of different chunks
+// overlap.  Work units are (group, 128-row A tile, token tile); every operand
+// tile is K-major with the 128-byte swizzle.
 //
-//   warps 1-3  producers: the copies of chunk c into ring slot c % S.  The
-//              A operand (16-bit weight rows, or int4 codes) goes by tensor
-//              copies that thread 0 issues against host-encoded maps (by
-//              cp.async when the layout rules out a map); the int4 scale/bias
-//              words and the B operand (the tokens' 16-bit rows, gathered
-//              per pair) go by cp.async.  Each producer's arrival on full[s]
-//              fires when its cp.async copies land, and thread 0 adds the
-//              tensor copies' byte count, so no producer waits for its own
-//              copies and the ring runs up to S chunks ahead of the MMAs.
-//              (A per-thread wait for landed copies before arriving tied
-//              the ring's progress to the MMAs two chunks back.)
+//   warps 1-3  producers: the copies of ring slot q (SUB = 1 or 2 chunks).
+//              Thread 0 issues tensor copies against host-encoded maps: the
+//              A operand (16-bit weight rows, or int4 codes and their
+//              group-major scale/bias words) and, where the rows form a
+//              plain matrix, the B operand (the dense tokens, or the pairs'
+//              rows in sorted order), and arrives on full[s] with their byte
+//              count.  What no map describes goes by cp.async from all 96
+//              threads, each arriving through cp.async.mbarrier.arrive.noinc
+//              when its copies land; no producer waits for its own copies,
+//              and with every operand by tensor copies thread 0 is the only
+//              producer.  (A per-thread wait for landed copies before
+//              arriving tied the ring to the MMAs two chunks back.)
 //   warps 4-7  dequant: int4 -> 16-bit A tile in buffer c % NA (after full[s]
 //              and after the MMAs of chunk c - NA released the buffer), then
 //              arrive on dfull[c % NA].  After a tile's last chunk they read
 //              the accumulators from tensor memory and write the epilogue.
 //   warp 0     lane 0 issues the tcgen05.mma of chunk c once dfull[c % NA]
-//              completes and commits them to empty[c % S] (the slot may be
-//              refilled), dempty[c % NA] (the A buffer may be rewritten) and,
-//              after a tile's last chunk, acc (the accumulators are final).
+//              completes and commits them to dempty[c % NA] (the A buffer may
+//              be rewritten), after a slot's last chunk to empty[s] (the slot
+//              may be refilled) and after a tile's last chunk to acc (the
+//              accumulators are final).
 //
-// Every role walks the same sequence of tiles and chunks, so the barrier
-// phases are implied by the chunk and tile counts.  Every wait is bounded;
-// on a timeout the role sets the status word's timeout bit and stops, the
-// other roles' waits then run out too, and the kernel drains its copies and
-// MMAs (bounded) before it frees tensor memory.
+// Every role walks the same sequence of tiles, slots and chunks, so the
+// barrier phases are implied by the counts.  Every wait is bounded (waiting
+// roles sleep between polls); on a timeout the role sets the status word's
+// timeout bit and stops, the other roles' waits then run out too, and the
+// kernel drains its copies and MMAs (bounded) before it frees tensor memory.
 #pragma once
 
 #include "moe_umma.cuh"
