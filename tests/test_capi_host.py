@@ -110,3 +110,37 @@ def test_create_refuses_before_any_allocation(lib):
     assert h.value is None
     assert lib.moe_debug_live_allocations() == before
     assert b"top_k" in lib.moe_layer_last_error(None)
+
+
+# --- bench.py's gate on captured DRAM traffic ------------------------------------
+
+def test_traffic_gate_ignores_comments_but_not_code():
+    """The captured-traffic hash follows the code only: comments and blank
+    lines do not change it, a changed statement or string literal does."""
+    import bench
+    a = 'int f() {\n  // launch 304 CTAs\n  return g("a // b", 304); /* grid */\n}\n'
+    b = 'int f() {\n\n  return g("a // b", 304);   // comments moved\n}\n'
+    c = 'int f() {\n  return g("a // b", 152);\n}\n'
+    d = 'int f() {\n  return g("a // c", 304);\n}\n'
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
+    assert bench._code_only(a) != bench._code_only(d)
+
+
+def test_traffic_gate_matches_the_committed_capture():
+    """Every captured kernel in profiles/traffic.json either matches the
+    current sources (reported) or is reported as null -- never a stale number."""
+    import json
+    import bench
+    path = os.path.join(os.path.dirname(os.path.dirname(__file__)), "profiles", "traffic.json")
+    if not os.path.exists(path):
+        pytest.skip("no captured traffic")
+    for key, rec in json.load(open(path))["kernels"].items():
+        kernel, tz = key.split("@T")
+        zipf = tz.endswith("z")
+        T = int(tz.rstrip("z"))
+        got = bench.captured_traffic(kernel, T, zipf)
+        if rec["source_sha256"] == bench.kernel_source_hash(kernel):
+            assert got == float(rec["dram_bytes_per_launch"])
+        else:
+            assert got is None
