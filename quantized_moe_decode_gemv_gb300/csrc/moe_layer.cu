@@ -563,7 +563,7 @@ moe_status moe_layer_destroy(moe_layer* h) {
   return MOE_OK;
 }
 
-// The driver's tensor-map encoder (looked up once through the runtime).
+// The CUDA driver API's tensor-map encoder (looked up once through the runtime).
 static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static bool tried = false;
