@@ -63,7 +63,8 @@ KERNEL_OF_STAGE_GROUPED = {"dense_in": "k_umma2", "route": "k_route", "expert_up
 KERNEL_SOURCES = {
     "k_dense_in": ["moe_kernels.cuh", "moe_layer.cu"],
     "k_dense_out": ["moe_kernels.cuh", "moe_layer.cu"],
-    "k_expert": ["moe_kernels.cuh", "moe_layer.cu"],
+    # the expert gemv kernel: its device code and the host code that launches it
+    "k_expert": ["moe_kernels.cuh", "moe_layer.cu:expert_gemv_launch"],
     "k_route": ["moe_kernels.cuh", "moe_layer.cu"],
     "k_umma": ["moe_kernels.cuh", "moe_umma.cuh", "moe_layer.cu"],
     "k_umma2": ["moe_kernels.cuh", "moe_umma.cuh", "moe_umma2.cuh", "moe_layer.cu"],
@@ -96,16 +97,51 @@ def _code_only(text):
     return "\n".join(ln for ln in lines if ln.strip())
 
 
+def _braced(text, start):
+    """text from `start` through the brace that closes the first "{" after it."""
+    i = text.index("{", start)
+    depth = 0
+    for j in range(i, len(text)):
+        depth += {"{": 1, "}": -1}.get(text[j], 0)
+        if depth == 0:
+            return text[start:j + 1]
+    raise ValueError("unbalanced braces")
+
+
+def _expert_gemv_launch(code):
+    """The host code that configures and launches the expert gemv kernel: its
+    launch helpers, the token-slot and grid sizing statements and the two
+    launch blocks of the forward."""
+    import re
+    parts = []
+    for fn in ("expert_pb_cap", "pow2_at_least", "launch_ex", "launch_expert_t", "launch_expert"):
+        m = re.search(r"^static [^\n(]*\b" + fn + r"\(", code, flags=re.M)
+        parts.append(_braced(code, m.start()))
+    for var in ("pb_split", "pb_up", "pb_dn", "slots", "target"):
+        i = code.index("const int " + var + " =")
+        parts.append(code[i:code.index(";", i) + 1])
+    for m in re.finditer(r"if \(experts_gemv\) \{", code):
+        parts.append(_braced(code, m.start()))
+    return "\n".join(parts)
+
+
+SOURCE_PARTS = {"expert_gemv_launch": _expert_gemv_launch}
+
+
 def kernel_source_hash(kernel):
-    """sha256 over the code (comments stripped) of a kernel's CUDA sources, so
-    that DRAM traffic captured by ncu is only reported for the code it was
-    captured from."""
+    """sha256 over the code (comments stripped) of a kernel's CUDA sources --
+    whole files, or the named part of a file ("file:part") -- so that DRAM
+    traffic captured by ncu is only reported for the code it was captured from."""
     import hashlib
     d = os.path.join(ROOT, "quantized_moe_decode_gemv_gb300", "csrc")
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES.get(kernel, sorted(os.listdir(d))):
+    for entry in KERNEL_SOURCES.get(kernel, sorted(os.listdir(d))):
+        name, _, part = entry.partition(":")
         with open(os.path.join(d, name), encoding="utf-8") as f:
-            h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
+            code = _code_only(f.read())
+        if part:
+            code = SOURCE_PARTS[part](code)
+        h.update(entry.encode() + b"\0" + code.encode())
     return h.hexdigest()
 
 

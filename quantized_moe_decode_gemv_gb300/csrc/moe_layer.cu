@@ -102,6 +102,7 @@ struct moe_layer {
   unsigned long long* fz_trace = nullptr;   // diagnostics (MOE_FUSED_TRACE): phase stamps
   unsigned long long* um_trace = nullptr;   // diagnostics (MOE_UMMA_TRACE): grouped GEMM role stamps
   int um_trace_n = 0;                       // grouped launches stamped in this forward
+  int pdl_grouped = 1;    // programmatic dependent launch between the grouped-path kernels too
   int use_pdl = 1;        // programmatic dependent launch between the gemv-path kernels
   int expert_pb = 2;      // max token slots per pass of the gemv-path expert kernels
   int expert_target = 4;  // gemv-path expert kernels: CTAs per SM the grid is sized for
@@ -411,6 +412,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   if (const char* env = std::getenv("MOE_COMBINE_MIN_T")) L->combine_min_t = std::max(1, std::atoi(env));
   if (const char* env = std::getenv("MOE_EXPERT_SPLIT")) L->expert_split = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_PDL")) L->use_pdl = std::atoi(env) != 0;
+  if (const char* env = std::getenv("MOE_PDL_GROUPED")) L->pdl_grouped = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_FUSED_MAX_T")) L->fused_max_t = std::atoi(env);
   if (const char* env = std::getenv("MOE_SD_PRE")) L->fused_sd_pre = std::max(0, std::min(100, std::atoi(env)));
   if (const char* env = std::getenv("MOE_SD_MID")) L->fused_sd_mid = std::max(0, std::min(100, std::atoi(env)));
@@ -677,7 +679,7 @@ static size_t umma_config(UmmaArgs& a, int T, size_t budget, int int4_cap) {
 
 // A grouped launch; a dense matrix with fewer 128-row tiles than SMs splits K
 // over several CTAs and sums the partials in a second, deterministic pass.
-static cudaError_t launch_umma(moe_layer* h, UmmaArgs& a, int T, cudaStream_t s, int* nl) {
+static cudaError_t launch_umma(moe_layer* h, UmmaArgs& a, int T, cudaStream_t s, int* nl, bool pdl) {
   // two CTAs per SM when the accumulators fit twice in TMEM (256 columns each:
   // not gated), so that one CTA's copies and dequantisation overlap the other's
   const bool gated = a.a_mode == UA_INT4 && a.q2 != nullptr;
@@ -739,18 +741,16 @@ static cudaError_t launch_umma(moe_layer* h, UmmaArgs& a, int T, cudaStream_t s,
     }
     a.wait_sleep_ns = h->umma_sleep_ns;
     if (h->um_trace && h->um_trace_n < 4) a.trace = h->um_trace + static_cast<size_t>(h->um_trace_n++) * UM_TRACE_WORDS;
-    k_umma2<<<h->num_sms * per_sm, UM_THREADS, smem, s>>>(a);
   } else {
     a.tma_a = a.tma_b = 0;
     if (a.b_sorted || a.out_sorted) return cudaErrorInvalidValue;   // sorted rows are k_umma2's
-    k_umma<<<h->num_sms * per_sm, UM_THREADS, smem, s>>>(a);
   }
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_ex<UmmaArgs>(v2 ? k_umma2 : k_umma, h->num_sms * per_sm, UM_THREADS, smem, s, pdl, a);
   if (e == cudaSuccess) ++*nl;
   if (e == cudaSuccess && a.ksplit > 1) {
     const int64_t n = static_cast<int64_t>(T) * a.n_rows;
-    k_umma_reduce<<<static_cast<int>(std::min<int64_t>((n + 255) / 256, h->num_sms * 8)), 256, 0, s>>>(a);
-    e = cudaGetLastError();
+    e = launch_ex<UmmaArgs>(k_umma_reduce, static_cast<int>(std::min<int64_t>((n + 255) / 256, h->num_sms * 8)),
+                            256, 0, s, pdl, a);
     if (e == cudaSuccess) ++*nl;
   }
   return e;
@@ -1031,7 +1031,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
   }
   const bool big_route = T > h->route_small_t;
   const bool fuse_route = !grouped && h->fuse_route && !big_route;
-  const bool pdl = h->use_pdl && !grouped && !h->profiling;
+  const bool pdl = h->use_pdl && (!grouped || h->pdl_grouped) && !h->profiling;
 
   // 1. dense matrices that read x: router, fc1_latent_proj, shared gate/up
   mark(0);
@@ -1112,7 +1112,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
         ua.out_col0 = col0;
         ua.k = k;
         ua.status = h->status;
-        if ((e = launch_umma(h, ua, T, s, &nl)) != cudaSuccess) goto cuda_fail;
+        if ((e = launch_umma(h, ua, T, s, &nl, pdl)) != cudaSuccess) goto cuda_fail;
       }
     }
   }
@@ -1231,7 +1231,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
         ga.out = static_cast<unsigned short*>(h->xs);
         const int64_t n = static_cast<int64_t>(T) * k * (kin / 8);
         const int gg = static_cast<int>(std::min<int64_t>((n + 255) / 256, h->num_sms * 8));
-        if ((e = launch_ex<GatherArgs>(k_gather_pairs, gg, 256, 0, s, false, ga)) != cudaSuccess) goto cuda_fail;
+        if ((e = launch_ex<GatherArgs>(k_gather_pairs, gg, 256, 0, s, pdl, ga)) != cudaSuccess) goto cuda_fail;
         ++nl;
         uup.b0 = h->xs; uup.b0_stride = kin; uup.b0_off = 0;
         uup.b_sorted = 1;
@@ -1242,7 +1242,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
       uup.act = c.act;
       uup.out_f32 = h->hbuf;
       uup.status = h->status;
-      if ((e = launch_umma(h, uup, T, s, &nl)) != cudaSuccess) goto cuda_fail;
+      if ((e = launch_umma(h, uup, T, s, &nl, pdl)) != cudaSuccess) goto cuda_fail;
 
     }
     mark(3);
@@ -1282,7 +1282,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
       udn.sbT2 = nullptr;
       udn.act = -1;
       udn.out_f32 = h->pexp;
-      if ((e = launch_umma(h, udn, T, s, &nl)) != cudaSuccess) goto cuda_fail;
+      if ((e = launch_umma(h, udn, T, s, &nl, pdl)) != cudaSuccess) goto cuda_fail;
     }
   }
 
@@ -1295,8 +1295,9 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     pa.sh_g_off = h->off_shg; pa.sh_u_off = h->off_shu;
     pa.bout = static_cast<unsigned short*>(h->bout);
     const int64_t n = static_cast<int64_t>(T) * kout;
-    k_prep_out<<<static_cast<int>(std::min<int64_t>((n + 255) / 256, 4096)), 256, 0, s>>>(pa);
-    if ((e = cudaGetLastError()) != cudaSuccess) goto cuda_fail;
+    if ((e = launch_ex<PrepOutArgs>(k_prep_out, static_cast<int>(std::min<int64_t>((n + 255) / 256, 4096)), 256, 0,
+                                    s, pdl, pa)) != cudaSuccess)
+      goto cuda_fail;
     ++nl;
     UmmaArgs ua{};
     DenseSeg& S = ua.seg[0];
@@ -1318,7 +1319,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     ua.x = x; ua.x_dt = c.act_dtype; ua.out = out; ua.delta = delta;
     ua.pexp = h->pexp; ua.wts = h->wts; ua.add_combine = Lt ? 0 : 1;
     ua.status = h->status;
-    if ((e = launch_umma(h, ua, T, s, &nl)) != cudaSuccess) goto cuda_fail;
+    if ((e = launch_umma(h, ua, T, s, &nl, pdl)) != cudaSuccess) goto cuda_fail;
   } else {
     DenseOutArgs dout{};
     dout.nseg = 0;
