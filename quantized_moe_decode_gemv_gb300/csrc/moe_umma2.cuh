@@ -216,10 +216,19 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
     const int pt = tid - 32;   // 0..95
     uint32_t c = 0;
     if (tma && pt == 0) {
-      const int nmaps = A.a_mode == UA_DENSE ? 2 * A.nseg : (gated ? 4 : 3);
-      for (int i = 0; i < nmaps; ++i)
-        if (A.a_mode == UA_DENSE || gated || i != 1)
-          asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&A.tm[i])) : "memory");
+      // the encoded maps only: dense [2 * seg + part]; int4 codes [0], scale/bias [2]
+      // (and the gate's [1], [3])
+      auto prefetch = [&](int i) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&A.tm[i])) : "memory");
+      };
+      if (A.a_mode == UA_DENSE) {
+        for (int si = 0; si < A.nseg; ++si)
+          for (int p = 0; p < A.seg[si].nparts; ++p) prefetch(2 * si + p);
+      } else {
+        prefetch(0);
+        prefetch(2);
+        if (gated) { prefetch(1); prefetch(3); }
+      }
     }
     if (A.tma_b && pt == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&A.tm[8])) : "memory");
