@@ -267,7 +267,13 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
         const uint32_t fb = smem_u32(&full[s]);
         const int k0 = (Tl.kc_begin + it) * UM_KC;
         if ((tma || A.tma_b) && pt == 0) {
-          // the slot's tensor copies, all counted on full[s]
+          // the slot's tensor copies, all counted on full[s].  Every innermost
+          // coordinate is a multiple of 16 bytes: dense A and B columns are
+          // multiples of 64 elements (128 bytes), code words k0 / 8 are
+          // multiples of 8 words (32 bytes), scale/bias rows m0 multiples of
+          // 128 words; destinations are 1024-byte (swizzled tiles) or 128-byte
+          // aligned (codes, scale/bias), as the plan guarantees.
+
           uint32_t tx = 0;
           if (tma) tx += A.a_mode == UA_DENSE ? static_cast<uint32_t>(UM_A_BYTES)
                                               : (gated ? 2u : 1u) * (CB + P.sb_box);
