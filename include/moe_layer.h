@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 typedef enum moe_status {
   MOE_OK = 0,
@@ -240,27 +240,32 @@ const char *moe_layer_last_error(const moe_layer *h);
  * allocator, an engine that fixes its memory plan up front, or a
  * latency-critical path where an allocation could synchronise the device.
  * Creating a moe_layer handle allocates a workspace; this call does not.  It
- * computes exactly what moe_layer_forward_ex returns in topk_ids / topk_w for
- * the same x, router weight, bias and routing options, with the same kernel,
- * and writes
+ * applies the same router gemv and top-k selection rules as
+ * moe_layer_forward_ex (the routing block fused into the dense gemv kernel)
+ * to the same x, router weight, bias and routing options, and writes
  *   topk_ids[T, k]  int32, selection order (larger key first, ties to the
  *                   lower index, non-finite keys last),
- *   topk_w[T, k]    fp32 combine weights.
+ *   topk_w[T, k]    fp32 combine weights,
+ *   *key_status     int32, only when key_status is not NULL: 0, or bit 0 set
+ *                   (value 1) when a selection key of this call was NaN or
+ *                   infinite -- the condition moe_layer_device_status reports
+ *                   as MOE_ERR_NONFINITE.  With key_status NULL that
+ *                   condition is not reported (the keys still rank last).
  * Inputs: x[T, hidden] (x_dtype BF16|FP16), router_w[n_experts, hidden]
  * (router_dtype), router_bias[n_experts] fp32 or NULL (sigmoid routing only).
  * All pointers are DEVICE pointers owned by the caller; the call is
  * asynchronous on `stream`.
  *
- * Scratch: a fixed array in the library's device memory (logits for up to
- * MOE_NOALLOC_MAX_TOKENS x 1024 experts plus route lists, about 270 KB) that
- * every GPU loading the library holds until the process exits.  Limits:
- * T <= MOE_NOALLOC_MAX_TOKENS, n_experts <= 1024, top_k <= 16; larger sizes
- * return MOE_ERR_UNSUPPORTED.  The first call on a device looks up the
- * array's device address and sets kernel attributes (once per device, with
- * that device current); make that first call before any stream capture.
- * Every call shares the one array and clears what must start at zero, so
- * calls that overlap on the GPU (on different streams, or from several host
- * threads without ordering) race and must not be issued.
+ * Scratch: a fixed array in the library's device memory (the fp32 logits of
+ * up to MOE_NOALLOC_MAX_TOKENS rows x 1024 experts, a counter and a status
+ * word: 256 KB) that every GPU loading the library holds until the process
+ * exits.  Limits: T <= MOE_NOALLOC_MAX_TOKENS, n_experts <= 1024,
+ * top_k <= 16; larger sizes return MOE_ERR_UNSUPPORTED.  The first call on a
+ * device looks up the array's device address and sets kernel attributes (once
+ * per device, with that device current); make that first call before any
+ * stream capture.  Every call shares the one array and clears what must start
+ * at zero, so calls that overlap on the GPU (on different streams, or from
+ * several host threads without ordering) race and must not be issued.
  * Errors: MOE_ERR_INVALID_ARG (NULL pointer, T < 1, hidden not a positive
  * multiple of 64, unknown enum), MOE_ERR_TOPK_GT_E, MOE_ERR_UNSUPPORTED,
  * MOE_ERR_DEVICE (not compute capability 10.3), MOE_ERR_CUDA (launch). */
@@ -268,7 +273,8 @@ moe_status moe_router_topk_noalloc(const void *x, int32_t T, int32_t hidden, int
                                    const void *router_w, int32_t router_dtype,
                                    const float *router_bias, int32_t n_experts, int32_t top_k,
                                    int32_t router, int32_t renormalize, float routed_scale,
-                                   int32_t *topk_ids, float *topk_w, void *stream);
+                                   int32_t *topk_ids, float *topk_w, int32_t *key_status,
+                                   void *stream);
 
 /* Device allocations currently held by all handles of this process (for leak
  * checks around refused creates). */

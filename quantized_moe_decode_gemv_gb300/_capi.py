@@ -87,7 +87,8 @@ SIGNATURES = {
                                                ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32,
                                                ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                                ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
-                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                               ctypes.c_void_p]),
     "moe_debug_live_allocations": (ctypes.c_int64, []),
     "moe_debug_fail_allocation": (None, [ctypes.c_int32]),
 }
@@ -255,13 +256,16 @@ def moe_layer_device_status(handle: int, stream: int = 0) -> int:
 def moe_router_topk_noalloc(x, T: int, hidden: int, x_dtype: str, router_w, router_dtype: str,
                             router_bias, n_experts: int, top_k: int, router: str,
                             renormalize: bool, routed_scale: float, topk_ids, topk_w,
-                            stream: int = 0) -> None:
-    """Router gemv + top-k with no device allocation (see include/moe_layer.h)."""
+                            stream: int = 0, key_status=None) -> None:
+    """Router gemv + top-k with no device allocation (see include/moe_layer.h).
+    ``key_status``: optional device int32 tensor of one element that receives 1
+    when a selection key was NaN or infinite, else 0."""
     lib = load_library()
     _check(lib.moe_router_topk_noalloc(_ptr(x), T, hidden, DTYPE[x_dtype], _ptr(router_w),
                                        DTYPE[router_dtype], _ptr(router_bias), n_experts, top_k,
                                        ROUTER[router], int(bool(renormalize)), float(routed_scale),
-                                       _ptr(topk_ids), _ptr(topk_w), ctypes.c_void_p(stream)))
+                                       _ptr(topk_ids), _ptr(topk_w), _ptr(key_status),
+                                       ctypes.c_void_p(stream)))
 
 
 def moe_layer_destroy(handle: int) -> None:

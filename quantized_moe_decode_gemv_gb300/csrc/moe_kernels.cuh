@@ -189,6 +189,7 @@ struct CombineArgs {
   const float* dense_in;  // [T, r_in]
   int r_in, sh_g_off, sh_u_off;
   float* comb;            // [T, L + Fs]
+  unsigned long long* trace;   // diagnostics: CTA stamps or null
 };
 
 // ---------------------------------------------------------------------------
@@ -225,6 +226,16 @@ __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+// Diagnostics (MOE_CTA_TRACE): per-CTA global-timer stamps of a launch --
+// 0 entry, 1 past the wait for the previous kernel, 2 main loop done, 3 exit.
+constexpr int CT_MAX_CTAS = 2048;
+constexpr int CT_STAMPS = 4;
+constexpr int CT_SLOTS = 12;   // launches stamped per forward
+__device__ __forceinline__ void cta_stamp(unsigned long long* t, int i) {
+  if (t != nullptr && threadIdx.x == 0 && blockIdx.x < CT_MAX_CTAS)
+    t[blockIdx.x * CT_STAMPS + i] = global_ns();
 }
 
 __device__ __forceinline__ bool key_better(float a, int ia, float b, int ib) {
@@ -728,6 +739,7 @@ struct DenseInArgs {
   int64_t pf_budget;         // at most this many bytes
   const uint32_t* pf_q; const uint32_t* pf_sb; const uint32_t* pf_q2; const uint32_t* pf_sb2;
   int64_t pf_q_bytes, pf_sb_bytes;   // per expert
+  unsigned long long* trace;   // diagnostics: CTA stamps or null
 };
 
 struct DenseOutArgs {
@@ -753,6 +765,7 @@ struct DenseOutArgs {
   int T;
   int prefetch;      // prefetch this CTA's weight rows into L2 before waiting
   const float* staged;  // [T, K] fp32 staged vector computed once (k_combine), or null
+  unsigned long long* trace;   // diagnostics: CTA stamps or null
 };
 
 // Rows of the dense weights per register batch: every thread keeps partial sums
@@ -950,8 +963,10 @@ __global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_in(const _
   float* xs = reinterpret_cast<float*>(smem4);
   float* red = xs + TB * A.K;
   const int K4 = A.K >> 2;
+  cta_stamp(A.trace, 0);
   griddep_wait();
   griddep_launch();
+  cta_stamp(A.trace, 1);
   int rb, re;
   if (A.fuse_route) {
     // the first route_ctas CTAs take the router rows [0, E) (fewer rows each,
@@ -990,6 +1005,7 @@ __global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_in(const _
       __syncthreads();
     }
   }
+  cta_stamp(A.trace, 2);
   if (A.fuse_route && static_cast<int>(blockIdx.x) < A.route_ctas) {
     // the last CTA to finish router rows routes all T rows
     __shared__ int s_last;
@@ -1019,6 +1035,7 @@ __global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_in(const _
       }
     }
   }
+  cta_stamp(A.trace, 3);
 }
 
 template <int TB>
@@ -1030,6 +1047,7 @@ __global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_out(const 
   const int L = A.latent;
   const int Kin = L ? L : A.total_rows;
   int rb, re;
+  cta_stamp(A.trace, 0);
   cta_rows(A.total_rows, rb, re);
   // the weights do not depend on this forward's earlier kernels: start them
   // towards L2 while those finish
@@ -1041,6 +1059,7 @@ __global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_out(const 
   }
   griddep_wait();
   griddep_launch();
+  cta_stamp(A.trace, 1);
   for (int t0 = 0; t0 < A.T; t0 += TB) {
     const int tb = min(TB, A.T - t0);
     if (t0) __syncthreads();
@@ -1106,6 +1125,7 @@ __global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_out(const 
       __syncthreads();
     }
   }
+  cta_stamp(A.trace, 3);
 }
 
 // ---------------------------------------------------------------------------
@@ -1143,6 +1163,7 @@ struct ExpertArgs {
   int prefetch;            // prefetch this CTA's weight rows into L2 (pre-wait phase)
   int cps;                 // CTAs per distinct-expert slot (grid = umax * cps)
   int max_pairs;           // > 0: slots with more token pairs are left to the grouped GEMM
+  unsigned long long* trace;   // diagnostics: CTA stamps or null
 };
 
 __device__ __forceinline__ void sb_decode(uint32_t v, int dt, float& s, float& b) {
@@ -1191,17 +1212,19 @@ __global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(c
   const int* uniq_e = A.meta + 1;
   const int* uniq_p0 = A.meta + 1 + A.umax;
   const int* pairs = A.meta + 2 + 2 * A.umax;
+  cta_stamp(A.trace, 0);
   if (!A.pre_wait_phase) griddep_wait();
   griddep_launch();
-  if (u >= A.meta[0]) return;
-  if (A.max_pairs > 0 && uniq_p0[u + 1] - uniq_p0[u] > A.max_pairs) return;
+  if (!A.pre_wait_phase) cta_stamp(A.trace, 1);
+  if (u >= A.meta[0]) { cta_stamp(A.trace, 3); return; }
+  if (A.max_pairs > 0 && uniq_p0[u + 1] - uniq_p0[u] > A.max_pairs) { cta_stamp(A.trace, 3); return; }
   const int64_t e = uniq_e[u];
   if (A.pre_wait_phase && A.prefetch && threadIdx.x == 0) {
     // the route metadata was final before the previous kernel began
     prefetch_l2(A.q + (e * A.n_rows + nb) * (K >> 3), static_cast<int64_t>(ne - nb) * (K >> 1));
     prefetch_l2(A.sb + (e * A.n_rows + nb) * ngr, static_cast<int64_t>(ne - nb) * ngr * 4);
   }
-  if (A.pre_wait_phase) griddep_wait();
+  if (A.pre_wait_phase) { griddep_wait(); cta_stamp(A.trace, 1); }
   const int pa = uniq_p0[u], pe = uniq_p0[u + 1];
 
   // first row batch: issue its weight loads before staging the inputs, so
@@ -1344,12 +1367,15 @@ __global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(c
       }
     }
   }
+  cta_stamp(A.trace, 3);
 }
 
 static __global__ void __launch_bounds__(NT) k_combine(const __grid_constant__ CombineArgs A) {
   // the output projection's pre-wait phase reads only weights: let it launch now
+  cta_stamp(A.trace, 0);
   griddep_launch();
   griddep_wait();
+  cta_stamp(A.trace, 1);
   const int K = A.L + A.Fs;
   const int64_t n = static_cast<int64_t>(A.T) * K;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(NT) + threadIdx.x; i < n;
@@ -1369,6 +1395,7 @@ static __global__ void __launch_bounds__(NT) k_combine(const __grid_constant__ C
     }
     A.comb[i] = v;
   }
+  cta_stamp(A.trace, 3);
 }
 
 // ---------------------------------------------------------------------------

@@ -102,6 +102,9 @@ struct moe_layer {
   unsigned long long* fz_trace = nullptr;   // diagnostics (MOE_FUSED_TRACE): phase stamps
   unsigned long long* um_trace = nullptr;   // diagnostics (MOE_UMMA_TRACE): grouped GEMM role stamps
   int um_trace_n = 0;                       // grouped launches stamped in this forward
+  unsigned long long* ct_trace = nullptr;   // diagnostics (MOE_CTA_TRACE): gemv-path CTA stamps
+  int ct_n = 0;                             // launches stamped in this forward
+  const char* ct_names[CT_SLOTS] = {};
   int pdl_grouped = 1;    // programmatic dependent launch between the grouped-path kernels too
   int use_pdl = 1;        // programmatic dependent launch between the gemv-path kernels
   int expert_pb = 2;      // max token slots per pass of the gemv-path expert kernels
@@ -536,6 +539,11 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     MOE_TRY_CUDA(cudaMemsetAsync(L->fsync, 0, FZ_WORDS * FZ_SYNC_STRIDE * 4, s), "counter clear");
     if (want_trace)
       MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->fz_trace), 4096 * FZ_TRACE * 8), "trace");
+    if (std::getenv("MOE_CTA_TRACE") && std::atoi(std::getenv("MOE_CTA_TRACE"))) {
+      const size_t n = static_cast<size_t>(CT_SLOTS) * CT_MAX_CTAS * CT_STAMPS * 8;
+      MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->ct_trace), n), "trace");
+      MOE_TRY_CUDA(cudaMemsetAsync(L->ct_trace, 0, n, s), "trace");
+    }
     if (std::getenv("MOE_UMMA_TRACE") && std::atoi(std::getenv("MOE_UMMA_TRACE"))) {
       MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->um_trace), 4 * UM_TRACE_WORDS * 8), "trace");
       MOE_TRY_CUDA(cudaMemsetAsync(L->um_trace, 0, 4 * UM_TRACE_WORDS * 8, s), "trace");
@@ -834,6 +842,44 @@ static void print_umma_trace(moe_layer* h, cudaStream_t s) {
   }
 }
 
+// Diagnostics: per launch of the last forward, the CTA count and the min /
+// median / max over its CTAs of each stamp, in microseconds since the earliest
+// stamp of the forward (one JSON line per launch on stderr).
+static void print_cta_trace(moe_layer* h, cudaStream_t s) {
+  const size_t per = static_cast<size_t>(CT_MAX_CTAS) * CT_STAMPS;
+  std::vector<unsigned long long> t(per * CT_SLOTS);
+  const bool got = cudaMemcpyAsync(t.data(), h->ct_trace, t.size() * 8, cudaMemcpyDeviceToHost, s) == cudaSuccess &&
+                   cudaStreamSynchronize(s) == cudaSuccess;
+  cudaMemsetAsync(h->ct_trace, 0, t.size() * 8, s);
+  const int n = h->ct_n;
+  h->ct_n = 0;
+  if (!got) return;
+  unsigned long long t0 = ~0ull;
+  for (size_t i = 0; i < per * n; ++i)
+    if (t[i] && t[i] < t0) t0 = t[i];
+  for (int l = 0; l < n; ++l) {
+    std::string line = std::string("cta_trace {\"launch\": ") + std::to_string(l) + ", \"kernel\": \"" +
+                       h->ct_names[l] + "\"";
+    int ctas = 0;
+    for (int c = 0; c < CT_MAX_CTAS; ++c) ctas += t[l * per + static_cast<size_t>(c) * CT_STAMPS] != 0;
+    line += ", \"ctas\": " + std::to_string(ctas);
+    for (int k = 0; k < CT_STAMPS; ++k) {
+      std::vector<double> v;
+      for (int c = 0; c < CT_MAX_CTAS; ++c) {
+        const unsigned long long x = t[l * per + static_cast<size_t>(c) * CT_STAMPS + k];
+        if (x) v.push_back((static_cast<double>(x) - static_cast<double>(t0)) * 1e-3);
+      }
+      if (v.empty()) continue;
+      std::sort(v.begin(), v.end());
+      char buf[160];
+      std::snprintf(buf, sizeof(buf), ", \"s%d\": [%.2f, %.2f, %.2f, %.2f]", k, v.front(), v[v.size() / 10],
+                    v[v.size() / 2], v.back());
+      line += buf;
+    }
+    std::fprintf(stderr, "%s}\n", line.c_str());
+  }
+}
+
 // Diagnostics: per phase stamp, the min / median / max over CTAs of the time
 // since the earliest kernel start (microseconds).
 static void print_fused_trace(moe_layer* h, cudaStream_t s) {
@@ -916,6 +962,12 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
   cudaError_t e = cudaSuccess;
   auto mark = [&](int i) {
     if (h->profiling) cudaEventRecord(h->ev[i], s);
+  };
+  // diagnostics: the stamp buffer of the next launch (null unless MOE_CTA_TRACE)
+  auto tslot = [&](const char* name) -> unsigned long long* {
+    if (!h->ct_trace || h->ct_n >= CT_SLOTS) return nullptr;
+    h->ct_names[h->ct_n] = name;
+    return h->ct_trace + static_cast<size_t>(h->ct_n++) * CT_MAX_CTAS * CT_STAMPS;
   };
   auto seg1 = [&](DenseSeg* segs, int& ns, const void* w, int dt, int rows, int row0) {
     DenseSeg& S = segs[ns++];
@@ -1079,6 +1131,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
           di.pf_sb_bytes = static_cast<int64_t>(F) * (kin / c.group_size) * 4;
         }
       }
+      di.trace = tslot("k_dense_in");
       if ((e = launch_dense_in(di, tb_in, grid_in, s)) != cudaSuccess) goto cuda_fail;
       ++nl;
     }
@@ -1192,6 +1245,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
       up.max_pairs = split_experts ? pb_split : 0;
       up.cps = std::max(1, std::min(std::max(1, F / 8), (target + slots - 1) / slots));
       const int grid_up = slots * up.cps;
+      up.trace = tslot("k_expert_up");
       if ((e = launch_expert(up, pb_up, grid_up, s, pdl)) != cudaSuccess) goto cuda_fail;
       ++nl;
 
@@ -1261,6 +1315,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
       dn.pre_wait_phase = 1;
       dn.prefetch = (h->prefetch >> 1) & 1;
       dn.cps = std::max(1, std::min(std::max(1, kin / 8), (target + slots - 1) / slots));
+      dn.trace = tslot("k_expert_down");
       if ((e = launch_expert(dn, pb_dn, slots * dn.cps, s, pdl)) != cudaSuccess) goto cuda_fail;
       ++nl;
     }
@@ -1360,12 +1415,14 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
       ca.comb = h->comb;
       const int64_t n = static_cast<int64_t>(T) * kout;
       const int gc = static_cast<int>(std::min<int64_t>((n + NT - 1) / NT, h->num_sms * 4));
+      ca.trace = tslot("k_combine");
       if ((e = launch_ex<CombineArgs>(k_combine, gc, NT, 0, s, pdl, ca)) != cudaSuccess) goto cuda_fail;
       ++nl;
       dout.staged = h->comb;
     }
     const int tb_out = kout ? std::min(pow2_at_least(T, 8), dense_tb_cap(kout)) : pow2_at_least(T, 8);
     const int grid_out = std::max(1, std::min(h->num_sms * 2, (H + 3) / 4));
+    dout.trace = tslot("k_dense_out");
     if ((e = launch_dense_out(dout, tb_out, grid_out, s, pdl)) != cudaSuccess) goto cuda_fail;
     ++nl;
   }
@@ -1373,6 +1430,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
   if (h->profiling) h->profiled = true;
   h->last_launches = nl;
   if (h->um_trace) print_umma_trace(h, s);
+  if (h->ct_trace && h->ct_n) print_cta_trace(h, s);
   return MOE_OK;
 cuda_fail:
   h->last_error = std::string("launch failed: ") + cudaGetErrorString(e);

@@ -6,12 +6,13 @@
 // device memory up front, or code on a latency-critical path where a device
 // allocation (which may synchronise the device) is not acceptable.  Creating a
 // moe_layer handle allocates a workspace, so those callers use this entry
-// point instead: it runs the same router gemv and the same top-k selection as
-// moe_layer_forward_ex (kernel k_dense_in with the routing fused into its last
-// router CTA) and writes the same topk_ids / topk_w, but keeps its scratch --
-// the router logits, the distinct-expert lists and a completion counter -- in
-// a fixed-size array declared in this file.  The caller passes only inputs and
-// outputs.
+// point instead.  It runs the router gemv and the top-k selection rules of
+// moe_layer_forward_ex (the routing block fused into the last router CTA of
+// the dense gemv kernel, stopping after the ids and weights) and writes
+// topk_ids / topk_w, but keeps its scratch -- the router logits, a completion
+// counter and a status word -- in a fixed-size array declared in this file.
+// The caller passes only inputs and outputs (and, optionally, a device word
+// that receives the non-finite-key flag).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -26,19 +27,15 @@ using namespace moe;
 namespace {
 
 constexpr int NA_MAX_T = MOE_NOALLOC_MAX_TOKENS;
-constexpr int NA_MAX_P = NA_MAX_T * MAX_K;
-constexpr int NA_UMAX = MAX_E < NA_MAX_P ? MAX_E : NA_MAX_P;
-// word offsets inside the scratch array
+// word offsets inside the scratch array (the selection writes its ids and
+// weights straight to the caller's outputs and builds no expert lists)
 constexpr size_t NA_OFF_LOGITS = 0;                                          // fp32 [T, E]
-constexpr size_t NA_OFF_META = NA_OFF_LOGITS + static_cast<size_t>(NA_MAX_T) * MAX_E;
-constexpr size_t NA_OFF_IDS = NA_OFF_META + 2 + 2 * static_cast<size_t>(NA_UMAX) + NA_MAX_P;
-constexpr size_t NA_OFF_W = NA_OFF_IDS + NA_MAX_P;
-constexpr size_t NA_OFF_COUNTER = NA_OFF_W + NA_MAX_P;
+constexpr size_t NA_OFF_COUNTER = NA_OFF_LOGITS + static_cast<size_t>(NA_MAX_T) * MAX_E;
 constexpr size_t NA_OFF_STATUS = NA_OFF_COUNTER + 1;
-constexpr size_t NA_WORDS = NA_OFF_STATUS + 64;
+constexpr size_t NA_WORDS = NA_OFF_STATUS + 63;
 
 // The scratch.  Every GPU that loads the library holds it until the process
-// exits (~270 KB).  In host code this name is only a host-side stand-in, so
+// exits (256 KB).  In host code this name is only a host-side stand-in, so
 // its device address is looked up with cudaGetSymbolAddress (noalloc_setup).
 static __device__ __align__(256) uint32_t g_noalloc_scratch[NA_WORDS];
 
@@ -95,7 +92,8 @@ extern "C" moe_status moe_router_topk_noalloc(const void* x, int32_t T, int32_t 
                                               int32_t router_dtype, const float* router_bias,
                                               int32_t n_experts, int32_t top_k, int32_t router,
                                               int32_t renormalize, float routed_scale,
-                                              int32_t* topk_ids, float* topk_w, void* stream) {
+                                              int32_t* topk_ids, float* topk_w,
+                                              int32_t* key_status, void* stream) {
   if (!x || !router_w || !topk_ids || !topk_w || T < 1 || hidden < 64 || hidden % 64)
     return MOE_ERR_INVALID_ARG;
   if (x_dtype != MOE_DTYPE_BF16 && x_dtype != MOE_DTYPE_FP16) return MOE_ERR_INVALID_ARG;
@@ -115,10 +113,13 @@ extern "C" moe_status moe_router_topk_noalloc(const void* x, int32_t T, int32_t 
   if (st != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* counter = reinterpret_cast<int*>(scratch + NA_OFF_COUNTER);
-  int* status = reinterpret_cast<int*>(scratch + NA_OFF_STATUS);
+  // the status word: the caller's when given (an output, not scratch)
+  int* status = key_status ? key_status : reinterpret_cast<int*>(scratch + NA_OFF_STATUS);
   // the scratch keeps the last call's contents: the completion counter and the
   // status word must start at zero
-  if (cudaMemsetAsync(counter, 0, 2 * sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(counter, 0, sizeof(int), s) != cudaSuccess ||
+      cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess)
+    return MOE_ERR_CUDA;
 
   DenseInArgs di{};
   DenseSeg& S = di.seg[0];
@@ -145,20 +146,19 @@ extern "C" moe_status moe_router_topk_noalloc(const void* x, int32_t T, int32_t 
   ra.router = router;
   ra.renorm = renormalize;
   ra.scale = routed_scale;
-  ra.ids = reinterpret_cast<int*>(scratch + NA_OFF_IDS);
-  ra.w = reinterpret_cast<float*>(scratch + NA_OFF_W);
-  ra.meta = reinterpret_cast<int*>(scratch + NA_OFF_META);
-  ra.umax = NA_UMAX;
-  ra.ext_ids = topk_ids;
-  ra.ext_w = topk_w;
+  ra.ids = topk_ids;
+  ra.w = topk_w;
+  ra.meta = nullptr;
+  ra.umax = 0;
+  ra.ext_ids = nullptr;
+  ra.ext_w = nullptr;
   ra.status = status;
-  const int P = T * top_k;
-  ra.mask_words = P > 256 ? (T + 31) / 32 : 0;
+  ra.mask_words = 0;
+  ra.topk_only = 1;   // ids and weights only: no distinct-expert lists
   di.fuse_route = 1;
   di.route_counter = counter;
   di.route_ctas = grid;   // every CTA holds router rows
-  const size_t smem = std::max(na_dense_smem(tb, hidden),
-                               ROUTE_SMEM_BYTES + static_cast<size_t>(n_experts) * ra.mask_words * 4);
+  const size_t smem = std::max<size_t>(na_dense_smem(tb, hidden), ROUTE_SMEM_BYTES);
   switch (tb) {
     case 1: k_dense_in<1><<<grid, NT, smem, s>>>(di); break;
     case 2: k_dense_in<2><<<grid, NT, smem, s>>>(di); break;

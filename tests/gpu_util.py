@@ -14,8 +14,10 @@ import oracle
 # (out - x) so the residual cannot hide an error in the routed or shared part.
 REL_RMS = 1e-2
 MAX_ABS_FRAC = 3e-2
-# Routing weights: fp32 logits/sigmoid/normalisation against fp64; a few ulps
-# of fp32 on values of order 1 (see the tolerance derivation in the design notes).
+# Routing weights: fp32 against fp64.  The fp32 logit of an H-long dot product
+# carries a relative error of about sqrt(H) * 2^-24 (4e-6 of its scale at
+# H = 4096-6144); the sigmoid's slope is at most 1/4, and the normalisation
+# and the routed scale add a few fp32 ulps (1.2e-7 each) on weights of order 1.
 W_RTOL, W_ATOL = 1e-5, 1e-6
 MIN_MARGIN = 1e-3
 

@@ -164,6 +164,27 @@ def pin_route_closed_forms(ora):
         assert np.allclose(w, want, rtol=1e-13, atol=0), (case["name"], w, want)
 
 
+def pin_routing_margin(ora):
+    """The k-th minus the (k+1)-th selection key against hand-derived gaps: on
+    the key (score + bias for sigmoid routing, not the logit), with
+    non-finite keys ranked last, infinite when no (k+1)-th finite key exists."""
+    for case in _golden_routing()["margin_cases"]:
+        if "z_ln" in case:
+            z = np.array([math.log(float(Fraction(v))) for v in case["z_ln"]])
+        else:
+            z = np.array([float(v) for v in case["z"]])
+        spec = mi.LayerSpec(name="m", hidden=8, n_experts=len(z), top_k=case["k"],
+                            expert_ffn=8, group_size=8, router=case["router"],
+                            router_bias=case["bias"] is not None)
+        bias = None if case["bias"] is None else np.array(case["bias"])
+        got = ora.routing_margin(z, spec, bias)
+        if case["margin"] == "inf":
+            assert got == math.inf, (case["name"], got)
+        else:
+            want = float(Fraction(case["margin"]))
+            assert abs(got - want) <= 1e-12, (case["name"], got, want)
+
+
 def pin_weight_sums(ora):
     """Normalised weights sum to the routed scale; a full softmax sums to 1
     over all experts."""

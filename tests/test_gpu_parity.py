@@ -102,6 +102,14 @@ ODD = {
                                expert_ffn=128, latent=128, group_size=64, shared_ffn=0,
                                act="relu2", router="sigmoid", renormalize=True,
                                routed_scale=2.5, router_bias=True, weight_std=0.05),
+    # the non-latent fp16 sigmoid top-k layer's options at a small size: fp32 router
+    # without bias, SwiGLU (gate + up in one launch), fp16 activations, fp16 scales,
+    # group 32, fp16 shared expert
+    "odd_c3_like": mi.LayerSpec(name="odd_c3_like", hidden=768, n_experts=24, top_k=4,
+                                expert_ffn=256, latent=0, group_size=32, shared_ffn=256,
+                                act="swiglu", router="sigmoid", renormalize=True,
+                                routed_scale=1.0, act_dtype="fp16", scale_dtype="fp16",
+                                router_dtype="fp32", weight_std=0.05),
     # a single expert (k = E = 1): the dense MLP special case
     "odd_single": mi.LayerSpec(name="odd_single", hidden=256, n_experts=1, top_k=1,
                                expert_ffn=128, latent=0, group_size=64, shared_ffn=64,
@@ -136,9 +144,16 @@ def test_latent_parity(T):
 
 # --- non-latent fp16 sigmoid top-8 layer (H=6144, E=256) at full size ---------
 
-@pytest.mark.parametrize("T,rows", [(1, None), (4, [0, 3]), (32, [0, 31])])
+@pytest.mark.parametrize("T,rows", [(1, None), (4, [0, 3]), (32, [0, 17, 31])])
 def test_nonlatent_parity(T, rows):
-    _parity("nonlatent", T, rows=rows, max_tokens=32, paths=SMALL_T_PATHS)
+    """Every path AUTO or a forced schedule gives this layer at its configured
+    batch sizes; at 32 rows AUTO takes the grouped tcgen05 path (SwiGLU gate and
+    up in one GEMM launch, fp16 scale/bias of group 32)."""
+    paths = SMALL_T_PATHS + (("auto",) if T >= 16 else ())
+    if T >= 16:
+        lay, h = handle_for("nonlatent", 32)
+        assert h.path_for(T) == "grouped"
+    _parity("nonlatent", T, rows=rows, max_tokens=32, paths=paths)
 
 
 # --- batched decode rows with Zipf-skewed expert load -------------------------
@@ -182,7 +197,8 @@ GEMM_ENV = {"k_umma": {"MOE_UMMA_V": "1"},
 @pytest.mark.parametrize("gemm", list(GEMM_ENV))
 @pytest.mark.parametrize("name,T", [("tiny", 1), ("tiny", 16), ("tiny", 37), ("latent", 4),
                                     ("latent", 16), ("odd_latent_fp16", 12),
-                                    ("odd_relu2_noshared", 9)])
+                                    ("odd_relu2_noshared", 9), ("odd_c3_like", 1),
+                                    ("odd_c3_like", 20)])
 def test_grouped_path_parity(name, T, gemm, monkeypatch):
     """Every grouped GEMM variant on the tiny, latent and odd layers."""
     for k, v in GEMM_ENV[gemm].items():

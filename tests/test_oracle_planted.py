@@ -40,6 +40,14 @@ MUTANTS = [
     ("sigmoid sign", "return 1.0 / (1.0 + np.exp(-z))", "return 1.0 / (1.0 + np.exp(z))"),
     ("selection ignores the bias", "s = s + np.asarray(bias, dtype=np.float64)", "s = s"),
     ("last pick dropped", "for j in range(k):", "for j in range(k - 1):"),
+    ("margin one rank too low", "return float(srt[k - 1] - srt[k])", "return float(srt[k] - srt[k + 1])"),
+    ("margin one rank too high", "return float(srt[k - 1] - srt[k])", "return float(srt[k - 2] - srt[k - 1])"),
+    ("margin on the logits", "keys = selection_keys(z, spec, bias)\n    k = spec.top_k",
+     "keys = np.asarray(z, dtype=np.float64)\n    k = spec.top_k"),
+    ("margin ranks NaN first", "ranked = np.where(np.isfinite(keys), keys, -np.inf)",
+     "ranked = np.where(np.isnan(keys), np.inf, keys)"),
+    ("margin zero past the finite keys", "return math.inf if srt[k - 1] > -np.inf else 0.0",
+     "return 0.0"),
     ("shared gate/up swapped", "    h = activation(sp, u, g)\n    return widen(layer.sh_down, dt) @ h",
      "    h = activation(sp, g, u) if g is not None else activation(sp, u, g)\n"
      "    return widen(layer.sh_down, dt) @ h"),
