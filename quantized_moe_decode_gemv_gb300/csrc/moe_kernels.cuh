@@ -9,10 +9,14 @@
 //                of distinct selected experts with the rows routed to each
 //   k_expert     int4 affine dequant gemv over the distinct experts; used for
 //                the up(+gate) projection with the activation fused, and for
-//                the down projection
-//   k_dense_out  weighted combine of the expert outputs (fp32, pick order),
-//                fc2_latent_proj, shared-expert down gemv and the residual,
+//                the down projection with the weighted combine (fp32, pick
+//                order) fused into its last CTA per column range
+//   k_dense_out  fc2_latent_proj, shared-expert down gemv and the residual,
 //                rounded once to the activation dtype
+//
+// The shared expert does not depend on the routing: on its own stream its
+// gate/up rows (k_dense_in) and down rows (k_dense_out, fp32 output) run while
+// the routed chain runs, and the output kernel adds their result.
 //
 // Dense gemv design: a CTA owns a contiguous range of output rows (so every
 // CTA streams the same number of bytes), its 256 threads stride the reduction
@@ -177,22 +181,6 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&v)[NV], int lane) {
 }
 
 // ---------------------------------------------------------------------------
-// combine: the operand of the output projection, computed once per forward
-// ---------------------------------------------------------------------------
-
-// comb[t, :] = [ y_t = sum_j w[t, j] * pexp[t*k + j, :]  (latent layers; picks in
-//               order j = 0..k-1, fp32) | act(shared gate, shared up)[t, :] ]
-struct CombineArgs {
-  int T, L, Fs, k, act;
-  const float* pexp;      // [T*k, L]
-  const float* wts;       // [T*k]
-  const float* dense_in;  // [T, r_in]
-  int r_in, sh_g_off, sh_u_off;
-  float* comb;            // [T, L + Fs]
-  unsigned long long* trace;   // diagnostics: CTA stamps or null
-};
-
-// ---------------------------------------------------------------------------
 // routing arguments
 // ---------------------------------------------------------------------------
 
@@ -220,6 +208,9 @@ struct RouteArgs {
   int debug_times;       // print per-phase timestamps (diagnostics only)
   int topk_only;         // 1: ids and weights only (the lists come from k_route_lists)
   int rows_per_cta;      // k_route_rows: rows of one CTA (fewer rows: more warps per row)
+  int max_w;             // route_block: most warps sharing a row's keys (1..8)
+  int dry;               // 1: run the top-k code without writing anything (warms the
+                         // instruction cache and the bias lines before the logits exist)
 };
 
 __device__ __forceinline__ unsigned long long global_ns() {
@@ -229,13 +220,33 @@ __device__ __forceinline__ unsigned long long global_ns() {
 }
 
 // Diagnostics (MOE_CTA_TRACE): per-CTA global-timer stamps of a launch --
-// 0 entry, 1 past the wait for the previous kernel, 2 main loop done, 3 exit.
+// 0 entry, 1 past the wait for the previous kernel, 2 main loop done, 3 exit;
+// 4..15 kernel-specific intermediate points.
 constexpr int CT_MAX_CTAS = 2048;
-constexpr int CT_STAMPS = 4;
+constexpr int CT_STAMPS = 16;
 constexpr int CT_SLOTS = 12;   // launches stamped per forward
 __device__ __forceinline__ void cta_stamp(unsigned long long* t, int i) {
-  if (t != nullptr && threadIdx.x == 0 && blockIdx.x < CT_MAX_CTAS)
+  if (t != nullptr && threadIdx.x == 0 && blockIdx.x < CT_MAX_CTAS) {
     t[blockIdx.x * CT_STAMPS + i] = global_ns();
+    // the SM clock at entry and exit (slots 14, 15): cycles per ns of the CTA
+    if (i == 0 || i == 3) t[blockIdx.x * CT_STAMPS + (i == 0 ? 14 : 15)] = clock64();
+  }
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded spin of one thread until *p >= target (false when the bound ran out).
+constexpr uint32_t SPIN_LIMIT = 1u << 22;   // polls (~0.2 s with the sleeps)
+__device__ __forceinline__ bool spin_until_geq(const int* p, int target, uint32_t limit = SPIN_LIMIT) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    if (ld_acquire_gpu(p) >= target) return true;
+    __nanosleep(40);
+  }
+  return false;
 }
 
 __device__ __forceinline__ bool key_better(float a, int ia, float b, int ib) {
@@ -361,7 +372,7 @@ static __device__ __noinline__ void route_block(const RouteArgs& A, int* smem) {
   int* cand_i = reinterpret_cast<int*>(cand_k + 32 * MAX_K);
   float* cand_s = reinterpret_cast<float*>(cand_i + 32 * MAX_K);
   int W = E > 16 * 32 ? 2 : 1;            // at most 16 keys per lane
-  while (W < 8 && A.T * W * 2 <= nwarp) W *= 2;
+  while (W < A.max_w && A.T * W * 2 <= nwarp) W *= 2;
   const int npl = (E + 32 * W - 1) / (32 * W);
   const int rows_per_pass = nwarp / W;
   for (int tb = 0; tb < A.T; tb += rows_per_pass) {
@@ -380,7 +391,7 @@ static __device__ __noinline__ void route_block(const RouteArgs& A, int* smem) {
       else if (npl <= 4) route_member<4>(A, z, W, g, lane, my_id, my_z, ck, ci, cs, bad);
       else if (npl <= 8) route_member<8>(A, z, W, g, lane, my_id, my_z, ck, ci, cs, bad);
       else route_member<16>(A, z, W, g, lane, my_id, my_z, ck, ci, cs, bad);
-      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(A.status, STATUS_NONFINITE);
+      if (__any_sync(0xffffffffu, bad) && lane == 0 && !A.dry) atomicOr(A.status, STATUS_NONFINITE);
     }
     if (W > 1) {
       __syncthreads();
@@ -435,7 +446,7 @@ static __device__ __noinline__ void route_block(const RouteArgs& A, int* smem) {
         }
       }
       wv *= A.scale;
-      if (lane < k) {
+      if (lane < k && !A.dry) {
         A.ids[t * k + lane] = my_id;
         A.w[t * k + lane] = wv;
         if (A.ext_ids) A.ext_ids[t * k + lane] = my_id;
@@ -472,9 +483,11 @@ static __device__ __noinline__ void route_block(const RouteArgs& A, int* smem) {
       int* uniq_e = A.meta + 1;
       int* uniq_p0 = A.meta + 1 + A.umax;
       int* pairs = A.meta + 2 + 2 * A.umax;
-      if (open) { uniq_e[u] = v >> 5; uniq_p0[u] = lane; }
-      if (valid) pairs[lane] = v & 31;
-      if (lane == 0) { A.meta[0] = __popc(om); uniq_p0[__popc(om)] = P; }
+      if (!A.dry) {
+        if (open) { uniq_e[u] = v >> 5; uniq_p0[u] = lane; }
+        if (valid) pairs[lane] = v & 31;
+        if (lane == 0) { A.meta[0] = __popc(om); uniq_p0[__popc(om)] = P; }
+      }
     }
     if (A.debug_times && tid == 0)
       printf("route phases (ns): topk %llu list %llu\n", tp[1] - tp[0], global_ns() - tp[1]);
@@ -733,6 +746,11 @@ struct DenseInArgs {
   int fuse_route;
   int route_ctas;    // CTAs whose row range meets the router rows [0, E)
   int* route_counter;
+  int route_warm;    // 1: CTA 0 holds no rows; it warms the top-k code with a dry
+                     // run, waits (bounded) for CTAs 1..route_ctas to write the
+                     // router rows, then routes
+  int debug_stall;   // tests only: CTA 0 waits for one router CTA more than exist
+                     // (the bounded wait runs out and reports a timeout)
   RouteArgs route;
   // after routing, prefetch the distinct experts' up(+gate) weights into L2
   int prefetch_up;
@@ -740,32 +758,42 @@ struct DenseInArgs {
   const uint32_t* pf_q; const uint32_t* pf_sb; const uint32_t* pf_q2; const uint32_t* pf_sb2;
   int64_t pf_q_bytes, pf_sb_bytes;   // per expert
   unsigned long long* trace;   // diagnostics: CTA stamps or null
+  int dep_tail;      // 1: rows that need nothing from the previous kernel: let the
+                     // next kernel launch at once, run without waiting, and wait
+                     // for the previous kernel only before exiting (so that this
+                     // launch completes after it, and a kernel waiting on this
+                     // one also waits on that one)
 };
 
 struct DenseOutArgs {
   DenseSeg seg[1];
   int nseg;
   int total_rows;    // hidden
-  int K;             // staged vector length: (latent) + shared_ffn
-  // staging sources
-  int latent;        // L (0: non-latent)
-  int shared;        // shared_ffn
-  int k;             // top_k
-  const float* pexp; // [T*k, Kin] unweighted expert outputs
-  const float* wts;  // [T*k] combine weights
-  const float* dense_in;  // [T, R_in]
+  int K;             // staged vector length: latent + shared
+  // staged vector [y (latent columns) | shared activation]
+  int latent;        // L: columns [0, L) come from `staged` (0: none)
+  int shared;        // shared_ffn columns computed from dense_in (0: none)
+  const float* staged;  // [T, staged_ld] combined routed output y (latent layers)
+  int staged_ld;
+  const float* dense_in;  // [T, r_in]
   int r_in;          // dense_in row stride
   int sh_g_off, sh_u_off; // column offsets of shared gate/up logits in dense_in
   int act;
-  // epilogue
+  // epilogue: s = dot + y_add + add_f32, then out = x + s (or out_f32 = s)
+  const float* y_add;  // [T, total_rows] combined routed output (non-latent layers) or null
+  const float* pexp;   // or, when y_add is null: unweighted per-pick outputs [T*k, total_rows]
+  const float* wts;    // and their weights [T*k], combined here in pick order (or null)
+  int k;
+  const float* add_f32;  // [T, total_rows] e.g. the shared expert's output or null
+  float* out_f32;    // [T, total_rows]: write s here and nothing else (null: residual output)
   const void* x;     // [T, H] residual, act dtype
   int x_dt;
   void* out;         // [T, H] act dtype
   float* delta;      // [T, H] fp32 or null
   int T;
   int prefetch;      // prefetch this CTA's weight rows into L2 before waiting
-  const float* staged;  // [T, K] fp32 staged vector computed once (k_combine), or null
   unsigned long long* trace;   // diagnostics: CTA stamps or null
+  int dep_tail;      // as DenseInArgs::dep_tail (its inputs are complete when it launches)
 };
 
 // Rows of the dense weights per register batch: every thread keeps partial sums
@@ -957,32 +985,13 @@ __device__ __forceinline__ void cta_rows(int rows, int& b, int& e) {
 template <int TB>
 constexpr int dense_min_blocks() { return 2; }
 
+// Rows [rb, re) of the dense matrices that read x, for all T token rows
+// (staged TB at a time): out[t, r] = W_r . x_t in fp32.
 template <int TB>
-__global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_in(const __grid_constant__ DenseInArgs A) {
-  extern __shared__ float4 smem4[];
+__device__ __forceinline__ void dense_in_rows(const DenseInArgs& A, int rb, int re, float4* smem4) {
   float* xs = reinterpret_cast<float*>(smem4);
   float* red = xs + TB * A.K;
   const int K4 = A.K >> 2;
-  cta_stamp(A.trace, 0);
-  griddep_wait();
-  griddep_launch();
-  cta_stamp(A.trace, 1);
-  int rb, re;
-  if (A.fuse_route) {
-    // the first route_ctas CTAs take the router rows [0, E) (fewer rows each,
-    // so the routing starts early and overlaps the rest of the pass)
-    const int E = A.route.E, rc = A.route_ctas, c = blockIdx.x, g = gridDim.x;
-    if (c < rc) {
-      rb = static_cast<int>(static_cast<int64_t>(c) * E / rc);
-      re = static_cast<int>(static_cast<int64_t>(c + 1) * E / rc);
-    } else {
-      const int64_t rest = A.total_rows - E;
-      rb = E + static_cast<int>(static_cast<int64_t>(c - rc) * rest / (g - rc));
-      re = E + static_cast<int>(static_cast<int64_t>(c - rc + 1) * rest / (g - rc));
-    }
-  } else {
-    cta_rows(A.total_rows, rb, re);
-  }
   for (int t0 = 0; t0 < A.T; t0 += TB) {
     const int tb = min(TB, A.T - t0);
     if (t0) __syncthreads();
@@ -1005,8 +1014,83 @@ __global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_in(const _
       __syncthreads();
     }
   }
+}
+
+template <int TB>
+__global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_in(const __grid_constant__ DenseInArgs A) {
+  extern __shared__ float4 smem4[];
+  cta_stamp(A.trace, 0);
+  if (!A.dep_tail) griddep_wait();
+  griddep_launch();
+  cta_stamp(A.trace, 1);
+  int rb, re;
+  if (A.fuse_route && A.route_warm) {
+    // CTA 0 routes and holds no rows; CTAs 1..route_ctas take the router rows
+    const int E = A.route.E, rc = A.route_ctas, c = blockIdx.x, g = gridDim.x;
+    if (c == 0) {
+      rb = re = 0;
+    } else if (c <= rc) {
+      rb = static_cast<int>(static_cast<int64_t>(c - 1) * E / rc);
+      re = static_cast<int>(static_cast<int64_t>(c) * E / rc);
+    } else {
+      const int64_t rest = A.total_rows - E;
+      rb = E + static_cast<int>(static_cast<int64_t>(c - 1 - rc) * rest / (g - 1 - rc));
+      re = E + static_cast<int>(static_cast<int64_t>(c - rc) * rest / (g - 1 - rc));
+    }
+  } else if (A.fuse_route) {
+    // the first route_ctas CTAs take the router rows [0, E) (fewer rows each,
+    // so the routing starts early and overlaps the rest of the pass)
+    const int E = A.route.E, rc = A.route_ctas, c = blockIdx.x, g = gridDim.x;
+    if (c < rc) {
+      rb = static_cast<int>(static_cast<int64_t>(c) * E / rc);
+      re = static_cast<int>(static_cast<int64_t>(c + 1) * E / rc);
+    } else {
+      const int64_t rest = A.total_rows - E;
+      rb = E + static_cast<int>(static_cast<int64_t>(c - rc) * rest / (g - rc));
+      re = E + static_cast<int>(static_cast<int64_t>(c - rc + 1) * rest / (g - rc));
+    }
+  } else {
+    cta_rows(A.total_rows, rb, re);
+  }
+  dense_in_rows<TB>(A, rb, re, smem4);
   cta_stamp(A.trace, 2);
-  if (A.fuse_route && static_cast<int>(blockIdx.x) < A.route_ctas) {
+  if (A.fuse_route && A.route_warm) {
+    if (blockIdx.x == 0) {
+      // first execution of the top-k code is slow (instruction fetch from a
+      // cold L2 while the other CTAs stream weights): run it once on whatever
+      // the logits buffer holds, writing nothing, while the router rows are
+      // being computed
+      RouteArgs D = A.route;
+      D.dry = 1;
+      // the few-pairs list code (a warp's sort of the ids as they stand) runs
+      // dry too; the counting path indexes shared memory by id, so not that
+      D.topk_only = D.T * D.k > 32;
+      route_block(D, reinterpret_cast<int*>(smem4));
+      cta_stamp(A.trace, 4);
+      __shared__ int s_ok;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const bool ok = spin_until_geq(A.route_counter, A.route_ctas + (A.debug_stall ? 1 : 0));
+        if (!ok) atomicOr(A.route.status, STATUS_TIMEOUT);
+        s_ok = ok;
+        __threadfence();
+      }
+      __syncthreads();
+      cta_stamp(A.trace, 5);
+      // on a timeout the routing still runs (on the logits as they stand), so
+      // that the ids and lists stay well formed; the status reports it
+      route_block(A.route, reinterpret_cast<int*>(smem4));
+      cta_stamp(A.trace, 6);
+      __syncthreads();
+      if (threadIdx.x == 0) *A.route_counter = 0;
+      (void)s_ok;
+    } else if (static_cast<int>(blockIdx.x) <= A.route_ctas) {
+      // release this CTA's router logits to the routing CTA
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) atomicAdd(A.route_counter, 1);
+    }
+  } else if (A.fuse_route && static_cast<int>(blockIdx.x) < A.route_ctas) {
     // the last CTA to finish router rows routes all T rows
     __shared__ int s_last;
     __threadfence();
@@ -1035,31 +1119,18 @@ __global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_in(const _
       }
     }
   }
+  if (A.dep_tail) griddep_wait();
   cta_stamp(A.trace, 3);
 }
 
+// Output rows [rb, re) of the output projection for all T token rows (staged
+// TB at a time): s = [fc2 | shared down] . [y | act(shared gate, up)] plus the
+// routed and shared terms given, then out = x + s rounded once (or s in fp32).
 template <int TB>
-__global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_out(const __grid_constant__ DenseOutArgs A) {
-  extern __shared__ float4 smem4[];
-  float* xs = reinterpret_cast<float*>(smem4);
-  float* red = xs + TB * A.K;
+__device__ __forceinline__ void dense_out_rows(const DenseOutArgs& A, int rb, int re, float4* smem4) {
+  float* red = reinterpret_cast<float*>(smem4) + TB * A.K;
   const int K4 = A.K >> 2;
   const int L = A.latent;
-  const int Kin = L ? L : A.total_rows;
-  int rb, re;
-  cta_stamp(A.trace, 0);
-  cta_rows(A.total_rows, rb, re);
-  // the weights do not depend on this forward's earlier kernels: start them
-  // towards L2 while those finish
-  if (A.prefetch && A.nseg && threadIdx.x < A.seg[0].nparts && re > rb) {
-    const DensePart& P = A.seg[0].part[threadIdx.x];
-    const int esz = P.dt == DT_FP32 ? 4 : 2;
-    prefetch_l2(static_cast<const char*>(P.w) + static_cast<int64_t>(rb) * P.wk * esz,
-                static_cast<int64_t>(re - rb) * P.wk * esz);
-  }
-  griddep_wait();
-  griddep_launch();
-  cta_stamp(A.trace, 1);
   for (int t0 = 0; t0 < A.T; t0 += TB) {
     const int tb = min(TB, A.T - t0);
     if (t0) __syncthreads();
@@ -1067,31 +1138,25 @@ __global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_out(const 
     auto stage_body = [&]() {
       for (int i = threadIdx.x; i < TB * K4; i += NT) {
         const int t = i / K4, f4 = i - t * K4;
-        float v[4] = {0.f, 0.f, 0.f, 0.f};
-        if (t < tb && A.staged) {
-          const float4 a = reinterpret_cast<const float4*>(A.staged)[static_cast<int64_t>(t0 + t) * K4 + f4];
-          v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        } else if (t < tb) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < tb) {
           const int tt = t0 + t;
+          if (4 * f4 < L) {
+            v = __ldcg(reinterpret_cast<const float4*>(A.staged + static_cast<int64_t>(tt) * A.staged_ld) + f4);
+          } else {
+            const float* di = A.dense_in + static_cast<int64_t>(tt) * A.r_in;
+            float r[4];
   #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int kk = 4 * f4 + j;
-            if (kk < L) {
-              float y = 0.f;
-              for (int p = 0; p < A.k; ++p)
-                y = fmaf(A.wts[tt * A.k + p],
-                         A.pexp[static_cast<int64_t>(tt * A.k + p) * Kin + kk], y);
-              v[j] = y;
-            } else {
-              const int f = kk - L;
-              const float* di = A.dense_in + static_cast<int64_t>(tt) * A.r_in;
-              const float u = di[A.sh_u_off + f];
-              const float g = (A.act == ACT_SWIGLU) ? di[A.sh_g_off + f] : 0.f;
-              v[j] = act_fn(A.act, g, u);
+            for (int j = 0; j < 4; ++j) {
+              const int f = 4 * f4 + j - L;
+              const float u = __ldcg(di + A.sh_u_off + f);
+              const float g = (A.act == ACT_SWIGLU) ? __ldcg(di + A.sh_g_off + f) : 0.f;
+              r[j] = act_fn(A.act, g, u);
             }
+            v = make_float4(r[0], r[1], r[2], r[3]);
           }
         }
-        smem4[t * K4 + swz(f4, 1)] = make_float4(v[0], v[1], v[2], v[3]);
+        smem4[t * K4 + swz(f4, 1)] = v;
       }
     };
     for (int r0 = rb; r0 < re; r0 += RED_ROWS) {
@@ -1111,13 +1176,20 @@ __global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_out(const 
 #pragma unroll
           for (int w = 0; w < NW; ++w) s += red[o * NW + w];
         }
-        if (!L) {  // non-latent: routed output is added directly
+        const int64_t e = static_cast<int64_t>(tt) * A.total_rows + n;
+        if (A.y_add) {
+          s += __ldcg(A.y_add + e);                  // non-latent: routed output added directly
+        } else if (A.pexp) {
           float y = 0.f;
           for (int p = 0; p < A.k; ++p)
-            y = fmaf(A.wts[tt * A.k + p], A.pexp[static_cast<int64_t>(tt * A.k + p) * Kin + n], y);
+            y = fmaf(A.wts[tt * A.k + p], A.pexp[static_cast<int64_t>(tt * A.k + p) * A.total_rows + n], y);
           s += y;
         }
-        const int64_t e = static_cast<int64_t>(tt) * A.total_rows + n;
+        if (A.add_f32) s += __ldcg(A.add_f32 + e);   // the shared expert's output
+        if (A.out_f32) {
+          A.out_f32[e] = s;
+          continue;
+        }
         const float xv = ld16(A.x, e, A.x_dt);
         reinterpret_cast<unsigned short*>(A.out)[e] = st16_bits(xv + s, A.x_dt);
         if (A.delta) A.delta[e] = s;
@@ -1125,6 +1197,27 @@ __global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_out(const 
       __syncthreads();
     }
   }
+}
+
+template <int TB>
+__global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_out(const __grid_constant__ DenseOutArgs A) {
+  extern __shared__ float4 smem4[];
+  int rb, re;
+  cta_stamp(A.trace, 0);
+  cta_rows(A.total_rows, rb, re);
+  // the weights do not depend on this forward's earlier kernels: start them
+  // towards L2 while those finish
+  if (A.prefetch && A.nseg && threadIdx.x < A.seg[0].nparts && re > rb) {
+    const DensePart& P = A.seg[0].part[threadIdx.x];
+    const int esz = P.dt == DT_FP32 ? 4 : 2;
+    prefetch_l2(static_cast<const char*>(P.w) + static_cast<int64_t>(rb) * P.wk * esz,
+                static_cast<int64_t>(re - rb) * P.wk * esz);
+  }
+  if (!A.dep_tail) griddep_wait();
+  griddep_launch();
+  cta_stamp(A.trace, 1);
+  dense_out_rows<TB>(A, rb, re, smem4);
+  if (A.dep_tail) griddep_wait();
   cta_stamp(A.trace, 3);
 }
 
@@ -1163,6 +1256,16 @@ struct ExpertArgs {
   int prefetch;            // prefetch this CTA's weight rows into L2 (pre-wait phase)
   int cps;                 // CTAs per distinct-expert slot (grid = umax * cps)
   int max_pairs;           // > 0: slots with more token pairs are left to the grouped GEMM
+  // weighted combine fused into the down projection: the last CTA to finish a
+  // column range [nb, ne) (over all distinct experts) writes
+  // comb[t, n] = sum_j w[t, j] * out[t*k + j, n], picks in order j = 0..k-1
+  float* comb;             // [T, n_rows] or null
+  const float* cwts;       // [T*k] combine weights
+  int* ccnt;               // [cps] completion counters (zero between launches)
+  int T;
+  int nst;                 // k_expert_bulk: shared-memory stages of the tile ring
+  int* status;             // k_expert_bulk: device status word (timeout bit)
+  int gsh;                 // k_expert_bulk: log2(G) - 5 (chunk c lies in group c >> gsh)
   unsigned long long* trace;   // diagnostics: CTA stamps or null
 };
 
@@ -1367,33 +1470,27 @@ __global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(c
       }
     }
   }
-  cta_stamp(A.trace, 3);
-}
-
-static __global__ void __launch_bounds__(NT) k_combine(const __grid_constant__ CombineArgs A) {
-  // the output projection's pre-wait phase reads only weights: let it launch now
-  cta_stamp(A.trace, 0);
-  griddep_launch();
-  griddep_wait();
-  cta_stamp(A.trace, 1);
-  const int K = A.L + A.Fs;
-  const int64_t n = static_cast<int64_t>(A.T) * K;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(NT) + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * NT) {
-    const int t = static_cast<int>(i / K), c = static_cast<int>(i - static_cast<int64_t>(t) * K);
-    float v;
-    if (c < A.L) {
-      v = 0.f;
-      for (int p = 0; p < A.k; ++p)
-        v = fmaf(A.wts[t * A.k + p], A.pexp[static_cast<int64_t>(t * A.k + p) * A.L + c], v);
-    } else {
-      const float* di = A.dense_in + static_cast<int64_t>(t) * A.r_in;
-      const int f = c - A.L;
-      const float u = di[A.sh_u_off + f];
-      const float g = (A.act == ACT_SWIGLU) ? di[A.sh_g_off + f] : 0.f;
-      v = act_fn(A.act, g, u);
+  cta_stamp(A.trace, 2);
+  if (A.comb) {
+    // every CTA of this column range counts itself done; the last one combines
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(A.ccnt + part, 1) == A.meta[0] - 1;
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      const int cols = ne - nb;
+      for (int i = threadIdx.x; i < A.T * cols; i += NT) {
+        const int t = i / cols, n = nb + (i - t * cols);
+        float y = 0.f;
+        for (int p = 0; p < A.k; ++p)
+          y = fmaf(__ldcg(A.cwts + t * A.k + p),
+                   __ldcg(A.out + static_cast<int64_t>(t * A.k + p) * A.n_rows + n), y);
+        A.comb[static_cast<int64_t>(t) * A.n_rows + n] = y;
+      }
+      if (threadIdx.x == 0) A.ccnt[part] = 0;
     }
-    A.comb[i] = v;
   }
   cta_stamp(A.trace, 3);
 }

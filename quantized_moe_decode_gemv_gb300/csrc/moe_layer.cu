@@ -13,6 +13,8 @@
 
 #include "moe_layer.h"
 #include "moe_kernels.cuh"
+#include "moe_expert_bulk.cuh"
+#include "moe_dense_bulk.cuh"
 #include "moe_umma.cuh"
 #include "moe_umma2.cuh"
 #include "moe_fused.cuh"
@@ -22,6 +24,7 @@ using namespace moe;
 namespace {
 
 constexpr int kSmemMax = 227 * 1024;
+constexpr int kCombineCounters = 4096;   // column ranges of the down projection's fused combine
 
 std::atomic<int64_t> g_live_allocs{0};
 std::atomic<int32_t> g_fail_countdown{0};
@@ -90,7 +93,6 @@ struct moe_layer {
   int umax = 0;
   int kin = 0;
   int grouped_min_t = 16;
-  int combine_min_t = 1;  // gemv path: the combine as its own kernel from this T
   int expert_split = 0;   // AUTO's grouped path: light experts on the int4 gemv kernel
   int fused_max_t = 0;    // AUTO: the persistent kernel for T <= this (below grouped_min_t)
   int fused_sd_pre = 60;  // persistent kernel: percent of a CTA's shared-down rows before the experts,
@@ -125,7 +127,20 @@ struct moe_layer {
   int umma_tma = 1;           // grouped path (k_umma2): A operand by tensor copies when the layout allows
   int umma_ntile_int4 = 128;  // grouped path: max tokens per MMA tile with int4 (dequantised) A
   int fuse_route = 1;     // routing in the last router CTA of the dense pass (0: own kernel)
+  int route_warm = 1;     // fused routing: a dedicated CTA warms the top-k code, then waits
+  int route_max_w = 8;    // routing block: most warps sharing a row's keys
   int debug_route = 0;    // diagnostics: print routing phase times
+  int expert_bulk = 1;    // gemv path: expert kernels with bulk-copied weight tiles (k_expert_bulk)
+  int expert_bulk_max_t = 2;   // the bulk expert kernel up to this many rows
+  int dense_bulk = 1;     // gemv path: shared expert and output projection by k_dense_bulk
+  int fill = 0;           // gemv path: the shared expert as launches of its own beside the routed chain
+  int fill_ctas = 0;      // those CTAs per launch (0: one per SM)
+  int side_stream = 0;    // gemv path: the shared expert on its own stream beside the routed chain
+  int side_grid = 0;      // CTAs of the shared expert's launches (0: one per SM)
+  cudaStream_t hi_s = nullptr;   // the routed chain (highest priority)
+  cudaStream_t lo_s = nullptr;   // the shared expert (lowest priority)
+  cudaEvent_t ev_fork = nullptr, ev_side = nullptr, ev_chain = nullptr;
+  int* ccnt = nullptr;    // completion counters of the down projection's fused combine
   int prefetch = 6;       // bit 0: experts' up weights from the routing CTA (one SM's
                           // bulk engine: slow, off by default); bit 1: down weights;
                           // bit 2: output-projection weights
@@ -149,8 +164,19 @@ struct moe_layer {
       e = nullptr;
     }
   }
+  void free_streams() {
+    for (cudaEvent_t* e : {&ev_fork, &ev_side, &ev_chain}) {
+      if (*e) cudaEventDestroy(*e);
+      *e = nullptr;
+    }
+    for (cudaStream_t* st : {&hi_s, &lo_s}) {
+      if (*st) cudaStreamDestroy(*st);
+      *st = nullptr;
+    }
+  }
   void free_all() {
     free_events();
+    free_streams();
     for (void* p : allocs) {
       cudaFree(p);
       g_live_allocs.fetch_sub(1);
@@ -285,6 +311,209 @@ static cudaError_t launch_expert_t(const ExpertArgs& a, int grid, cudaStream_t s
   return launch_ex<ExpertArgs>(k_expert<PB, false>, grid, NT, smem, s, pdl, a);
 }
 
+// The gemv path's expert kernel with bulk-copied weight groups: token pairs
+// per pass, rows per warp per group, ring stages, CTAs per SM and dynamic
+// shared memory of one launch.
+struct EbLaunch {
+  int pb = 0, r = 0, nst = 0, per_sm = 0;
+  size_t smem = 0;
+};
+
+// Largest pass of token pairs (up to pb_max); then two CTAs per SM before one;
+// then groups of 8 rows per warp over the pass's pairs (R x PB = 8) before
+// groups of one row per warp.  The ring holds a CTA's row groups, up to
+// EB_MAX_STAGES, and at least two when the CTA has more than one (so that
+// copies overlap the arithmetic).  `cps` is the CTAs per distinct expert of the
+// chosen plan.  False when no plan fits shared memory (the caller falls back
+// to k_expert).
+static bool eb_choose(int K, int G, bool gated, int pb_max, int n_rows, int slots, int num_sms, EbLaunch* o,
+                      int* cps_out) {
+  for (int pb = pb_max; pb >= 1; pb >>= 1) {
+    for (int per_sm = 2; per_sm >= 1; --per_sm) {
+      const int rs[2] = {8 / pb, 1};
+      for (int ri = 0; ri < (rs[0] > 1 ? 2 : 1); ++ri) {
+        const int budget = (per_sm == 2 ? kSmemMax / 2 : kSmemMax) - 2048;
+        const EbPlan p = eb_plan(K, G, pb, rs[ri], gated);
+        const int cps = std::max(1, std::min(std::max(1, n_rows / 8), num_sms * per_sm / std::max(1, slots)));
+        const int rows = (n_rows + cps - 1) / cps;
+        const int groups = (rows + EB_WARPS * rs[ri] - 1) / (EB_WARPS * rs[ri]);
+        const int nst = std::min(std::min(EB_MAX_STAGES, groups), (budget - p.x_bytes) / (p.st_bytes + 8));
+        if (nst >= std::min(groups, 2)) {
+          o->pb = pb;
+          o->r = rs[ri];
+          o->nst = nst;
+          o->per_sm = per_sm;
+          o->smem = static_cast<size_t>(p.x_bytes) + static_cast<size_t>(nst) * (p.st_bytes + 8);
+          *cps_out = cps;
+          return true;
+        }
+      }
+    }
+  }
+  return false;
+}
+
+// The bulk-copy dense gemv (one or two token rows): token rows per launch, input
+// chunks per lane, ring stages, grid and dynamic shared memory.
+struct DbLaunch {
+  int tb = 0, cpl = 0, nst = 0, grid = 0, stage_bytes = 0;
+  size_t smem = 0;
+};
+
+// A plan when every segment has the same 16-bit parts and the reduction width
+// fits three chunks per lane; token rows in passes of two (one when T = 1);
+// two CTAs per SM when their rings fit.
+static bool db_choose(const DenseSeg* segs, int nseg, int total_rows, int T, int num_sms, DbLaunch* o) {
+  if (nseg < 1 || total_rows < 1) return false;
+  const DenseSeg& S0 = segs[0];
+  int K = 0;
+  for (int p = 0; p < S0.nparts; ++p) {
+    if (S0.part[p].dt == DT_FP32 || S0.part[p].wk % 8 || S0.part[p].k0 != K) return false;
+    if (reinterpret_cast<uintptr_t>(S0.part[p].w) % 16) return false;
+    K += S0.part[p].wk;
+  }
+  for (int si = 1; si < nseg; ++si) {
+    if (segs[si].nparts != S0.nparts) return false;
+    for (int p = 0; p < S0.nparts; ++p)
+      if (segs[si].part[p].wk != S0.part[p].wk || segs[si].part[p].dt != S0.part[p].dt ||
+          reinterpret_cast<uintptr_t>(segs[si].part[p].w) % 16)
+        return false;
+  }
+  const int cpl = (K / 8 + NT - 1) / NT;
+  if (cpl > DB_MAX_CPL) return false;
+  const int tb = T == 1 ? 1 : 2;
+  const int stage_bytes = (DB_SR * K * 2 + 127) & ~127;
+  const int fixed = DB_SR * tb * NW * 4 + DB_MAX_STAGES * 8 + 128;
+  for (int per_sm = 2; per_sm >= 1; --per_sm) {
+    const int budget = (per_sm == 2 ? kSmemMax / 2 : kSmemMax) - 2048;
+    const int grid = std::min(num_sms * per_sm, (total_rows + DB_SR - 1) / DB_SR);
+    const int rows = (total_rows + grid - 1) / grid;
+    const int nstage = (rows + DB_SR - 1) / DB_SR * ((T + tb - 1) / tb);   // over all passes
+    const int nst = std::min(std::min(DB_MAX_STAGES, nstage), (budget - fixed) / stage_bytes);
+    if (nst >= std::min(2, nstage) && nst >= 1) {
+      o->tb = tb;
+      o->cpl = cpl;
+      o->nst = nst;
+      o->grid = grid;
+      o->stage_bytes = stage_bytes;
+      o->smem = static_cast<size_t>(nst) * stage_bytes + fixed;
+      return true;
+    }
+  }
+  return false;
+}
+
+template <int TB, int CPL>
+static cudaError_t launch_dense_bulk_t(const DbArgs& a, const DbLaunch& d, cudaStream_t s, bool pdl) {
+  return launch_ex<DbArgs>(k_dense_bulk<TB, CPL>, d.grid, NT, d.smem, s, pdl, a);
+}
+static cudaError_t launch_dense_bulk(DbArgs a, const DbLaunch& d, cudaStream_t s, bool pdl) {
+  a.nst = d.nst;
+  a.stage_bytes = d.stage_bytes;
+  if (d.tb == 1) {
+    if (d.cpl == 1) return launch_dense_bulk_t<1, 1>(a, d, s, pdl);
+    if (d.cpl == 2) return launch_dense_bulk_t<1, 2>(a, d, s, pdl);
+    return launch_dense_bulk_t<1, 3>(a, d, s, pdl);
+  }
+  if (d.cpl == 1) return launch_dense_bulk_t<2, 1>(a, d, s, pdl);
+  if (d.cpl == 2) return launch_dense_bulk_t<2, 2>(a, d, s, pdl);
+  return launch_dense_bulk_t<2, 3>(a, d, s, pdl);
+}
+
+// The bulk dense gemv over a DenseInArgs' rows (input x; fp32 rows out).
+static DbArgs db_from_in(const DenseInArgs& a, float* out, int64_t out_ld, int out_col0, int* status) {
+  DbArgs d{};
+  for (int i = 0; i < a.nseg; ++i) d.seg[i] = a.seg[i];
+  d.nseg = a.nseg;
+  d.total_rows = a.total_rows;
+  d.K = a.K;
+  d.T = a.T;
+  d.src = DB_SRC_X;
+  d.x = a.x;
+  d.x_dt = a.x_dt;
+  d.epi = DB_EPI_F32;
+  d.out = out;
+  d.out_ld = out_ld;
+  d.out_col0 = out_col0;
+  d.status = status;
+  d.dep_tail = a.dep_tail;
+  return d;
+}
+
+// The bulk dense gemv over a DenseOutArgs' rows (input [y | act(shared)]).
+static DbArgs db_from_out(const DenseOutArgs& a, int* status) {
+  DbArgs d{};
+  d.seg[0] = a.seg[0];
+  d.nseg = a.nseg;
+  d.total_rows = a.total_rows;
+  d.K = a.K;
+  d.T = a.T;
+  d.src = DB_SRC_OUT;
+  d.staged = a.staged;
+  d.staged_ld = a.staged_ld;
+  d.latent = a.latent;
+  d.dense_in = a.dense_in;
+  d.r_in = a.r_in;
+  d.sh_g_off = a.sh_g_off;
+  d.sh_u_off = a.sh_u_off;
+  d.act = a.act;
+  if (a.out_f32) {
+    d.epi = DB_EPI_F32;
+    d.out = a.out_f32;
+    d.out_ld = a.total_rows;
+    d.out_col0 = 0;
+  } else {
+    d.epi = DB_EPI_OUT;
+    d.y_add = a.y_add;
+    d.add_f32 = a.add_f32;
+    d.xres = a.x;
+    d.x_dt = a.x_dt;
+    d.outb = a.out;
+    d.delta = a.delta;
+  }
+  d.status = status;
+  d.dep_tail = a.dep_tail;
+  return d;
+}
+
+template <int PB, int R>
+static cudaError_t launch_expert_bulk_t(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl) {
+  if (a.q_gate) return launch_ex<ExpertArgs>(k_expert_bulk<PB, R, true>, grid, NT, smem, s, pdl, a);
+  return launch_ex<ExpertArgs>(k_expert_bulk<PB, R, false>, grid, NT, smem, s, pdl, a);
+}
+static cudaError_t launch_expert_bulk(const ExpertArgs& a, const EbLaunch& eb, int grid, cudaStream_t s,
+                                      bool pdl) {
+  const size_t m = eb.smem;
+  if (eb.r == 1) {
+    switch (eb.pb) {
+      case 1: return launch_expert_bulk_t<1, 1>(a, grid, m, s, pdl);
+      case 2: return launch_expert_bulk_t<2, 1>(a, grid, m, s, pdl);
+      case 4: return launch_expert_bulk_t<4, 1>(a, grid, m, s, pdl);
+      default: return launch_expert_bulk_t<8, 1>(a, grid, m, s, pdl);
+    }
+  }
+  switch (eb.pb) {
+    case 1: return launch_expert_bulk_t<1, 8>(a, grid, m, s, pdl);
+    case 2: return launch_expert_bulk_t<2, 4>(a, grid, m, s, pdl);
+    case 4: return launch_expert_bulk_t<4, 2>(a, grid, m, s, pdl);
+    default: return launch_expert_bulk_t<8, 1>(a, grid, m, s, pdl);
+  }
+}
+
+template <int TB>
+static cudaError_t launch_dense_in_pdl_t(const DenseInArgs& a, int grid, cudaStream_t s) {
+  return launch_ex<DenseInArgs>(k_dense_in<TB>, grid, NT, dense_smem<TB>(a.K), s, true, a);
+}
+// A dense_in launch (no fused routing) that may start before its predecessor ends.
+static cudaError_t launch_dense_in_pdl(const DenseInArgs& a, int tb, int grid, cudaStream_t s) {
+  switch (tb) {
+    case 1: return launch_dense_in_pdl_t<1>(a, grid, s);
+    case 2: return launch_dense_in_pdl_t<2>(a, grid, s);
+    case 4: return launch_dense_in_pdl_t<4>(a, grid, s);
+    default: return launch_dense_in_pdl_t<8>(a, grid, s);
+  }
+}
+
 static cudaError_t launch_dense_in(const DenseInArgs& a, int tb, int grid, cudaStream_t s) {
   switch (tb) {
     case 1: return launch_dense_in_t<DenseInArgs, 1>(a, grid, s);
@@ -334,6 +563,16 @@ static cudaError_t set_smem_attrs() {
   MOE_SMEM_ATTR((k_expert<4, false>)) MOE_SMEM_ATTR((k_expert<8, false>))
   MOE_SMEM_ATTR((k_expert<1, true>)) MOE_SMEM_ATTR((k_expert<2, true>))
   MOE_SMEM_ATTR((k_expert<4, true>)) MOE_SMEM_ATTR((k_expert<8, true>))
+  MOE_SMEM_ATTR((k_expert_bulk<1, 8, false>)) MOE_SMEM_ATTR((k_expert_bulk<2, 4, false>))
+  MOE_SMEM_ATTR((k_expert_bulk<4, 2, false>)) MOE_SMEM_ATTR((k_expert_bulk<8, 1, false>))
+  MOE_SMEM_ATTR((k_expert_bulk<1, 1, false>)) MOE_SMEM_ATTR((k_expert_bulk<2, 1, false>))
+  MOE_SMEM_ATTR((k_expert_bulk<4, 1, false>))
+  MOE_SMEM_ATTR((k_expert_bulk<1, 8, true>)) MOE_SMEM_ATTR((k_expert_bulk<2, 4, true>))
+  MOE_SMEM_ATTR((k_expert_bulk<4, 2, true>)) MOE_SMEM_ATTR((k_expert_bulk<8, 1, true>))
+  MOE_SMEM_ATTR((k_expert_bulk<1, 1, true>)) MOE_SMEM_ATTR((k_expert_bulk<2, 1, true>))
+  MOE_SMEM_ATTR((k_expert_bulk<4, 1, true>))
+  MOE_SMEM_ATTR((k_dense_bulk<1, 1>)) MOE_SMEM_ATTR((k_dense_bulk<1, 2>)) MOE_SMEM_ATTR((k_dense_bulk<1, 3>))
+  MOE_SMEM_ATTR((k_dense_bulk<2, 1>)) MOE_SMEM_ATTR((k_dense_bulk<2, 2>)) MOE_SMEM_ATTR((k_dense_bulk<2, 3>))
   MOE_SMEM_ATTR(k_umma) MOE_SMEM_ATTR(k_umma2) MOE_SMEM_ATTR(k_route) MOE_SMEM_ATTR(k_route_rows)
 #undef MOE_SMEM_ATTR
   return e;
@@ -412,7 +651,6 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   L->r_in = L->off_shu + Fs;
   L->umax = std::min(E, T * k);
   if (const char* env = std::getenv("MOE_GROUPED_MIN_T")) L->grouped_min_t = std::max(1, std::atoi(env));
-  if (const char* env = std::getenv("MOE_COMBINE_MIN_T")) L->combine_min_t = std::max(1, std::atoi(env));
   if (const char* env = std::getenv("MOE_EXPERT_SPLIT")) L->expert_split = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_PDL")) L->use_pdl = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_PDL_GROUPED")) L->pdl_grouped = std::atoi(env) != 0;
@@ -440,6 +678,15 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   if (const char* env = std::getenv("MOE_UMMA_NTILE"))
     L->umma_ntile_int4 = std::max(16, std::min(128, std::atoi(env))) & ~15;
   if (const char* env = std::getenv("MOE_FUSE_ROUTE")) L->fuse_route = std::atoi(env) != 0;
+  if (const char* env = std::getenv("MOE_SIDE_STREAM")) L->side_stream = std::atoi(env) != 0;
+  if (const char* env = std::getenv("MOE_EXPERT_BULK")) L->expert_bulk = std::atoi(env) != 0;
+  if (const char* env = std::getenv("MOE_DENSE_BULK")) L->dense_bulk = std::atoi(env) != 0;
+  if (const char* env = std::getenv("MOE_EXPERT_BULK_MAX_T")) L->expert_bulk_max_t = std::max(0, std::atoi(env));
+  if (const char* env = std::getenv("MOE_FILL")) L->fill = std::atoi(env) != 0;
+  if (const char* env = std::getenv("MOE_FILL_CTAS")) L->fill_ctas = std::max(0, std::atoi(env));
+  if (const char* env = std::getenv("MOE_ROUTE_WARM")) L->route_warm = std::atoi(env) != 0;
+  if (const char* env = std::getenv("MOE_ROUTE_MAXW")) L->route_max_w = std::max(1, std::min(8, std::atoi(env)));
+  if (const char* env = std::getenv("MOE_SIDE_GRID")) L->side_grid = std::max(0, std::atoi(env));
   if (const char* env = std::getenv("MOE_DEBUG_ROUTE")) L->debug_route = std::atoi(env) != 0;
   {
     const size_t adt = dt_size(c.act_dtype), rdt = dt_size(c.router_dtype);
@@ -523,7 +770,8 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->route_counter), 4), "workspace");
     MOE_TRY_CUDA(cudaMemsetAsync(L->route_counter, 0, 4, s), "counter clear");
     MOE_TRY_CUDA(L->alloc(&L->bout, static_cast<size_t>(T) * (Lt + Fs + 64) * 2), "workspace");
-    MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->comb), static_cast<size_t>(T) * (Lt + Fs + 64) * 4), "workspace");
+    MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->comb),
+                          static_cast<size_t>(T) * (std::max(kin, Lt + Fs) + 64) * 4), "workspace");
     MOE_TRY_CUDA(L->alloc(&L->xl16, static_cast<size_t>(T) * (Lt + 64) * 2), "workspace");
     MOE_TRY_CUDA(L->alloc(&L->h16, P * F * 2), "workspace");
     if (T >= L->gather_min_t) MOE_TRY_CUDA(L->alloc(&L->xs, P * L->kin * 2), "workspace");
@@ -549,6 +797,18 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
       MOE_TRY_CUDA(cudaMemsetAsync(L->um_trace, 0, 4 * UM_TRACE_WORDS * 8, s), "trace");
     }
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->sdbuf), static_cast<size_t>(T) * H * 4), "workspace");
+    MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->ccnt), kCombineCounters * 4), "workspace");
+    MOE_TRY_CUDA(cudaMemsetAsync(L->ccnt, 0, kCombineCounters * 4, s), "counter clear");
+    if (Fs && L->side_stream) {
+      // the routed chain and the shared expert each on a stream of their own,
+      // forked from and joined back into the caller's stream every forward
+      int least = 0, greatest = 0;
+      MOE_TRY_CUDA(cudaDeviceGetStreamPriorityRange(&least, &greatest), "stream priorities");
+      MOE_TRY_CUDA(cudaStreamCreateWithPriority(&L->hi_s, cudaStreamNonBlocking, greatest), "stream");
+      MOE_TRY_CUDA(cudaStreamCreateWithPriority(&L->lo_s, cudaStreamNonBlocking, least), "stream");
+      for (cudaEvent_t* ev : {&L->ev_fork, &L->ev_side, &L->ev_chain})
+        MOE_TRY_CUDA(cudaEventCreateWithFlags(ev, cudaEventDisableTiming), "event");
+    }
     MOE_TRY_CUDA(L->alloc(&L->x_stage, static_cast<size_t>(T) * H * adt), "workspace");
     MOE_TRY_CUDA(L->alloc(&L->out_stage, static_cast<size_t>(T) * H * adt), "workspace");
     MOE_TRY_CUDA(cudaStreamSynchronize(s), "create synchronise");
@@ -856,14 +1116,28 @@ static void print_cta_trace(moe_layer* h, cudaStream_t s) {
   if (!got) return;
   unsigned long long t0 = ~0ull;
   for (size_t i = 0; i < per * n; ++i)
-    if (t[i] && t[i] < t0) t0 = t[i];
+    if (t[i] && t[i] < t0 && (i % CT_STAMPS) < 14) t0 = t[i];
   for (int l = 0; l < n; ++l) {
     std::string line = std::string("cta_trace {\"launch\": ") + std::to_string(l) + ", \"kernel\": \"" +
                        h->ct_names[l] + "\"";
     int ctas = 0;
     for (int c = 0; c < CT_MAX_CTAS; ++c) ctas += t[l * per + static_cast<size_t>(c) * CT_STAMPS] != 0;
     line += ", \"ctas\": " + std::to_string(ctas);
-    for (int k = 0; k < CT_STAMPS; ++k) {
+    {
+      // SM clock of the launch: clock64 cycles over globaltimer ns, entry to exit
+      std::vector<double> mhz;
+      for (int c = 0; c < CT_MAX_CTAS; ++c) {
+        const unsigned long long* r = t.data() + l * per + static_cast<size_t>(c) * CT_STAMPS;
+        if (r[0] && r[3] > r[0] + 1000 && r[15] > r[14]) mhz.push_back(1e3 * (r[15] - r[14]) / double(r[3] - r[0]));
+      }
+      if (!mhz.empty()) {
+        std::sort(mhz.begin(), mhz.end());
+        char buf[64];
+        std::snprintf(buf, sizeof(buf), ", \"sm_mhz\": %.0f", mhz[mhz.size() / 2]);
+        line += buf;
+      }
+    }
+    for (int k = 0; k < 14; ++k) {
       std::vector<double> v;
       for (int c = 0; c < CT_MAX_CTAS; ++c) {
         const unsigned long long x = t[l * per + static_cast<size_t>(c) * CT_STAMPS + k];
@@ -876,7 +1150,15 @@ static void print_cta_trace(moe_layer* h, cudaStream_t s) {
                     v[v.size() / 2], v.back());
       line += buf;
     }
-    std::fprintf(stderr, "%s}\n", line.c_str());
+    line += ", \"cta0\": [";
+    for (int k = 0; k < 14; ++k) {
+      const unsigned long long x = t[l * per + k];
+      char buf[32];
+      std::snprintf(buf, sizeof(buf), "%s%.2f", k ? ", " : "",
+                    x ? (static_cast<double>(x) - static_cast<double>(t0)) * 1e-3 : -1.0);
+      line += buf;
+    }
+    std::fprintf(stderr, "%s]}\n", line.c_str());
   }
 }
 
@@ -995,6 +1277,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
   ra.ext_w = ext_w;
   ra.status = h->status;
   ra.debug_times = h->debug_route;
+  ra.max_w = h->route_max_w;
   {
     const int P = T * k;
     const int W = (T + 31) / 32;
@@ -1084,6 +1367,88 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
   const bool big_route = T > h->route_small_t;
   const bool fuse_route = !grouped && h->fuse_route && !big_route;
   const bool pdl = h->use_pdl && (!grouped || h->pdl_grouped) && !h->profiling;
+  // The shared expert does not depend on the routing.  On the gemv path its
+  // gate/up rows (sa) and down rows (so, fp32 output added by the output
+  // kernel) leave the routed chain (router and fc1 rows, top-k, expert up,
+  // expert down with the combine): either as CTAs of their own inside the
+  // expert launches (fill: sa beside the up projection, so beside the down
+  // projection), or on a stream of their own (side).  Not while profiling: the
+  // per-stage events time the kernels one after the other.
+  DenseInArgs sa{};
+  DenseOutArgs so{};
+  if (Fs) {
+    int ns = 0;
+    if (gated) seg1(sa.seg, ns, h->sh_gate, c.act_dtype, Fs, 0);
+    seg1(sa.seg, ns, h->sh_up, c.act_dtype, Fs, gated ? Fs : 0);
+    sa.nseg = ns;
+    sa.total_rows = ns * Fs;
+    sa.out_ld = h->r_in;
+    sa.K = H;
+    sa.x = x;
+    sa.x_dt = c.act_dtype;
+    sa.out = h->dense_in + h->off_shg;
+    sa.T = T;
+    so.seg[0].part[0] = DensePart{h->sh_down, c.act_dtype, 0, Fs};
+    so.seg[0].nparts = 1;
+    so.seg[0].row0 = 0;
+    so.seg[0].rows = H;
+    so.nseg = 1;
+    so.total_rows = H;
+    so.K = Fs;
+    so.shared = Fs;
+    so.dense_in = h->dense_in;
+    so.r_in = h->r_in;
+    so.sh_g_off = h->off_shg;
+    so.sh_u_off = h->off_shu;
+    so.act = c.act;
+    so.out_f32 = h->sdbuf;
+    so.x = x;
+    so.x_dt = c.act_dtype;
+    so.T = T;
+    so.prefetch = (h->prefetch >> 2) & 1;
+  }
+  // expert kernels of the gemv path: bulk-copied weight groups for up to
+  // expert_bulk_max_t rows (latency-bound: every CTA's bytes requested at once),
+  // register-streamed k_expert above (both give the same bits for a row)
+  const bool use_bulk = h->expert_bulk && !grouped && T <= h->expert_bulk_max_t;
+  EbLaunch eb_up, eb_dn;
+  int cps_up = 1, cps_dn = 1;
+  const int slots_e = std::min(E, T * k);   // distinct-expert slots of the expert launches
+  const bool bulk_up = use_bulk && eb_choose(kin, c.group_size, gated, pow2_at_least(T, 8), F, slots_e,
+                                             h->num_sms, &eb_up, &cps_up);
+  const bool bulk_dn = use_bulk && eb_choose(F, c.group_size, false, pow2_at_least(T, 8), kin, slots_e,
+                                             h->num_sms, &eb_dn, &cps_dn);
+  // the filler CTAs stage PB token rows of the dense rows' input: their shared
+  // memory must fit beside the plan's CTAs per SM
+  // fill: the shared expert's gate/up rows as a launch right after the first
+  // kernel and its down rows right after the down projection, each starting
+  // without a wait (its inputs are complete when it launches) beside the routed
+  // chain's latency-bound kernels, and waiting for its predecessor only at its
+  // end so that the stream's dependencies still run through it
+  const bool fill = !grouped && Fs > 0 && h->fill && !h->profiling && h->use_pdl;
+  const bool side = !grouped && !fill && Fs > 0 && h->side_stream && h->hi_s && !h->profiling;
+  const bool shared_apart = side || fill;   // the shared expert is not in the first and last kernels
+  const int fill_ctas = h->fill_ctas > 0 ? h->fill_ctas : h->num_sms;
+  cudaStream_t cs = s;   // the routed chain's stream
+  if (side) {
+    if ((e = cudaEventRecord(h->ev_fork, s)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(h->hi_s, h->ev_fork, 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(h->lo_s, h->ev_fork, 0)) != cudaSuccess)
+      goto cuda_fail;
+    cs = h->hi_s;
+    const int sgrid = h->side_grid > 0 ? h->side_grid : h->num_sms;
+    sa.trace = tslot("k_dense_in_shared");
+    if ((e = launch_dense_in(sa, std::min(pow2_at_least(T, 8), dense_tb_cap(H)),
+                             std::max(1, std::min(sgrid, (sa.total_rows + 3) / 4)), h->lo_s)) != cudaSuccess)
+      goto cuda_fail;
+    ++nl;
+    so.trace = tslot("k_dense_out_shared");
+    if ((e = launch_dense_out(so, std::min(pow2_at_least(T, 8), dense_tb_cap(Fs)),
+                              std::max(1, std::min(sgrid, (H + 3) / 4)), h->lo_s, false)) != cudaSuccess)
+      goto cuda_fail;
+    ++nl;
+    if ((e = cudaEventRecord(h->ev_side, h->lo_s)) != cudaSuccess) goto cuda_fail;
+  }
 
   // 1. dense matrices that read x: router, fc1_latent_proj, shared gate/up
   mark(0);
@@ -1097,11 +1462,11 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
       seg1(di.seg, ns, h->router_w, c.router_dtype, E, 0);
       if (!grouped) {
         if (Lt) seg1(di.seg, ns, h->fc1, c.act_dtype, Lt, h->off_fc1);
-        if (Fs && gated) seg1(di.seg, ns, h->sh_gate, c.act_dtype, Fs, h->off_shg);
-        if (Fs) seg1(di.seg, ns, h->sh_up, c.act_dtype, Fs, h->off_shu);
+        if (Fs && gated && !shared_apart) seg1(di.seg, ns, h->sh_gate, c.act_dtype, Fs, h->off_shg);
+        if (Fs && !shared_apart) seg1(di.seg, ns, h->sh_up, c.act_dtype, Fs, h->off_shu);
       }
       di.nseg = ns;
-      di.total_rows = grouped ? E : h->r_in;
+      di.total_rows = grouped ? E : (shared_apart ? E + Lt : h->r_in);
       di.out_ld = h->r_in;
       di.K = H;
       di.x = x;
@@ -1109,7 +1474,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
       di.out = h->dense_in;
       di.T = T;
       const int tb_in = std::min(pow2_at_least(T, 8), dense_tb_cap(H));
-      const int grid_in = std::max(1, std::min(h->num_sms * 2, (di.total_rows + 3) / 4));
+      int grid_in = std::max(1, std::min(h->num_sms * 2, (di.total_rows + 3) / 4));
       if (fuse_route) {
         di.fuse_route = 1;
         di.route = ra;
@@ -1117,8 +1482,20 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
         // router rows get half the average rows per CTA
         const double share = static_cast<double>(E) / di.total_rows;
         int rc = static_cast<int>(grid_in * share * 2.0 + 0.5);
-        rc = std::max(1, std::min(rc, std::min(E, grid_in - 1)));
-        if (grid_in < 2) rc = 1;
+        if (h->route_warm) {
+          // CTA 0 routes; CTAs 1..rc take the router rows, the rest the others
+          const int rest = di.total_rows - E;
+          grid_in = std::max(grid_in, rest ? 3 : 2);
+          rc = rest ? std::max(1, std::min(rc, grid_in - 2)) : grid_in - 1;
+          di.route_warm = 1;
+          // MOE_DEBUG_STALL (tests of failure detection, read at every launch):
+          // the routing CTA's bounded wait runs out
+          const char* stall = std::getenv("MOE_DEBUG_STALL");
+          di.debug_stall = stall && std::atoi(stall) ? 1 : 0;
+        } else {
+          rc = std::max(1, std::min(rc, std::min(E, grid_in - 1)));
+          if (grid_in < 2) rc = 1;
+        }
         di.route_ctas = rc;
         if (h->prefetch & 1) {
           di.prefetch_up = 1;
@@ -1132,8 +1509,23 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
         }
       }
       di.trace = tslot("k_dense_in");
-      if ((e = launch_dense_in(di, tb_in, grid_in, s)) != cudaSuccess) goto cuda_fail;
+      if ((e = launch_dense_in(di, tb_in, grid_in, cs)) != cudaSuccess) goto cuda_fail;
       ++nl;
+      if (fill) {
+        sa.dep_tail = 1;
+        DbLaunch dl;
+        if (h->dense_bulk && db_choose(sa.seg, sa.nseg, sa.total_rows, T, h->num_sms, &dl)) {
+          DbArgs d = db_from_in(sa, h->dense_in, h->r_in, h->off_shg, h->status);
+          d.trace = tslot("k_dense_bulk_shared_in");
+          if ((e = launch_dense_bulk(d, dl, cs, true)) != cudaSuccess) goto cuda_fail;
+        } else {
+          sa.trace = tslot("k_dense_in_shared");
+          if ((e = launch_dense_in_pdl(sa, std::min(pow2_at_least(T, 8), dense_tb_cap(H)),
+                                       std::max(1, std::min(fill_ctas, (sa.total_rows + 3) / 4)), cs)) != cudaSuccess)
+            goto cuda_fail;
+        }
+        ++nl;
+      }
     }
     if (grouped) {
       UmmaArgs ua{};
@@ -1179,7 +1571,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     // few rows per CTA while the grid stays small: four warps share a row's keys
     rr.rows_per_cta = T <= h->route_rpc_max_t ? h->route_rpc : ROUTE_ROWS_PER_CTA;
     if ((e = launch_ex<RouteArgs>(k_route_rows, (T + rr.rows_per_cta - 1) / rr.rows_per_cta,
-                                  ROUTE_THREADS, ROUTE_SMEM_BYTES, s, pdl, rr)) != cudaSuccess)
+                                  ROUTE_THREADS, ROUTE_SMEM_BYTES, cs, pdl, rr)) != cudaSuccess)
       goto cuda_fail;
     ++nl;
     ListArgs la{};
@@ -1192,12 +1584,12 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     la.mask = h->rmask;
     la.pref = h->rpref;
     la.W = (T + 31) / 32;
-    if ((e = launch_ex<ListArgs>(k_route_lists, 1, LIST_THREADS, 0, s, pdl, la)) != cudaSuccess)
+    if ((e = launch_ex<ListArgs>(k_route_lists, 1, LIST_THREADS, 0, cs, pdl, la)) != cudaSuccess)
       goto cuda_fail;
     ++nl;
   } else if (!fuse_route) {
     if ((e = launch_ex<RouteArgs>(k_route, 1, ROUTE_THREADS,
-                                  ROUTE_SMEM_BYTES + static_cast<size_t>(E) * ra.mask_words * 4, s,
+                                  ROUTE_SMEM_BYTES + static_cast<size_t>(E) * ra.mask_words * 4, cs,
                                   pdl, ra)) != cudaSuccess)
       goto cuda_fail;
     ++nl;
@@ -1243,10 +1635,21 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
       up.pre_wait_phase = 0;
       up.prefetch = 0;
       up.max_pairs = split_experts ? pb_split : 0;
-      up.cps = std::max(1, std::min(std::max(1, F / 8), (target + slots - 1) / slots));
-      const int grid_up = slots * up.cps;
-      up.trace = tslot("k_expert_up");
-      if ((e = launch_expert(up, pb_up, grid_up, s, pdl)) != cudaSuccess) goto cuda_fail;
+      up.status = h->status;
+      up.gsh = c.group_size == 32 ? 0 : (c.group_size == 64 ? 1 : 2);
+      if (bulk_up) {
+        // one wave: at most per_sm CTAs on every SM (one when the filler CTAs
+        // take the other slot)
+        up.cps = cps_up;
+        up.nst = eb_up.nst;
+        up.trace = tslot("k_expert_bulk_up");
+        if ((e = launch_expert_bulk(up, eb_up, slots * up.cps, cs, pdl)) != cudaSuccess) goto cuda_fail;
+      } else {
+        up.cps = std::max(1, std::min(std::max(1, F / 8), (target + slots - 1) / slots));
+        const int grid_up = slots * up.cps;
+        up.trace = tslot("k_expert_up");
+        if ((e = launch_expert(up, pb_up, grid_up, cs, pdl)) != cudaSuccess) goto cuda_fail;
+      }
       ++nl;
 
     }
@@ -1314,9 +1717,39 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
       dn.out = h->pexp;
       dn.pre_wait_phase = 1;
       dn.prefetch = (h->prefetch >> 1) & 1;
-      dn.cps = std::max(1, std::min(std::max(1, kin / 8), (target + slots - 1) / slots));
-      dn.trace = tslot("k_expert_down");
-      if ((e = launch_expert(dn, pb_dn, slots * dn.cps, s, pdl)) != cudaSuccess) goto cuda_fail;
+      if (!grouped) {
+        // the weighted combine in the last CTA of each column range
+        dn.comb = h->comb;
+        dn.cwts = h->wts;
+        dn.ccnt = h->ccnt;
+        dn.T = T;
+      }
+      if (bulk_dn) {
+        dn.cps = std::min(cps_dn, kCombineCounters);
+        dn.nst = eb_dn.nst;
+        dn.trace = tslot("k_expert_bulk_down");
+        if ((e = launch_expert_bulk(dn, eb_dn, slots * dn.cps, cs, pdl)) != cudaSuccess) goto cuda_fail;
+      } else {
+        dn.cps = std::max(1, std::min(std::min(std::max(1, kin / 8), kCombineCounters),
+                                      (target + slots - 1) / slots));
+        dn.trace = tslot("k_expert_down");
+        if ((e = launch_expert(dn, pb_dn, slots * dn.cps, cs, pdl)) != cudaSuccess) goto cuda_fail;
+      }
+      if (fill) {
+        so.dep_tail = 1;
+        DbLaunch dl;
+        if (h->dense_bulk && db_choose(so.seg, so.nseg, so.total_rows, T, h->num_sms, &dl)) {
+          DbArgs d = db_from_out(so, h->status);
+          d.trace = tslot("k_dense_bulk_shared_down");
+          if ((e = launch_dense_bulk(d, dl, cs, true)) != cudaSuccess) goto cuda_fail;
+        } else {
+          so.trace = tslot("k_dense_out_shared");
+          if ((e = launch_dense_out(so, std::min(pow2_at_least(T, 8), dense_tb_cap(Fs)),
+                                    std::max(1, std::min(fill_ctas, (H + 3) / 4)), cs, true)) != cudaSuccess)
+            goto cuda_fail;
+        }
+        ++nl;
+      }
       ++nl;
     }
     if (experts_tc) {
@@ -1376,55 +1809,61 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     ua.status = h->status;
     if ((e = launch_umma(h, ua, T, s, &nl, pdl)) != cudaSuccess) goto cuda_fail;
   } else {
+    // the shared expert's output (side stream) is ready before the output kernel
+    if (side && (e = cudaStreamWaitEvent(cs, h->ev_side, 0)) != cudaSuccess) goto cuda_fail;
     DenseOutArgs dout{};
+    const int ks = Lt + (shared_apart ? 0 : Fs);   // staged width: [y (latent) | shared activation]
     dout.nseg = 0;
-    if (kout) {
+    if (ks) {
       DenseSeg& S = dout.seg[0];
       S.nparts = 0;
       if (Lt) S.part[S.nparts++] = DensePart{h->fc2, c.act_dtype, 0, Lt};
-      if (Fs) S.part[S.nparts++] = DensePart{h->sh_down, c.act_dtype, Lt, Fs};
+      if (Fs && !shared_apart) S.part[S.nparts++] = DensePart{h->sh_down, c.act_dtype, Lt, Fs};
       S.row0 = 0;
       S.rows = H;
       dout.nseg = 1;
     }
     dout.total_rows = H;
-    dout.K = kout;
+    dout.K = ks;
     dout.latent = Lt;
-    dout.shared = Fs;
-    dout.k = k;
-    dout.pexp = h->pexp;
-    dout.wts = h->wts;
+    dout.shared = shared_apart ? 0 : Fs;
+    dout.staged = h->comb;          // y [T, kin] from the down projection's combine
+    dout.staged_ld = kin;
     dout.dense_in = h->dense_in;
     dout.r_in = h->r_in;
     dout.sh_g_off = h->off_shg;
     dout.sh_u_off = h->off_shu;
     dout.act = c.act;
+    if (grouped) {
+      // grouped path without output projection: the experts wrote per-pick rows
+      dout.pexp = h->pexp;
+      dout.wts = h->wts;
+      dout.k = k;
+    } else {
+      dout.y_add = Lt ? nullptr : h->comb;
+    }
+    dout.add_f32 = shared_apart ? h->sdbuf : nullptr;
     dout.x = x;
     dout.x_dt = c.act_dtype;
     dout.out = out;
     dout.delta = delta;
     dout.T = T;
     dout.prefetch = (h->prefetch >> 2) & 1;
-    if (kout && T >= h->combine_min_t) {
-      // the output projection's operand once per forward; below combine_min_t
-      // rows every dense_out CTA stages it itself (one launch fewer)
-      CombineArgs ca{};
-      ca.T = T; ca.L = Lt; ca.Fs = Fs; ca.k = k; ca.act = c.act;
-      ca.pexp = h->pexp; ca.wts = h->wts; ca.dense_in = h->dense_in; ca.r_in = h->r_in;
-      ca.sh_g_off = h->off_shg; ca.sh_u_off = h->off_shu;
-      ca.comb = h->comb;
-      const int64_t n = static_cast<int64_t>(T) * kout;
-      const int gc = static_cast<int>(std::min<int64_t>((n + NT - 1) / NT, h->num_sms * 4));
-      ca.trace = tslot("k_combine");
-      if ((e = launch_ex<CombineArgs>(k_combine, gc, NT, 0, s, pdl, ca)) != cudaSuccess) goto cuda_fail;
-      ++nl;
-      dout.staged = h->comb;
-    }
-    const int tb_out = kout ? std::min(pow2_at_least(T, 8), dense_tb_cap(kout)) : pow2_at_least(T, 8);
+    const int tb_out = ks ? std::min(pow2_at_least(T, 8), dense_tb_cap(ks)) : pow2_at_least(T, 8);
     const int grid_out = std::max(1, std::min(h->num_sms * 2, (H + 3) / 4));
-    dout.trace = tslot("k_dense_out");
-    if ((e = launch_dense_out(dout, tb_out, grid_out, s, pdl)) != cudaSuccess) goto cuda_fail;
+    DbLaunch dl;
+    if (h->dense_bulk && !grouped && ks && db_choose(dout.seg, dout.nseg, H, T, h->num_sms, &dl)) {
+      DbArgs d = db_from_out(dout, h->status);
+      d.trace = tslot("k_dense_bulk_out");
+      if ((e = launch_dense_bulk(d, dl, cs, pdl && !side)) != cudaSuccess) goto cuda_fail;
+    } else {
+      dout.trace = tslot("k_dense_out");
+      if ((e = launch_dense_out(dout, tb_out, grid_out, cs, pdl && !side)) != cudaSuccess) goto cuda_fail;
+    }
     ++nl;
+    if (side && ((e = cudaEventRecord(h->ev_chain, cs)) != cudaSuccess ||
+                 (e = cudaStreamWaitEvent(s, h->ev_chain, 0)) != cudaSuccess))
+      goto cuda_fail;
   }
   mark(5);
   if (h->profiling) h->profiled = true;

@@ -155,6 +155,7 @@ extern "C" moe_status moe_router_topk_noalloc(const void* x, int32_t T, int32_t 
   ra.status = status;
   ra.mask_words = 0;
   ra.topk_only = 1;   // ids and weights only: no distinct-expert lists
+  ra.max_w = 8;
   di.fuse_route = 1;
   di.route_counter = counter;
   di.route_ctas = grid;   // every CTA holds router rows

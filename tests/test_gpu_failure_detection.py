@@ -2,10 +2,13 @@
 out is recorded in the handle's status word, the launch still completes, the
 host reads MOE_ERR_TIMEOUT, and the next forward is exact again.
 
-The persistent kernel's routing CTA is made to wait (with a short bound) on a
-counter word that nothing sets (MOE_DEBUG_STALL=1, read by the launcher at
-every launch).  No kernel traps, faults or hangs: every wait in the library is
-bounded, and a CTA whose wait ran out keeps signalling, so the others finish.
+A routing CTA is made to wait on a count that is never reached
+(MOE_DEBUG_STALL=1, read by the launcher at every launch): on the gemv path the
+dense pass's routing CTA waits for one router CTA more than exist; in the
+persistent kernel CTA 0 waits on a counter word that nothing sets.  No kernel
+traps, faults or hangs: every wait in the library is bounded, and a CTA whose
+wait ran out still completes its work (the routing runs on the logits as they
+stand), so the launch completes and the next forward is exact.
 """
 import pytest
 
@@ -42,6 +45,27 @@ def test_persistent_kernel_wait_timeout_is_reported_and_recovers(monkeypatch):
         monkeypatch.delenv("MOE_DEBUG_STALL")
         got = gu.run_layer(h, x, lay.spec.act_dtype)
         gu.check_parity(got, gu.ora_forward(lay, x), what="after a recorded timeout")
+        assert h.device_status() == 0
+    finally:
+        h.close()
+
+
+def test_routing_wait_timeout_is_reported_and_recovers(monkeypatch):
+    import quantized_moe_decode_gemv_gb300 as pkg
+    lay = gu.cached_layer("tiny")
+    h = gu.build_layer(lay, 4)
+    try:
+        h.set_path("gemv")
+        x, _ = gu.margin_x(lay, 4, seed=124)
+        xt = gu.to_torch_x(x, lay.spec.act_dtype)
+        assert h.device_status() == 0
+        monkeypatch.setenv("MOE_DEBUG_STALL", "1")
+        h.forward(xt)
+        torch.cuda.synchronize()
+        assert pkg._capi.STATUS_NAMES[h.device_status()] == "MOE_ERR_TIMEOUT"
+        monkeypatch.delenv("MOE_DEBUG_STALL")
+        got = gu.run_layer(h, x, lay.spec.act_dtype)
+        gu.check_parity(got, gu.ora_forward(lay, x), what="after a recorded routing timeout")
         assert h.device_status() == 0
     finally:
         h.close()
