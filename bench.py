@@ -1,13 +1,21 @@
 #!/usr/bin/env python
 """MoE-layer decode benchmark on one GB300 (or N independent replicas).
 
-Workload: the latent MoE layer at the Bolt 74B-A9B shapes (H=4096, latent
-L=1024, E=496 routed experts, top-k=9 sigmoid router with fp32 bias and
+Headline workload: the latent MoE layer at the Bolt 74B-A9B shapes (H=4096,
+latent L=1024, E=496 routed experts, top-k=9 sigmoid router with fp32 bias and
 normalised weights x2.5, experts F=1856 squared-ReLU int4 affine group 64 with
-bf16 scale/bias, bf16 shared expert F=3712), decoding T=1 token row per step
-(T=16 reported alongside).  Inputs are seeded synthetic data resident in HBM;
-32 distinct token batches are cycled so the selected experts change, and L2 is
-flushed (a 256 MB write) before every timed step.
+bf16 scale/bias, bf16 shared expert F=3712), decoding T=1 token row per step.
+Inputs are seeded synthetic data resident in HBM; 32 distinct token batches
+are cycled so the selected experts change, and L2 is flushed before every
+timed step.
+
+Alongside (``also``), every other configured workload is measured the same way:
+the latent layer at T=16; the non-latent sigmoid top-8 layer (H=6144, E=256,
+SwiGLU F=2048 int4 g32 fp16) at T=1/4/32; the five-layer heterogeneous stack
+(E=240..496) at T=2/9/16, layers run round-robin with the residual carried;
+the batched-serving sweep of the latent layer with Zipf(1.1)-skewed expert load
+at T=64/256 (grouped tcgen05 path, with tensor-pipe throughput); and the tiny
+layer at T=1/4.
 
 Prints ONE JSON line: tokens/s (``value``), achieved HBM GB/s over the
 algorithmic bytes, the roofline of the dominant kernel, the end-to-end number
@@ -51,8 +59,11 @@ class L2Flush:
         self.w.zero_()
         self.r.sum()
 STAGES = ["dense_in", "route", "expert_up", "expert_down", "dense_out"]
-KERNEL_OF_STAGE = {"dense_in": "k_dense_in", "route": "k_route", "expert_up": "k_expert",
-                   "expert_down": "k_expert", "dense_out": "k_dense_out", "k_fused": "k_fused"}
+# the kernels of the gemv path's stages (the expert kernel moves its weights by
+# bulk copies up to two rows, by register loads above)
+KERNEL_OF_STAGE = {"dense_in": "k_dense_in", "route": "k_route", "expert_up": "k_expert_bulk",
+                   "expert_down": "k_expert_bulk", "dense_out": "k_dense_bulk"}
+KERNEL_OF_STAGE_REG = dict(KERNEL_OF_STAGE, expert_up="k_expert", expert_down="k_expert")
 # the grouped path runs every projection through the tcgen05 GEMM (its split-K
 # sums and the combine ride in the same stages)
 KERNEL_OF_STAGE_GROUPED = {"dense_in": "k_umma2", "route": "k_route", "expert_up": "k_umma2",
@@ -68,7 +79,8 @@ KERNEL_SOURCES = {
     "k_route": ["moe_kernels.cuh", "moe_layer.cu"],
     "k_umma": ["moe_kernels.cuh", "moe_umma.cuh", "moe_layer.cu"],
     "k_umma2": ["moe_kernels.cuh", "moe_umma.cuh", "moe_umma2.cuh", "moe_layer.cu"],
-    "k_fused": ["moe_kernels.cuh", "moe_fused.cuh", "moe_fused.cu", "moe_layer.cu"],
+    "k_expert_bulk": ["moe_kernels.cuh", "moe_expert_bulk.cuh", "moe_layer.cu"],
+    "k_dense_bulk": ["moe_kernels.cuh", "moe_expert_bulk.cuh", "moe_dense_bulk.cuh", "moe_layer.cu"],
 }
 
 
@@ -170,18 +182,16 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle sample budget")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--seed", type=int, default=0)
-    p.add_argument("--path", choices=["auto", "fused", "gemv", "grouped"], default="auto",
-                   help="kernel schedule (A/B); auto: one persistent kernel below 64 rows, "
-                        "the grouped tcgen05 path from 64")
+    p.add_argument("--path", choices=["auto", "gemv", "grouped"], default="auto",
+                   help="kernel schedule (A/B); auto: the gemv path below 16 rows, the grouped "
+                        "tcgen05 path from 16")
+    p.add_argument("--config", choices=["latent", "nonlatent", "tiny"], default="latent",
+                   help="layer of the main line (the headline metric is the latent layer at T=1)")
+    p.add_argument("--no-also", action="store_true", help="skip the other configured workloads")
     p.add_argument("--zipf", action="store_true", help="Zipf-skewed expert load (batched sweep)")
     p.add_argument("--sweep", default="", help="comma-separated T values: time each and write "
                    "one JSON line per T to --sweep-out (the main line is unchanged)")
     p.add_argument("--sweep-out", default="sweep.jsonl")
-    p.add_argument("--stack", action="store_true",
-                   help="also time the five-layer heterogeneous stack (E = 240..496) at --stack-T "
-                        "rows, layers round-robin with the residual carried; one JSON line per T "
-                        "appended to --sweep-out")
-    p.add_argument("--stack-T", default="2,9,16")
     return p.parse_args()
 
 
@@ -339,7 +349,7 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    spec = mi.SPECS["latent"]
+    spec = mi.SPECS[args.config]
     layer = mi.make_layer(spec, args.seed)
     for i in range(args.warmup):
         time_oracle(layer, 1, 1e9, args.seed + 500 + i)
@@ -354,7 +364,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "T": 1},
+            "config": {"workload": WORKLOAD if args.config == "latent" else spec.name + " layer", "T": 1},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": f"{args.steps} one-row forwards of the fp64 oracle"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -399,6 +409,72 @@ def measure(torch, pkg, spec, layer_h, T, steps, warmup, seed, flush, stream, pr
     return {"step_ms": step_ms, "stage_ms": stage_ms / steps, "n_uniq": n_uniq, "xs": xs}
 
 
+def workload_line(torch, pkg, spec, T, steps, warmup, seed, flush, stream, hbm_peak, tc_peak,
+                  zipf=False, path="auto", label=None):
+    """One configured workload measured like the main line (L2 flushed before
+    every timed forward): tokens/s, step time, achieved GB/s over the
+    algorithmic bytes and its fraction of the HBM peak, and the flops of the
+    step against the bf16 tensor peak."""
+    import moe_inputs as mi
+    rb = mi.zipf_router_bias(spec.n_experts, seed) if zipf else None
+    layer = mi.make_layer(spec, seed, router_bias=rb)
+    h = pkg.MoELayer(pkg.MoEConfig.from_spec(spec, max_tokens=max(T, 16)),
+                     pkg.upload_arrays(layer.arrays()))
+    torch.cuda.empty_cache()
+    try:
+        h.set_path(path)
+        m = measure(torch, pkg, spec, h, T, steps, warmup, seed, flush, stream, profile=False)
+        tt = sum(m["step_ms"]) / len(m["step_ms"])
+        bb = float(np.mean([layer_bytes(spec, T, u) for u in m["n_uniq"]]))
+        fl = layer_flops(spec, T)
+        return {"workload": label or spec.name, "T": T, "zipf": bool(zipf), "path": h.path_for(T),
+                "tokens_per_s": T / (tt / 1e3), "ms_per_step": tt,
+                "ms_p10_p50_p90": [float(np.percentile(m["step_ms"], q)) for q in (10, 50, 90)],
+                "gbs": bb / (tt / 1e3) / 1e9, "hbm_frac": bb / (tt / 1e3) / 1e9 / hbm_peak,
+                "mean_distinct_experts": float(np.mean(m["n_uniq"])),
+                "tflops": fl / (tt / 1e3) / 1e12, "tensor_frac": fl / (tt / 1e3) / 1e12 / tc_peak,
+                "launches": h.last_launch_count(), "steps": steps}
+    finally:
+        h.close()
+        torch.cuda.empty_cache()
+
+
+def stack_line(torch, pkg, T, steps, warmup, flush, stream):
+    """The five-layer heterogeneous stack (E = 240..496, latent shapes) run like
+    a model: the layers in order on the same rows, the residual carried, L2
+    flushed before every timed pass."""
+    import moe_inputs as mi
+    specs = mi.stack_specs()
+    hs = [pkg.MoELayer(pkg.MoEConfig.from_spec(sp, max_tokens=16), pkg.upload_arrays(mi.make_layer(sp, i).arrays()))
+          for i, sp in enumerate(specs)]
+    torch.cuda.empty_cache()
+    try:
+        xs = [torch.from_numpy(mi.make_x(specs[0], T, 900 + i).view(np.int16)).cuda()
+              .view(torch.bfloat16) for i in range(8)]
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        with torch.cuda.stream(stream):
+            for i in range(warmup + steps):
+                flush.zero_()
+                if i >= warmup:
+                    evs[i - warmup][0].record(stream)
+                cur = xs[i % 8]
+                for hh in hs:
+                    cur = hh.forward(cur, stream=stream)
+                if i >= warmup:
+                    evs[i - warmup][1].record(stream)
+            stream.synchronize()
+        ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+        return {"workload": "stack of five latent layers, E = " + "/".join(str(sp.n_experts) for sp in specs),
+                "T": T, "paths": [hh.path_for(T) for hh in hs], "ms_per_stack_step": ms,
+                "tokens_per_s": T / (ms / 1e3), "layer_forwards_per_s": len(hs) / (ms / 1e3),
+                "steps": steps}
+    finally:
+        for hh in hs:
+            hh.close()
+        torch.cuda.empty_cache()
+
+
 def run_ours(args):
     import torch
 
@@ -420,12 +496,12 @@ def run_ours(args):
     tc_peak = peaks.get("bf16_tflops", 1900.0)
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
 
-    spec = mi.SPECS["latent"]
+    spec = mi.SPECS[args.config]
     rb = mi.zipf_router_bias(spec.n_experts, args.seed + rank) if args.zipf else None
     layer = mi.make_layer(spec, args.seed + rank, router_bias=rb)
     sweep = [int(v) for v in args.sweep.split(",") if v.strip()]
     maxT = max([args.T, args.also_T or 1] + sweep)
-    cfg = pkg.MoEConfig.from_spec(spec, max_tokens=maxT)
+    cfg = pkg.MoEConfig.from_spec(spec, max_tokens=max(maxT, 16))
     h = pkg.MoELayer(cfg, pkg.upload_arrays(layer.arrays(), device=dev))
     h.set_path(args.path)
     torch.cuda.empty_cache()
@@ -448,61 +524,61 @@ def run_ours(args):
     bytes_steps = [layer_bytes(spec, args.T, u) for u in m["n_uniq"]]
     gbs = sum(bytes_steps) / (sum(m["step_ms"]) / 1e3) / 1e9
 
-    # dominant kernel roofline (stage with the largest share of the step)
+    # dominant kernel roofline: the kernel with the largest share of the step,
+    # its launches pooled (the expert kernel runs twice: up and down)
     st = mp["stage_ms"]
     avg_uniq = float(np.mean(mp["n_uniq"]))
     sb = stage_bytes(spec, args.T, avg_uniq)
     path = h.path_for(args.T)
     launches = h.last_launch_count()
-    if path == "fused":
-        # one kernel per forward: the whole layer's bytes over its duration
-        dom_name = "k_fused"
-        fused_b = layer_bytes(spec, args.T, avg_uniq)
-        achieved = fused_b / (st[0] / 1e3) / 1e9
-        stages = {"k_fused": {"ms": round(float(st[0]), 5), "share": 1.0, "alg_bytes": int(fused_b),
-                              "gbs": round(achieved, 1)}}
-    else:
-        # the dominant kernel: the largest share of the step, its launches
-        # pooled (the expert kernel runs twice: up and down)
-        per_kernel = {}
-        kmap = KERNEL_OF_STAGE_GROUPED if path == "grouped" else KERNEL_OF_STAGE
-        for i, n in enumerate(STAGES):
-            kname = kmap[n]
-            b, t = per_kernel.get(kname, (0.0, 0.0))
-            per_kernel[kname] = (b + sb[n], t + float(st[i]))
-        dom_name = max(per_kernel, key=lambda kn: per_kernel[kn][1])
-        achieved = per_kernel[dom_name][0] / (per_kernel[dom_name][1] / 1e3) / 1e9
-        stages = {n: {"ms": round(float(st[i]), 5), "share": round(float(st[i] / st.sum()), 4),
-                      "alg_bytes": int(sb[n]), "gbs": round(sb[n] / (st[i] / 1e3) / 1e9, 1)}
-                  for i, n in enumerate(STAGES)}
+    per_kernel = {}
+    kmap = (KERNEL_OF_STAGE_GROUPED if path == "grouped" else
+            KERNEL_OF_STAGE if args.T <= 2 else KERNEL_OF_STAGE_REG)
+    for i, n in enumerate(STAGES):
+        kname = kmap[n]
+        b, t = per_kernel.get(kname, (0.0, 0.0))
+        per_kernel[kname] = (b + sb[n], t + float(st[i]))
+    dom_name = max(per_kernel, key=lambda kn: per_kernel[kn][1])
+    achieved = per_kernel[dom_name][0] / (per_kernel[dom_name][1] / 1e3) / 1e9
+    stages = {n: {"kernel": kmap[n], "ms": round(float(st[i]), 5), "share": round(float(st[i] / st.sum()), 4),
+                  "alg_bytes": int(sb[n]), "gbs": round(sb[n] / (st[i] / 1e3) / 1e9, 1)}
+              for i, n in enumerate(STAGES)}
 
-    # second T reported alongside
-    also = None
-    if args.also_T and args.also_T != args.T:
-        m2 = measure(torch, pkg, spec, h, args.also_T, max(20, args.steps // 4), args.warmup,
-                     args.seed + 1, flush, stream, profile=False)
-        t2 = sum(m2["step_ms"])
-        b2 = sum(layer_bytes(spec, args.also_T, u) for u in m2["n_uniq"])
-        also = {"T": args.also_T, "tokens_per_s": len(m2["step_ms"]) * args.also_T / (t2 / 1e3),
-                "ms_per_step": t2 / len(m2["step_ms"]), "gbs": b2 / (t2 / 1e3) / 1e9,
-                "hbm_frac": b2 / (t2 / 1e3) / 1e9 / hbm_peak,
-                "mean_distinct_experts": float(np.mean(m2["n_uniq"])), "path": h.path_for(args.also_T)}
+    # every other configured workload, measured the same way
+    also = []
+    if rank == 0 and not args.no_also:
+        st_also = max(30, args.steps // 4)
+        if args.also_T and args.also_T != args.T:
+            also.append(workload_line(torch, pkg, mi.SPECS["latent"], args.also_T, st_also, args.warmup,
+                                      args.seed + 1, flush, stream, hbm_peak, tc_peak,
+                                      label="latent layer (uniform load)"))
+        for T in (1, 4, 32):
+            also.append(workload_line(torch, pkg, mi.SPECS["nonlatent"], T, st_also, args.warmup,
+                                      args.seed, flush, stream, hbm_peak, tc_peak,
+                                      label="non-latent sigmoid top-8 layer"))
+        for T in (64, 256):
+            also.append(workload_line(torch, pkg, mi.SPECS["latent"], T, st_also, args.warmup,
+                                      args.seed, flush, stream, hbm_peak, tc_peak, zipf=True,
+                                      label="latent layer, Zipf(1.1) expert load"))
+        for T in (2, 9, 16):
+            also.append(stack_line(torch, pkg, T, max(20, args.steps // 8), args.warmup, flush, stream))
+        for T in (1, 4):
+            also.append(workload_line(torch, pkg, mi.SPECS["tiny"], T, st_also, args.warmup, args.seed,
+                                      flush, stream, hbm_peak, tc_peak, label="tiny layer"))
 
     # batched serving sweep (separate output file)
     if sweep and rank == 0:
         with open(args.sweep_out, "w") as f:
             for T in sweep:
-                # beyond 256 rows (prefill) only the grouped path is timed
-                paths = (["grouped"] if T > 256 else
-                         ["fused", "gemv", "grouped"] if T >= 16 else ["fused", "gemv"])
-                for path in paths:
-                    h.set_path(path)
+                paths = ["grouped"] if T > 256 else ["gemv", "grouped"] if T >= 16 else ["gemv"]
+                for pth in paths:
+                    h.set_path(pth)
                     ms = measure(torch, pkg, spec, h, T, max(20, args.steps // 4), 3,
                                  args.seed + 7, flush, stream, profile=False)
                     tt = sum(ms["step_ms"])
                     bb = sum(layer_bytes(spec, T, u) for u in ms["n_uniq"])
                     f.write(json.dumps({
-                        "T": T, "path": path, "zipf": bool(args.zipf),
+                        "T": T, "path": pth, "zipf": bool(args.zipf),
                         "tokens_per_s": len(ms["step_ms"]) * T / (tt / 1e3),
                         "ms_per_step": tt / len(ms["step_ms"]),
                         "gbs": bb / (tt / 1e3) / 1e9, "hbm_frac": bb / (tt / 1e3) / 1e9 / hbm_peak,
@@ -513,39 +589,6 @@ def run_ours(args):
                         "tensor_frac": (layer_flops(spec, T) / (tt / len(ms["step_ms"]) / 1e3) / 1e12
                                         / tc_peak)}) + "\n")
         h.set_path(args.path)
-
-    # the heterogeneous five-layer stack, run like a model (layers round-robin)
-    if args.stack and rank == 0:
-        specs = mi.stack_specs()
-        stack_T = [int(v) for v in args.stack_T.split(",") if v.strip()]
-        layers = [mi.make_layer(sp, i) for i, sp in enumerate(specs)]
-        hs = [pkg.MoELayer(pkg.MoEConfig.from_spec(sp, max_tokens=max(stack_T)),
-                           pkg.upload_arrays(l.arrays(), device=dev)) for sp, l in zip(specs, layers)]
-        with open(args.sweep_out, "a") as f:
-            for T in stack_T:
-                xs = [torch.from_numpy(mi.make_x(specs[0], T, 900 + i).view(np.int16)).cuda()
-                      .view(torch.bfloat16) for i in range(8)]
-                evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                       for _ in range(args.steps)]
-                with torch.cuda.stream(stream):
-                    for i in range(args.warmup + args.steps):
-                        flush.zero_()
-                        if i >= args.warmup:
-                            evs[i - args.warmup][0].record(stream)
-                        cur = xs[i % 8]
-                        for hh in hs:
-                            cur = hh.forward(cur, stream=stream)
-                        if i >= args.warmup:
-                            evs[i - args.warmup][1].record(stream)
-                    stream.synchronize()
-                ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
-                f.write(json.dumps({
-                    "stack_experts": [sp.n_experts for sp in specs], "T": T,
-                    "paths": [hh.path_for(T) for hh in hs],
-                    "ms_per_stack_step": ms, "tokens_per_s": T / (ms / 1e3),
-                    "layer_forwards_per_s": len(hs) / (ms / 1e3)}) + "\n")
-        for hh in hs:
-            hh.close()
 
     # end to end through the host-buffer C-ABI call
     xs_host = [x.cpu().pin_memory() for x in m["xs"][:8]]
@@ -572,13 +615,14 @@ def run_ours(args):
                          f"selected experts dequantised per row), {dt:.1f} s"}
 
     if rank == 0:
+        workload = WORKLOAD if args.config == "latent" else spec.name + " layer"
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
             "ms_p10_p50_p90": [float(np.percentile(m["step_ms"], q)) for q in (10, 50, 90)],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded random weights and activations)",
-            "config": {"workload": WORKLOAD, "T": args.T, "parallelism": "replicas" if world > 1 else "single",
+            "config": {"workload": workload, "T": args.T, "parallelism": "replicas" if world > 1 else "single",
                        "l2": "flushed before every timed step: 256 MB write, then 256 MB read (clean L2)",
                        "input_batches": 32},
             "hbm_gbs": gbs, "hbm_frac": gbs / hbm_peak, "hbm_peak_gbs": hbm_peak,

@@ -73,20 +73,19 @@ typedef enum moe_router {
 typedef enum moe_dtype { MOE_DTYPE_BF16 = 0, MOE_DTYPE_FP16 = 1, MOE_DTYPE_FP32 = 2 } moe_dtype;
 
 /* Kernel schedule of a forward.
- *   FUSED    one persistent cooperative kernel runs the whole layer; the
- *            routing-independent shared-expert rows stream while the routed
- *            chain (router -> top-k -> expert up -> expert down -> combine)
- *            waits on its dependencies.  CUDA cores; for few token rows.
- *   GEMV     the same arithmetic as five stream-ordered kernels.
+ *   GEMV     CUDA-core kernels on one stream with programmatic dependent
+ *            launch: the dense pass over x (router, fc1_latent_proj, shared
+ *            gate/up) with the top-k fused into a routing CTA, the expert up
+ *            and down projections (the weighted combine fused into the down
+ *            projection's last CTA per column range), and the output pass
+ *            (fc2_latent_proj, shared down, residual).  For few token rows.
  *   GROUPED  row-grouped tcgen05 GEMMs for the experts and dense projections
  *            (many token rows per forward).
- *   AUTO     GROUPED when T >= 16 (MOE_GROUPED_MIN_T), else FUSED when
- *            T <= MOE_FUSED_MAX_T (default 0: off), else GEMV. */
+ *   AUTO     GROUPED when T >= 16 (MOE_GROUPED_MIN_T), else GEMV. */
 typedef enum moe_path {
   MOE_PATH_AUTO = 0,
   MOE_PATH_GEMV = 1,
-  MOE_PATH_GROUPED = 2,
-  MOE_PATH_FUSED = 3
+  MOE_PATH_GROUPED = 2
 } moe_path;
 
 typedef struct moe_layer_config {

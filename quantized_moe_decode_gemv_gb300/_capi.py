@@ -25,7 +25,7 @@ STATUS_NAMES = ["MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR
 ACT = {"swiglu": 0, "relu2": 1}
 ROUTER = {"softmax": 0, "sigmoid": 1}
 DTYPE = {"bf16": 0, "fp16": 1, "fp32": 2}
-PATH = {"auto": 0, "gemv": 1, "grouped": 2, "fused": 3}
+PATH = {"auto": 0, "gemv": 1, "grouped": 2}
 NUM_STAGES = 5
 STAGE_NAMES = ["dense_in", "route", "expert_up", "expert_down", "dense_out"]
 
@@ -336,7 +336,7 @@ class MoELayer:
         return load_library().moe_layer_device_bytes(self.handle)
 
     def path_for(self, T: int) -> str:
-        """The path ("fused", "gemv" or "grouped") a forward of T rows takes."""
+        """The path ("gemv" or "grouped") a forward of T rows takes."""
         v = load_library().moe_layer_path_for(self.handle, int(T))
         if v < 0:
             raise MoEError(f"no path for T={T}")

@@ -20,10 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libmoe_gb300.so")
 
-# (source, object name, extra flags): the persistent kernel is compiled once per
-# staging width so that its instantiations build in parallel
-SOURCES = [("moe_layer.cu", "moe_layer", []), ("moe_noalloc.cu", "moe_noalloc", [])] + [
-    ("moe_fused.cu", f"moe_fused_tb{tb}", [f"-DFZ_TB={tb}"]) for tb in (1, 2, 4, 8)]
+# (source, object name, extra flags)
+SOURCES = [("moe_layer.cu", "moe_layer", []), ("moe_noalloc.cu", "moe_noalloc", [])]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-warn-spills"]

@@ -17,7 +17,6 @@
 #include "moe_dense_bulk.cuh"
 #include "moe_umma.cuh"
 #include "moe_umma2.cuh"
-#include "moe_fused.cuh"
 
 using namespace moe;
 
@@ -79,8 +78,7 @@ struct moe_layer {
   void* bout = nullptr;       // [Tmax, L + F_sh] 16-bit operand of the grouped output GEMM
   uint32_t* rmask = nullptr;  // [E, (Tmax+31)/32] routing row bitmasks (Tmax > route_small_t)
   int* rpref = nullptr;       // [E, (Tmax+31)/32] their popcount prefixes
-  int* fsync = nullptr;       // FZ_WORDS phase counters of the persistent kernel
-  float* sdbuf = nullptr;     // [Tmax, H] shared-expert down output (persistent kernel)
+  float* sdbuf = nullptr;     // [Tmax, H] shared-expert down output (fp32)
   void* x_stage = nullptr;    // [Tmax, H] act dtype (host-buffer forward)
   void* out_stage = nullptr;
 
@@ -94,14 +92,7 @@ struct moe_layer {
   int kin = 0;
   int grouped_min_t = 16;
   int expert_split = 0;   // AUTO's grouped path: light experts on the int4 gemv kernel
-  int fused_max_t = 0;    // AUTO: the persistent kernel for T <= this (below grouped_min_t)
-  int fused_sd_pre = 60;  // persistent kernel: percent of a CTA's shared-down rows before the experts,
-  int fused_sd_mid = 20;  // and between the expert up and down rows
-  int fused_depth = 4;    // slots per warp ring (at most)
-  int fused_chunk = 4096; // slot bytes (at least)
-  FusedLaunchCache fused_grid[4][2];  // cooperative grid of k_fused<TB, ., gated>
   int last_launches = 0;  // kernel launches of the last forward
-  unsigned long long* fz_trace = nullptr;   // diagnostics (MOE_FUSED_TRACE): phase stamps
   unsigned long long* um_trace = nullptr;   // diagnostics (MOE_UMMA_TRACE): grouped GEMM role stamps
   int um_trace_n = 0;                       // grouped launches stamped in this forward
   unsigned long long* ct_trace = nullptr;   // diagnostics (MOE_CTA_TRACE): gemv-path CTA stamps
@@ -654,12 +645,6 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   if (const char* env = std::getenv("MOE_EXPERT_SPLIT")) L->expert_split = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_PDL")) L->use_pdl = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_PDL_GROUPED")) L->pdl_grouped = std::atoi(env) != 0;
-  if (const char* env = std::getenv("MOE_FUSED_MAX_T")) L->fused_max_t = std::atoi(env);
-  if (const char* env = std::getenv("MOE_SD_PRE")) L->fused_sd_pre = std::max(0, std::min(100, std::atoi(env)));
-  if (const char* env = std::getenv("MOE_SD_MID")) L->fused_sd_mid = std::max(0, std::min(100, std::atoi(env)));
-  if (const char* env = std::getenv("MOE_FZ_DEPTH")) L->fused_depth = std::max(2, std::atoi(env));
-  if (const char* env = std::getenv("MOE_FZ_CHUNK")) L->fused_chunk = std::max(1024, std::atoi(env)) & ~127;
-  const bool want_trace = std::getenv("MOE_FUSED_TRACE") && std::atoi(std::getenv("MOE_FUSED_TRACE"));
   if (const char* env = std::getenv("MOE_PREFETCH")) L->prefetch = std::atoi(env);
   if (const char* env = std::getenv("MOE_EXPERT_PB")) L->expert_pb = std::max(1, std::min(8, std::atoi(env)));
   if (const char* env = std::getenv("MOE_EXPERT_TARGET")) L->expert_target = std::max(1, std::min(16, std::atoi(env)));
@@ -783,10 +768,6 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
       MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->rmask), nw * 4), "workspace");
       MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->rpref), nw * 4), "workspace");
     }
-    MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->fsync), FZ_WORDS * FZ_SYNC_STRIDE * 4), "workspace");
-    MOE_TRY_CUDA(cudaMemsetAsync(L->fsync, 0, FZ_WORDS * FZ_SYNC_STRIDE * 4, s), "counter clear");
-    if (want_trace)
-      MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->fz_trace), 4096 * FZ_TRACE * 8), "trace");
     if (std::getenv("MOE_CTA_TRACE") && std::atoi(std::getenv("MOE_CTA_TRACE"))) {
       const size_t n = static_cast<size_t>(CT_SLOTS) * CT_MAX_CTAS * CT_STAMPS * 8;
       MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->ct_trace), n), "trace");
@@ -1028,52 +1009,6 @@ static cudaError_t launch_umma(moe_layer* h, UmmaArgs& a, int T, cudaStream_t s,
 
 // Plan of a persistent-kernel launch: staged token rows per pass, per-warp
 // ring depth and slot size, and the shared memory of one CTA.
-struct FusedPlan {
-  int tb = 0, depth = 0, chunk = 0;
-  size_t smem = 0;
-};
-
-static FusedPlan fused_plan(const moe_layer* h, int T, int mask_words) {
-  const moe_layer_config& c = h->cfg;
-  FusedPlan fp;
-  if (T > 32) return fp;   // the segment list is sized for up to 32 token rows
-  const int H = c.hidden, Fs = c.shared_ffn, L = c.latent, F = c.expert_ffn, kin = h->kin;
-  // a slot holds at least one expert row (dense rows are split over slots)
-  const int gm = c.act == MOE_ACT_SWIGLU ? 2 : 1;
-  int row = std::max(gm * (kin / 2 + (kin / c.group_size) * 4) + 32, F / 2 + (F / c.group_size) * 4 + 16);
-  const int chunk = std::max(h->fused_chunk, (row + 127) & ~127);
-  const size_t route = ROUTE_SMEM_BYTES + static_cast<size_t>(c.n_experts) * mask_words * 4;
-  for (int tb = pow2_at_least(T, 8); tb >= 1; tb >>= 1) {
-    // two CTAs per SM when a ring of depth 2 fits, else one CTA with deeper rings
-    const size_t two = 112 * 1024, one = static_cast<size_t>(kSmemMax) - 2048;
-    for (int pass = 0; pass < 2; ++pass) {
-      const size_t budget = pass == 0 ? two : one;
-      if (pass == 0 && tb >= 8) continue;   // TB = 8 is compiled for one CTA per SM
-      for (int d = std::min(h->fused_depth, FZ_MAX_DEPTH); d >= 2; --d) {
-        const size_t sm = fused_smem_bytes(tb, d, chunk, H, Fs, L, kin, F, route);
-        if (sm <= budget) {
-          fp.tb = tb;
-          fp.depth = d;
-          fp.chunk = chunk;
-          fp.smem = sm;
-          return fp;
-        }
-      }
-    }
-  }
-  return fp;
-}
-
-static cudaError_t launch_fused(moe_layer* h, const FusedArgs& a, int tb, size_t smem, bool gated,
-                                cudaStream_t s) {
-  switch (tb) {
-    case 1: return fused_launch_tb1(a, gated, smem, h->num_sms, &h->fused_grid[0][gated], s);
-    case 2: return fused_launch_tb2(a, gated, smem, h->num_sms, &h->fused_grid[1][gated], s);
-    case 4: return fused_launch_tb4(a, gated, smem, h->num_sms, &h->fused_grid[2][gated], s);
-    default: return fused_launch_tb8(a, gated, smem, h->num_sms, &h->fused_grid[3][gated], s);
-  }
-}
-
 // Diagnostics: CTA 0's role stamps per chunk of each grouped launch of the last
 // forward, in microseconds since the CTA started (SM cycles at 2070 MHz).
 static void print_umma_trace(moe_layer* h, cudaStream_t s) {
@@ -1162,47 +1097,10 @@ static void print_cta_trace(moe_layer* h, cudaStream_t s) {
   }
 }
 
-// Diagnostics: per phase stamp, the min / median / max over CTAs of the time
-// since the earliest kernel start (microseconds).
-static void print_fused_trace(moe_layer* h, cudaStream_t s) {
-  const int G = 4096;
-  std::vector<unsigned long long> t(static_cast<size_t>(G) * FZ_TRACE);
-  if (cudaMemcpyAsync(t.data(), h->fz_trace, t.size() * 8, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      cudaStreamSynchronize(s) != cudaSuccess)
-    return;
-  unsigned long long t0 = ~0ull;
-  int n = 0;
-  for (int c = 0; c < G; ++c)
-    if (t[static_cast<size_t>(c) * FZ_TRACE]) { t0 = std::min(t0, t[static_cast<size_t>(c) * FZ_TRACE]); n = c + 1; }
-  std::fprintf(stderr, "fused trace (%d CTAs, us since first start: min/med/max; CTA 0):\n", n);
-  for (int i = 0; i < 13; ++i) {
-    std::vector<double> v;
-    for (int c = 1; c < n; ++c)
-      if (t[static_cast<size_t>(c) * FZ_TRACE + i]) v.push_back((t[static_cast<size_t>(c) * FZ_TRACE + i] - t0) * 1e-3);
-    std::sort(v.begin(), v.end());
-    const double c0 = t[i] ? (t[i] - t0) * 1e-3 : -1.0;
-    if (v.empty())
-      std::fprintf(stderr, "  stamp %2d: -  (cta0 %.2f)\n", i, c0);
-    else
-      std::fprintf(stderr, "  stamp %2d: %7.2f %7.2f %7.2f  (cta0 %.2f)\n", i, v.front(), v[v.size() / 2],
-                   v.back(), c0);
-  }
-  std::fprintf(stderr, "  CTA 1 detail:");
-  for (int i = 13; i < 25; ++i)
-    std::fprintf(stderr, " %.2f", t[FZ_TRACE + i] ? (t[FZ_TRACE + i] - t0) * 1e-3 : -1.0);
-  std::fprintf(stderr, "\n");
-}
-
 // The path a forward of T rows takes (never AUTO).
 static int choose_path(const moe_layer* h, int T) {
   if (h->path == MOE_PATH_GROUPED || (h->path == MOE_PATH_AUTO && T >= h->grouped_min_t))
     return MOE_PATH_GROUPED;
-  if (h->path == MOE_PATH_FUSED || (h->path == MOE_PATH_AUTO && T <= h->fused_max_t)) {
-    const int P = T * h->cfg.top_k;
-    const int W = (T + 31) / 32;
-    const int mw = (P > 256 && static_cast<int64_t>(h->cfg.n_experts) * W * 4 <= 160 * 1024) ? W : 0;
-    if (fused_plan(h, T, mw).tb > 0) return MOE_PATH_FUSED;
-  }
   return MOE_PATH_GEMV;
 }
 
@@ -1282,87 +1180,6 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     const int P = T * k;
     const int W = (T + 31) / 32;
     ra.mask_words = (P > 256 && static_cast<int64_t>(E) * W * 4 <= 160 * 1024) ? W : 0;
-  }
-  const bool fused = path == MOE_PATH_FUSED;
-  const FusedPlan fzp = fused ? fused_plan(h, T, ra.mask_words) : FusedPlan{};
-  if (fused && fzp.tb > 0) {
-    // the whole layer as one persistent kernel
-    FusedArgs fa{};
-    fa.T = T;
-    fa.H = H; fa.E = E; fa.L = Lt; fa.Fs = Fs; fa.k = k;
-    fa.act = c.act;
-    fa.x = x;
-    fa.x_dt = c.act_dtype;
-    fa.router_w = h->router_w;
-    fa.router_dt = c.router_dtype;
-    fa.fc1 = h->fc1;
-    fa.sh_gate = h->sh_gate;
-    fa.sh_up = h->sh_up;
-    fa.sh_down = h->sh_down;
-    fa.fc2 = h->fc2;
-    fa.dense_in = h->dense_in;
-    fa.din_rows = h->r_in;
-    fa.off_fc1 = h->off_fc1;
-    fa.off_shg = h->off_shg;
-    fa.off_shu = h->off_shu;
-    fa.route = ra;
-    ExpertArgs& up = fa.up;
-    up.n_rows = F;
-    up.K = kin;
-    up.G = c.group_size;
-    up.q = h->up_q;
-    up.sb = h->up_sb;
-    up.q_gate = gated ? h->gate_q : nullptr;
-    up.sb_gate = gated ? h->gate_sb : nullptr;
-    up.s_dt = c.scale_dtype;
-    up.act = c.act;
-    up.meta = h->meta;
-    up.umax = h->umax;
-    up.k = k;
-    if (Lt) {
-      up.xin = h->dense_in; up.xin_dt = DT_FP32; up.xin_stride = h->r_in; up.xin_off = h->off_fc1;
-    } else {
-      up.xin = x; up.xin_dt = c.act_dtype; up.xin_stride = H; up.xin_off = 0;
-    }
-    up.xin_by_pair = 0;
-    up.out = h->hbuf;
-    ExpertArgs& dn = fa.dn;
-    dn = up;
-    dn.n_rows = kin;
-    dn.K = F;
-    dn.q = h->down_q;
-    dn.sb = h->down_sb;
-    dn.q_gate = nullptr;
-    dn.sb_gate = nullptr;
-    dn.act = -1;
-    dn.xin = h->hbuf; dn.xin_dt = DT_FP32; dn.xin_stride = F; dn.xin_off = 0;
-    dn.xin_by_pair = 1;
-    dn.out = h->pexp;
-    fa.sdbuf = h->sdbuf;
-    fa.pexp = h->pexp;
-    fa.wts = h->wts;
-    fa.ybuf = h->comb;
-    fa.out = out;
-    fa.delta = delta;
-    fa.sync = h->fsync;
-    fa.status = h->status;
-    fa.depth = fzp.depth;
-    fa.chunk_bytes = fzp.chunk;
-    fa.sd_pre = h->fused_sd_pre;
-    fa.sd_mid = h->fused_sd_mid;
-    fa.trace = h->fz_trace;
-    if (h->fz_trace) cudaMemsetAsync(h->fz_trace, 0, 4096 * FZ_TRACE * 8, s);
-    mark(0);
-    e = launch_fused(h, fa, fzp.tb, fzp.smem, gated, s);
-    if (e != cudaSuccess) {
-      h->last_error = std::string("launch failed: ") + cudaGetErrorString(e);
-      return MOE_ERR_CUDA;
-    }
-    for (int i = 1; i <= MOE_NUM_STAGES; ++i) mark(i);
-    if (h->profiling) h->profiled = true;
-    h->last_launches = 1;
-    if (h->fz_trace) print_fused_trace(h, s);
-    return MOE_OK;
   }
   const bool big_route = T > h->route_small_t;
   const bool fuse_route = !grouped && h->fuse_route && !big_route;
@@ -1911,8 +1728,7 @@ moe_status moe_layer_forward_host(moe_layer* h, const void* x_host, int32_t T, v
 
 moe_status moe_layer_set_path(moe_layer* h, int32_t path) {
   if (!h) return MOE_ERR_INVALID_ARG;
-  if (path != MOE_PATH_AUTO && path != MOE_PATH_GEMV && path != MOE_PATH_GROUPED &&
-      path != MOE_PATH_FUSED)
+  if (path != MOE_PATH_AUTO && path != MOE_PATH_GEMV && path != MOE_PATH_GROUPED)
     return MOE_ERR_INVALID_ARG;
   if (path == MOE_PATH_GROUPED && h->cfg.act_dtype == MOE_DTYPE_FP32) {
     h->last_error = "the grouped path needs 16-bit activations";
