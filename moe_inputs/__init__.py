@@ -12,16 +12,17 @@ Storage conventions (the library's input format):
 * bf16 tensors are numpy ``uint16`` arrays of bf16 bit patterns; fp16 tensors
   are numpy ``float16``; fp32 tensors are ``float32``.
 * Expert matrices are row-major ``[E, N_out, K_in]`` with the quantisation
-  groups of ``G`` consecutive elements along ``K_in``.  ``q`` is packed eight
-  4-bit codes per ``uint32`` word, element ``8*w + i`` in bits ``4*i..4*i+3``
-  (lowest nibble first), giving ``[E, N_out, K_in/8]``.  ``scale`` and
+  groups of ``G`` consecutive elements along ``K_in``.  ``q`` holds b-bit
+  codes (b = 3, 4 or 8) packed into ``uint32`` words as one little-endian bit
+  stream per row, code ``i`` in bits ``b*i .. b*i+b-1`` (for b = 4: eight per
+  word, lowest nibble first), giving ``[E, N_out, K_in*b/32]``.  ``scale`` and
   ``bias`` are ``[E, N_out, K_in/G]`` in the layer's scale dtype and a weight
   is reconstructed as ``scale * q + bias`` (MLX-style affine quantisation, as
   the mlx-bun decode-speed program describes its "affine 2/3/4/5/6/8-bit with
   supported group sizes 32/64/128" weights).
 * The quantiser used to make synthetic weights is round-to-nearest over each
-  group's min/max: ``bias = min``, ``scale = (max - min) / 15`` (both rounded
-  to the scale dtype), ``q = clip(rint((w - bias) / scale), 0, 15)``.  The pages
+  group's min/max: ``bias = min``, ``scale = (max - min) / (2^b - 1)`` (both
+  rounded to the scale dtype), ``q = clip(rint((w - bias) / scale), 0, 2^b - 1)``.  The pages
   give no quantiser; this one only shapes the test weights.
 """
 from __future__ import annotations
@@ -35,7 +36,8 @@ import numpy as np
 __all__ = [
     "LayerSpec", "LayerWeights", "SPECS", "stack_specs", "make_layer", "make_x",
     "draw_x_rows", "round_to_bf16_bits", "bf16_bits_to_f32", "quantize_affine_int4",
-    "pack_int4", "unpack_int4", "zipf_router_bias", "spec_for", "ROUTED_BYTES",
+    "quantize_affine", "pack_codes", "unpack_codes", "CODE_BITS", "pack_int4", "unpack_int4",
+    "zipf_router_bias", "spec_for", "ROUTED_BYTES",
 ]
 
 
@@ -79,20 +81,49 @@ def _storage_to_f64(a: np.ndarray, dtype: str) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
-# int4 packing and the synthetic-weight quantiser
+# b-bit packing and the synthetic-weight quantiser
 # ---------------------------------------------------------------------------
 
-def pack_int4(q: np.ndarray) -> np.ndarray:
-    """Pack 4-bit codes ``[..., K]`` (values 0..15) into ``uint32 [..., K/8]``,
-    element ``8*w + i`` at bits ``4*i``."""
+CODE_BITS = (3, 4, 8)   # code widths of the expert weight formats
+
+
+def pack_codes(q: np.ndarray, bits: int) -> np.ndarray:
+    """Pack b-bit codes ``[..., K]`` (values 0..2^b-1) into ``uint32 [..., K*b/32]``
+    as one little-endian bit stream per row: code ``i`` occupies bits
+    ``b*i .. b*i+b-1`` of the row, counted from bit 0 of word 0 (a code may
+    straddle two words).  For b = 4 this is eight codes per word, lowest
+    nibble first; for b = 8 four per word, lowest byte first."""
     q = np.asarray(q)
-    if q.shape[-1] % 8:
-        raise ValueError("K must be a multiple of 8")
-    if q.size and (q.min() < 0 or q.max() > 15):
-        raise ValueError("codes must be in 0..15")
-    q = q.astype(np.uint32).reshape(*q.shape[:-1], q.shape[-1] // 8, 8)
-    shifts = (4 * np.arange(8, dtype=np.uint32))
-    return np.bitwise_or.reduce(q << shifts, axis=-1).astype(np.uint32)
+    K = q.shape[-1]
+    if (K * bits) % 32:
+        raise ValueError("K * bits must be a multiple of 32")
+    if q.size and (q.min() < 0 or q.max() > (1 << bits) - 1):
+        raise ValueError(f"codes must be in 0..{(1 << bits) - 1}")
+    bitarr = ((q.astype(np.uint32)[..., None] >> np.arange(bits, dtype=np.uint32)) & 1).astype(np.uint8)
+    bitarr = bitarr.reshape(*q.shape[:-1], K * bits)
+    by = np.packbits(bitarr, axis=-1, bitorder="little")
+    return np.ascontiguousarray(by).view("<u4").astype(np.uint32)
+
+
+def unpack_codes(packed: np.ndarray, bits: int) -> np.ndarray:
+    """Inverse of :func:`pack_codes` (used by the generator's own checks)."""
+    p = np.ascontiguousarray(np.asarray(packed, dtype=np.uint32))
+    K = p.shape[-1] * 32 // bits
+    out = np.zeros(p.shape[:-1] + (K,), dtype=np.uint8)
+    for i in range(K):
+        pos = bits * i
+        w, off = pos >> 5, pos & 31
+        v = p[..., w].astype(np.uint64) >> np.uint64(off)
+        if off + bits > 32:
+            v = v | (p[..., w + 1].astype(np.uint64) << np.uint64(32 - off))
+        out[..., i] = (v & np.uint64((1 << bits) - 1)).astype(np.uint8)
+    return out
+
+
+def pack_int4(q: np.ndarray) -> np.ndarray:
+    """4-bit codes ``[..., K]`` into ``uint32 [..., K/8]``, element ``8*w + i``
+    at bits ``4*i``."""
+    return pack_codes(q, 4)
 
 
 def unpack_int4(packed: np.ndarray) -> np.ndarray:
@@ -103,10 +134,13 @@ def unpack_int4(packed: np.ndarray) -> np.ndarray:
     return q.reshape(*p.shape[:-1], p.shape[-1] * 8).astype(np.uint8)
 
 
-def quantize_affine_int4(w: np.ndarray, group: int, scale_dtype: str):
-    """Round-to-nearest int4 affine quantisation of ``w [..., K]`` in groups of
-    ``group`` along the last axis.  Returns ``(q uint8 [..., K], scale, bias)``
-    with scale/bias in storage form ``[..., K/group]``."""
+def quantize_affine(w: np.ndarray, group: int, bits: int, scale_dtype: str):
+    """Round-to-nearest b-bit affine quantisation of ``w [..., K]`` in groups of
+    ``group`` along the last axis: bias = group min, scale = (max - min) /
+    (2^b - 1), both rounded to the scale dtype, q = clip(rint((w - bias) /
+    scale), 0, 2^b - 1).  Returns ``(q uint8 [..., K], scale, bias)`` with
+    scale/bias in storage form ``[..., K/group]``."""
+    levels = (1 << bits) - 1
     w = np.asarray(w, dtype=np.float64)
     K = w.shape[-1]
     if K % group:
@@ -115,13 +149,18 @@ def quantize_affine_int4(w: np.ndarray, group: int, scale_dtype: str):
     lo = wg.min(axis=-1)
     hi = wg.max(axis=-1)
     bias_st = _round_to_dtype(lo, scale_dtype)
-    scale_st = _round_to_dtype((hi - lo) / 15.0, scale_dtype)
+    scale_st = _round_to_dtype((hi - lo) / float(levels), scale_dtype)
     b = _storage_to_f64(bias_st, scale_dtype)[..., None]
     s = _storage_to_f64(scale_st, scale_dtype)[..., None]
     with np.errstate(divide="ignore", invalid="ignore"):
         qf = np.where(s > 0, np.rint((wg - b) / np.where(s > 0, s, 1.0)), 0.0)
-    q = np.clip(qf, 0, 15).astype(np.uint8).reshape(w.shape)
+    q = np.clip(qf, 0, levels).astype(np.uint8).reshape(w.shape)
     return q, scale_st, bias_st
+
+
+def quantize_affine_int4(w: np.ndarray, group: int, scale_dtype: str):
+    """:func:`quantize_affine` with 4-bit codes."""
+    return quantize_affine(w, group, 4, scale_dtype)
 
 
 # ---------------------------------------------------------------------------
@@ -149,6 +188,7 @@ class LayerSpec:
     router_dtype: str = "bf16"  # router weight
     weight_std: float = 0.02
     bias_std: float = 0.01
+    bits: int = 4               # expert code width (3, 4 or 8)
 
     @property
     def k_in(self) -> int:
@@ -261,23 +301,25 @@ def _quant_expert_exact(rng, E, N, K, spec: LayerSpec):
     G = spec.group_size
     for e in range(E):
         w = rng.normal(0.0, spec.weight_std, size=(N, K))
-        q, s, b = quantize_affine_int4(w, G, spec.scale_dtype)
+        q, s, b = quantize_affine(w, G, spec.bits, spec.scale_dtype)
         if s_all is None:
             s_all = np.empty((E,) + s.shape, dtype=s.dtype)
             b_all = np.empty((E,) + b.shape, dtype=b.dtype)
         q_all[e], s_all[e], b_all[e] = q, s, b
-    return pack_int4(q_all), s_all, b_all
+    return pack_codes(q_all, spec.bits), s_all, b_all
 
 
 def _quant_expert_direct(rng, E, N, K, spec: LayerSpec):
-    """Draw packed codes uniformly (each nibble uniform on 0..15) and per-group
-    scale/bias so that the reconstructed weights have mean ~0 and standard
-    deviation ~weight_std (a uniform code has std 15/sqrt(12) ~= 4.33 steps)."""
+    """Draw packed codes uniformly (uniform bits: each code uniform on
+    0..2^b-1) and per-group scale/bias so that the reconstructed weights have
+    mean ~0 and standard deviation ~weight_std (a uniform b-bit code has std
+    (2^b - 1)/sqrt(12) steps; 4.33 for b = 4)."""
     G = spec.group_size
-    words = rng.integers(0, 1 << 32, size=(E, N, K // 8), dtype=np.uint32)
-    step = spec.weight_std / (15.0 / np.sqrt(12.0))
+    levels = (1 << spec.bits) - 1
+    words = rng.integers(0, 1 << 32, size=(E, N, K * spec.bits // 32), dtype=np.uint32)
+    step = spec.weight_std / (levels / np.sqrt(12.0))
     sg = np.abs(step * (1.0 + 0.1 * rng.standard_normal(size=(E, N, K // G))))
-    bg = -7.5 * sg + 0.1 * spec.weight_std * rng.standard_normal(size=(E, N, K // G))
+    bg = -0.5 * levels * sg + 0.1 * spec.weight_std * rng.standard_normal(size=(E, N, K // G))
     return words, _round_to_dtype(sg, spec.scale_dtype), _round_to_dtype(bg, spec.scale_dtype)
 
 
@@ -363,4 +405,4 @@ def ROUTED_BYTES(spec: LayerSpec) -> int:
     per_in = spec.expert_ffn * spec.k_in          # up (and gate) elements
     per_down = spec.k_in * spec.expert_ffn
     elems = n_mats_in * per_in + per_down
-    return elems // 2 + 2 * sb * (elems // spec.group_size)
+    return elems * spec.bits // 8 + 2 * sb * (elems // spec.group_size)

@@ -1,10 +1,10 @@
-"""fp64 CPU oracle for the decode-time forward of a routed MoE layer with int4
-affine group-quantised experts.
+"""fp64 CPU oracle for the decode-time forward of a routed MoE layer with b-bit
+(3, 4 or 8) affine group-quantised experts.
 
 TEST INFRASTRUCTURE ONLY.  Nothing in the library imports this module; only the
 tests, the smoke check and the benchmark's CPU-baseline leg call it.  It shares
 no code with the CUDA path: it decodes the storage formats itself (bf16 bits,
-packed nibbles), and every step is the plain definition written out in float64,
+packed codes), and every step is the plain definition written out in float64,
 one token row at a time, with no blocking, fusion or reordering.
 
 Sources (page titles and sections):
@@ -17,14 +17,16 @@ Sources (page titles and sections):
   "Checklist": an fp32 router with sigmoid top-8 and a per-expert
   normalisation and sum; fp16 activations with fp32 sums.
 * mlx-bun decode-speed program, weight-format table and the affine shared-M
-  section: MLX affine quantisation, packed codes with a scale and a bias per
-  group (group sizes 32/64/128).
+  section: MLX affine quantisation, packed codes of 2..8 bits with a scale
+  and a bias per group (group sizes 32/64/128).
 
 Where the pages leave a step open, the readings are:
 
-1. affine dequantisation is ``w = scale * q + bias`` with unsigned codes
-   ``q in 0..15`` and groups of G consecutive elements along the input axis;
-2. packed storage: eight codes per uint32, lowest nibble first;
+1. affine dequantisation is ``w = scale * q + bias`` with unsigned b-bit codes
+   ``q in 0..2^b-1`` (b = 3, 4 or 8) and groups of G consecutive elements
+   along the input axis;
+2. packed storage: the codes of a row as one little-endian bit stream of
+   uint32 words (for b = 4: eight codes per word, lowest nibble first);
 3. the router bias only steers *selection* (key = sigmoid(z) + bias); the
    combine weights use sigmoid(z) without it;
 4. weights are normalised over the selected set first, then multiplied by the
@@ -68,21 +70,24 @@ def widen(a: np.ndarray, dtype: str) -> np.ndarray:
     raise ValueError(f"unknown storage dtype {dtype!r}")
 
 
-def unpack_codes(packed: np.ndarray) -> np.ndarray:
-    """uint32 words -> 4-bit codes, element ``8*w + i`` from bits ``4*i``."""
-    p = np.asarray(packed, dtype=np.uint64)
-    codes = np.empty(p.shape + (8,), dtype=np.int64)
-    for i in range(8):
-        codes[..., i] = (p >> np.uint64(4 * i)) & np.uint64(15)
-    return codes.reshape(*p.shape[:-1], p.shape[-1] * 8)
+def unpack_codes(packed: np.ndarray, bits: int = 4) -> np.ndarray:
+    """uint32 words -> b-bit codes.  The words of a row are one little-endian
+    bit stream (bit j of word w is stream bit 32*w + j) and code ``i`` is the
+    unsigned integer in stream bits ``b*i .. b*i+b-1``, lowest bit first
+    (reading 2: for b = 4, element ``8*w + i`` in bits ``4*i``)."""
+    p = np.ascontiguousarray(np.asarray(packed, dtype="<u4"))
+    stream = np.unpackbits(p.view(np.uint8), axis=-1, bitorder="little")
+    n = stream.shape[-1] // bits
+    digits = stream[..., : n * bits].reshape(*p.shape[:-1], n, bits).astype(np.int64)
+    return (digits << np.arange(bits, dtype=np.int64)).sum(axis=-1)
 
 
 def dequantize(packed: np.ndarray, scale: np.ndarray, bias: np.ndarray, group: int,
-               scale_dtype: str) -> np.ndarray:
-    """Affine int4 dequantisation ``w[n, k] = scale[n, k // G] * q[n, k] +
+               scale_dtype: str, bits: int = 4) -> np.ndarray:
+    """Affine b-bit dequantisation ``w[n, k] = scale[n, k // G] * q[n, k] +
     bias[n, k // G]`` in float64 (mlx-bun decode-speed program, affine
-    weight format; reading 1)."""
-    q = unpack_codes(packed).astype(np.float64)
+    weight formats of 2..8 bits; reading 1)."""
+    q = unpack_codes(packed, bits).astype(np.float64)
     s = widen(scale, scale_dtype)
     b = widen(bias, scale_dtype)
     K = q.shape[-1]
@@ -199,10 +204,10 @@ class _ExpertCache:
     def get(self, e: int):
         if e not in self.mats:
             L, sp = self.layer, self.spec
-            G, sd = sp.group_size, sp.scale_dtype
-            up = dequantize(L.up_q[e], L.up_s[e], L.up_b[e], G, sd)
-            gate = dequantize(L.gate_q[e], L.gate_s[e], L.gate_b[e], G, sd) if sp.gated else None
-            down = dequantize(L.down_q[e], L.down_s[e], L.down_b[e], G, sd)
+            G, sd, nb = sp.group_size, sp.scale_dtype, getattr(sp, "bits", 4)
+            up = dequantize(L.up_q[e], L.up_s[e], L.up_b[e], G, sd, nb)
+            gate = dequantize(L.gate_q[e], L.gate_s[e], L.gate_b[e], G, sd, nb) if sp.gated else None
+            down = dequantize(L.down_q[e], L.down_s[e], L.down_b[e], G, sd, nb)
             size = up.nbytes + down.nbytes + (gate.nbytes if gate is not None else 0)
             while self.mats and self.bytes + size > self.max_bytes:
                 old = next(iter(self.mats))

@@ -127,6 +127,25 @@ __device__ __forceinline__ float eb_dot32(const uint4 w, const float (&x)[32]) {
   return s;
 }
 
+// The 32 codes of a chunk as the floats 1 + q/16 (element order).
+__device__ __forceinline__ void eb_decode32(const uint4 w, float (&q)[32]) {
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t v = ws[i];
+    q[8 * i + 0] = nib<0>(v); q[8 * i + 1] = nib<1>(v); q[8 * i + 2] = nib<2>(v); q[8 * i + 3] = nib<3>(v);
+    q[8 * i + 4] = nib<4>(v); q[8 * i + 5] = nib<5>(v); q[8 * i + 6] = nib<6>(v); q[8 * i + 7] = nib<7>(v);
+  }
+}
+
+// eb_dot32 on decoded codes: the same single chain in element order.
+__device__ __forceinline__ float eb_dot32f(const float (&q)[32], const float (&x)[32]) {
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) s = fmaf(q[i], x[i], s);
+  return s;
+}
+
 template <int PB, int R, bool GATED>
 __global__ void __launch_bounds__(NT, 2) k_expert_bulk(const __grid_constant__ ExpertArgs A) {
   extern __shared__ __align__(128) unsigned char eb_smem_raw[];
@@ -164,7 +183,11 @@ __global__ void __launch_bounds__(NT, 2) k_expert_bulk(const __grid_constant__ E
   const int pa = uniq_p0[u], pe = uniq_p0[u + 1];
   const int ngroups = (ne - nb + GR - 1) / GR;
   const int nbatch = (pe - pa + PB - 1) / PB;
-  const int total = ngroups * nbatch;   // groups streamed (the weights once per pair batch)
+  // when the ring holds all of the CTA's groups they stay resident and every
+  // pair batch reuses them (each weight byte read once); otherwise the groups
+  // are streamed again per batch
+  const bool resident = nst >= ngroups;
+  const int total = resident ? ngroups : ngroups * nbatch;
   cta_stamp(A.trace, 4);
 
   // group g -> stage g % nst: per matrix the codes [rows, K/2], then the 16-byte
@@ -213,8 +236,8 @@ __global__ void __launch_bounds__(NT, 2) k_expert_bulk(const __grid_constant__ E
     eb_stage_pairs<PB>(A, pairs, pc, np, xs4, xsum);
     if (b == 0) cta_stamp(A.trace, 6);
     for (int t = 0; t < ngroups; ++t, ++g) {
-      const int s = g % nst;
-      if (ok && !eb_wait(eb_smem(bars + s), static_cast<uint32_t>(g / nst) & 1u)) {
+      const int s = resident ? t : g % nst;
+      if (ok && (!resident || b == 0) && !eb_wait(eb_smem(bars + s), static_cast<uint32_t>(g / nst) & 1u)) {
         ok = false;
         g_fail = g;
         if (threadIdx.x == 0) atomicOr(A.status, STATUS_TIMEOUT);
@@ -244,6 +267,9 @@ __global__ void __launch_bounds__(NT, 2) k_expert_bulk(const __grid_constant__ E
               float sc, bi;
               sb_decode(reinterpret_cast<const uint32_t*>(d + P.q_bytes)[sb_w0 + rl * ngr + gi], s_dt, sc, bi);
               const float s16 = 16.f * sc, bb = bi - s16;
+              // the 32 codes as floats 1 + q/16, once for all the pairs
+              float qf[32];
+              eb_decode32(w, qf);
 #pragma unroll
               for (int pp = 0; pp < PB; ++pp) {
                 if (pp < np) {
@@ -257,7 +283,7 @@ __global__ void __launch_bounds__(NT, 2) k_expert_bulk(const __grid_constant__ E
                     xr[4 * i] = a4.x; xr[4 * i + 1] = a4.y; xr[4 * i + 2] = a4.z; xr[4 * i + 3] = a4.w;
                   }
                   float& dst = (m == 1) ? accg[pp] : acc[pp];
-                  dst = fmaf(s16, eb_dot32(w, xr), fmaf(bb, xsum[pp * nchunk + c], dst));
+                  dst = fmaf(s16, eb_dot32f(qf, xr), fmaf(bb, xsum[pp * nchunk + c], dst));
                 }
               }
             }
@@ -283,7 +309,7 @@ __global__ void __launch_bounds__(NT, 2) k_expert_bulk(const __grid_constant__ E
       }
       if (g == 0) cta_stamp(A.trace, 8);
       __syncthreads();   // stage s is free
-      if (threadIdx.x == 0 && ok && g + nst < total) issue(issued++);
+      if (threadIdx.x == 0 && ok && !resident && g + nst < total) issue(issued++);
     }
   }
   cta_stamp(A.trace, 2);

@@ -123,6 +123,7 @@ struct moe_layer {
   int debug_route = 0;    // diagnostics: print routing phase times
   int expert_bulk = 1;    // gemv path: expert kernels with bulk-copied weight tiles (k_expert_bulk)
   int expert_bulk_max_t = 2;   // the bulk expert kernel up to this many rows
+  int expert_bulk_pb = 2;      // its token pairs per pass
   int dense_bulk = 1;     // gemv path: shared expert and output projection by k_dense_bulk
   int fill = 0;           // gemv path: the shared expert as launches of its own beside the routed chain
   int fill_ctas = 0;      // those CTAs per launch (0: one per SM)
@@ -667,6 +668,8 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   if (const char* env = std::getenv("MOE_EXPERT_BULK")) L->expert_bulk = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_DENSE_BULK")) L->dense_bulk = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_EXPERT_BULK_MAX_T")) L->expert_bulk_max_t = std::max(0, std::atoi(env));
+  if (const char* env = std::getenv("MOE_EXPERT_BULK_PB"))
+    L->expert_bulk_pb = std::max(1, std::min(8, pow2_at_least(std::atoi(env), 8)));
   if (const char* env = std::getenv("MOE_FILL")) L->fill = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_FILL_CTAS")) L->fill_ctas = std::max(0, std::atoi(env));
   if (const char* env = std::getenv("MOE_ROUTE_WARM")) L->route_warm = std::atoi(env) != 0;
@@ -1231,9 +1234,12 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
   EbLaunch eb_up, eb_dn;
   int cps_up = 1, cps_dn = 1;
   const int slots_e = std::min(E, T * k);   // distinct-expert slots of the expert launches
-  const bool bulk_up = use_bulk && eb_choose(kin, c.group_size, gated, pow2_at_least(T, 8), F, slots_e,
+  // pairs per pass: a distinct expert of a small batch holds one or two of its
+  // rows, and its weights stay resident in the ring across passes
+  const int eb_pb = std::min(pow2_at_least(T, 8), h->expert_bulk_pb);
+  const bool bulk_up = use_bulk && eb_choose(kin, c.group_size, gated, eb_pb, F, slots_e,
                                              h->num_sms, &eb_up, &cps_up);
-  const bool bulk_dn = use_bulk && eb_choose(F, c.group_size, false, pow2_at_least(T, 8), kin, slots_e,
+  const bool bulk_dn = use_bulk && eb_choose(F, c.group_size, false, eb_pb, kin, slots_e,
                                              h->num_sms, &eb_dn, &cps_dn);
   // the filler CTAs stage PB token rows of the dense rows' input: their shared
   // memory must fit beside the plan's CTAs per SM

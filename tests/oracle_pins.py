@@ -36,7 +36,10 @@ TINY_FP16 = mi.LayerSpec(name="t_fp16", hidden=24, n_experts=6, top_k=3, expert_
                          act_dtype="fp16", scale_dtype="fp16", router_dtype="fp32",
                          weight_std=0.3)
 TINY_UNNORM = TINY_SOFTMAX.with_(name="t_unnorm", renormalize=False, n_experts=5, top_k=3)
-TINY_SPECS = (TINY_SOFTMAX, TINY_LATENT, TINY_FP16, TINY_UNNORM)
+# 3- and 8-bit expert codes (rows of K codes fill whole words: K * bits % 32 == 0)
+TINY_B3 = TINY_SOFTMAX.with_(name="t_b3", hidden=32, expert_ffn=32, bits=3)
+TINY_B8 = TINY_LATENT.with_(name="t_b8", bits=8)
+TINY_SPECS = (TINY_SOFTMAX, TINY_LATENT, TINY_FP16, TINY_UNNORM, TINY_B3, TINY_B8)
 
 
 def _rel(a, b):
@@ -53,7 +56,9 @@ def _layer_and_x(spec, seed=0, T=3):
 # --- storage ---------------------------------------------------------------
 
 def pin_unpack_fixture(ora):
-    """Nibble order of packed words against hand-written words."""
+    """Code order of packed words against hand-written words: 4-bit codes
+    (int4_words.txt) and 3-bit and 8-bit codes (packed_words.txt, codes that
+    straddle two words included)."""
     with open(os.path.join(GOLDEN, "int4_words.txt")) as f:
         for line in f:
             line = line.split("#")[0].split()
@@ -63,6 +68,21 @@ def pin_unpack_fixture(ora):
             want = [int(v) for v in line[1:]]
             got = ora.unpack_codes(word).tolist()
             assert got == want, (line[0], got, want)
+    n = 0
+    with open(os.path.join(GOLDEN, "packed_words.txt")) as f:
+        for line in f:
+            line = line.split("#")[0]
+            if not line.strip():
+                continue
+            head, codes = line.split("|")
+            head = head.split()
+            bits = int(head[0])
+            words = np.array([int(v, 16) for v in head[1:]], dtype=np.uint32)
+            want = [int(v) for v in codes.split()]
+            got = ora.unpack_codes(words, bits).tolist()
+            assert got == want, (bits, head[1:], got, want)
+            n += 1
+    assert n >= 7
 
 
 def pin_dequant_closed_form(ora):
@@ -85,6 +105,51 @@ def pin_dequant_closed_form(ora):
     for n in range(N):
         for kk in range(K):
             assert got[n, kk] == (kk % 16) * scale[n, kk // G] + bias[n, kk // G]
+
+
+def pin_dequant_closed_form_bits(ora):
+    """3- and 8-bit codes: code 0 -> bias, the top code 2^b - 1 -> (2^b - 1)*scale +
+    bias, every element on its own group's scale and bias."""
+    N, K, G = 2, 64, 32
+    ng = K // G
+    scale = np.array([[0.25 * (g + 1) + n for g in range(ng)] for n in range(N)])
+    bias = np.array([[-(g + 1) * 0.5 - n for g in range(ng)] for n in range(N)])
+    s_st, b_st = mi.round_to_bf16_bits(scale), mi.round_to_bf16_bits(bias)
+    for bits in (3, 8):
+        top = (1 << bits) - 1
+        for code in (0, 1, top // 2, top):
+            packed = mi.pack_codes(np.full((N, K), code, dtype=np.uint8), bits)
+            got = ora.dequantize(packed, s_st, b_st, G, "bf16", bits)
+            for n in range(N):
+                for kk in range(K):
+                    assert got[n, kk] == code * scale[n, kk // G] + bias[n, kk // G], (bits, code)
+        codes = np.array([[(7 * kk + n) % (top + 1) for kk in range(K)] for n in range(N)], dtype=np.uint8)
+        got = ora.dequantize(mi.pack_codes(codes, bits), s_st, b_st, G, "bf16", bits)
+        for n in range(N):
+            for kk in range(K):
+                assert got[n, kk] == codes[n, kk] * scale[n, kk // G] + bias[n, kk // G]
+
+
+def pin_quant_roundtrip_bits(ora):
+    """3- and 8-bit: the generator's quantiser applied to the oracle's
+    dequantised weights gives back the same codes where a group holds both end
+    codes (its min/max reproduce scale and bias), and the error of a round trip
+    is at most half a step plus the scale/bias storage rounding."""
+    rng = np.random.Generator(np.random.PCG64(21))
+    for bits, sdt, G, eps in ((3, "bf16", 64, 2.0 ** -8), (8, "fp16", 32, 2.0 ** -11)):
+        top = (1 << bits) - 1
+        w = rng.normal(0, 0.02, size=(6, 256))
+        q, s, b = mi.quantize_affine(w, G, bits, sdt)
+        deq = ora.dequantize(mi.pack_codes(q, bits), s, b, G, sdt, bits)
+        qg = q.reshape(6, 256 // G, G)
+        keep = (qg.min(-1) == 0) & (qg.max(-1) == top)
+        q2, _, _ = mi.quantize_affine(deq, G, bits, sdt)
+        assert keep.mean() > 0.9
+        assert np.array_equal(q2.reshape(6, 256 // G, G)[keep], qg[keep])
+        sf = np.repeat(mi.bf16_bits_to_f32(s) if sdt == "bf16" else s.astype(np.float64), G, -1)
+        bf = np.repeat(mi.bf16_bits_to_f32(b) if sdt == "bf16" else b.astype(np.float64), G, -1)
+        bound = sf / 2 + top * eps * np.abs(sf) + eps * np.abs(bf) + 1e-12
+        assert np.all(np.abs(w - deq) <= bound)
 
 
 def pin_quant_roundtrip(ora):

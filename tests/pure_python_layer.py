@@ -1,7 +1,7 @@
 """Brute-force pure-Python forward of a *tiny* MoE layer, used to pin the oracle.
 
 Written independently of ``oracle/``: plain Python ints and floats, explicit
-loops, its own storage decoding (struct for bf16 bits, shifts for nibbles), a
+loops, its own storage decoding (struct for bf16 bits, shifts for codes), a
 selection by exhaustive search over all k-subsets, and exact-order sums.  It is
 only meant for layers with a handful of experts and rows of a few dozen
 elements.
@@ -28,14 +28,16 @@ def _matrix(arr, dtype):
         [[_bf16(v) for v in row] for row in arr.tolist()]
 
 
-def _deq(words, scale, bias, G, sdt):
-    """One expert matrix: words [N][K/8] -> [N][K] floats."""
+def _deq(words, scale, bias, G, sdt, bits=4):
+    """One expert matrix: words [N][K*bits/32] -> [N][K] floats.  The row's
+    words are one integer, word w at bit 32*w; code i is bits bits*i.. of it."""
     rows = []
     for n, wrow in enumerate(words.tolist()):
-        codes = []
-        for w in wrow:
-            for i in range(8):
-                codes.append((int(w) >> (4 * i)) & 0xF)
+        big = 0
+        for w_i, w in enumerate(wrow):
+            big |= int(w) << (32 * w_i)
+        K = 32 * len(wrow) // bits
+        codes = [(big >> (bits * i)) & ((1 << bits) - 1) for i in range(K)]
         srow = scale[n].tolist()
         brow = bias[n].tolist()
         rows.append([_val(srow[kk // G], sdt) * codes[kk] + _val(brow[kk // G], sdt)
@@ -80,9 +82,10 @@ def forward(layer, x):
     W2 = _matrix(layer.fc2, adt) if sp.latent else None
     experts = []
     for e in range(sp.n_experts):
-        up = _deq(layer.up_q[e], layer.up_s[e], layer.up_b[e], G, sdt)
-        gate = _deq(layer.gate_q[e], layer.gate_s[e], layer.gate_b[e], G, sdt) if sp.gated else None
-        down = _deq(layer.down_q[e], layer.down_s[e], layer.down_b[e], G, sdt)
+        nb = getattr(sp, "bits", 4)
+        up = _deq(layer.up_q[e], layer.up_s[e], layer.up_b[e], G, sdt, nb)
+        gate = _deq(layer.gate_q[e], layer.gate_s[e], layer.gate_b[e], G, sdt, nb) if sp.gated else None
+        down = _deq(layer.down_q[e], layer.down_s[e], layer.down_b[e], G, sdt, nb)
         experts.append((gate, up, down))
     if sp.shared_ffn:
         shu = _matrix(layer.sh_up, adt)

@@ -16,7 +16,10 @@ from tests import oracle_pins
 SRC_PATH = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.py")
 
 MUTANTS = [
-    ("nibble order reversed", "(p >> np.uint64(4 * i))", "(p >> np.uint64(4 * (7 - i)))"),
+    ("bit stream read big-endian", 'axis=-1, bitorder="little")', 'axis=-1, bitorder="big")'),
+    ("code bits reversed", "(digits << np.arange(bits, dtype=np.int64))",
+     "(digits << np.arange(bits, dtype=np.int64)[::-1])"),
+    ("code width ignored", "n = stream.shape[-1] // bits\n", "bits = 4\n    n = stream.shape[-1] // bits\n"),
     ("dequant drops bias", "return s_full * q + b_full", "return s_full * q"),
     ("group index k % groups", "s_full = np.repeat(s, group, axis=-1)", "s_full = np.tile(s, group)"),
     ("bias leaks into weights", "w = s[ids]", "w = keys[ids]"),
