@@ -200,13 +200,14 @@ def parse_args():
 # ---------------------------------------------------------------------------
 
 def expert_bytes(spec):
-    """(up-side bytes, down-side bytes) of one routed expert: packed codes +
-    scale + bias (2 bytes each per group)."""
+    """(up-side bytes, down-side bytes) of one routed expert: packed b-bit codes
+    + scale + bias (2 bytes each per group)."""
     n_in = 2 if spec.gated else 1
     e_in = n_in * spec.expert_ffn * spec.k_in
     e_dn = spec.k_in * spec.expert_ffn
     sb = 2 * 2
-    return (e_in // 2 + sb * (e_in // spec.group_size), e_dn // 2 + sb * (e_dn // spec.group_size))
+    b = spec.bits
+    return (e_in * b // 8 + sb * (e_in // spec.group_size), e_dn * b // 8 + sb * (e_dn // spec.group_size))
 
 
 def stage_bytes(spec, T, n_uniq):

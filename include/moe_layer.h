@@ -2,7 +2,7 @@
  * moe_layer.h -- C ABI of the GB300 (sm_103a) quantized MoE decode layer.
  *
  * One handle holds one routed mixture-of-experts layer whose expert weights are
- * 4-bit affine group-quantised.  moe_layer_forward() runs, for every token row,
+ * affine group-quantised to 4 bits (or 3 or 8: moe_layer_config.bits).  moe_layer_forward() runs, for every token row,
  *
  *   router gemv -> softmax/sigmoid top-k -> (fc1_latent_proj) -> per selected
  *   expert: dequant gemv up (+gate), activation, dequant gemv down -> weighted
@@ -14,7 +14,10 @@
  * -> + shared -> + residual), with the fp32 router / sigmoid top-k / per-expert
  * norm and sum of TensorFold PR #1295 (Muse Spark Open, "What this changes"),
  * and MLX-style affine int4 weights (mlx-bun decode-speed program, weight
- * format table: affine, group sizes 32/64/128, a scale and a bias per group).
+ * format table: affine, group sizes 32/64/128, a scale and a bias per group;
+ * 3- and 8-bit affine codes: the same program, section 7.2 "Freeze the
+ * controls and workload matrix", weights row, and section 7.8 "Execution
+ * progress and next measurements", the 3/8-bit affine dispatches).
  *
  * Every call's arithmetic runs in this library's CUDA kernels on the GPU; there
  * is no CPU fallback.  The library serves one GPU (compute capability 10.3).
@@ -23,10 +26,13 @@
  *   - "device pointer": memory of the GPU the handle was created on;
  *     "host pointer": ordinary or pinned host memory.
  *   - Matrices are row-major and contiguous.
- *   - Packed int4 codes: eight 4-bit codes per uint32, element 8*w+i in bits
- *     4*i..4*i+3 (lowest nibble first).  A weight is scale*q + bias, with the
- *     scale and bias of its group of group_size consecutive elements along the
- *     input (reduction) axis.
+ *   - Packed b-bit codes (b = bits: 3, 4 or 8): the codes of a row form one
+ *     little-endian bit stream of uint32 words -- element i occupies stream
+ *     bits b*i..b*i+b-1, stream bit j is bit j%32 of word j/32, so a 3-bit code
+ *     may straddle two words.  For b = 4: eight codes per uint32, element 8*w+i
+ *     in bits 4*i..4*i+3 (lowest nibble first).  A weight is scale*q + bias
+ *     (q unsigned, 0..2^b-1), with the scale and bias of its group of
+ *     group_size consecutive elements along the input (reduction) axis.
  *   - bf16/fp16 buffers hold IEEE/bfloat16 16-bit values.
  *   - Every function returns a moe_status; MOE_OK is 0.  On error nothing that
  *     the call allocated stays allocated, and moe_layer_last_error() (where a
@@ -41,7 +47,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 
 typedef enum moe_status {
   MOE_OK = 0,
@@ -54,7 +60,8 @@ typedef enum moe_status {
   MOE_ERR_OOM = 7,          /* device allocation failed */
   MOE_ERR_CUDA = 8,         /* a CUDA runtime call failed */
   MOE_ERR_TIMEOUT = 9,      /* a bounded device-side wait ran out */
-  MOE_ERR_NONFINITE = 10    /* a router selection key was NaN or infinite */
+  MOE_ERR_NONFINITE = 10,   /* a router selection key was NaN or infinite */
+  MOE_ERR_INDEX = 11        /* MOE_CHECKS builds: a kernel's index check failed */
 } moe_status;
 
 typedef enum moe_act {
@@ -105,6 +112,9 @@ typedef struct moe_layer_config {
   int32_t act_dtype;     /* BF16|FP16: x, out, fc1/fc2 and shared expert weights */
   int32_t scale_dtype;   /* BF16|FP16: expert scales and biases */
   int32_t router_dtype;  /* BF16|FP16|FP32: router weight (x is widened to fp32) */
+  int32_t bits;          /* code width of the routed experts: 3, 4 or 8 (0 = 4).
+                            3- and 8-bit layers run the GEMV schedule only: AUTO
+                            selects it at every T, GROUPED is refused */
 } moe_layer_config;
 
 /* Weights, all DEVICE pointers owned by the caller.  moe_layer_create copies
@@ -114,9 +124,9 @@ typedef struct moe_layer_config {
  *   router_w   [E, H]           router_dtype
  *   router_bias[E]              fp32 (has_router_bias only, else NULL)
  *   fc1_latent [L, H], fc2_latent [H, L]  act_dtype (latent layers only)
- *   gate_q, up_q [E, F, Kin/8]  uint32 packed codes (gate_q: SWIGLU only)
+ *   gate_q, up_q [E, F, Kin*bits/32]  uint32 packed codes (gate_q: SWIGLU only)
  *   gate_s, gate_b, up_s, up_b [E, F, Kin/G]  scale_dtype
- *   down_q     [E, Kin, F/8]    uint32 packed codes
+ *   down_q     [E, Kin, F*bits/32]  uint32 packed codes
  *   down_s, down_b [E, Kin, F/G] scale_dtype
  *   sh_gate, sh_up [shared_ffn, H], sh_down [H, shared_ffn]  act_dtype
  *     (sh_gate for SWIGLU only; all NULL when shared_ffn == 0) */
@@ -134,10 +144,26 @@ typedef struct moe_layer moe_layer;
 /* Library ABI version (MOE_ABI_VERSION of the build). */
 int32_t moe_abi_version(void);
 
+/* How the library was built: bit MOE_BUILD_CHECKS is set in the debug build
+ * (libmoe_gb300_checks.so, compiled with MOE_CHECKS=1).  There, every index a
+ * kernel reads from data -- an expert id, a token-pair id or a pair range taken
+ * from the route metadata -- is checked against its bound before it addresses
+ * memory; a violation is recorded in the device status word (the first one
+ * with its site, index and bound), the access is skipped or redirected to
+ * index 0, and moe_layer_device_status() returns MOE_ERR_INDEX with the site
+ * in moe_layer_last_error().  No kernel traps.  The debug build also opens
+ * NVTX ranges around each forward and each of its stages (bit
+ * MOE_BUILD_NVTX_DEFAULT; in either build the environment variable MOE_NVTX=1
+ * or 0 at moe_layer_create turns them on or off). */
+#define MOE_BUILD_CHECKS 1
+#define MOE_BUILD_NVTX_DEFAULT 2
+int32_t moe_build_flags(void);
+
 /* Host-only validation of a config and of which weight pointers are present,
  * with the same refusals and codes as moe_layer_create; touches no device.
  * `w` may be NULL to check the config alone.  Refusals, in order:
- *   MOE_ERR_INVALID_ARG   null cfg, non-positive sizes, bad enum values
+ *   MOE_ERR_INVALID_ARG   null cfg, non-positive sizes, bad enum values, bits
+ *                         not 0, 3, 4 or 8
  *   MOE_ERR_TOPK_GT_E     top_k < 1 or top_k > n_experts (a layer whose top-k
  *                         exceeds its own expert count is refused before any
  *                         weight is read: TensorFold PR #1038, "What's in it")
@@ -184,12 +210,13 @@ moe_status moe_layer_forward_host(moe_layer *h, const void *x_host, int32_t T, v
                                   void *stream);
 
 /* Choose the routed-expert path for later forwards (A/B testing).  A path this
- * build cannot serve for the layer returns MOE_ERR_UNSUPPORTED. */
+ * build cannot serve for the layer returns MOE_ERR_UNSUPPORTED (GROUPED for a
+ * layer with bits 3 or 8, or with fp32 activations). */
 moe_status moe_layer_set_path(moe_layer *h, int32_t path);
 
 /* Synchronises `stream`, reads and clears the device status word: MOE_OK, or
- * MOE_ERR_NONFINITE / MOE_ERR_TIMEOUT for conditions kernels recorded since
- * the last call. */
+ * MOE_ERR_INDEX / MOE_ERR_TIMEOUT / MOE_ERR_NONFINITE (in that precedence) for
+ * conditions kernels recorded since the last call. */
 moe_status moe_layer_device_status(moe_layer *h, void *stream);
 
 /* Kernel stages of one forward, in launch order: 0 dense projections of x

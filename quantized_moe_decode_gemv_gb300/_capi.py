@@ -14,14 +14,15 @@ from typing import Any, Dict, Optional
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_NAME = "libmoe_gb300.so"
+# MOE_CHECKS=1: the debug build (kernel index checks, NVTX ranges)
+LIB_NAME = "libmoe_gb300_checks.so" if os.environ.get("MOE_CHECKS") == "1" else "libmoe_gb300.so"
 LIB_PATH = os.path.join(_HERE, LIB_NAME)
 
 # enums (include/moe_layer.h)
 MOE_OK = 0
 STATUS_NAMES = ["MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR_TOPK_GT_E",
                 "MOE_ERR_LATENT_PROJ", "MOE_ERR_SHAPE", "MOE_ERR_DEVICE", "MOE_ERR_OOM",
-                "MOE_ERR_CUDA", "MOE_ERR_TIMEOUT", "MOE_ERR_NONFINITE"]
+                "MOE_ERR_CUDA", "MOE_ERR_TIMEOUT", "MOE_ERR_NONFINITE", "MOE_ERR_INDEX"]
 ACT = {"swiglu": 0, "relu2": 1}
 ROUTER = {"softmax": 0, "sigmoid": 1}
 DTYPE = {"bf16": 0, "fp16": 1, "fp32": 2}
@@ -45,7 +46,8 @@ class moe_layer_config(ctypes.Structure):
                 ("act", ctypes.c_int32), ("router", ctypes.c_int32),
                 ("renormalize", ctypes.c_int32), ("routed_scale", ctypes.c_float),
                 ("has_router_bias", ctypes.c_int32), ("act_dtype", ctypes.c_int32),
-                ("scale_dtype", ctypes.c_int32), ("router_dtype", ctypes.c_int32)]
+                ("scale_dtype", ctypes.c_int32), ("router_dtype", ctypes.c_int32),
+                ("bits", ctypes.c_int32)]
 
 
 _WEIGHT_FIELDS = ["router_w", "router_bias", "fc1_latent", "fc2_latent", "gate_q", "up_q",
@@ -60,6 +62,7 @@ class moe_layer_weights(ctypes.Structure):
 # symbol -> (restype, argtypes)
 SIGNATURES = {
     "moe_abi_version": (ctypes.c_int32, []),
+    "moe_build_flags": (ctypes.c_int32, []),
     "moe_layer_validate": (ctypes.c_int, [ctypes.POINTER(moe_layer_config),
                                           ctypes.POINTER(moe_layer_weights)]),
     "moe_layer_create": (ctypes.c_int, [ctypes.POINTER(moe_layer_config),
@@ -143,6 +146,7 @@ class MoEConfig:
     act_dtype: str = "bf16"
     scale_dtype: str = "bf16"
     router_dtype: str = "bf16"
+    bits: int = 4
 
     @classmethod
     def from_spec(cls, spec: Any, max_tokens: int) -> "MoEConfig":
@@ -159,7 +163,7 @@ class MoEConfig:
             router=ROUTER[self.router], renormalize=int(bool(self.renormalize)),
             routed_scale=float(self.routed_scale), has_router_bias=int(bool(self.router_bias)),
             act_dtype=DTYPE[self.act_dtype], scale_dtype=DTYPE[self.scale_dtype],
-            router_dtype=DTYPE[self.router_dtype])
+            router_dtype=DTYPE[self.router_dtype], bits=int(self.bits))
 
 
 def _ptr(t) -> Optional[int]:

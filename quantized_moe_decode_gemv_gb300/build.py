@@ -2,8 +2,12 @@
 
 ``python -m quantized_moe_decode_gemv_gb300.build`` (or ``build()``) compiles
 each translation unit in parallel and links ``libmoe_gb300.so`` next to this
-file.  Only nvcc and the host C++ compiler are needed (no cmake, no torch
-extension machinery).
+file, and beside it the debug build ``libmoe_gb300_checks.so`` (the same
+sources compiled with ``-DMOE_CHECKS=1``: kernels check the indices they read
+from data and record violations in the status word; NVTX ranges on).  The
+binding loads the debug build when ``MOE_CHECKS=1`` is set in the environment.
+Only nvcc and the host C++ compiler are needed (no cmake, no torch extension
+machinery).
 """
 from __future__ import annotations
 
@@ -19,6 +23,9 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libmoe_gb300.so")
+LIB_CHECKS = os.path.join(HERE, "libmoe_gb300_checks.so")
+# (library, object directory, extra flags) of each variant
+VARIANTS = [(LIB, BUILD_DIR, []), (LIB_CHECKS, os.path.join(BUILD_DIR, "checks"), ["-DMOE_CHECKS=1"])]
 
 # (source, object name, extra flags)
 SOURCES = [("moe_layer.cu", "moe_layer", []), ("moe_noalloc.cu", "moe_noalloc", [])]
@@ -41,20 +48,26 @@ def _run(cmd):
     return r.stdout + r.stderr
 
 
-def build(verbose: bool = False) -> str:
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(verbose: bool = False, checks: bool = True) -> str:
+    """Compile and link the library (and, with ``checks``, its debug build);
+    returns the path of the default library."""
     nvcc = _nvcc()
-    objs, cmds = [], []
-    for src, name, extra in SOURCES:
-        obj = os.path.join(BUILD_DIR, name + ".o")
-        objs.append(obj)
-        cmds.append([nvcc, *ARCH, *FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-c",
-                     os.path.join(CSRC, src), "-o", obj])
+    cmds, links = [], []
+    for lib, odir, vflags in (VARIANTS if checks else VARIANTS[:1]):
+        os.makedirs(odir, exist_ok=True)
+        objs = []
+        for src, name, extra in SOURCES:
+            obj = os.path.join(odir, name + ".o")
+            objs.append(obj)
+            cmds.append([nvcc, *ARCH, *FLAGS, *vflags, *extra, "-I", INCLUDE, "-I", CSRC, "-c",
+                         os.path.join(CSRC, src), "-o", obj])
+        links.append((lib, objs))
     with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, len(cmds))) as ex:
         logs = list(ex.map(_run, cmds))
-    tmp = LIB + ".tmp"
-    logs.append(_run([nvcc, *ARCH, "-shared", "-o", tmp, *objs]))
-    os.replace(tmp, LIB)
+    for lib, objs in links:
+        tmp = lib + ".tmp"
+        logs.append(_run([nvcc, *ARCH, "-shared", "-o", tmp, *objs]))
+        os.replace(tmp, lib)
     if verbose:
         sys.stdout.write("".join(logs))
     return LIB

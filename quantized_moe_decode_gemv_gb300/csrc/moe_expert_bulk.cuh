@@ -80,7 +80,8 @@ __device__ __forceinline__ void eb_stage_pairs(const ExpertArgs& A, const int* p
     const int pp = i / K4, f4 = i - pp * K4;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (pp < np) {
-      const int pid = pairs[pc + pp];
+      int pid = pairs[pc + pp];
+      if (!idx_ok(A.status, CK_BULK_PAIR, pid, static_cast<long long>(A.T) * A.k)) pid = 0;
       const int64_t row = A.xin_by_pair ? pid : (pid / A.k);
       const int64_t base = A.xin_off + row * A.xin_stride + 4 * f4;
       if (A.xin_dt == DT_FP32) {
@@ -179,9 +180,12 @@ __global__ void __launch_bounds__(NT, 2) k_expert_bulk(const __grid_constant__ E
   griddep_launch();
   if (!A.pre_wait_phase) cta_stamp(A.trace, 1);
   if (u >= A.meta[0]) { cta_stamp(A.trace, 3); return; }
-  const int64_t e = uniq_e[u];
-  const int pa = uniq_p0[u], pe = uniq_p0[u + 1];
-  const int ngroups = (ne - nb + GR - 1) / GR;
+  // a bad expert id (index checks) copies nothing and writes nothing
+  const bool e_ok = idx_ok(A.status, CK_BULK_E, uniq_e[u], A.n_experts) &&
+                    range_ok(A.status, uniq_p0[u], uniq_p0[u + 1], static_cast<long long>(A.T) * A.k);
+  const int64_t e = e_ok ? uniq_e[u] : 0;
+  const int pa = uniq_p0[u], pe = e_ok ? uniq_p0[u + 1] : pa;
+  const int ngroups = e_ok ? (ne - nb + GR - 1) / GR : 0;
   const int nbatch = (pe - pa + PB - 1) / PB;
   // when the ring holds all of the CTA's groups they stay resident and every
   // pair batch reuses them (each weight byte read once); otherwise the groups
@@ -302,7 +306,8 @@ __global__ void __launch_bounds__(NT, 2) k_expert_bulk(const __grid_constant__ E
             if (pp < np) {
               const int pid = pairs[pc + pp];
               const float val = (A.act >= 0) ? act_fn(A.act, other, tot) : tot;
-              A.out[static_cast<int64_t>(pid) * A.n_rows + r0 + rl] = val;
+              if (idx_ok(A.status, CK_BULK_PAIR, pid, static_cast<long long>(A.T) * A.k))
+                A.out[static_cast<int64_t>(pid) * A.n_rows + r0 + rl] = val;
             }
           }
         }

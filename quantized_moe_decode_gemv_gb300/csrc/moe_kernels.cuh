@@ -52,7 +52,66 @@ constexpr int MAX_K = 16;     // top-k served
 enum : int { DT_BF16 = 0, DT_FP16 = 1, DT_FP32 = 2 };
 enum : int { ACT_SWIGLU = 0, ACT_RELU2 = 1 };
 enum : int { ROUTER_SOFTMAX = 0, ROUTER_SIGMOID = 1 };
-enum : int { STATUS_NONFINITE = 1, STATUS_TIMEOUT = 2 };
+enum : int { STATUS_NONFINITE = 1, STATUS_TIMEOUT = 2, STATUS_INDEX = 4 };
+
+// ---------------------------------------------------------------------------
+// index checks (builds with MOE_CHECKS=1)
+// ---------------------------------------------------------------------------
+// The indices a kernel reads from data -- an expert id or a token-pair id taken
+// from the route metadata -- are checked against their bound before they
+// address memory.  A violation sets STATUS_INDEX in status word 0 and the first
+// one stores (site, index, bound) in words 1..3; the caller then skips the
+// access or substitutes index 0, so the kernel neither traps nor reads outside
+// a buffer.  Every other index of these kernels is a loop counter over launch
+// sizes checked on the host.  In the default build a check is `true`.
+#ifndef MOE_CHECKS
+#define MOE_CHECKS 0
+#endif
+enum : int {
+  CK_EXPERT_E = 1,     // k_expert: distinct expert id
+  CK_EXPERT_PAIR = 2,  // k_expert: pair id of a staged input / output row
+  CK_BULK_E = 3,       // k_expert_bulk: distinct expert id
+  CK_BULK_PAIR = 4,    // k_expert_bulk: pair id
+  CK_GATHER_PAIR = 5,  // k_gather_pairs: pair id
+  CK_UMMA_E = 6,       // grouped GEMMs: expert id of a group
+  CK_UMMA_PAIR = 7,    // grouped GEMMs: pair id of a token slot
+  CK_PREFETCH_E = 8,   // routing CTA: expert id of an L2 prefetch
+  CK_SLOT_RANGE = 9    // pair range [p0, p1) of a distinct expert outside [0, T*k]
+};
+
+#if MOE_CHECKS
+static __device__ __noinline__ void check_fail(int* status, int site, long long idx, long long bound) {
+  if (!status) return;
+  atomicOr(status, STATUS_INDEX);
+  if (atomicCAS(status + 1, 0, site) == 0) {
+    status[2] = static_cast<int>(idx);
+    status[3] = static_cast<int>(bound);
+  }
+}
+#endif
+
+__device__ __forceinline__ bool idx_ok(int* status, int site, long long idx, long long bound) {
+#if MOE_CHECKS
+  if (idx >= 0 && idx < bound) return true;
+  check_fail(status, site, idx, bound);
+  return false;
+#else
+  (void)status; (void)site; (void)idx; (void)bound;
+  return true;
+#endif
+}
+
+// a distinct expert's pair range: 0 <= p0 <= p1 <= n_pairs
+__device__ __forceinline__ bool range_ok(int* status, long long p0, long long p1, long long n_pairs) {
+#if MOE_CHECKS
+  if (p0 >= 0 && p0 <= p1 && p1 <= n_pairs) return true;
+  check_fail(status, CK_SLOT_RANGE, p0 < 0 || p0 > p1 ? p0 : p1, n_pairs + 1);
+  return false;
+#else
+  (void)status; (void)p0; (void)p1; (void)n_pairs;
+  return true;
+#endif
+}
 
 // ---------------------------------------------------------------------------
 // small helpers
@@ -211,6 +270,9 @@ struct RouteArgs {
   int max_w;             // route_block: most warps sharing a row's keys (1..8)
   int dry;               // 1: run the top-k code without writing anything (warms the
                          // instruction cache and the bias lines before the logits exist)
+  int debug_bad;         // MOE_CHECKS builds, few-pair lists only: plant an out-of-range
+                         // index in the metadata (1: first expert id = E + 3, 2: first
+                         // pair id = T*k + 5) for the consumers' checks to catch
 };
 
 __device__ __forceinline__ unsigned long long global_ns() {
@@ -487,6 +549,10 @@ static __device__ __noinline__ void route_block(const RouteArgs& A, int* smem) {
         if (open) { uniq_e[u] = v >> 5; uniq_p0[u] = lane; }
         if (valid) pairs[lane] = v & 31;
         if (lane == 0) { A.meta[0] = __popc(om); uniq_p0[__popc(om)] = P; }
+#if MOE_CHECKS
+        if (lane == 0 && A.debug_bad == 1) uniq_e[0] = A.E + 3;
+        if (lane == 0 && A.debug_bad == 2) pairs[0] = P + 5;
+#endif
       }
     }
     if (A.debug_times && tid == 0)
@@ -1109,6 +1175,7 @@ __global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_in(const _
         const int nmax = static_cast<int>(nu < cap ? nu : cap);
         for (int u = threadIdx.x; u < nmax; u += blockDim.x) {
           const int64_t e = A.route.meta[1 + u];
+          if (!idx_ok(A.route.status, CK_PREFETCH_E, e, A.route.E)) continue;
           prefetch_l2(reinterpret_cast<const char*>(A.pf_q) + e * A.pf_q_bytes, A.pf_q_bytes);
           prefetch_l2(reinterpret_cast<const char*>(A.pf_sb) + e * A.pf_sb_bytes, A.pf_sb_bytes);
           if (A.pf_q2) {
@@ -1233,7 +1300,7 @@ struct ExpertArgs {
   int n_rows;              // output rows per expert
   int K;                   // reduction length
   int G;                   // group size
-  const uint32_t* q;       // [E, n_rows, K/8]
+  const uint32_t* q;       // [E, n_rows, K*bits/32] (bits: k_expert's code width)
   const uint32_t* sb;      // [E, n_rows, K/G]  (scale bits | bias bits << 16)
   const uint32_t* q_gate;  // SWIGLU up only: gate codes, else null
   const uint32_t* sb_gate;
@@ -1264,8 +1331,9 @@ struct ExpertArgs {
   int* ccnt;               // [cps] completion counters (zero between launches)
   int T;
   int nst;                 // k_expert_bulk: shared-memory stages of the tile ring
-  int* status;             // k_expert_bulk: device status word (timeout bit)
+  int* status;             // device status words (timeout bit; index checks)
   int gsh;                 // k_expert_bulk: log2(G) - 5 (chunk c lies in group c >> gsh)
+  int n_experts;           // bound of expert ids (index checks)
   unsigned long long* trace;   // diagnostics: CTA stamps or null
 };
 
@@ -1292,19 +1360,94 @@ __device__ __forceinline__ float chunk_dot(const uint4 w, const float4* x8, int 
   return s;
 }
 
+// 32 consecutive codes of a row: BITS words of its little-endian bit stream
+// (code i in bits [i*BITS, i*BITS + BITS)); one 16-byte vector for 4-bit codes
+template <int BITS>
+struct CodeChunk { uint32_t w[BITS]; };
+template <>
+struct CodeChunk<4> { uint4 v; };
+
+__device__ __forceinline__ uint32_t ldg_stream_u32(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
+// chunk c of a row starts at word c * BITS (16-byte aligned for 4 and 8 bits)
+template <int BITS>
+__device__ __forceinline__ CodeChunk<BITS> ld_chunk(const uint32_t* p) {
+  CodeChunk<BITS> r;
+  if constexpr (BITS == 4) {
+    r.v = ldg_stream(p);
+  } else if constexpr (BITS % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < BITS; i += 4) {
+      const uint4 v = ldg_stream(p + i);
+      r.w[i] = v.x; r.w[i + 1] = v.y; r.w[i + 2] = v.z; r.w[i + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < BITS; ++i) r.w[i] = ldg_stream_u32(p + i);
+  }
+  return r;
+}
+
+// code I of a chunk -> float 1 + q / 2^BITS (the code placed under the
+// mantissa of 1.0); a code that straddles two words is joined by a funnel shift
+template <int BITS, int I>
+__device__ __forceinline__ float code_f(const CodeChunk<BITS>& ch) {
+  constexpr int p = I * BITS, wi = p >> 5, off = p & 31;
+  uint32_t v;
+  if constexpr (off + BITS <= 32) v = ch.w[wi] >> off;
+  else v = __funnelshift_r(ch.w[wi], ch.w[wi + 1], off);
+  return __uint_as_float(((v & ((1u << BITS) - 1u)) << (23 - BITS)) | 0x3f800000u);
+}
+
+template <int BITS, int I>
+__device__ __forceinline__ float chunk_dot_part(const CodeChunk<BITS>& w, const float4* x8, int sw, float s) {
+  const float4 a = x8[(2 * I) ^ sw];
+  const float4 b = x8[(2 * I + 1) ^ sw];
+  s = fmaf(code_f<BITS, 8 * I + 0>(w), a.x, s); s = fmaf(code_f<BITS, 8 * I + 1>(w), a.y, s);
+  s = fmaf(code_f<BITS, 8 * I + 2>(w), a.z, s); s = fmaf(code_f<BITS, 8 * I + 3>(w), a.w, s);
+  s = fmaf(code_f<BITS, 8 * I + 4>(w), b.x, s); s = fmaf(code_f<BITS, 8 * I + 5>(w), b.y, s);
+  s = fmaf(code_f<BITS, 8 * I + 6>(w), b.z, s); s = fmaf(code_f<BITS, 8 * I + 7>(w), b.w, s);
+  return s;
+}
+
+// chunk_dot for any code width: the same order of products (code 0 first)
+template <int BITS>
+__device__ __forceinline__ float chunk_dot_b(const CodeChunk<BITS>& w, const float4* x8, int c) {
+  if constexpr (BITS == 4) {
+    return chunk_dot(w.v, x8, c);
+  } else {
+    const int sw = c & 7;
+    float s = chunk_dot_part<BITS, 0>(w, x8, sw, 0.f);
+    s = chunk_dot_part<BITS, 1>(w, x8, sw, s);
+    s = chunk_dot_part<BITS, 2>(w, x8, sw, s);
+    return chunk_dot_part<BITS, 3>(w, x8, sw, s);
+  }
+}
+
 template <int PB, bool GATED>
 constexpr int expert_min_blocks() { return PB <= 2 ? (GATED ? 2 : 3) : 2; }
 
-template <int PB, bool GATED>
+// Expert rows as gemvs over the selected experts' b-bit codes:
+//   sum_i (S q_i + B) x_i = 2^b S * sum_i (1 + q_i / 2^b) x_i + (B - 2^b S) * sum_i x_i
+// per group (the code sum is exact in fp32: 1 + q / 2^b has b + 1 significant bits).
+template <int PB, bool GATED, int BITS = 4>
 __global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(const __grid_constant__ ExpertArgs A) {
   extern __shared__ float4 smem4[];
   const int K = A.K, K4 = K >> 2, nchunk = K >> 5;
+  const int64_t rw = static_cast<int64_t>(nchunk) * BITS;   // code words a row
   float* xsum = reinterpret_cast<float*>(smem4 + PB * K4);   // [PB][nchunk]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ngr = K / A.G;
   constexpr bool gated = GATED;
-  // rows of a weight matrix in flight per warp (rows warp, warp + NW, ...)
-  constexpr int RR = (PB <= 2) ? (GATED ? 2 : 4) : (PB <= 4 ? 2 : 1);
+  constexpr float QS = static_cast<float>(1 << BITS);
+  // rows of a weight matrix in flight per warp (rows warp, warp + NW, ...);
+  // halved for 8-bit codes (twice the registers a chunk)
+  constexpr int RR0 = (PB <= 2) ? (GATED ? 2 : 4) : (PB <= 4 ? 2 : 1);
+  constexpr int RR = (BITS > 4 && RR0 > 1) ? RR0 / 2 : RR0;
   constexpr int NV = RR * PB * 2;   // up and gate partial sums (gate 0 when not gated)
   // Static partition, independent of how many experts were selected: CTA
   // blockIdx.x serves slot u (the u-th distinct selected expert) and rows
@@ -1321,18 +1464,20 @@ __global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(c
   if (!A.pre_wait_phase) cta_stamp(A.trace, 1);
   if (u >= A.meta[0]) { cta_stamp(A.trace, 3); return; }
   if (A.max_pairs > 0 && uniq_p0[u + 1] - uniq_p0[u] > A.max_pairs) { cta_stamp(A.trace, 3); return; }
-  const int64_t e = uniq_e[u];
+  const bool e_ok = idx_ok(A.status, CK_EXPERT_E, uniq_e[u], A.n_experts) &&
+                    range_ok(A.status, uniq_p0[u], uniq_p0[u + 1], static_cast<long long>(A.T) * A.k);
+  const int64_t e = e_ok ? uniq_e[u] : 0;   // a bad slot reads expert 0 and writes nothing
   if (A.pre_wait_phase && A.prefetch && threadIdx.x == 0) {
     // the route metadata was final before the previous kernel began
-    prefetch_l2(A.q + (e * A.n_rows + nb) * (K >> 3), static_cast<int64_t>(ne - nb) * (K >> 1));
+    prefetch_l2(A.q + (e * A.n_rows + nb) * rw, static_cast<int64_t>(ne - nb) * rw * 4);
     prefetch_l2(A.sb + (e * A.n_rows + nb) * ngr, static_cast<int64_t>(ne - nb) * ngr * 4);
   }
   if (A.pre_wait_phase) { griddep_wait(); cta_stamp(A.trace, 1); }
-  const int pa = uniq_p0[u], pe = uniq_p0[u + 1];
+  const int pa = uniq_p0[u], pe = e_ok ? uniq_p0[u + 1] : pa;
 
   // first row batch: issue its weight loads before staging the inputs, so
   // their memory latency overlaps the staging
-  uint4 w0[RR], wg0[RR];
+  CodeChunk<BITS> w0[RR], wg0[RR];
   uint32_t sb0[RR], sbg0[RR];
   {
     const int c = lane;
@@ -1341,10 +1486,10 @@ __global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(c
       const int n = nb + warp + NW * j;
       if (n < ne && c < nchunk) {
         const int64_t row = e * A.n_rows + n;
-        w0[j] = ldg_stream(A.q + row * (K >> 3) + 4 * c);
+        w0[j] = ld_chunk<BITS>(A.q + row * rw + BITS * c);
         sb0[j] = ldg_u32(A.sb + row * ngr + (c << 5) / A.G);
         if (gated) {
-          wg0[j] = ldg_stream(A.q_gate + row * (K >> 3) + 4 * c);
+          wg0[j] = ld_chunk<BITS>(A.q_gate + row * rw + BITS * c);
           sbg0[j] = ldg_u32(A.sb_gate + row * ngr + (c << 5) / A.G);
         }
       }
@@ -1358,7 +1503,8 @@ __global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(c
       const int pp = i / K4, f4 = i - pp * K4;
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
       if (pp < np) {
-        const int pid = pairs[pc + pp];
+        int pid = pairs[pc + pp];
+        if (!idx_ok(A.status, CK_EXPERT_PAIR, pid, static_cast<long long>(A.T) * A.k)) pid = 0;
         const int64_t row = A.xin_by_pair ? pid : (pid / A.k);
         const int64_t base = A.xin_off + row * A.xin_stride + 4 * f4;
         if (A.xin_dt == DT_FP32) {
@@ -1395,7 +1541,7 @@ __global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(c
         const int n = rbase + NW * j;
         live[j] = n < ne;
         nn[j] = live[j] ? n : rbase;
-        rowq[j] = (e * A.n_rows + nn[j]) * (K >> 3);
+        rowq[j] = (e * A.n_rows + nn[j]) * rw;
         rows[j] = (e * A.n_rows + nn[j]) * ngr;
       }
       float acc[RR][PB], accg[RR][PB];
@@ -1405,7 +1551,7 @@ __global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(c
         for (int pp = 0; pp < PB; ++pp) { acc[j][pp] = 0.f; accg[j][pp] = 0.f; }
       for (int c = lane; c < nchunk; c += 32) {
         const int g = (c << 5) / A.G;
-        uint4 w[RR], wg[RR];
+        CodeChunk<BITS> w[RR], wg[RR];
         uint32_t sbv[RR], sbg[RR];
         if (first && c == lane) {
 #pragma unroll
@@ -1414,10 +1560,10 @@ __global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(c
 #pragma unroll
           for (int j = 0; j < RR; ++j) {
             if (live[j]) {
-              w[j] = ldg_stream(A.q + rowq[j] + 4 * c);
+              w[j] = ld_chunk<BITS>(A.q + rowq[j] + BITS * c);
               sbv[j] = ldg_u32(A.sb + rows[j] + g);
               if (gated) {
-                wg[j] = ldg_stream(A.q_gate + rowq[j] + 4 * c);
+                wg[j] = ld_chunk<BITS>(A.q_gate + rowq[j] + BITS * c);
                 sbg[j] = ldg_u32(A.sb_gate + rows[j] + g);
               }
             }
@@ -1428,21 +1574,21 @@ __global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(c
           if (!live[j]) continue;
           float sc, bi;
           sb_decode(sbv[j], A.s_dt, sc, bi);
-          const float s16 = 16.f * sc, bb = bi - s16;
+          const float s16 = QS * sc, bb = bi - s16;
           float sg16 = 0.f, bbg = 0.f;
           if (gated) {
             float sg, bg;
             sb_decode(sbg[j], A.s_dt, sg, bg);
-            sg16 = 16.f * sg; bbg = bg - sg16;
+            sg16 = QS * sg; bbg = bg - sg16;
           }
 #pragma unroll
           for (int pp = 0; pp < PB; ++pp) {
             if (pp < np) {
               const float4* x8 = smem4 + pp * K4 + 8 * c;
               const float xs = xsum[pp * nchunk + c];
-              acc[j][pp] = fmaf(s16, chunk_dot(w[j], x8, c), fmaf(bb, xs, acc[j][pp]));
+              acc[j][pp] = fmaf(s16, chunk_dot_b<BITS>(w[j], x8, c), fmaf(bb, xs, acc[j][pp]));
               if (gated)
-                accg[j][pp] = fmaf(sg16, chunk_dot(wg[j], x8, c), fmaf(bbg, xs, accg[j][pp]));
+                accg[j][pp] = fmaf(sg16, chunk_dot_b<BITS>(wg[j], x8, c), fmaf(bbg, xs, accg[j][pp]));
             }
           }
         }
@@ -1465,7 +1611,8 @@ __global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(c
         if (live[j] && pp < np) {
           const int pid = pairs[pc + pp];
           const float val = (A.act >= 0) ? act_fn(A.act, other, tot) : tot;
-          A.out[static_cast<int64_t>(pid) * A.n_rows + nn[j]] = val;
+          if (idx_ok(A.status, CK_EXPERT_PAIR, pid, static_cast<long long>(A.T) * A.k))
+            A.out[static_cast<int64_t>(pid) * A.n_rows + nn[j]] = val;
         }
       }
     }
@@ -1512,6 +1659,7 @@ static __global__ void k_interleave_sb(const unsigned short* __restrict__ s,
 struct GatherArgs {
   const int* meta;      // route metadata: pairs at meta[2 + 2 * umax + p]
   int umax, k, P, K;    // pairs, row length (multiple of 8)
+  int* status;          // index checks (MOE_CHECKS builds)
   const unsigned short* in;
   int64_t in_stride;    // elements between input rows
   unsigned short* out;  // [P, K]
@@ -1525,7 +1673,9 @@ static __global__ void k_gather_pairs(const __grid_constant__ GatherArgs A) {
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int p = static_cast<int>(i / v), j = static_cast<int>(i - static_cast<int64_t>(p) * v);
-    const int row = A.meta[2 + 2 * A.umax + p] / A.k;
+    int pid = A.meta[2 + 2 * A.umax + p];
+    if (!idx_ok(A.status, CK_GATHER_PAIR, pid, A.P)) pid = 0;
+    const int row = pid / A.k;
     reinterpret_cast<uint4*>(A.out)[i] =
         reinterpret_cast<const uint4*>(A.in + static_cast<int64_t>(row) * A.in_stride)[j];
   }

@@ -2,6 +2,7 @@
 // forward orchestration and the C ABI declared in include/moe_layer.h.
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>   // PFN_cuTensorMapEncodeTiled
+#include <nvtx3/nvToolsExt.h>   // header-only NVTX v3
 
 #include <algorithm>
 #include <atomic>
@@ -84,12 +85,16 @@ struct moe_layer {
 
   // per-stage timing
   bool profiling = false;
+  // NVTX ranges around the forward and its stages (on by default in MOE_CHECKS
+  // builds; MOE_NVTX=0/1 overrides)
+  bool nvtx = MOE_CHECKS != 0;
   bool profiled = false;
   cudaEvent_t ev[MOE_NUM_STAGES + 1] = {};
 
   int r_in = 0, off_fc1 = 0, off_shg = 0, off_shu = 0;
   int umax = 0;
   int kin = 0;
+  int bits = 4;           // code width of the routed experts (3, 4 or 8)
   int grouped_min_t = 16;
   int expert_split = 0;   // AUTO's grouped path: light experts on the int4 gemv kernel
   int last_launches = 0;  // kernel launches of the last forward
@@ -209,6 +214,8 @@ static moe_status validate_impl(const moe_layer_config* c, const moe_layer_weigh
   } else if (w && (w->fc1_latent || w->fc2_latent)) {
     return fail(MOE_ERR_LATENT_PROJ, "latent projections given for a non-latent layer");
   }
+  if (c->bits != 0 && c->bits != 3 && c->bits != 4 && c->bits != 8)
+    return fail(MOE_ERR_INVALID_ARG, "bits must be 0 (= 4), 3, 4 or 8");
   const int G = c->group_size;
   if (G != 32 && G != 64 && G != 128) return fail(MOE_ERR_SHAPE, "group_size must be 32, 64 or 128");
   const int kin = c->latent > 0 ? c->latent : c->hidden;
@@ -296,11 +303,11 @@ template <typename Args, int TB>
 static cudaError_t launch_dense_out_t(const Args& a, int grid, cudaStream_t s, bool pdl) {
   return launch_ex<Args>(k_dense_out<TB>, grid, NT, dense_smem<TB>(a.K), s, pdl, a);
 }
-template <int PB>
+template <int PB, int BITS = 4>
 static cudaError_t launch_expert_t(const ExpertArgs& a, int grid, cudaStream_t s, bool pdl) {
   const size_t smem = static_cast<size_t>(PB) * (4ull * a.K + 4ull * (a.K / 32));
-  if (a.q_gate) return launch_ex<ExpertArgs>(k_expert<PB, true>, grid, NT, smem, s, pdl, a);
-  return launch_ex<ExpertArgs>(k_expert<PB, false>, grid, NT, smem, s, pdl, a);
+  if (a.q_gate) return launch_ex<ExpertArgs>(k_expert<PB, true, BITS>, grid, NT, smem, s, pdl, a);
+  return launch_ex<ExpertArgs>(k_expert<PB, false, BITS>, grid, NT, smem, s, pdl, a);
 }
 
 // The gemv path's expert kernel with bulk-copied weight groups: token pairs
@@ -523,7 +530,11 @@ static cudaError_t launch_dense_out(const DenseOutArgs& a, int tb, int grid, cud
     default: return launch_dense_out_t<DenseOutArgs, 8>(a, grid, s, pdl);
   }
 }
-static cudaError_t launch_expert(const ExpertArgs& a, int pb, int grid, cudaStream_t s, bool pdl) {
+// 3- and 8-bit codes: passes of one or two token pairs (pb above 2 is clamped)
+static cudaError_t launch_expert(const ExpertArgs& a, int pb, int grid, cudaStream_t s, bool pdl,
+                                 int bits = 4) {
+  if (bits == 3) return pb <= 1 ? launch_expert_t<1, 3>(a, grid, s, pdl) : launch_expert_t<2, 3>(a, grid, s, pdl);
+  if (bits == 8) return pb <= 1 ? launch_expert_t<1, 8>(a, grid, s, pdl) : launch_expert_t<2, 8>(a, grid, s, pdl);
   switch (pb) {
     case 1: return launch_expert_t<1>(a, grid, s, pdl);
     case 2: return launch_expert_t<2>(a, grid, s, pdl);
@@ -555,6 +566,10 @@ static cudaError_t set_smem_attrs() {
   MOE_SMEM_ATTR((k_expert<4, false>)) MOE_SMEM_ATTR((k_expert<8, false>))
   MOE_SMEM_ATTR((k_expert<1, true>)) MOE_SMEM_ATTR((k_expert<2, true>))
   MOE_SMEM_ATTR((k_expert<4, true>)) MOE_SMEM_ATTR((k_expert<8, true>))
+  MOE_SMEM_ATTR((k_expert<1, false, 3>)) MOE_SMEM_ATTR((k_expert<2, false, 3>))
+  MOE_SMEM_ATTR((k_expert<1, true, 3>)) MOE_SMEM_ATTR((k_expert<2, true, 3>))
+  MOE_SMEM_ATTR((k_expert<1, false, 8>)) MOE_SMEM_ATTR((k_expert<2, false, 8>))
+  MOE_SMEM_ATTR((k_expert<1, true, 8>)) MOE_SMEM_ATTR((k_expert<2, true, 8>))
   MOE_SMEM_ATTR((k_expert_bulk<1, 8, false>)) MOE_SMEM_ATTR((k_expert_bulk<2, 4, false>))
   MOE_SMEM_ATTR((k_expert_bulk<4, 2, false>)) MOE_SMEM_ATTR((k_expert_bulk<8, 1, false>))
   MOE_SMEM_ATTR((k_expert_bulk<1, 1, false>)) MOE_SMEM_ATTR((k_expert_bulk<2, 1, false>))
@@ -587,6 +602,10 @@ static cudaError_t set_smem_attrs() {
 extern "C" {
 
 int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+int32_t moe_build_flags(void) {
+  return MOE_CHECKS ? (MOE_BUILD_CHECKS | MOE_BUILD_NVTX_DEFAULT) : 0;
+}
 
 moe_status moe_layer_validate(const moe_layer_config* cfg, const moe_layer_weights* w) {
   std::string why;
@@ -637,6 +656,8 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   L->device = dev;
   L->num_sms = prop.multiProcessorCount;
   L->kin = kin;
+  L->bits = c.bits == 0 ? 4 : c.bits;
+  L->cfg.bits = L->bits;
   L->off_fc1 = E;
   L->off_shg = E + Lt;
   L->off_shu = E + Lt + (gated ? Fs : 0);
@@ -676,12 +697,13 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   if (const char* env = std::getenv("MOE_ROUTE_MAXW")) L->route_max_w = std::max(1, std::min(8, std::atoi(env)));
   if (const char* env = std::getenv("MOE_SIDE_GRID")) L->side_grid = std::max(0, std::atoi(env));
   if (const char* env = std::getenv("MOE_DEBUG_ROUTE")) L->debug_route = std::atoi(env) != 0;
+  if (const char* env = std::getenv("MOE_NVTX")) L->nvtx = std::atoi(env) != 0;
   {
     const size_t adt = dt_size(c.act_dtype), rdt = dt_size(c.router_dtype);
     const size_t sdt = dt_size(c.scale_dtype);
-    const size_t nq_in = static_cast<size_t>(E) * F * (kin / 8);
+    const size_t nq_in = static_cast<size_t>(E) * F * (kin / 32) * L->bits;
     const size_t ng_in = static_cast<size_t>(E) * F * (kin / G);
-    const size_t nq_dn = static_cast<size_t>(E) * kin * (F / 8);
+    const size_t nq_dn = static_cast<size_t>(E) * kin * (F / 32) * L->bits;
     const size_t ng_dn = static_cast<size_t>(E) * kin * (F / G);
     (void)sdt;
     MOE_TRY_CUDA(set_smem_attrs(), "kernel attributes");
@@ -730,9 +752,11 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
       k_sb_group_major<<<blocks, 256, 0, s>>>(src, *dst, E, rows, ngr);
       return cudaGetLastError();
     };
-    if (gated) MOE_TRY_CUDA(group_major(&L->gate_sbT, L->gate_sb, F, kin / G), "gate scales");
-    MOE_TRY_CUDA(group_major(&L->up_sbT, L->up_sb, F, kin / G), "up scales");
-    MOE_TRY_CUDA(group_major(&L->down_sbT, L->down_sb, kin, F / G), "down scales");
+    if (L->bits == 4) {   // the grouped GEMM's scale layout (4-bit codes only)
+      if (gated) MOE_TRY_CUDA(group_major(&L->gate_sbT, L->gate_sb, F, kin / G), "gate scales");
+      MOE_TRY_CUDA(group_major(&L->up_sbT, L->up_sb, F, kin / G), "up scales");
+      MOE_TRY_CUDA(group_major(&L->down_sbT, L->down_sb, kin, F / G), "down scales");
+    }
     if (Fs) {
       const size_t n = static_cast<size_t>(Fs) * H * adt;
       if (gated) {
@@ -753,8 +777,9 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     MOE_TRY_CUDA(cudaMemsetAsync(L->meta, 0, (2 + 2 * static_cast<size_t>(L->umax) + P) * 4, s), "workspace clear");
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->hbuf), P * F * 4), "workspace");
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->pexp), P * kin * 4), "workspace");
-    MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->status), 4), "workspace");
-    MOE_TRY_CUDA(cudaMemsetAsync(L->status, 0, 4, s), "status clear");
+    // status words: flags, then the first index-check violation (site, index, bound)
+    MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->status), 16), "workspace");
+    MOE_TRY_CUDA(cudaMemsetAsync(L->status, 0, 16, s), "status clear");
     MOE_TRY_CUDA(L->alloc(reinterpret_cast<void**>(&L->route_counter), 4), "workspace");
     MOE_TRY_CUDA(cudaMemsetAsync(L->route_counter, 0, 4, s), "counter clear");
     MOE_TRY_CUDA(L->alloc(&L->bout, static_cast<size_t>(T) * (Lt + Fs + 64) * 2), "workspace");
@@ -1102,6 +1127,7 @@ static void print_cta_trace(moe_layer* h, cudaStream_t s) {
 
 // The path a forward of T rows takes (never AUTO).
 static int choose_path(const moe_layer* h, int T) {
+  if (h->bits != 4) return MOE_PATH_GEMV;   // the tensor-core path decodes 4-bit codes only
   if (h->path == MOE_PATH_GROUPED || (h->path == MOE_PATH_AUTO && T >= h->grouped_min_t))
     return MOE_PATH_GROUPED;
   return MOE_PATH_GEMV;
@@ -1143,9 +1169,23 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
   const int kout = Lt + Fs;
   const int mma_dt = c.act_dtype;
   cudaError_t e = cudaSuccess;
+  // stage boundaries: profiling events and, with h->nvtx, one NVTX range per
+  // stage inside the forward's range (popped on every exit)
+  static const char* const kStageRange[MOE_NUM_STAGES] = {
+      "moe dense_in (router, fc1_latent, shared gate/up)", "moe route", "moe expert up",
+      "moe expert down + combine", "moe dense_out (fc2_latent, shared down, residual)"};
+  int nvtx_open = 0;
   auto mark = [&](int i) {
     if (h->profiling) cudaEventRecord(h->ev[i], s);
+    if (h->nvtx) {
+      if (i > 0 && nvtx_open > 1) { nvtxRangePop(); --nvtx_open; }
+      if (i < MOE_NUM_STAGES) { nvtxRangePushA(kStageRange[i]); ++nvtx_open; }
+    }
   };
+  if (h->nvtx) {
+    nvtxRangePushA(grouped ? "moe_layer_forward grouped" : "moe_layer_forward gemv");
+    ++nvtx_open;
+  }
   // diagnostics: the stamp buffer of the next launch (null unless MOE_CTA_TRACE)
   auto tslot = [&](const char* name) -> unsigned long long* {
     if (!h->ct_trace || h->ct_n >= CT_SLOTS) return nullptr;
@@ -1178,6 +1218,10 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
   ra.ext_w = ext_w;
   ra.status = h->status;
   ra.debug_times = h->debug_route;
+#if MOE_CHECKS
+  // planted out-of-range metadata index for the checks' own test (read per call)
+  if (const char* env = std::getenv("MOE_DEBUG_BAD_INDEX")) ra.debug_bad = std::atoi(env);
+#endif
   ra.max_w = h->route_max_w;
   {
     const int P = T * k;
@@ -1230,7 +1274,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
   // expert kernels of the gemv path: bulk-copied weight groups for up to
   // expert_bulk_max_t rows (latency-bound: every CTA's bytes requested at once),
   // register-streamed k_expert above (both give the same bits for a row)
-  const bool use_bulk = h->expert_bulk && !grouped && T <= h->expert_bulk_max_t;
+  const bool use_bulk = h->expert_bulk && !grouped && T <= h->expert_bulk_max_t && h->bits == 4;
   EbLaunch eb_up, eb_dn;
   int cps_up = 1, cps_dn = 1;
   const int slots_e = std::min(E, T * k);   // distinct-expert slots of the expert launches
@@ -1459,6 +1503,8 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
       up.prefetch = 0;
       up.max_pairs = split_experts ? pb_split : 0;
       up.status = h->status;
+      up.T = T;
+      up.n_experts = E;
       up.gsh = c.group_size == 32 ? 0 : (c.group_size == 64 ? 1 : 2);
       if (bulk_up) {
         // one wave: at most per_sm CTAs on every SM (one when the filler CTAs
@@ -1471,7 +1517,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
         up.cps = std::max(1, std::min(std::max(1, F / 8), (target + slots - 1) / slots));
         const int grid_up = slots * up.cps;
         up.trace = tslot("k_expert_up");
-        if ((e = launch_expert(up, pb_up, grid_up, cs, pdl)) != cudaSuccess) goto cuda_fail;
+        if ((e = launch_expert(up, pb_up, grid_up, cs, pdl, h->bits)) != cudaSuccess) goto cuda_fail;
       }
       ++nl;
 
@@ -1507,6 +1553,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
         // the B rows in sorted pair order: an expert's rows are one block
         GatherArgs ga{};
         ga.meta = h->meta; ga.umax = h->umax; ga.k = k; ga.P = T * k; ga.K = kin;
+        ga.status = h->status;
         ga.in = static_cast<const unsigned short*>(uup.b0); ga.in_stride = uup.b0_stride;
         ga.out = static_cast<unsigned short*>(h->xs);
         const int64_t n = static_cast<int64_t>(T) * k * (kin / 8);
@@ -1522,6 +1569,8 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
       uup.act = c.act;
       uup.out_f32 = h->hbuf;
       uup.status = h->status;
+      uup.n_experts = E;
+      uup.n_pairs = T * k;
       if ((e = launch_umma(h, uup, T, s, &nl, pdl)) != cudaSuccess) goto cuda_fail;
 
     }
@@ -1556,7 +1605,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
         dn.cps = std::max(1, std::min(std::min(std::max(1, kin / 8), kCombineCounters),
                                       (target + slots - 1) / slots));
         dn.trace = tslot("k_expert_down");
-        if ((e = launch_expert(dn, pb_dn, slots * dn.cps, cs, pdl)) != cudaSuccess) goto cuda_fail;
+        if ((e = launch_expert(dn, pb_dn, slots * dn.cps, cs, pdl, h->bits)) != cudaSuccess) goto cuda_fail;
       }
       if (fill) {
         so.dep_tail = 1;
@@ -1689,12 +1738,14 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
       goto cuda_fail;
   }
   mark(5);
+  for (; nvtx_open > 0; --nvtx_open) nvtxRangePop();
   if (h->profiling) h->profiled = true;
   h->last_launches = nl;
   if (h->um_trace) print_umma_trace(h, s);
   if (h->ct_trace && h->ct_n) print_cta_trace(h, s);
   return MOE_OK;
 cuda_fail:
+  for (; nvtx_open > 0; --nvtx_open) nvtxRangePop();
   h->last_error = std::string("launch failed: ") + cudaGetErrorString(e);
   return MOE_ERR_CUDA;
 }
@@ -1740,6 +1791,10 @@ moe_status moe_layer_set_path(moe_layer* h, int32_t path) {
     h->last_error = "the grouped path needs 16-bit activations";
     return MOE_ERR_UNSUPPORTED;
   }
+  if (path == MOE_PATH_GROUPED && h->bits != 4) {
+    h->last_error = "the grouped path decodes 4-bit codes only";
+    return MOE_ERR_UNSUPPORTED;
+  }
   h->path = path;
   return MOE_OK;
 }
@@ -1747,16 +1802,27 @@ moe_status moe_layer_set_path(moe_layer* h, int32_t path) {
 moe_status moe_layer_device_status(moe_layer* h, void* stream) {
   if (!h) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int v = 0;
-  cudaError_t e = cudaMemcpyAsync(&v, h->status, 4, cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(h->status, 0, 4, s);
+  int v[4] = {0, 0, 0, 0};
+  cudaError_t e = cudaMemcpyAsync(v, h->status, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->status, 0, sizeof(v), s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) {
     h->last_error = std::string("status read: ") + cudaGetErrorString(e);
     return MOE_ERR_CUDA;
   }
-  if (v & STATUS_TIMEOUT) return MOE_ERR_TIMEOUT;
-  if (v & STATUS_NONFINITE) return MOE_ERR_NONFINITE;
+  if (v[0] & STATUS_INDEX) {
+    static const char* const kSites[] = {"?", "k_expert expert id", "k_expert pair id",
+                                         "k_expert_bulk expert id", "k_expert_bulk pair id",
+                                         "k_gather_pairs pair id", "grouped GEMM expert id",
+                                         "grouped GEMM pair id", "routing prefetch expert id",
+                                         "distinct-expert pair range"};
+    const int site = (v[1] >= 1 && v[1] <= 9) ? v[1] : 0;
+    h->last_error = std::string("index check failed: ") + kSites[site] + " " + std::to_string(v[2]) +
+                    " outside [0, " + std::to_string(v[3]) + ")";
+    return MOE_ERR_INDEX;
+  }
+  if (v[0] & STATUS_TIMEOUT) return MOE_ERR_TIMEOUT;
+  if (v[0] & STATUS_NONFINITE) return MOE_ERR_NONFINITE;
   return MOE_OK;
 }
 
@@ -1814,6 +1880,7 @@ const char* moe_status_string(moe_status s) {
     case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
     case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
     case MOE_ERR_NONFINITE: return "MOE_ERR_NONFINITE";
+    case MOE_ERR_INDEX: return "MOE_ERR_INDEX";
   }
   return "MOE_ERR_UNKNOWN";
 }

@@ -95,6 +95,7 @@ struct UmmaArgs {
   const float* pexp; const float* wts; int add_combine;
   int* status;
   int min_pairs;            // experts mode: groups with fewer token pairs are left to the gemv kernel
+  int n_experts, n_pairs;   // experts mode: bounds of expert and pair ids (index checks)
   unsigned long long* trace;   // diagnostics: CTA 0's per-chunk role stamps (k_umma2), or null
   // ---- operands by tensor copies (k_umma2; host-encoded maps) ----
   // tma_a (else cp.async): dense: map [2 * seg + part] over that part's [rows, wk]
@@ -301,12 +302,20 @@ struct UmmaGroup {
   int n;      // tokens
 };
 
+// pair id at sorted position i of the route metadata (index checks: 0 if bad)
+__device__ __forceinline__ int umma_pair(const UmmaArgs& A, int i) {
+  const int pid = A.meta[2 + 2 * A.umax + i];
+  return idx_ok(A.status, CK_UMMA_PAIR, pid, A.n_pairs) ? pid : 0;
+}
+
 __device__ __forceinline__ UmmaGroup umma_group(const UmmaArgs& A, int g) {
   UmmaGroup G;
   if (A.experts) {
     G.e = A.meta[1 + g];
+    if (!idx_ok(A.status, CK_UMMA_E, G.e, A.n_experts)) G.e = 0;
     G.p0 = A.meta[1 + A.umax + g];
     G.n = A.meta[1 + A.umax + g + 1] - G.p0;
+    if (!range_ok(A.status, G.p0, G.p0 + G.n, A.n_pairs)) { G.p0 = 0; G.n = 0; }
     if (G.n < A.min_pairs) G.n = 0;   // served by the int4 gemv kernel
   } else {
     G.e = 0;
@@ -504,7 +513,7 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma(const __grid_constant__ 
       for (int n = tid; n < nvalid; n += UM_THREADS) {
         int row = n0 + n;
         if (A.experts) {
-          const int pid = A.meta[2 + 2 * A.umax + G.p0 + n0 + n];
+          const int pid = umma_pair(A, G.p0 + n0 + n);
           row = A.by_pair ? pid : pid / A.k;
         }
         tok_row[n] = row;
@@ -675,7 +684,7 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma(const __grid_constant__ 
         for (int i = 0; i < 16; ++i) {
           const int n = c0 + i;
           if (n >= nvalid) break;
-          const int pid = A.experts ? A.meta[2 + 2 * A.umax + G.p0 + n0 + n] : n0 + n;
+          const int pid = A.experts ? umma_pair(A, G.p0 + n0 + n) : n0 + n;
           if (A.ksplit > 1) {
             A.part[(static_cast<int64_t>(split) * A.n_tokens + pid) * A.n_rows + m] = acc[i];
           } else {

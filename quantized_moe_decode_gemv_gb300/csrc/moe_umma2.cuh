@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
           if (A.experts && A.b_sorted) {
             brow[q] = G.p0 + n0 + n;
           } else if (A.experts) {
-            const int pid = A.meta[2 + 2 * A.umax + G.p0 + n0 + n];
+            const int pid = umma_pair(A, G.p0 + n0 + n);
             brow[q] = A.by_pair ? pid : pid / A.k;
           } else {
             brow[q] = n0 + n;
@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
           if (A.experts && A.b_sorted) {
             row = G.p0 + n0 + n;
           } else if (A.experts) {
-            const int pid = A.meta[2 + 2 * A.umax + G.p0 + n0 + n];
+            const int pid = umma_pair(A, G.p0 + n0 + n);
             row = A.by_pair ? pid : pid / A.k;
           }
           cp_async16(sbb + sw_off(n, 8 * j),
@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(UM_THREADS, 2) k_umma2(const __grid_constant__
         for (int i = 0; i < 16; ++i) {
           const int n = c0 + i;
           if (n >= nvalid) break;
-          const int pid = A.experts ? A.meta[2 + 2 * A.umax + G.p0 + n0 + n] : n0 + n;
+          const int pid = A.experts ? umma_pair(A, G.p0 + n0 + n) : n0 + n;
           if (A.ksplit > 1)
             A.part[(static_cast<int64_t>(Tl.split) * A.n_tokens + pid) * A.n_rows + m] = acc[i];
           else

@@ -117,6 +117,12 @@ def check_parity(got: dict, ref: dict, rows=None, what=""):
 
 
 @functools.lru_cache(maxsize=None)
+def cached_layer_spec(spec, seed: int = 0):
+    """A layer of any spec (LayerSpec is frozen and hashable), built once."""
+    return mi.make_layer(spec, seed)
+
+
+@functools.lru_cache(maxsize=None)
 def cached_layer(name: str, seed: int = 0, zipf: bool = False):
     spec = mi.spec_for(name)
     rb = mi.zipf_router_bias(spec.n_experts, seed) if zipf else None

@@ -36,7 +36,7 @@ def test_header_declares_the_boundary():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
-    assert lib.moe_abi_version() == 2
+    assert lib.moe_abi_version() == 3
 
 
 def test_status_strings(lib):
@@ -88,6 +88,12 @@ CASES = [
     ("shared weights without shared_ffn", {"shared_ffn": 0}, {}, "MOE_ERR_SHAPE"),
     ("no router", {}, {"router_w": None}, "MOE_ERR_INVALID_ARG"),
     ("zero max_tokens", {"max_tokens": 0}, {}, "MOE_ERR_INVALID_ARG"),
+    ("3-bit codes", {"bits": 3}, {}, "MOE_OK"),
+    ("8-bit codes", {"bits": 8}, {}, "MOE_OK"),
+    ("bits 0 means 4", {"bits": 0}, {}, "MOE_OK"),
+    ("2-bit codes", {"bits": 2}, {}, "MOE_ERR_INVALID_ARG"),
+    ("5-bit codes", {"bits": 5}, {}, "MOE_ERR_INVALID_ARG"),
+    ("16-bit codes", {"bits": 16}, {}, "MOE_ERR_INVALID_ARG"),
 ]
 
 

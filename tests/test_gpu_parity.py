@@ -142,6 +142,47 @@ def test_latent_parity(T):
     _parity("latent", T, paths=SMALL_T_PATHS)
 
 
+# --- 3- and 8-bit affine codes (gemv schedule): tiny and latent shapes ---------
+
+def _bits_layer(base, bits, seed=0):
+    spec = mi.spec_for(base).with_(name=f"{base}_b{bits}", bits=bits)
+    return gu.cached_layer_spec(spec, seed)
+
+
+@pytest.mark.parametrize("bits", [3, 8])
+@pytest.mark.parametrize("T", [1, 2, 3, 5, 16])
+def test_code_width_tiny_parity(bits, T):
+    """Little-endian b-bit code streams (3-bit codes straddle words) through
+    the gemv expert kernels, on every row; AUTO keeps the gemv schedule."""
+    lay = _bits_layer("tiny", bits)
+    _, h = handle_for(lay.spec.name, 16, layer=lay)
+    assert h.path_for(T) == "gemv"
+    _parity(lay.spec.name, T, max_tokens=16, paths=("auto",))
+
+
+@pytest.mark.parametrize("bits", [3, 8])
+@pytest.mark.parametrize("T,rows", [(1, None), (2, None), (9, [0, 4, 8])])
+def test_code_width_latent_parity(bits, T, rows):
+    """The latent layer (E=496, k=9, latent 1024, group 64) with 3- and 8-bit
+    expert codes at full size."""
+    lay = _bits_layer("latent", bits)
+    handle_for(lay.spec.name, 16, layer=lay)
+    _parity(lay.spec.name, T, rows=rows, max_tokens=16, paths=("auto",))
+
+
+@pytest.mark.parametrize("bits", [3, 8])
+def test_code_width_grouped_refused(bits):
+    """The tensor-core schedule decodes 4-bit codes only: forcing it on a 3- or
+    8-bit layer is refused and the layer keeps its gemv schedule."""
+    import quantized_moe_decode_gemv_gb300 as pkg
+    lay = _bits_layer("tiny", bits)
+    _, h = handle_for(lay.spec.name, 16, layer=lay)
+    with pytest.raises(pkg.MoEError) as ei:
+        h.set_path("grouped")
+    assert "MOE_ERR_UNSUPPORTED" in str(ei.value)
+    assert h.path_for(16) == "gemv"
+
+
 # --- non-latent fp16 sigmoid top-8 layer (H=6144, E=256) at full size ---------
 
 @pytest.mark.parametrize("T,rows", [(1, None), (4, [0, 3]), (32, [0, 17, 31])])
