@@ -59,11 +59,10 @@ class L2Flush:
         self.w.zero_()
         self.r.sum()
 STAGES = ["dense_in", "route", "expert_up", "expert_down", "dense_out"]
-# the kernels of the gemv path's stages (the expert kernel moves its weights by
-# bulk copies up to two rows, by register loads above)
-KERNEL_OF_STAGE = {"dense_in": "k_dense_in", "route": "k_route", "expert_up": "k_expert_bulk",
-                   "expert_down": "k_expert_bulk", "dense_out": "k_dense_bulk"}
-KERNEL_OF_STAGE_REG = dict(KERNEL_OF_STAGE, expert_up="k_expert", expert_down="k_expert")
+# the kernels of the gemv path's stages (4-bit experts: the warp-MMA expert
+# kernel at every batch size)
+KERNEL_OF_STAGE = {"dense_in": "k_dense_in", "route": "k_route", "expert_up": "k_expert_mma",
+                   "expert_down": "k_expert_mma", "dense_out": "k_dense_bulk"}
 # the grouped path runs every projection through the tcgen05 GEMM (its split-K
 # sums and the combine ride in the same stages)
 KERNEL_OF_STAGE_GROUPED = {"dense_in": "k_umma2", "route": "k_route", "expert_up": "k_umma2",
@@ -80,6 +79,7 @@ KERNEL_SOURCES = {
     "k_umma": ["moe_kernels.cuh", "moe_umma.cuh", "moe_layer.cu"],
     "k_umma2": ["moe_kernels.cuh", "moe_umma.cuh", "moe_umma2.cuh", "moe_layer.cu"],
     "k_expert_bulk": ["moe_kernels.cuh", "moe_expert_bulk.cuh", "moe_layer.cu"],
+    "k_expert_mma": ["moe_kernels.cuh", "moe_expert_bulk.cuh", "moe_expert_mma.cuh", "moe_layer.cu"],
     "k_dense_bulk": ["moe_kernels.cuh", "moe_expert_bulk.cuh", "moe_dense_bulk.cuh", "moe_layer.cu"],
 }
 
@@ -533,8 +533,7 @@ def run_ours(args):
     path = h.path_for(args.T)
     launches = h.last_launch_count()
     per_kernel = {}
-    kmap = (KERNEL_OF_STAGE_GROUPED if path == "grouped" else
-            KERNEL_OF_STAGE if args.T <= 2 else KERNEL_OF_STAGE_REG)
+    kmap = KERNEL_OF_STAGE_GROUPED if path == "grouped" else KERNEL_OF_STAGE
     for i, n in enumerate(STAGES):
         kname = kmap[n]
         b, t = per_kernel.get(kname, (0.0, 0.0))

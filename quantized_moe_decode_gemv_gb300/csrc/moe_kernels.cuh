@@ -1334,6 +1334,13 @@ struct ExpertArgs {
   int* status;             // device status words (timeout bit; index checks)
   int gsh;                 // k_expert_bulk: log2(G) - 5 (chunk c lies in group c >> gsh)
   int n_experts;           // bound of expert ids (index checks)
+  // k_expert_mma: codes and scale/bias words in its tiled layouts, chunks of
+  // 64 columns per ring stage (ck; nst stages per warp), pairs per pass (pp)
+  const uint32_t* qt;
+  const uint32_t* sbt;
+  const uint32_t* qt_gate;
+  const uint32_t* sbt_gate;
+  int ck, pp, ks;   // ks: warps sharing a tile's K range (1, 2 or 4)
   unsigned long long* trace;   // diagnostics: CTA stamps or null
 };
 

@@ -15,6 +15,7 @@
 #include "moe_layer.h"
 #include "moe_kernels.cuh"
 #include "moe_expert_bulk.cuh"
+#include "moe_expert_mma.cuh"
 #include "moe_dense_bulk.cuh"
 #include "moe_umma.cuh"
 #include "moe_umma2.cuh"
@@ -60,6 +61,9 @@ struct moe_layer {
   uint32_t *gate_sb = nullptr, *up_sb = nullptr, *down_sb = nullptr;
   // group-major copies of the scale/bias words ([E, K/G, rows]: the grouped GEMM's tensor copies)
   uint32_t *gate_sbT = nullptr, *up_sbT = nullptr, *down_sbT = nullptr;
+  // the warp-MMA expert kernel's tiled copies (4-bit codes only)
+  uint32_t *gate_qt = nullptr, *up_qt = nullptr, *down_qt = nullptr;
+  uint32_t *gate_sbt = nullptr, *up_sbt = nullptr, *down_sbt = nullptr;
   void *sh_gate = nullptr, *sh_up = nullptr, *sh_down = nullptr;
 
   // workspace
@@ -128,6 +132,9 @@ struct moe_layer {
   int debug_route = 0;    // diagnostics: print routing phase times
   int expert_bulk = 1;    // gemv path: expert kernels with bulk-copied weight tiles (k_expert_bulk)
   int expert_bulk_max_t = 2;   // the bulk expert kernel up to this many rows
+  bool expert_mma = true;      // gemv path: warp-MMA expert kernel (4-bit codes)
+  int expert_mma_max_t = 1 << 30;   // ... up to this many rows
+  int expert_mma_pp = 8;       // its token pairs per pass (more pairs: more passes)
   int expert_bulk_pb = 2;      // its token pairs per pass
   int dense_bulk = 1;     // gemv path: shared expert and output projection by k_dense_bulk
   int fill = 0;           // gemv path: the shared expert as launches of its own beside the routed chain
@@ -499,6 +506,68 @@ static cudaError_t launch_expert_bulk(const ExpertArgs& a, const EbLaunch& eb, i
   }
 }
 
+// The warp-MMA expert kernel's plan: pairs per pass (a multiple of 4, up to
+// the T rows' worth, at most EM_MAX_PAIRS), then two CTAs per SM before one,
+// then the deepest ring (4 chunks of 64 columns a stage before 2; 4 stages a
+// warp before fewer).  `cps` puts one wave of CTAs over the distinct-expert
+// slots.  False when no plan fits shared memory.
+struct EmLaunch {
+  EmPlan plan{};
+  int per_sm = 0, cps = 1;
+};
+static bool em_choose(int K, int G, bool gated, int T, int pp_cap, int n_rows, int slots, int num_sms,
+                      EmLaunch* o) {
+  const int pp_want = std::min(std::min(EM_MAX_PAIRS, std::max(4, pp_cap & ~3)), std::max(4, (T + 3) & ~3));
+  // warps per tile: a function of K alone, so that a row's sums do not depend
+  // on the batch (about 6 to 12 chunks of 64 columns a warp)
+  const int nkc = K / 64, nu = nkc / (G > 64 ? G / 64 : 1);   // group-aligned K units
+  const int ks = (nkc >= 24 && nu >= 4) ? 4 : ((nkc >= 12 && nu >= 2) ? 2 : 1);
+  static const int kCkNs[][2] = {{4, 4}, {4, 3}, {2, 4}, {2, 3}, {2, 2}};
+  for (int pp = pp_want; pp >= 4; pp -= 4) {
+    // two CTAs per SM only with up to two n-tiles of accumulators (registers)
+    for (int per_sm = pp <= 8 ? 2 : 1; per_sm >= 1; --per_sm) {
+      const int budget = per_sm == 2 ? 110 * 1024 : kSmemMax - 2048;
+      for (const auto& cn : kCkNs) {
+        if (G == 128 && cn[0] % 2) continue;
+        const EmPlan p = em_plan(K, G, gated, cn[0], cn[1], pp, ks);
+        if (p.smem > budget) continue;
+        o->plan = p;
+        o->per_sm = per_sm;
+        o->cps = std::max(1, std::min(n_rows / 16, num_sms * per_sm / std::max(1, slots)));
+        return true;
+      }
+    }
+  }
+  return false;
+}
+template <int NTP, int GB>
+static cudaError_t launch_expert_mma_t(const ExpertArgs& a, bool gated, int grid, size_t smem, cudaStream_t s,
+                                       bool pdl) {
+  if (gated) return launch_ex<ExpertArgs>(k_expert_mma<true, NTP, GB>, grid, EM_NT, smem, s, pdl, a);
+  return launch_ex<ExpertArgs>(k_expert_mma<false, NTP, GB>, grid, EM_NT, smem, s, pdl, a);
+}
+template <int GB>
+static cudaError_t launch_expert_mma_g(const ExpertArgs& a, bool gated, int pp, int grid, size_t smem,
+                                       cudaStream_t s, bool pdl) {
+  if (pp <= 4) return launch_expert_mma_t<1, GB>(a, gated, grid, smem, s, pdl);
+  if (pp <= 8) return launch_expert_mma_t<2, GB>(a, gated, grid, smem, s, pdl);
+  return launch_expert_mma_t<4, GB>(a, gated, grid, smem, s, pdl);
+}
+static cudaError_t launch_expert_mma(ExpertArgs a, const EmLaunch& el, int grid, cudaStream_t s, bool pdl) {
+  a.ck = el.plan.ck;
+  a.nst = el.plan.ns;
+  a.pp = el.plan.pp;
+  a.ks = el.plan.ks;
+  a.cps = el.cps;
+  const size_t smem = static_cast<size_t>(el.plan.smem);
+  const bool gated = a.qt_gate != nullptr;
+  switch (a.G) {
+    case 32: return launch_expert_mma_g<2>(a, gated, el.plan.pp, grid, smem, s, pdl);
+    case 64: return launch_expert_mma_g<4>(a, gated, el.plan.pp, grid, smem, s, pdl);
+    default: return launch_expert_mma_g<8>(a, gated, el.plan.pp, grid, smem, s, pdl);
+  }
+}
+
 template <int TB>
 static cudaError_t launch_dense_in_pdl_t(const DenseInArgs& a, int grid, cudaStream_t s) {
   return launch_ex<DenseInArgs>(k_dense_in<TB>, grid, NT, dense_smem<TB>(a.K), s, true, a);
@@ -566,6 +635,12 @@ static cudaError_t set_smem_attrs() {
   MOE_SMEM_ATTR((k_expert<4, false>)) MOE_SMEM_ATTR((k_expert<8, false>))
   MOE_SMEM_ATTR((k_expert<1, true>)) MOE_SMEM_ATTR((k_expert<2, true>))
   MOE_SMEM_ATTR((k_expert<4, true>)) MOE_SMEM_ATTR((k_expert<8, true>))
+#define MOE_SMEM_ATTR_EM(GB)                                                               \
+  MOE_SMEM_ATTR((k_expert_mma<false, 1, GB>)) MOE_SMEM_ATTR((k_expert_mma<true, 1, GB>)) \
+  MOE_SMEM_ATTR((k_expert_mma<false, 2, GB>)) MOE_SMEM_ATTR((k_expert_mma<true, 2, GB>)) \
+  MOE_SMEM_ATTR((k_expert_mma<false, 4, GB>)) MOE_SMEM_ATTR((k_expert_mma<true, 4, GB>))
+  MOE_SMEM_ATTR_EM(2) MOE_SMEM_ATTR_EM(4) MOE_SMEM_ATTR_EM(8)
+#undef MOE_SMEM_ATTR_EM
   MOE_SMEM_ATTR((k_expert<1, false, 3>)) MOE_SMEM_ATTR((k_expert<2, false, 3>))
   MOE_SMEM_ATTR((k_expert<1, true, 3>)) MOE_SMEM_ATTR((k_expert<2, true, 3>))
   MOE_SMEM_ATTR((k_expert<1, false, 8>)) MOE_SMEM_ATTR((k_expert<2, false, 8>))
@@ -689,6 +764,10 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   if (const char* env = std::getenv("MOE_EXPERT_BULK")) L->expert_bulk = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_DENSE_BULK")) L->dense_bulk = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_EXPERT_BULK_MAX_T")) L->expert_bulk_max_t = std::max(0, std::atoi(env));
+  if (const char* env = std::getenv("MOE_EXPERT_MMA")) L->expert_mma = std::atoi(env) != 0;
+  if (const char* env = std::getenv("MOE_EXPERT_MMA_MAX_T")) L->expert_mma_max_t = std::max(0, std::atoi(env));
+  if (const char* env = std::getenv("MOE_EXPERT_MMA_PP"))
+    L->expert_mma_pp = std::max(4, std::min(EM_MAX_PAIRS, std::atoi(env)));
   if (const char* env = std::getenv("MOE_EXPERT_BULK_PB"))
     L->expert_bulk_pb = std::max(1, std::min(8, pow2_at_least(std::atoi(env), 8)));
   if (const char* env = std::getenv("MOE_FILL")) L->fill = std::atoi(env) != 0;
@@ -756,6 +835,33 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
       if (gated) MOE_TRY_CUDA(group_major(&L->gate_sbT, L->gate_sb, F, kin / G), "gate scales");
       MOE_TRY_CUDA(group_major(&L->up_sbT, L->up_sb, F, kin / G), "up scales");
       MOE_TRY_CUDA(group_major(&L->down_sbT, L->down_sb, kin, F / G), "down scales");
+    }
+    // the warp-MMA expert kernel's tiled codes and scale/bias words (4-bit codes)
+    auto tile_q = [&](uint32_t** dst, const uint32_t* src, int rows, int K) -> cudaError_t {
+      const size_t n = static_cast<size_t>(E) * rows * (K / 8);
+      cudaError_t e = L->alloc(reinterpret_cast<void**>(dst), n * 4);
+      if (e != cudaSuccess) return e;
+      const int blocks = static_cast<int>(std::min<size_t>((n + 255) / 256, 8192));
+      k_tile_codes<<<blocks, 256, 0, s>>>(src, *dst, E, rows, K);
+      return cudaGetLastError();
+    };
+    auto tile_sb = [&](uint32_t** dst, const uint32_t* src, int rows, int ngr) -> cudaError_t {
+      const size_t n = static_cast<size_t>(E) * rows * ngr;
+      cudaError_t e = L->alloc(reinterpret_cast<void**>(dst), n * 4);
+      if (e != cudaSuccess) return e;
+      const int blocks = static_cast<int>(std::min<size_t>((n + 255) / 256, 8192));
+      k_tile_sb<<<blocks, 256, 0, s>>>(src, *dst, E, rows, ngr);
+      return cudaGetLastError();
+    };
+    if (L->bits == 4 && L->expert_mma) {
+      if (gated) {
+        MOE_TRY_CUDA(tile_q(&L->gate_qt, L->gate_q, F, kin), "gate tiles");
+        MOE_TRY_CUDA(tile_sb(&L->gate_sbt, L->gate_sb, F, kin / G), "gate tiles");
+      }
+      MOE_TRY_CUDA(tile_q(&L->up_qt, L->up_q, F, kin), "up tiles");
+      MOE_TRY_CUDA(tile_sb(&L->up_sbt, L->up_sb, F, kin / G), "up tiles");
+      MOE_TRY_CUDA(tile_q(&L->down_qt, L->down_q, kin, F), "down tiles");
+      MOE_TRY_CUDA(tile_sb(&L->down_sbt, L->down_sb, kin, F / G), "down tiles");
     }
     if (Fs) {
       const size_t n = static_cast<size_t>(Fs) * H * adt;
@@ -1274,10 +1380,17 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
   // expert kernels of the gemv path: bulk-copied weight groups for up to
   // expert_bulk_max_t rows (latency-bound: every CTA's bytes requested at once),
   // register-streamed k_expert above (both give the same bits for a row)
+  const int slots_e = std::min(E, T * k);   // distinct-expert slots of the expert launches
+  // the warp-MMA expert kernel (4-bit codes in its tiled layout)
+  EmLaunch em_up, em_dn;
+  const bool use_mma = h->expert_mma && h->up_qt && T <= h->expert_mma_max_t;
+  const bool mma_up = use_mma && em_choose(kin, c.group_size, gated, T, h->expert_mma_pp, F, slots_e,
+                                           h->num_sms, &em_up);
+  const bool mma_dn = use_mma && em_choose(F, c.group_size, false, T, h->expert_mma_pp, kin, slots_e,
+                                           h->num_sms, &em_dn);
   const bool use_bulk = h->expert_bulk && !grouped && T <= h->expert_bulk_max_t && h->bits == 4;
   EbLaunch eb_up, eb_dn;
   int cps_up = 1, cps_dn = 1;
-  const int slots_e = std::min(E, T * k);   // distinct-expert slots of the expert launches
   // pairs per pass: a distinct expert of a small batch holds one or two of its
   // rows, and its weights stay resident in the ring across passes
   const int eb_pb = std::min(pow2_at_least(T, 8), h->expert_bulk_pb);
@@ -1506,7 +1619,15 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
       up.T = T;
       up.n_experts = E;
       up.gsh = c.group_size == 32 ? 0 : (c.group_size == 64 ? 1 : 2);
-      if (bulk_up) {
+      if (mma_up) {
+        up.qt = h->up_qt;
+        up.sbt = h->up_sbt;
+        up.qt_gate = gated ? h->gate_qt : nullptr;
+        up.sbt_gate = gated ? h->gate_sbt : nullptr;
+        up.trace = tslot("k_expert_mma_up");
+        if ((e = launch_expert_mma(up, em_up, slots * em_up.cps, cs, pdl)) != cudaSuccess) goto cuda_fail;
+        up.cps = em_up.cps;
+      } else if (bulk_up) {
         // one wave: at most per_sm CTAs on every SM (one when the filler CTAs
         // take the other slot)
         up.cps = cps_up;
@@ -1596,7 +1717,15 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
         dn.ccnt = h->ccnt;
         dn.T = T;
       }
-      if (bulk_dn) {
+      if (mma_dn) {
+        dn.qt = h->down_qt;
+        dn.sbt = h->down_sbt;
+        dn.qt_gate = nullptr;
+        dn.sbt_gate = nullptr;
+        em_dn.cps = std::min(em_dn.cps, kCombineCounters);
+        dn.trace = tslot("k_expert_mma_down");
+        if ((e = launch_expert_mma(dn, em_dn, slots * em_dn.cps, cs, pdl)) != cudaSuccess) goto cuda_fail;
+      } else if (bulk_dn) {
         dn.cps = std::min(cps_dn, kCombineCounters);
         dn.nst = eb_dn.nst;
         dn.trace = tslot("k_expert_bulk_down");
