@@ -59,10 +59,11 @@ class L2Flush:
         self.w.zero_()
         self.r.sum()
 STAGES = ["dense_in", "route", "expert_up", "expert_down", "dense_out"]
-# the kernels of the gemv path's stages (4-bit experts: the warp-MMA expert
-# kernel at every batch size)
-KERNEL_OF_STAGE = {"dense_in": "k_dense_in", "route": "k_route", "expert_up": "k_expert_mma",
-                   "expert_down": "k_expert_mma", "dense_out": "k_dense_bulk"}
+# the kernels of the gemv path's stages (bf16 layers with 4-bit experts: the
+# warp-MMA dense and expert kernels at every batch size; the routing rides in
+# the first dense pass)
+KERNEL_OF_STAGE = {"dense_in": "k_dense_mma", "route": "k_dense_mma", "expert_up": "k_expert_mma",
+                   "expert_down": "k_expert_mma", "dense_out": "k_dense_mma"}
 # the grouped path runs every projection through the tcgen05 GEMM (its split-K
 # sums and the combine ride in the same stages)
 KERNEL_OF_STAGE_GROUPED = {"dense_in": "k_umma2", "route": "k_route", "expert_up": "k_umma2",
@@ -80,6 +81,8 @@ KERNEL_SOURCES = {
     "k_umma2": ["moe_kernels.cuh", "moe_umma.cuh", "moe_umma2.cuh", "moe_layer.cu"],
     "k_expert_bulk": ["moe_kernels.cuh", "moe_expert_bulk.cuh", "moe_layer.cu"],
     "k_expert_mma": ["moe_kernels.cuh", "moe_expert_bulk.cuh", "moe_expert_mma.cuh", "moe_layer.cu"],
+    "k_dense_mma": ["moe_kernels.cuh", "moe_expert_bulk.cuh", "moe_expert_mma.cuh", "moe_dense_mma.cuh",
+                    "moe_layer.cu"],
     "k_dense_bulk": ["moe_kernels.cuh", "moe_expert_bulk.cuh", "moe_dense_bulk.cuh", "moe_layer.cu"],
 }
 

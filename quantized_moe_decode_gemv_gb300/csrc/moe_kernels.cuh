@@ -1086,6 +1086,19 @@ template <int TB>
 __global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_in(const __grid_constant__ DenseInArgs A) {
   extern __shared__ float4 smem4[];
   cta_stamp(A.trace, 0);
+  if (A.fuse_route && A.route_warm && blockIdx.x == 0) {
+    // The first run of the top-k code is slow (its instructions come from a
+    // cold L2): the routing CTA runs it once on whatever the buffers hold,
+    // writing nothing, before it waits for the previous kernel (that run reads
+    // no value this launch depends on and stores nothing).
+    RouteArgs D = A.route;
+    D.dry = 1;
+    // the few-pairs list code (a warp's sort of the ids as they stand) runs
+    // dry too; the counting path indexes shared memory by id, so not that
+    D.topk_only = D.T * D.k > 32;
+    route_block(D, reinterpret_cast<int*>(smem4));
+    cta_stamp(A.trace, 4);
+  }
   if (!A.dep_tail) griddep_wait();
   griddep_launch();
   cta_stamp(A.trace, 1);
@@ -1122,17 +1135,6 @@ __global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_in(const _
   cta_stamp(A.trace, 2);
   if (A.fuse_route && A.route_warm) {
     if (blockIdx.x == 0) {
-      // first execution of the top-k code is slow (instruction fetch from a
-      // cold L2 while the other CTAs stream weights): run it once on whatever
-      // the logits buffer holds, writing nothing, while the router rows are
-      // being computed
-      RouteArgs D = A.route;
-      D.dry = 1;
-      // the few-pairs list code (a warp's sort of the ids as they stand) runs
-      // dry too; the counting path indexes shared memory by id, so not that
-      D.topk_only = D.T * D.k > 32;
-      route_block(D, reinterpret_cast<int*>(smem4));
-      cta_stamp(A.trace, 4);
       __shared__ int s_ok;
       __syncthreads();
       if (threadIdx.x == 0) {

@@ -16,6 +16,7 @@
 #include "moe_kernels.cuh"
 #include "moe_expert_bulk.cuh"
 #include "moe_expert_mma.cuh"
+#include "moe_dense_mma.cuh"
 #include "moe_dense_bulk.cuh"
 #include "moe_umma.cuh"
 #include "moe_umma2.cuh"
@@ -64,6 +65,9 @@ struct moe_layer {
   // the warp-MMA expert kernel's tiled copies (4-bit codes only)
   uint32_t *gate_qt = nullptr, *up_qt = nullptr, *down_qt = nullptr;
   uint32_t *gate_sbt = nullptr, *up_sbt = nullptr, *down_sbt = nullptr;
+  // the warp-MMA dense kernel's tiled copies of the bf16 matrices
+  void *router_t = nullptr, *fc1_t = nullptr, *fc2_t = nullptr;
+  void *shg_t = nullptr, *shu_t = nullptr, *shd_t = nullptr;
   void *sh_gate = nullptr, *sh_up = nullptr, *sh_down = nullptr;
 
   // workspace
@@ -135,6 +139,7 @@ struct moe_layer {
   bool expert_mma = true;      // gemv path: warp-MMA expert kernel (4-bit codes)
   int expert_mma_max_t = 1 << 30;   // ... up to this many rows
   int expert_mma_pp = 8;       // its token pairs per pass (more pairs: more passes)
+  bool dense_mma = true;       // gemv path: warp-MMA dense passes (bf16 layers)
   int expert_bulk_pb = 2;      // its token pairs per pass
   int dense_bulk = 1;     // gemv path: shared expert and output projection by k_dense_bulk
   int fill = 0;           // gemv path: the shared expert as launches of its own beside the routed chain
@@ -540,6 +545,69 @@ static bool em_choose(int K, int G, bool gated, int T, int pp_cap, int n_rows, i
   }
   return false;
 }
+// The warp-MMA dense kernel's plan and grid: tokens per pass (all T rows up to
+// four n-tiles), warps per tile by K alone, then the ring with the most bytes
+// in flight on an SM (chunks of 1 or 2 64-column blocks, 2 to 4 stages a warp,
+// one or two CTAs an SM); one wave of CTAs over the 16-row tiles, plus the
+// routing CTA.  False when no plan fits shared memory.
+struct DmLaunch {
+  DmPlan plan{};
+  int tile_ctas = 1, grid = 1, route_ctas = 0;
+};
+static bool dm_choose(int K, int T, bool split, int ntiles, int t_router, int num_sms, bool fuse,
+                      size_t min_smem, DmLaunch* o) {
+  const int tpn = split ? 4 : 8;
+  const int nkc = K / 64;
+  const int ks = nkc >= 64 ? 8 : (nkc >= 32 ? 4 : (nkc >= 16 ? 2 : 1));
+  int ntp = 1;
+  while (ntp < 4 && ntp * tpn < T) ntp *= 2;
+  static const int kCkNs[][2] = {{2, 4}, {2, 3}, {1, 4}, {2, 2}, {1, 3}, {1, 2}};
+  for (; ntp >= 1; ntp >>= 1) {
+    long best = -1;
+    for (int per_sm = 1; per_sm <= (ntp == 1 ? 2 : 1); ++per_sm) {   // registers: two CTAs with one n-tile
+      const int budget = per_sm == 2 ? 110 * 1024 : kSmemMax - 2048;
+      for (const auto& cn : kCkNs) {
+        const DmPlan p = dm_plan(K, cn[0], cn[1], ntp * tpn, ks, split);
+        if (static_cast<size_t>(p.smem) > static_cast<size_t>(budget) || min_smem > static_cast<size_t>(budget)) continue;
+        const long inflight = static_cast<long>(per_sm) * cn[0] * cn[1];
+        if (inflight > best) {
+          best = inflight;
+          o->plan = p;
+          o->tile_ctas = std::max(1, std::min(ntiles, num_sms * per_sm - (fuse ? 1 : 0)));
+        }
+      }
+    }
+    if (best > 0) break;
+  }
+  if (ntp < 1) return false;
+  o->grid = o->tile_ctas + (fuse ? 1 : 0);
+  // router tiles first, about one a CTA on a quarter of the CTAs at most
+  // (dm_cta_tiles); a single tile CTA holds everything
+  o->route_ctas = fuse ? std::min(o->tile_ctas, std::min(t_router, std::max(1, o->tile_ctas / 4))) : 0;
+  return true;
+}
+template <int NTP, bool SPLIT>
+static cudaError_t launch_dense_mma_t(const DmArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl) {
+  return launch_ex<DmArgs>(k_dense_mma<NTP, SPLIT>, grid, EM_NT, smem, s, pdl, a);
+}
+static cudaError_t launch_dense_mma(DmArgs a, const DmLaunch& dl, size_t smem, cudaStream_t s, bool pdl) {
+  a.ck = dl.plan.ck;
+  a.ns = dl.plan.ns;
+  a.tp = dl.plan.tp;
+  a.ks = dl.plan.ks;
+  a.tile_ctas = dl.tile_ctas;
+  a.route_ctas = dl.route_ctas;
+  const int ntp = dm_ntp(dl.plan.tp, dl.plan.split);
+  if (dl.plan.split) {
+    if (ntp == 1) return launch_dense_mma_t<1, true>(a, dl.grid, smem, s, pdl);
+    if (ntp == 2) return launch_dense_mma_t<2, true>(a, dl.grid, smem, s, pdl);
+    return launch_dense_mma_t<4, true>(a, dl.grid, smem, s, pdl);
+  }
+  if (ntp == 1) return launch_dense_mma_t<1, false>(a, dl.grid, smem, s, pdl);
+  if (ntp == 2) return launch_dense_mma_t<2, false>(a, dl.grid, smem, s, pdl);
+  return launch_dense_mma_t<4, false>(a, dl.grid, smem, s, pdl);
+}
+
 template <int NTP, int GB>
 static cudaError_t launch_expert_mma_t(const ExpertArgs& a, bool gated, int grid, size_t smem, cudaStream_t s,
                                        bool pdl) {
@@ -640,6 +708,9 @@ static cudaError_t set_smem_attrs() {
   MOE_SMEM_ATTR((k_expert_mma<false, 2, GB>)) MOE_SMEM_ATTR((k_expert_mma<true, 2, GB>)) \
   MOE_SMEM_ATTR((k_expert_mma<false, 4, GB>)) MOE_SMEM_ATTR((k_expert_mma<true, 4, GB>))
   MOE_SMEM_ATTR_EM(2) MOE_SMEM_ATTR_EM(4) MOE_SMEM_ATTR_EM(8)
+  MOE_SMEM_ATTR((k_dense_mma<1, false>)) MOE_SMEM_ATTR((k_dense_mma<2, false>))
+  MOE_SMEM_ATTR((k_dense_mma<4, false>)) MOE_SMEM_ATTR((k_dense_mma<1, true>))
+  MOE_SMEM_ATTR((k_dense_mma<2, true>)) MOE_SMEM_ATTR((k_dense_mma<4, true>))
 #undef MOE_SMEM_ATTR_EM
   MOE_SMEM_ATTR((k_expert<1, false, 3>)) MOE_SMEM_ATTR((k_expert<2, false, 3>))
   MOE_SMEM_ATTR((k_expert<1, true, 3>)) MOE_SMEM_ATTR((k_expert<2, true, 3>))
@@ -766,6 +837,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   if (const char* env = std::getenv("MOE_EXPERT_BULK_MAX_T")) L->expert_bulk_max_t = std::max(0, std::atoi(env));
   if (const char* env = std::getenv("MOE_EXPERT_MMA")) L->expert_mma = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_EXPERT_MMA_MAX_T")) L->expert_mma_max_t = std::max(0, std::atoi(env));
+  if (const char* env = std::getenv("MOE_DENSE_MMA")) L->dense_mma = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_EXPERT_MMA_PP"))
     L->expert_mma_pp = std::max(4, std::min(EM_MAX_PAIRS, std::atoi(env)));
   if (const char* env = std::getenv("MOE_EXPERT_BULK_PB"))
@@ -873,6 +945,28 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
       MOE_TRY_CUDA(cudaMemcpyAsync(L->sh_up, w->sh_up, n, cudaMemcpyDeviceToDevice, s), "shared up copy");
       MOE_TRY_CUDA(L->alloc(&L->sh_down, n), "shared down");
       MOE_TRY_CUDA(cudaMemcpyAsync(L->sh_down, w->sh_down, n, cudaMemcpyDeviceToDevice, s), "shared down copy");
+    }
+    // the warp-MMA dense kernel's tiled bf16 matrices
+    if (L->dense_mma && c.act_dtype == MOE_DTYPE_BF16 && c.router_dtype == MOE_DTYPE_BF16) {
+      auto tile_d = [&](void** dst, const void* src, int rows, int K) -> cudaError_t {
+        const size_t n = static_cast<size_t>((rows + 15) / 16) * 16 * K;
+        cudaError_t e = L->alloc(dst, n * 2);
+        if (e != cudaSuccess) return e;
+        const int blocks = static_cast<int>(std::min<size_t>((n + 255) / 256, 8192));
+        k_tile_dense<<<blocks, 256, 0, s>>>(static_cast<const unsigned short*>(src),
+                                            static_cast<unsigned short*>(*dst), rows, K);
+        return cudaGetLastError();
+      };
+      MOE_TRY_CUDA(tile_d(&L->router_t, L->router_w, E, H), "router tiles");
+      if (Lt) {
+        MOE_TRY_CUDA(tile_d(&L->fc1_t, L->fc1, Lt, H), "fc1 tiles");
+        MOE_TRY_CUDA(tile_d(&L->fc2_t, L->fc2, H, Lt), "fc2 tiles");
+      }
+      if (Fs) {
+        if (gated) MOE_TRY_CUDA(tile_d(&L->shg_t, L->sh_gate, Fs, H), "shared gate tiles");
+        MOE_TRY_CUDA(tile_d(&L->shu_t, L->sh_up, Fs, H), "shared up tiles");
+        MOE_TRY_CUDA(tile_d(&L->shd_t, L->sh_down, H, Fs), "shared down tiles");
+      }
     }
     // workspace
     const size_t P = static_cast<size_t>(T) * k;
@@ -1436,7 +1530,53 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     const bool router_on_tc = grouped && c.router_dtype == c.act_dtype;
     DenseInArgs di{};
     int ns = 0;
-    if (!grouped || !router_on_tc) {
+    // the warp-MMA dense pass (bf16 layers on the gemv path)
+    DmArgs dm{};
+    DmLaunch dl_in;
+    size_t rsm = 0;
+    bool dm_in = false;
+    if (!grouped && h->router_t && !shared_apart) {
+      int n = 0;
+      auto dseg = [&](const void* w, int rows, int col0) {
+        dm.seg[n].w[0] = static_cast<const uint4*>(w);
+        dm.seg[n].w[1] = nullptr;
+        dm.seg[n].rows = rows;
+        dm.seg[n].col0 = col0;
+        ++n;
+      };
+      dseg(h->router_t, E, 0);
+      if (Lt) dseg(h->fc1_t, Lt, h->off_fc1);
+      if (Fs && gated) dseg(h->shg_t, Fs, h->off_shg);
+      if (Fs) dseg(h->shu_t, Fs, h->off_shu);
+      dm.nseg = n;
+      dm.seg_t0[0] = 0;
+      for (int i = 0; i < n; ++i) dm.seg_t0[i + 1] = dm.seg_t0[i] + (dm.seg[i].rows + 15) / 16;
+      dm.in[0] = DmIn{x, c.act_dtype, H, 0, 0, 0, 0, H};
+      dm.nparts = 1;
+      dm.T = T;
+      dm.out_mode = 0;
+      dm.outf = h->dense_in;
+      dm.out_ld = h->r_in;
+      dm.status = h->status;
+      dm.prefetch = 1;
+      rsm = fuse_route ? ROUTE_SMEM_BYTES + static_cast<size_t>(E) * ra.mask_words * 4 : 0;
+      dm_in = dm_choose(H, T, false, dm.seg_t0[n], dm.seg_t0[1], h->num_sms, fuse_route, rsm, &dl_in);
+    }
+    if (dm_in) {
+      if (fuse_route) {
+        dm.fuse_route = 1;
+        dm.route = ra;
+        dm.route_counter = h->route_counter;
+        // MOE_DEBUG_STALL (tests of failure detection, read at every launch):
+        // the routing CTA's bounded wait runs out
+        const char* stall = std::getenv("MOE_DEBUG_STALL");
+        dm.debug_stall = stall && std::atoi(stall) ? 1 : 0;
+      }
+      dm.trace = tslot("k_dense_mma_in");
+      if ((e = launch_dense_mma(dm, dl_in, std::max(static_cast<size_t>(dl_in.plan.smem), rsm), cs, pdl)) != cudaSuccess)
+        goto cuda_fail;
+      ++nl;
+    } else if (!grouped || !router_on_tc) {
       // CUDA-core pass: everything (gemv path) or only the router (grouped path
       // with a router dtype the tensor-core operands do not share)
       seg1(di.seg, ns, h->router_w, c.router_dtype, E, 0);
@@ -1852,8 +1992,42 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     dout.prefetch = (h->prefetch >> 2) & 1;
     const int tb_out = ks ? std::min(pow2_at_least(T, 8), dense_tb_cap(ks)) : pow2_at_least(T, 8);
     const int grid_out = std::max(1, std::min(h->num_sms * 2, (H + 3) / 4));
+    // the warp-MMA output pass (bf16 layers on the gemv path)
+    DmArgs dmo{};
+    DmLaunch dl_out;
+    bool dm_out = false;
+    if (!grouped && h->shd_t != nullptr && !shared_apart) {
+      dmo.nseg = 1;
+      dmo.seg[0].rows = H;
+      dmo.seg[0].col0 = 0;
+      dmo.seg_t0[0] = 0;
+      dmo.seg_t0[1] = (H + 15) / 16;
+      int np = 0;
+      if (Lt) {
+        dmo.seg[0].w[np] = static_cast<const uint4*>(h->fc2_t);
+        dmo.in[np++] = DmIn{h->comb, DT_FP32, kin, 0, 0, 0, 0, Lt};
+      }
+      dmo.seg[0].w[np] = static_cast<const uint4*>(h->shd_t);
+      dmo.in[np++] = DmIn{h->dense_in, DT_FP32, h->r_in, h->off_shu, h->off_shg, 1, c.act, Fs};
+      dmo.nparts = np;
+      dmo.T = T;
+      dmo.out_mode = 1;
+      dmo.x = x;
+      dmo.x_dt = c.act_dtype;
+      dmo.out = out;
+      dmo.delta = delta;
+      dmo.y_add = Lt ? nullptr : h->comb;
+      dmo.H = H;
+      dmo.status = h->status;
+      dmo.prefetch = 1;
+      dm_out = dm_choose(Lt + Fs, T, true, dmo.seg_t0[1], 0, h->num_sms, false, 0, &dl_out);
+    }
     DbLaunch dl;
-    if (h->dense_bulk && !grouped && ks && db_choose(dout.seg, dout.nseg, H, T, h->num_sms, &dl)) {
+    if (dm_out) {
+      dmo.trace = tslot("k_dense_mma_out");
+      if ((e = launch_dense_mma(dmo, dl_out, static_cast<size_t>(dl_out.plan.smem), cs, pdl && !side)) != cudaSuccess)
+        goto cuda_fail;
+    } else if (h->dense_bulk && !grouped && ks && db_choose(dout.seg, dout.nseg, H, T, h->num_sms, &dl)) {
       DbArgs d = db_from_out(dout, h->status);
       d.trace = tslot("k_dense_bulk_out");
       if ((e = launch_dense_bulk(d, dl, cs, pdl && !side)) != cudaSuccess) goto cuda_fail;
