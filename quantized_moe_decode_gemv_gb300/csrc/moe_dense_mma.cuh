@@ -208,13 +208,14 @@ __global__ void __launch_bounds__(EM_NT, NTP == 1 ? 2 : 1) k_dense_mma(const __g
     while (issued < min(NS, total)) issue_next();
   if (route_cta) {
     // The first run of the top-k code is slow (its instructions come from a
-    // cold L2), so the routing CTA runs it once on whatever the buffers hold,
-    // writing nothing, before it waits for the previous kernel: that run reads
-    // no value this launch depends on and stores nothing.
+    // cold L2), so the routing CTA runs its phases once, one per warp at once,
+    // on whatever the buffers hold, writing nothing, before it waits for the
+    // previous kernel: that run reads no value this launch depends on and
+    // stores nothing.
     RouteArgs D = A.route;
     D.dry = 1;
     D.topk_only = D.T * D.k > 32;
-    route_block(D, reinterpret_cast<int*>(dm_smem));
+    route_warm(D, reinterpret_cast<int*>(dm_smem));
     cta_stamp(A.trace, 4);
   }
   griddep_wait();

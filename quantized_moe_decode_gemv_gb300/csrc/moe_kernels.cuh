@@ -416,6 +416,173 @@ __device__ __forceinline__ void route_member(const RouteArgs& A, const float* z,
   topk_rounds<NPL>(kv, ev, sv, A.k, lane, my_id, my_z, ck, ci, cs);
 }
 
+// The warp-level phases of route_block, each compiled as its own function (not
+// inlined) so that a dry run can execute all of them at once, one per warp
+// (route_warm): the first run of each fetches its instructions from a cold L2,
+// and in parallel warps those fetches overlap instead of adding up.
+struct RoutePick {
+  int id;      // lane j < k: pick j's expert id
+  float z;     // its weight input (logit or sigmoid score)
+  int bad;     // a selection key of the warp's slice was not finite
+};
+
+// One member warp's top-k over its slice of the experts (route_member).
+template <int NPL>
+static __device__ __noinline__ RoutePick route_member_fn(const RouteArgs& A, const float* z, int W, int g,
+                                                         float* ck, int* ci, float* cs) {
+  RoutePick r{-1, 0.f, 0};
+  bool bad = false;
+  route_member<NPL>(A, z, W, g, threadIdx.x & 31, r.id, r.z, ck, ci, cs, bad);
+  r.bad = bad ? 1 : 0;
+  return r;
+}
+
+// The first warp of a row's group merges the W member lists of k picks.
+static __device__ __noinline__ RoutePick route_merge_fn(const float* cand_k, const int* cand_i,
+                                                        const float* cand_s, int warp, int W, int k) {
+  const int lane = threadIdx.x & 31;
+  RoutePick r{-1, 0.f, 0};
+  float kv[4], sv[4];
+  int ev[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int c = lane + 32 * i;            // candidate c of W * k
+    const int wl = c / k, jl = c - wl * k;
+    const bool ok = c < W * k;
+    kv[i] = ok ? cand_k[(warp + wl) * MAX_K + jl] : -INFINITY;
+    ev[i] = ok ? cand_i[(warp + wl) * MAX_K + jl] : 0x7fffffff;
+    sv[i] = ok ? cand_s[(warp + wl) * MAX_K + jl] : 0.f;
+  }
+  topk_rounds<4>(kv, ev, sv, k, lane, r.id, r.z, nullptr, nullptr, nullptr);
+  return r;
+}
+
+// Combine weights of row t (lane j < k holds pick j; its z is the logit for
+// softmax routing and the sigmoid score for sigmoid routing), written unless dry.
+static __device__ __noinline__ void route_weights_fn(const RouteArgs& A, const float* z, int t, int my_id,
+                                                     float my_z) {
+  const int lane = threadIdx.x & 31, k = A.k, E = A.E;
+  const float zj = (lane < k) ? my_z : 0.f;
+  float wv = 0.f;
+  if (A.router == ROUTER_SOFTMAX) {
+    const float m = __shfl_sync(0xffffffffu, zj, 0);   // largest selected logit
+    float den = 0.f;
+    if (A.renorm) {
+      const float ex = (lane < k) ? expf(zj - m) : 0.f;
+      den = ex;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+      wv = ex / den;
+    } else {
+      float mm = -INFINITY;
+      for (int i = lane; i < E; i += 32) mm = fmaxf(mm, __ldcg(z + i));
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+      for (int i = lane; i < E; i += 32) den += expf(__ldcg(z + i) - mm);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+      wv = (lane < k) ? expf(zj - mm) / den : 0.f;
+    }
+  } else {
+    const float sg = zj;
+    wv = sg;
+    if (A.renorm) {
+      float den = sg;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+      wv = sg / den;
+    }
+  }
+  wv *= A.scale;
+  if (lane < k && !A.dry) {
+    A.ids[t * k + lane] = my_id;
+    A.w[t * k + lane] = wv;
+    if (A.ext_ids) A.ext_ids[t * k + lane] = my_id;
+    if (A.ext_w) A.ext_w[t * k + lane] = wv;
+  }
+}
+
+// Few pairs (T k <= 32): one warp sorts the pairs by (expert, pair) with a
+// bitonic network; the first pair of each expert opens its group.  Writes the
+// route metadata unless dry.
+static __device__ __noinline__ void route_lists_few_fn(const RouteArgs& A) {
+  const int lane = threadIdx.x & 31;
+  const int P = A.T * A.k;
+  int v = lane < P ? ((A.ids[lane] << 5) | lane) : 0x7fffffff;
+#pragma unroll
+  for (int k2 = 2; k2 <= 32; k2 <<= 1) {
+#pragma unroll
+    for (int j = k2 >> 1; j > 0; j >>= 1) {
+      const int o = __shfl_xor_sync(0xffffffffu, v, j);
+      const bool asc = (lane & k2) == 0, low = (lane & j) == 0;
+      v = (low == asc) ? min(v, o) : max(v, o);
+    }
+  }
+  const bool valid = lane < P;
+  const int prev = __shfl_up_sync(0xffffffffu, v, 1);
+  const bool open = valid && (lane == 0 || (prev >> 5) != (v >> 5));
+  const unsigned om = __ballot_sync(0xffffffffu, open);
+  const int u = __popc(om & ((2u << lane) - 1u)) - 1;
+  int* uniq_e = A.meta + 1;
+  int* uniq_p0 = A.meta + 1 + A.umax;
+  int* pairs = A.meta + 2 + 2 * A.umax;
+  if (!A.dry) {
+    if (open) { uniq_e[u] = v >> 5; uniq_p0[u] = lane; }
+    if (valid) pairs[lane] = v & 31;
+    if (lane == 0) { A.meta[0] = __popc(om); uniq_p0[__popc(om)] = P; }
+#if MOE_CHECKS
+    if (lane == 0 && A.debug_bad == 1) uniq_e[0] = A.E + 3;
+    if (lane == 0 && A.debug_bad == 2) pairs[0] = P + 5;
+#endif
+  }
+}
+
+// Warps per row of route_block and the keys a lane holds.
+__device__ __forceinline__ void route_shape(const RouteArgs& A, int nwarp, int* W, int* npl) {
+  int w = A.E > 16 * 32 ? 2 : 1;            // at most 16 keys per lane
+  while (w < A.max_w && A.T * w * 2 <= nwarp) w *= 2;
+  *W = w;
+  *npl = (A.E + 32 * w - 1) / (32 * w);
+}
+
+template <int NPL>
+__device__ __forceinline__ RoutePick route_member_call(const RouteArgs& A, const float* z, int W, int g, float* ck,
+                                                       int* ci, float* cs) {
+  return route_member_fn<NPL>(A, z, W, g, ck, ci, cs);
+}
+__device__ __forceinline__ RoutePick route_member_any(const RouteArgs& A, int npl, const float* z, int W, int g,
+                                                      float* ck, int* ci, float* cs) {
+  if (npl <= 1) return route_member_call<1>(A, z, W, g, ck, ci, cs);
+  if (npl <= 2) return route_member_call<2>(A, z, W, g, ck, ci, cs);
+  if (npl <= 4) return route_member_call<4>(A, z, W, g, ck, ci, cs);
+  if (npl <= 8) return route_member_call<8>(A, z, W, g, ck, ci, cs);
+  return route_member_call<16>(A, z, W, g, ck, ci, cs);
+}
+
+// A dry run of route_block's warp-level phases, one per warp at once (reads
+// the buffers as they stand, writes no global memory; D.dry must be set).
+static __device__ void route_warm(const RouteArgs& D, int* smem) {
+  const int warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+  float* cand_k = reinterpret_cast<float*>(smem + 2 * MAX_E + 64);
+  int* cand_i = reinterpret_cast<int*>(cand_k + 32 * MAX_K);
+  float* cand_s = reinterpret_cast<float*>(cand_i + 32 * MAX_K);
+  int W, npl;
+  route_shape(D, nwarp, &W, &npl);
+  RoutePick r{-1, 0.f, 0};
+  if (warp == 0) {
+    r = route_member_any(D, npl, D.logits, W, 0, W > 1 ? cand_k + warp * MAX_K : nullptr,
+                         cand_i + warp * MAX_K, cand_s + warp * MAX_K);
+  } else if (warp == 1 % nwarp) {
+    r = route_merge_fn(cand_k, cand_i, cand_s, 0, 1, D.k);
+  } else if (warp == 2 % nwarp) {
+    route_weights_fn(D, D.logits, 0, r.id, r.z);
+  } else if (warp == 3 % nwarp && D.T * D.k <= 32 && !D.topk_only) {
+    route_lists_few_fn(D);
+  }
+  (void)r;
+  __syncthreads();
+}
+
 static __device__ __noinline__ void route_block(const RouteArgs& A, int* smem) {
   int* s_cnt = smem;
   int* s_scan_c = smem + MAX_E;
@@ -433,128 +600,35 @@ static __device__ __noinline__ void route_block(const RouteArgs& A, int* smem) {
   float* cand_k = reinterpret_cast<float*>(smem + 2 * MAX_E + 64);
   int* cand_i = reinterpret_cast<int*>(cand_k + 32 * MAX_K);
   float* cand_s = reinterpret_cast<float*>(cand_i + 32 * MAX_K);
-  int W = E > 16 * 32 ? 2 : 1;            // at most 16 keys per lane
-  while (W < A.max_w && A.T * W * 2 <= nwarp) W *= 2;
-  const int npl = (E + 32 * W - 1) / (32 * W);
+  int W, npl;
+  route_shape(A, nwarp, &W, &npl);
   const int rows_per_pass = nwarp / W;
   for (int tb = 0; tb < A.T; tb += rows_per_pass) {
     const int t = tb + warp / W, g = warp % W;
     const bool active = t < A.T;
     const float* z = A.logits + static_cast<int64_t>(active ? t : 0) * A.r_in;
-    int my_id = -1;
-    float my_z = 0.f;
-    bool bad = false;
+    RoutePick r{-1, 0.f, 0};
     float* ck = (W > 1) ? cand_k + warp * MAX_K : nullptr;
     int* ci = cand_i + warp * MAX_K;
     float* cs = cand_s + warp * MAX_K;
     if (active) {
-      if (npl <= 1) route_member<1>(A, z, W, g, lane, my_id, my_z, ck, ci, cs, bad);
-      else if (npl <= 2) route_member<2>(A, z, W, g, lane, my_id, my_z, ck, ci, cs, bad);
-      else if (npl <= 4) route_member<4>(A, z, W, g, lane, my_id, my_z, ck, ci, cs, bad);
-      else if (npl <= 8) route_member<8>(A, z, W, g, lane, my_id, my_z, ck, ci, cs, bad);
-      else route_member<16>(A, z, W, g, lane, my_id, my_z, ck, ci, cs, bad);
-      if (__any_sync(0xffffffffu, bad) && lane == 0 && !A.dry) atomicOr(A.status, STATUS_NONFINITE);
+      r = route_member_any(A, npl, z, W, g, ck, ci, cs);
+      if (__any_sync(0xffffffffu, r.bad) && lane == 0 && !A.dry) atomicOr(A.status, STATUS_NONFINITE);
     }
     if (W > 1) {
       __syncthreads();
-      if (active && g == 0) {
-        // merge the W lists of k picks held by warps warp .. warp + W - 1
-        float kv[4], sv[4];
-        int ev[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int c = lane + 32 * i;            // candidate c of W * k
-          const int wl = c / k, jl = c - wl * k;
-          const bool ok = c < W * k;
-          kv[i] = ok ? cand_k[(warp + wl) * MAX_K + jl] : -INFINITY;
-          ev[i] = ok ? cand_i[(warp + wl) * MAX_K + jl] : 0x7fffffff;
-          sv[i] = ok ? cand_s[(warp + wl) * MAX_K + jl] : 0.f;
-        }
-        topk_rounds<4>(kv, ev, sv, k, lane, my_id, my_z, nullptr, nullptr, nullptr);
-      }
+      if (active && g == 0) r = route_merge_fn(cand_k, cand_i, cand_s, warp, W, k);
     }
-    if (active && g == 0) {
-      // combine weights (lane j < k holds pick j; my_z is its logit for softmax
-      // routing and its sigmoid score for sigmoid routing)
-      const float zj = (lane < k) ? my_z : 0.f;
-      float wv = 0.f;
-      if (A.router == ROUTER_SOFTMAX) {
-        const float m = __shfl_sync(0xffffffffu, zj, 0);   // largest selected logit
-        float den = 0.f;
-        if (A.renorm) {
-          const float ex = (lane < k) ? expf(zj - m) : 0.f;
-          den = ex;
-  #pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-          wv = ex / den;
-        } else {
-          float mm = -INFINITY;
-          for (int i = lane; i < E; i += 32) mm = fmaxf(mm, __ldcg(z + i));
-  #pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
-          for (int i = lane; i < E; i += 32) den += expf(__ldcg(z + i) - mm);
-  #pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-          wv = (lane < k) ? expf(zj - mm) / den : 0.f;
-        }
-      } else {
-        const float sg = zj;
-        wv = sg;
-        if (A.renorm) {
-          float den = sg;
-  #pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-          wv = sg / den;
-        }
-      }
-      wv *= A.scale;
-      if (lane < k && !A.dry) {
-        A.ids[t * k + lane] = my_id;
-        A.w[t * k + lane] = wv;
-        if (A.ext_ids) A.ext_ids[t * k + lane] = my_id;
-        if (A.ext_w) A.ext_w[t * k + lane] = wv;
-      }
-  
-    }
+    if (active && g == 0) route_weights_fn(A, z, t, r.id, r.z);
     if (W > 1) __syncthreads();
   }
   if (A.topk_only) return;
   // ---- distinct experts and their pairs ----
   if (A.debug_times) tp[1] = global_ns();
   if (A.T * k <= 32) {
-    // few pairs: one warp sorts them by (expert, pair) with a bitonic network;
-    // the first pair of each expert opens its group
+    // few pairs: one warp sorts them (route_lists_few_fn)
     __syncthreads();
-    if (warp == 0) {
-      const int P = A.T * k;
-      int v = lane < P ? ((A.ids[lane] << 5) | lane) : 0x7fffffff;
-#pragma unroll
-      for (int k2 = 2; k2 <= 32; k2 <<= 1) {
-#pragma unroll
-        for (int j = k2 >> 1; j > 0; j >>= 1) {
-          const int o = __shfl_xor_sync(0xffffffffu, v, j);
-          const bool asc = (lane & k2) == 0, low = (lane & j) == 0;
-          v = (low == asc) ? min(v, o) : max(v, o);
-        }
-      }
-      const bool valid = lane < P;
-      const int prev = __shfl_up_sync(0xffffffffu, v, 1);
-      const bool open = valid && (lane == 0 || (prev >> 5) != (v >> 5));
-      const unsigned om = __ballot_sync(0xffffffffu, open);
-      const int u = __popc(om & ((2u << lane) - 1u)) - 1;
-      int* uniq_e = A.meta + 1;
-      int* uniq_p0 = A.meta + 1 + A.umax;
-      int* pairs = A.meta + 2 + 2 * A.umax;
-      if (!A.dry) {
-        if (open) { uniq_e[u] = v >> 5; uniq_p0[u] = lane; }
-        if (valid) pairs[lane] = v & 31;
-        if (lane == 0) { A.meta[0] = __popc(om); uniq_p0[__popc(om)] = P; }
-#if MOE_CHECKS
-        if (lane == 0 && A.debug_bad == 1) uniq_e[0] = A.E + 3;
-        if (lane == 0 && A.debug_bad == 2) pairs[0] = P + 5;
-#endif
-      }
-    }
+    if (warp == 0) route_lists_few_fn(A);
     if (A.debug_times && tid == 0)
       printf("route phases (ns): topk %llu list %llu\n", tp[1] - tp[0], global_ns() - tp[1]);
     return;
@@ -1088,15 +1162,16 @@ __global__ void __launch_bounds__(NT, dense_min_blocks<TB>()) k_dense_in(const _
   cta_stamp(A.trace, 0);
   if (A.fuse_route && A.route_warm && blockIdx.x == 0) {
     // The first run of the top-k code is slow (its instructions come from a
-    // cold L2): the routing CTA runs it once on whatever the buffers hold,
-    // writing nothing, before it waits for the previous kernel (that run reads
-    // no value this launch depends on and stores nothing).
+    // cold L2): the routing CTA runs its phases once, one per warp at once, on
+    // whatever the buffers hold, writing nothing, before it waits for the
+    // previous kernel (that run reads no value this launch depends on and
+    // stores nothing).
     RouteArgs D = A.route;
     D.dry = 1;
     // the few-pairs list code (a warp's sort of the ids as they stand) runs
     // dry too; the counting path indexes shared memory by id, so not that
     D.topk_only = D.T * D.k > 32;
-    route_block(D, reinterpret_cast<int*>(smem4));
+    route_warm(D, reinterpret_cast<int*>(smem4));
     cta_stamp(A.trace, 4);
   }
   if (!A.dep_tail) griddep_wait();
