@@ -266,9 +266,12 @@ const char *moe_layer_last_error(const moe_layer *h);
  * allocator, an engine that fixes its memory plan up front, or a
  * latency-critical path where an allocation could synchronise the device.
  * Creating a moe_layer handle allocates a workspace; this call does not.  It
- * applies the same router gemv and top-k selection rules as
- * moe_layer_forward_ex (the routing block fused into the dense gemv kernel)
- * to the same x, router weight, bias and routing options, and writes
+ * applies the top-k selection rules of moe_layer_forward_ex (the same routing
+ * block, stopped after the ids and weights) to fp32 router logits from its own
+ * CUDA-core router gemv of the same x, router weight, bias and routing
+ * options.  (The layer computes bf16 router logits on the tensor cores, with
+ * exact products and fp32 sums in another order, so the two agree on the ids
+ * except at exact ties and on the weights to a few ulps.)  It writes
  *   topk_ids[T, k]  int32, selection order (larger key first, ties to the
  *                   lower index, non-finite keys last),
  *   topk_w[T, k]    fp32 combine weights,

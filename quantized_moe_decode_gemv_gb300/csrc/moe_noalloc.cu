@@ -6,9 +6,9 @@
 // device memory up front, or code on a latency-critical path where a device
 // allocation (which may synchronise the device) is not acceptable.  Creating a
 // moe_layer handle allocates a workspace, so those callers use this entry
-// point instead.  It runs the router gemv and the top-k selection rules of
-// moe_layer_forward_ex (the routing block fused into the last router CTA of
-// the dense gemv kernel, stopping after the ids and weights) and writes
+// point instead.  It runs a CUDA-core router gemv (k_dense_in) and the top-k
+// selection rules of moe_layer_forward_ex (the same routing block, stopping
+// after the ids and weights) and writes
 // topk_ids / topk_w, but keeps its scratch -- the router logits, a completion
 // counter and a status word -- in a fixed-size array declared in this file.
 // The caller passes only inputs and outputs (and, optionally, a device word
