@@ -249,11 +249,8 @@ __global__ void __launch_bounds__(EM_NT, NTP == 1 ? 2 : 1) k_dense_mma(const __g
     if (pass) __syncthreads();   // every warp is done with the previous pass's B
     // ---- stage B: token tl -> n-tile tl / TPN, column tl % TPN (or the hi/lo
     // pair 2 (tl % 4), + 1); thread i takes block kb of token tl (kb fastest)
-    // padding columns of the last n-tile: zeros
-    for (int i = threadIdx.x; i < (nnt * TPN - ntok) * (SPLIT ? 2 : 1) * nkb * 4; i += EM_NT) {
-      const int tt = i & 3, r = i >> 2, kb = r % nkb, col = (SPLIT ? 2 * (ntok & 3) : (ntok & 7)) + r / nkb;
-      bfrag[(static_cast<int64_t>(nnt - 1) * nkb + kb) * 32 + col * 4 + tt] = make_uint2(0u, 0u);
-    }
+    // (the padding columns of the last n-tile are left as they are: an MMA
+    // output column depends on its own B column only, and theirs are not stored)
     const int nblk = ntok * nkb;
 #pragma unroll 2
     for (int i = threadIdx.x; i < nblk; i += EM_NT) {
