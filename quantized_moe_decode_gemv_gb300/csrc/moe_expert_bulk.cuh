@@ -325,27 +325,7 @@ __global__ void __launch_bounds__(NT, 2) k_expert_bulk(const __grid_constant__ E
       (void)eb_wait(eb_smem(bars + gg % nst), static_cast<uint32_t>(gg / nst) & 1u);
   }
   __syncthreads();
-  if (A.comb) {
-    // every CTA of this column range counts itself done; the last one combines
-    __shared__ int s_last;
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(A.ccnt + part, 1) == A.meta[0] - 1;
-    __syncthreads();
-    if (s_last) {
-      __threadfence();
-      const int cols = ne - nb;
-      for (int i = threadIdx.x; i < A.T * cols; i += NT) {
-        const int t = i / cols, n = nb + (i - t * cols);
-        float y = 0.f;
-        for (int p = 0; p < A.k; ++p)
-          y = fmaf(__ldcg(A.cwts + t * A.k + p),
-                   __ldcg(A.out + static_cast<int64_t>(t * A.k + p) * A.n_rows + n), y);
-        A.comb[static_cast<int64_t>(t) * A.n_rows + n] = y;
-      }
-      if (threadIdx.x == 0) A.ccnt[part] = 0;
-    }
-  }
+  if (A.comb) expert_fused_combine(A, part, nb, ne);
   cta_stamp(A.trace, 3);
 }
 

@@ -442,27 +442,7 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
       (void)eb_wait(eb_smem(bars + j % NS), static_cast<uint32_t>(j / NS) & 1u);
   }
   __syncthreads();
-  if (A.comb) {
-    // every CTA of this column range counts itself done; the last one combines
-    __shared__ int s_last;
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(A.ccnt + part, 1) == A.meta[0] - 1;
-    __syncthreads();
-    if (s_last) {
-      __threadfence();
-      const int cols = ne - nb;
-      for (int i = threadIdx.x; i < A.T * cols; i += EM_NT) {
-        const int tk = i / cols, n = nb + (i - tk * cols);
-        float yv = 0.f;
-        for (int p = 0; p < A.k; ++p)
-          yv = fmaf(__ldcg(A.cwts + tk * A.k + p),
-                    __ldcg(A.out + static_cast<int64_t>(tk * A.k + p) * A.n_rows + n), yv);
-        A.comb[static_cast<int64_t>(tk) * A.n_rows + n] = yv;
-      }
-      if (threadIdx.x == 0) A.ccnt[part] = 0;
-    }
-  }
+  if (A.comb) expert_fused_combine(A, part, nb, ne);
   cta_stamp(A.trace, 3);
 }
 

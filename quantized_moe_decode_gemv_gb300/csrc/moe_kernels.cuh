@@ -1512,6 +1512,40 @@ __device__ __forceinline__ float chunk_dot_b(const CodeChunk<BITS>& w, const flo
   }
 }
 
+// The weighted combine fused into the down projection's launch: every CTA of the
+// column range [nb, ne) (counter `part`) counts itself done, and the last one
+// writes comb[t, n] = sum_j w[t, j] * out[t*k + j, n], picks in order
+// j = 0 .. k-1 (one fp32 fma chain).  All of an output's loads are issued before
+// its chain, so they overlap instead of following one another.
+__device__ __forceinline__ void expert_fused_combine(const ExpertArgs& A, int part, int nb, int ne) {
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(A.ccnt + part, 1) == A.meta[0] - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int cols = ne - nb, k = A.k;
+#pragma unroll 2
+  for (int i = threadIdx.x; i < A.T * cols; i += blockDim.x) {
+    const int tk = i / cols, n = nb + (i - tk * cols);
+    const float* wr = A.cwts + tk * k;
+    const float* xr = A.out + static_cast<int64_t>(tk * k) * A.n_rows + n;
+    float wv[MAX_K], xv[MAX_K];
+#pragma unroll
+    for (int p = 0; p < MAX_K; ++p) {
+      wv[p] = p < k ? __ldcg(wr + p) : 0.f;
+      xv[p] = p < k ? __ldcg(xr + static_cast<int64_t>(p) * A.n_rows) : 0.f;
+    }
+    float yv = 0.f;
+#pragma unroll
+    for (int p = 0; p < MAX_K; ++p)
+      if (p < k) yv = fmaf(wv[p], xv[p], yv);
+    A.comb[static_cast<int64_t>(tk) * A.n_rows + n] = yv;
+  }
+  if (threadIdx.x == 0) A.ccnt[part] = 0;
+}
+
 template <int PB, bool GATED>
 constexpr int expert_min_blocks() { return PB <= 2 ? (GATED ? 2 : 3) : 2; }
 
@@ -1702,27 +1736,7 @@ __global__ void __launch_bounds__(NT, expert_min_blocks<PB, GATED>()) k_expert(c
     }
   }
   cta_stamp(A.trace, 2);
-  if (A.comb) {
-    // every CTA of this column range counts itself done; the last one combines
-    __shared__ int s_last;
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(A.ccnt + part, 1) == A.meta[0] - 1;
-    __syncthreads();
-    if (s_last) {
-      __threadfence();
-      const int cols = ne - nb;
-      for (int i = threadIdx.x; i < A.T * cols; i += NT) {
-        const int t = i / cols, n = nb + (i - t * cols);
-        float y = 0.f;
-        for (int p = 0; p < A.k; ++p)
-          y = fmaf(__ldcg(A.cwts + t * A.k + p),
-                   __ldcg(A.out + static_cast<int64_t>(t * A.k + p) * A.n_rows + n), y);
-        A.comb[static_cast<int64_t>(t) * A.n_rows + n] = y;
-      }
-      if (threadIdx.x == 0) A.ccnt[part] = 0;
-    }
-  }
+  if (A.comb) expert_fused_combine(A, part, nb, ne);
   cta_stamp(A.trace, 3);
 }
 
