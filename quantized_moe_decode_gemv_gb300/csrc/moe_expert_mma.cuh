@@ -161,10 +161,6 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
   uint64_t* bars = reinterpret_cast<uint64_t*>(em_smem_raw + P.bar_off) + warp * NS;
 
   const int ntiles = A.n_rows >> 4;
-  const int u = blockIdx.x / A.cps, part = blockIdx.x - u * A.cps;
-  const int tb = static_cast<int>(static_cast<int64_t>(part) * ntiles / A.cps);
-  const int te = static_cast<int>(static_cast<int64_t>(part + 1) * ntiles / A.cps);
-  const int nb = tb * 16, ne = te * 16;
   const int* uniq_e = A.meta + 1;
   const int* uniq_p0 = A.meta + 1 + A.umax;
   const int* pairs = A.meta + 2 + 2 * A.umax;
@@ -180,21 +176,81 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
   if (!A.pre_wait_phase) griddep_wait();
   griddep_launch();
   if (!A.pre_wait_phase) cta_stamp(A.trace, 1);
-  if (u >= A.meta[0]) { cta_stamp(A.trace, 3); return; }
-  if (A.max_pairs > 0 && uniq_p0[u + 1] - uniq_p0[u] > A.max_pairs) { cta_stamp(A.trace, 3); return; }
-  // a bad slot (index checks) copies nothing and writes nothing
-  const bool e_ok = idx_ok(A.status, CK_EXPERT_E, uniq_e[u], A.n_experts) &&
-                    range_ok(A.status, uniq_p0[u], uniq_p0[u + 1], n_pairs);
-  const int64_t e = e_ok ? uniq_e[u] : 0;
-  const int pa = uniq_p0[u], pe = e_ok ? uniq_p0[u + 1] : pa;
-  const int npass = (pe - pa + P.pp - 1) / P.pp;
+
+  // ---- work: the segments (distinct expert u, pass of up to pp of its pairs)
+  // of this routing, spread evenly over the grid.  With nseg <= grid CTAs,
+  // every segment has grid / nseg CTAs, each a contiguous range of its 16-row
+  // tiles; with more segments, CTA c takes segments c, c + grid, ... whole.
+  // (The grid is sized before the routing is known; spreading by the segments
+  // the routing made keeps the CTAs busy whatever the load.)
+  __shared__ int s_seg[6];   // nseg, slot and pass of a segment, tile range, first segment
+  auto npass_of = [&](int u) -> int {
+    const int n = uniq_p0[u + 1] - uniq_p0[u];
+    if (n <= 0 || (A.max_pairs > 0 && n > A.max_pairs)) return 0;
+    return (n + P.pp - 1) / P.pp;
+  };
+  const int nslots = A.meta[0], gsz = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
+  // warp 0: slot u and pass of segment sgi (the slots' pass counts scanned 32 at
+  // a time; the counts were just read, so these reads hit L1)
+  auto lookup = [&](int sgi) {
+    int base = 0;
+    for (int u0 = 0; u0 < nslots; u0 += 32) {
+      const int u = u0 + lane;
+      const int v = u < nslots ? npass_of(u) : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int tot = __shfl_sync(0xffffffffu, incl, 31);
+      const unsigned hit = __ballot_sync(0xffffffffu, sgi < base + incl && sgi >= base + incl - v);
+      if (hit) {
+        if (lane == __ffs(hit) - 1) { s_seg[1] = u; s_seg[2] = sgi - (base + incl - v); }
+        break;
+      }
+      base += tot;
+    }
+  };
+  if (warp == 0) {
+    // the segment count, this CTA's first segment and its tile range
+    int cnt = 0;
+    if (A.one_pass) {
+      // every slot has at most pp pairs: the segments are the slots.  Their
+      // entries come to L1 while the count is read.
+      if (lane * 32 < 2 * A.umax + 1)
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(uniq_e + lane * 32));
+      cnt = nslots;
+    } else {
+      for (int u = lane; u < nslots; u += 32) cnt += npass_of(u);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    }
+    const int ns_ = cnt;
+    // with nseg <= grid, m = grid / nseg CTAs a segment (at most one a tile),
+    // CTA j of them on tiles [j ntiles / m, (j + 1) ntiles / m): the same
+    // ranges in every segment; the CTAs past nseg m stay idle
+    int sg0 = cta, t0 = 0, t1 = ntiles;
+    if (ns_ <= gsz && ns_ > 0) {
+      const int m = min(ntiles, gsz / ns_);
+      sg0 = cta / m;
+      const int j = cta - sg0 * m;
+      t0 = j * ntiles / m;
+      t1 = (j + 1) * ntiles / m;
+    }
+    if (lane == 0) { s_seg[0] = ns_; s_seg[3] = t0; s_seg[4] = t1; s_seg[5] = sg0; }
+  }
+  __syncthreads();
+  const int nseg = s_seg[0];
+  const bool one_seg = nseg <= gsz;
+  const int tb = s_seg[3], te = s_seg[4];
+  int sg = s_seg[5];
 
   // The CTA's warps form EM_WARPS / KS tile slots of KS warps; warp ks of slot
   // sl takes the tiles tb + sl + nslot ti, and of each its part of K in
-  // chunks of CK 64-column blocks, once per pass.  The
-  // slot's partial sums meet in shared memory at the end of a tile.  The
-  // issuing lane and the computing warp walk the same sequence with
-  // incremental counters.
+  // chunks of CK 64-column blocks.  The slot's partial sums meet in shared
+  // memory at the end of a tile.  The issuing lane and the computing warp walk
+  // the same sequence with incremental counters.
   const int KS = P.ks, nslot = EM_WARPS / KS, slot = warp / KS, ks = warp - slot * KS;
   // K part of warp ks, in 64-column blocks [kc_lo, kc_hi): whole groups, and a
   // function of K and KS alone (not of the ring's chunk size, which the batch
@@ -203,10 +259,11 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
   const int kc_lo = (ks * nu / KS) * unit, kc_hi = ((ks + 1) * nu / KS) * unit;
   const int nit = (kc_hi - kc_lo + CK - 1) / CK;   // items (chunks) a tile
   const int my_tiles = (te - tb > slot) ? (te - tb - slot + nslot - 1) / nslot : 0;
-  const int total = my_tiles * nit * npass;
   const uint32_t* qm[2] = {GATED ? A.qt_gate : A.qt, A.qt};
   const uint32_t* sm[2] = {GATED ? A.sbt_gate : A.sbt, A.sbt};
-  int iss_ti = 0, iss_ch = 0, iss_s = 0, issued = 0;   // lane 0's issue position
+  int64_t e = 0;                        // the segment's expert
+  int total = 0;                        // this warp's items of the segment
+  int iss_ti = 0, iss_ch = 0, iss_s = 0, issued = 0, iss_seg = 0;   // lane 0's issue position
   auto issue_next = [&]() {
     const int64_t tile = e * ntiles + tb + slot + nslot * iss_ti;
     const int kc0 = kc_lo + iss_ch * CK, ckt = min(CK, kc_hi - kc0);
@@ -221,24 +278,40 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
       eb_bulk(eb_smem(st + NM * CK * 512 + m * CK * 128), sm[m] + (tile * ngr + g0) * 16, ng * 64u, bar);
     }
     ++issued;
+    ++iss_seg;
     if (++iss_s == NS) iss_s = 0;
-    if (++iss_ch == nit) { iss_ch = 0; if (++iss_ti == my_tiles) iss_ti = 0; }
+    if (++iss_ch == nit) { iss_ch = 0; ++iss_ti; }
   };
-  if (lane == 0)
-    while (issued < min(NS, total)) issue_next();
   // the pair ids of a pass (-1: failed its index check)
   __shared__ int s_pid[EM_MAX_PAIRS];
-  auto load_pids = [&](int p0, int npp) {
+  int p0 = 0, npp = 0, nnt = 0;
+  // Segment sg: its slot and pass (warp 0 scans the slots' pass counts), its
+  // pairs; the first copies of this warp's items go out at once.
+  auto prepare = [&](int sgi) {
+    if (warp == 0) {
+      if (!A.one_pass) lookup(sgi);
+      else if (lane == 0) { s_seg[1] = sgi; s_seg[2] = 0; }
+    }
+    __syncthreads();
+    const int u = s_seg[1], pass = s_seg[2];
+    // a bad slot (index checks) copies nothing and writes nothing
+    const bool e_ok = idx_ok(A.status, CK_EXPERT_E, uniq_e[u], A.n_experts) &&
+                      range_ok(A.status, uniq_p0[u], uniq_p0[u + 1], n_pairs);
+    e = e_ok ? uniq_e[u] : 0;
+    p0 = uniq_p0[u] + pass * P.pp;
+    npp = e_ok ? min(P.pp, uniq_p0[u + 1] - p0) : 0;
+    nnt = (npp + 3) >> 2;
+    total = npp > 0 ? my_tiles * nit : 0;
+    iss_ti = 0;
+    iss_ch = 0;
+    iss_seg = 0;
+    if (lane == 0)
+      for (int n0 = 0; n0 < min(NS, total); ++n0) issue_next();
     if (threadIdx.x < npp) {
       const int pid = pairs[p0 + threadIdx.x];
       s_pid[threadIdx.x] = idx_ok(A.status, CK_EXPERT_PAIR, pid, n_pairs) ? pid : -1;
     }
   };
-  if (A.pre_wait_phase) {
-    load_pids(pa, min(P.pp, pe - pa));   // the metadata is final: before the wait
-    griddep_wait();
-    cta_stamp(A.trace, 1);
-  }
 
   // input rows may be read as vectors when every row start is 16-byte aligned
   const bool xvec = A.xin_dt == DT_FP32 ? ((A.xin_off | A.xin_stride) & 3) == 0
@@ -246,10 +319,18 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
   bool ok = true;
   int gi = 0, gi_fail = 0, cs = 0;   // items consumed; the next one's stage
   uint32_t phase = 0;                // its mbarrier phase
-  for (int pass = 0; pass < npass; ++pass) {
-    const int p0 = pa + pass * P.pp, npp = min(P.pp, pe - p0), nnt = (npp + 3) >> 2;
-    if (pass) __syncthreads();   // every warp is done with the previous pass's B and ids
-    if (pass || !A.pre_wait_phase) load_pids(p0, npp);
+  __shared__ int s_cflag[EM_NT];
+  // the down projection's metadata is final at launch: its first segment
+  // (copies and pair ids) is prepared before the wait
+  bool waited = !A.pre_wait_phase;
+  for (bool first = true; nseg > 0 && sg < nseg; sg += (one_seg ? nseg : gsz), first = false) {
+    if (!first) __syncthreads();   // every warp is done with the previous segment's B and ids
+    prepare(sg);
+    if (!waited) {
+      griddep_wait();
+      cta_stamp(A.trace, 1);
+      waited = true;
+    }
     __syncthreads();
     // ---- stage B: pair pl -> n-tile pl / 4, columns 2 (pl % 4) (hi) and + 1 (lo).
     // Thread i takes block kb of pair pl (i = pl * nkb + kb): its 16 elements,
@@ -293,13 +374,15 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
       if (i < nblk && (kb & (GB - 1)) == 0) xs[pl * ngr + kb / GB] = sx;
     }
     __syncthreads();
-    if (pass == 0) cta_stamp(A.trace, 6);
+    if (first) cta_stamp(A.trace, 6);
 
     // ---- this warp's tiles
     const uint2* bl = bfrag + lane;   // + (nt * nkb + kb) * 32
     const float* xsl = xs + t * ngr;  // + nt * 4 * ngr + grp
     float y[NTP][2], yg[NTP][2], acc[NTP][4], accg[NTP][4];
-    for (int ti = 0; ti < my_tiles; ++ti) {
+    // (a segment whose slot failed its index check issued no copies: no tiles)
+    const int seg_tiles = npp > 0 ? my_tiles : 0;
+    for (int ti = 0; ti < seg_tiles; ++ti) {
      const int rt = tb + slot + nslot * ti;
 #pragma unroll
      for (int nt = 0; nt < NTP; ++nt) y[nt][0] = y[nt][1] = yg[nt][0] = yg[nt][1] = 0.f;
@@ -380,7 +463,7 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
         }
       }
       __syncwarp();   // every lane has read the stage
-      if (lane == 0 && ok && issued < total) issue_next();
+      if (lane == 0 && ok && iss_seg < total) issue_next();
       if (++cs == NS) { cs = 0; phase ^= 1u; }
      }
      // The slot's partial sums: each warp stores its part of K; the slot's
@@ -433,7 +516,35 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
        }
      }
     }
+    // The down projection's combine, per 16-row tile: every segment's CTAs
+    // count each tile they finished; the CTA that completes a tile's count
+    // (nseg: one per segment) writes its combined rows for all T tokens.
+    if (A.comb) {
+      __threadfence();
+      __syncthreads();
+      for (int c0 = tb; c0 < te; c0 += EM_NT) {
+        // count this segment's tiles; the ones this CTA completed go to a list,
+        // and their rows x T tokens are combined by all threads in one pass
+        if (threadIdx.x == 0) s_seg[0] = 0;
+        __syncthreads();
+        const int tt = c0 + static_cast<int>(threadIdx.x);
+        if (tt < te && atomicAdd(A.ccnt + tt, 1) == nseg - 1) s_cflag[atomicAdd(&s_seg[0], 1)] = tt;
+        __syncthreads();
+        const int nf = s_seg[0];
+        if (nf) {
+          __threadfence();
+          for (int i = threadIdx.x; i < nf * A.T * 16; i += EM_NT) {
+            const int f = i / (A.T * 16), r = i - f * (A.T * 16);
+            expert_combine_one(A, r >> 4, s_cflag[f] * 16 + (r & 15));
+          }
+          __syncthreads();
+          if (threadIdx.x < nf) A.ccnt[s_cflag[threadIdx.x]] = 0;
+        }
+        __syncthreads();
+      }
+    }
   }
+  if (!waited) griddep_wait();
   cta_stamp(A.trace, 2);
   if (!ok && lane == 0) {
     // after a wait ran out: let this warp's copies in flight land (bounded)
@@ -441,8 +552,6 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
     for (int j = gi_fail; j < issued; ++j)
       (void)eb_wait(eb_smem(bars + j % NS), static_cast<uint32_t>(j / NS) & 1u);
   }
-  __syncthreads();
-  if (A.comb) expert_fused_combine(A, part, nb, ne);
   cta_stamp(A.trace, 3);
 }
 

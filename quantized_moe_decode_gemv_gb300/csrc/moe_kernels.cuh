@@ -1401,11 +1401,12 @@ struct ExpertArgs {
   int cps;                 // CTAs per distinct-expert slot (grid = umax * cps)
   int max_pairs;           // > 0: slots with more token pairs are left to the grouped GEMM
   // weighted combine fused into the down projection: the last CTA to finish a
-  // column range [nb, ne) (over all distinct experts) writes
-  // comb[t, n] = sum_j w[t, j] * out[t*k + j, n], picks in order j = 0..k-1
+  // column range [nb, ne) (k_expert_mma: a 16-row tile) over all distinct
+  // experts writes comb[t, n] = sum_j w[t, j] * out[t*k + j, n], picks in
+  // order j = 0..k-1
   float* comb;             // [T, n_rows] or null
   const float* cwts;       // [T*k] combine weights
-  int* ccnt;               // [cps] completion counters (zero between launches)
+  int* ccnt;               // completion counters, one a range or tile (zero between launches)
   int T;
   int nst;                 // k_expert_bulk: shared-memory stages of the tile ring
   int* status;             // device status words (timeout bit; index checks)
@@ -1418,6 +1419,7 @@ struct ExpertArgs {
   const uint32_t* qt_gate;
   const uint32_t* sbt_gate;
   int ck, pp, ks;   // ks: warps sharing a tile's K range (1, 2 or 4)
+  int one_pass;     // every slot has at most pp pairs (T <= pp): one segment a slot
   unsigned long long* trace;   // diagnostics: CTA stamps or null
 };
 
@@ -1517,6 +1519,25 @@ __device__ __forceinline__ float chunk_dot_b(const CodeChunk<BITS>& w, const flo
 // writes comb[t, n] = sum_j w[t, j] * out[t*k + j, n], picks in order
 // j = 0 .. k-1 (one fp32 fma chain).  All of an output's loads are issued before
 // its chain, so they overlap instead of following one another.
+// comb[tk, n] = sum_j w[tk, j] * out[tk*k + j, n], picks in order j = 0 .. k-1
+// (one fp32 fma chain), every load issued before the chain
+__device__ __forceinline__ void expert_combine_one(const ExpertArgs& A, int tk, int n) {
+  const int k = A.k;
+  const float* wr = A.cwts + tk * k;
+  const float* xr = A.out + static_cast<int64_t>(tk * k) * A.n_rows + n;
+  float wv[MAX_K], xv[MAX_K];
+#pragma unroll
+  for (int p = 0; p < MAX_K; ++p) {
+    wv[p] = p < k ? __ldcg(wr + p) : 0.f;
+    xv[p] = p < k ? __ldcg(xr + static_cast<int64_t>(p) * A.n_rows) : 0.f;
+  }
+  float yv = 0.f;
+#pragma unroll
+  for (int p = 0; p < MAX_K; ++p)
+    if (p < k) yv = fmaf(wv[p], xv[p], yv);
+  A.comb[static_cast<int64_t>(tk) * A.n_rows + n] = yv;
+}
+
 __device__ __forceinline__ void expert_fused_combine(const ExpertArgs& A, int part, int nb, int ne) {
   __shared__ int s_last;
   __threadfence();
@@ -1525,23 +1546,11 @@ __device__ __forceinline__ void expert_fused_combine(const ExpertArgs& A, int pa
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  const int cols = ne - nb, k = A.k;
+  const int cols = ne - nb;
 #pragma unroll 2
   for (int i = threadIdx.x; i < A.T * cols; i += blockDim.x) {
-    const int tk = i / cols, n = nb + (i - tk * cols);
-    const float* wr = A.cwts + tk * k;
-    const float* xr = A.out + static_cast<int64_t>(tk * k) * A.n_rows + n;
-    float wv[MAX_K], xv[MAX_K];
-#pragma unroll
-    for (int p = 0; p < MAX_K; ++p) {
-      wv[p] = p < k ? __ldcg(wr + p) : 0.f;
-      xv[p] = p < k ? __ldcg(xr + static_cast<int64_t>(p) * A.n_rows) : 0.f;
-    }
-    float yv = 0.f;
-#pragma unroll
-    for (int p = 0; p < MAX_K; ++p)
-      if (p < k) yv = fmaf(wv[p], xv[p], yv);
-    A.comb[static_cast<int64_t>(tk) * A.n_rows + n] = yv;
+    const int tk = i / cols;
+    expert_combine_one(A, tk, nb + (i - tk * cols));
   }
   if (threadIdx.x == 0) A.ccnt[part] = 0;
 }

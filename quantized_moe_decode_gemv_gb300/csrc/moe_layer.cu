@@ -621,12 +621,15 @@ static cudaError_t launch_expert_mma_g(const ExpertArgs& a, bool gated, int pp, 
   if (pp <= 8) return launch_expert_mma_t<2, GB>(a, gated, grid, smem, s, pdl);
   return launch_expert_mma_t<4, GB>(a, gated, grid, smem, s, pdl);
 }
-static cudaError_t launch_expert_mma(ExpertArgs a, const EmLaunch& el, int grid, cudaStream_t s, bool pdl) {
+static cudaError_t launch_expert_mma(ExpertArgs a, const EmLaunch& el, int T, int grid, cudaStream_t s,
+                                     bool pdl) {
   a.ck = el.plan.ck;
   a.nst = el.plan.ns;
   a.pp = el.plan.pp;
   a.ks = el.plan.ks;
   a.cps = el.cps;
+  // a slot holds at most T pairs (a token picks an expert once)
+  a.one_pass = T <= a.pp && (a.max_pairs <= 0 || a.max_pairs >= T);
   const size_t smem = static_cast<size_t>(el.plan.smem);
   const bool gated = a.qt_gate != nullptr;
   switch (a.G) {
@@ -1768,7 +1771,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
         up.qt_gate = gated ? h->gate_qt : nullptr;
         up.sbt_gate = gated ? h->gate_sbt : nullptr;
         up.trace = tslot("k_expert_mma_up");
-        if ((e = launch_expert_mma(up, em_up, slots * em_up.cps, cs, pdl)) != cudaSuccess) goto cuda_fail;
+        if ((e = launch_expert_mma(up, em_up, T, h->num_sms * em_up.per_sm, cs, pdl)) != cudaSuccess) goto cuda_fail;
         up.cps = em_up.cps;
       } else if (bulk_up) {
         // one wave: at most per_sm CTAs on every SM (one when the filler CTAs
@@ -1865,9 +1868,8 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
         dn.sbt = h->down_sbt;
         dn.qt_gate = nullptr;
         dn.sbt_gate = nullptr;
-        em_dn.cps = std::min(em_dn.cps, kCombineCounters);
         dn.trace = tslot("k_expert_mma_down");
-        if ((e = launch_expert_mma(dn, em_dn, slots * em_dn.cps, cs, pdl)) != cudaSuccess) goto cuda_fail;
+        if ((e = launch_expert_mma(dn, em_dn, T, h->num_sms * em_dn.per_sm, cs, pdl)) != cudaSuccess) goto cuda_fail;
       } else if (bulk_dn) {
         dn.cps = std::min(cps_dn, kCombineCounters);
         dn.nst = eb_dn.nst;
