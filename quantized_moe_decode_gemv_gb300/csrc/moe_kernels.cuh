@@ -38,6 +38,7 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 #include <cstdio>
+#include <climits>
 
 namespace moe {
 
@@ -335,49 +336,52 @@ constexpr int ROUTE_SMEM_BYTES = (2 * MAX_E + 64 + ROUTE_CAND_WORDS) * 4;
 // order.  Logits are read with ld.global.cg, so this may run in the last CTA
 // of the kernel that produced them.
 
-// k rounds of selection over register-held keys: every round takes the lane's
-// best remaining key with a pairwise tree, then the warp's best by a
-// butterfly; the owner lane retires it.  Lane j ends with pick j (its expert
-// id and its weight input sv).  With ck != nullptr lanes j < k also write the
-// picks to ck/ci/cs[j] (a candidate list for a later merge).
+// k rounds of selection over register-held keys.  Every round takes the
+// lane's best remaining key with a pairwise tree (keys as order-preserving
+// integers, ties to the smaller expert id, its weight input carried along),
+// then the warp's largest key by a warp max and, among the lanes that hold
+// it, the smallest expert id by a warp min: pick j.  The lane that holds it
+// writes its key, id and weight input to ck/ci/cs[j] (ck and ci may be null;
+// cs is the warp's scratch of MAX_K) and retires it.  Lane j ends with pick
+// j (its expert id and its weight input).  The two warp reductions are the
+// round's only collectives.
 template <int NPL>
 __device__ __forceinline__ void topk_rounds(float (&kv)[NPL], const int (&ev)[NPL], const float (&sv)[NPL],
                                             int k, int lane, int& my_id, float& my_z, float* ck,
                                             int* ci, float* cs) {
-  for (int j = 0; j < k; ++j) {
-    float tk[NPL];
-    int tix[NPL];
+  int ik[NPL];   // keys carry no -0 and no NaN
 #pragma unroll
-    for (int i = 0; i < NPL; ++i) { tk[i] = kv[i]; tix[i] = ev[i]; }
+  for (int i = 0; i < NPL; ++i) ik[i] = ordered_bits(kv[i]);
+  for (int j = 0; j < k; ++j) {
+    int tk[NPL], tix[NPL];
+    float ts[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) { tk[i] = ik[i]; tix[i] = ev[i]; ts[i] = sv[i]; }
 #pragma unroll
     for (int w = NPL / 2; w >= 1; w >>= 1) {
 #pragma unroll
       for (int i = 0; i < w; ++i) {
-        const bool b1 = key_better(tk[i + w], tix[i + w], tk[i], tix[i]);
+        const bool b1 = tk[i + w] > tk[i] || (tk[i + w] == tk[i] && tix[i + w] < tix[i]);
         tk[i] = b1 ? tk[i + w] : tk[i];
         tix[i] = b1 ? tix[i + w] : tix[i];
+        ts[i] = b1 ? ts[i + w] : ts[i];
       }
     }
-    // warp best: the largest key by an integer max over order-preserving
-    // bits (keys carry no -0 and no NaN), then the smallest expert id among
-    // the lanes that hold it
-    const int ik = ordered_bits(tk[0]);
-    const int mx = __reduce_max_sync(0xffffffffu, ik);
+    const int mx = __reduce_max_sync(0xffffffffu, tk[0]);
     const int bi = static_cast<int>(__reduce_min_sync(
-        0xffffffffu, ik == mx ? static_cast<unsigned>(tix[0]) : 0xffffffffu));
-    const float bk = from_ordered_bits(mx);
-    // the owner lane retires the key and publishes its weight input
-    float ws = 0.f;
-    int owner = -1;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      if (ev[i] == bi) { ws = sv[i]; kv[i] = -INFINITY; owner = lane; }
+        0xffffffffu, tk[0] == mx ? static_cast<unsigned>(tix[0]) : 0xffffffffu));
+    if (tk[0] == mx && tix[0] == bi) {
+      cs[j] = ts[0];
+      if (ck) { ck[j] = from_ordered_bits(mx); ci[j] = bi; }
     }
-    owner = __reduce_max_sync(0xffffffffu, owner);
-    ws = __shfl_sync(0xffffffffu, ws, owner < 0 ? 0 : owner);
-    if (lane == j) { my_id = bi; my_z = ws; }
-    if (ck && lane == j) { ck[j] = bk; ci[j] = bi; cs[j] = ws; }
+#pragma unroll
+    for (int i = 0; i < NPL; ++i)
+      if (ev[i] == bi) ik[i] = INT_MIN;
+    if (lane == j) my_id = bi;
   }
+  __syncwarp();
+  my_z = lane < k ? cs[lane] : 0.f;
+  __syncwarp();
 }
 
 // Keys of one member warp: experts lane + 32 * (g + W * i), i < NPL.
@@ -439,7 +443,7 @@ static __device__ __noinline__ RoutePick route_member_fn(const RouteArgs& A, con
 
 // The first warp of a row's group merges the W member lists of k picks.
 static __device__ __noinline__ RoutePick route_merge_fn(const float* cand_k, const int* cand_i,
-                                                        const float* cand_s, int warp, int W, int k) {
+                                                        float* cand_s, int warp, int W, int k) {
   const int lane = threadIdx.x & 31;
   RoutePick r{-1, 0.f, 0};
   float kv[4], sv[4];
@@ -453,28 +457,35 @@ static __device__ __noinline__ RoutePick route_merge_fn(const float* cand_k, con
     ev[i] = ok ? cand_i[(warp + wl) * MAX_K + jl] : 0x7fffffff;
     sv[i] = ok ? cand_s[(warp + wl) * MAX_K + jl] : 0.f;
   }
-  topk_rounds<4>(kv, ev, sv, k, lane, r.id, r.z, nullptr, nullptr, nullptr);
+  topk_rounds<4>(kv, ev, sv, k, lane, r.id, r.z, nullptr, nullptr, cand_s + warp * MAX_K);
   return r;
 }
 
 // Combine weights of row t (lane j < k holds pick j; its z is the logit for
-// softmax routing and the sigmoid score for sigmoid routing), written unless dry.
+// softmax routing and the sigmoid score for sigmoid routing; zs[j] holds pick
+// j's z for every lane), written unless dry.  Renormalising sums run over the
+// picks in order j = 0..k-1.  With few pairs (T k <= 32) the ids also go to
+// s_ids[t k + j] for the lists.
 static __device__ __noinline__ void route_weights_fn(const RouteArgs& A, const float* z, int t, int my_id,
-                                                     float my_z) {
-  const int lane = threadIdx.x & 31, k = A.k, E = A.E;
+                                                     float my_z, const float* zs, int* s_ids) {
+  // the arguments' fields, read once before any store
+  const int lane = threadIdx.x & 31, k = A.k, E = A.E, T = A.T;
+  const bool softmax = A.router == ROUTER_SOFTMAX, renorm = A.renorm != 0, dry = A.dry != 0;
+  const float scale = A.scale;
+  int* ids = A.ids;
+  float* w = A.w;
+  int* ext_ids = A.ext_ids;
+  float* ext_w = A.ext_w;
   const float zj = (lane < k) ? my_z : 0.f;
   float wv = 0.f;
-  if (A.router == ROUTER_SOFTMAX) {
-    const float m = __shfl_sync(0xffffffffu, zj, 0);   // largest selected logit
-    float den = 0.f;
-    if (A.renorm) {
-      const float ex = (lane < k) ? expf(zj - m) : 0.f;
-      den = ex;
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-      wv = ex / den;
+  if (softmax) {
+    const float m = zs[0];   // the largest selected logit
+    if (renorm) {
+      float den = 0.f;
+      for (int j = 0; j < k; ++j) den += expf(zs[j] - m);
+      wv = (lane < k) ? expf(zj - m) / den : 0.f;
     } else {
-      float mm = -INFINITY;
+      float mm = -INFINITY, den = 0.f;
       for (int i = lane; i < E; i += 32) mm = fmaxf(mm, __ldcg(z + i));
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
@@ -484,40 +495,39 @@ static __device__ __noinline__ void route_weights_fn(const RouteArgs& A, const f
       wv = (lane < k) ? expf(zj - mm) / den : 0.f;
     }
   } else {
-    const float sg = zj;
-    wv = sg;
-    if (A.renorm) {
-      float den = sg;
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-      wv = sg / den;
+    wv = zj;
+    if (renorm) {
+      float den = 0.f;
+      for (int j = 0; j < k; ++j) den += zs[j];
+      wv = zj / den;
     }
   }
-  wv *= A.scale;
-  if (lane < k && !A.dry) {
-    A.ids[t * k + lane] = my_id;
-    A.w[t * k + lane] = wv;
-    if (A.ext_ids) A.ext_ids[t * k + lane] = my_id;
-    if (A.ext_w) A.ext_w[t * k + lane] = wv;
+  wv *= scale;
+  if (lane < k && T * k <= 32) s_ids[t * k + lane] = my_id;
+  if (lane < k && !dry) {
+    ids[t * k + lane] = my_id;
+    w[t * k + lane] = wv;
+    if (ext_ids) ext_ids[t * k + lane] = my_id;
+    if (ext_w) ext_w[t * k + lane] = wv;
   }
 }
 
-// Few pairs (T k <= 32): one warp sorts the pairs by (expert, pair) with a
-// bitonic network; the first pair of each expert opens its group.  Writes the
-// route metadata unless dry.
-static __device__ __noinline__ void route_lists_few_fn(const RouteArgs& A) {
+// Few pairs (T k <= 32): one warp sorts the pairs by (expert, pair): pair p's
+// rank is the number of pairs with a smaller (expert, pair) key, and it goes
+// to that place in s_ids[32..64); the first pair of each expert opens its
+// group.  The pairs' ids come from s_ids[0..P) (written by route_weights_fn).
+// Writes the route metadata unless dry.
+static __device__ __noinline__ void route_lists_few_fn(const RouteArgs& A, int* s_ids) {
   const int lane = threadIdx.x & 31;
   const int P = A.T * A.k;
-  int v = lane < P ? ((A.ids[lane] << 5) | lane) : 0x7fffffff;
-#pragma unroll
-  for (int k2 = 2; k2 <= 32; k2 <<= 1) {
-#pragma unroll
-    for (int j = k2 >> 1; j > 0; j >>= 1) {
-      const int o = __shfl_xor_sync(0xffffffffu, v, j);
-      const bool asc = (lane & k2) == 0, low = (lane & j) == 0;
-      v = (low == asc) ? min(v, o) : max(v, o);
-    }
-  }
+  int v = lane < P ? ((s_ids[lane] << 5) | lane) : 0x7fffffff;
+  int rank = 0;
+  for (int q = 0; q < P; ++q) rank += __shfl_sync(0xffffffffu, v, q) < v;
+  int* s_sorted = s_ids + 32;
+  if (lane < P) s_sorted[rank] = v;
+  __syncwarp();
+  v = lane < P ? s_sorted[lane] : 0x7fffffff;
+  __syncwarp();
   const bool valid = lane < P;
   const int prev = __shfl_up_sync(0xffffffffu, v, 1);
   const bool open = valid && (lane == 0 || (prev >> 5) != (v >> 5));
@@ -575,9 +585,9 @@ static __device__ void route_warm(const RouteArgs& D, int* smem) {
   } else if (warp == 1 % nwarp) {
     r = route_merge_fn(cand_k, cand_i, cand_s, 0, 1, D.k);
   } else if (warp == 2 % nwarp) {
-    route_weights_fn(D, D.logits, 0, r.id, r.z);
+    route_weights_fn(D, D.logits, 0, r.id, r.z, cand_s + warp * MAX_K, smem);
   } else if (warp == 3 % nwarp && D.T * D.k <= 32 && !D.topk_only) {
-    route_lists_few_fn(D);
+    route_lists_few_fn(D, smem + 32);
   }
   (void)r;
   __syncthreads();
@@ -592,7 +602,7 @@ static __device__ __noinline__ void route_block(const RouteArgs& A, int* smem) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = blockDim.x >> 5;
   const int nthr = blockDim.x;
   const int E = A.E, k = A.k;
-  unsigned long long tp[8];
+  unsigned long long tp[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   if (A.debug_times) tp[0] = global_ns();
 
   // W warps cooperate on one row (more when there are few rows), each with
@@ -615,11 +625,14 @@ static __device__ __noinline__ void route_block(const RouteArgs& A, int* smem) {
       r = route_member_any(A, npl, z, W, g, ck, ci, cs);
       if (__any_sync(0xffffffffu, r.bad) && lane == 0 && !A.dry) atomicOr(A.status, STATUS_NONFINITE);
     }
+    if (A.debug_times && tb == 0) tp[5] = global_ns();
     if (W > 1) {
       __syncthreads();
+      if (A.debug_times && tb == 0) tp[6] = global_ns();
       if (active && g == 0) r = route_merge_fn(cand_k, cand_i, cand_s, warp, W, k);
     }
-    if (active && g == 0) route_weights_fn(A, z, t, r.id, r.z);
+    if (A.debug_times && tb == 0) tp[7] = global_ns();
+    if (active && g == 0) route_weights_fn(A, z, t, r.id, r.z, cand_s + warp * MAX_K, s_cnt);
     if (W > 1) __syncthreads();
   }
   if (A.topk_only) return;
@@ -628,9 +641,11 @@ static __device__ __noinline__ void route_block(const RouteArgs& A, int* smem) {
   if (A.T * k <= 32) {
     // few pairs: one warp sorts them (route_lists_few_fn)
     __syncthreads();
-    if (warp == 0) route_lists_few_fn(A);
+    if (warp == 0) route_lists_few_fn(A, s_cnt);
     if (A.debug_times && tid == 0)
-      printf("route phases (ns): topk %llu list %llu\n", tp[1] - tp[0], global_ns() - tp[1]);
+      printf("route phases (ns): topk %llu (member %llu sync %llu merge %llu weights %llu) list %llu\n",
+             tp[1] - tp[0], tp[5] - tp[0], tp[6] - tp[5], tp[7] - tp[6], tp[1] - tp[7],
+             global_ns() - tp[1]);
     return;
   }
   for (int e = tid; e < MAX_E; e += nthr) s_cnt[e] = 0;
