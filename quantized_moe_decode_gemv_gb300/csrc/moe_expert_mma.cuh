@@ -177,13 +177,16 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
   griddep_launch();
   if (!A.pre_wait_phase) cta_stamp(A.trace, 1);
 
-  // ---- work: the segments (distinct expert u, pass of up to pp of its pairs)
-  // of this routing, spread evenly over the grid.  With nseg <= grid CTAs,
-  // every segment has grid / nseg CTAs, each a contiguous range of its 16-row
-  // tiles; with more segments, CTA c takes segments c, c + grid, ... whole.
-  // (The grid is sized before the routing is known; spreading by the segments
-  // the routing made keeps the CTAs busy whatever the load.)
-  __shared__ int s_seg[6];   // nseg, slot and pass of a segment, tile range, first segment
+  // ---- work: the units (segment, 16-row tile) of this routing, a segment
+  // being a distinct expert u and a pass of up to pp of its pairs, spread
+  // evenly over the grid.  With at least 4 CTAs a segment (m = grid / nseg),
+  // CTA j of a segment's m takes its tiles [j ntiles / m, (j + 1) ntiles / m):
+  // one segment a CTA, the same ranges in every segment.  Otherwise CTA c
+  // takes the units [c U / grid, (c + 1) U / grid) in segment-major order (U =
+  // nseg ntiles), which may span segments.  (The grid is sized before the
+  // routing is known; spreading by the units the routing made keeps every CTA
+  // busy whatever the load, and spreads the tiles' combines over the CTAs.)
+  __shared__ int s_seg[6];   // nseg, slot and pass of a segment, this CTA's units [u0, u1)
   auto npass_of = [&](int u) -> int {
     const int n = uniq_p0[u + 1] - uniq_p0[u];
     if (n <= 0 || (A.max_pairs > 0 && n > A.max_pairs)) return 0;
@@ -227,24 +230,29 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
       for (int o = 16; o >= 1; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
     }
     const int ns_ = cnt;
-    // with nseg <= grid, m = grid / nseg CTAs a segment (at most one a tile),
-    // CTA j of them on tiles [j ntiles / m, (j + 1) ntiles / m): the same
-    // ranges in every segment; the CTAs past nseg m stay idle
-    int sg0 = cta, t0 = 0, t1 = ntiles;
-    if (ns_ <= gsz && ns_ > 0) {
-      const int m = min(ntiles, gsz / ns_);
-      sg0 = cta / m;
-      const int j = cta - sg0 * m;
-      t0 = j * ntiles / m;
-      t1 = (j + 1) * ntiles / m;
+    int64_t u0 = 0, u1 = 0;
+    if (ns_ > 0) {
+      const int m = gsz / ns_;
+      if (m >= 4) {
+        // (the CTAs past nseg m stay idle)
+        const int mm = min(ntiles, m), sgc = cta / mm, j = cta - sgc * mm;
+        if (sgc < ns_) {
+          u0 = static_cast<int64_t>(sgc) * ntiles + j * ntiles / mm;
+          u1 = static_cast<int64_t>(sgc) * ntiles + (j + 1) * ntiles / mm;
+        }
+      } else {
+        const int64_t U = static_cast<int64_t>(ns_) * ntiles;
+        u0 = cta * U / gsz;
+        u1 = (cta + 1) * U / gsz;
+      }
     }
-    if (lane == 0) { s_seg[0] = ns_; s_seg[3] = t0; s_seg[4] = t1; s_seg[5] = sg0; }
+    if (lane == 0) { s_seg[0] = ns_; s_seg[3] = static_cast<int>(u0); s_seg[4] = static_cast<int>(u1); }
   }
   __syncthreads();
   const int nseg = s_seg[0];
-  const bool one_seg = nseg <= gsz;
-  const int tb = s_seg[3], te = s_seg[4];
-  int sg = s_seg[5];
+  const int cu0 = s_seg[3], cu1 = s_seg[4];
+  int sg = cu0 / ntiles;
+  int tb = 0, te = 0;   // this CTA's tiles of segment sg
 
   // The CTA's warps form EM_WARPS / KS tile slots of KS warps; warp ks of slot
   // sl takes the tiles tb + sl + nslot ti, and of each its part of K in
@@ -258,7 +266,7 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
   const int unit = G > 64 ? G / 64 : 1, nu = nkc / unit;
   const int kc_lo = (ks * nu / KS) * unit, kc_hi = ((ks + 1) * nu / KS) * unit;
   const int nit = (kc_hi - kc_lo + CK - 1) / CK;   // items (chunks) a tile
-  const int my_tiles = (te - tb > slot) ? (te - tb - slot + nslot - 1) / nslot : 0;
+  int my_tiles = 0;
   const uint32_t* qm[2] = {GATED ? A.qt_gate : A.qt, A.qt};
   const uint32_t* sm[2] = {GATED ? A.sbt_gate : A.sbt, A.sbt};
   int64_t e = 0;                        // the segment's expert
@@ -288,6 +296,9 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
   // Segment sg: its slot and pass (warp 0 scans the slots' pass counts), its
   // pairs; the first copies of this warp's items go out at once.
   auto prepare = [&](int sgi) {
+    tb = max(cu0 - sgi * ntiles, 0);
+    te = min(cu1 - sgi * ntiles, ntiles);
+    my_tiles = (te - tb > slot) ? (te - tb - slot + nslot - 1) / nslot : 0;
     if (warp == 0) {
       if (!A.one_pass) lookup(sgi);
       else if (lane == 0) { s_seg[1] = sgi; s_seg[2] = 0; }
@@ -323,7 +334,7 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
   // the down projection's metadata is final at launch: its first segment
   // (copies and pair ids) is prepared before the wait
   bool waited = !A.pre_wait_phase;
-  for (bool first = true; nseg > 0 && sg < nseg; sg += (one_seg ? nseg : gsz), first = false) {
+  for (bool first = true; cu0 < cu1 && sg * ntiles < cu1; ++sg, first = false) {
     if (!first) __syncthreads();   // every warp is done with the previous segment's B and ids
     prepare(sg);
     if (!waited) {
