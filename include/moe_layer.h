@@ -88,7 +88,7 @@ typedef enum moe_dtype { MOE_DTYPE_BF16 = 0, MOE_DTYPE_FP16 = 1, MOE_DTYPE_FP32 
  *            (fc2_latent_proj, shared down, residual).  For few token rows.
  *   GROUPED  row-grouped tcgen05 GEMMs for the experts and dense projections
  *            (many token rows per forward).
- *   AUTO     GROUPED when T >= 16 (MOE_GROUPED_MIN_T), else GEMV. */
+ *   AUTO     GROUPED when T >= 32 (MOE_GROUPED_MIN_T), else GEMV. */
 typedef enum moe_path {
   MOE_PATH_AUTO = 0,
   MOE_PATH_GEMV = 1,

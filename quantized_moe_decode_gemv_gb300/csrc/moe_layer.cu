@@ -103,7 +103,7 @@ struct moe_layer {
   int umax = 0;
   int kin = 0;
   int bits = 4;           // code width of the routed experts (3, 4 or 8)
-  int grouped_min_t = 16;
+  int grouped_min_t = 32;
   int expert_split = 0;   // AUTO's grouped path: light experts on the int4 gemv kernel
   int last_launches = 0;  // kernel launches of the last forward
   unsigned long long* um_trace = nullptr;   // diagnostics (MOE_UMMA_TRACE): grouped GEMM role stamps

@@ -338,14 +338,14 @@ def test_stack_parity(T, rows):
 # --- properties of the CUDA path ------------------------------------------------
 
 def test_path_selection_and_launch_counts():
-    """AUTO takes the grouped tcgen05 path from 16 rows and the gemv path below;
+    """AUTO takes the grouped tcgen05 path from 32 rows and the gemv path below;
     a forced path is honoured; a gemv forward of the latent layer is four
     launches (dense pass with the routing, expert up, expert down with the
     combine, output pass)."""
     lay, h = handle_for("latent", 256, zipf=True)
     x = gu.to_torch_x(mi.make_x(lay.spec, 64, 5), "bf16")
-    assert [h.path_for(T) for T in (16, 64, 256)] == ["grouped"] * 3
-    assert [h.path_for(T) for T in (1, 8, 15)] == ["gemv"] * 3
+    assert [h.path_for(T) for T in (32, 64, 256)] == ["grouped"] * 3
+    assert [h.path_for(T) for T in (1, 8, 16, 31)] == ["gemv"] * 4
     try:
         h.set_path("gemv")
         assert h.path_for(64) == "gemv"
