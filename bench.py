@@ -204,10 +204,13 @@ def parse_args():
 
 def expert_bytes(spec):
     """(up-side bytes, down-side bytes) of one routed expert: packed b-bit codes
-    + scale + bias (2 bytes each per group)."""
+    + scale + bias (2 bytes each per group); NVFP4: 4-bit codes, one E4M3 byte
+    per 16 elements and a 4-byte matrix scale per matrix."""
     n_in = 2 if spec.gated else 1
     e_in = n_in * spec.expert_ffn * spec.k_in
     e_dn = spec.k_in * spec.expert_ffn
+    if getattr(spec, "fmt", "affine") == "nvfp4":
+        return (e_in // 2 + e_in // 16 + 4 * n_in, e_dn // 2 + e_dn // 16 + 4)
     sb = 2 * 2
     b = spec.bits
     return (e_in * b // 8 + sb * (e_in // spec.group_size), e_dn * b // 8 + sb * (e_dn // spec.group_size))
@@ -568,6 +571,11 @@ def run_ours(args):
         for T in (1, 4):
             also.append(workload_line(torch, pkg, mi.SPECS["tiny"], T, st_also, args.warmup, args.seed,
                                       flush, stream, hbm_peak, tc_peak, label="tiny layer"))
+        fp4 = mi.SPECS["latent"].with_(name="latent_nvfp4", fmt="nvfp4", group_size=16)
+        for T in (1, 16):
+            also.append(workload_line(torch, pkg, fp4, T, st_also, args.warmup, args.seed, flush, stream,
+                                      hbm_peak, tc_peak,
+                                      label="latent layer, NVFP4 experts (E2M1, E4M3 per 16, fp32 per matrix)"))
 
     # batched serving sweep (separate output file)
     if sweep and rank == 0:

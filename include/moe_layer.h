@@ -33,6 +33,16 @@
  *     in bits 4*i..4*i+3 (lowest nibble first).  A weight is scale*q + bias
  *     (q unsigned, 0..2^b-1), with the scale and bias of its group of
  *     group_size consecutive elements along the input (reduction) axis.
+ *   - NVFP4 experts (weight_format = MOE_WFMT_NVFP4): the codes are 4-bit
+ *     E2M1 values (bit 3 sign, bits 2..1 exponent, bit 0 mantissa: magnitudes
+ *     0, 0.5, 1, 1.5, 2, 3, 4, 6), packed like 4-bit affine codes; every block
+ *     of 16 consecutive elements along the input axis has one E4M3 scale byte
+ *     (sign, 4 exponent bits with bias 7, 3 mantissa bits; 0x7F/0xFF are NaN),
+ *     and every expert matrix one fp32 scale: a weight is
+ *     e2m1(q) * e4m3(block scale) * matrix scale.  The mlx-bun decode-speed
+ *     program's weight-format table lists "mxfp4/nvfp4" among its supported
+ *     formats; the element and scale encodings are those of the OCP
+ *     Microscaling (MX) specification's FP4 E2M1 and FP8 E4M3 types.
  *   - bf16/fp16 buffers hold IEEE/bfloat16 16-bit values.
  *   - Every function returns a moe_status; MOE_OK is 0.  On error nothing that
  *     the call allocated stays allocated, and moe_layer_last_error() (where a
@@ -47,7 +57,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 3
+#define MOE_ABI_VERSION 4
 
 typedef enum moe_status {
   MOE_OK = 0,
@@ -95,13 +105,19 @@ typedef enum moe_path {
   MOE_PATH_GROUPED = 2
 } moe_path;
 
+/* Expert weight formats (moe_layer_config.weight_format). */
+typedef enum moe_weight_format {
+  MOE_WFMT_AFFINE = 0,   /* b-bit codes, scale and bias per group of group_size */
+  MOE_WFMT_NVFP4 = 1     /* E2M1 codes, E4M3 scale per 16, fp32 scale per matrix */
+} moe_weight_format;
+
 typedef struct moe_layer_config {
   int32_t hidden;        /* H: width of x and out; multiple of 64 */
   int32_t n_experts;     /* E: routed experts, 1..1024 */
   int32_t top_k;         /* k: experts per token, 1..min(E, 16) */
   int32_t expert_ffn;    /* F: routed expert width; multiple of 64 and of group_size */
   int32_t latent;        /* L: latent width of the routed experts, 0 = none (experts on H) */
-  int32_t group_size;    /* G: 32, 64 or 128 */
+  int32_t group_size;    /* G: 32, 64 or 128 (NVFP4: 16, the scale block) */
   int32_t shared_ffn;    /* shared expert width, 0 = no shared expert */
   int32_t max_tokens;    /* largest T a forward call may pass, >= 1 */
   int32_t act;           /* moe_act (routed and shared experts alike) */
@@ -110,11 +126,14 @@ typedef struct moe_layer_config {
   float routed_scale;    /* multiplies the combine weights (after normalising) */
   int32_t has_router_bias; /* sigmoid routing: per-expert fp32 selection bias */
   int32_t act_dtype;     /* BF16|FP16: x, out, fc1/fc2 and shared expert weights */
-  int32_t scale_dtype;   /* BF16|FP16: expert scales and biases */
+  int32_t scale_dtype;   /* BF16|FP16: expert scales and biases (ignored by NVFP4) */
   int32_t router_dtype;  /* BF16|FP16|FP32: router weight (x is widened to fp32) */
   int32_t bits;          /* code width of the routed experts: 3, 4 or 8 (0 = 4).
                             3- and 8-bit layers run the GEMV schedule only: AUTO
                             selects it at every T, GROUPED is refused */
+  int32_t weight_format; /* moe_weight_format (0 = affine).  NVFP4 needs bits 0
+                            or 4 and group_size 16, and like 3/8-bit layers runs
+                            the GEMV schedule only (the warp-MMA expert kernel) */
 } moe_layer_config;
 
 /* Weights, all DEVICE pointers owned by the caller.  moe_layer_create copies
@@ -129,7 +148,10 @@ typedef struct moe_layer_config {
  *   down_q     [E, Kin, F*bits/32]  uint32 packed codes
  *   down_s, down_b [E, Kin, F/G] scale_dtype
  *   sh_gate, sh_up [shared_ffn, H], sh_down [H, shared_ffn]  act_dtype
- *     (sh_gate for SWIGLU only; all NULL when shared_ffn == 0) */
+ *     (sh_gate for SWIGLU only; all NULL when shared_ffn == 0)
+ * NVFP4 layers: *_q as above (bits 4); *_s the E4M3 block scales, one byte per
+ * 16 elements: [E, F, Kin/16] (gate, up) and [E, Kin, F/16] (down) uint8; *_b
+ * the per-matrix fp32 scales [E]. */
 typedef struct moe_layer_weights {
   const void *router_w;
   const float *router_bias;
@@ -163,16 +185,17 @@ int32_t moe_build_flags(void);
  * with the same refusals and codes as moe_layer_create; touches no device.
  * `w` may be NULL to check the config alone.  Refusals, in order:
  *   MOE_ERR_INVALID_ARG   null cfg, non-positive sizes, bad enum values, bits
- *                         not 0, 3, 4 or 8
+ *                         not 0, 3, 4 or 8 (NVFP4: not 0 or 4), an unknown
+ *                         weight_format
  *   MOE_ERR_TOPK_GT_E     top_k < 1 or top_k > n_experts (a layer whose top-k
  *                         exceeds its own expert count is refused before any
  *                         weight is read: TensorFold PR #1038, "What's in it")
  *   MOE_ERR_LATENT_PROJ   latent > 0 with fc1/fc2 missing or act_dtype not
  *                         16-bit (missing/non-bf16 latent projections are
  *                         refused by name in the same passage)
- *   MOE_ERR_SHAPE         G not 32/64/128, or H, F, Kin not multiples of 64 and
- *                         of G, or expert weights present for a shape that
- *                         cannot hold them
+ *   MOE_ERR_SHAPE         G not 32/64/128 (NVFP4: not 16), or H, F, Kin not
+ *                         multiples of 64 and of G, or expert weights present
+ *                         for a shape that cannot hold them
  *   MOE_ERR_UNSUPPORTED   E > 1024 or top_k > 16 or shared expert without a
  *                         weight, router_bias with softmax routing */
 moe_status moe_layer_validate(const moe_layer_config *cfg, const moe_layer_weights *w);
@@ -211,7 +234,7 @@ moe_status moe_layer_forward_host(moe_layer *h, const void *x_host, int32_t T, v
 
 /* Choose the routed-expert path for later forwards (A/B testing).  A path this
  * build cannot serve for the layer returns MOE_ERR_UNSUPPORTED (GROUPED for a
- * layer with bits 3 or 8, or with fp32 activations). */
+ * layer with bits 3 or 8, NVFP4 experts, or fp32 activations). */
 moe_status moe_layer_set_path(moe_layer *h, int32_t path);
 
 /* Synchronises `stream`, reads and clears the device status word: MOE_OK, or

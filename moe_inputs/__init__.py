@@ -24,6 +24,13 @@ Storage conventions (the library's input format):
   group's min/max: ``bias = min``, ``scale = (max - min) / (2^b - 1)`` (both
   rounded to the scale dtype), ``q = clip(rint((w - bias) / scale), 0, 2^b - 1)``.  The pages
   give no quantiser; this one only shapes the test weights.
+* NVFP4 experts (``LayerSpec.fmt == "nvfp4"``, group size 16): ``q`` holds
+  4-bit E2M1 codes packed as above, ``scale`` one E4M3 byte per 16 elements
+  (``uint8 [E, N_out, K_in/16]``) and ``bias`` one float32 scale per expert
+  matrix (``[E]``); a weight is ``e2m1(q) * e4m3(scale) * bias``.  The
+  synthetic quantiser takes the matrix scale ``amax / (6 * 448)``, each block's
+  E4M3 scale as the nearest to ``block amax / (6 * matrix scale)`` and each
+  code as the nearest E2M1 value of ``w / (block scale * matrix scale)``.
 """
 from __future__ import annotations
 
@@ -37,7 +44,8 @@ __all__ = [
     "LayerSpec", "LayerWeights", "SPECS", "stack_specs", "make_layer", "make_x",
     "draw_x_rows", "round_to_bf16_bits", "bf16_bits_to_f32", "quantize_affine_int4",
     "quantize_affine", "pack_codes", "unpack_codes", "CODE_BITS", "pack_int4", "unpack_int4",
-    "zipf_router_bias", "spec_for", "ROUTED_BYTES",
+    "zipf_router_bias", "spec_for", "ROUTED_BYTES", "quantize_nvfp4", "e4m3_round",
+    "e2m1_round",
 ]
 
 
@@ -163,6 +171,65 @@ def quantize_affine_int4(w: np.ndarray, group: int, scale_dtype: str):
     return quantize_affine(w, group, 4, scale_dtype)
 
 
+# E2M1 magnitudes by the low three code bits (the encoder's grid)
+_E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def e2m1_round(r: np.ndarray) -> np.ndarray:
+    """Nearest E2M1 code (sign in bit 3) of each element of ``r`` (magnitudes
+    above 6 saturate to 6; an exact tie takes the smaller magnitude)."""
+    r = np.asarray(r, dtype=np.float64)
+    idx = np.abs(np.abs(r)[..., None] - _E2M1_GRID).argmin(axis=-1)
+    return (idx | np.where(r < 0, 8, 0)).astype(np.uint8)
+
+
+def e4m3_round(a: np.ndarray):
+    """Nearest E4M3 byte of each non-negative element of ``a`` (round half to
+    even on the mantissa, saturating at 448).  Returns ``(bytes uint8, values
+    float64)``: normal values (1 + m/8) 2^(e-7) for e = 1..15 (e = 15 stops at
+    m = 6), subnormal m/8 2^-6."""
+    a = np.asarray(a, dtype=np.float64)
+    if (a < 0).any() or not np.isfinite(a).all():
+        raise ValueError("E4M3 scales are encoded from finite non-negative values")
+    a = np.minimum(a, 448.0)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.clip(e, -6, 8)                       # unbiased exponent; below -6: subnormal grid
+    step = np.exp2(e - 3)                       # mantissa step at that exponent
+    m8 = np.rint(a / step)                      # 8 + m (normal) or m (subnormal, e = -6)
+    norm = a >= 2.0 ** -6
+    # a carry to 16 moves to the next exponent (still exact: 16 * step = 8 * 2 step)
+    carry = norm & (m8 >= 16)
+    e = np.where(carry, e + 1, e)
+    m8 = np.where(carry, 8, m8)
+    val = m8 * np.exp2(e - 3)
+    sub_m = np.where(norm, 0, m8).astype(np.int64)            # subnormal 0..8 (8: rounds up to 2^-6)
+    byte_norm = ((e + 7).astype(np.int64) << 3) | (m8.astype(np.int64) - 8)
+    byte_sub = np.where(sub_m >= 8, 1 << 3, sub_m)
+    byte = np.where(norm, byte_norm, byte_sub)
+    val = np.where(norm, val, np.where(sub_m >= 8, 2.0 ** -6, sub_m * 2.0 ** -9))
+    return byte.astype(np.uint8), val
+
+
+def quantize_nvfp4(w: np.ndarray):
+    """NVFP4 quantisation of ``w [..., N, K]`` (blocks of 16 along K): returns
+    ``(q uint8 [..., N, K] E2M1 codes, scale uint8 [..., N, K/16] E4M3 bytes,
+    matrix scale float32)`` as described in the module notes."""
+    w = np.asarray(w, dtype=np.float64)
+    K = w.shape[-1]
+    if K % 16:
+        raise ValueError("K must be a multiple of 16")
+    amax = float(np.abs(w).max())
+    gs = np.float32(amax / (6.0 * 448.0) if amax > 0 else 1.0)
+    wb = w.reshape(*w.shape[:-1], K // 16, 16)
+    bmax = np.abs(wb).max(axis=-1)
+    sb, sv = e4m3_round(bmax / (6.0 * float(gs)))
+    S = sv[..., None] * float(gs)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.where(S > 0, wb / np.where(S > 0, S, 1.0), 0.0)
+    q = e2m1_round(r).reshape(w.shape)
+    return q, sb, gs
+
+
 # ---------------------------------------------------------------------------
 # Layer shapes
 # ---------------------------------------------------------------------------
@@ -189,6 +256,7 @@ class LayerSpec:
     weight_std: float = 0.02
     bias_std: float = 0.01
     bits: int = 4               # expert code width (3, 4 or 8)
+    fmt: str = "affine"         # expert weight format: "affine" or "nvfp4" (group_size 16)
 
     @property
     def k_in(self) -> int:
@@ -323,7 +391,29 @@ def _quant_expert_direct(rng, E, N, K, spec: LayerSpec):
     return words, _round_to_dtype(sg, spec.scale_dtype), _round_to_dtype(bg, spec.scale_dtype)
 
 
+def _quant_expert_nvfp4(rng, E, N, K, spec: LayerSpec):
+    """NVFP4 expert matrices: small layers draw N(0, weight_std) weights and
+    quantise them (``quantize_nvfp4``); large ones draw uniform codes (each of
+    the 16 E2M1 codes equally likely: RMS 2.93) with E4M3 block scales near 64
+    and a matrix scale giving weights of standard deviation ~weight_std."""
+    if N * K <= EXACT_QUANT_MAX_ELEMS // max(E, 1):
+        q_all = np.empty((E, N, K), dtype=np.uint8)
+        s_all = np.empty((E, N, K // 16), dtype=np.uint8)
+        g_all = np.empty(E, dtype=np.float32)
+        for e in range(E):
+            q_all[e], s_all[e], g_all[e] = quantize_nvfp4(rng.normal(0.0, spec.weight_std, size=(N, K)))
+        return pack_codes(q_all, 4), s_all, g_all
+    words = rng.integers(0, 1 << 32, size=(E, N, K // 8), dtype=np.uint32)
+    target = np.abs(64.0 * (1.0 + 0.1 * rng.standard_normal(size=(E, N, K // 16))))
+    s_all, _ = e4m3_round(target)
+    rms = float(np.sqrt(np.mean(_E2M1_GRID ** 2)))
+    g_all = np.full(E, spec.weight_std / (rms * 64.0), dtype=np.float32)
+    return words, s_all, g_all
+
+
 def _quant_expert(rng, E, N, K, spec: LayerSpec):
+    if spec.fmt == "nvfp4":
+        return _quant_expert_nvfp4(rng, E, N, K, spec)
     if N * K <= EXACT_QUANT_MAX_ELEMS // max(E, 1):
         return _quant_expert_exact(rng, E, N, K, spec)
     return _quant_expert_direct(rng, E, N, K, spec)

@@ -1,5 +1,5 @@
 """fp64 CPU oracle for the decode-time forward of a routed MoE layer with b-bit
-(3, 4 or 8) affine group-quantised experts.
+(3, 4 or 8) affine group-quantised experts, or NVFP4 experts.
 
 TEST INFRASTRUCTURE ONLY.  Nothing in the library imports this module; only the
 tests, the smoke check and the benchmark's CPU-baseline leg call it.  It shares
@@ -18,7 +18,8 @@ Sources (page titles and sections):
   normalisation and sum; fp16 activations with fp32 sums.
 * mlx-bun decode-speed program, weight-format table and the affine shared-M
   section: MLX affine quantisation, packed codes of 2..8 bits with a scale
-  and a bias per group (group sizes 32/64/128).
+  and a bias per group (group sizes 32/64/128); the same table lists
+  "mxfp4/nvfp4" among the supported formats.
 
 Where the pages leave a step open, the readings are:
 
@@ -36,7 +37,14 @@ Where the pages leave a step open, the readings are:
 6. softmax routing with renormalisation equals a softmax over the selected
    logits; without renormalisation the weights are the full softmax;
 7. the shared expert has the routed experts' activation form and weight 1;
-8. the residual is the layer input; the layer has no norm.
+8. the residual is the layer input; the layer has no norm;
+9. NVFP4 (named, not defined, by the pages): 4-bit E2M1 codes (sign bit 3,
+   exponent bits 2..1 with bias 1, mantissa bit 0; exponent 0 is subnormal)
+   with one E4M3 scale (sign bit 7, exponent bits 6..3 with bias 7, mantissa
+   bits 2..0; exponent 0 subnormal; exponent 15 with mantissa 7 is NaN) per
+   16 consecutive elements along the input axis and one fp32 scale per
+   expert matrix: w = e2m1(q) * e4m3(s) * matrix scale (the OCP
+   Microscaling specification's FP4 E2M1 and FP8 E4M3 element types).
 
 Every function here is pinned by tests that do not reuse its formulas
 (brute-force top-k, closed forms, invariants, a pure-Python loop).
@@ -49,7 +57,8 @@ from typing import Dict, Optional, Sequence
 import numpy as np
 
 __all__ = [
-    "widen", "unpack_codes", "dequantize", "router_logits", "selection_keys",
+    "widen", "unpack_codes", "dequantize", "e2m1_values", "e4m3_values", "dequantize_nvfp4",
+    "router_logits", "selection_keys",
     "topk_order", "route", "activation", "expert_output", "shared_output",
     "oracle_forward", "routing_margin", "forward_rows", "expert_cache",
 ]
@@ -96,6 +105,41 @@ def dequantize(packed: np.ndarray, scale: np.ndarray, bias: np.ndarray, group: i
     s_full = np.repeat(s, group, axis=-1)
     b_full = np.repeat(b, group, axis=-1)
     return s_full * q + b_full
+
+
+def e2m1_values(codes: np.ndarray) -> np.ndarray:
+    """Values of 4-bit E2M1 codes (reading 9): sign bit 3; exponent field
+    bits 2..1 (bias 1); mantissa bit 0; exponent field 0 is subnormal
+    (0.5 * mantissa)."""
+    c = np.asarray(codes, dtype=np.int64)
+    sign = (c >> 3) & 1
+    ef = (c >> 2 & 1) * 2 + (c >> 1 & 1)
+    mf = c & 1
+    mag = np.where(ef == 0, 0.5 * mf, np.exp2(ef - 1.0) * (1.0 + 0.5 * mf))
+    return np.where(sign == 1, -mag, mag)
+
+
+def e4m3_values(b: np.ndarray) -> np.ndarray:
+    """Values of E4M3 bytes (reading 9): sign bit 7; exponent field bits 6..3
+    (bias 7); mantissa bits 2..0; exponent field 0 is subnormal (m/8 * 2^-6);
+    exponent 15 with mantissa 7 is NaN (there is no infinity)."""
+    v = np.asarray(b, dtype=np.int64)
+    sign = (v >> 7) & 1
+    ef = (v >> 3) & 15
+    mf = v & 7
+    mag = np.where(ef == 0, (mf / 8.0) * 2.0 ** -6, (1.0 + mf / 8.0) * np.exp2(ef - 7.0))
+    mag = np.where((ef == 15) & (mf == 7), np.nan, mag)
+    return np.where(sign == 1, -mag, mag)
+
+
+def dequantize_nvfp4(packed: np.ndarray, scale_bytes: np.ndarray, matrix_scale) -> np.ndarray:
+    """NVFP4 dequantisation ``w[n, k] = e2m1(q[n, k]) * e4m3(s[n, k // 16]) *
+    matrix_scale`` in float64 (reading 9)."""
+    q = e2m1_values(unpack_codes(packed, 4))
+    s = e4m3_values(scale_bytes)
+    if s.shape[-1] * 16 != q.shape[-1]:
+        raise ValueError("NVFP4 scales do not match blocks of 16")
+    return q * np.repeat(s, 16, axis=-1) * float(np.float32(matrix_scale))
 
 
 # ---------------------------------------------------------------------------
@@ -205,9 +249,14 @@ class _ExpertCache:
         if e not in self.mats:
             L, sp = self.layer, self.spec
             G, sd, nb = sp.group_size, sp.scale_dtype, getattr(sp, "bits", 4)
-            up = dequantize(L.up_q[e], L.up_s[e], L.up_b[e], G, sd, nb)
-            gate = dequantize(L.gate_q[e], L.gate_s[e], L.gate_b[e], G, sd, nb) if sp.gated else None
-            down = dequantize(L.down_q[e], L.down_s[e], L.down_b[e], G, sd, nb)
+            if getattr(sp, "fmt", "affine") == "nvfp4":
+                up = dequantize_nvfp4(L.up_q[e], L.up_s[e], L.up_b[e])
+                gate = dequantize_nvfp4(L.gate_q[e], L.gate_s[e], L.gate_b[e]) if sp.gated else None
+                down = dequantize_nvfp4(L.down_q[e], L.down_s[e], L.down_b[e])
+            else:
+                up = dequantize(L.up_q[e], L.up_s[e], L.up_b[e], G, sd, nb)
+                gate = dequantize(L.gate_q[e], L.gate_s[e], L.gate_b[e], G, sd, nb) if sp.gated else None
+                down = dequantize(L.down_q[e], L.down_s[e], L.down_b[e], G, sd, nb)
             size = up.nbytes + down.nbytes + (gate.nbytes if gate is not None else 0)
             while self.mats and self.bytes + size > self.max_bytes:
                 old = next(iter(self.mats))

@@ -26,6 +26,7 @@ STATUS_NAMES = ["MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR
 ACT = {"swiglu": 0, "relu2": 1}
 ROUTER = {"softmax": 0, "sigmoid": 1}
 DTYPE = {"bf16": 0, "fp16": 1, "fp32": 2}
+WFMT = {"affine": 0, "nvfp4": 1}
 PATH = {"auto": 0, "gemv": 1, "grouped": 2}
 NUM_STAGES = 5
 STAGE_NAMES = ["dense_in", "route", "expert_up", "expert_down", "dense_out"]
@@ -47,7 +48,7 @@ class moe_layer_config(ctypes.Structure):
                 ("renormalize", ctypes.c_int32), ("routed_scale", ctypes.c_float),
                 ("has_router_bias", ctypes.c_int32), ("act_dtype", ctypes.c_int32),
                 ("scale_dtype", ctypes.c_int32), ("router_dtype", ctypes.c_int32),
-                ("bits", ctypes.c_int32)]
+                ("bits", ctypes.c_int32), ("weight_format", ctypes.c_int32)]
 
 
 _WEIGHT_FIELDS = ["router_w", "router_bias", "fc1_latent", "fc2_latent", "gate_q", "up_q",
@@ -147,6 +148,7 @@ class MoEConfig:
     scale_dtype: str = "bf16"
     router_dtype: str = "bf16"
     bits: int = 4
+    fmt: str = "affine"          # expert weight format: "affine" or "nvfp4"
 
     @classmethod
     def from_spec(cls, spec: Any, max_tokens: int) -> "MoEConfig":
@@ -163,7 +165,8 @@ class MoEConfig:
             router=ROUTER[self.router], renormalize=int(bool(self.renormalize)),
             routed_scale=float(self.routed_scale), has_router_bias=int(bool(self.router_bias)),
             act_dtype=DTYPE[self.act_dtype], scale_dtype=DTYPE[self.scale_dtype],
-            router_dtype=DTYPE[self.router_dtype], bits=int(self.bits))
+            router_dtype=DTYPE[self.router_dtype], bits=int(self.bits),
+            weight_format=WFMT[self.fmt])
 
 
 def _ptr(t) -> Optional[int]:

@@ -55,7 +55,7 @@ constexpr int EM_MAX_PAIRS = 4 * EM_MAX_NTP;
 
 // Shared-memory plan of one k_expert_mma launch (host and device agree).
 //   [B fragments: pp/4 n-tiles x K/16 blocks x 32 lanes x 8 bytes]
-//   [group sums of x: pp x K/G floats, 128-aligned]
+//   [group sums of x: pp x K/gx floats, 128-aligned (gx: G, or 16 for NVFP4)]
 //   [K-split partials (ks > 1): 2 x EM_WARPS x 4 NTP x 32 floats]
 //   [rings: EM_WARPS x ns stages of stage_bytes]  [mbarriers: EM_WARPS x ns]
 // A stage holds, per matrix (gate first for SwiGLU, then up), ck x 512 bytes of
@@ -70,7 +70,8 @@ struct EmPlan {
 // n-tiles of accumulators of a pass of pp pairs (the kernel's NTP)
 __host__ __device__ inline int em_ntp(int pp) { return pp <= 4 ? 1 : (pp <= 8 ? 2 : 4); }
 
-__host__ __device__ inline EmPlan em_plan(int K, int G, bool gated, int ck, int ns, int pp, int ks) {
+__host__ __device__ inline EmPlan em_plan(int K, int G, bool gated, int ck, int ns, int pp, int ks, int gx = 0) {
+  if (gx <= 0) gx = G;
   EmPlan p;
   p.ck = ck;
   p.ns = ns;
@@ -78,7 +79,7 @@ __host__ __device__ inline EmPlan em_plan(int K, int G, bool gated, int ck, int 
   p.ks = ks;
   p.stage_bytes = (gated ? 2 : 1) * ck * (512 + 128);
   p.b_bytes = (pp / 4) * (K / 16) * 256;
-  p.xs_bytes = (pp * (K / G) * 4 + 127) & ~127;
+  p.xs_bytes = (pp * (K / gx) * 4 + 127) & ~127;
   p.red_off = p.b_bytes + p.xs_bytes;
   p.ring_off = p.red_off + (ks > 1 ? 2 * EM_WARPS * 4 * em_ntp(pp) * 32 * 4 : 0);
   p.bar_off = p.ring_off + EM_WARPS * ns * p.stage_bytes;
@@ -101,6 +102,48 @@ __device__ __forceinline__ void em_decode(uint32_t w, uint32_t (&a)[4]) {
   constexpr uint32_t M = 0x43004300u;   // bf16 128.0 in both halves
 #pragma unroll
   for (int i = 0; i < 4; ++i) a[i] = ((w >> (4 * i)) & 0x000F000Fu) | M;
+}
+
+// NVFP4 codes (E2M1: sign, two exponent bits, one mantissa bit; magnitudes
+// 0, 0.5, 1, 1.5, 2, 3, 4, 6) -> the same four registers, holding 128 + n with
+// n = 2 v + 12 in 0..24 (exact in bf16; the fold removes the 140 offset).  Two
+// byte permutes look n up for four codes: the positive table by the code
+// nibble, the negative one by the nibble with its sign bit flipped; a nibble
+// whose bit 3 is set selects in sign-replicate mode, which yields 0x00 from
+// these tables (every entry is below 0x80), so exactly one lookup is nonzero.
+__device__ __forceinline__ uint32_t em_prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+__device__ __forceinline__ void em_decode_fp4(uint32_t w, uint32_t (&a)[4]) {
+  constexpr uint32_t TP0 = 0x0F0E0D0Cu, TP1 = 0x18141210u;   // 12 + 2v, v = 0 .. 1.5 | 2 .. 6
+  constexpr uint32_t TN0 = 0x090A0B0Cu, TN1 = 0x00040608u;   // 12 - 2v
+  const uint32_t x = w ^ 0x88888888u;
+  const uint32_t p0 = em_prmt(TP0, TP1, w) | em_prmt(TN0, TN1, x);               // codes 0..3
+  const uint32_t p1 = em_prmt(TP0, TP1, w >> 16) | em_prmt(TN0, TN1, x >> 16);   // codes 4..7
+  // register i: n of code i (byte 0) and of code i + 4 (byte 2); bytes 1 and 3
+  // replicate the clear top bit of a table byte (0x00), then take 0x43
+  a[0] = em_prmt(p0, p1, 0xC480u) | 0x43004300u;
+  a[1] = em_prmt(p0, p1, 0xD591u) | 0x43004300u;
+  a[2] = em_prmt(p0, p1, 0xE6A2u) | 0x43004300u;
+  a[3] = em_prmt(p0, p1, 0xF7B3u) | 0x43004300u;
+}
+
+// Four E4M3 block scales (byte j: block j of a 64-column chunk) -> floats
+// times m (exact conversions: every E4M3 value is an fp16 value)
+__device__ __forceinline__ void em_e4m3x4(uint32_t w, float m, float (&s)[4]) {
+  uint32_t h01, h23;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+      : "=r"(h01), "=r"(h23)
+      : "r"(w));
+  const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+  const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+  s[0] = f01.x * m;
+  s[1] = f01.y * m;
+  s[2] = f23.x * m;
+  s[3] = f23.y * m;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -143,14 +186,19 @@ __device__ __forceinline__ void em_ld16(const void* p, int dt, int64_t base, boo
 
 // NTP: n-tiles of accumulators (pairs per pass = 4 NTP; up to two n-tiles
 // keep the registers for two CTAs per SM).  GB: 16-column blocks per scale
-// group (G / 16).
-template <bool GATED, int NTP, int GB>
+// group (G / 16).  FP4: NVFP4 codes (GB = 4: a row's scale word of a
+// 64-column chunk holds the chunk's four E4M3 block scales), folded per
+// 16-column block:
+//   y += (S / 2) ((d_hi + d_lo) - 140 X),   S = E4M3 scale x matrix scale
+template <bool GATED, int NTP, int GB, bool FP4 = false>
 __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __grid_constant__ ExpertArgs A) {
   extern __shared__ __align__(128) unsigned char em_smem_raw[];
+  static_assert(!FP4 || GB == 4, "NVFP4 scale words cover 64 columns");
   constexpr int G = 16 * GB;
+  constexpr int GX = FP4 ? 16 : G, GBX = GX / 16;   // columns of a sum of x
   constexpr int NM = GATED ? 2 : 1;
-  const int K = A.K, nkc = K >> 6, nkb = K >> 4, ngr = K / G;
-  const EmPlan P = em_plan(K, G, GATED, A.ck, A.nst, A.pp, A.ks);
+  const int K = A.K, nkc = K >> 6, nkb = K >> 4, ngr = K / G, ngx = K / GX;
+  const EmPlan P = em_plan(K, G, GATED, A.ck, A.nst, A.pp, A.ks, GX);
   const int CK = P.ck, NS = P.ns;
   uint2* bfrag = reinterpret_cast<uint2*>(em_smem_raw);
   float* xs = reinterpret_cast<float*>(em_smem_raw + P.b_bytes);
@@ -381,15 +429,18 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
         for (int q = 0; q < 16; q += 4) sx += (v[q] + v[q + 1]) + (v[q + 2] + v[q + 3]);
       }
 #pragma unroll
-      for (int o = 1; o < GB; o <<= 1) sx += __shfl_xor_sync(0xffffffffu, sx, o);
-      if (i < nblk && (kb & (GB - 1)) == 0) xs[pl * ngr + kb / GB] = sx;
+      for (int o = 1; o < GBX; o <<= 1) sx += __shfl_xor_sync(0xffffffffu, sx, o);
+      if (i < nblk && (kb & (GBX - 1)) == 0) xs[pl * ngx + kb / GBX] = sx;
     }
     __syncthreads();
     if (first) cta_stamp(A.trace, 6);
 
     // ---- this warp's tiles
     const uint2* bl = bfrag + lane;   // + (nt * nkb + kb) * 32
-    const float* xsl = xs + t * ngr;  // + nt * 4 * ngr + grp
+    const float* xsl = xs + t * ngx;  // + nt * 4 * ngx + grp
+    // NVFP4: the segment's matrix scales, halved (the fold's 2 v)
+    const float gsu = FP4 ? 0.5f * __ldg(A.gsc + e) : 0.f;
+    const float gsg = (FP4 && GATED) ? 0.5f * __ldg(A.gsc_gate + e) : 0.f;
     float y[NTP][2], yg[NTP][2], acc[NTP][4], accg[NTP][4];
     // (a segment whose slot failed its index check issued no copies: no tiles)
     const int seg_tiles = npp > 0 ? my_tiles : 0;
@@ -423,6 +474,41 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
           const uint32_t wqs[4] = {wq.x, wq.y, wq.z, wq.w};
           const uint32_t wgs[4] = {wg.x, wg.y, wg.z, wg.w};
           const uint2* bk = bl + static_cast<int64_t>(kc0 + c) * 4 * 32;
+          if constexpr (FP4) {
+            // rows g and g + 8: the chunk's four block scales, times gs / 2
+            float su0[4], su1[4], sg0[4], sg1[4];
+            em_e4m3x4(sbu[c * 16], gsu, su0);
+            em_e4m3x4(sbu[c * 16 + 8], gsu, su1);
+            if (GATED) {
+              em_e4m3x4(sbg[c * 16], gsg, sg0);
+              em_e4m3x4(sbg[c * 16 + 8], gsg, sg1);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+              for (int nt = 0; nt < NTP; ++nt)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) acc[nt][r] = accg[nt][r] = 0.f;
+              uint32_t a[4], ag[4];
+              em_decode_fp4(wqs[j], a);
+              if (GATED) em_decode_fp4(wgs[j], ag);
+#pragma unroll
+              for (int nt = 0; nt < NTP; ++nt) {
+                if (nt < nnt) {
+                  const uint2 b = bk[(static_cast<int64_t>(nt) * nkb + j) * 32];
+                  mma_16816(acc[nt], a, b.x, b.y);
+                  if (GATED) mma_16816(accg[nt], ag, b.x, b.y);
+                  const float xv = xsl[nt * 4 * ngx + (kc0 + c) * 4 + j];
+                  y[nt][0] = fmaf(su0[j], fmaf(-140.f, xv, acc[nt][0] + acc[nt][1]), y[nt][0]);
+                  y[nt][1] = fmaf(su1[j], fmaf(-140.f, xv, acc[nt][2] + acc[nt][3]), y[nt][1]);
+                  if (GATED) {
+                    yg[nt][0] = fmaf(sg0[j], fmaf(-140.f, xv, accg[nt][0] + accg[nt][1]), yg[nt][0]);
+                    yg[nt][1] = fmaf(sg1[j], fmaf(-140.f, xv, accg[nt][2] + accg[nt][3]), yg[nt][1]);
+                  }
+                }
+              }
+            }
+          } else {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             if (j % GB == 0 && (GB <= 4 || (c & 1) == 0)) {
@@ -456,7 +542,7 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
 #pragma unroll
               for (int nt = 0; nt < NTP; ++nt) {
                 if (nt < nnt) {
-                  const float xv = xsl[nt * 4 * ngr + grp];
+                  const float xv = xsl[nt * 4 * ngx + grp];
                   const float r0 = fmaf(-128.f, xv, acc[nt][0] + acc[nt][1]);
                   const float r1 = fmaf(-128.f, xv, acc[nt][2] + acc[nt][3]);
                   y[nt][0] = fmaf(s0, r0, fmaf(b0, xv, y[nt][0]));
@@ -470,6 +556,7 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
                 }
               }
             }
+          }
           }
         }
       }

@@ -1435,6 +1435,10 @@ struct ExpertArgs {
   const uint32_t* sbt_gate;
   int ck, pp, ks;   // ks: warps sharing a tile's K range (1, 2 or 4)
   int one_pass;     // every slot has at most pp pairs (T <= pp): one segment a slot
+  // NVFP4 experts (k_expert_mma<..., true>): sbt/sbt_gate hold the E4M3 block
+  // scales, four a word; the per-matrix fp32 scales of the experts [E]
+  const float* gsc;
+  const float* gsc_gate;
   unsigned long long* trace;   // diagnostics: CTA stamps or null
 };
 

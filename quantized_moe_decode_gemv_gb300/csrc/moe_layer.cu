@@ -103,6 +103,10 @@ struct moe_layer {
   int umax = 0;
   int kin = 0;
   int bits = 4;           // code width of the routed experts (3, 4 or 8)
+  int fmt = 0;            // MOE_WFMT_AFFINE or MOE_WFMT_NVFP4
+  float* up_gs = nullptr;     // NVFP4: per-matrix scales of the experts [E]
+  float* gate_gs = nullptr;
+  float* down_gs = nullptr;
   int grouped_min_t = 32;
   int expert_split = 0;   // AUTO's grouped path: light experts on the int4 gemv kernel
   int last_launches = 0;  // kernel launches of the last forward
@@ -228,8 +232,15 @@ static moe_status validate_impl(const moe_layer_config* c, const moe_layer_weigh
   }
   if (c->bits != 0 && c->bits != 3 && c->bits != 4 && c->bits != 8)
     return fail(MOE_ERR_INVALID_ARG, "bits must be 0 (= 4), 3, 4 or 8");
+  if (c->weight_format != MOE_WFMT_AFFINE && c->weight_format != MOE_WFMT_NVFP4)
+    return fail(MOE_ERR_INVALID_ARG, "unknown weight_format");
   const int G = c->group_size;
-  if (G != 32 && G != 64 && G != 128) return fail(MOE_ERR_SHAPE, "group_size must be 32, 64 or 128");
+  if (c->weight_format == MOE_WFMT_NVFP4) {
+    if (c->bits != 0 && c->bits != 4) return fail(MOE_ERR_INVALID_ARG, "NVFP4 codes are 4 bits");
+    if (G != 16) return fail(MOE_ERR_SHAPE, "NVFP4 blocks are 16 elements: group_size must be 16");
+  } else if (G != 32 && G != 64 && G != 128) {
+    return fail(MOE_ERR_SHAPE, "group_size must be 32, 64 or 128");
+  }
   const int kin = c->latent > 0 ? c->latent : c->hidden;
   if (c->hidden % 64 || c->expert_ffn % 64 || kin % 64 || (c->shared_ffn % 64))
     return fail(MOE_ERR_SHAPE, "hidden, expert_ffn, latent and shared_ffn must be multiples of 64");
@@ -238,7 +249,8 @@ static moe_status validate_impl(const moe_layer_config* c, const moe_layer_weigh
   if (c->n_experts > MAX_E) return fail(MOE_ERR_UNSUPPORTED, "more than 1024 experts");
   if (c->top_k > MAX_K) return fail(MOE_ERR_UNSUPPORTED, "top_k above 16");
   if (c->act_dtype == MOE_DTYPE_FP32) return fail(MOE_ERR_UNSUPPORTED, "fp32 activations");
-  if (c->scale_dtype == MOE_DTYPE_FP32) return fail(MOE_ERR_UNSUPPORTED, "fp32 scales");
+  if (c->scale_dtype == MOE_DTYPE_FP32 && c->weight_format == MOE_WFMT_AFFINE)
+    return fail(MOE_ERR_UNSUPPORTED, "fp32 scales");
   if (c->has_router_bias && c->router != MOE_ROUTER_SIGMOID)
     return fail(MOE_ERR_UNSUPPORTED, "router bias is defined for sigmoid routing only");
   if (w) {
@@ -521,7 +533,7 @@ struct EmLaunch {
   int per_sm = 0, cps = 1;
 };
 static bool em_choose(int K, int G, bool gated, int T, int pp_cap, int n_rows, int slots, int num_sms,
-                      EmLaunch* o) {
+                      EmLaunch* o, bool fp4 = false) {
   const int pp_want = std::min(std::min(EM_MAX_PAIRS, std::max(4, pp_cap & ~3)), std::max(4, (T + 3) & ~3));
   // warps per tile: a function of K alone, so that a row's sums do not depend
   // on the batch (about 6 to 12 chunks of 64 columns a warp)
@@ -534,7 +546,7 @@ static bool em_choose(int K, int G, bool gated, int T, int pp_cap, int n_rows, i
       const int budget = per_sm == 2 ? 110 * 1024 : kSmemMax - 2048;
       for (const auto& cn : kCkNs) {
         if (G == 128 && cn[0] % 2) continue;
-        const EmPlan p = em_plan(K, G, gated, cn[0], cn[1], pp, ks);
+        const EmPlan p = em_plan(K, G, gated, cn[0], cn[1], pp, ks, fp4 ? 16 : 0);
         if (p.smem > budget) continue;
         o->plan = p;
         o->per_sm = per_sm;
@@ -608,19 +620,20 @@ static cudaError_t launch_dense_mma(DmArgs a, const DmLaunch& dl, size_t smem, c
   return launch_dense_mma_t<4, false>(a, dl.grid, smem, s, pdl);
 }
 
-template <int NTP, int GB>
+template <int NTP, int GB, bool FP4>
 static cudaError_t launch_expert_mma_t(const ExpertArgs& a, bool gated, int grid, size_t smem, cudaStream_t s,
                                        bool pdl) {
-  if (gated) return launch_ex<ExpertArgs>(k_expert_mma<true, NTP, GB>, grid, EM_NT, smem, s, pdl, a);
-  return launch_ex<ExpertArgs>(k_expert_mma<false, NTP, GB>, grid, EM_NT, smem, s, pdl, a);
+  if (gated) return launch_ex<ExpertArgs>(k_expert_mma<true, NTP, GB, FP4>, grid, EM_NT, smem, s, pdl, a);
+  return launch_ex<ExpertArgs>(k_expert_mma<false, NTP, GB, FP4>, grid, EM_NT, smem, s, pdl, a);
 }
-template <int GB>
+template <int GB, bool FP4 = false>
 static cudaError_t launch_expert_mma_g(const ExpertArgs& a, bool gated, int pp, int grid, size_t smem,
                                        cudaStream_t s, bool pdl) {
-  if (pp <= 4) return launch_expert_mma_t<1, GB>(a, gated, grid, smem, s, pdl);
-  if (pp <= 8) return launch_expert_mma_t<2, GB>(a, gated, grid, smem, s, pdl);
-  return launch_expert_mma_t<4, GB>(a, gated, grid, smem, s, pdl);
+  if (pp <= 4) return launch_expert_mma_t<1, GB, FP4>(a, gated, grid, smem, s, pdl);
+  if (pp <= 8) return launch_expert_mma_t<2, GB, FP4>(a, gated, grid, smem, s, pdl);
+  return launch_expert_mma_t<4, GB, FP4>(a, gated, grid, smem, s, pdl);
 }
+// (a.G: the columns a scale word covers -- 64 for NVFP4, whose a.gsc is set)
 static cudaError_t launch_expert_mma(ExpertArgs a, const EmLaunch& el, int T, int grid, cudaStream_t s,
                                      bool pdl) {
   a.ck = el.plan.ck;
@@ -632,6 +645,7 @@ static cudaError_t launch_expert_mma(ExpertArgs a, const EmLaunch& el, int T, in
   a.one_pass = T <= a.pp && (a.max_pairs <= 0 || a.max_pairs >= T);
   const size_t smem = static_cast<size_t>(el.plan.smem);
   const bool gated = a.qt_gate != nullptr;
+  if (a.gsc) return launch_expert_mma_g<4, true>(a, gated, el.plan.pp, grid, smem, s, pdl);
   switch (a.G) {
     case 32: return launch_expert_mma_g<2>(a, gated, el.plan.pp, grid, smem, s, pdl);
     case 64: return launch_expert_mma_g<4>(a, gated, el.plan.pp, grid, smem, s, pdl);
@@ -711,6 +725,9 @@ static cudaError_t set_smem_attrs() {
   MOE_SMEM_ATTR((k_expert_mma<false, 2, GB>)) MOE_SMEM_ATTR((k_expert_mma<true, 2, GB>)) \
   MOE_SMEM_ATTR((k_expert_mma<false, 4, GB>)) MOE_SMEM_ATTR((k_expert_mma<true, 4, GB>))
   MOE_SMEM_ATTR_EM(2) MOE_SMEM_ATTR_EM(4) MOE_SMEM_ATTR_EM(8)
+  MOE_SMEM_ATTR((k_expert_mma<false, 1, 4, true>)) MOE_SMEM_ATTR((k_expert_mma<true, 1, 4, true>))
+  MOE_SMEM_ATTR((k_expert_mma<false, 2, 4, true>)) MOE_SMEM_ATTR((k_expert_mma<true, 2, 4, true>))
+  MOE_SMEM_ATTR((k_expert_mma<false, 4, 4, true>)) MOE_SMEM_ATTR((k_expert_mma<true, 4, 4, true>))
   MOE_SMEM_ATTR((k_dense_mma<1, false>)) MOE_SMEM_ATTR((k_dense_mma<2, false>))
   MOE_SMEM_ATTR((k_dense_mma<4, false>)) MOE_SMEM_ATTR((k_dense_mma<1, true>))
   MOE_SMEM_ATTR((k_dense_mma<2, true>)) MOE_SMEM_ATTR((k_dense_mma<4, true>))
@@ -799,6 +816,15 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     g_create_error = "a reduction width exceeds the shared-memory staging limit";
     return MOE_ERR_UNSUPPORTED;
   }
+  if (c.weight_format == MOE_WFMT_NVFP4) {
+    // the NVFP4 expert kernel at four pairs a pass, which every batch can use
+    EmLaunch p_up, p_dn;
+    if (!em_choose(kin, 64, gated, 1, 4, F, 1, prop.multiProcessorCount, &p_up, true) ||
+        !em_choose(F, 64, false, 1, 4, kin, 1, prop.multiProcessorCount, &p_dn, true)) {
+      g_create_error = "no shared-memory plan of the NVFP4 expert kernel fits this shape";
+      return MOE_ERR_UNSUPPORTED;
+    }
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   L = new moe_layer();
   L->cfg = c;
@@ -807,6 +833,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   L->kin = kin;
   L->bits = c.bits == 0 ? 4 : c.bits;
   L->cfg.bits = L->bits;
+  L->fmt = c.weight_format;
   L->off_fc1 = E;
   L->off_shg = E + Lt;
   L->off_shu = E + Lt + (gated ? Fs : 0);
@@ -839,6 +866,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   if (const char* env = std::getenv("MOE_DENSE_BULK")) L->dense_bulk = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_EXPERT_BULK_MAX_T")) L->expert_bulk_max_t = std::max(0, std::atoi(env));
   if (const char* env = std::getenv("MOE_EXPERT_MMA")) L->expert_mma = std::atoi(env) != 0;
+  if (L->fmt == MOE_WFMT_NVFP4) L->expert_mma = true;   // the only kernel that decodes NVFP4
   if (const char* env = std::getenv("MOE_EXPERT_MMA_MAX_T")) L->expert_mma_max_t = std::max(0, std::atoi(env));
   if (const char* env = std::getenv("MOE_DENSE_MMA")) L->dense_mma = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_EXPERT_MMA_PP"))
@@ -890,14 +918,29 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
                                              static_cast<int64_t>(n));
       return cudaGetLastError();
     };
+    const bool fp4 = L->fmt == MOE_WFMT_NVFP4;
+    // NVFP4: the E4M3 block scales as they are (four to a word: one word per
+    // row and 64 columns) and the per-matrix fp32 scales
+    auto copy_fp4 = [&](uint32_t** dst, float** gdst, const void* sc, const void* gs, int rows,
+                        int K) -> cudaError_t {
+      const size_t n = static_cast<size_t>(E) * rows * (K / 64);
+      cudaError_t e = L->alloc(reinterpret_cast<void**>(dst), n * 4);
+      if (e == cudaSuccess) e = cudaMemcpyAsync(*dst, sc, n * 4, cudaMemcpyDeviceToDevice, s);
+      if (e == cudaSuccess) e = L->alloc(reinterpret_cast<void**>(gdst), E * sizeof(float));
+      if (e == cudaSuccess) e = cudaMemcpyAsync(*gdst, gs, E * sizeof(float), cudaMemcpyDeviceToDevice, s);
+      return e;
+    };
     if (gated) {
       MOE_TRY_CUDA(copy_q(&L->gate_q, w->gate_q, nq_in), "gate codes");
-      MOE_TRY_CUDA(copy_sb(&L->gate_sb, w->gate_s, w->gate_b, ng_in), "gate scales");
+      MOE_TRY_CUDA(fp4 ? copy_fp4(&L->gate_sb, &L->gate_gs, w->gate_s, w->gate_b, F, kin)
+                       : copy_sb(&L->gate_sb, w->gate_s, w->gate_b, ng_in), "gate scales");
     }
     MOE_TRY_CUDA(copy_q(&L->up_q, w->up_q, nq_in), "up codes");
-    MOE_TRY_CUDA(copy_sb(&L->up_sb, w->up_s, w->up_b, ng_in), "up scales");
+    MOE_TRY_CUDA(fp4 ? copy_fp4(&L->up_sb, &L->up_gs, w->up_s, w->up_b, F, kin)
+                     : copy_sb(&L->up_sb, w->up_s, w->up_b, ng_in), "up scales");
     MOE_TRY_CUDA(copy_q(&L->down_q, w->down_q, nq_dn), "down codes");
-    MOE_TRY_CUDA(copy_sb(&L->down_sb, w->down_s, w->down_b, ng_dn), "down scales");
+    MOE_TRY_CUDA(fp4 ? copy_fp4(&L->down_sb, &L->down_gs, w->down_s, w->down_b, kin, F)
+                     : copy_sb(&L->down_sb, w->down_s, w->down_b, ng_dn), "down scales");
     auto group_major = [&](uint32_t** dst, const uint32_t* src, int rows, int ngr) -> cudaError_t {
       const size_t n = static_cast<size_t>(E) * rows * ngr;
       cudaError_t e = L->alloc(reinterpret_cast<void**>(dst), n * 4);
@@ -906,7 +949,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
       k_sb_group_major<<<blocks, 256, 0, s>>>(src, *dst, E, rows, ngr);
       return cudaGetLastError();
     };
-    if (L->bits == 4) {   // the grouped GEMM's scale layout (4-bit codes only)
+    if (L->bits == 4 && !fp4) {   // the grouped GEMM's scale layout (4-bit affine codes only)
       if (gated) MOE_TRY_CUDA(group_major(&L->gate_sbT, L->gate_sb, F, kin / G), "gate scales");
       MOE_TRY_CUDA(group_major(&L->up_sbT, L->up_sb, F, kin / G), "up scales");
       MOE_TRY_CUDA(group_major(&L->down_sbT, L->down_sb, kin, F / G), "down scales");
@@ -929,14 +972,15 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
       return cudaGetLastError();
     };
     if (L->bits == 4 && L->expert_mma) {
+      const int Gs = fp4 ? 64 : G;   // columns a scale word covers
       if (gated) {
         MOE_TRY_CUDA(tile_q(&L->gate_qt, L->gate_q, F, kin), "gate tiles");
-        MOE_TRY_CUDA(tile_sb(&L->gate_sbt, L->gate_sb, F, kin / G), "gate tiles");
+        MOE_TRY_CUDA(tile_sb(&L->gate_sbt, L->gate_sb, F, kin / Gs), "gate tiles");
       }
       MOE_TRY_CUDA(tile_q(&L->up_qt, L->up_q, F, kin), "up tiles");
-      MOE_TRY_CUDA(tile_sb(&L->up_sbt, L->up_sb, F, kin / G), "up tiles");
+      MOE_TRY_CUDA(tile_sb(&L->up_sbt, L->up_sb, F, kin / Gs), "up tiles");
       MOE_TRY_CUDA(tile_q(&L->down_qt, L->down_q, kin, F), "down tiles");
-      MOE_TRY_CUDA(tile_sb(&L->down_sbt, L->down_sb, kin, F / G), "down tiles");
+      MOE_TRY_CUDA(tile_sb(&L->down_sbt, L->down_sb, kin, F / Gs), "down tiles");
     }
     if (Fs) {
       const size_t n = static_cast<size_t>(Fs) * H * adt;
@@ -1330,7 +1374,8 @@ static void print_cta_trace(moe_layer* h, cudaStream_t s) {
 
 // The path a forward of T rows takes (never AUTO).
 static int choose_path(const moe_layer* h, int T) {
-  if (h->bits != 4) return MOE_PATH_GEMV;   // the tensor-core path decodes 4-bit codes only
+  // the tensor-core path decodes 4-bit affine codes only
+  if (h->bits != 4 || h->fmt != MOE_WFMT_AFFINE) return MOE_PATH_GEMV;
   if (h->path == MOE_PATH_GROUPED || (h->path == MOE_PATH_AUTO && T >= h->grouped_min_t))
     return MOE_PATH_GROUPED;
   return MOE_PATH_GEMV;
@@ -1480,15 +1525,26 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
   const int slots_e = std::min(E, T * k);   // distinct-expert slots of the expert launches
   // the warp-MMA expert kernel (4-bit codes in its tiled layout)
   EmLaunch em_up, em_dn;
-  const bool use_mma = h->expert_mma && h->up_qt && T <= h->expert_mma_max_t;
+  // (NVFP4 layers have no other expert kernel: their scale words cover 64
+  // columns, sums of x 16)
+  const bool fp4 = h->fmt == MOE_WFMT_NVFP4;
+  const int Gm = fp4 ? 64 : c.group_size;
+  const bool use_mma = h->expert_mma && h->up_qt && (fp4 || T <= h->expert_mma_max_t);
   // (a gated up projection with 32-column groups folds twice per 64 columns and
   // two matrices: there the CUDA-core kernels measured faster, 59 vs 73 us at
   // T = 1 on the non-latent layer; the choice depends on the shape alone)
-  const bool mma_up = use_mma && !(gated && c.group_size == 32) &&
-                      em_choose(kin, c.group_size, gated, T, h->expert_mma_pp, F, slots_e, h->num_sms, &em_up);
-  const bool mma_dn = use_mma && em_choose(F, c.group_size, false, T, h->expert_mma_pp, kin, slots_e,
-                                           h->num_sms, &em_dn);
-  const bool use_bulk = h->expert_bulk && !grouped && T <= h->expert_bulk_max_t && h->bits == 4;
+  const bool mma_up = use_mma && (fp4 || !(gated && c.group_size == 32)) &&
+                      em_choose(kin, Gm, gated, T, h->expert_mma_pp, F, slots_e, h->num_sms, &em_up, fp4);
+  const bool mma_dn = use_mma && em_choose(F, Gm, false, T, h->expert_mma_pp, kin, slots_e,
+                                           h->num_sms, &em_dn, fp4);
+  if (fp4 && !grouped && (!mma_up || !mma_dn)) {
+    // (create refused layers without a plan at four pairs a pass, which every
+    // batch size can fall back to)
+    for (; nvtx_open > 0; --nvtx_open) nvtxRangePop();
+    h->last_error = "no shared-memory plan of the NVFP4 expert kernel fits this shape";
+    return MOE_ERR_UNSUPPORTED;
+  }
+  const bool use_bulk = h->expert_bulk && !grouped && T <= h->expert_bulk_max_t && h->bits == 4 && !fp4;
   EbLaunch eb_up, eb_dn;
   int cps_up = 1, cps_dn = 1;
   // pairs per pass: a distinct expert of a small batch holds one or two of its
@@ -1741,7 +1797,9 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
     if (experts_gemv) {
       up.n_rows = F;
       up.K = kin;
-      up.G = c.group_size;
+      up.G = Gm;
+      up.gsc = fp4 ? h->up_gs : nullptr;
+      up.gsc_gate = (fp4 && gated) ? h->gate_gs : nullptr;
       up.q = h->up_q;
       up.sb = h->up_sb;
       up.q_gate = gated ? h->gate_q : nullptr;
@@ -1867,6 +1925,8 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
         dn.qt = h->down_qt;
         dn.sbt = h->down_sbt;
         dn.qt_gate = nullptr;
+        dn.gsc = fp4 ? h->down_gs : nullptr;
+        dn.gsc_gate = nullptr;
         dn.sbt_gate = nullptr;
         dn.trace = tslot("k_expert_mma_down");
         if ((e = launch_expert_mma(dn, em_dn, T, h->num_sms * em_dn.per_sm, cs, pdl)) != cudaSuccess) goto cuda_fail;
@@ -2099,8 +2159,8 @@ moe_status moe_layer_set_path(moe_layer* h, int32_t path) {
     h->last_error = "the grouped path needs 16-bit activations";
     return MOE_ERR_UNSUPPORTED;
   }
-  if (path == MOE_PATH_GROUPED && h->bits != 4) {
-    h->last_error = "the grouped path decodes 4-bit codes only";
+  if (path == MOE_PATH_GROUPED && (h->bits != 4 || h->fmt != MOE_WFMT_AFFINE)) {
+    h->last_error = "the grouped path decodes 4-bit affine codes only";
     return MOE_ERR_UNSUPPORTED;
   }
   h->path = path;

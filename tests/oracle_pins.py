@@ -152,6 +152,84 @@ def pin_quant_roundtrip_bits(ora):
         assert np.all(np.abs(w - deq) <= bound)
 
 
+def _nvfp4_fixture():
+    e2m1, e4m3 = {}, {}
+    for line in open(os.path.join(GOLDEN, "nvfp4_formats.txt")):
+        f = line.split()
+        if not f or f[0].startswith("#"):
+            continue
+        key = int(f[1], 16)
+        val = math.nan if f[2] == "nan" else (-0.0 if f[2] == "-0" else float(Fraction(f[2])))
+        (e2m1 if f[0] == "e2m1" else e4m3)[key] = val
+    return e2m1, e4m3
+
+
+def pin_nvfp4_format_fixture(ora):
+    """Every E2M1 code and the listed E4M3 bytes decode to the hand-worked
+    values of nvfp4_formats.txt (signs of zeros included, NaN where listed)."""
+    e2m1, e4m3 = _nvfp4_fixture()
+    assert len(e2m1) == 16 and len(e4m3) >= 20
+    for tab, fn in ((e2m1, ora.e2m1_values), (e4m3, ora.e4m3_values)):
+        keys = np.array(sorted(tab))
+        got = np.asarray(fn(keys), dtype=np.float64)
+        for k, g in zip(keys, got):
+            want = tab[int(k)]
+            if math.isnan(want):
+                assert math.isnan(g), (hex(k), g)
+            else:
+                assert g == want and math.copysign(1, g) == math.copysign(1, want), (hex(k), g, want)
+
+
+def pin_e4m3_grid(ora):
+    """The 127 non-negative finite E4M3 bytes (0x00..0x7E) decode to strictly
+    increasing multiples of 2^-9 from 0 to 448; setting the sign bit negates;
+    0x7F and 0xFF are NaN; between consecutive powers of two from 2^-6 on
+    there are exactly 8 values (3 mantissa bits)."""
+    v = np.asarray(ora.e4m3_values(np.arange(0x7F)), dtype=np.float64)
+    assert v[0] == 0 and v[-1] == 448 and np.all(np.diff(v) > 0)
+    assert np.all(v * 512 == np.rint(v * 512))
+    assert np.array_equal(np.asarray(ora.e4m3_values(np.arange(0x7F) | 0x80)), -v)
+    assert np.isnan(ora.e4m3_values(np.array([0x7F, 0xFF]))).all()
+    for p2 in range(-6, 8):
+        n = int(((v >= 2.0 ** p2) & (v < 2.0 ** (p2 + 1))).sum())
+        assert n == 8, (p2, n)
+
+
+def pin_dequant_nvfp4_worked_example(ora):
+    """Two blocks of one row, worked by hand: block 0 holds every code with
+    scale byte 0x40 (2.0); block 1 repeats codes 0x7 and 0x9 with scale byte 0x01
+    (2^-9); the matrix scale is 0.25."""
+    codes = np.array([[0x2, 0xA, 0x7, 0xF, 0x1, 0x9, 0x0, 0x8, 0x3, 0x4, 0x5, 0x6, 0xB, 0xC, 0xD, 0xE]
+                      + [0x7, 0x9] * 8], dtype=np.uint8)
+    scale = np.array([[0x40, 0x01]], dtype=np.uint8)
+    want = [0.5, -0.5, 3, -3, 0.25, -0.25, 0, -0, 0.75, 1, 1.5, 2, -0.75, -1, -1.5, -2] + \
+           [6 / 2048, -0.5 / 2048] * 8
+    got = ora.dequantize_nvfp4(mi.pack_codes(codes, 4), scale, np.float32(0.25))
+    assert got.shape == (1, 32)
+    assert np.array_equal(got[0], np.array(want, dtype=np.float64)), got
+
+
+def pin_nvfp4_quant_roundtrip(ora):
+    """The generator's NVFP4 quantiser and the oracle's decoder: every weight is
+    within half the largest E2M1 gap (1.0) of its block scale S of its value,
+    each block's largest magnitude is reproduced to within the E4M3 rounding
+    (1/16 relative) or is saturated at 6 S, and re-quantising the decoded
+    weights gives back the same codes and scales."""
+    rng = np.random.Generator(np.random.PCG64(33))
+    w = rng.normal(0, 0.02, size=(8, 128))
+    q, sb, gs = mi.quantize_nvfp4(w)
+    deq = ora.dequantize_nvfp4(mi.pack_codes(q, 4), sb, gs)
+    S = np.repeat(ora.e4m3_values(sb), 16, axis=-1) * float(gs)
+    assert np.all(np.abs(w - deq) <= S * 1.0 + 1e-15)
+    bmax = np.abs(w).reshape(8, 8, 16).max(-1)
+    dmax = np.abs(deq).reshape(8, 8, 16).max(-1)
+    assert np.all(np.abs(dmax - bmax) <= bmax / 16 + 1e-12)
+    q2, sb2, gs2 = mi.quantize_nvfp4(deq)
+    assert np.float32(gs2) <= np.float32(gs)
+    deq2 = ora.dequantize_nvfp4(mi.pack_codes(q2, 4), sb2, gs2)
+    assert np.allclose(deq2, deq, rtol=0, atol=float(np.max(S)))
+
+
 def pin_quant_roundtrip(ora):
     """The generator's quantiser applied to the oracle's dequantised weights
     gives back the same codes (groups hold codes 0 and 15, so the recomputed

@@ -36,7 +36,7 @@ def test_header_declares_the_boundary():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
-    assert lib.moe_abi_version() == 3
+    assert lib.moe_abi_version() == 4
 
 
 def test_status_strings(lib):
@@ -94,6 +94,13 @@ CASES = [
     ("2-bit codes", {"bits": 2}, {}, "MOE_ERR_INVALID_ARG"),
     ("5-bit codes", {"bits": 5}, {}, "MOE_ERR_INVALID_ARG"),
     ("16-bit codes", {"bits": 16}, {}, "MOE_ERR_INVALID_ARG"),
+    ("nvfp4", {"fmt": "nvfp4", "group_size": 16}, {}, "MOE_OK"),
+    ("nvfp4 bits 0", {"fmt": "nvfp4", "group_size": 16, "bits": 0}, {}, "MOE_OK"),
+    ("nvfp4 fp32 scale dtype ignored", {"fmt": "nvfp4", "group_size": 16, "scale_dtype": "fp32"}, {},
+     "MOE_OK"),
+    ("nvfp4 block 32", {"fmt": "nvfp4", "group_size": 32}, {}, "MOE_ERR_SHAPE"),
+    ("nvfp4 8-bit", {"fmt": "nvfp4", "group_size": 16, "bits": 8}, {}, "MOE_ERR_INVALID_ARG"),
+    ("affine group 16", {"group_size": 16}, {}, "MOE_ERR_SHAPE"),
 ]
 
 

@@ -49,7 +49,7 @@ def test_debug_build_is_selected_and_flagged():
     assert checks["lib"] == "libmoe_gb300_checks.so"
     assert checks["flags"] == 3   # MOE_BUILD_CHECKS | MOE_BUILD_NVTX_DEFAULT
     for r in (plain, checks):
-        assert r["abi"] == 3
+        assert r["abi"] == 4
         assert r["refusal"] == "MOE_ERR_TOPK_GT_E"
         assert r["index_name"] == "MOE_ERR_INDEX"
 

@@ -183,6 +183,52 @@ def test_code_width_grouped_refused(bits):
     assert h.path_for(16) == "gemv"
 
 
+# --- NVFP4 experts: E2M1 codes, E4M3 block scales, fp32 matrix scales ------------
+
+def _fp4_layer(spec, seed=0):
+    return gu.cached_layer_spec(spec.with_(name=f"{spec.name}_nvfp4", fmt="nvfp4", group_size=16), seed)
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 5, 16, 33])
+def test_nvfp4_tiny_parity(T):
+    """The tiny SwiGLU layer with NVFP4 experts (gate and up in one kernel),
+    every row; 33 rows take several passes of 16 pairs over an expert."""
+    lay = _fp4_layer(mi.spec_for("tiny"))
+    _, h = handle_for(lay.spec.name, 48, layer=lay)
+    assert h.path_for(T) == "gemv"
+    _parity(lay.spec.name, T, max_tokens=48, paths=("auto",))
+
+
+@pytest.mark.parametrize("T,rows", [(1, None), (2, None), (9, [0, 4, 8]), (16, [0, 15])])
+def test_nvfp4_latent_parity(T, rows):
+    """The latent layer (E=496, k=9, latent 1024, squared ReLU) with NVFP4
+    experts at full size."""
+    lay = _fp4_layer(mi.spec_for("latent"))
+    handle_for(lay.spec.name, 16, layer=lay)
+    _parity(lay.spec.name, T, rows=rows, max_tokens=16, paths=("auto",))
+
+
+@pytest.mark.parametrize("T", [1, 4, 12])
+def test_nvfp4_fp16_softmax_parity(T):
+    """fp16 activations, softmax without renormalisation, SwiGLU, latent 256,
+    F = 384 (not a power of two) with NVFP4 experts."""
+    lay = _fp4_layer(ODD["odd_latent_fp16"])
+    handle_for(lay.spec.name, 16, layer=lay)
+    _parity(lay.spec.name, T, max_tokens=16, paths=("auto",))
+
+
+def test_nvfp4_grouped_refused():
+    """The tensor-core schedule decodes affine codes only: forcing it on an
+    NVFP4 layer is refused and AUTO keeps the gemv schedule at every T."""
+    import quantized_moe_decode_gemv_gb300 as pkg
+    lay = _fp4_layer(mi.spec_for("tiny"))
+    _, h = handle_for(lay.spec.name, 48, layer=lay)
+    with pytest.raises(pkg.MoEError) as ei:
+        h.set_path("grouped")
+    assert "MOE_ERR_UNSUPPORTED" in str(ei.value)
+    assert [h.path_for(T) for T in (1, 32, 48)] == ["gemv"] * 3
+
+
 # --- non-latent fp16 sigmoid top-8 layer (H=6144, E=256) at full size ---------
 
 @pytest.mark.parametrize("T,rows", [(1, None), (4, [0, 3]), (32, [0, 17, 31])])

@@ -54,6 +54,17 @@ MUTANTS = [
     ("shared gate/up swapped", "    h = activation(sp, u, g)\n    return widen(layer.sh_down, dt) @ h",
      "    h = activation(sp, g, u) if g is not None else activation(sp, u, g)\n"
      "    return widen(layer.sh_down, dt) @ h"),
+    ("E2M1 exponent bias dropped", "np.exp2(ef - 1.0) * (1.0 + 0.5 * mf)", "np.exp2(ef) * (1.0 + 0.5 * mf)"),
+    ("E2M1 subnormal as normal", "mag = np.where(ef == 0, 0.5 * mf, ", "mag = np.where(ef < 0, 0.5 * mf, "),
+    ("E2M1 sign ignored", "    return np.where(sign == 1, -mag, mag)\n\n\ndef e4m3_values",
+     "    return mag\n\n\ndef e4m3_values"),
+    ("E2M1 exponent bits swapped", "ef = (c >> 2 & 1) * 2 + (c >> 1 & 1)", "ef = (c >> 1 & 1) * 2 + (c >> 2 & 1)"),
+    ("E4M3 exponent bias 8", "(1.0 + mf / 8.0) * np.exp2(ef - 7.0)", "(1.0 + mf / 8.0) * np.exp2(ef - 8.0)"),
+    ("E4M3 subnormal off by a power of two", "(mf / 8.0) * 2.0 ** -6", "(mf / 8.0) * 2.0 ** -7"),
+    ("E4M3 mantissa of 4 bits", "mf = v & 7\n", "mf = v & 15\n"),
+    ("NVFP4 blocks of 32", "np.repeat(s, 16, axis=-1) * float", "np.repeat(s, 32, axis=-1)[..., : q.shape[-1]] * float"),
+    ("NVFP4 matrix scale dropped", "return q * np.repeat(s, 16, axis=-1) * float(np.float32(matrix_scale))",
+     "return q * np.repeat(s, 16, axis=-1)"),
 ]
 
 
