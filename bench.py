@@ -205,12 +205,15 @@ def parse_args():
 def expert_bytes(spec):
     """(up-side bytes, down-side bytes) of one routed expert: packed b-bit codes
     + scale + bias (2 bytes each per group); NVFP4: 4-bit codes, one E4M3 byte
-    per 16 elements and a 4-byte matrix scale per matrix."""
+    per 16 elements and a 4-byte matrix scale per matrix; MXFP4: 4-bit codes and
+    one E8M0 byte per 32 elements."""
     n_in = 2 if spec.gated else 1
     e_in = n_in * spec.expert_ffn * spec.k_in
     e_dn = spec.k_in * spec.expert_ffn
     if getattr(spec, "fmt", "affine") == "nvfp4":
         return (e_in // 2 + e_in // 16 + 4 * n_in, e_dn // 2 + e_dn // 16 + 4)
+    if getattr(spec, "fmt", "affine") == "mxfp4":
+        return (e_in // 2 + e_in // 32, e_dn // 2 + e_dn // 32)
     sb = 2 * 2
     b = spec.bits
     return (e_in * b // 8 + sb * (e_in // spec.group_size), e_dn * b // 8 + sb * (e_dn // spec.group_size))
@@ -576,6 +579,9 @@ def run_ours(args):
             also.append(workload_line(torch, pkg, fp4, T, st_also, args.warmup, args.seed, flush, stream,
                                       hbm_peak, tc_peak,
                                       label="latent layer, NVFP4 experts (E2M1, E4M3 per 16, fp32 per matrix)"))
+        mx = mi.SPECS["latent"].with_(name="latent_mxfp4", fmt="mxfp4", group_size=32)
+        also.append(workload_line(torch, pkg, mx, 1, st_also, args.warmup, args.seed, flush, stream,
+                                  hbm_peak, tc_peak, label="latent layer, MXFP4 experts (E2M1, E8M0 per 32)"))
 
     # batched serving sweep (separate output file)
     if sweep and rank == 0:

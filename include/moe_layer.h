@@ -43,6 +43,10 @@
  *     program's weight-format table lists "mxfp4/nvfp4" among its supported
  *     formats; the element and scale encodings are those of the OCP
  *     Microscaling (MX) specification's FP4 E2M1 and FP8 E4M3 types.
+ *   - MXFP4 experts (weight_format = MOE_WFMT_MXFP4): the same E2M1 codes with
+ *     one E8M0 scale byte per 32 consecutive elements along the input axis
+ *     (the power of two 2^(byte - 127); 0xFF is NaN) and no other term: a
+ *     weight is e2m1(q) * 2^(s - 127) (the same specification's MXFP4).
  *   - bf16/fp16 buffers hold IEEE/bfloat16 16-bit values.
  *   - Every function returns a moe_status; MOE_OK is 0.  On error nothing that
  *     the call allocated stays allocated, and moe_layer_last_error() (where a
@@ -108,7 +112,8 @@ typedef enum moe_path {
 /* Expert weight formats (moe_layer_config.weight_format). */
 typedef enum moe_weight_format {
   MOE_WFMT_AFFINE = 0,   /* b-bit codes, scale and bias per group of group_size */
-  MOE_WFMT_NVFP4 = 1     /* E2M1 codes, E4M3 scale per 16, fp32 scale per matrix */
+  MOE_WFMT_NVFP4 = 1,    /* E2M1 codes, E4M3 scale per 16, fp32 scale per matrix */
+  MOE_WFMT_MXFP4 = 2     /* E2M1 codes, E8M0 scale per 32 */
 } moe_weight_format;
 
 typedef struct moe_layer_config {
@@ -132,8 +137,9 @@ typedef struct moe_layer_config {
                             3- and 8-bit layers run the GEMV schedule only: AUTO
                             selects it at every T, GROUPED is refused */
   int32_t weight_format; /* moe_weight_format (0 = affine).  NVFP4 needs bits 0
-                            or 4 and group_size 16, and like 3/8-bit layers runs
-                            the GEMV schedule only (the warp-MMA expert kernel) */
+                            or 4 and group_size 16, MXFP4 bits 0 or 4 and
+                            group_size 32; like 3/8-bit layers they run the
+                            GEMV schedule only (the warp-MMA expert kernel) */
 } moe_layer_config;
 
 /* Weights, all DEVICE pointers owned by the caller.  moe_layer_create copies
@@ -151,7 +157,9 @@ typedef struct moe_layer_config {
  *     (sh_gate for SWIGLU only; all NULL when shared_ffn == 0)
  * NVFP4 layers: *_q as above (bits 4); *_s the E4M3 block scales, one byte per
  * 16 elements: [E, F, Kin/16] (gate, up) and [E, Kin, F/16] (down) uint8; *_b
- * the per-matrix fp32 scales [E]. */
+ * the per-matrix fp32 scales [E].
+ * MXFP4 layers: *_q as above; *_s the E8M0 block scales, one byte per 32
+ * elements: [E, F, Kin/32] and [E, Kin, F/32] uint8; *_b unused (may be NULL). */
 typedef struct moe_layer_weights {
   const void *router_w;
   const float *router_bias;
@@ -185,7 +193,7 @@ int32_t moe_build_flags(void);
  * with the same refusals and codes as moe_layer_create; touches no device.
  * `w` may be NULL to check the config alone.  Refusals, in order:
  *   MOE_ERR_INVALID_ARG   null cfg, non-positive sizes, bad enum values, bits
- *                         not 0, 3, 4 or 8 (NVFP4: not 0 or 4), an unknown
+ *                         not 0, 3, 4 or 8 (NVFP4, MXFP4: not 0 or 4), an unknown
  *                         weight_format
  *   MOE_ERR_TOPK_GT_E     top_k < 1 or top_k > n_experts (a layer whose top-k
  *                         exceeds its own expert count is refused before any
@@ -193,7 +201,7 @@ int32_t moe_build_flags(void);
  *   MOE_ERR_LATENT_PROJ   latent > 0 with fc1/fc2 missing or act_dtype not
  *                         16-bit (missing/non-bf16 latent projections are
  *                         refused by name in the same passage)
- *   MOE_ERR_SHAPE         G not 32/64/128 (NVFP4: not 16), or H, F, Kin not
+ *   MOE_ERR_SHAPE         G not 32/64/128 (NVFP4: not 16; MXFP4: not 32), or H, F, Kin not
  *                         multiples of 64 and of G, or expert weights present
  *                         for a shape that cannot hold them
  *   MOE_ERR_UNSUPPORTED   E > 1024 or top_k > 16 or shared expert without a
@@ -234,7 +242,7 @@ moe_status moe_layer_forward_host(moe_layer *h, const void *x_host, int32_t T, v
 
 /* Choose the routed-expert path for later forwards (A/B testing).  A path this
  * build cannot serve for the layer returns MOE_ERR_UNSUPPORTED (GROUPED for a
- * layer with bits 3 or 8, NVFP4 experts, or fp32 activations). */
+ * layer with bits 3 or 8, NVFP4 or MXFP4 experts, or fp32 activations). */
 moe_status moe_layer_set_path(moe_layer *h, int32_t path);
 
 /* Synchronises `stream`, reads and clears the device status word: MOE_OK, or

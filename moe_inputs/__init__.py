@@ -31,6 +31,12 @@ Storage conventions (the library's input format):
   synthetic quantiser takes the matrix scale ``amax / (6 * 448)``, each block's
   E4M3 scale as the nearest to ``block amax / (6 * matrix scale)`` and each
   code as the nearest E2M1 value of ``w / (block scale * matrix scale)``.
+* MXFP4 experts (``fmt == "mxfp4"``, group size 32): ``q`` as for NVFP4,
+  ``scale`` one E8M0 byte per 32 elements (``uint8 [E, N_out, K_in/32]``, the
+  power of two ``2^(byte - 127)``) and no ``bias``; the synthetic quantiser
+  takes each block's scale as ``2^(floor(log2(block amax)) - 2)`` (2 being the
+  largest E2M1 exponent) and each code as the nearest E2M1 value of
+  ``w / scale`` (saturating at 6).
 """
 from __future__ import annotations
 
@@ -45,7 +51,7 @@ __all__ = [
     "draw_x_rows", "round_to_bf16_bits", "bf16_bits_to_f32", "quantize_affine_int4",
     "quantize_affine", "pack_codes", "unpack_codes", "CODE_BITS", "pack_int4", "unpack_int4",
     "zipf_router_bias", "spec_for", "ROUTED_BYTES", "quantize_nvfp4", "e4m3_round",
-    "e2m1_round",
+    "e2m1_round", "quantize_mxfp4",
 ]
 
 
@@ -210,6 +216,23 @@ def e4m3_round(a: np.ndarray):
     return byte.astype(np.uint8), val
 
 
+def quantize_mxfp4(w: np.ndarray):
+    """MXFP4 quantisation of ``w [..., N, K]`` (blocks of 32 along K): returns
+    ``(q uint8 [..., N, K] E2M1 codes, scale uint8 [..., N, K/32] E8M0 bytes)``
+    as described in the module notes (an all-zero block takes 2^0)."""
+    w = np.asarray(w, dtype=np.float64)
+    K = w.shape[-1]
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    wb = w.reshape(*w.shape[:-1], K // 32, 32)
+    bmax = np.abs(wb).max(axis=-1)
+    e = np.where(bmax > 0, np.floor(np.log2(np.where(bmax > 0, bmax, 1.0))) - 2, 0)
+    e = np.clip(e, -127, 127)
+    sb = (e + 127).astype(np.uint8)
+    q = e2m1_round(wb / np.exp2(e)[..., None]).reshape(w.shape)
+    return q, sb
+
+
 def quantize_nvfp4(w: np.ndarray):
     """NVFP4 quantisation of ``w [..., N, K]`` (blocks of 16 along K): returns
     ``(q uint8 [..., N, K] E2M1 codes, scale uint8 [..., N, K/16] E4M3 bytes,
@@ -256,7 +279,7 @@ class LayerSpec:
     weight_std: float = 0.02
     bias_std: float = 0.01
     bits: int = 4               # expert code width (3, 4 or 8)
-    fmt: str = "affine"         # expert weight format: "affine" or "nvfp4" (group_size 16)
+    fmt: str = "affine"         # "affine", "nvfp4" (group_size 16) or "mxfp4" (group_size 32)
 
     @property
     def k_in(self) -> int:
@@ -411,9 +434,29 @@ def _quant_expert_nvfp4(rng, E, N, K, spec: LayerSpec):
     return words, s_all, g_all
 
 
+def _quant_expert_mxfp4(rng, E, N, K, spec: LayerSpec):
+    """MXFP4 expert matrices (no bias term: the third item is None): small
+    layers quantise N(0, weight_std) weights (``quantize_mxfp4``); large ones
+    draw uniform codes (RMS 2.93) with E8M0 scales within one binade of
+    weight_std / 2.93."""
+    if N * K <= EXACT_QUANT_MAX_ELEMS // max(E, 1):
+        q_all = np.empty((E, N, K), dtype=np.uint8)
+        s_all = np.empty((E, N, K // 32), dtype=np.uint8)
+        for e in range(E):
+            q_all[e], s_all[e] = quantize_mxfp4(rng.normal(0.0, spec.weight_std, size=(N, K)))
+        return pack_codes(q_all, 4), s_all, None
+    words = rng.integers(0, 1 << 32, size=(E, N, K // 8), dtype=np.uint32)
+    rms = float(np.sqrt(np.mean(_E2M1_GRID ** 2)))
+    e0 = int(np.rint(np.log2(spec.weight_std / rms)))
+    s_all = (127 + e0 + rng.integers(-1, 1, size=(E, N, K // 32), endpoint=True)).astype(np.uint8)
+    return words, s_all, None
+
+
 def _quant_expert(rng, E, N, K, spec: LayerSpec):
     if spec.fmt == "nvfp4":
         return _quant_expert_nvfp4(rng, E, N, K, spec)
+    if spec.fmt == "mxfp4":
+        return _quant_expert_mxfp4(rng, E, N, K, spec)
     if N * K <= EXACT_QUANT_MAX_ELEMS // max(E, 1):
         return _quant_expert_exact(rng, E, N, K, spec)
     return _quant_expert_direct(rng, E, N, K, spec)

@@ -44,7 +44,11 @@ Where the pages leave a step open, the readings are:
    bits 2..0; exponent 0 subnormal; exponent 15 with mantissa 7 is NaN) per
    16 consecutive elements along the input axis and one fp32 scale per
    expert matrix: w = e2m1(q) * e4m3(s) * matrix scale (the OCP
-   Microscaling specification's FP4 E2M1 and FP8 E4M3 element types).
+   Microscaling specification's FP4 E2M1 and FP8 E4M3 element types);
+10. MXFP4 (named with NVFP4 by the same table): the same E2M1 codes with one
+   E8M0 scale (the power of two 2^(byte - 127); 0xFF is NaN) per 32
+   consecutive elements along the input axis and no other term:
+   w = e2m1(q) * 2^(s - 127) (the OCP Microscaling specification's MXFP4).
 
 Every function here is pinned by tests that do not reuse its formulas
 (brute-force top-k, closed forms, invariants, a pure-Python loop).
@@ -58,6 +62,7 @@ import numpy as np
 
 __all__ = [
     "widen", "unpack_codes", "dequantize", "e2m1_values", "e4m3_values", "dequantize_nvfp4",
+    "e8m0_values", "dequantize_mxfp4",
     "router_logits", "selection_keys",
     "topk_order", "route", "activation", "expert_output", "shared_output",
     "oracle_forward", "routing_margin", "forward_rows", "expert_cache",
@@ -140,6 +145,22 @@ def dequantize_nvfp4(packed: np.ndarray, scale_bytes: np.ndarray, matrix_scale) 
     if s.shape[-1] * 16 != q.shape[-1]:
         raise ValueError("NVFP4 scales do not match blocks of 16")
     return q * np.repeat(s, 16, axis=-1) * float(np.float32(matrix_scale))
+
+
+def e8m0_values(b: np.ndarray) -> np.ndarray:
+    """Values of E8M0 bytes (reading 10): 2^(b - 127); 0xFF is NaN."""
+    v = np.asarray(b, dtype=np.int64)
+    return np.where(v == 255, np.nan, np.exp2(v - 127.0))
+
+
+def dequantize_mxfp4(packed: np.ndarray, scale_bytes: np.ndarray) -> np.ndarray:
+    """MXFP4 dequantisation ``w[n, k] = e2m1(q[n, k]) * e8m0(s[n, k // 32])`` in
+    float64 (reading 10)."""
+    q = e2m1_values(unpack_codes(packed, 4))
+    s = e8m0_values(scale_bytes)
+    if s.shape[-1] * 32 != q.shape[-1]:
+        raise ValueError("MXFP4 scales do not match blocks of 32")
+    return q * np.repeat(s, 32, axis=-1)
 
 
 # ---------------------------------------------------------------------------
@@ -249,7 +270,11 @@ class _ExpertCache:
         if e not in self.mats:
             L, sp = self.layer, self.spec
             G, sd, nb = sp.group_size, sp.scale_dtype, getattr(sp, "bits", 4)
-            if getattr(sp, "fmt", "affine") == "nvfp4":
+            if getattr(sp, "fmt", "affine") == "mxfp4":
+                up = dequantize_mxfp4(L.up_q[e], L.up_s[e])
+                gate = dequantize_mxfp4(L.gate_q[e], L.gate_s[e]) if sp.gated else None
+                down = dequantize_mxfp4(L.down_q[e], L.down_s[e])
+            elif getattr(sp, "fmt", "affine") == "nvfp4":
                 up = dequantize_nvfp4(L.up_q[e], L.up_s[e], L.up_b[e])
                 gate = dequantize_nvfp4(L.gate_q[e], L.gate_s[e], L.gate_b[e]) if sp.gated else None
                 down = dequantize_nvfp4(L.down_q[e], L.down_s[e], L.down_b[e])

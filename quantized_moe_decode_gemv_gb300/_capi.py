@@ -26,7 +26,7 @@ STATUS_NAMES = ["MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR
 ACT = {"swiglu": 0, "relu2": 1}
 ROUTER = {"softmax": 0, "sigmoid": 1}
 DTYPE = {"bf16": 0, "fp16": 1, "fp32": 2}
-WFMT = {"affine": 0, "nvfp4": 1}
+WFMT = {"affine": 0, "nvfp4": 1, "mxfp4": 2}
 PATH = {"auto": 0, "gemv": 1, "grouped": 2}
 NUM_STAGES = 5
 STAGE_NAMES = ["dense_in", "route", "expert_up", "expert_down", "dense_out"]
@@ -148,7 +148,7 @@ class MoEConfig:
     scale_dtype: str = "bf16"
     router_dtype: str = "bf16"
     bits: int = 4
-    fmt: str = "affine"          # expert weight format: "affine" or "nvfp4"
+    fmt: str = "affine"          # expert weight format: "affine", "nvfp4" or "mxfp4"
 
     @classmethod
     def from_spec(cls, spec: Any, max_tokens: int) -> "MoEConfig":

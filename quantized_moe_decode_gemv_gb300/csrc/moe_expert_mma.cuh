@@ -55,7 +55,7 @@ constexpr int EM_MAX_PAIRS = 4 * EM_MAX_NTP;
 
 // Shared-memory plan of one k_expert_mma launch (host and device agree).
 //   [B fragments: pp/4 n-tiles x K/16 blocks x 32 lanes x 8 bytes]
-//   [group sums of x: pp x K/gx floats, 128-aligned (gx: G, or 16 for NVFP4)]
+//   [group sums of x: pp x K/gx floats, 128-aligned (gx: G; 16 NVFP4; 32 MXFP4)]
 //   [K-split partials (ks > 1): 2 x EM_WARPS x 4 NTP x 32 floats]
 //   [rings: EM_WARPS x ns stages of stage_bytes]  [mbarriers: EM_WARPS x ns]
 // A stage holds, per matrix (gate first for SwiGLU, then up), ck x 512 bytes of
@@ -146,6 +146,12 @@ __device__ __forceinline__ void em_e4m3x4(uint32_t w, float m, float (&s)[4]) {
   s[3] = f23.y * m;
 }
 
+// An E8M0 scale byte (2^(b - 127); 0xFF is NaN) times m (a power of two: exact)
+__device__ __forceinline__ float em_e8m0(uint32_t b, float m) {
+  const uint32_t bits = b == 0u ? 0x00400000u : (b == 255u ? 0x7FC00000u : (b << 23));
+  return __uint_as_float(bits) * m;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&r);
@@ -186,16 +192,20 @@ __device__ __forceinline__ void em_ld16(const void* p, int dt, int64_t base, boo
 
 // NTP: n-tiles of accumulators (pairs per pass = 4 NTP; up to two n-tiles
 // keep the registers for two CTAs per SM).  GB: 16-column blocks per scale
-// group (G / 16).  FP4: NVFP4 codes (GB = 4: a row's scale word of a
+// group (G / 16).  FMT 1: NVFP4 codes (GB = 4: a row's scale word of a
 // 64-column chunk holds the chunk's four E4M3 block scales), folded per
 // 16-column block:
 //   y += (S / 2) ((d_hi + d_lo) - 140 X),   S = E4M3 scale x matrix scale
-template <bool GATED, int NTP, int GB, bool FP4 = false>
+// FMT 2: MXFP4 codes (GB = 4; a row's 16-bit scale entry of a 64-column chunk
+// holds its two E8M0 block scales), folded the same way per 32-column block
+// with S = the E8M0 scale.
+template <bool GATED, int NTP, int GB, int FMT = 0>
 __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __grid_constant__ ExpertArgs A) {
   extern __shared__ __align__(128) unsigned char em_smem_raw[];
-  static_assert(!FP4 || GB == 4, "NVFP4 scale words cover 64 columns");
+  constexpr bool FP4 = FMT != 0, MX = FMT == 2;
+  static_assert(!FP4 || GB == 4, "fp4 scales are staged per 64-column chunk");
   constexpr int G = 16 * GB;
-  constexpr int GX = FP4 ? 16 : G, GBX = GX / 16;   // columns of a sum of x
+  constexpr int GX = FMT == 1 ? 16 : (MX ? 32 : G), GBX = GX / 16;   // columns of a sum of x
   constexpr int NM = GATED ? 2 : 1;
   const int K = A.K, nkc = K >> 6, nkb = K >> 4, ngr = K / G, ngx = K / GX;
   const EmPlan P = em_plan(K, G, GATED, A.ck, A.nst, A.pp, A.ks, GX);
@@ -326,12 +336,18 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
     const int g0 = (kc0 * 64) / G, ng = (ckt * 64) / G;
     const uint32_t bar = eb_smem(bars + iss_s);
     unsigned char* st = ring + iss_s * P.stage_bytes;
-    const uint32_t bytes = NM * (ckt * 512u + ng * 64u);
+    // scale bytes of the chunks: 64 per chunk (16 rows x one word), MXFP4 32
+    // (16 rows x one 16-bit entry)
+    const uint32_t sbytes = MX ? ckt * 32u : ng * 64u;
+    const uint32_t bytes = NM * (ckt * 512u + sbytes);
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 #pragma unroll
     for (int m = 0; m < NM; ++m) {
       eb_bulk(eb_smem(st + m * CK * 512), qm[m] + (tile * nkc + kc0) * 128, ckt * 512u, bar);
-      eb_bulk(eb_smem(st + NM * CK * 512 + m * CK * 128), sm[m] + (tile * ngr + g0) * 16, ng * 64u, bar);
+      const void* ssrc = MX ? static_cast<const void*>(reinterpret_cast<const unsigned char*>(sm[m]) +
+                                                        (tile * nkc + kc0) * 32)
+                            : static_cast<const void*>(sm[m] + (tile * ngr + g0) * 16);
+      eb_bulk(eb_smem(st + NM * CK * 512 + m * CK * 128), ssrc, sbytes, bar);
     }
     ++issued;
     ++iss_seg;
@@ -438,9 +454,9 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
     // ---- this warp's tiles
     const uint2* bl = bfrag + lane;   // + (nt * nkb + kb) * 32
     const float* xsl = xs + t * ngx;  // + nt * 4 * ngx + grp
-    // NVFP4: the segment's matrix scales, halved (the fold's 2 v)
-    const float gsu = FP4 ? 0.5f * __ldg(A.gsc + e) : 0.f;
-    const float gsg = (FP4 && GATED) ? 0.5f * __ldg(A.gsc_gate + e) : 0.f;
+    // NVFP4: the segment's matrix scales, halved (the fold's 2 v); MXFP4: 1/2
+    const float gsu = FMT == 1 ? 0.5f * __ldg(A.gsc + e) : 0.5f;
+    const float gsg = (FMT == 1 && GATED) ? 0.5f * __ldg(A.gsc_gate + e) : 0.5f;
     float y[NTP][2], yg[NTP][2], acc[NTP][4], accg[NTP][4];
     // (a segment whose slot failed its index check issued no copies: no tiles)
     const int seg_tiles = npp > 0 ? my_tiles : 0;
@@ -475,35 +491,56 @@ __global__ void __launch_bounds__(EM_NT, NTP <= 2 ? 2 : 1) k_expert_mma(const __
           const uint32_t wgs[4] = {wg.x, wg.y, wg.z, wg.w};
           const uint2* bk = bl + static_cast<int64_t>(kc0 + c) * 4 * 32;
           if constexpr (FP4) {
-            // rows g and g + 8: the chunk's four block scales, times gs / 2
+            // rows g and g + 8: the chunk's block scales (NVFP4: four E4M3, times
+            // gs / 2; MXFP4: two E8M0, times 1/2)
             float su0[4], su1[4], sg0[4], sg1[4];
-            em_e4m3x4(sbu[c * 16], gsu, su0);
-            em_e4m3x4(sbu[c * 16 + 8], gsu, su1);
-            if (GATED) {
-              em_e4m3x4(sbg[c * 16], gsg, sg0);
-              em_e4m3x4(sbg[c * 16 + 8], gsg, sg1);
+            constexpr int NB = MX ? 2 : 4;   // scale blocks of a chunk
+            if constexpr (MX) {
+              const uint16_t* s16u = reinterpret_cast<const uint16_t*>(sbu - g) + g;
+              const uint16_t* s16g = reinterpret_cast<const uint16_t*>(sbg - g) + g;
+              const uint32_t w0 = s16u[c * 16], w1 = s16u[c * 16 + 8];
+              su0[0] = em_e8m0(w0 & 0xFFu, gsu); su0[1] = em_e8m0(w0 >> 8, gsu);
+              su1[0] = em_e8m0(w1 & 0xFFu, gsu); su1[1] = em_e8m0(w1 >> 8, gsu);
+              if (GATED) {
+                const uint32_t v0 = s16g[c * 16], v1 = s16g[c * 16 + 8];
+                sg0[0] = em_e8m0(v0 & 0xFFu, gsg); sg0[1] = em_e8m0(v0 >> 8, gsg);
+                sg1[0] = em_e8m0(v1 & 0xFFu, gsg); sg1[1] = em_e8m0(v1 >> 8, gsg);
+              }
+            } else {
+              em_e4m3x4(sbu[c * 16], gsu, su0);
+              em_e4m3x4(sbu[c * 16 + 8], gsu, su1);
+              if (GATED) {
+                em_e4m3x4(sbg[c * 16], gsg, sg0);
+                em_e4m3x4(sbg[c * 16 + 8], gsg, sg1);
+              }
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
+              constexpr int JB = 4 / NB;   // 16-column blocks of a scale block
+              if (j % JB == 0) {
 #pragma unroll
-              for (int nt = 0; nt < NTP; ++nt)
+                for (int nt = 0; nt < NTP; ++nt)
 #pragma unroll
-                for (int r = 0; r < 4; ++r) acc[nt][r] = accg[nt][r] = 0.f;
+                  for (int r = 0; r < 4; ++r) acc[nt][r] = accg[nt][r] = 0.f;
+              }
               uint32_t a[4], ag[4];
               em_decode_fp4(wqs[j], a);
               if (GATED) em_decode_fp4(wgs[j], ag);
+              const int q = j / JB;   // this block's scale
 #pragma unroll
               for (int nt = 0; nt < NTP; ++nt) {
                 if (nt < nnt) {
                   const uint2 b = bk[(static_cast<int64_t>(nt) * nkb + j) * 32];
                   mma_16816(acc[nt], a, b.x, b.y);
                   if (GATED) mma_16816(accg[nt], ag, b.x, b.y);
-                  const float xv = xsl[nt * 4 * ngx + (kc0 + c) * 4 + j];
-                  y[nt][0] = fmaf(su0[j], fmaf(-140.f, xv, acc[nt][0] + acc[nt][1]), y[nt][0]);
-                  y[nt][1] = fmaf(su1[j], fmaf(-140.f, xv, acc[nt][2] + acc[nt][3]), y[nt][1]);
-                  if (GATED) {
-                    yg[nt][0] = fmaf(sg0[j], fmaf(-140.f, xv, accg[nt][0] + accg[nt][1]), yg[nt][0]);
-                    yg[nt][1] = fmaf(sg1[j], fmaf(-140.f, xv, accg[nt][2] + accg[nt][3]), yg[nt][1]);
+                  if (j % JB == JB - 1) {
+                    const float xv = xsl[nt * 4 * ngx + (kc0 + c) * NB + q];
+                    y[nt][0] = fmaf(su0[q], fmaf(-140.f, xv, acc[nt][0] + acc[nt][1]), y[nt][0]);
+                    y[nt][1] = fmaf(su1[q], fmaf(-140.f, xv, acc[nt][2] + acc[nt][3]), y[nt][1]);
+                    if (GATED) {
+                      yg[nt][0] = fmaf(sg0[q], fmaf(-140.f, xv, accg[nt][0] + accg[nt][1]), yg[nt][0]);
+                      yg[nt][1] = fmaf(sg1[q], fmaf(-140.f, xv, accg[nt][2] + accg[nt][3]), yg[nt][1]);
+                    }
                   }
                 }
               }
@@ -690,6 +727,22 @@ static __global__ void k_tile_codes(const uint32_t* __restrict__ in, uint32_t* _
 
 // Scale/bias words [E, rows, K/G] -> [E, rows/16, K/G, 16]: a tile's words of
 // one group are contiguous.
+// MXFP4: the two E8M0 bytes of a row's 64-column chunk as one 16-bit entry,
+// [E, rows, K/64] -> [E, rows/16, K/64, 16] (a tile's entries of one chunk
+// contiguous, 32 bytes)
+static __global__ void k_tile_sb16(const uint16_t* __restrict__ in, uint16_t* __restrict__ out, int E, int rows,
+                                   int nch) {
+  const int64_t n = static_cast<int64_t>(E) * rows * nch;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int rr = static_cast<int>(i & 15);
+    const int64_t r = i >> 4;   // (e, tile, chunk)
+    const int ch = static_cast<int>(r % nch);
+    const int64_t et = r / nch;
+    out[i] = in[(et * 16 + rr) * nch + ch];
+  }
+}
+
 static __global__ void k_tile_sb(const uint32_t* __restrict__ in, uint32_t* __restrict__ out, int E, int rows,
                                  int ngr) {
   const int64_t n = static_cast<int64_t>(E) * rows * ngr;

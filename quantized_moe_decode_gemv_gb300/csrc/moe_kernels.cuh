@@ -1435,8 +1435,10 @@ struct ExpertArgs {
   const uint32_t* sbt_gate;
   int ck, pp, ks;   // ks: warps sharing a tile's K range (1, 2 or 4)
   int one_pass;     // every slot has at most pp pairs (T <= pp): one segment a slot
-  // NVFP4 experts (k_expert_mma<..., true>): sbt/sbt_gate hold the E4M3 block
-  // scales, four a word; the per-matrix fp32 scales of the experts [E]
+  // k_expert_mma's weight format: 0 affine, 1 NVFP4 (sbt/sbt_gate hold the E4M3
+  // block scales, four a word; gsc/gsc_gate the per-matrix fp32 scales [E]),
+  // 2 MXFP4 (sbt/sbt_gate hold the E8M0 block scales, two a 16-bit entry)
+  int wfmt;
   const float* gsc;
   const float* gsc_gate;
   unsigned long long* trace;   // diagnostics: CTA stamps or null

@@ -232,12 +232,16 @@ static moe_status validate_impl(const moe_layer_config* c, const moe_layer_weigh
   }
   if (c->bits != 0 && c->bits != 3 && c->bits != 4 && c->bits != 8)
     return fail(MOE_ERR_INVALID_ARG, "bits must be 0 (= 4), 3, 4 or 8");
-  if (c->weight_format != MOE_WFMT_AFFINE && c->weight_format != MOE_WFMT_NVFP4)
+  if (c->weight_format != MOE_WFMT_AFFINE && c->weight_format != MOE_WFMT_NVFP4 &&
+      c->weight_format != MOE_WFMT_MXFP4)
     return fail(MOE_ERR_INVALID_ARG, "unknown weight_format");
   const int G = c->group_size;
+  const bool fp4_fmt = c->weight_format != MOE_WFMT_AFFINE;
+  if (fp4_fmt && c->bits != 0 && c->bits != 4) return fail(MOE_ERR_INVALID_ARG, "fp4 codes are 4 bits");
   if (c->weight_format == MOE_WFMT_NVFP4) {
-    if (c->bits != 0 && c->bits != 4) return fail(MOE_ERR_INVALID_ARG, "NVFP4 codes are 4 bits");
     if (G != 16) return fail(MOE_ERR_SHAPE, "NVFP4 blocks are 16 elements: group_size must be 16");
+  } else if (c->weight_format == MOE_WFMT_MXFP4) {
+    if (G != 32) return fail(MOE_ERR_SHAPE, "MXFP4 blocks are 32 elements: group_size must be 32");
   } else if (G != 32 && G != 64 && G != 128) {
     return fail(MOE_ERR_SHAPE, "group_size must be 32, 64 or 128");
   }
@@ -256,9 +260,11 @@ static moe_status validate_impl(const moe_layer_config* c, const moe_layer_weigh
   if (w) {
     if (!w->router_w) return fail(MOE_ERR_INVALID_ARG, "router weight missing");
     if (c->has_router_bias && !w->router_bias) return fail(MOE_ERR_INVALID_ARG, "router bias missing");
-    if (!w->up_q || !w->up_s || !w->up_b || !w->down_q || !w->down_s || !w->down_b)
+    // (MXFP4 has no per-matrix or bias term: its *_b pointers are unused)
+    const bool need_b = c->weight_format != MOE_WFMT_MXFP4;
+    if (!w->up_q || !w->up_s || (need_b && !w->up_b) || !w->down_q || !w->down_s || (need_b && !w->down_b))
       return fail(MOE_ERR_INVALID_ARG, "expert up/down weights missing");
-    if (c->act == MOE_ACT_SWIGLU && (!w->gate_q || !w->gate_s || !w->gate_b))
+    if (c->act == MOE_ACT_SWIGLU && (!w->gate_q || !w->gate_s || (need_b && !w->gate_b)))
       return fail(MOE_ERR_INVALID_ARG, "SwiGLU experts need gate weights");
     if (c->act == MOE_ACT_RELU2 && (w->gate_q || w->sh_gate))
       return fail(MOE_ERR_SHAPE, "squared-ReLU experts take no gate matrix");
@@ -533,7 +539,7 @@ struct EmLaunch {
   int per_sm = 0, cps = 1;
 };
 static bool em_choose(int K, int G, bool gated, int T, int pp_cap, int n_rows, int slots, int num_sms,
-                      EmLaunch* o, bool fp4 = false) {
+                      EmLaunch* o, int gx = 0) {
   const int pp_want = std::min(std::min(EM_MAX_PAIRS, std::max(4, pp_cap & ~3)), std::max(4, (T + 3) & ~3));
   // warps per tile: a function of K alone, so that a row's sums do not depend
   // on the batch (about 6 to 12 chunks of 64 columns a warp)
@@ -546,7 +552,7 @@ static bool em_choose(int K, int G, bool gated, int T, int pp_cap, int n_rows, i
       const int budget = per_sm == 2 ? 110 * 1024 : kSmemMax - 2048;
       for (const auto& cn : kCkNs) {
         if (G == 128 && cn[0] % 2) continue;
-        const EmPlan p = em_plan(K, G, gated, cn[0], cn[1], pp, ks, fp4 ? 16 : 0);
+        const EmPlan p = em_plan(K, G, gated, cn[0], cn[1], pp, ks, gx);
         if (p.smem > budget) continue;
         o->plan = p;
         o->per_sm = per_sm;
@@ -620,20 +626,20 @@ static cudaError_t launch_dense_mma(DmArgs a, const DmLaunch& dl, size_t smem, c
   return launch_dense_mma_t<4, false>(a, dl.grid, smem, s, pdl);
 }
 
-template <int NTP, int GB, bool FP4>
+template <int NTP, int GB, int FMT>
 static cudaError_t launch_expert_mma_t(const ExpertArgs& a, bool gated, int grid, size_t smem, cudaStream_t s,
                                        bool pdl) {
-  if (gated) return launch_ex<ExpertArgs>(k_expert_mma<true, NTP, GB, FP4>, grid, EM_NT, smem, s, pdl, a);
-  return launch_ex<ExpertArgs>(k_expert_mma<false, NTP, GB, FP4>, grid, EM_NT, smem, s, pdl, a);
+  if (gated) return launch_ex<ExpertArgs>(k_expert_mma<true, NTP, GB, FMT>, grid, EM_NT, smem, s, pdl, a);
+  return launch_ex<ExpertArgs>(k_expert_mma<false, NTP, GB, FMT>, grid, EM_NT, smem, s, pdl, a);
 }
-template <int GB, bool FP4 = false>
+template <int GB, int FMT = 0>
 static cudaError_t launch_expert_mma_g(const ExpertArgs& a, bool gated, int pp, int grid, size_t smem,
                                        cudaStream_t s, bool pdl) {
-  if (pp <= 4) return launch_expert_mma_t<1, GB, FP4>(a, gated, grid, smem, s, pdl);
-  if (pp <= 8) return launch_expert_mma_t<2, GB, FP4>(a, gated, grid, smem, s, pdl);
-  return launch_expert_mma_t<4, GB, FP4>(a, gated, grid, smem, s, pdl);
+  if (pp <= 4) return launch_expert_mma_t<1, GB, FMT>(a, gated, grid, smem, s, pdl);
+  if (pp <= 8) return launch_expert_mma_t<2, GB, FMT>(a, gated, grid, smem, s, pdl);
+  return launch_expert_mma_t<4, GB, FMT>(a, gated, grid, smem, s, pdl);
 }
-// (a.G: the columns a scale word covers -- 64 for NVFP4, whose a.gsc is set)
+// (a.G: the columns a scale word covers -- 64 for the fp4 formats)
 static cudaError_t launch_expert_mma(ExpertArgs a, const EmLaunch& el, int T, int grid, cudaStream_t s,
                                      bool pdl) {
   a.ck = el.plan.ck;
@@ -645,7 +651,8 @@ static cudaError_t launch_expert_mma(ExpertArgs a, const EmLaunch& el, int T, in
   a.one_pass = T <= a.pp && (a.max_pairs <= 0 || a.max_pairs >= T);
   const size_t smem = static_cast<size_t>(el.plan.smem);
   const bool gated = a.qt_gate != nullptr;
-  if (a.gsc) return launch_expert_mma_g<4, true>(a, gated, el.plan.pp, grid, smem, s, pdl);
+  if (a.wfmt == MOE_WFMT_NVFP4) return launch_expert_mma_g<4, 1>(a, gated, el.plan.pp, grid, smem, s, pdl);
+  if (a.wfmt == MOE_WFMT_MXFP4) return launch_expert_mma_g<4, 2>(a, gated, el.plan.pp, grid, smem, s, pdl);
   switch (a.G) {
     case 32: return launch_expert_mma_g<2>(a, gated, el.plan.pp, grid, smem, s, pdl);
     case 64: return launch_expert_mma_g<4>(a, gated, el.plan.pp, grid, smem, s, pdl);
@@ -725,9 +732,12 @@ static cudaError_t set_smem_attrs() {
   MOE_SMEM_ATTR((k_expert_mma<false, 2, GB>)) MOE_SMEM_ATTR((k_expert_mma<true, 2, GB>)) \
   MOE_SMEM_ATTR((k_expert_mma<false, 4, GB>)) MOE_SMEM_ATTR((k_expert_mma<true, 4, GB>))
   MOE_SMEM_ATTR_EM(2) MOE_SMEM_ATTR_EM(4) MOE_SMEM_ATTR_EM(8)
-  MOE_SMEM_ATTR((k_expert_mma<false, 1, 4, true>)) MOE_SMEM_ATTR((k_expert_mma<true, 1, 4, true>))
-  MOE_SMEM_ATTR((k_expert_mma<false, 2, 4, true>)) MOE_SMEM_ATTR((k_expert_mma<true, 2, 4, true>))
-  MOE_SMEM_ATTR((k_expert_mma<false, 4, 4, true>)) MOE_SMEM_ATTR((k_expert_mma<true, 4, 4, true>))
+#define MOE_SMEM_ATTR_FP4(F)                                                                   \
+  MOE_SMEM_ATTR((k_expert_mma<false, 1, 4, F>)) MOE_SMEM_ATTR((k_expert_mma<true, 1, 4, F>)) \
+  MOE_SMEM_ATTR((k_expert_mma<false, 2, 4, F>)) MOE_SMEM_ATTR((k_expert_mma<true, 2, 4, F>)) \
+  MOE_SMEM_ATTR((k_expert_mma<false, 4, 4, F>)) MOE_SMEM_ATTR((k_expert_mma<true, 4, 4, F>))
+  MOE_SMEM_ATTR_FP4(1) MOE_SMEM_ATTR_FP4(2)
+#undef MOE_SMEM_ATTR_FP4
   MOE_SMEM_ATTR((k_dense_mma<1, false>)) MOE_SMEM_ATTR((k_dense_mma<2, false>))
   MOE_SMEM_ATTR((k_dense_mma<4, false>)) MOE_SMEM_ATTR((k_dense_mma<1, true>))
   MOE_SMEM_ATTR((k_dense_mma<2, true>)) MOE_SMEM_ATTR((k_dense_mma<4, true>))
@@ -816,12 +826,13 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
     g_create_error = "a reduction width exceeds the shared-memory staging limit";
     return MOE_ERR_UNSUPPORTED;
   }
-  if (c.weight_format == MOE_WFMT_NVFP4) {
-    // the NVFP4 expert kernel at four pairs a pass, which every batch can use
+  if (c.weight_format != MOE_WFMT_AFFINE) {
+    // the fp4 expert kernel at four pairs a pass, which every batch can use
     EmLaunch p_up, p_dn;
-    if (!em_choose(kin, 64, gated, 1, 4, F, 1, prop.multiProcessorCount, &p_up, true) ||
-        !em_choose(F, 64, false, 1, 4, kin, 1, prop.multiProcessorCount, &p_dn, true)) {
-      g_create_error = "no shared-memory plan of the NVFP4 expert kernel fits this shape";
+    const int gx = c.weight_format == MOE_WFMT_NVFP4 ? 16 : 32;
+    if (!em_choose(kin, 64, gated, 1, 4, F, 1, prop.multiProcessorCount, &p_up, gx) ||
+        !em_choose(F, 64, false, 1, 4, kin, 1, prop.multiProcessorCount, &p_dn, gx)) {
+      g_create_error = "no shared-memory plan of the fp4 expert kernel fits this shape";
       return MOE_ERR_UNSUPPORTED;
     }
   }
@@ -866,7 +877,7 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
   if (const char* env = std::getenv("MOE_DENSE_BULK")) L->dense_bulk = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_EXPERT_BULK_MAX_T")) L->expert_bulk_max_t = std::max(0, std::atoi(env));
   if (const char* env = std::getenv("MOE_EXPERT_MMA")) L->expert_mma = std::atoi(env) != 0;
-  if (L->fmt == MOE_WFMT_NVFP4) L->expert_mma = true;   // the only kernel that decodes NVFP4
+  if (L->fmt != MOE_WFMT_AFFINE) L->expert_mma = true;   // the only kernel that decodes fp4
   if (const char* env = std::getenv("MOE_EXPERT_MMA_MAX_T")) L->expert_mma_max_t = std::max(0, std::atoi(env));
   if (const char* env = std::getenv("MOE_DENSE_MMA")) L->dense_mma = std::atoi(env) != 0;
   if (const char* env = std::getenv("MOE_EXPERT_MMA_PP"))
@@ -918,16 +929,19 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
                                              static_cast<int64_t>(n));
       return cudaGetLastError();
     };
-    const bool fp4 = L->fmt == MOE_WFMT_NVFP4;
-    // NVFP4: the E4M3 block scales as they are (four to a word: one word per
-    // row and 64 columns) and the per-matrix fp32 scales
+    const bool fp4 = L->fmt != MOE_WFMT_AFFINE, mx = L->fmt == MOE_WFMT_MXFP4;
+    // the fp4 block scales as they are -- NVFP4: four E4M3 bytes a word (one
+    // word per row and 64 columns) and the per-matrix fp32 scales; MXFP4: two
+    // E8M0 bytes per row and 64 columns
     auto copy_fp4 = [&](uint32_t** dst, float** gdst, const void* sc, const void* gs, int rows,
                         int K) -> cudaError_t {
-      const size_t n = static_cast<size_t>(E) * rows * (K / 64);
-      cudaError_t e = L->alloc(reinterpret_cast<void**>(dst), n * 4);
-      if (e == cudaSuccess) e = cudaMemcpyAsync(*dst, sc, n * 4, cudaMemcpyDeviceToDevice, s);
-      if (e == cudaSuccess) e = L->alloc(reinterpret_cast<void**>(gdst), E * sizeof(float));
-      if (e == cudaSuccess) e = cudaMemcpyAsync(*gdst, gs, E * sizeof(float), cudaMemcpyDeviceToDevice, s);
+      const size_t nb = static_cast<size_t>(E) * rows * (K / 64) * (mx ? 2 : 4);
+      cudaError_t e = L->alloc(reinterpret_cast<void**>(dst), nb);
+      if (e == cudaSuccess) e = cudaMemcpyAsync(*dst, sc, nb, cudaMemcpyDeviceToDevice, s);
+      if (!mx) {
+        if (e == cudaSuccess) e = L->alloc(reinterpret_cast<void**>(gdst), E * sizeof(float));
+        if (e == cudaSuccess) e = cudaMemcpyAsync(*gdst, gs, E * sizeof(float), cudaMemcpyDeviceToDevice, s);
+      }
       return e;
     };
     if (gated) {
@@ -971,16 +985,29 @@ moe_status moe_layer_create(const moe_layer_config* cfg, const moe_layer_weights
       k_tile_sb<<<blocks, 256, 0, s>>>(src, *dst, E, rows, ngr);
       return cudaGetLastError();
     };
+    // MXFP4: 16-bit scale entries (two E8M0 bytes) per row and 64 columns
+    auto tile_sb16 = [&](uint32_t** dst, const uint32_t* src, int rows, int nch) -> cudaError_t {
+      const size_t n = static_cast<size_t>(E) * rows * nch;
+      cudaError_t e = L->alloc(reinterpret_cast<void**>(dst), n * 2);
+      if (e != cudaSuccess) return e;
+      const int blocks = static_cast<int>(std::min<size_t>((n + 255) / 256, 8192));
+      k_tile_sb16<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint16_t*>(src), reinterpret_cast<uint16_t*>(*dst),
+                                         E, rows, nch);
+      return cudaGetLastError();
+    };
     if (L->bits == 4 && L->expert_mma) {
-      const int Gs = fp4 ? 64 : G;   // columns a scale word covers
+      const int Gs = fp4 ? 64 : G;   // columns a scale word (MXFP4: entry) covers
+      auto tile_s = [&](uint32_t** dst, const uint32_t* src, int rows, int ngr) {
+        return mx ? tile_sb16(dst, src, rows, ngr) : tile_sb(dst, src, rows, ngr);
+      };
       if (gated) {
         MOE_TRY_CUDA(tile_q(&L->gate_qt, L->gate_q, F, kin), "gate tiles");
-        MOE_TRY_CUDA(tile_sb(&L->gate_sbt, L->gate_sb, F, kin / Gs), "gate tiles");
+        MOE_TRY_CUDA(tile_s(&L->gate_sbt, L->gate_sb, F, kin / Gs), "gate tiles");
       }
       MOE_TRY_CUDA(tile_q(&L->up_qt, L->up_q, F, kin), "up tiles");
-      MOE_TRY_CUDA(tile_sb(&L->up_sbt, L->up_sb, F, kin / Gs), "up tiles");
+      MOE_TRY_CUDA(tile_s(&L->up_sbt, L->up_sb, F, kin / Gs), "up tiles");
       MOE_TRY_CUDA(tile_q(&L->down_qt, L->down_q, kin, F), "down tiles");
-      MOE_TRY_CUDA(tile_sb(&L->down_sbt, L->down_sb, kin, F / Gs), "down tiles");
+      MOE_TRY_CUDA(tile_s(&L->down_sbt, L->down_sb, kin, F / Gs), "down tiles");
     }
     if (Fs) {
       const size_t n = static_cast<size_t>(Fs) * H * adt;
@@ -1527,16 +1554,17 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
   EmLaunch em_up, em_dn;
   // (NVFP4 layers have no other expert kernel: their scale words cover 64
   // columns, sums of x 16)
-  const bool fp4 = h->fmt == MOE_WFMT_NVFP4;
+  const bool fp4 = h->fmt != MOE_WFMT_AFFINE;
   const int Gm = fp4 ? 64 : c.group_size;
+  const int gx = h->fmt == MOE_WFMT_NVFP4 ? 16 : (h->fmt == MOE_WFMT_MXFP4 ? 32 : 0);   // columns of a sum of x
   const bool use_mma = h->expert_mma && h->up_qt && (fp4 || T <= h->expert_mma_max_t);
   // (a gated up projection with 32-column groups folds twice per 64 columns and
   // two matrices: there the CUDA-core kernels measured faster, 59 vs 73 us at
   // T = 1 on the non-latent layer; the choice depends on the shape alone)
   const bool mma_up = use_mma && (fp4 || !(gated && c.group_size == 32)) &&
-                      em_choose(kin, Gm, gated, T, h->expert_mma_pp, F, slots_e, h->num_sms, &em_up, fp4);
+                      em_choose(kin, Gm, gated, T, h->expert_mma_pp, F, slots_e, h->num_sms, &em_up, gx);
   const bool mma_dn = use_mma && em_choose(F, Gm, false, T, h->expert_mma_pp, kin, slots_e,
-                                           h->num_sms, &em_dn, fp4);
+                                           h->num_sms, &em_dn, gx);
   if (fp4 && !grouped && (!mma_up || !mma_dn)) {
     // (create refused layers without a plan at four pairs a pass, which every
     // batch size can fall back to)
@@ -1798,8 +1826,9 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
       up.n_rows = F;
       up.K = kin;
       up.G = Gm;
-      up.gsc = fp4 ? h->up_gs : nullptr;
-      up.gsc_gate = (fp4 && gated) ? h->gate_gs : nullptr;
+      up.wfmt = h->fmt;
+      up.gsc = h->up_gs;          // (NVFP4 only; null otherwise)
+      up.gsc_gate = gated ? h->gate_gs : nullptr;
       up.q = h->up_q;
       up.sb = h->up_sb;
       up.q_gate = gated ? h->gate_q : nullptr;
@@ -1925,7 +1954,7 @@ static moe_status forward_impl(moe_layer* h, const void* x, int32_t T, void* out
         dn.qt = h->down_qt;
         dn.sbt = h->down_sbt;
         dn.qt_gate = nullptr;
-        dn.gsc = fp4 ? h->down_gs : nullptr;
+        dn.gsc = h->down_gs;
         dn.gsc_gate = nullptr;
         dn.sbt_gate = nullptr;
         dn.trace = tslot("k_expert_mma_down");

@@ -153,23 +153,29 @@ def pin_quant_roundtrip_bits(ora):
 
 
 def _nvfp4_fixture():
-    e2m1, e4m3 = {}, {}
+    tabs = {"e2m1": {}, "e4m3": {}, "e8m0": {}}
     for line in open(os.path.join(GOLDEN, "nvfp4_formats.txt")):
         f = line.split()
         if not f or f[0].startswith("#"):
             continue
-        key = int(f[1], 16)
-        val = math.nan if f[2] == "nan" else (-0.0 if f[2] == "-0" else float(Fraction(f[2])))
-        (e2m1 if f[0] == "e2m1" else e4m3)[key] = val
-    return e2m1, e4m3
+        key, txt = int(f[1], 16), f[2]
+        if txt == "nan":
+            val = math.nan
+        elif txt.startswith("2^"):
+            val = math.ldexp(1.0, int(txt[2:]))
+        else:
+            val = -0.0 if txt == "-0" else float(Fraction(txt))
+        tabs[f[0]][key] = val
+    return tabs["e2m1"], tabs["e4m3"], tabs["e8m0"]
 
 
 def pin_nvfp4_format_fixture(ora):
-    """Every E2M1 code and the listed E4M3 bytes decode to the hand-worked
-    values of nvfp4_formats.txt (signs of zeros included, NaN where listed)."""
-    e2m1, e4m3 = _nvfp4_fixture()
-    assert len(e2m1) == 16 and len(e4m3) >= 20
-    for tab, fn in ((e2m1, ora.e2m1_values), (e4m3, ora.e4m3_values)):
+    """Every E2M1 code and the listed E4M3 and E8M0 bytes decode to the
+    hand-worked values of nvfp4_formats.txt (signs of zeros included, NaN
+    where listed)."""
+    e2m1, e4m3, e8m0 = _nvfp4_fixture()
+    assert len(e2m1) == 16 and len(e4m3) >= 20 and len(e8m0) >= 8
+    for tab, fn in ((e2m1, ora.e2m1_values), (e4m3, ora.e4m3_values), (e8m0, ora.e8m0_values)):
         keys = np.array(sorted(tab))
         got = np.asarray(fn(keys), dtype=np.float64)
         for k, g in zip(keys, got):
@@ -207,6 +213,35 @@ def pin_dequant_nvfp4_worked_example(ora):
     got = ora.dequantize_nvfp4(mi.pack_codes(codes, 4), scale, np.float32(0.25))
     assert got.shape == (1, 32)
     assert np.array_equal(got[0], np.array(want, dtype=np.float64)), got
+
+
+def pin_dequant_mxfp4_worked_example(ora):
+    """Two 32-element blocks of one row, worked by hand: block 0 holds the
+    sixteen codes twice with scale byte 0x7F (1), block 1 codes 0x7 and 0xD
+    with scale byte 0x7C (1/8)."""
+    order = [0x2, 0xA, 0x7, 0xF, 0x1, 0x9, 0x0, 0x8, 0x3, 0x4, 0x5, 0x6, 0xB, 0xC, 0xD, 0xE]
+    codes = np.array([order * 2 + [0x7, 0xD] * 16], dtype=np.uint8)
+    scale = np.array([[0x7F, 0x7C]], dtype=np.uint8)
+    vals = [1, -1, 6, -6, 0.5, -0.5, 0, -0, 1.5, 2, 3, 4, -1.5, -2, -3, -4]
+    want = vals * 2 + [0.75, -0.375] * 16
+    got = ora.dequantize_mxfp4(mi.pack_codes(codes, 4), scale)
+    assert got.shape == (1, 64)
+    assert np.array_equal(got[0], np.array(want, dtype=np.float64)), got
+
+
+def pin_mxfp4_quant_roundtrip(ora):
+    """The generator's MXFP4 quantiser and the oracle's decoder: each block's
+    scale X puts the block's largest magnitude in [4 X, 8 X) (the largest E2M1
+    exponent is 2), and every weight is within 2 X of its value (at most the
+    clip from 8 X to 6 X; inside the grid at most half the largest gap)."""
+    rng = np.random.Generator(np.random.PCG64(35))
+    w = rng.normal(0, 0.02, size=(8, 128))
+    q, sb = mi.quantize_mxfp4(w)
+    deq = ora.dequantize_mxfp4(mi.pack_codes(q, 4), sb)
+    X = ora.e8m0_values(sb)
+    bmax = np.abs(w).reshape(8, 4, 32).max(-1)
+    assert np.all((bmax >= 4 * X) & (bmax < 8 * X))
+    assert np.all(np.abs(w - deq) <= 2 * np.repeat(X, 32, axis=-1) + 1e-15)
 
 
 def pin_nvfp4_quant_roundtrip(ora):

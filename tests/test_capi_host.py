@@ -101,6 +101,12 @@ CASES = [
     ("nvfp4 block 32", {"fmt": "nvfp4", "group_size": 32}, {}, "MOE_ERR_SHAPE"),
     ("nvfp4 8-bit", {"fmt": "nvfp4", "group_size": 16, "bits": 8}, {}, "MOE_ERR_INVALID_ARG"),
     ("affine group 16", {"group_size": 16}, {}, "MOE_ERR_SHAPE"),
+    ("mxfp4", {"fmt": "mxfp4", "group_size": 32}, {}, "MOE_OK"),
+    ("mxfp4 without bias pointers", {"fmt": "mxfp4", "group_size": 32},
+     {"up_b": None, "down_b": None, "gate_b": None}, "MOE_OK"),
+    ("mxfp4 block 16", {"fmt": "mxfp4", "group_size": 16}, {}, "MOE_ERR_SHAPE"),
+    ("mxfp4 3-bit", {"fmt": "mxfp4", "group_size": 32, "bits": 3}, {}, "MOE_ERR_INVALID_ARG"),
+    ("nvfp4 needs matrix scales", {"fmt": "nvfp4", "group_size": 16}, {"up_b": None}, "MOE_ERR_INVALID_ARG"),
 ]
 
 
@@ -157,3 +163,11 @@ def test_traffic_gate_matches_the_committed_capture():
             assert got == float(rec["dram_bytes_per_launch"])
         else:
             assert got is None
+
+
+def test_unknown_weight_format_refused(lib):
+    c = _cfg().to_c()
+    c.weight_format = 7
+    st = lib.moe_layer_validate(ctypes.byref(c), ctypes.byref(_w()))
+    assert _capi.STATUS_NAMES[st] == "MOE_ERR_INVALID_ARG"
+    assert b"weight_format" in lib.moe_layer_last_error(None)

@@ -185,8 +185,9 @@ def test_code_width_grouped_refused(bits):
 
 # --- NVFP4 experts: E2M1 codes, E4M3 block scales, fp32 matrix scales ------------
 
-def _fp4_layer(spec, seed=0):
-    return gu.cached_layer_spec(spec.with_(name=f"{spec.name}_nvfp4", fmt="nvfp4", group_size=16), seed)
+def _fp4_layer(spec, seed=0, fmt="nvfp4"):
+    return gu.cached_layer_spec(spec.with_(name=f"{spec.name}_{fmt}", fmt=fmt,
+                                           group_size=16 if fmt == "nvfp4" else 32), seed)
 
 
 @pytest.mark.parametrize("T", [1, 2, 3, 5, 16, 33])
@@ -213,6 +214,32 @@ def test_nvfp4_fp16_softmax_parity(T):
     """fp16 activations, softmax without renormalisation, SwiGLU, latent 256,
     F = 384 (not a power of two) with NVFP4 experts."""
     lay = _fp4_layer(ODD["odd_latent_fp16"])
+    handle_for(lay.spec.name, 16, layer=lay)
+    _parity(lay.spec.name, T, max_tokens=16, paths=("auto",))
+
+
+@pytest.mark.parametrize("T", [1, 3, 16, 33])
+def test_mxfp4_tiny_parity(T):
+    """MXFP4 experts (E2M1 codes, E8M0 scale per 32) on the tiny SwiGLU layer,
+    every row."""
+    lay = _fp4_layer(mi.spec_for("tiny"), fmt="mxfp4")
+    _, h = handle_for(lay.spec.name, 48, layer=lay)
+    assert h.path_for(T) == "gemv"
+    _parity(lay.spec.name, T, max_tokens=48, paths=("auto",))
+
+
+@pytest.mark.parametrize("T,rows", [(1, None), (9, [0, 4, 8]), (16, [0, 15])])
+def test_mxfp4_latent_parity(T, rows):
+    """The latent layer with MXFP4 experts at full size (the down projection's
+    F = 1856 is not a multiple of 128: two scale bytes per 64-column chunk)."""
+    lay = _fp4_layer(mi.spec_for("latent"), fmt="mxfp4")
+    handle_for(lay.spec.name, 16, layer=lay)
+    _parity(lay.spec.name, T, rows=rows, max_tokens=16, paths=("auto",))
+
+
+@pytest.mark.parametrize("T", [1, 12])
+def test_mxfp4_fp16_softmax_parity(T):
+    lay = _fp4_layer(ODD["odd_latent_fp16"], fmt="mxfp4")
     handle_for(lay.spec.name, 16, layer=lay)
     _parity(lay.spec.name, T, max_tokens=16, paths=("auto",))
 

@@ -63,6 +63,9 @@ MUTANTS = [
     ("E4M3 subnormal off by a power of two", "(mf / 8.0) * 2.0 ** -6", "(mf / 8.0) * 2.0 ** -7"),
     ("E4M3 mantissa of 4 bits", "mf = v & 7\n", "mf = v & 15\n"),
     ("NVFP4 blocks of 32", "np.repeat(s, 16, axis=-1) * float", "np.repeat(s, 32, axis=-1)[..., : q.shape[-1]] * float"),
+    ("E8M0 bias 128", "np.exp2(v - 127.0))", "np.exp2(v - 128.0))"),
+    ("MXFP4 blocks of 16", "q * np.repeat(s, 32, axis=-1)", "q * np.repeat(s, 16, axis=-1)[..., : q.shape[-1]]"),
+    ("E8M0 NaN at zero", "np.where(v == 255, np.nan", "np.where(v == 0, np.nan"),
     ("NVFP4 matrix scale dropped", "return q * np.repeat(s, 16, axis=-1) * float(np.float32(matrix_scale))",
      "return q * np.repeat(s, 16, axis=-1)"),
 ]
