@@ -2,7 +2,8 @@
  * moe_layer.h -- C ABI of the GB300 (sm_103a) quantized MoE decode layer.
  *
  * One handle holds one routed mixture-of-experts layer whose expert weights are
- * affine group-quantised to 4 bits (or 3 or 8: moe_layer_config.bits).  moe_layer_forward() runs, for every token row,
+ * affine group-quantised to 4 bits (or 2, 3, 5, 6 or 8: moe_layer_config.bits; or
+ * block-scaled fp4: moe_layer_config.weight_format).  moe_layer_forward() runs, for every token row,
  *
  *   router gemv -> softmax/sigmoid top-k -> (fc1_latent_proj) -> per selected
  *   expert: dequant gemv up (+gate), activation, dequant gemv down -> weighted
@@ -26,9 +27,9 @@
  *   - "device pointer": memory of the GPU the handle was created on;
  *     "host pointer": ordinary or pinned host memory.
  *   - Matrices are row-major and contiguous.
- *   - Packed b-bit codes (b = bits: 3, 4 or 8): the codes of a row form one
+ *   - Packed b-bit codes (b = bits: 2, 3, 4, 5, 6 or 8): the codes of a row form one
  *     little-endian bit stream of uint32 words -- element i occupies stream
- *     bits b*i..b*i+b-1, stream bit j is bit j%32 of word j/32, so a 3-bit code
+ *     bits b*i..b*i+b-1, stream bit j is bit j%32 of word j/32, so a 3-, 5- or 6-bit code
  *     may straddle two words.  For b = 4: eight codes per uint32, element 8*w+i
  *     in bits 4*i..4*i+3 (lowest nibble first).  A weight is scale*q + bias
  *     (q unsigned, 0..2^b-1), with the scale and bias of its group of
@@ -133,8 +134,8 @@ typedef struct moe_layer_config {
   int32_t act_dtype;     /* BF16|FP16: x, out, fc1/fc2 and shared expert weights */
   int32_t scale_dtype;   /* BF16|FP16: expert scales and biases (ignored by NVFP4) */
   int32_t router_dtype;  /* BF16|FP16|FP32: router weight (x is widened to fp32) */
-  int32_t bits;          /* code width of the routed experts: 3, 4 or 8 (0 = 4).
-                            3- and 8-bit layers run the GEMV schedule only: AUTO
+  int32_t bits;          /* code width of the routed experts: 2, 3, 4, 5, 6 or 8
+                            (0 = 4).  Widths other than 4 run the GEMV schedule only: AUTO
                             selects it at every T, GROUPED is refused */
   int32_t weight_format; /* moe_weight_format (0 = affine).  NVFP4 needs bits 0
                             or 4 and group_size 16, MXFP4 bits 0 or 4 and
@@ -193,7 +194,7 @@ int32_t moe_build_flags(void);
  * with the same refusals and codes as moe_layer_create; touches no device.
  * `w` may be NULL to check the config alone.  Refusals, in order:
  *   MOE_ERR_INVALID_ARG   null cfg, non-positive sizes, bad enum values, bits
- *                         not 0, 3, 4 or 8 (NVFP4, MXFP4: not 0 or 4), an unknown
+ *                         not 0, 2, 3, 4, 5, 6 or 8 (NVFP4, MXFP4: not 0 or 4), an unknown
  *                         weight_format
  *   MOE_ERR_TOPK_GT_E     top_k < 1 or top_k > n_experts (a layer whose top-k
  *                         exceeds its own expert count is refused before any
@@ -242,7 +243,8 @@ moe_status moe_layer_forward_host(moe_layer *h, const void *x_host, int32_t T, v
 
 /* Choose the routed-expert path for later forwards (A/B testing).  A path this
  * build cannot serve for the layer returns MOE_ERR_UNSUPPORTED (GROUPED for a
- * layer with bits 3 or 8, NVFP4 or MXFP4 experts, or fp32 activations). */
+ * layer with a code width other than 4, NVFP4 or MXFP4 experts, or fp32
+ * activations). */
 moe_status moe_layer_set_path(moe_layer *h, int32_t path);
 
 /* Synchronises `stream`, reads and clears the device status word: MOE_OK, or

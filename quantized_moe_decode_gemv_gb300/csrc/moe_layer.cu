@@ -102,7 +102,7 @@ struct moe_layer {
   int r_in = 0, off_fc1 = 0, off_shg = 0, off_shu = 0;
   int umax = 0;
   int kin = 0;
-  int bits = 4;           // code width of the routed experts (3, 4 or 8)
+  int bits = 4;           // code width of the routed experts (2, 3, 4, 5, 6 or 8)
   int fmt = 0;            // MOE_WFMT_AFFINE or MOE_WFMT_NVFP4
   float* up_gs = nullptr;     // NVFP4: per-matrix scales of the experts [E]
   float* gate_gs = nullptr;
@@ -230,8 +230,8 @@ static moe_status validate_impl(const moe_layer_config* c, const moe_layer_weigh
   } else if (w && (w->fc1_latent || w->fc2_latent)) {
     return fail(MOE_ERR_LATENT_PROJ, "latent projections given for a non-latent layer");
   }
-  if (c->bits != 0 && c->bits != 3 && c->bits != 4 && c->bits != 8)
-    return fail(MOE_ERR_INVALID_ARG, "bits must be 0 (= 4), 3, 4 or 8");
+  if (c->bits != 0 && (c->bits < 2 || c->bits > 8 || c->bits == 7))
+    return fail(MOE_ERR_INVALID_ARG, "bits must be 0 (= 4), 2, 3, 4, 5, 6 or 8");
   if (c->weight_format != MOE_WFMT_AFFINE && c->weight_format != MOE_WFMT_NVFP4 &&
       c->weight_format != MOE_WFMT_MXFP4)
     return fail(MOE_ERR_INVALID_ARG, "unknown weight_format");
@@ -691,11 +691,22 @@ static cudaError_t launch_dense_out(const DenseOutArgs& a, int tb, int grid, cud
     default: return launch_dense_out_t<DenseOutArgs, 8>(a, grid, s, pdl);
   }
 }
-// 3- and 8-bit codes: passes of one or two token pairs (pb above 2 is clamped)
+// 2-, 3-, 5-, 6- and 8-bit codes: passes of one or two token pairs (pb above 2
+// is clamped)
+template <int B>
+static cudaError_t launch_expert_b(const ExpertArgs& a, int pb, int grid, cudaStream_t s, bool pdl) {
+  return pb <= 1 ? launch_expert_t<1, B>(a, grid, s, pdl) : launch_expert_t<2, B>(a, grid, s, pdl);
+}
 static cudaError_t launch_expert(const ExpertArgs& a, int pb, int grid, cudaStream_t s, bool pdl,
                                  int bits = 4) {
-  if (bits == 3) return pb <= 1 ? launch_expert_t<1, 3>(a, grid, s, pdl) : launch_expert_t<2, 3>(a, grid, s, pdl);
-  if (bits == 8) return pb <= 1 ? launch_expert_t<1, 8>(a, grid, s, pdl) : launch_expert_t<2, 8>(a, grid, s, pdl);
+  switch (bits) {
+    case 2: return launch_expert_b<2>(a, pb, grid, s, pdl);
+    case 3: return launch_expert_b<3>(a, pb, grid, s, pdl);
+    case 5: return launch_expert_b<5>(a, pb, grid, s, pdl);
+    case 6: return launch_expert_b<6>(a, pb, grid, s, pdl);
+    case 8: return launch_expert_b<8>(a, pb, grid, s, pdl);
+    default: break;
+  }
   switch (pb) {
     case 1: return launch_expert_t<1>(a, grid, s, pdl);
     case 2: return launch_expert_t<2>(a, grid, s, pdl);
@@ -742,10 +753,12 @@ static cudaError_t set_smem_attrs() {
   MOE_SMEM_ATTR((k_dense_mma<4, false>)) MOE_SMEM_ATTR((k_dense_mma<1, true>))
   MOE_SMEM_ATTR((k_dense_mma<2, true>)) MOE_SMEM_ATTR((k_dense_mma<4, true>))
 #undef MOE_SMEM_ATTR_EM
-  MOE_SMEM_ATTR((k_expert<1, false, 3>)) MOE_SMEM_ATTR((k_expert<2, false, 3>))
-  MOE_SMEM_ATTR((k_expert<1, true, 3>)) MOE_SMEM_ATTR((k_expert<2, true, 3>))
-  MOE_SMEM_ATTR((k_expert<1, false, 8>)) MOE_SMEM_ATTR((k_expert<2, false, 8>))
-  MOE_SMEM_ATTR((k_expert<1, true, 8>)) MOE_SMEM_ATTR((k_expert<2, true, 8>))
+#define MOE_SMEM_ATTR_BITS(B)                                                         \
+  MOE_SMEM_ATTR((k_expert<1, false, B>)) MOE_SMEM_ATTR((k_expert<2, false, B>)) \
+  MOE_SMEM_ATTR((k_expert<1, true, B>)) MOE_SMEM_ATTR((k_expert<2, true, B>))
+  MOE_SMEM_ATTR_BITS(2) MOE_SMEM_ATTR_BITS(3) MOE_SMEM_ATTR_BITS(5) MOE_SMEM_ATTR_BITS(6)
+  MOE_SMEM_ATTR_BITS(8)
+#undef MOE_SMEM_ATTR_BITS
   MOE_SMEM_ATTR((k_expert_bulk<1, 8, false>)) MOE_SMEM_ATTR((k_expert_bulk<2, 4, false>))
   MOE_SMEM_ATTR((k_expert_bulk<4, 2, false>)) MOE_SMEM_ATTR((k_expert_bulk<8, 1, false>))
   MOE_SMEM_ATTR((k_expert_bulk<1, 1, false>)) MOE_SMEM_ATTR((k_expert_bulk<2, 1, false>))

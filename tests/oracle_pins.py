@@ -36,10 +36,14 @@ TINY_FP16 = mi.LayerSpec(name="t_fp16", hidden=24, n_experts=6, top_k=3, expert_
                          act_dtype="fp16", scale_dtype="fp16", router_dtype="fp32",
                          weight_std=0.3)
 TINY_UNNORM = TINY_SOFTMAX.with_(name="t_unnorm", renormalize=False, n_experts=5, top_k=3)
-# 3- and 8-bit expert codes (rows of K codes fill whole words: K * bits % 32 == 0)
+# 2-, 3-, 5-, 6- and 8-bit expert codes (rows of K codes fill whole words: K * bits % 32 == 0)
 TINY_B3 = TINY_SOFTMAX.with_(name="t_b3", hidden=32, expert_ffn=32, bits=3)
 TINY_B8 = TINY_LATENT.with_(name="t_b8", bits=8)
-TINY_SPECS = (TINY_SOFTMAX, TINY_LATENT, TINY_FP16, TINY_UNNORM, TINY_B3, TINY_B8)
+TINY_B2 = TINY_SOFTMAX.with_(name="t_b2", hidden=32, expert_ffn=32, bits=2)
+TINY_B5 = TINY_LATENT.with_(name="t_b5", bits=5, latent=32, hidden=32, expert_ffn=32)
+TINY_B6 = TINY_FP16.with_(name="t_b6", bits=6, hidden=32, expert_ffn=32)
+TINY_SPECS = (TINY_SOFTMAX, TINY_LATENT, TINY_FP16, TINY_UNNORM, TINY_B3, TINY_B8, TINY_B2, TINY_B5,
+              TINY_B6)
 
 
 def _rel(a, b):
@@ -108,14 +112,14 @@ def pin_dequant_closed_form(ora):
 
 
 def pin_dequant_closed_form_bits(ora):
-    """3- and 8-bit codes: code 0 -> bias, the top code 2^b - 1 -> (2^b - 1)*scale +
+    """2-, 3-, 5-, 6- and 8-bit codes: code 0 -> bias, the top code 2^b - 1 -> (2^b - 1)*scale +
     bias, every element on its own group's scale and bias."""
     N, K, G = 2, 64, 32
     ng = K // G
     scale = np.array([[0.25 * (g + 1) + n for g in range(ng)] for n in range(N)])
     bias = np.array([[-(g + 1) * 0.5 - n for g in range(ng)] for n in range(N)])
     s_st, b_st = mi.round_to_bf16_bits(scale), mi.round_to_bf16_bits(bias)
-    for bits in (3, 8):
+    for bits in (2, 3, 5, 6, 8):
         top = (1 << bits) - 1
         for code in (0, 1, top // 2, top):
             packed = mi.pack_codes(np.full((N, K), code, dtype=np.uint8), bits)
@@ -131,12 +135,14 @@ def pin_dequant_closed_form_bits(ora):
 
 
 def pin_quant_roundtrip_bits(ora):
-    """3- and 8-bit: the generator's quantiser applied to the oracle's
+    """2-, 3-, 5-, 6- and 8-bit: the generator's quantiser applied to the oracle's
     dequantised weights gives back the same codes where a group holds both end
     codes (its min/max reproduce scale and bias), and the error of a round trip
     is at most half a step plus the scale/bias storage rounding."""
     rng = np.random.Generator(np.random.PCG64(21))
-    for bits, sdt, G, eps in ((3, "bf16", 64, 2.0 ** -8), (8, "fp16", 32, 2.0 ** -11)):
+    for bits, sdt, G, eps in ((3, "bf16", 64, 2.0 ** -8), (8, "fp16", 32, 2.0 ** -11),
+                              (2, "bf16", 32, 2.0 ** -8), (5, "fp16", 128, 2.0 ** -11),
+                              (6, "bf16", 64, 2.0 ** -8)):
         top = (1 << bits) - 1
         w = rng.normal(0, 0.02, size=(6, 256))
         q, s, b = mi.quantize_affine(w, G, bits, sdt)

@@ -91,8 +91,11 @@ CASES = [
     ("3-bit codes", {"bits": 3}, {}, "MOE_OK"),
     ("8-bit codes", {"bits": 8}, {}, "MOE_OK"),
     ("bits 0 means 4", {"bits": 0}, {}, "MOE_OK"),
-    ("2-bit codes", {"bits": 2}, {}, "MOE_ERR_INVALID_ARG"),
-    ("5-bit codes", {"bits": 5}, {}, "MOE_ERR_INVALID_ARG"),
+    ("2-bit codes", {"bits": 2}, {}, "MOE_OK"),
+    ("5-bit codes", {"bits": 5}, {}, "MOE_OK"),
+    ("6-bit codes", {"bits": 6}, {}, "MOE_OK"),
+    ("7-bit codes", {"bits": 7}, {}, "MOE_ERR_INVALID_ARG"),
+    ("1-bit codes", {"bits": 1}, {}, "MOE_ERR_INVALID_ARG"),
     ("16-bit codes", {"bits": 16}, {}, "MOE_ERR_INVALID_ARG"),
     ("nvfp4", {"fmt": "nvfp4", "group_size": 16}, {}, "MOE_OK"),
     ("nvfp4 bits 0", {"fmt": "nvfp4", "group_size": 16, "bits": 0}, {}, "MOE_OK"),

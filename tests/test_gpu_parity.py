@@ -149,10 +149,10 @@ def _bits_layer(base, bits, seed=0):
     return gu.cached_layer_spec(spec, seed)
 
 
-@pytest.mark.parametrize("bits", [3, 8])
+@pytest.mark.parametrize("bits", [2, 3, 5, 6, 8])
 @pytest.mark.parametrize("T", [1, 2, 3, 5, 16])
 def test_code_width_tiny_parity(bits, T):
-    """Little-endian b-bit code streams (3-bit codes straddle words) through
+    """Little-endian b-bit code streams (3-, 5- and 6-bit codes straddle words) through
     the gemv expert kernels, on every row; AUTO keeps the gemv schedule."""
     lay = _bits_layer("tiny", bits)
     _, h = handle_for(lay.spec.name, 16, layer=lay)
@@ -160,17 +160,17 @@ def test_code_width_tiny_parity(bits, T):
     _parity(lay.spec.name, T, max_tokens=16, paths=("auto",))
 
 
-@pytest.mark.parametrize("bits", [3, 8])
-@pytest.mark.parametrize("T,rows", [(1, None), (2, None), (9, [0, 4, 8])])
+@pytest.mark.parametrize("bits,T,rows", [(b, T, r) for b in (3, 8) for T, r in ((1, None), (2, None), (9, [0, 4, 8]))]
+                         + [(b, T, r) for b in (2, 5, 6) for T, r in ((1, None), (9, [0, 4, 8]))])
 def test_code_width_latent_parity(bits, T, rows):
-    """The latent layer (E=496, k=9, latent 1024, group 64) with 3- and 8-bit
-    expert codes at full size."""
+    """The latent layer (E=496, k=9, latent 1024, group 64) with 2-, 3-, 5-,
+    6- and 8-bit expert codes at full size."""
     lay = _bits_layer("latent", bits)
     handle_for(lay.spec.name, 16, layer=lay)
     _parity(lay.spec.name, T, rows=rows, max_tokens=16, paths=("auto",))
 
 
-@pytest.mark.parametrize("bits", [3, 8])
+@pytest.mark.parametrize("bits", [2, 3, 5, 6, 8])
 def test_code_width_grouped_refused(bits):
     """The tensor-core schedule decodes 4-bit codes only: forcing it on a 3- or
     8-bit layer is refused and the layer keeps its gemv schedule."""
