@@ -13,7 +13,7 @@ Storage conventions (the library's input format):
   are numpy ``float16``; fp32 tensors are ``float32``.
 * Expert matrices are row-major ``[E, N_out, K_in]`` with the quantisation
   groups of ``G`` consecutive elements along ``K_in``.  ``q`` holds b-bit
-  codes (b = 3, 4 or 8) packed into ``uint32`` words as one little-endian bit
+  codes (b = 2, 3, 4, 5, 6 or 8) packed into ``uint32`` words as one little-endian bit
   stream per row, code ``i`` in bits ``b*i .. b*i+b-1`` (for b = 4: eight per
   word, lowest nibble first), giving ``[E, N_out, K_in*b/32]``.  ``scale`` and
   ``bias`` are ``[E, N_out, K_in/G]`` in the layer's scale dtype and a weight
@@ -278,7 +278,7 @@ class LayerSpec:
     router_dtype: str = "bf16"  # router weight
     weight_std: float = 0.02
     bias_std: float = 0.01
-    bits: int = 4               # expert code width (3, 4 or 8)
+    bits: int = 4               # expert code width (2, 3, 4, 5, 6 or 8)
     fmt: str = "affine"         # "affine", "nvfp4" (group_size 16) or "mxfp4" (group_size 32)
 
     @property

@@ -1,5 +1,5 @@
 """fp64 CPU oracle for the decode-time forward of a routed MoE layer with b-bit
-(3, 4 or 8) affine group-quantised experts, or NVFP4 experts.
+(2, 3, 4, 5, 6 or 8) affine group-quantised experts, or NVFP4 / MXFP4 experts.
 
 TEST INFRASTRUCTURE ONLY.  Nothing in the library imports this module; only the
 tests, the smoke check and the benchmark's CPU-baseline leg call it.  It shares
@@ -24,7 +24,7 @@ Sources (page titles and sections):
 Where the pages leave a step open, the readings are:
 
 1. affine dequantisation is ``w = scale * q + bias`` with unsigned b-bit codes
-   ``q in 0..2^b-1`` (b = 3, 4 or 8) and groups of G consecutive elements
+   ``q in 0..2^b-1`` (b = 2, 3, 4, 5, 6 or 8) and groups of G consecutive elements
    along the input axis;
 2. packed storage: the codes of a row as one little-endian bit stream of
    uint32 words (for b = 4: eight codes per word, lowest nibble first);
