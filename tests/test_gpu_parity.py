@@ -373,7 +373,11 @@ def test_stack_parity(T, rows):
     layer is no test here: with relu^2 experts and no normalisation the
     synthetic stream grows about quadratically per layer, the later routers'
     logits saturate, and a 1e-4 relative change of the input already moves
-    the oracle's own expert choice."""
+    the oracle's own expert choice.
+
+    Each layer is also run on the oracle's stream itself (its bf16 input to
+    that layer, on which the checked rows keep the routing margin): the same
+    input bits on both sides, held to the single-layer parity gate."""
     layers = stack_layers()
     sel = list(range(T)) if rows is None else rows
     xs, _ = gu.margin_x(layers[0], len(sel), seed=40 + T, stack=layers)
@@ -396,6 +400,9 @@ def test_stack_parity(T, rows):
             # layers are held to the parity bound itself.
             rtol, atol = (gu.W_RTOL, gu.W_ATOL) if li == 0 else (gu.REL_RMS, gu.REL_RMS * 0.1)
             np.testing.assert_allclose(w.cpu().numpy()[sel], ref["w"], rtol=rtol, atol=atol)
+            # the same layer on the oracle's input to it
+            same = gu.run_layer(h, ref_in, "bf16")
+            gu.check_parity(same, ref, what=f"stack layer {li} on the oracle's stream")
             ref_in = mi._round_to_dtype(ref["out"], "bf16")
             cur = out
         final = cur.float().cpu().numpy().astype(np.float64)[sel]
