@@ -30,6 +30,12 @@
 // are independent and every fold runs in a fixed order), so a row gives the
 // same bits whatever the batch.
 //
+// The same kernel reads NVFP4 and MXFP4 experts (E2M1 codes in the same
+// fragment order; A holds 128 + 2v + 12, exact in bf16) and folds each scale
+// block (16 or 32 columns) with its E4M3 or E8M0 scale.  The work of a launch
+// is the routing's units (distinct expert and pass of its pairs, 16-row tile)
+// spread over a grid sized before the routing is known.
+//
 // Weights stream through a private ring per warp: lane 0 issues the bulk copies
 // of one (16-row tile, CK x 64 columns) chunk -- the codes and the chunk's
 // scale/bias words (gate and up for SwiGLU), each one contiguous range -- that
