@@ -190,6 +190,9 @@ def parse_args():
                         "tcgen05 path from 16")
     p.add_argument("--config", choices=["latent", "nonlatent", "tiny"], default="latent",
                    help="layer of the main line (the headline metric is the latent layer at T=1)")
+    p.add_argument("--fmt", choices=["affine", "nvfp4", "mxfp4"], default="affine",
+                   help="expert weight format of the main line's layer (nvfp4: blocks of 16, "
+                        "mxfp4: blocks of 32)")
     p.add_argument("--no-also", action="store_true", help="skip the other configured workloads")
     p.add_argument("--zipf", action="store_true", help="Zipf-skewed expert load (batched sweep)")
     p.add_argument("--sweep", default="", help="comma-separated T values: time each and write "
@@ -507,6 +510,9 @@ def run_ours(args):
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
 
     spec = mi.SPECS[args.config]
+    if args.fmt != "affine":
+        spec = spec.with_(name=f"{spec.name}_{args.fmt}", fmt=args.fmt,
+                          group_size=16 if args.fmt == "nvfp4" else 32)
     rb = mi.zipf_router_bias(spec.n_experts, args.seed + rank) if args.zipf else None
     layer = mi.make_layer(spec, args.seed + rank, router_bias=rb)
     sweep = [int(v) for v in args.sweep.split(",") if v.strip()]
@@ -633,6 +639,8 @@ def run_ours(args):
 
     if rank == 0:
         workload = WORKLOAD if args.config == "latent" else spec.name + " layer"
+        if args.fmt != "affine":
+            workload += f", {args.fmt.upper()} experts"
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
