@@ -174,3 +174,25 @@ def test_unknown_weight_format_refused(lib):
     st = lib.moe_layer_validate(ctypes.byref(c), ctypes.byref(_w()))
     assert _capi.STATUS_NAMES[st] == "MOE_ERR_INVALID_ARG"
     assert b"weight_format" in lib.moe_layer_last_error(None)
+
+
+def test_algorithmic_byte_model():
+    """The bench's algorithmic bytes on the latent layer at T = 1 with 9
+    distinct experts: router 4.06 + fc1 8.39 + shared gate 30.4 MB in the pass
+    over x, 1.07 MB per expert projection (0.95 MB of codes, 0.12 MB of
+    scale/bias words at G = 64; NVFP4 the same; MXFP4 0.06 MB of E8M0 bytes),
+    fc2 8.39 + shared down 30.4 MB in the output pass; 100.9 MB in all."""
+    import bench
+    import moe_inputs as mi
+    sp = mi.SPECS["latent"]
+    H, E, L, F, Fs = 4096, 496, 1024, 1856, 3712
+    b = bench.stage_bytes(sp, 1, 9)
+    assert b["dense_in"] == E * H * 2 + L * H * 2 + Fs * H * 2 + H * 2 + E * 4
+    assert b["dense_out"] == H * L * 2 + H * Fs * 2 + 2 * H * 2
+    assert bench.expert_bytes(sp) == (F * L // 2 + 4 * F * L // 64,) * 2
+    assert b["expert_up"] == b["expert_down"] == 9 * (F * L // 2 + F * L // 16)
+    assert abs(bench.layer_bytes(sp, 1, 9) - 100.9e6) < 0.1e6
+    nv = bench.expert_bytes(sp.with_(fmt="nvfp4", group_size=16))
+    mx = bench.expert_bytes(sp.with_(fmt="mxfp4", group_size=32))
+    assert nv == (F * L // 2 + F * L // 16 + 4,) * 2
+    assert mx == (F * L // 2 + F * L // 32,) * 2
